@@ -1,0 +1,64 @@
+"""Oracle: chunk table and wave packing (integer bookkeeping only).
+
+[WB] "Batch Transcription": all 30-second chunks of several requests are fused
+into one generate pass to fill the GPU's memory; "VRAM usage guide": memory
+grows linearly with the number of chunks in flight (a fixed per-chunk cost plus
+the weights); "Serving at Scale": concurrent requests are grouped into GPU
+batches.
+
+Readings:
+  * chunk c of the batch is (request r, index k) in request order, then index
+    order; it holds min(480000, samples_r - 480000 k) real samples;
+  * a chunk's decode state costs, per decoder layer, the bf16 cross-attention
+    K and V over 1500 encoder positions plus its float8 self-attention K and V
+    over its own decode length L_c, plus its token row (448 int32);
+  * waves: chunks sorted by decode length, longest first (ties by chunk
+    index), are packed greedily in that order; a new wave opens when the next
+    chunk would push the running total of per-chunk bytes past the budget.
+    Within a wave the chunks keep that order, so the chunks still decoding at
+    any step form a prefix of the wave.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+CHUNK = 480000
+N_CTX = 1500
+MAX_POS = 448
+
+
+def chunk_table(req_samples):
+    """(req_of_chunk, index_in_req, valid_samples) as int32 arrays."""
+    req, idx, valid = [], [], []
+    for r, s in enumerate(np.asarray(req_samples, dtype=np.int64)):
+        n = int((s + CHUNK - 1) // CHUNK)
+        for k in range(n):
+            req.append(r)
+            idx.append(k)
+            valid.append(int(min(CHUNK, s - CHUNK * k)))
+    return (np.array(req, np.int32), np.array(idx, np.int32), np.array(valid, np.int32))
+
+
+def chunk_state_bytes(d_model: int, dec_layers: int, length: int) -> int:
+    cross = dec_layers * 2 * N_CTX * d_model * 2
+    self_kv = dec_layers * 2 * int(length) * d_model
+    return cross + self_kv + MAX_POS * 4
+
+
+def plan_waves(chunk_len, d_model: int, dec_layers: int, budget_bytes: int):
+    """List of waves, each an int32 array of chunk indices in decode order."""
+    chunk_len = np.asarray(chunk_len, dtype=np.int64)
+    order = sorted(range(chunk_len.size), key=lambda c: (-int(chunk_len[c]), c))
+    waves, cur, used = [], [], 0
+    for c in order:
+        b = chunk_state_bytes(d_model, dec_layers, int(chunk_len[c]))
+        if b > budget_bytes:
+            raise ValueError("one chunk exceeds the wave budget")
+        if cur and used + b > budget_bytes:
+            waves.append(np.array(cur, np.int32))
+            cur, used = [], 0
+        cur.append(c)
+        used += b
+    if cur:
+        waves.append(np.array(cur, np.int32))
+    return waves

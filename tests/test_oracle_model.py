@@ -1,0 +1,225 @@
+"""Pins for the oracle's model arithmetic.
+
+Each block is checked against an independent implementation (torch's CPU
+modules in float64), a closed form, or an invariant the architecture implies.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+import torch.nn.functional as F
+
+from oracle import e4m3, model
+from synth import ModelDims, make_weights
+
+torch.set_default_dtype(torch.float64)
+MINI = ModelDims("mini", 8, 128, 2, 256, 2, 2, 97)
+
+
+def T(x):
+    return torch.from_numpy(np.asarray(x, dtype=np.float64))
+
+
+def test_gelu_exact_form():
+    x = np.linspace(-6, 6, 1001)
+    np.testing.assert_allclose(model.gelu(x), F.gelu(T(x)).numpy(), atol=1e-15)
+    assert model.gelu(0.0) == 0.0
+    np.testing.assert_allclose(model.gelu(x) - model.gelu(-x), x, atol=1e-14)
+
+
+def test_layer_norm_matches_torch_and_moments():
+    rng = np.random.default_rng(0)
+    x = rng.normal(2.0, 3.0, size=(7, 384))
+    g, b = rng.normal(size=384), rng.normal(size=384)
+    ref = F.layer_norm(T(x), (384,), T(g), T(b), eps=1e-5).numpy()
+    np.testing.assert_allclose(model.layer_norm(x, g, b), ref, atol=1e-12)
+    y = model.layer_norm(x, np.ones(384), np.zeros(384))
+    var = x.var(axis=1)
+    np.testing.assert_allclose(y.mean(axis=1), 0, atol=1e-12)
+    np.testing.assert_allclose(y.var(axis=1), var / (var + 1e-5), rtol=1e-12)
+
+
+def test_sinusoids_closed_forms():
+    pe = model.sinusoids(1500, 1280)
+    assert pe.shape == (1500, 1280)
+    np.testing.assert_array_equal(pe[0, :640], 0.0)
+    np.testing.assert_array_equal(pe[0, 640:], 1.0)
+    np.testing.assert_allclose(pe[:, :640] ** 2 + pe[:, 640:] ** 2, 1.0, atol=1e-12)
+    np.testing.assert_allclose(pe[:, 0], np.sin(np.arange(1500)), atol=1e-12)
+    np.testing.assert_allclose(pe[1, 639], math.sin(1e-4), rtol=1e-9)   # slowest timescale
+
+
+@pytest.mark.parametrize("stride", [1, 2])
+def test_conv1d_matches_torch(stride):
+    rng = np.random.default_rng(1)
+    x = rng.normal(size=(16, 50))
+    w = rng.normal(size=(24, 16, 3))
+    b = rng.normal(size=24)
+    ref = F.conv1d(T(x)[None], T(w), T(b), stride=stride, padding=1)[0].numpy()
+    np.testing.assert_allclose(model.conv1d_k3(x, w, b, stride), ref, atol=1e-12)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_attention_brute_force_and_torch(causal):
+    rng = np.random.default_rng(2)
+    q, k, v = (rng.normal(size=(12, 64)) for _ in range(3))
+    out = model.attention(q, k, v, causal=causal)
+    for i in range(12):
+        n = i + 1 if causal else 12
+        s = [sum(q[i, c] * k[j, c] for c in range(64)) / 8.0 for j in range(n)]
+        m = max(s)
+        e = [math.exp(t - m) for t in s]
+        ref = sum(e[j] * v[j] for j in range(n)) / sum(e)
+        np.testing.assert_allclose(out[i], ref, atol=1e-12)
+    sdpa = F.scaled_dot_product_attention(T(q)[None], T(k)[None], T(v)[None],
+                                          is_causal=causal)[0].numpy()
+    np.testing.assert_allclose(out, sdpa, atol=1e-12)
+
+
+def _torch_encoder_layer(W, l, d, H, f):
+    layer = torch.nn.TransformerEncoderLayer(d, H, f, dropout=0.0, activation="gelu",
+                                             batch_first=True, norm_first=True)
+    p = f"enc.{l}."
+    sd = {
+        "self_attn.in_proj_weight": T(np.concatenate([W[p + "q.w"], W[p + "k.w"], W[p + "v.w"]])),
+        "self_attn.in_proj_bias": T(np.concatenate([W[p + "q.b"], W[p + "k.b"], W[p + "v.b"]])),
+        "self_attn.out_proj.weight": T(W[p + "o.w"]), "self_attn.out_proj.bias": T(W[p + "o.b"]),
+        "linear1.weight": T(W[p + "fc1.w"]), "linear1.bias": T(W[p + "fc1.b"]),
+        "linear2.weight": T(W[p + "fc2.w"]), "linear2.bias": T(W[p + "fc2.b"]),
+        "norm1.weight": T(W[p + "ln1.g"]), "norm1.bias": T(W[p + "ln1.b"]),
+        "norm2.weight": T(W[p + "ln2.g"]), "norm2.bias": T(W[p + "ln2.b"]),
+    }
+    layer.load_state_dict(sd)
+    return layer.eval()
+
+
+def test_encoder_layer_matches_torch_pre_ln_layer():
+    W = make_weights(MINI, 3, bf16=False, decoder=False)
+    h = np.random.default_rng(3).normal(size=(40, MINI.d_model))
+    ours = model.encoder_layer(h, W, 1, MINI.n_heads)
+    layer = _torch_encoder_layer(W, 1, MINI.d_model, MINI.n_heads, MINI.d_ffn)
+    with torch.no_grad():
+        ref = layer(T(h)[None])[0].numpy()
+    np.testing.assert_allclose(ours, ref, atol=1e-10)
+
+
+def test_decoder_matches_torch_pre_ln_decoder_layers():
+    W = make_weights(MINI, 4, bf16=False)
+    rng = np.random.default_rng(4)
+    enc = rng.normal(size=(30, MINI.d_model))
+    tok = rng.integers(0, MINI.vocab, size=9)
+    logits, info = model.decode_teacher_forced(tok, enc, W, MINI, return_hidden=True)
+    d, H = MINI.d_model, MINI.n_heads
+    x = (T(W["dec.tok"][tok]) + T(W["dec.pos"][:9]))[None]
+    mask = torch.nn.Transformer.generate_square_subsequent_mask(9)
+    for l in range(MINI.dec_layers):
+        p = f"dec.{l}."
+        layer = torch.nn.TransformerDecoderLayer(d, H, MINI.d_ffn, dropout=0.0,
+                                                 activation="gelu", batch_first=True,
+                                                 norm_first=True)
+        cat = lambda a, b, c: T(np.concatenate([W[p + a], W[p + b], W[p + c]]))  # noqa: E731
+        sd = {"self_attn.in_proj_weight": cat("sq.w", "sk.w", "sv.w"),
+              "self_attn.in_proj_bias": cat("sq.b", "sk.b", "sv.b"),
+              "self_attn.out_proj.weight": T(W[p + "so.w"]),
+              "self_attn.out_proj.bias": T(W[p + "so.b"]),
+              "multihead_attn.in_proj_weight": cat("cq.w", "ck.w", "cv.w"),
+              "multihead_attn.in_proj_bias": cat("cq.b", "ck.b", "cv.b"),
+              "multihead_attn.out_proj.weight": T(W[p + "co.w"]),
+              "multihead_attn.out_proj.bias": T(W[p + "co.b"]),
+              "linear1.weight": T(W[p + "fc1.w"]), "linear1.bias": T(W[p + "fc1.b"]),
+              "linear2.weight": T(W[p + "fc2.w"]), "linear2.bias": T(W[p + "fc2.b"]),
+              "norm1.weight": T(W[p + "ln1.g"]), "norm1.bias": T(W[p + "ln1.b"]),
+              "norm2.weight": T(W[p + "ln2.g"]), "norm2.bias": T(W[p + "ln2.b"]),
+              "norm3.weight": T(W[p + "ln3.g"]), "norm3.bias": T(W[p + "ln3.b"])}
+        layer.load_state_dict(sd)
+        with torch.no_grad():
+            x = layer.eval()(x, T(enc)[None], tgt_mask=mask, tgt_is_causal=True)
+    hf = F.layer_norm(x[0], (d,), T(W["dec.lnf.g"]), T(W["dec.lnf.b"]), eps=1e-5)
+    np.testing.assert_allclose(info["hidden"], hf.numpy(), atol=1e-10)
+    np.testing.assert_allclose(logits, (hf @ T(W["dec.tok"]).T).numpy(), atol=1e-10)
+
+
+def test_encoder_permutation_equivariance_without_positions():
+    W = make_weights(MINI, 5, bf16=False, decoder=False)
+    h = np.random.default_rng(5).normal(size=(33, MINI.d_model))
+    perm = np.random.default_rng(6).permutation(33)
+    a = model.encoder_layer(h, W, 0, MINI.n_heads)
+    b = model.encoder_layer(h[perm], W, 0, MINI.n_heads)
+    np.testing.assert_allclose(a[perm], b, atol=1e-12)
+
+
+@pytest.mark.parametrize("kv_fp8", [False, True])
+def test_decoder_causality_and_prefix_consistency(kv_fp8):
+    W = make_weights(MINI, 7, bf16=True)
+    rng = np.random.default_rng(7)
+    enc = rng.normal(size=(20, MINI.d_model))
+    tok = rng.integers(0, MINI.vocab, size=12)
+    full, _ = model.decode_teacher_forced(tok, enc, W, MINI, kv_fp8=kv_fp8)
+    tok2 = tok.copy()
+    tok2[8:] = rng.integers(0, MINI.vocab, size=4)
+    alt, _ = model.decode_teacher_forced(tok2, enc, W, MINI, kv_fp8=kv_fp8)
+    np.testing.assert_array_equal(full[:8], alt[:8])          # future tokens are invisible
+    for t in (4, 6, 11):                                      # cache-append == full pass
+        part, _ = model.decode_teacher_forced(tok[:t + 1], enc, W, MINI, kv_fp8=kv_fp8)
+        np.testing.assert_allclose(part[t], full[t], atol=1e-12)
+
+
+def test_key_bias_does_not_change_attention():
+    W = make_weights(MINI, 8, bf16=False)
+    rng = np.random.default_rng(8)
+    enc = rng.normal(size=(20, MINI.d_model))
+    tok = rng.integers(0, MINI.vocab, size=6)
+    a, _ = model.decode_teacher_forced(tok, enc, W, MINI)
+    W2 = dict(W)
+    W2["dec.0.sk.b"] = W["dec.0.sk.b"] + 5.0
+    W2["dec.1.ck.b"] = W["dec.1.ck.b"] - 3.0
+    b, _ = model.decode_teacher_forced(tok, enc, W2, MINI)
+    np.testing.assert_allclose(a, b, atol=1e-10)
+    W3 = dict(W)
+    W3["dec.0.sv.b"] = W["dec.0.sv.b"] + 0.5                  # a value bias does matter
+    c, _ = model.decode_teacher_forced(tok, enc, W3, MINI)
+    assert np.abs(a - c).max() > 1e-3
+
+
+def test_fp8_linear_exact_on_representable_inputs():
+    rng = np.random.default_rng(9)
+    vals = e4m3.decode_table()[:0x7F]
+    w = rng.choice(vals, size=(16, 32)) * rng.choice([-1, 1], size=(16, 32))
+    w[0, 0] = 448.0
+    x = rng.choice(vals, size=(5, 32))
+    x[:, 3] = 448.0
+    lin = model.Linear(w, np.zeros(16), fp8=True)
+    np.testing.assert_allclose(lin(x), x @ w.T, rtol=1e-15)
+    y = rng.normal(size=(5, 32))
+    rel = np.abs(lin(y) - model.Linear(w, np.zeros(16))(y)).max() / np.abs(y @ w.T).max()
+    assert rel < 0.1
+
+
+def test_fp8_row_scales_are_independent():
+    rng = np.random.default_rng(10)
+    w = rng.normal(size=(8, 16))
+    x = rng.normal(size=(4, 16))
+    lin = model.Linear(w, np.zeros(8), fp8=True)
+    full = lin(x)
+    for i in range(4):
+        np.testing.assert_array_equal(lin(x[i:i + 1])[0], full[i])
+
+
+def test_greedy_lowest_index_on_ties():
+    logits = np.array([[0.0, 3.0, 3.0, 1.0], [5.0, 5.0, 5.0, 5.0]])
+    assert list(model.greedy(logits)) == [1, 0]
+
+
+def test_conv_stem_shape_and_positions():
+    m = ModelDims("stem", 8, 64, 1, 128, 0, 0, 10)
+    W = make_weights(m, 11, bf16=False, decoder=False)
+    W0 = dict(W)
+    W0["enc.conv1.w"] = np.zeros_like(W["enc.conv1.w"])
+    W0["enc.conv1.b"] = np.zeros_like(W["enc.conv1.b"])
+    mel = np.random.default_rng(11).normal(size=(8, 3000))
+    out = model.conv_stem(mel, W0)
+    assert out.shape == (1500, 64)
+    # zero conv1 -> conv2 sees zeros -> GELU(b2) + PE on every row
+    np.testing.assert_allclose(out, model.gelu(W["enc.conv2.b"])[None, :] + model.sinusoids(1500, 64),
+                               atol=1e-12)

@@ -1,0 +1,54 @@
+"""Pins for the oracle's chunk table and wave packing."""
+import numpy as np
+import pytest
+
+from oracle import plan
+from synth import serving_requests
+
+
+def test_chunk_table_counts():
+    req, idx, valid = plan.chunk_table([480000, 480001, 1, 1_000_000])
+    assert list(req) == [0, 1, 1, 2, 3, 3, 3]
+    assert list(idx) == [0, 0, 1, 0, 0, 1, 2]
+    assert list(valid) == [480000, 480000, 1, 1, 480000, 480000, 40000]
+
+
+def test_chunk_state_bytes_closed_form():
+    # large-v3 decoder: 32 layers x (2 x 1500 x 1280 x 2 + 2 x L x 1280) + 448 x 4
+    assert plan.chunk_state_bytes(1280, 32, 448) == 32 * (7_680_000 + 1_146_880) + 1792
+
+
+@pytest.mark.parametrize("budget", [10**9, 5 * 10**9, 180 * 10**9])
+def test_waves_cover_each_chunk_once_within_budget(budget):
+    rng = np.random.default_rng(0)
+    lens = rng.integers(64, 449, size=300)
+    waves = plan.plan_waves(lens, 1280, 4, budget)
+    allc = np.concatenate(waves)
+    assert sorted(allc.tolist()) == list(range(300))
+    prev_min = None
+    for w in waves:
+        assert sum(plan.chunk_state_bytes(1280, 4, lens[c]) for c in w) <= budget
+        wl = lens[w]
+        assert (np.diff(wl) <= 0).all()                       # longest first
+        if prev_min is not None:
+            assert wl[0] <= prev_min
+        prev_min = wl[-1]
+    # greedy: each wave but the last could not take the next chunk
+    for a, b in zip(waves[:-1], waves[1:]):
+        used = sum(plan.chunk_state_bytes(1280, 4, lens[c]) for c in a)
+        assert used + plan.chunk_state_bytes(1280, 4, lens[b[0]]) > budget
+
+
+def test_serving_batch_waves():
+    sb = serving_requests(0, n_req=48, with_audio=False)
+    req, idx, valid = plan.chunk_table(sb.req_samples)
+    assert req.size == sb.chunk_len.size
+    assert 600 <= req.size <= 1100
+    waves = plan.plan_waves(sb.chunk_len, 1280, 32, 180 * 10**9)
+    assert len(waves) == 2
+    assert int(valid.sum()) == int(sb.req_samples.sum())
+
+
+def test_oversize_chunk_rejected():
+    with pytest.raises(ValueError):
+        plan.plan_waves([448], 1280, 32, 10**6)
