@@ -1,0 +1,113 @@
+"""The C-ABI library loads, exports every declared symbol, and its host-only
+logic (weight layout, wave plan, argument checks) behaves -- no GPU needed."""
+import ctypes
+import os
+import re
+import subprocess
+
+import numpy as np
+import pytest
+
+import whisper_encoder_decoder_log_b300 as wb
+from oracle import plan as oplan
+from synth import LARGE_V3, TINY, TURBO, decoder_tensor_specs, encoder_tensor_specs, serving_requests
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from whisper_encoder_decoder_log_b300 import build
+    build.build()
+    yield
+
+
+def header_functions():
+    text = open(os.path.join(ROOT, "include", "wb.h")).read()
+    return sorted(set(re.findall(r"WB_API\s+[\w\s\*]+?\b(wb_\w+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported():
+    names = header_functions()
+    assert len(names) >= 20
+    out = subprocess.run(["nm", "-D", "--defined-only", wb.LIB_PATH], capture_output=True, text=True).stdout
+    exported = set(re.findall(r" T (wb_\w+)", out))
+    missing = [n for n in names if n not in exported]
+    assert not missing, missing
+    L = ctypes.CDLL(wb.LIB_PATH)
+    for n in names:
+        assert getattr(L, n) is not None
+    assert sorted(wb.exported_symbols()) == names
+
+
+def test_version_and_error_text():
+    assert wb.wb_version() == 100
+    assert isinstance(wb.lib().wb_last_error(), bytes)
+
+
+@pytest.mark.parametrize("dims,prec", [(TINY, wb.PREC_FP32), (LARGE_V3, wb.PREC_BF16), (TURBO, wb.PREC_MIXED_FP8)])
+def test_weight_layout_is_complete_and_disjoint(dims, prec):
+    desc = wb.make_desc(dims, prec, prec != wb.PREC_FP32)
+    total = wb.wb_weights_bytes(desc)
+    wsz = 4 if prec == wb.PREC_FP32 else 2
+    spans = []
+    for name, shape, kind in encoder_tensor_specs(dims) + decoder_tensor_specs(dims):
+        off, n = wb.wb_weight_offset(desc, name)
+        assert n == int(np.prod(shape)), name
+        assert off % 16 == 0, name
+        size = n * (wsz if (name.endswith(".w") or name in ("dec.tok", "dec.pos")) else 4)
+        spans.append((off, off + size, name))
+    spans.sort()
+    for (a0, a1, na), (b0, b1, nb) in zip(spans, spans[1:]):
+        assert a1 <= b0, (na, nb)
+    assert spans[-1][1] <= total
+    # fused operands are contiguous
+    q, _ = wb.wb_weight_offset(desc, "enc.0.q.w")
+    k, _ = wb.wb_weight_offset(desc, "enc.0.k.w")
+    v, _ = wb.wb_weight_offset(desc, "enc.0.v.w")
+    d = dims.d_model
+    assert k == q + d * d * wsz and v == k + d * d * wsz
+    ck0, _ = wb.wb_weight_offset(desc, "dec.0.ck.w")
+    cv_last, _ = wb.wb_weight_offset(desc, f"dec.{dims.dec_layers - 1}.cv.w")
+    assert cv_last == ck0 + (2 * dims.dec_layers - 1) * d * d * wsz
+
+
+def test_unknown_weight_name_is_an_error():
+    desc = wb.make_desc(TINY, wb.PREC_FP32, False)
+    with pytest.raises(wb.WBError) as e:
+        wb.wb_weight_offset(desc, "enc.99.q.w")
+    assert e.value.status == -1
+
+
+@pytest.mark.parametrize("budget", [2 * 10**9, 50 * 10**9, 180 * 10**9])
+def test_wave_plan_matches_oracle_bit_exact(budget):
+    sb = serving_requests(0, n_req=48, with_audio=False)
+    desc = wb.make_desc(LARGE_V3, wb.PREC_MIXED_FP8, True)
+    wave, order, nw = wb.wb_plan_waves(desc, sb.chunk_len, budget)
+    ref = oplan.plan_waves(sb.chunk_len, LARGE_V3.d_model, LARGE_V3.dec_layers, budget)
+    assert nw == len(ref)
+    assert np.array_equal(order, np.concatenate(ref))
+    for w, chunks in enumerate(ref):
+        assert (wave[chunks] == w).all()
+
+
+def test_wave_plan_rejects_oversize_chunk():
+    desc = wb.make_desc(LARGE_V3, wb.PREC_BF16, True)
+    with pytest.raises(wb.WBError) as e:
+        wb.wb_plan_waves(desc, np.array([448], np.int32), 10**6)
+    assert e.value.status == -2
+
+
+def test_host_side_argument_checks_need_no_gpu():
+    L = wb.lib()
+    assert L.wb_mel(None, 1, 128, None, None) == -1
+    assert L.wb_mel(16, 0, 128, 16, None) == -2
+    assert L.wb_mel(16, 1, 64, 16, None) == -2
+    assert L.wb_mel(8, 1, 128, 16, None) == -3
+    bad = wb.ModelDesc(128, 1000, 20, 5120, 1, 1, 10, 1, 0)
+    h = ctypes.c_void_p(0)
+    assert L.wb_model_create(ctypes.byref(bad), 16, ctypes.byref(h)) == -1
+    assert L.wb_gemm(None, None, 1, 8, 64, 0, None, None, None, 0, None, 0, None) == -1
+    assert L.wb_gemm(16, 16, 1, 8, 63, 0, None, None, None, 0, 16, 0, None) == -2
+    assert L.wb_decode_step(None, 1, None, None) == -1
+    assert L.wb_weights_bytes(ctypes.byref(bad)) == 0

@@ -1,0 +1,134 @@
+"""GPU parity of the single kernels reachable through the C ABI: the log-Mel
+front end, the tcgen05 GEMM (bf16 and E4M3) and the E4M3 quantiser, against
+the CPU oracle on the same seeded inputs."""
+import numpy as np
+import pytest
+import torch
+
+import whisper_encoder_decoder_log_b300 as wb
+from oracle import e4m3 as oe4m3
+from oracle import mel as omel
+from oracle import model as omodel
+from synth import batch_audio, round_to_bf16
+
+pytestmark = pytest.mark.gpu
+
+MEL_TOL = 1e-4      # absolute, normalised log domain
+
+
+def run_mel(audio, n_mels):
+    a = torch.from_numpy(audio).cuda()
+    out = torch.empty(audio.shape[0], n_mels, 3000, device="cuda")
+    wb.wb_mel(a, n_mels, out)
+    wb.wb_sync_status()
+    return out.cpu().numpy()
+
+
+@pytest.mark.parametrize("n_mels,kind", [(128, "pink"), (80, "sine"), (128, "sine")])
+def test_mel_matches_oracle(n_mels, kind):
+    audio = batch_audio(kind, 3, seed=11)
+    got = run_mel(audio, n_mels)
+    for i in range(3):
+        ref = omel.log_mel(audio[i].astype(np.float64), n_mels)
+        err = np.abs(got[i] - ref).max()
+        assert err <= MEL_TOL, (i, err)
+
+
+def test_mel_silence_and_edge_cases():
+    audio = np.zeros((2, 480000), np.float32)
+    audio[1, 240000] = 1.0          # a single click: energy in ~3 frames only
+    got = run_mel(audio, 128)
+    assert (got[0] == -1.5).all()
+    ref = omel.log_mel(audio[1].astype(np.float64), 128)
+    assert np.abs(got[1] - ref).max() <= MEL_TOL
+
+
+def test_mel_full_batch_sampled():
+    """The 64-chunk mel workload; the oracle checks a sample of whole chunks."""
+    audio = batch_audio("pink", 64, seed=2)
+    got = run_mel(audio, 128)
+    for i in (0, 17, 63):
+        ref = omel.log_mel(audio[i].astype(np.float64), 128)
+        assert np.abs(got[i] - ref).max() <= MEL_TOL, i
+    # chunk independence: chunk 17 alone gives the same bits
+    alone = run_mel(audio[17:18].copy(), 128)
+    assert np.array_equal(alone[0], got[17])
+
+
+def _bf16(x):
+    return round_to_bf16(np.asarray(x, np.float32))
+
+
+@pytest.mark.parametrize("M,N,K", [(300, 320, 640), (128, 256, 64), (3000, 1280, 1280), (37, 3840, 1280),
+                                   (1, 64, 128), (5, 51866 - 51866 % 8, 384)])
+def test_gemm_bf16_matches_oracle(M, N, K):
+    rng = np.random.default_rng(M * 7 + N)
+    a = _bf16(rng.normal(size=(M, K)))
+    b = _bf16(rng.normal(size=(N, K)) * 0.05)
+    bias = rng.normal(size=N).astype(np.float32)
+    A = torch.from_numpy(a).to(torch.bfloat16).cuda()
+    B = torch.from_numpy(b).to(torch.bfloat16).cuda()
+    C = torch.empty(M, N, device="cuda")
+    wb.wb_gemm(A, B, C, bias=torch.from_numpy(bias).cuda())
+    wb.wb_sync_status()
+    ref = omodel.Linear(b, bias)(a)
+    got = C.cpu().numpy()
+    scale = np.abs(a).max() * np.abs(b).max() * np.sqrt(K)
+    assert np.abs(got - ref).max() <= 1e-5 * scale + 1e-6
+
+
+def test_gemm_bf16_gelu_bf16_out():
+    rng = np.random.default_rng(3)
+    M, N, K = 500, 512, 256
+    a, b = _bf16(rng.normal(size=(M, K))), _bf16(rng.normal(size=(N, K)) * 0.05)
+    bias = rng.normal(size=N).astype(np.float32)
+    C = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+    wb.wb_gemm(torch.from_numpy(a).to(torch.bfloat16).cuda(), torch.from_numpy(b).to(torch.bfloat16).cuda(), C,
+               bias=torch.from_numpy(bias).cuda(), gelu=True)
+    wb.wb_sync_status()
+    ref = omodel.gelu(omodel.Linear(b, bias)(a))
+    got = C.float().cpu().numpy()
+    assert np.abs(got - ref).max() <= 2 ** -8 * np.abs(ref).max() + 1e-3
+
+
+@pytest.mark.parametrize("M,N,K", [(200, 256, 256), (1500, 1280, 1280), (3, 5120, 1280)])
+def test_gemm_e4m3_matches_oracle(M, N, K):
+    rng = np.random.default_rng(N + K)
+    x = rng.normal(size=(M, K)).astype(np.float32)
+    w = (rng.normal(size=(N, K)) * 0.02).astype(np.float32)
+    lin = omodel.Linear(w, np.zeros(N), fp8=True)
+    ref = lin(x)
+    # identical codes and scales on both sides: the oracle's own quantisation
+    amax = np.abs(x).max(axis=1)
+    sx = np.array([oe4m3.scale_of(a) for a in amax], np.float32)
+    qx = np.stack([oe4m3.quantise(x[i], sx[i]) for i in range(M)])
+    A = torch.from_numpy(qx).cuda()
+    B = torch.from_numpy(lin.w_codes).cuda()
+    C = torch.empty(M, N, device="cuda")
+    wb.wb_gemm(A, B, C, row_scale=torch.from_numpy(sx).cuda(),
+               col_scale=torch.full((N,), float(lin.w_scale), device="cuda"))
+    wb.wb_sync_status()
+    got = C.cpu().numpy()
+    assert np.abs(got - ref).max() <= 1e-5 * np.abs(ref).max() * np.sqrt(K / 64) + 1e-7
+
+
+@pytest.mark.parametrize("bf16", [False, True])
+@pytest.mark.parametrize("n", [1, 1000, 1 << 20])
+def test_quantiser_codes_bit_exact(bf16, n):
+    rng = np.random.default_rng(n)
+    x = rng.normal(0, 3, size=n).astype(np.float32)
+    if bf16:
+        x = _bf16(x)
+    X = torch.from_numpy(x).cuda()
+    if bf16:
+        X = X.to(torch.bfloat16)
+    codes = torch.empty(n, dtype=torch.uint8, device="cuda")
+    scale = torch.empty(1, device="cuda")
+    wb.wb_quantise_e4m3(X, codes, scale)
+    out = torch.empty(n, device="cuda")
+    wb.wb_dequantise_e4m3(codes, scale, out)
+    wb.wb_sync_status()
+    ref_codes, ref_scale = oe4m3.quantise_tensor(x)
+    assert np.float32(scale.item()) == ref_scale
+    assert np.array_equal(codes.cpu().numpy(), ref_codes)
+    assert np.array_equal(out.cpu().numpy(), (oe4m3.decode(ref_codes) * np.float64(ref_scale)).astype(np.float32))

@@ -1,0 +1,261 @@
+"""Python binding of libwb.so, the B300 Whisper transcription hot path.
+
+Argument marshalling only: every function below forwards device pointers,
+sizes and the current CUDA stream to the C ABI declared in include/wb.h and
+raises WBError on a negative status.  There is no Python or CPU fallback: if
+the shared library is missing, the first call raises.  PyTorch supplies device
+memory and streams.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Dict, Optional
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libwb.so")
+
+PREC_FP32, PREC_BF16, PREC_MIXED_FP8 = 0, 1, 2
+CHUNK_SAMPLES, N_FRAMES, N_CTX, MAX_POS = 480000, 3000, 1500, 448
+
+_lib = None
+
+
+class WBError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"libwb status {status}: {msg}")
+        self.status = status
+
+
+class ModelDesc(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in ("n_mels", "d_model", "n_heads", "d_ffn", "enc_layers",
+                                               "dec_layers", "vocab", "precision", "kv_fp8")]
+
+
+_VP, _I64, _I32, _SZ, _U64 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_size_t, ctypes.c_uint64
+_SIGS = {
+    "wb_last_error": (ctypes.c_char_p, []),
+    "wb_version": (ctypes.c_int, []),
+    "wb_mel": (ctypes.c_int, [_VP, _I64, _I32, _VP, _VP]),
+    "wb_weights_bytes": (_SZ, [ctypes.POINTER(ModelDesc)]),
+    "wb_weight_offset": (ctypes.c_int, [ctypes.POINTER(ModelDesc), ctypes.c_char_p, ctypes.POINTER(_SZ),
+                                        ctypes.POINTER(_I64)]),
+    "wb_model_create": (ctypes.c_int, [ctypes.POINTER(ModelDesc), _VP, ctypes.POINTER(_VP)]),
+    "wb_model_destroy": (ctypes.c_int, [_VP]),
+    "wb_encode_workspace_size": (_SZ, [_VP, _I64]),
+    "wb_encode": (ctypes.c_int, [_VP, _VP, _I64, _VP, _VP, _SZ, _VP]),
+    "wb_decoder_workspace_size": (_SZ, [_VP, _I64, _VP]),
+    "wb_decoder_init": (ctypes.c_int, [_VP, _I64, _VP, _VP, _VP, _VP, _SZ, _VP, ctypes.POINTER(_VP)]),
+    "wb_decode_prefix": (ctypes.c_int, [_VP, _I32, _VP, _VP]),
+    "wb_decode_step": (ctypes.c_int, [_VP, _I64, _VP, _VP]),
+    "wb_decoder_position": (_I32, [_VP]),
+    "wb_decoder_destroy": (ctypes.c_int, [_VP]),
+    "wb_transcribe_workspace_size": (_SZ, [_VP, _I32, _VP, _VP, _U64]),
+    "wb_transcribe_batch": (ctypes.c_int, [_VP, _VP, _VP, _VP, _I32, _VP, _VP, _VP, _U64, _VP, _SZ, _VP, _VP]),
+    "wb_plan_waves": (ctypes.c_int, [ctypes.POINTER(ModelDesc), _I32, _VP, _U64, _VP, _VP, _VP]),
+    "wb_quantise_e4m3": (ctypes.c_int, [_VP, _I32, _I64, _VP, _VP, _VP]),
+    "wb_dequantise_e4m3": (ctypes.c_int, [_VP, _VP, _I64, _VP, _VP]),
+    "wb_sync_status": (ctypes.c_int, [_VP, _VP]),
+    "wb_gemm": (ctypes.c_int, [_VP, _VP, _I64, _I64, _I64, _I32, _VP, _VP, _VP, _I32, _VP, _I32, _VP]),
+}
+
+
+def lib():
+    """Load libwb.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                               "`python -m whisper_encoder_decoder_log_b300.build`")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGS.items():
+            f = getattr(L, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = L
+    return _lib
+
+
+def exported_symbols():
+    return list(_SIGS)
+
+
+def _check(st: int):
+    if st != 0:
+        raise WBError(st, lib().wb_last_error().decode())
+
+
+def _p(t) -> Optional[int]:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream=None) -> Optional[int]:
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream
+
+
+def _host_arr(a, dtype):
+    a = np.ascontiguousarray(a, dtype=dtype)
+    return a, a.ctypes.data
+
+
+# ----------------------------------------------------------------- thin wrappers
+
+def wb_version() -> int:
+    return lib().wb_version()
+
+
+def wb_mel(audio, n_mels: int, mel, stream=None):
+    _check(lib().wb_mel(_p(audio), audio.shape[0], n_mels, _p(mel), _stream(stream)))
+
+
+def wb_weights_bytes(desc: ModelDesc) -> int:
+    return lib().wb_weights_bytes(ctypes.byref(desc))
+
+
+def wb_weight_offset(desc: ModelDesc, name: str):
+    off, n = _SZ(0), _I64(0)
+    _check(lib().wb_weight_offset(ctypes.byref(desc), name.encode(), ctypes.byref(off), ctypes.byref(n)))
+    return off.value, n.value
+
+
+def wb_model_create(desc: ModelDesc, weights) -> int:
+    h = _VP(0)
+    _check(lib().wb_model_create(ctypes.byref(desc), _p(weights), ctypes.byref(h)))
+    return h.value
+
+
+def wb_model_destroy(model: int):
+    _check(lib().wb_model_destroy(model))
+
+
+def wb_encode_workspace_size(model: int, B: int) -> int:
+    return lib().wb_encode_workspace_size(model, B)
+
+
+def wb_encode(model: int, mel, enc, workspace, stream=None):
+    _check(lib().wb_encode(model, _p(mel), mel.shape[0], _p(enc), _p(workspace), workspace.numel() *
+                           workspace.element_size(), _stream(stream)))
+
+
+def wb_decoder_workspace_size(model: int, chunk_len) -> int:
+    arr, ptr = _host_arr(chunk_len, np.int32)
+    return lib().wb_decoder_workspace_size(model, arr.size, ptr)
+
+
+def wb_decoder_init(model: int, chunk_len, enc, tokens, workspace, stream=None) -> int:
+    arr, ptr = _host_arr(chunk_len, np.int32)
+    h = _VP(0)
+    _check(lib().wb_decoder_init(model, arr.size, ptr, _p(enc), _p(tokens), _p(workspace),
+                                 workspace.numel() * workspace.element_size(), _stream(stream), ctypes.byref(h)))
+    return h.value
+
+
+def wb_decode_prefix(dec: int, P: int, logits=None, stream=None):
+    _check(lib().wb_decode_prefix(dec, P, _p(logits), _stream(stream)))
+
+
+def wb_decode_step(dec: int, n_active: int, logits=None, stream=None):
+    _check(lib().wb_decode_step(dec, n_active, _p(logits), _stream(stream)))
+
+
+def wb_decoder_position(dec: int) -> int:
+    return lib().wb_decoder_position(dec)
+
+
+def wb_decoder_destroy(dec: int):
+    _check(lib().wb_decoder_destroy(dec))
+
+
+def wb_transcribe_workspace_size(model: int, req_samples, chunk_len, budget: int) -> int:
+    rs, rsp = _host_arr(req_samples, np.int64)
+    cl, clp = _host_arr(chunk_len, np.int32)
+    return lib().wb_transcribe_workspace_size(model, rs.size, rsp, clp, budget)
+
+
+def wb_transcribe_batch(model: int, audio, req_offset, req_samples, prefix, chunk_len, tokens, budget: int,
+                        workspace, stream=None) -> int:
+    ro, rop = _host_arr(req_offset, np.int64)
+    rs, rsp = _host_arr(req_samples, np.int64)
+    pf, pfp = _host_arr(prefix, np.int32)
+    cl, clp = _host_arr(chunk_len, np.int32)
+    nw = _I32(0)
+    _check(lib().wb_transcribe_batch(model, _p(audio), rop, rsp, rs.size, pfp, clp, _p(tokens), budget,
+                                     _p(workspace), workspace.numel() * workspace.element_size(),
+                                     ctypes.addressof(nw), _stream(stream)))
+    return nw.value
+
+
+def wb_plan_waves(desc: ModelDesc, chunk_len, budget: int):
+    cl, clp = _host_arr(chunk_len, np.int32)
+    wave = np.zeros(cl.size, np.int32)
+    order = np.zeros(cl.size, np.int32)
+    nw = _I32(0)
+    _check(lib().wb_plan_waves(ctypes.byref(desc), cl.size, clp, budget, wave.ctypes.data, order.ctypes.data,
+                               ctypes.addressof(nw)))
+    return wave, order, nw.value
+
+
+def wb_quantise_e4m3(x, codes, scale, stream=None):
+    import torch
+    _check(lib().wb_quantise_e4m3(_p(x), 1 if x.dtype == torch.bfloat16 else 0, x.numel(), _p(codes), _p(scale),
+                                  _stream(stream)))
+
+
+def wb_dequantise_e4m3(codes, scale, out, stream=None):
+    _check(lib().wb_dequantise_e4m3(_p(codes), _p(scale), codes.numel(), _p(out), _stream(stream)))
+
+
+def wb_gemm(A, B, C, bias=None, gelu=False, row_scale=None, col_scale=None, stream=None):
+    import torch
+    fp8 = A.dtype == torch.uint8
+    M, K = A.shape
+    N = B.shape[0]
+    _check(lib().wb_gemm(_p(A), _p(B), M, N, K, 1 if fp8 else 0, _p(row_scale), _p(col_scale), _p(bias),
+                         1 if gelu else 0, _p(C), 1 if C.dtype == torch.bfloat16 else 0, _stream(stream)))
+
+
+def wb_sync_status(model: Optional[int] = None, stream=None):
+    _check(lib().wb_sync_status(model, _stream(stream)))
+
+
+# ----------------------------------------------------------------- marshalling helpers
+
+def make_desc(dims, precision: int, kv_fp8: bool) -> ModelDesc:
+    return ModelDesc(dims.n_mels, dims.d_model, dims.n_heads, dims.d_ffn, dims.enc_layers, dims.dec_layers,
+                     dims.vocab, precision, 1 if kv_fp8 else 0)
+
+
+def pack_weights(desc: ModelDesc, tensors: Dict[str, np.ndarray], device="cuda"):
+    """Copy named tensors into one device buffer at the offsets libwb reports.
+
+    Matrices are stored as bf16 (values must already be bf16-exact) unless the
+    model is fp32; vectors as fp32.  Returns a uint8 CUDA tensor.
+    """
+    import torch
+    total = wb_weights_bytes(desc)
+    if total == 0:
+        raise WBError(-1, "invalid model descriptor")
+    host = torch.zeros(total, dtype=torch.uint8, pin_memory=torch.cuda.is_available())
+    hnp = host.numpy()
+    bf = desc.precision != PREC_FP32
+    for name, arr in tensors.items():
+        off, n = wb_weight_offset(desc, name)
+        a = np.ascontiguousarray(arr, dtype=np.float32).reshape(-1)
+        if a.size != n:
+            raise ValueError(f"{name}: {a.size} elements, layout expects {n}")
+        is_matrix = name.endswith(".w") or name in ("dec.tok", "dec.pos")
+        if bf and is_matrix:
+            bits = (a.view(np.uint32) >> 16).astype(np.uint16)
+            hnp[off:off + 2 * n] = bits.view(np.uint8)
+        else:
+            hnp[off:off + 4 * n] = a.view(np.uint8)
+    return host.to(device, non_blocking=True)

@@ -1,0 +1,1102 @@
+// C ABI and host orchestration (include/wb.h).  The host issues kernels on
+// the caller's stream and never reads device data inside a step: per-chunk
+// decode lengths are host-known, and the chunks still decoding at a step are
+// a prefix of the (length-sorted) batch.
+#include <algorithm>
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <unordered_map>
+#include <vector>
+
+#include "attn.cuh"
+#include "common.cuh"
+#include "gemm.cuh"
+#include "internal.h"
+#include "layers.cuh"
+
+namespace wb {
+
+static thread_local std::string t_last_error;
+static std::mutex g_err_mu;
+static unsigned* g_lib_err[64] = {};
+
+void set_error(const std::string& msg) { t_last_error = msg; }
+wb_status fail(wb_status code, const std::string& msg) {
+    t_last_error = msg;
+    return code;
+}
+wb_status cuda_fail(cudaError_t e, const char* what) {
+    t_last_error = std::string(what) + ": " + cudaGetErrorString(e);
+    return WB_ERR_CUDA;
+}
+unsigned* lib_error_word() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lk(g_err_mu);
+    if (!g_lib_err[dev]) {
+        if (cudaMalloc(&g_lib_err[dev], sizeof(unsigned)) != cudaSuccess) return nullptr;
+        cudaMemset(g_lib_err[dev], 0, sizeof(unsigned));
+    }
+    return g_lib_err[dev];
+}
+
+namespace {
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// ------------------------------------------------------------------ weight layout
+struct Entry {
+    size_t offset;
+    int64_t numel;
+    bool matrix;
+};
+struct Layout {
+    std::unordered_map<std::string, Entry> map;
+    size_t total = 0;
+};
+struct LayoutBuilder {
+    Layout* L;
+    size_t wsz;
+    size_t cur = 0;
+    void group() { cur = align_up(cur, 256); }
+    void add(const std::string& n, int64_t numel, bool matrix) {
+        L->map[n] = Entry{cur, numel, matrix};
+        cur += (size_t)numel * (matrix ? wsz : 4);
+    }
+};
+
+bool valid_desc(const wb_model_desc* d, std::string* why) {
+    if (!d) { *why = "null descriptor"; return false; }
+    if (d->n_mels != 80 && d->n_mels != 128) { *why = "n_mels must be 80 or 128"; return false; }
+    if (d->d_model <= 0 || d->d_model % 64 || d->d_model > 1280) { *why = "d_model must be a multiple of 64, <= 1280"; return false; }
+    if (d->n_heads * 64 != d->d_model) { *why = "n_heads must be d_model / 64"; return false; }
+    if (d->d_ffn <= 0 || d->d_ffn % 256) { *why = "d_ffn must be a positive multiple of 256"; return false; }
+    if (d->enc_layers < 0 || d->dec_layers < 0 || d->enc_layers > 256 || d->dec_layers > 256) { *why = "bad layer count"; return false; }
+    if (d->vocab <= 0) { *why = "vocab must be positive"; return false; }
+    if (d->precision < WB_PREC_FP32 || d->precision > WB_PREC_MIXED_FP8) { *why = "bad precision"; return false; }
+    if (d->kv_fp8 && d->precision == WB_PREC_FP32) { *why = "kv_fp8 needs a bf16 precision"; return false; }
+    return true;
+}
+
+std::string nm(const char* pre, int l, const char* name) { return std::string(pre) + std::to_string(l) + "." + name; }
+
+void build_layout(const wb_model_desc& d, Layout* L) {
+    LayoutBuilder b{L, (size_t)(d.precision == WB_PREC_FP32 ? 4 : 2)};
+    const int64_t D = d.d_model, F = d.d_ffn, C = d.n_mels;
+    b.group(); b.add("enc.conv1.w", D * C * 3, true);
+    b.group(); b.add("enc.conv1.b", D, false);
+    b.group(); b.add("enc.conv2.w", D * D * 3, true);
+    b.group(); b.add("enc.conv2.b", D, false);
+    for (int l = 0; l < d.enc_layers; ++l) {
+        b.group(); b.add(nm("enc.", l, "ln1.g"), D, false); b.add(nm("enc.", l, "ln1.b"), D, false);
+        b.group(); b.add(nm("enc.", l, "q.w"), D * D, true); b.add(nm("enc.", l, "k.w"), D * D, true); b.add(nm("enc.", l, "v.w"), D * D, true);
+        b.group(); b.add(nm("enc.", l, "q.b"), D, false); b.add(nm("enc.", l, "k.b"), D, false); b.add(nm("enc.", l, "v.b"), D, false);
+        b.group(); b.add(nm("enc.", l, "o.w"), D * D, true);
+        b.group(); b.add(nm("enc.", l, "o.b"), D, false);
+        b.group(); b.add(nm("enc.", l, "ln2.g"), D, false); b.add(nm("enc.", l, "ln2.b"), D, false);
+        b.group(); b.add(nm("enc.", l, "fc1.w"), F * D, true);
+        b.group(); b.add(nm("enc.", l, "fc1.b"), F, false);
+        b.group(); b.add(nm("enc.", l, "fc2.w"), D * F, true);
+        b.group(); b.add(nm("enc.", l, "fc2.b"), D, false);
+    }
+    b.group(); b.add("enc.lnp.g", D, false); b.add("enc.lnp.b", D, false);
+    b.group(); b.add("dec.tok", (int64_t)d.vocab * D, true);
+    b.group(); b.add("dec.pos", (int64_t)kMaxPos * D, true);
+    for (int l = 0; l < d.dec_layers; ++l) {
+        b.group(); b.add(nm("dec.", l, "ln1.g"), D, false); b.add(nm("dec.", l, "ln1.b"), D, false);
+        b.group(); b.add(nm("dec.", l, "sq.w"), D * D, true); b.add(nm("dec.", l, "sk.w"), D * D, true); b.add(nm("dec.", l, "sv.w"), D * D, true);
+        b.group(); b.add(nm("dec.", l, "sq.b"), D, false); b.add(nm("dec.", l, "sk.b"), D, false); b.add(nm("dec.", l, "sv.b"), D, false);
+        b.group(); b.add(nm("dec.", l, "so.w"), D * D, true);
+        b.group(); b.add(nm("dec.", l, "so.b"), D, false);
+        b.group(); b.add(nm("dec.", l, "ln2.g"), D, false); b.add(nm("dec.", l, "ln2.b"), D, false);
+        b.group(); b.add(nm("dec.", l, "cq.w"), D * D, true);
+        b.group(); b.add(nm("dec.", l, "cq.b"), D, false);
+        b.group(); b.add(nm("dec.", l, "co.w"), D * D, true);
+        b.group(); b.add(nm("dec.", l, "co.b"), D, false);
+        b.group(); b.add(nm("dec.", l, "ln3.g"), D, false); b.add(nm("dec.", l, "ln3.b"), D, false);
+        b.group(); b.add(nm("dec.", l, "fc1.w"), F * D, true);
+        b.group(); b.add(nm("dec.", l, "fc1.b"), F, false);
+        b.group(); b.add(nm("dec.", l, "fc2.w"), D * F, true);
+        b.group(); b.add(nm("dec.", l, "fc2.b"), D, false);
+    }
+    // cross-attention K and V of every decoder layer form one [L * 2d, d] operand
+    b.group();
+    for (int l = 0; l < d.dec_layers; ++l) { b.add(nm("dec.", l, "ck.w"), D * D, true); b.add(nm("dec.", l, "cv.w"), D * D, true); }
+    b.group();
+    for (int l = 0; l < d.dec_layers; ++l) { b.add(nm("dec.", l, "ck.b"), D, false); b.add(nm("dec.", l, "cv.b"), D, false); }
+    b.group(); b.add("dec.lnf.g", D, false); b.add("dec.lnf.b", D, false);
+    b.group();
+    L->total = b.cur;
+}
+
+void sinusoids(int n_ctx, int d, std::vector<float>& out) {
+    out.resize((size_t)n_ctx * d);
+    const int half = d / 2;
+    const double inc = std::log(10000.0) / (half - 1);
+    for (int s = 0; s < n_ctx; ++s)
+        for (int i = 0; i < half; ++i) {
+            const double a = s * std::exp(-i * inc);
+            out[(size_t)s * d + i] = (float)std::sin(a);
+            out[(size_t)s * d + half + i] = (float)std::cos(a);
+        }
+}
+
+__global__ void expand_scale_kernel(float* col_scale, int64_t rows_each) {
+    const float s = col_scale[0];
+    for (int64_t r = 1 + threadIdx.x; r < rows_each; r += blockDim.x) col_scale[r] = s;
+}
+
+// Bump allocator over a caller-provided workspace.
+struct Carve {
+    uint8_t* base;
+    size_t cap;
+    size_t cur = 0;
+    bool overflow = false;
+    template <typename T>
+    T* take(size_t count) {
+        cur = align_up(cur, 256);
+        T* p = reinterpret_cast<T*>(base ? base + cur : nullptr);
+        cur += count * sizeof(T);
+        if (base && cur > cap) overflow = true;
+        return p;
+    }
+};
+
+}  // namespace
+}  // namespace wb
+
+using namespace wb;
+
+struct FP8Weight {
+    uint8_t* w = nullptr;
+    float* col_scale = nullptr;
+};
+
+struct wb_model {
+    wb_model_desc desc{};
+    int device = 0;
+    const uint8_t* w = nullptr;
+    Layout layout;
+    void* conv1_w = nullptr;
+    void* conv2_w = nullptr;
+    float* pe = nullptr;
+    unsigned* err = nullptr;
+    unsigned* scratch_bits = nullptr;
+    std::vector<FP8Weight> enc_qkv, enc_fc1, enc_fc2, dec_qkv, dec_fc1, dec_fc2;
+    std::vector<void*> allocs;
+
+    const void* W(const std::string& n) const { return w + layout.map.at(n).offset; }
+    const float* V(const std::string& n) const { return reinterpret_cast<const float*>(w + layout.map.at(n).offset); }
+    bool fp32() const { return desc.precision == WB_PREC_FP32; }
+    bool fp8() const { return desc.precision == WB_PREC_MIXED_FP8; }
+    int d() const { return desc.d_model; }
+    int H() const { return desc.n_heads; }
+    int F() const { return desc.d_ffn; }
+    size_t wsz() const { return fp32() ? 4 : 2; }
+};
+
+namespace wb {
+namespace {
+
+wb_status dev_alloc(wb_model* m, void** p, size_t bytes) {
+    cudaError_t e = cudaMalloc(p, bytes);
+    if (e != cudaSuccess) return fail(WB_ERR_OOM, std::string("cudaMalloc: ") + cudaGetErrorString(e));
+    m->allocs.push_back(*p);
+    return WB_OK;
+}
+
+// E4M3 copy of a fused weight block: member i (rows_each x K) gets its own
+// per-tensor scale amax / 448, expanded to that member's output columns.
+wb_status make_fp8(wb_model* m, const std::vector<std::string>& names, int64_t rows_each, int64_t K, FP8Weight* out,
+                   cudaStream_t s) {
+    const int64_t n = (int64_t)names.size();
+    if (wb_status st = dev_alloc(m, (void**)&out->w, (size_t)(n * rows_each * K))) return st;
+    if (wb_status st = dev_alloc(m, (void**)&out->col_scale, (size_t)(n * rows_each) * 4)) return st;
+    for (int64_t i = 0; i < n; ++i) {
+        float* sc = out->col_scale + i * rows_each;
+        if (wb_status st = quant_tensor(m->W(names[i]), true, rows_each * K, out->w + i * rows_each * K, sc,
+                                        m->scratch_bits, s))
+            return st;
+        expand_scale_kernel<<<1, 256, 0, s>>>(sc, rows_each);
+    }
+    WB_CUDA(cudaGetLastError());
+    return WB_OK;
+}
+
+// ------------------------------------------------------------------ GEMM helper
+// y = x W^T (+ epilogue) with the model's arithmetic: SIMT fp32 for the fp32
+// model, tcgen05 otherwise (E4M3 when fp8 is given).
+struct Lin {
+    const void* a = nullptr;      // activations
+    int64_t rows = 0, lda = 0;
+    int64_t batches = 1, batch_stride = 0;
+    const void* w = nullptr;      // [N, K]
+    int64_t N = 0, K = 0;
+    const FP8Weight* f8 = nullptr;
+    const float* a_scale = nullptr;
+};
+
+wb_status linear(const wb_model* m, const Lin& L, GemmEpi e, cudaStream_t s) {
+    GemmOperand A;
+    A.ptr = L.a;
+    A.rows = L.rows;
+    A.batches = L.batches;
+    A.row_stride = L.lda;
+    A.batch_stride = L.batch_stride;
+    GemmOperand B;
+    B.ptr = L.f8 ? (const void*)L.f8->w : L.w;
+    B.rows = L.N;
+    B.row_stride = L.K;
+    if (L.rows <= 0 || L.N <= 0) return WB_OK;
+    if (m->fp32()) return gemm_simt(A, false, B, false, L.N, L.K, e, s);
+    const bool f8 = L.f8 != nullptr;
+    if (f8) {
+        e.row_scale = L.a_scale;
+        e.col_scale = L.f8->col_scale;
+    }
+    if (L.K % (f8 ? 128 : 64) != 0) return gemm_simt(A, true, B, true, L.N, L.K, e, s);
+    const int64_t tiles_m = ((L.rows + 127) / 128) * L.batches;
+    int bn = 256;
+    if (tiles_m * ((L.N + 255) / 256) < num_sms()) bn = 128;
+    if (tiles_m * ((L.N + 127) / 128) < num_sms()) bn = 64;
+    GemmPlan p;
+    if (wb_status st = gemm_plan(&p, A, B, L.N, L.K, f8, bn)) return st;
+    return gemm_run(p, e, m->err, s);
+}
+
+GemmEpi epi_out(void* out, int64_t ldo, int type, const float* bias, int gelu = 0) {
+    GemmEpi e;
+    e.out = out;
+    e.ldo = ldo;
+    e.out_type = type;
+    e.bias = bias;
+    e.gelu = gelu;
+    return e;
+}
+
+}  // namespace
+}  // namespace wb
+
+// ------------------------------------------------------------------ decoder state
+struct wb_decoder {
+    wb_model* m = nullptr;
+    int64_t B = 0;
+    std::vector<int32_t> len;
+    int32_t* tokens = nullptr;
+    int pos = 0;
+    int P = 0;
+    // device buffers carved from the workspace
+    void* crosskv = nullptr;
+    void* cache = nullptr;
+    float* kscale = nullptr;
+    float* vscale = nullptr;
+    int64_t* off = nullptr;
+    int32_t* len_dev = nullptr;
+    float* h = nullptr;
+    void* a = nullptr;
+    float* a_scale = nullptr;
+    float* qkv = nullptr;
+    void* attn = nullptr;
+    float* cq = nullptr;
+    void* f = nullptr;
+    uint8_t* fq = nullptr;
+    float* f_scale = nullptr;
+    float* logits = nullptr;
+};
+
+namespace wb {
+namespace {
+
+constexpr int kMaxPrefix = 32;
+
+struct DecLayout {
+    size_t total = 0;
+};
+
+// Carve (or size, with base == nullptr) the decoder workspace.
+size_t carve_decoder(const wb_model* m, int64_t B, const int32_t* len, wb_decoder* dec, uint8_t* base, size_t cap,
+                     bool* overflow) {
+    Carve c{base, cap};
+    const int Ld = m->desc.dec_layers, d = m->d(), H = m->H(), F = m->F();
+    const size_t act = m->fp32() ? 4 : 2;
+    const int64_t R = B * kMaxPrefix;
+    void* crosskv = c.take<uint8_t>((size_t)Ld * B * 2 * kCtx * d * act);
+    int64_t cache_elems = 0;
+    for (int64_t i = 0; i < B; ++i) cache_elems += (int64_t)Ld * 2 * H * len[i] * 64;
+    void* cache = c.take<uint8_t>((size_t)cache_elems * (m->desc.kv_fp8 ? 1 : 4));
+    float* kscale = c.take<float>((size_t)std::max(1, Ld) * B);
+    float* vscale = c.take<float>((size_t)std::max(1, Ld) * B);
+    int64_t* off = c.take<int64_t>(B);
+    int32_t* lend = c.take<int32_t>(B);
+    float* h = c.take<float>((size_t)R * d);
+    void* a = c.take<uint8_t>((size_t)R * d * 4);
+    float* a_scale = c.take<float>(R);
+    float* qkv = c.take<float>((size_t)R * 3 * d);
+    void* attn = c.take<uint8_t>((size_t)R * d * 4);
+    float* cq = c.take<float>((size_t)R * d);
+    void* f = c.take<uint8_t>((size_t)R * F * 4);
+    uint8_t* fq = c.take<uint8_t>((size_t)R * F);
+    float* f_scale = c.take<float>(R);
+    float* logits = c.take<float>((size_t)B * m->desc.vocab);
+    if (dec) {
+        dec->crosskv = crosskv; dec->cache = cache; dec->kscale = kscale; dec->vscale = vscale;
+        dec->off = off; dec->len_dev = lend; dec->h = h; dec->a = a; dec->a_scale = a_scale; dec->qkv = qkv;
+        dec->attn = attn; dec->cq = cq; dec->f = f; dec->fq = fq; dec->f_scale = f_scale; dec->logits = logits;
+    }
+    if (overflow) *overflow = c.overflow;
+    return align_up(c.cur, 256);
+}
+
+struct EncBufs {
+    void* melT;
+    void* x1;
+    float* h;
+    void* a;
+    float* a_scale;
+    void* qkv;
+    void* attn;
+    void* f;
+    uint8_t* fq;
+    float* f_scale;
+};
+
+size_t carve_encoder(const wb_model* m, int64_t B, EncBufs* eb, uint8_t* base, size_t cap, bool* overflow) {
+    Carve c{base, cap};
+    const int d = m->d(), C = m->desc.n_mels, F = m->F();
+    const size_t act = m->fp32() ? 4 : 2;
+    const int64_t M = B * kCtx;
+    EncBufs e;
+    e.melT = c.take<uint8_t>((size_t)B * (kFrames + 2) * C * act);
+    e.x1 = c.take<uint8_t>((size_t)B * (kFrames + 2) * d * act);
+    e.h = c.take<float>((size_t)M * d);
+    e.a = c.take<uint8_t>((size_t)M * d * act);
+    e.a_scale = c.take<float>(M);
+    e.qkv = c.take<uint8_t>((size_t)M * 3 * d * act);
+    e.attn = c.take<uint8_t>((size_t)M * d * act);
+    e.f = c.take<uint8_t>((size_t)M * F * act);
+    e.fq = m->fp8() ? c.take<uint8_t>((size_t)M * F) : nullptr;
+    e.f_scale = c.take<float>(M);
+    if (eb) *eb = e;
+    if (overflow) *overflow = c.overflow;
+    return align_up(c.cur, 256);
+}
+
+// One decoder layer over R rows (rows_per_chunk per chunk, first position p0).
+wb_status decoder_layers(wb_decoder* dec, int64_t n_chunks, int rows_per_chunk, int p0, bool set_scales,
+                         cudaStream_t s) {
+    wb_model* m = dec->m;
+    const int d = m->d(), H = m->H(), F = m->F();
+    const int64_t R = n_chunks * rows_per_chunk;
+    const bool f32 = m->fp32(), f8 = m->fp8();
+    const LnOut ln_plain = f32 ? LN_F32 : LN_BF16;
+    const DType act_dt = f32 ? DT_F32 : DT_BF16;
+    const int act_out = f32 ? OUT_F32 : OUT_BF16;
+    for (int l = 0; l < m->desc.dec_layers; ++l) {
+        // ---- self-attention
+        if (wb_status st = layernorm(dec->h, d, R, d, m->V(nm("dec.", l, "ln1.g")), m->V(nm("dec.", l, "ln1.b")),
+                                     f8 ? LN_E4M3 : ln_plain, dec->a, d, dec->a_scale, s))
+            return st;
+        {
+            Lin L;
+            L.a = dec->a; L.rows = R; L.lda = d; L.w = m->W(nm("dec.", l, "sq.w")); L.N = 3 * d; L.K = d;
+            if (f8) { L.f8 = &m->dec_qkv[l]; L.a_scale = dec->a_scale; }
+            if (wb_status st = linear(m, L, epi_out(dec->qkv, 3 * d, OUT_F32, m->V(nm("dec.", l, "sq.b"))), s)) return st;
+        }
+        const bool kv8 = m->desc.kv_fp8 != 0;
+        float* ks = dec->kscale + (int64_t)l * dec->B;
+        float* vs = dec->vscale + (int64_t)l * dec->B;
+        if (kv8 && set_scales)
+            if (wb_status st = kv_scales(dec->qkv, n_chunks, rows_per_chunk, d, ks, vs, s)) return st;
+        if (wb_status st = kv_append(dec->qkv, n_chunks, rows_per_chunk, p0, d, H, l, kv8, dec->cache, dec->off,
+                                     dec->len_dev, ks, vs, m->err, s))
+            return st;
+        {
+            KVView kv;
+            kv.ptr = dec->cache; kv.chunk_off = dec->off; kv.head_stride = 64; kv.chunk_len = dec->len_dev;
+            kv.heads = H; kv.k_blk = 2 * l; kv.v_blk = 2 * l + 1; kv.row_stride = 64;
+            if (kv8) { kv.k_scale = ks; kv.v_scale = vs; }
+            if (wb_status st = attn_rows(DT_F32, kv8 ? DT_E4M3 : DT_F32, act_dt, dec->qkv, 3 * d, n_chunks,
+                                         rows_per_chunk, H, kv, p0 + rows_per_chunk, true, p0, dec->attn, d, s))
+                return st;
+        }
+        {
+            Lin L;
+            L.a = dec->attn; L.rows = R; L.lda = d; L.w = m->W(nm("dec.", l, "so.w")); L.N = d; L.K = d;
+            if (wb_status st = linear(m, L, epi_out(dec->h, d, OUT_F32_ACC, m->V(nm("dec.", l, "so.b"))), s)) return st;
+        }
+        // ---- cross-attention
+        if (wb_status st = layernorm(dec->h, d, R, d, m->V(nm("dec.", l, "ln2.g")), m->V(nm("dec.", l, "ln2.b")),
+                                     ln_plain, dec->a, d, nullptr, s))
+            return st;
+        {
+            Lin L;
+            L.a = dec->a; L.rows = R; L.lda = d; L.w = m->W(nm("dec.", l, "cq.w")); L.N = d; L.K = d;
+            if (wb_status st = linear(m, L, epi_out(dec->cq, d, OUT_F32, m->V(nm("dec.", l, "cq.b"))), s)) return st;
+        }
+        {
+            const size_t act = f32 ? 4 : 2;
+            KVView kv;
+            kv.ptr = reinterpret_cast<uint8_t*>(dec->crosskv) + (size_t)l * dec->B * 2 * H * kCtx * 64 * act;
+            kv.chunk_stride = (int64_t)2 * H * kCtx * 64; kv.head_stride = (int64_t)kCtx * 64; kv.heads = H;
+            kv.k_blk = 0; kv.v_blk = 1; kv.row_stride = 64;
+            if (wb_status st = attn_rows(DT_F32, act_dt, act_dt, dec->cq, d, n_chunks, rows_per_chunk, H, kv, kCtx,
+                                         false, 0, dec->attn, d, s))
+                return st;
+        }
+        {
+            Lin L;
+            L.a = dec->attn; L.rows = R; L.lda = d; L.w = m->W(nm("dec.", l, "co.w")); L.N = d; L.K = d;
+            if (wb_status st = linear(m, L, epi_out(dec->h, d, OUT_F32_ACC, m->V(nm("dec.", l, "co.b"))), s)) return st;
+        }
+        // ---- FFN
+        if (wb_status st = layernorm(dec->h, d, R, d, m->V(nm("dec.", l, "ln3.g")), m->V(nm("dec.", l, "ln3.b")),
+                                     f8 ? LN_E4M3 : ln_plain, dec->a, d, dec->a_scale, s))
+            return st;
+        {
+            Lin L;
+            L.a = dec->a; L.rows = R; L.lda = d; L.w = m->W(nm("dec.", l, "fc1.w")); L.N = F; L.K = d;
+            if (f8) { L.f8 = &m->dec_fc1[l]; L.a_scale = dec->a_scale; }
+            if (wb_status st = linear(m, L, epi_out(dec->f, F, act_out, m->V(nm("dec.", l, "fc1.b")), 1), s)) return st;
+        }
+        {
+            Lin L;
+            L.rows = R; L.w = m->W(nm("dec.", l, "fc2.w")); L.N = d; L.K = F;
+            if (f8) {
+                if (wb_status st = quant_rows(dec->f, R, F, dec->fq, dec->f_scale, s)) return st;
+                L.a = dec->fq; L.lda = F; L.f8 = &m->dec_fc2[l]; L.a_scale = dec->f_scale;
+            } else {
+                L.a = dec->f; L.lda = F;
+            }
+            if (wb_status st = linear(m, L, epi_out(dec->h, d, OUT_F32_ACC, m->V(nm("dec.", l, "fc2.b"))), s)) return st;
+        }
+    }
+    return WB_OK;
+}
+
+// Final LayerNorm, logits = LN(h) E^T, greedy token into column pos+1.
+wb_status decoder_head(wb_decoder* dec, int64_t n_chunks, int rows_per_chunk, int pos_last, float* logits_all,
+                       cudaStream_t s) {
+    wb_model* m = dec->m;
+    const int d = m->d(), V = m->desc.vocab;
+    const LnOut ln_plain = m->fp32() ? LN_F32 : LN_BF16;
+    const int64_t R = n_chunks * rows_per_chunk;
+    Lin L;
+    L.w = m->W("dec.tok"); L.N = V; L.K = d; L.lda = d;
+    if (logits_all) {
+        if (wb_status st = layernorm(dec->h, d, R, d, m->V("dec.lnf.g"), m->V("dec.lnf.b"), ln_plain, dec->a, d,
+                                     nullptr, s))
+            return st;
+        L.a = dec->a; L.rows = R;
+        if (wb_status st = linear(m, L, epi_out(logits_all, V, OUT_F32, nullptr), s)) return st;
+        return argmax_tokens(logits_all + (int64_t)(rows_per_chunk - 1) * V, (int64_t)rows_per_chunk * V, n_chunks, V,
+                             dec->tokens, dec->len_dev, nullptr, pos_last, s);
+    }
+    // only the last row of each chunk matters
+    if (wb_status st = layernorm(dec->h + (int64_t)(rows_per_chunk - 1) * d, (int64_t)rows_per_chunk * d, n_chunks, d,
+                                 m->V("dec.lnf.g"), m->V("dec.lnf.b"), ln_plain, dec->a, d, nullptr, s))
+        return st;
+    L.a = dec->a; L.rows = n_chunks;
+    if (wb_status st = linear(m, L, epi_out(dec->logits, V, OUT_F32, nullptr), s)) return st;
+    return argmax_tokens(dec->logits, V, n_chunks, V, dec->tokens, dec->len_dev, nullptr, pos_last, s);
+}
+
+__global__ void gather_chunks_kernel(const float* __restrict__ audio, const int64_t* __restrict__ src,
+                                     const int32_t* __restrict__ valid, float* __restrict__ out) {
+    const int64_t c = blockIdx.y;
+    const int64_t i0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * 4;
+    if (i0 >= kChunkSamples) return;
+    const int v = valid[c];
+    float4 o;
+    float* op = reinterpret_cast<float*>(&o);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) op[j] = (i0 + j < v) ? audio[src[c] + i0 + j] : 0.f;
+    *reinterpret_cast<float4*>(out + c * kChunkSamples + i0) = o;
+}
+
+__global__ void fill_prefix_kernel(int32_t* tokens, int64_t n, int32_t p0, int32_t p1, int32_t p2, int32_t p3) {
+    const int64_t c = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (c >= n) return;
+    tokens[c * kMaxPos + 0] = p0;
+    tokens[c * kMaxPos + 1] = p1;
+    tokens[c * kMaxPos + 2] = p2;
+    tokens[c * kMaxPos + 3] = p3;
+}
+
+__global__ void scatter_tokens_kernel(const int32_t* __restrict__ wave_tok, const int32_t* __restrict__ dst_row,
+                                      const int32_t* __restrict__ len, int32_t* __restrict__ out) {
+    const int64_t c = blockIdx.x;
+    const int64_t r = dst_row[c];
+    for (int i = threadIdx.x; i < len[c]; i += blockDim.x) out[r * kMaxPos + i] = wave_tok[c * kMaxPos + i];
+}
+
+void plan_waves_host(const wb_model_desc& d, int32_t n, const int32_t* len, uint64_t budget,
+                     std::vector<std::vector<int32_t>>& waves, bool* too_big) {
+    std::vector<int32_t> order(n);
+    for (int32_t i = 0; i < n; ++i) order[i] = i;
+    std::stable_sort(order.begin(), order.end(), [&](int32_t a, int32_t b) { return len[a] > len[b]; });
+    auto bytes = [&](int32_t L) {
+        return (uint64_t)d.dec_layers * 2 * kCtx * d.d_model * 2 + (uint64_t)d.dec_layers * 2 * L * d.d_model +
+               (uint64_t)kMaxPos * 4;
+    };
+    *too_big = false;
+    waves.clear();
+    std::vector<int32_t> cur;
+    uint64_t used = 0;
+    for (int32_t c : order) {
+        const uint64_t b = bytes(len[c]);
+        if (b > budget) { *too_big = true; return; }
+        if (!cur.empty() && used + b > budget) { waves.push_back(cur); cur.clear(); used = 0; }
+        cur.push_back(c);
+        used += b;
+    }
+    if (!cur.empty()) waves.push_back(cur);
+}
+
+constexpr int64_t kEncSubBatch = 32;
+
+}  // namespace
+}  // namespace wb
+
+extern "C" {
+
+const char* wb_last_error(void) { return t_last_error.c_str(); }
+int wb_version(void) { return 100; }
+
+wb_status wb_mel(const float* audio, int64_t B, int32_t n_mels, float* mel, wb_stream stream) {
+    if (!audio || !mel) return fail(WB_ERR_INVALID_ARG, "wb_mel: null pointer");
+    if (B < 1 || B > (1 << 20)) return fail(WB_ERR_SHAPE, "wb_mel: B must be in [1, 2^20]");
+    if (n_mels != 80 && n_mels != 128) return fail(WB_ERR_SHAPE, "wb_mel: n_mels must be 80 or 128");
+    if (!aligned16(audio) || !aligned16(mel)) return fail(WB_ERR_ALIGN, "wb_mel: pointers must be 16-byte aligned");
+    return mel_launch(audio, B, n_mels, mel, reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t wb_weights_bytes(const wb_model_desc* desc) {
+    std::string why;
+    if (!valid_desc(desc, &why)) return 0;
+    Layout L;
+    build_layout(*desc, &L);
+    return L.total;
+}
+
+wb_status wb_weight_offset(const wb_model_desc* desc, const char* name, size_t* offset, int64_t* numel) {
+    std::string why;
+    if (!valid_desc(desc, &why)) return fail(WB_ERR_INVALID_ARG, "wb_weight_offset: " + why);
+    if (!name || !offset || !numel) return fail(WB_ERR_INVALID_ARG, "wb_weight_offset: null argument");
+    Layout L;
+    build_layout(*desc, &L);
+    auto it = L.map.find(name);
+    if (it == L.map.end()) return fail(WB_ERR_INVALID_ARG, std::string("unknown weight ") + name);
+    *offset = it->second.offset;
+    *numel = it->second.numel;
+    return WB_OK;
+}
+
+wb_status wb_model_create(const wb_model_desc* desc, const void* weights, wb_model** out) {
+    std::string why;
+    if (!out) return fail(WB_ERR_INVALID_ARG, "wb_model_create: null out");
+    *out = nullptr;
+    if (!valid_desc(desc, &why)) return fail(WB_ERR_INVALID_ARG, "wb_model_create: " + why);
+    if (!weights) return fail(WB_ERR_INVALID_ARG, "wb_model_create: null weights");
+    if (!aligned16(weights)) return fail(WB_ERR_ALIGN, "wb_model_create: weights not 16-byte aligned");
+    int dev = 0;
+    WB_CUDA(cudaGetDevice(&dev));
+    cudaDeviceProp prop;
+    WB_CUDA(cudaGetDeviceProperties(&prop, dev));
+    if (prop.major != 10 || prop.minor != 3)
+        return fail(WB_ERR_UNSUPPORTED, "wb_model_create: needs a compute capability 10.3 GPU");
+    wb_model* m = new wb_model();
+    m->desc = *desc;
+    m->device = dev;
+    m->w = reinterpret_cast<const uint8_t*>(weights);
+    build_layout(*desc, &m->layout);
+    cudaStream_t s = nullptr;
+    auto bail = [&](wb_status st) {
+        for (void* p : m->allocs) cudaFree(p);
+        delete m;
+        return st;
+    };
+    const int d = m->d(), C = desc->n_mels, F = m->F();
+    const bool bf = !m->fp32();
+    if (wb_status st = dev_alloc(m, (void**)&m->err, 16)) return bail(st);
+    m->scratch_bits = m->err + 1;
+    if (cudaMemset(m->err, 0, 16) != cudaSuccess) return bail(fail(WB_ERR_CUDA, "memset"));
+    if (wb_status st = dev_alloc(m, &m->conv1_w, (size_t)d * C * 3 * m->wsz())) return bail(st);
+    if (wb_status st = dev_alloc(m, &m->conv2_w, (size_t)d * d * 3 * m->wsz())) return bail(st);
+    if (wb_status st = conv_reorder(m->W("enc.conv1.w"), d, C, bf, m->conv1_w, s)) return bail(st);
+    if (wb_status st = conv_reorder(m->W("enc.conv2.w"), d, d, bf, m->conv2_w, s)) return bail(st);
+    {
+        std::vector<float> pe;
+        sinusoids(kCtx, d, pe);
+        if (wb_status st = dev_alloc(m, (void**)&m->pe, pe.size() * 4)) return bail(st);
+        if (cudaMemcpy(m->pe, pe.data(), pe.size() * 4, cudaMemcpyHostToDevice) != cudaSuccess)
+            return bail(fail(WB_ERR_CUDA, "upload positions"));
+    }
+    if (m->fp8()) {
+        for (int l = 0; l < desc->enc_layers; ++l) {
+            FP8Weight q, f1, f2;
+            wb_status st = make_fp8(m, {nm("enc.", l, "q.w"), nm("enc.", l, "k.w"), nm("enc.", l, "v.w")}, d, d, &q, s);
+            if (!st) st = make_fp8(m, {nm("enc.", l, "fc1.w")}, F, d, &f1, s);
+            if (!st) st = make_fp8(m, {nm("enc.", l, "fc2.w")}, d, F, &f2, s);
+            if (st) return bail(st);
+            m->enc_qkv.push_back(q); m->enc_fc1.push_back(f1); m->enc_fc2.push_back(f2);
+        }
+        for (int l = 0; l < desc->dec_layers; ++l) {
+            FP8Weight q, f1, f2;
+            wb_status st = make_fp8(m, {nm("dec.", l, "sq.w"), nm("dec.", l, "sk.w"), nm("dec.", l, "sv.w")}, d, d, &q, s);
+            if (!st) st = make_fp8(m, {nm("dec.", l, "fc1.w")}, F, d, &f1, s);
+            if (!st) st = make_fp8(m, {nm("dec.", l, "fc2.w")}, d, F, &f2, s);
+            if (st) return bail(st);
+            m->dec_qkv.push_back(q); m->dec_fc1.push_back(f1); m->dec_fc2.push_back(f2);
+        }
+    }
+    if (cudaDeviceSynchronize() != cudaSuccess) return bail(fail(WB_ERR_CUDA, "model setup failed"));
+    *out = m;
+    return WB_OK;
+}
+
+wb_status wb_model_destroy(wb_model* m) {
+    if (!m) return fail(WB_ERR_INVALID_ARG, "wb_model_destroy: null model");
+    for (void* p : m->allocs) cudaFree(p);
+    delete m;
+    return WB_OK;
+}
+
+size_t wb_encode_workspace_size(const wb_model* m, int64_t B) {
+    if (!m || B < 1) return 0;
+    return carve_encoder(m, B, nullptr, nullptr, 0, nullptr);
+}
+
+wb_status wb_encode(wb_model* m, const float* mel, int64_t B, void* enc, void* workspace, size_t ws_bytes,
+                    wb_stream stream) {
+    if (!m || !mel || !enc || !workspace) return fail(WB_ERR_INVALID_ARG, "wb_encode: null argument");
+    if (B < 1 || B > 65535) return fail(WB_ERR_SHAPE, "wb_encode: B must be in [1, 65535]");
+    if (!aligned16(mel) || !aligned16(enc) || !aligned16(workspace)) return fail(WB_ERR_ALIGN, "wb_encode: alignment");
+    EncBufs e;
+    bool over = false;
+    carve_encoder(m, B, &e, reinterpret_cast<uint8_t*>(workspace), ws_bytes, &over);
+    if (over) return fail(WB_ERR_SHAPE, "wb_encode: workspace too small");
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const int d = m->d(), C = m->desc.n_mels, H = m->H(), F = m->F();
+    const int64_t M = B * kCtx;
+    const bool f32 = m->fp32(), f8 = m->fp8();
+    const size_t act = f32 ? 4 : 2;
+    const int act_out = f32 ? OUT_F32 : OUT_BF16;
+    const LnOut ln_plain = f32 ? LN_F32 : LN_BF16;
+    // ---- stem: mel -> [B, 3002, C] -> conv1 (+GELU) -> padded [B, 3002, d] -> conv2 (+GELU, +PE)
+    if (wb_status st = mel_transpose_pad(mel, B, C, e.melT, !f32, s)) return st;
+    WB_CUDA(cudaMemset2DAsync(e.x1, (size_t)(kFrames + 2) * d * act, 0, (size_t)d * act, (size_t)B, s));
+    WB_CUDA(cudaMemset2DAsync(reinterpret_cast<uint8_t*>(e.x1) + (size_t)(kFrames + 1) * d * act,
+                              (size_t)(kFrames + 2) * d * act, 0, (size_t)d * act, (size_t)B, s));
+    {
+        Lin L;
+        L.a = e.melT; L.rows = kFrames; L.lda = C; L.batches = B; L.batch_stride = (int64_t)(kFrames + 2) * C;
+        L.w = m->conv1_w; L.N = d; L.K = 3 * C;
+        GemmEpi ep = epi_out(e.x1, d, act_out, m->V("enc.conv1.b"), 1);
+        ep.out_batch_rows = kFrames + 2;
+        ep.out_row_offset = 1;
+        if (wb_status st = linear(m, L, ep, s)) return st;
+    }
+    {
+        Lin L;
+        L.a = e.x1; L.rows = kCtx; L.lda = 2 * d; L.batches = B; L.batch_stride = (int64_t)(kFrames + 2) * d;
+        L.w = m->conv2_w; L.N = d; L.K = 3 * d;
+        GemmEpi ep = epi_out(e.h, d, OUT_F32, m->V("enc.conv2.b"), 1);
+        ep.add = m->pe;
+        ep.ld_add = d;
+        ep.out_batch_rows = kCtx;
+        if (wb_status st = linear(m, L, ep, s)) return st;
+    }
+    // ---- layers
+    for (int l = 0; l < m->desc.enc_layers; ++l) {
+        if (wb_status st = layernorm(e.h, d, M, d, m->V(nm("enc.", l, "ln1.g")), m->V(nm("enc.", l, "ln1.b")),
+                                     f8 ? LN_E4M3 : ln_plain, e.a, d, e.a_scale, s))
+            return st;
+        {
+            Lin L;
+            L.a = e.a; L.rows = M; L.lda = d; L.w = m->W(nm("enc.", l, "q.w")); L.N = 3 * d; L.K = d;
+            if (f8) { L.f8 = &m->enc_qkv[l]; L.a_scale = e.a_scale; }
+            if (wb_status st = linear(m, L, epi_out(e.qkv, 3 * d, act_out, m->V(nm("enc.", l, "q.b"))), s)) return st;
+        }
+        if (f32) {
+            KVView kv;
+            kv.ptr = e.qkv; kv.chunk_stride = (int64_t)kCtx * 3 * d; kv.head_stride = 64; kv.heads = H;
+            kv.k_blk = 1; kv.v_blk = 2; kv.row_stride = 3 * d;
+            if (wb_status st = attn_rows(DT_F32, DT_F32, DT_F32, e.qkv, 3 * d, B, kCtx, H, kv, kCtx, false, 0, e.attn,
+                                         d, s))
+                return st;
+        } else {
+            if (wb_status st = attn_flash_enc_bf16(e.qkv, B, d, H, e.attn, s)) return st;
+        }
+        {
+            Lin L;
+            L.a = e.attn; L.rows = M; L.lda = d; L.w = m->W(nm("enc.", l, "o.w")); L.N = d; L.K = d;
+            if (wb_status st = linear(m, L, epi_out(e.h, d, OUT_F32_ACC, m->V(nm("enc.", l, "o.b"))), s)) return st;
+        }
+        if (wb_status st = layernorm(e.h, d, M, d, m->V(nm("enc.", l, "ln2.g")), m->V(nm("enc.", l, "ln2.b")),
+                                     f8 ? LN_E4M3 : ln_plain, e.a, d, e.a_scale, s))
+            return st;
+        {
+            Lin L;
+            L.a = e.a; L.rows = M; L.lda = d; L.w = m->W(nm("enc.", l, "fc1.w")); L.N = F; L.K = d;
+            if (f8) { L.f8 = &m->enc_fc1[l]; L.a_scale = e.a_scale; }
+            if (wb_status st = linear(m, L, epi_out(e.f, F, act_out, m->V(nm("enc.", l, "fc1.b")), 1), s)) return st;
+        }
+        {
+            Lin L;
+            L.rows = M; L.w = m->W(nm("enc.", l, "fc2.w")); L.N = d; L.K = F;
+            if (f8) {
+                if (wb_status st = quant_rows(e.f, M, F, e.fq, e.f_scale, s)) return st;
+                L.a = e.fq; L.lda = F; L.f8 = &m->enc_fc2[l]; L.a_scale = e.f_scale;
+            } else {
+                L.a = e.f; L.lda = F;
+            }
+            if (wb_status st = linear(m, L, epi_out(e.h, d, OUT_F32_ACC, m->V(nm("enc.", l, "fc2.b"))), s)) return st;
+        }
+    }
+    return layernorm(e.h, d, M, d, m->V("enc.lnp.g"), m->V("enc.lnp.b"), ln_plain, enc, d, nullptr, s);
+}
+
+size_t wb_decoder_workspace_size(const wb_model* m, int64_t B, const int32_t* len) {
+    if (!m || B < 1 || !len) return 0;
+    return carve_decoder(m, B, len, nullptr, nullptr, 0, nullptr);
+}
+
+wb_status wb_decoder_init(wb_model* m, int64_t B, const int32_t* len, const void* enc, int32_t* tokens,
+                          void* workspace, size_t ws_bytes, wb_stream stream, wb_decoder** out) {
+    if (!out) return fail(WB_ERR_INVALID_ARG, "wb_decoder_init: null out");
+    *out = nullptr;
+    if (!m || !len || !enc || !tokens || !workspace) return fail(WB_ERR_INVALID_ARG, "wb_decoder_init: null argument");
+    if (B < 1 || B > 65535) return fail(WB_ERR_SHAPE, "wb_decoder_init: B must be in [1, 65535]");
+    if (!aligned16(enc) || !aligned16(tokens) || !aligned16(workspace)) return fail(WB_ERR_ALIGN, "wb_decoder_init: alignment");
+    for (int64_t i = 0; i < B; ++i) {
+        if (len[i] < 1 || len[i] > kMaxPos) return fail(WB_ERR_SHAPE, "wb_decoder_init: chunk_len must be in [1, 448]");
+        if (i && len[i] > len[i - 1]) return fail(WB_ERR_SHAPE, "wb_decoder_init: chunk_len must be non-increasing");
+    }
+    wb_decoder* dec = new wb_decoder();
+    dec->m = m;
+    dec->B = B;
+    dec->len.assign(len, len + B);
+    dec->tokens = tokens;
+    bool over = false;
+    carve_decoder(m, B, len, dec, reinterpret_cast<uint8_t*>(workspace), ws_bytes, &over);
+    if (over) {
+        delete dec;
+        return fail(WB_ERR_SHAPE, "wb_decoder_init: workspace too small");
+    }
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const int d = m->d(), H = m->H(), Ld = m->desc.dec_layers;
+    // per-chunk cache offsets (elements) and lengths
+    std::vector<int64_t> off(B);
+    int64_t acc = 0;
+    for (int64_t i = 0; i < B; ++i) {
+        off[i] = acc;
+        acc += (int64_t)Ld * 2 * H * len[i] * 64;
+    }
+    auto fail_free = [&](wb_status st) { delete dec; return st; };
+    if (cudaMemcpyAsync(dec->off, off.data(), B * 8, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+        cudaMemcpyAsync(dec->len_dev, len, B * 4, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+        return fail_free(fail(WB_ERR_CUDA, "wb_decoder_init: upload"));
+    if (Ld > 0) {
+        Lin L;
+        L.a = enc; L.rows = B * kCtx; L.lda = d; L.w = m->W("dec.0.ck.w"); L.N = (int64_t)Ld * 2 * d; L.K = d;
+        GemmEpi ep = epi_out(dec->crosskv, 0, m->fp32() ? OUT_F32 : OUT_BF16, m->V("dec.0.ck.b"));
+        ep.mode = MODE_CROSS_KV;
+        ep.ckv_d = d;
+        ep.ckv_heads = H;
+        ep.ckv_chunks = B;
+        if (wb_status st = linear(m, L, ep, s)) return fail_free(st);
+    }
+    *out = dec;
+    return WB_OK;
+}
+
+wb_status wb_decode_prefix(wb_decoder* dec, int32_t P, float* logits, wb_stream stream) {
+    if (!dec) return fail(WB_ERR_INVALID_ARG, "wb_decode_prefix: null decoder");
+    if (P < 1 || P > kMaxPrefix || P > dec->len.back()) return fail(WB_ERR_SHAPE, "wb_decode_prefix: bad P");
+    if (logits && !aligned16(logits)) return fail(WB_ERR_ALIGN, "wb_decode_prefix: logits alignment");
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    wb_model* m = dec->m;
+    const int64_t R = dec->B * P;
+    if (wb_status st = embed(dec->tokens, R, P, 0, m->d(), m->W("dec.tok"), m->W("dec.pos"), !m->fp32(),
+                             m->desc.vocab, dec->h, m->err, s))
+        return st;
+    if (wb_status st = decoder_layers(dec, dec->B, P, 0, true, s)) return st;
+    if (wb_status st = decoder_head(dec, dec->B, P, P - 1, logits, s)) return st;
+    dec->P = P;
+    dec->pos = P;
+    return WB_OK;
+}
+
+wb_status wb_decode_step(wb_decoder* dec, int64_t n_active, float* logits, wb_stream stream) {
+    if (!dec) return fail(WB_ERR_INVALID_ARG, "wb_decode_step: null decoder");
+    if (dec->P == 0) return fail(WB_ERR_INVALID_ARG, "wb_decode_step: run wb_decode_prefix first");
+    if (n_active < 1 || n_active > dec->B) return fail(WB_ERR_SHAPE, "wb_decode_step: bad n_active");
+    if (dec->len[n_active - 1] <= dec->pos + 1)
+        return fail(WB_ERR_SHAPE, "wb_decode_step: an active chunk has reached its length");
+    if (logits && !aligned16(logits)) return fail(WB_ERR_ALIGN, "wb_decode_step: logits alignment");
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    wb_model* m = dec->m;
+    if (wb_status st = embed(dec->tokens, n_active, 1, dec->pos, m->d(), m->W("dec.tok"), m->W("dec.pos"), !m->fp32(),
+                             m->desc.vocab, dec->h, m->err, s))
+        return st;
+    if (wb_status st = decoder_layers(dec, n_active, 1, dec->pos, false, s)) return st;
+    if (wb_status st = decoder_head(dec, n_active, 1, dec->pos, logits, s)) return st;
+    dec->pos += 1;
+    return WB_OK;
+}
+
+int32_t wb_decoder_position(const wb_decoder* dec) { return dec ? dec->pos : -1; }
+
+wb_status wb_decoder_destroy(wb_decoder* dec) {
+    if (!dec) return fail(WB_ERR_INVALID_ARG, "wb_decoder_destroy: null decoder");
+    delete dec;
+    return WB_OK;
+}
+
+wb_status wb_plan_waves(const wb_model_desc* desc, int32_t n, const int32_t* len, uint64_t budget,
+                        int32_t* wave_of_chunk, int32_t* order, int32_t* n_waves_out) {
+    std::string why;
+    if (!valid_desc(desc, &why)) return fail(WB_ERR_INVALID_ARG, "wb_plan_waves: " + why);
+    if (n < 0 || (n > 0 && (!len || !wave_of_chunk || !order))) return fail(WB_ERR_INVALID_ARG, "wb_plan_waves: args");
+    std::vector<std::vector<int32_t>> waves;
+    bool too_big = false;
+    plan_waves_host(*desc, n, len, budget, waves, &too_big);
+    if (too_big) return fail(WB_ERR_SHAPE, "wb_plan_waves: one chunk exceeds the wave budget");
+    int32_t k = 0;
+    for (size_t w = 0; w < waves.size(); ++w)
+        for (int32_t c : waves[w]) {
+            wave_of_chunk[c] = (int32_t)w;
+            order[k++] = c;
+        }
+    if (n_waves_out) *n_waves_out = (int32_t)waves.size();
+    return WB_OK;
+}
+
+struct TranscribeBufs {
+    float* chunk_audio = nullptr;
+    float* mel = nullptr;
+    uint8_t* enc = nullptr;
+    int32_t* wave_tok = nullptr;
+    int64_t* src = nullptr;
+    int32_t* valid = nullptr;
+    int32_t* dst_row = nullptr;
+    int32_t* wlen = nullptr;
+    uint8_t* enc_ws = nullptr;
+    size_t enc_ws_bytes = 0;
+    uint8_t* dec_ws = nullptr;
+    size_t dec_ws_bytes = 0;
+};
+
+static size_t transcribe_ws(const wb_model* m, int64_t max_wave, const std::vector<std::vector<int32_t>>& waves,
+                            const std::vector<int32_t>& lens, uint8_t* base, size_t cap, TranscribeBufs* tb,
+                            bool* overflow) {
+    Carve c{base, cap};
+    const int d = m->d();
+    const size_t act = m->fp32() ? 4 : 2;
+    const int64_t EB = std::min<int64_t>(kEncSubBatch, std::max<int64_t>(1, max_wave));
+    TranscribeBufs t;
+    t.chunk_audio = c.take<float>((size_t)max_wave * kChunkSamples);
+    t.mel = c.take<float>((size_t)max_wave * m->desc.n_mels * kFrames);
+    t.enc = c.take<uint8_t>((size_t)max_wave * kCtx * d * act);
+    t.wave_tok = c.take<int32_t>((size_t)max_wave * kMaxPos);
+    t.src = c.take<int64_t>(max_wave);
+    t.valid = c.take<int32_t>(max_wave);
+    t.dst_row = c.take<int32_t>(max_wave);
+    t.wlen = c.take<int32_t>(max_wave);
+    t.enc_ws_bytes = carve_encoder(m, EB, nullptr, nullptr, 0, nullptr);
+    t.enc_ws = c.take<uint8_t>(t.enc_ws_bytes);
+    for (const auto& w : waves) {
+        std::vector<int32_t> l;
+        for (int32_t ci : w) l.push_back(lens[ci]);
+        t.dec_ws_bytes = std::max(t.dec_ws_bytes, carve_decoder(m, (int64_t)w.size(), l.data(), nullptr, nullptr, 0, nullptr));
+    }
+    t.dec_ws = c.take<uint8_t>(t.dec_ws_bytes);
+    if (tb) *tb = t;
+    if (overflow) *overflow = c.overflow;
+    return align_up(c.cur, 256);
+}
+
+static bool chunk_table(int32_t n_req, const int64_t* req_samples, std::vector<int32_t>& req, std::vector<int64_t>& idx,
+                        std::vector<int32_t>& valid) {
+    for (int32_t r = 0; r < n_req; ++r) {
+        if (req_samples[r] < 1) return false;
+        const int64_t n = (req_samples[r] + kChunkSamples - 1) / kChunkSamples;
+        for (int64_t k = 0; k < n; ++k) {
+            req.push_back(r);
+            idx.push_back(k);
+            valid.push_back((int32_t)std::min<int64_t>(kChunkSamples, req_samples[r] - k * kChunkSamples));
+        }
+    }
+    return true;
+}
+
+size_t wb_transcribe_workspace_size(const wb_model* m, int32_t n_req, const int64_t* req_samples,
+                                    const int32_t* chunk_len, uint64_t budget) {
+    if (!m || n_req < 1 || !req_samples || !chunk_len) return 0;
+    std::vector<int32_t> req, valid;
+    std::vector<int64_t> idx;
+    if (!chunk_table(n_req, req_samples, req, idx, valid)) return 0;
+    std::vector<int32_t> lens(chunk_len, chunk_len + req.size());
+    std::vector<std::vector<int32_t>> waves;
+    bool too_big = false;
+    plan_waves_host(m->desc, (int32_t)req.size(), lens.data(), budget, waves, &too_big);
+    if (too_big) return 0;
+    int64_t mw = 0;
+    for (auto& w : waves) mw = std::max<int64_t>(mw, (int64_t)w.size());
+    return transcribe_ws(m, mw, waves, lens, nullptr, 0, nullptr, nullptr);
+}
+
+wb_status wb_transcribe_batch(wb_model* m, const float* audio, const int64_t* req_offset, const int64_t* req_samples,
+                              int32_t n_req, const int32_t* prefix, const int32_t* chunk_len, int32_t* tokens,
+                              uint64_t budget, void* workspace, size_t ws_bytes, int32_t* n_waves_out,
+                              wb_stream stream) {
+    if (!m || !audio || !req_offset || !req_samples || !prefix || !chunk_len || !tokens || !workspace)
+        return fail(WB_ERR_INVALID_ARG, "wb_transcribe_batch: null argument");
+    if (n_req < 1) return fail(WB_ERR_SHAPE, "wb_transcribe_batch: n_req < 1");
+    if (!aligned16(audio) || !aligned16(tokens) || !aligned16(workspace))
+        return fail(WB_ERR_ALIGN, "wb_transcribe_batch: alignment");
+    for (int i = 0; i < 4; ++i)
+        if (prefix[i] < 0 || prefix[i] >= m->desc.vocab) return fail(WB_ERR_SHAPE, "wb_transcribe_batch: prefix id");
+    std::vector<int32_t> req, valid;
+    std::vector<int64_t> idx;
+    if (!chunk_table(n_req, req_samples, req, idx, valid)) return fail(WB_ERR_SHAPE, "wb_transcribe_batch: empty request");
+    const int32_t n = (int32_t)req.size();
+    std::vector<int32_t> lens(chunk_len, chunk_len + n);
+    for (int32_t c = 0; c < n; ++c)
+        if (lens[c] < 5 || lens[c] > kMaxPos) return fail(WB_ERR_SHAPE, "wb_transcribe_batch: chunk_len must be in [5, 448]");
+    std::vector<std::vector<int32_t>> waves;
+    bool too_big = false;
+    plan_waves_host(m->desc, n, lens.data(), budget, waves, &too_big);
+    if (too_big) return fail(WB_ERR_SHAPE, "wb_transcribe_batch: one chunk exceeds the wave budget");
+    int64_t mw = 0;
+    for (auto& w : waves) mw = std::max<int64_t>(mw, (int64_t)w.size());
+    TranscribeBufs tb;
+    bool over = false;
+    transcribe_ws(m, mw, waves, lens, reinterpret_cast<uint8_t*>(workspace), ws_bytes, &tb, &over);
+    if (over) return fail(WB_ERR_SHAPE, "wb_transcribe_batch: workspace too small");
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const int d = m->d();
+    const size_t act = m->fp32() ? 4 : 2;
+    for (const auto& w : waves) {
+        const int64_t nw = (int64_t)w.size();
+        std::vector<int64_t> hsrc(nw);
+        std::vector<int32_t> hvalid(nw), hdst(nw), wl(nw);
+        for (int64_t i = 0; i < nw; ++i) {
+            const int32_t c = w[i];
+            hsrc[i] = req_offset[req[c]] + idx[c] * kChunkSamples;
+            hvalid[i] = valid[c];
+            hdst[i] = c;
+            wl[i] = lens[c];
+        }
+        WB_CUDA(cudaMemcpyAsync(tb.src, hsrc.data(), nw * 8, cudaMemcpyHostToDevice, s));
+        WB_CUDA(cudaMemcpyAsync(tb.valid, hvalid.data(), nw * 4, cudaMemcpyHostToDevice, s));
+        WB_CUDA(cudaMemcpyAsync(tb.dst_row, hdst.data(), nw * 4, cudaMemcpyHostToDevice, s));
+        WB_CUDA(cudaMemcpyAsync(tb.wlen, wl.data(), nw * 4, cudaMemcpyHostToDevice, s));
+        // pageable host sources: make sure they are consumed before the vectors go away
+        WB_CUDA(cudaStreamSynchronize(s));
+        gather_chunks_kernel<<<dim3((kChunkSamples / 4 + 255) / 256, (unsigned)nw), 256, 0, s>>>(
+            audio, tb.src, tb.valid, tb.chunk_audio);
+        WB_CUDA(cudaGetLastError());
+        if (wb_status st = wb_mel(tb.chunk_audio, nw, m->desc.n_mels, tb.mel, stream)) return st;
+        for (int64_t i0 = 0; i0 < nw; i0 += kEncSubBatch) {
+            const int64_t nb = std::min<int64_t>(kEncSubBatch, nw - i0);
+            if (wb_status st = wb_encode(m, tb.mel + i0 * m->desc.n_mels * kFrames, nb,
+                                         tb.enc + (size_t)i0 * kCtx * d * act, tb.enc_ws, tb.enc_ws_bytes, stream))
+                return st;
+        }
+        fill_prefix_kernel<<<(unsigned)((nw + 255) / 256), 256, 0, s>>>(tb.wave_tok, nw, prefix[0], prefix[1],
+                                                                        prefix[2], prefix[3]);
+        WB_CUDA(cudaGetLastError());
+        wb_decoder* dec = nullptr;
+        if (wb_status st = wb_decoder_init(m, nw, wl.data(), tb.enc, tb.wave_tok, tb.dec_ws, tb.dec_ws_bytes, stream,
+                                           &dec))
+            return st;
+        wb_status st = wb_decode_prefix(dec, 4, nullptr, stream);
+        for (int t = 4; !st && t + 1 < wl[0]; ++t) {
+            int64_t na = 0;
+            while (na < nw && wl[na] > t + 1) ++na;
+            st = wb_decode_step(dec, na, nullptr, stream);
+        }
+        wb_decoder_destroy(dec);
+        if (st) return st;
+        scatter_tokens_kernel<<<(unsigned)nw, 128, 0, s>>>(tb.wave_tok, tb.dst_row, tb.wlen, tokens);
+        WB_CUDA(cudaGetLastError());
+    }
+    if (n_waves_out) *n_waves_out = (int32_t)waves.size();
+    return wb_sync_status(m, stream);
+}
+
+wb_status wb_quantise_e4m3(const void* x, int32_t x_is_bf16, int64_t n, uint8_t* codes, float* scale, wb_stream stream) {
+    if (!x || !codes || !scale) return fail(WB_ERR_INVALID_ARG, "wb_quantise_e4m3: null argument");
+    if (n < 0) return fail(WB_ERR_SHAPE, "wb_quantise_e4m3: n < 0");
+    unsigned* err = lib_error_word();
+    if (!err) return fail(WB_ERR_CUDA, "wb_quantise_e4m3: no device error word");
+    static unsigned* bits[64] = {};
+    int dev = 0;
+    WB_CUDA(cudaGetDevice(&dev));
+    {
+        std::lock_guard<std::mutex> lk(g_err_mu);
+        if (!bits[dev & 63]) WB_CUDA(cudaMalloc(&bits[dev & 63], 16));
+    }
+    return quant_tensor(x, x_is_bf16 != 0, n, codes, scale, bits[dev & 63], reinterpret_cast<cudaStream_t>(stream));
+}
+
+wb_status wb_dequantise_e4m3(const uint8_t* codes, const float* scale, int64_t n, float* out, wb_stream stream) {
+    if (!codes || !scale || !out) return fail(WB_ERR_INVALID_ARG, "wb_dequantise_e4m3: null argument");
+    if (n < 0) return fail(WB_ERR_SHAPE, "wb_dequantise_e4m3: n < 0");
+    return dequant_tensor(codes, scale, n, out, reinterpret_cast<cudaStream_t>(stream));
+}
+
+wb_status wb_gemm(const void* A, const void* Bw, int64_t M, int64_t N, int64_t K, int32_t ab_type,
+                  const float* row_scale, const float* col_scale, const float* bias, int32_t gelu, void* C,
+                  int32_t c_bf16, wb_stream stream) {
+    if (!A || !Bw || !C) return fail(WB_ERR_INVALID_ARG, "wb_gemm: null pointer");
+    if (ab_type != 0 && ab_type != 1) return fail(WB_ERR_INVALID_ARG, "wb_gemm: ab_type must be 0 or 1");
+    if (ab_type == 1 && (!row_scale || !col_scale)) return fail(WB_ERR_INVALID_ARG, "wb_gemm: E4M3 needs scales");
+    if (M < 1 || N < 1 || K < 1 || N % 8) return fail(WB_ERR_SHAPE, "wb_gemm: bad M/N/K");
+    if (K % (ab_type ? 128 : 64)) return fail(WB_ERR_SHAPE, "wb_gemm: K must be a multiple of 64 (bf16) / 128 (E4M3)");
+    unsigned* err = lib_error_word();
+    if (!err) return fail(WB_ERR_CUDA, "wb_gemm: no error word");
+    GemmOperand a;
+    a.ptr = A; a.rows = M; a.row_stride = K;
+    GemmOperand b;
+    b.ptr = Bw; b.rows = N; b.row_stride = K;
+    const int64_t tiles_m = (M + 127) / 128;
+    int bn = 256;
+    if (tiles_m * ((N + 255) / 256) < num_sms()) bn = 128;
+    if (tiles_m * ((N + 127) / 128) < num_sms()) bn = 64;
+    GemmPlan p;
+    if (wb_status st = gemm_plan(&p, a, b, N, K, ab_type == 1, bn)) return st;
+    GemmEpi e;
+    e.out = C;
+    e.ldo = N;
+    e.out_type = c_bf16 ? OUT_BF16 : OUT_F32;
+    e.bias = bias;
+    e.gelu = gelu;
+    if (ab_type == 1) { e.row_scale = row_scale; e.col_scale = col_scale; }
+    return gemm_run(p, e, err, reinterpret_cast<cudaStream_t>(stream));
+}
+
+wb_status wb_sync_status(wb_model* m, wb_stream stream) {
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    WB_CUDA(cudaStreamSynchronize(s));
+    unsigned* err = m ? m->err : lib_error_word();
+    if (!err) return fail(WB_ERR_CUDA, "wb_sync_status: no error word");
+    unsigned v = 0;
+    WB_CUDA(cudaMemcpy(&v, err, sizeof(unsigned), cudaMemcpyDeviceToHost));
+    if (v) {
+        WB_CUDA(cudaMemset(err, 0, sizeof(unsigned)));
+        char buf[96];
+        snprintf(buf, sizeof(buf), "device error word 0x%x", v);
+        return fail((v & (WB_DEVERR_TIMEOUT_TMA | WB_DEVERR_TIMEOUT_MMA | WB_DEVERR_TIMEOUT_EPI)) ? WB_ERR_TIMEOUT
+                                                                                                     : WB_ERR_SHAPE,
+                    buf);
+    }
+    return WB_OK;
+}
+
+}  // extern "C"

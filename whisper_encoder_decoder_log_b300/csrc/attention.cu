@@ -1,0 +1,415 @@
+// Attention kernels ("whisper-blaze 0.1.8", "Direct Kernel API":
+// encoder_self_attn without mask, decoder_self_attn with a causal mask,
+// decoder_cross_attn without mask; "Unlocking the power of OpenAI's Whisper",
+// section 3).  Every head has width 64 and computes softmax(q k^T / 8) v.
+//
+//  * flash_enc_kernel: encoder self-attention in bf16.  One CTA = 64 query
+//    rows of one (chunk, head); 4 warps x 16 rows; K/V tiles of 64 keys are
+//    double-buffered in XOR-swizzled shared memory with cp.async; both
+//    products use the warp-level bf16 tensor-core MMA (m16n8k16) with the
+//    online softmax in fp32.
+//  * attn_rows_kernel: one CTA per (chunk, head, group of up to 4 query rows)
+//    streams the chunk's keys with 16-byte loads (8 lanes per bf16/fp32 key
+//    row, 4 lanes per E4M3 row), keeps the scores in shared memory, and
+//    reduces p . V across the CTA.  It serves the fp32 model's encoder, the
+//    decoder's cross-attention over the precomputed bf16 K/V, and the decoder's
+//    causal self-attention over the (E4M3 or fp32) KV cache, where query row
+//    p of a chunk sees cache rows 0..p.
+#include "attn.cuh"
+#include "common.cuh"
+
+namespace wb {
+namespace {
+
+// ------------------------------------------------------------------ flash (bf16)
+constexpr int kFaRows = 64;
+constexpr int kFaKeys = 64;
+
+WB_DEV uint32_t swz(int row, int chunk) {   // element offset in a [rows][64] bf16 tile
+    return (uint32_t)(row * 64 + ((chunk ^ (row & 7)) * 8));
+}
+
+WB_DEV void cp_async16(void* dst, const void* src, bool valid) {
+    const uint32_t d = smem_u32(dst);
+    const int n = valid ? 16 : 0;
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(d), "l"(src), "r"(n) : "memory");
+}
+WB_DEV void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+WB_DEV void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+WB_DEV void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
+}
+WB_DEV void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
+}
+WB_DEV void mma16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__global__ void __launch_bounds__(128)
+flash_enc_kernel(const __nv_bfloat16* __restrict__ qkv, int d, int S, __nv_bfloat16* __restrict__ out) {
+    __shared__ __align__(128) __nv_bfloat16 sQ[kFaRows * 64];
+    __shared__ __align__(128) __nv_bfloat16 sK[2][kFaKeys * 64];
+    __shared__ __align__(128) __nv_bfloat16 sV[2][kFaKeys * 64];
+    const int qb = blockIdx.x, h = blockIdx.y;
+    const int64_t chunk = blockIdx.z;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int64_t ld = 3 * (int64_t)d;
+    const __nv_bfloat16* base = qkv + chunk * S * ld;
+    const int q0 = qb * kFaRows;
+
+    // Q tile
+    for (int i = tid; i < kFaRows * 8; i += 128) {
+        const int r = i >> 3, c = i & 7;
+        const bool ok = q0 + r < S;
+        cp_async16(sQ + swz(r, c), base + (int64_t)(ok ? q0 + r : 0) * ld + h * 64 + c * 8, ok);
+    }
+    auto load_kv = [&](int buf, int k0) {
+        for (int i = tid; i < kFaKeys * 8; i += 128) {
+            const int r = i >> 3, c = i & 7;
+            const bool ok = k0 + r < S;
+            const __nv_bfloat16* src = base + (int64_t)(ok ? k0 + r : 0) * ld + h * 64 + c * 8;
+            cp_async16(sK[buf] + swz(r, c), src + d, ok);
+            cp_async16(sV[buf] + swz(r, c), src + 2 * d, ok);
+        }
+    };
+    load_kv(0, 0);
+    cp_async_commit();
+
+    const int nkb = (S + kFaKeys - 1) / kFaKeys;
+    uint32_t qf[4][4];
+    float o[8][4];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+    float m_r[2] = {-1e30f, -1e30f}, l_r[2] = {0.f, 0.f};
+    const float sc = 0.125f * 1.4426950408889634f;   // 1/sqrt(64) * log2(e)
+
+    for (int kb = 0; kb < nkb; ++kb) {
+        if (kb + 1 < nkb) load_kv((kb + 1) & 1, (kb + 1) * kFaKeys);
+        cp_async_commit();
+        cp_async_wait<1>();
+        __syncthreads();
+        if (kb == 0) {
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+                const int mi = lane >> 3, rr = lane & 7;
+                const int row = warp * 16 + rr + (mi & 1) * 8;
+                const int ch = kk * 2 + (mi >> 1);
+                ldsm_x4(smem_u32(sQ + swz(row, ch)), qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3]);
+            }
+        }
+        const __nv_bfloat16* k_t = sK[kb & 1];
+        const __nv_bfloat16* v_t = sV[kb & 1];
+        float s[8][4];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) s[j][0] = s[j][1] = s[j][2] = s[j][3] = 0.f;
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+#pragma unroll
+            for (int j = 0; j < 8; j += 2) {
+                const int mi = lane >> 3, rr = lane & 7;
+                const int key = 8 * (j + (mi >> 1)) + rr;
+                const int ch = kk * 2 + (mi & 1);
+                uint32_t b0, b1, b2, b3;
+                ldsm_x4(smem_u32(k_t + swz(key, ch)), b0, b1, b2, b3);
+                mma16816(s[j], qf[kk], b0, b1);
+                mma16816(s[j + 1], qf[kk], b2, b3);
+            }
+        }
+        // mask keys past S
+        const int k0 = kb * kFaKeys;
+        if (k0 + kFaKeys > S) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int kc = k0 + 8 * j + 2 * (lane & 3);
+                if (kc >= S) { s[j][0] = -1e30f; s[j][2] = -1e30f; }
+                if (kc + 1 >= S) { s[j][1] = -1e30f; s[j][3] = -1e30f; }
+            }
+        }
+        // online softmax: rows g (c0,c1) and g+8 (c2,c3)
+        float mx[2] = {m_r[0], m_r[1]};
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            mx[0] = fmaxf(mx[0], fmaxf(s[j][0], s[j][1]));
+            mx[1] = fmaxf(mx[1], fmaxf(s[j][2], s[j][3]));
+        }
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            mx[i] = fmaxf(mx[i], __shfl_xor_sync(0xffffffffu, mx[i], 1));
+            mx[i] = fmaxf(mx[i], __shfl_xor_sync(0xffffffffu, mx[i], 2));
+        }
+        float alpha[2], rs[2] = {0.f, 0.f};
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            alpha[i] = exp2f((m_r[i] - mx[i]) * sc);
+            m_r[i] = mx[i];
+        }
+        uint32_t pf[4][4];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const float p0 = exp2f((s[j][0] - mx[0]) * sc), p1 = exp2f((s[j][1] - mx[0]) * sc);
+            const float p2 = exp2f((s[j][2] - mx[1]) * sc), p3 = exp2f((s[j][3] - mx[1]) * sc);
+            rs[0] += p0 + p1;
+            rs[1] += p2 + p3;
+            const int kt = j >> 1, hi = j & 1;
+            pf[kt][hi * 2 + 0] = pack_bf16x2(p0, p1);
+            pf[kt][hi * 2 + 1] = pack_bf16x2(p2, p3);
+        }
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            rs[i] += __shfl_xor_sync(0xffffffffu, rs[i], 1);
+            rs[i] += __shfl_xor_sync(0xffffffffu, rs[i], 2);
+            l_r[i] = l_r[i] * alpha[i] + rs[i];
+        }
+#pragma unroll
+        for (int dn = 0; dn < 8; ++dn) {
+            o[dn][0] *= alpha[0]; o[dn][1] *= alpha[0];
+            o[dn][2] *= alpha[1]; o[dn][3] *= alpha[1];
+        }
+#pragma unroll
+        for (int kt = 0; kt < 4; ++kt) {
+            // A fragment order: a0 (row g, keys lo), a1 (row g+8, lo), a2 (row g, hi), a3 (row g+8, hi)
+            const uint32_t a[4] = {pf[kt][0], pf[kt][1], pf[kt][2], pf[kt][3]};
+#pragma unroll
+            for (int dn = 0; dn < 8; dn += 2) {
+                const int mi = lane >> 3, rr = lane & 7;
+                const int key = 16 * kt + rr + (mi & 1) * 8;
+                const int ch = dn + (mi >> 1);
+                uint32_t b0, b1, b2, b3;
+                ldsm_x4_t(smem_u32(v_t + swz(key, ch)), b0, b1, b2, b3);
+                mma16816(o[dn], a, b0, b1);
+                mma16816(o[dn + 1], a, b2, b3);
+            }
+        }
+        __syncthreads();
+    }
+    // normalise and store
+    const int g = lane >> 2, t4 = lane & 3;
+    const float inv0 = 1.f / l_r[0], inv1 = 1.f / l_r[1];
+    const int r0 = q0 + warp * 16 + g, r1 = r0 + 8;
+    __nv_bfloat16* ob = out + chunk * S * (int64_t)d + h * 64;
+#pragma unroll
+    for (int dn = 0; dn < 8; ++dn) {
+        const int col = dn * 8 + 2 * t4;
+        if (r0 < S)
+            *reinterpret_cast<uint32_t*>(ob + (int64_t)r0 * d + col) = pack_bf16x2(o[dn][0] * inv0, o[dn][1] * inv0);
+        if (r1 < S)
+            *reinterpret_cast<uint32_t*>(ob + (int64_t)r1 * d + col) = pack_bf16x2(o[dn][2] * inv1, o[dn][3] * inv1);
+    }
+}
+
+// ------------------------------------------------------------------ row attention
+constexpr int kRowThreads = 256;
+constexpr int kQGroup = 4;
+
+template <typename T>
+WB_DEV void load8(const T* p, float (&v)[8]);
+template <>
+WB_DEV void load8<float>(const float* p, float (&v)[8]) {
+    const float4 a = *reinterpret_cast<const float4*>(p);
+    const float4 b = *reinterpret_cast<const float4*>(p + 4);
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+template <>
+WB_DEV void load8<__nv_bfloat16>(const __nv_bfloat16* p, float (&v)[8]) {
+    const uint4 a = *reinterpret_cast<const uint4*>(p);
+    const uint32_t w[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        v[2 * i] = __uint_as_float(w[i] << 16);
+        v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+}
+template <>
+WB_DEV void load8<uint8_t>(const uint8_t* p, float (&v)[8]) {
+    const uint2 a = *reinterpret_cast<const uint2*>(p);
+    const uint32_t w[2] = {a.x, a.y};
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        __nv_fp8x4_e4m3 q;
+        q.__x = w[i];
+        const float4 f = static_cast<float4>(q);
+        v[4 * i] = f.x; v[4 * i + 1] = f.y; v[4 * i + 2] = f.z; v[4 * i + 3] = f.w;
+    }
+}
+
+template <typename TQ, typename TKV, typename TO>
+__global__ void __launch_bounds__(kRowThreads)
+attn_rows_kernel(const TQ* __restrict__ q, int64_t q_ld, int rows_per_chunk, int n_rows_total,
+                 KVView kv, int kv_len, int causal, int q_pos0, TO* __restrict__ out, int64_t o_ld) {
+    // scores for up to 4 query rows over up to kMaxKeys keys
+    extern __shared__ float sm[];
+    float* sq = sm;                              // [4][64]
+    float* ss = sq + kQGroup * 64;               // [4][kv_len]
+    float* sred = ss + kQGroup * kv_len;         // [32][4][64] partial outputs, reused for maxima
+    const int64_t chunk = blockIdx.x;
+    const int h = blockIdx.y;
+    const int tid = threadIdx.x;
+    const int r_first = blockIdx.z * kQGroup;
+    const int nq = min(kQGroup, rows_per_chunk - r_first);
+    if (nq <= 0) return;
+    const int64_t row0 = chunk * rows_per_chunk + r_first;
+    if (row0 >= n_rows_total) return;
+
+    for (int i = tid; i < kQGroup * 64; i += kRowThreads) {
+        const int qi = i / 64, c = i % 64;
+        sq[i] = qi < nq ? (float)q[(row0 + qi) * q_ld + h * 64 + c] * 0.125f : 0.f;
+    }
+    // key range
+    const int64_t cb = kv.chunk_off ? kv.chunk_off[chunk] : chunk * kv.chunk_stride;
+    const int64_t hs = kv.head_stride * (kv.chunk_len ? (int64_t)kv.chunk_len[chunk] : 1);
+    const TKV* Kp = reinterpret_cast<const TKV*>(kv.ptr) + cb + ((int64_t)kv.k_blk * kv.heads + h) * hs;
+    const TKV* Vp = reinterpret_cast<const TKV*>(kv.ptr) + cb + ((int64_t)kv.v_blk * kv.heads + h) * hs;
+    const float ks = kv.k_scale ? kv.k_scale[chunk] : 1.f;
+    const float vs = kv.v_scale ? kv.v_scale[chunk] : 1.f;
+    int nk = kv_len;
+    if (causal) nk = min(kv_len, q_pos0 + r_first + nq);
+    __syncthreads();
+
+    // phase 1: scores, 8 lanes per key row (8 elements each); the trip count
+    // is uniform per warp so the 8-lane shuffles always see full warps
+    const int sub = tid & 7;
+    const int grp = tid >> 3;
+    for (int jb = 0; jb < nk; jb += kRowThreads / 8) {
+        const int j0 = jb + grp;
+        const bool valid = j0 < nk;
+        float kf[8];
+        if (valid) load8<TKV>(Kp + (int64_t)j0 * kv.row_stride + sub * 8, kf);
+        else {
+#pragma unroll
+            for (int c = 0; c < 8; ++c) kf[c] = 0.f;
+        }
+        float acc[kQGroup];
+#pragma unroll
+        for (int qi = 0; qi < kQGroup; ++qi) {
+            float a = 0.f;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) a = fmaf(sq[qi * 64 + sub * 8 + c], kf[c], a);
+            acc[qi] = a;
+        }
+#pragma unroll
+        for (int qi = 0; qi < kQGroup; ++qi) {
+            acc[qi] += __shfl_xor_sync(0xffffffffu, acc[qi], 1);
+            acc[qi] += __shfl_xor_sync(0xffffffffu, acc[qi], 2);
+            acc[qi] += __shfl_xor_sync(0xffffffffu, acc[qi], 4);
+        }
+        if (valid && sub < nq) {
+            const int qi = sub;
+            float v = acc[0];
+            if (qi == 1) v = acc[1];
+            if (qi == 2) v = acc[2];
+            if (qi == 3) v = acc[3];
+            v *= ks;
+            if (causal && j0 > q_pos0 + r_first + qi) v = -INFINITY;
+            ss[qi * kv_len + j0] = v;
+        }
+    }
+    __syncthreads();
+    // softmax per query row: warp qi handles row qi
+    const int warp = tid >> 5, lane = tid & 31;
+    if (warp < nq) {
+        float* sr = ss + warp * kv_len;
+        float m = -INFINITY;
+        for (int j = lane; j < nk; j += 32) m = fmaxf(m, sr[j]);
+        m = warp_max(m);
+        float sum = 0.f;
+        for (int j = lane; j < nk; j += 32) {
+            const float e = __expf(sr[j] - m);   // fast exp: inputs <= 0, error ~2 ulp
+            sr[j] = e;
+            sum += e;
+        }
+        sum = warp_sum(sum);
+        const float inv = 1.f / sum;
+        for (int j = lane; j < nk; j += 32) sr[j] *= inv;
+    }
+    __syncthreads();
+    // phase 2: o = p . V ; thread (row group rg = tid/8, dims 8*sub..)
+    const int rg = tid >> 3;
+    float o[kQGroup][8];
+#pragma unroll
+    for (int qi = 0; qi < kQGroup; ++qi)
+#pragma unroll
+        for (int c = 0; c < 8; ++c) o[qi][c] = 0.f;
+    for (int j = rg; j < nk; j += kRowThreads / 8) {
+        float vf[8];
+        load8<TKV>(Vp + (int64_t)j * kv.row_stride + sub * 8, vf);
+#pragma unroll
+        for (int qi = 0; qi < kQGroup; ++qi) {
+            const float p = ss[qi * kv_len + j];
+#pragma unroll
+            for (int c = 0; c < 8; ++c) o[qi][c] = fmaf(p, vf[c], o[qi][c]);
+        }
+    }
+    // reduce the 32 row groups
+#pragma unroll
+    for (int qi = 0; qi < kQGroup; ++qi)
+#pragma unroll
+        for (int c = 0; c < 8; ++c) sred[(rg * kQGroup + qi) * 64 + sub * 8 + c] = o[qi][c];
+    __syncthreads();
+    for (int i = tid; i < nq * 64; i += kRowThreads) {
+        const int qi = i / 64, c = i % 64;
+        float a = 0.f;
+        for (int g = 0; g < kRowThreads / 8; ++g) a += sred[(g * kQGroup + qi) * 64 + c];
+        out[(row0 + qi) * o_ld + h * 64 + c] = (TO)(a * vs);
+    }
+}
+
+template <typename TQ, typename TKV, typename TO>
+wb_status launch_rows(const void* q, int64_t q_ld, int64_t n_chunks, int rows_per_chunk, int heads,
+                      const KVView& kv, int kv_len, bool causal, int q_pos0, void* out, int64_t o_ld,
+                      cudaStream_t s) {
+    const size_t smem = sizeof(float) * (kQGroup * 64 + kQGroup * (size_t)kv_len + 32 * kQGroup * 64);
+    static bool attr[64] = {};
+    int dev = 0;
+    WB_CUDA(cudaGetDevice(&dev));
+    if (!attr[dev & 63]) {
+        WB_CUDA(cudaFuncSetAttribute(attn_rows_kernel<TQ, TKV, TO>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024));
+        attr[dev & 63] = true;
+    }
+    if (smem > 200 * 1024) return fail(WB_ERR_SHAPE, "attention key length too large");
+    dim3 grid((unsigned)n_chunks, (unsigned)heads, (unsigned)((rows_per_chunk + kQGroup - 1) / kQGroup));
+    attn_rows_kernel<TQ, TKV, TO><<<grid, kRowThreads, smem, s>>>(
+        reinterpret_cast<const TQ*>(q), q_ld, rows_per_chunk, (int)(n_chunks * rows_per_chunk), kv, kv_len,
+        causal ? 1 : 0, q_pos0, reinterpret_cast<TO*>(out), o_ld);
+    WB_CUDA(cudaGetLastError());
+    return WB_OK;
+}
+
+}  // namespace
+
+wb_status attn_flash_enc_bf16(const void* qkv, int64_t n_chunks, int d, int heads, void* out,
+                              cudaStream_t s) {
+    if (n_chunks > 65535) return fail(WB_ERR_SHAPE, "too many chunks for one attention launch");
+    dim3 grid((kCtx + kFaRows - 1) / kFaRows, heads, (unsigned)n_chunks);
+    flash_enc_kernel<<<grid, 128, 0, s>>>(reinterpret_cast<const __nv_bfloat16*>(qkv), d, kCtx,
+                                          reinterpret_cast<__nv_bfloat16*>(out));
+    WB_CUDA(cudaGetLastError());
+    return WB_OK;
+}
+
+wb_status attn_rows(DType tq, DType tkv, DType to, const void* q, int64_t q_ld, int64_t n_chunks,
+                    int rows_per_chunk, int heads, const KVView& kv, int kv_len, bool causal, int q_pos0,
+                    void* out, int64_t o_ld, cudaStream_t s) {
+    if (n_chunks <= 0 || rows_per_chunk <= 0) return WB_OK;
+    if (n_chunks > 0x7FFFFFFF || heads > 65535) return fail(WB_ERR_SHAPE, "attention grid too large");
+#define WB_ROWS(TQ_, TKV_, TO_) \
+    return launch_rows<TQ_, TKV_, TO_>(q, q_ld, n_chunks, rows_per_chunk, heads, kv, kv_len, causal, q_pos0, out, o_ld, s)
+    if (tq == DT_F32 && tkv == DT_F32 && to == DT_F32) WB_ROWS(float, float, float);
+    if (tq == DT_F32 && tkv == DT_BF16 && to == DT_BF16) WB_ROWS(float, __nv_bfloat16, __nv_bfloat16);
+    if (tq == DT_BF16 && tkv == DT_BF16 && to == DT_BF16) WB_ROWS(__nv_bfloat16, __nv_bfloat16, __nv_bfloat16);
+    if (tq == DT_F32 && tkv == DT_E4M3 && to == DT_BF16) WB_ROWS(float, uint8_t, __nv_bfloat16);
+    if (tq == DT_F32 && tkv == DT_F32 && to == DT_BF16) WB_ROWS(float, float, __nv_bfloat16);
+#undef WB_ROWS
+    return fail(WB_ERR_UNSUPPORTED, "attention type combination not built");
+}
+
+}  // namespace wb

@@ -1,0 +1,42 @@
+// Attention launch interface.
+#pragma once
+
+#include <stdint.h>
+
+#include "internal.h"
+
+namespace wb {
+
+enum DType : int { DT_F32 = 0, DT_BF16 = 1, DT_E4M3 = 2 };
+
+// Where the keys/values of (chunk c, head h, key j) live (element offsets):
+//   hs(c)   = head_stride * (chunk_len ? chunk_len[c] : 1)
+//   base(c) = chunk_off ? chunk_off[c] : c * chunk_stride
+//   K[c,h,j] = ptr + base(c) + (k_blk * heads + h) * hs(c) + j * row_stride
+//   V[c,h,j] = ptr + base(c) + (v_blk * heads + h) * hs(c) + j * row_stride
+// E4M3 keys/values are multiplied by k_scale[c] / v_scale[c].
+struct KVView {
+    const void* ptr = nullptr;
+    int64_t chunk_stride = 0;
+    const int64_t* chunk_off = nullptr;
+    int64_t head_stride = 0;
+    const int32_t* chunk_len = nullptr;
+    int heads = 0;
+    int k_blk = 0, v_blk = 1;
+    int64_t row_stride = 64;
+    const float* k_scale = nullptr;
+    const float* v_scale = nullptr;
+};
+
+// Encoder self-attention, bf16: qkv [n_chunks*1500, 3d] -> out [n_chunks*1500, d].
+wb_status attn_flash_enc_bf16(const void* qkv, int64_t n_chunks, int d, int heads, void* out,
+                              cudaStream_t s);
+
+// Row attention: query row r of chunk c is q[(c*rows_per_chunk + r) * q_ld + h*64 ..]
+// (pre-scaling by 1/8 inside); it attends over keys 0..kv_len-1, or, when
+// causal, over keys 0..q_pos0 + r.  Output row likewise with o_ld.
+wb_status attn_rows(DType tq, DType tkv, DType to, const void* q, int64_t q_ld, int64_t n_chunks,
+                    int rows_per_chunk, int heads, const KVView& kv, int kv_len, bool causal, int q_pos0,
+                    void* out, int64_t o_ld, cudaStream_t s);
+
+}  // namespace wb

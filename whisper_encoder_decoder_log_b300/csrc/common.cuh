@@ -1,0 +1,236 @@
+// Shared device helpers for the sm_103a kernels: bf16/E4M3 conversions,
+// warp reductions, mbarrier / TMA / tcgen05 wrappers (inline PTX) and the
+// bounded-wait error word.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#define WB_DEV __device__ __forceinline__
+
+// ----------------------------------------------------------------- error word
+// Device-side failures (a bounded wait that ran out, a bounds check) set bits
+// in a global word the host reads with wb_sync_status.  Kernels never trap.
+#define WB_DEVERR_TIMEOUT_TMA   0x1u
+#define WB_DEVERR_TIMEOUT_MMA   0x2u
+#define WB_DEVERR_TIMEOUT_EPI   0x4u
+#define WB_DEVERR_BOUNDS        0x8u
+#define WB_DEVERR_TMEM          0x10u
+
+// Every spin on an mbarrier is bounded by wall time read from %globaltimer:
+// a legitimate wait lasts microseconds to milliseconds; after 2 s the waiter
+// gives up, records an error bit and lets its CTA wind down.
+#define WB_WAIT_NS 2000000000ull
+
+WB_DEV void wb_set_error(unsigned* err, unsigned bits) {
+    if (err) atomicOr(err, bits);
+}
+
+// ----------------------------------------------------------------- numerics
+WB_DEV float bf2f(__nv_bfloat16 x) { return __bfloat162float(x); }
+WB_DEV __nv_bfloat16 f2bf(float x) { return __float2bfloat16_rn(x); }
+
+WB_DEV uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Two fp32 -> two E4M3 codes, round to nearest even with saturation (the
+// hardware conversion; the byte for `lo` is the low byte).
+WB_DEV uint16_t f2e4m3x2(float lo, float hi) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+WB_DEV float e4m3_to_f(uint8_t c) {
+    __nv_fp8_e4m3 v;
+    v.__x = c;
+    return float(v);
+}
+
+WB_DEV float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+WB_DEV float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+// Exact GELU x * Phi(x) via the library erf.
+WB_DEV float gelu_f(float x) { return 0.5f * x * (1.0f + erff(x * 0.70710678118654752f)); }
+
+// ----------------------------------------------------------------- smem/mbarrier
+WB_DEV uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+WB_DEV void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
+}
+
+WB_DEV void fence_barrier_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+WB_DEV void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+WB_DEV void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;"
+                 ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+
+WB_DEV void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];"
+                 ::"r"(smem_u32(bar)) : "memory");
+}
+
+WB_DEV bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n"
+        " mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
+    return ok != 0;
+}
+
+WB_DEV uint64_t globaltimer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Deadline helper: expired() is true once WB_WAIT_NS have passed since
+// construction (the clock is read every 64 polls).
+struct WaitClock {
+    uint64_t t0 = 0;
+    uint32_t n = 0;
+    WB_DEV bool expired() {
+        if ((++n & 63u) != 1u) return false;
+        const uint64_t t = globaltimer_ns();
+        if (t0 == 0) { t0 = t; return false; }
+        return t - t0 > WB_WAIT_NS;
+    }
+};
+
+// Bounded wait: returns false (and sets `bits` in the error word) when the
+// phase did not complete within the deadline.
+WB_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned* err, unsigned bits) {
+    WaitClock clk;
+    while (!mbar_try_wait(bar, parity))
+        if (clk.expired()) {
+            wb_set_error(err, bits);
+            return false;
+        }
+    return true;
+}
+
+// ----------------------------------------------------------------- TMA
+WB_DEV void tma_prefetch_desc(const CUtensorMap* m) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
+}
+
+WB_DEV void tma_load_2d(void* dst, const CUtensorMap* m, uint64_t* bar, int x, int y) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4}], [%2];"
+        ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(m)), "r"(smem_u32(bar)),
+          "r"(x), "r"(y) : "memory");
+}
+
+WB_DEV void tma_load_3d(void* dst, const CUtensorMap* m, uint64_t* bar, int x, int y, int z) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5}], [%2];"
+        ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(m)), "r"(smem_u32(bar)),
+          "r"(x), "r"(y), "r"(z) : "memory");
+}
+
+// ----------------------------------------------------------------- tcgen05
+// Shared-memory matrix descriptor for a K-major operand tile stored with the
+// 128-byte swizzle (8 rows x 128 B atoms, atoms stacked every 1024 B):
+// start address >> 4 in bits 0-13, leading byte offset (unused for swizzled
+// K-major, set to 1) in 16-29, stride byte offset 1024 >> 4 in 32-45, the
+// descriptor version 1 in bits 46-47, swizzle mode 2 (128 B) in bits 61-63.
+WB_DEV uint64_t umma_desc_sw128(uint32_t smem_addr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((smem_addr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)1 << 16;
+    d |= (uint64_t)(1024 >> 4) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+
+// Instruction descriptor: dense, fp32 accumulator (bits 4-5 = 1), A/B type
+// in bits 7-9 / 10-12, both K-major, N >> 3 in bits 17-22, M >> 4 in 24-28.
+//   kind::f16    : type 1 = bf16
+//   kind::f8f6f4 : type 0 = E4M3
+template <int M, int N, int AB_TYPE>
+struct UmmaIdesc {
+    static constexpr uint32_t value = (1u << 4) | ((uint32_t)AB_TYPE << 7) |
+                                      ((uint32_t)AB_TYPE << 10) | ((uint32_t)(N >> 3) << 17) |
+                                      ((uint32_t)(M >> 4) << 24);
+};
+
+WB_DEV void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                 ::"r"(smem_u32(dst_smem)), "r"(ncols) : "memory");
+}
+WB_DEV void tmem_relinquish() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+WB_DEV void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;"
+                 ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+WB_DEV void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                      uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n"
+        ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate) : "memory");
+}
+
+WB_DEV void umma_fp8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                     uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n}\n"
+        ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate) : "memory");
+}
+
+// Arrive on an mbarrier once all previously issued tcgen05.mma of this thread
+// have completed.
+WB_DEV void umma_commit(uint64_t* bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+        ::"r"(smem_u32(bar)) : "memory");
+}
+
+WB_DEV void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+WB_DEV void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// 32 lanes x 32 consecutive 32-bit columns from TMEM into registers.
+WB_DEV void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32"
+        " {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+          "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]),
+          "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]),
+          "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]),
+          "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+}
+WB_DEV void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }

@@ -1,0 +1,551 @@
+// Dense contractions of the encoder/decoder on the 5th-generation tensor
+// cores ("whisper-blaze 0.1.8" lists FP16/FP8 tensor-core GEMMs fed by TMA for
+// the QKV, output and FFN projections; here they are tcgen05 with TMEM
+// accumulators for sm_103a).
+//
+// Kernel shape: persistent, one CTA per SM, 192 threads in three roles.
+//   warp 0      TMA producer: 128 x 128-byte A box and BN x 128-byte B box per
+//               k-block into a STAGES-deep ring (128-byte swizzle).
+//   warp 1      owns TMEM (2 x BN fp32 columns: a double-buffered accumulator)
+//               and, from one thread, issues tcgen05.mma (M 128, N BN, K 16
+//               for bf16 / 32 for E4M3) and tcgen05.commit to release stages
+//               and to hand a finished accumulator to the epilogue.
+//   warps 2-5   epilogue: tcgen05.ld 32 columns at a time, scale, bias, GELU,
+//               positional table, residual accumulate, store.
+// Tiles are visited in groups of 16 M-tiles so that the A panel of a group and
+// the whole B operand stay in L2.  Every mbarrier wait is bounded; a wait that
+// runs out records an error bit and the CTA winds down (waiting, bounded, for
+// its own TMA copies and MMAs) before releasing TMEM.
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "common.cuh"
+#include "gemm.cuh"
+
+namespace wb {
+
+namespace {
+
+constexpr int kBM = 128;
+constexpr int kRowBytes = 128;       // one k-block row: 64 bf16 or 128 E4M3
+constexpr int kGroupM = 16;
+
+template <int BN>
+struct Cfg {
+    static constexpr int A_BYTES = kBM * kRowBytes;
+    static constexpr int B_BYTES = BN * kRowBytes;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int STAGES = (196 * 1024) / STAGE_BYTES > 8 ? 8 : (196 * 1024) / STAGE_BYTES;
+    static constexpr int TMEM_COLS = 2 * BN;
+    static constexpr int SMEM = STAGES * STAGE_BYTES + 1024 + 256;
+};
+
+struct GemmArgs {
+    int64_t rows;            // rows per batch
+    int64_t batches;
+    int64_t N, K;
+    int64_t mt_per_batch, mt_total, nt_total, tiles;
+    int kblocks;
+    GemmEpi epi;
+};
+
+__device__ __forceinline__ void tile_coords(const GemmArgs& a, int64_t t, int64_t& mt, int64_t& nt) {
+    const int64_t group = (int64_t)kGroupM * a.nt_total;
+    const int64_t gid = t / group;
+    const int64_t first_m = gid * kGroupM;
+    const int64_t gsz = min((int64_t)kGroupM, a.mt_total - first_m);
+    const int64_t local = t % group;
+    mt = first_m + local % gsz;
+    nt = local / gsz;
+}
+
+__device__ __forceinline__ void store_chunk(const GemmArgs& a, int64_t b, int64_t r, int64_t n0,
+                                            float (&v)[32]) {
+    const GemmEpi& e = a.epi;
+    const int64_t N = a.N;
+    const bool full = n0 + 32 <= N;
+    // scale, bias, GELU, positional table
+    if (e.row_scale || e.col_scale) {
+        const float rs = e.row_scale ? e.row_scale[b * a.rows + r] : 1.f;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            const float cs = (e.col_scale && (full || n0 + j < N)) ? e.col_scale[n0 + j] : 1.f;
+            v[j] *= rs * cs;
+        }
+    }
+    if (e.bias) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] += (full || n0 + j < N) ? e.bias[n0 + j] : 0.f;
+    }
+    if (e.gelu) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = gelu_f(v[j]);
+    }
+    if (e.add) {
+        const float* ap = e.add + r * e.ld_add + n0;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] += (full || n0 + j < N) ? ap[j] : 0.f;
+    }
+    int64_t orow;
+    void* base;
+    if (e.mode == MODE_CROSS_KV) {
+        const int64_t m = b * a.rows + r;
+        const int64_t ch = m / kCtx, s = m % kCtx;
+        const int64_t two_d = 2 * (int64_t)e.ckv_d;
+        const int64_t l = n0 / two_d, rem = n0 % two_d;
+        const int64_t kv = rem / e.ckv_d, h = (rem % e.ckv_d) / 64, c0 = n0 % 64;
+        const int64_t off = ((((l * e.ckv_chunks + ch) * 2 + kv) * e.ckv_heads + h) * kCtx + s) * 64 + c0;
+        __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(e.out) + off;
+        uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            d4[q] = make_uint4(pack_bf16x2(v[8 * q + 0], v[8 * q + 1]), pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
+                               pack_bf16x2(v[8 * q + 4], v[8 * q + 5]), pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
+        return;
+    }
+    const int64_t obr = e.out_batch_rows ? e.out_batch_rows : a.rows;
+    orow = b * obr + e.out_row_offset + r;
+    base = e.out;
+    if (e.out_type == OUT_BF16) {
+        __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(base) + orow * e.ldo + n0;
+        if (full) {
+            uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                d4[q] = make_uint4(pack_bf16x2(v[8 * q + 0], v[8 * q + 1]),
+                                   pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
+                                   pack_bf16x2(v[8 * q + 4], v[8 * q + 5]),
+                                   pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
+        } else {
+            for (int j = 0; j < 32 && n0 + j < N; ++j) dst[j] = f2bf(v[j]);
+        }
+    } else {
+        float* dst = reinterpret_cast<float*>(base) + orow * e.ldo + n0;
+        const bool acc = e.out_type == OUT_F32_ACC;
+        if (full) {
+            float4* d4 = reinterpret_cast<float4*>(dst);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                float4 w = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+                if (acc) {
+                    const float4 o = d4[q];
+                    w.x += o.x; w.y += o.y; w.z += o.z; w.w += o.w;
+                }
+                d4[q] = w;
+            }
+        } else {
+            for (int j = 0; j < 32 && n0 + j < N; ++j) dst[j] = acc ? dst[j] + v[j] : v[j];
+        }
+    }
+}
+
+template <int BN, bool FP8>
+__global__ void __launch_bounds__(192, 1)
+gemm_tc_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUtensorMap tma_b,
+               const GemmArgs args, unsigned* err) {
+    using C = Cfg<BN>;
+    constexpr int STAGES = C::STAGES;
+    constexpr uint32_t IDESC = UmmaIdesc<kBM, BN, FP8 ? 0 : 1>::value;
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    unsigned char* smem = reinterpret_cast<unsigned char*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + STAGES * C::STAGE_BYTES);
+    uint64_t* empty_bar = full_bar + STAGES;
+    uint64_t* tfull_bar = empty_bar + STAGES;     // [2]
+    uint64_t* tempty_bar = tfull_bar + 2;         // [2]
+    uint64_t* drain_bar = tempty_bar + 2;         // [1]
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain_bar + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&full_bar[s], 1);
+            mbar_init(&empty_bar[s], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&tfull_bar[i], 1);
+            mbar_init(&tempty_bar[i], 128);
+        }
+        mbar_init(drain_bar, 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+        tma_prefetch_desc(&tma_a);
+        tma_prefetch_desc(&tma_b);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t last_parity[8];
+            bool issued[8];
+            for (int s = 0; s < 8; ++s) { issued[s] = false; last_parity[s] = 0; }
+            bool ok = true;
+            for (int64_t t = blockIdx.x; t < args.tiles && ok; t += gridDim.x) {
+                int64_t mt, nt;
+                tile_coords(args, t, mt, nt);
+                const int b = (int)(mt / args.mt_per_batch);
+                const int r0 = (int)((mt % args.mt_per_batch) * kBM);
+                const int n0 = (int)(nt * BN);
+                for (int kb = 0; kb < args.kblocks; ++kb) {
+                    bool got = false;
+                    for (WaitClock clk; !clk.expired();) {
+                        if (mbar_try_wait(&empty_bar[stage], phase ^ 1)) { got = true; break; }
+                        if (*abort_flag) break;
+                    }
+                    if (!got) {
+                        wb_set_error(err, WB_DEVERR_TIMEOUT_TMA);
+                        *abort_flag = 1;
+                        ok = false;
+                        break;
+                    }
+                    unsigned char* sa = smem + stage * C::STAGE_BYTES;
+                    unsigned char* sb = sa + C::A_BYTES;
+                    mbar_arrive_expect_tx(&full_bar[stage], C::STAGE_BYTES);
+                    const int kx = kb * (FP8 ? 128 : 64);
+                    tma_load_3d(sa, &tma_a, &full_bar[stage], kx, r0, b);
+                    tma_load_2d(sb, &tma_b, &full_bar[stage], kx, n0);
+                    issued[stage] = true;
+                    last_parity[stage] = phase;
+                    if (++stage == STAGES) { stage = 0; phase ^= 1; }
+                }
+            }
+            // never leave TMA writes in flight into this CTA's shared memory
+            for (int s = 0; s < STAGES; ++s)
+                if (issued[s]) mbar_wait(&full_bar[s], last_parity[s], err, WB_DEVERR_TIMEOUT_TMA);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            int local = 0;
+            bool ok = true;
+            bool any = false;
+            for (int64_t t = blockIdx.x; t < args.tiles && ok; t += gridDim.x, ++local) {
+                const int acc = local & 1;
+                const uint32_t aphase = (local >> 1) & 1;
+                bool got = false;
+                for (WaitClock clk; !clk.expired();) {
+                    if (mbar_try_wait(&tempty_bar[acc], aphase ^ 1)) { got = true; break; }
+                    if (*abort_flag) break;
+                }
+                if (!got) { wb_set_error(err, WB_DEVERR_TIMEOUT_MMA); *abort_flag = 1; break; }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + acc * BN;
+                for (int kb = 0; kb < args.kblocks; ++kb) {
+                    got = false;
+                    for (WaitClock clk; !clk.expired();) {
+                        if (mbar_try_wait(&full_bar[stage], phase)) { got = true; break; }
+                        if (*abort_flag) break;
+                    }
+                    if (!got) { wb_set_error(err, WB_DEVERR_TIMEOUT_MMA); *abort_flag = 1; ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t a_addr = smem_u32(smem + stage * C::STAGE_BYTES);
+                    const uint32_t b_addr = a_addr + C::A_BYTES;
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const uint64_t ad = umma_desc_sw128(a_addr + 32 * k);
+                        const uint64_t bd = umma_desc_sw128(b_addr + 32 * k);
+                        if (FP8) umma_fp8(d_tmem, ad, bd, IDESC, (kb | k) ? 1u : 0u);
+                        else umma_bf16(d_tmem, ad, bd, IDESC, (kb | k) ? 1u : 0u);
+                    }
+                    any = true;
+                    umma_commit(&empty_bar[stage]);
+                    if (++stage == STAGES) { stage = 0; phase ^= 1; }
+                }
+                if (!ok) break;
+                umma_commit(&tfull_bar[acc]);
+            }
+            // all issued MMAs complete before TMEM can be released
+            if (any) {
+                umma_commit(drain_bar);
+                mbar_wait(drain_bar, 0, err, WB_DEVERR_TIMEOUT_MMA);
+            }
+        }
+    } else {
+        // epilogue warps 2..5 -> TMEM lane groups 2,3,0,1
+        const int g = warp & 3;
+        int local = 0;
+        for (int64_t t = blockIdx.x; t < args.tiles; t += gridDim.x, ++local) {
+            const int acc = local & 1;
+            const uint32_t aphase = (local >> 1) & 1;
+            bool got = false;
+            for (WaitClock clk; !clk.expired();) {
+                if (mbar_try_wait(&tfull_bar[acc], aphase)) { got = true; break; }
+                if (*abort_flag) break;
+            }
+            if (!got) { wb_set_error(err, WB_DEVERR_TIMEOUT_EPI); *abort_flag = 1; break; }
+            tc_fence_after();
+            int64_t mt, nt;
+            tile_coords(args, t, mt, nt);
+            const int64_t b = mt / args.mt_per_batch;
+            const int64_t r = (mt % args.mt_per_batch) * kBM + g * 32 + lane;
+            const bool row_ok = r < args.rows;
+            const uint32_t taddr = tmem_base + ((uint32_t)(g * 32) << 16) + acc * BN;
+#pragma unroll 1
+            for (int c = 0; c < BN / 32; ++c) {
+                uint32_t raw[32];
+                tmem_ld32(taddr + c * 32, raw);
+                tmem_wait_ld();
+                const int64_t n0 = nt * BN + c * 32;
+                if (row_ok && n0 < args.N) {
+                    float v[32];
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(raw[j]);
+                    store_chunk(args, b, r, n0, v);
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(&tempty_bar[acc]);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem_base, C::TMEM_COLS);
+}
+
+// ------------------------------------------------------------------ host: TMA
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+wb_status get_encoder() {
+    std::call_once(g_encode_once, [] {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    if (!g_encode) return fail(WB_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
+    return WB_OK;
+}
+
+wb_status encode_map(CUtensorMap* m, const void* ptr, int rank, const uint64_t* dims,
+                     const uint64_t* strides_bytes, const uint32_t* box, bool fp8) {
+    uint32_t estr[3] = {1, 1, 1};
+    CUresult r = g_encode(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                          rank, const_cast<void*>(ptr), dims, strides_bytes, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(WB_ERR_SHAPE, "cuTensorMapEncodeTiled rejected an operand");
+    return WB_OK;
+}
+
+int g_num_sms = 0;
+
+template <int BN, bool FP8>
+wb_status launch_tc(const GemmPlan& p, const GemmArgs& a, unsigned* err, cudaStream_t s, int max_ctas) {
+    using C = Cfg<BN>;
+    static bool attr_set[64] = {};
+    int dev = 0;
+    WB_CUDA(cudaGetDevice(&dev));
+    if (!attr_set[dev & 63]) {
+        WB_CUDA(cudaFuncSetAttribute(gemm_tc_kernel<BN, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     C::SMEM));
+        attr_set[dev & 63] = true;
+    }
+    int grid = num_sms();
+    if (max_ctas > 0) grid = std::min(grid, max_ctas);
+    grid = (int)std::min<int64_t>(grid, a.tiles);
+    if (grid <= 0) return WB_OK;
+    gemm_tc_kernel<BN, FP8><<<grid, 192, C::SMEM, s>>>(p.tma_a, p.tma_b, a, err);
+    WB_CUDA(cudaGetLastError());
+    return WB_OK;
+}
+
+}  // namespace
+
+int num_sms() {
+    if (!g_num_sms) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev);
+        if (g_num_sms <= 0) g_num_sms = 148;
+    }
+    return g_num_sms;
+}
+
+wb_status gemm_plan(GemmPlan* plan, const GemmOperand& A, const GemmOperand& B, int64_t N, int64_t K,
+                    bool fp8, int bn) {
+    if (wb_status st = get_encoder()) return st;
+    const int esz = fp8 ? 1 : 2;
+    const int bk = fp8 ? 128 : 64;
+    if (K % bk != 0) return fail(WB_ERR_SHAPE, "GEMM K must be a multiple of the k-block");
+    if (bn != 64 && bn != 128 && bn != 256) return fail(WB_ERR_SHAPE, "GEMM BN must be 64/128/256");
+    if (!aligned16(A.ptr) || !aligned16(B.ptr)) return fail(WB_ERR_ALIGN, "GEMM operand not 16-byte aligned");
+    if ((A.row_stride * esz) % 16 || (B.row_stride * esz) % 16 || (A.batch_stride * esz) % 16)
+        return fail(WB_ERR_ALIGN, "GEMM operand stride not a multiple of 16 bytes");
+    {
+        uint64_t dims[3] = {(uint64_t)K, (uint64_t)A.rows, (uint64_t)A.batches};
+        uint64_t bstride = A.batches > 1 ? A.batch_stride : A.rows * A.row_stride;
+        uint64_t strides[2] = {(uint64_t)(A.row_stride * esz), (uint64_t)(bstride * esz)};
+        uint32_t box[3] = {(uint32_t)bk, (uint32_t)kBM, 1};
+        if (wb_status st = encode_map(&plan->tma_a, A.ptr, 3, dims, strides, box, fp8)) return st;
+    }
+    {
+        uint64_t dims[2] = {(uint64_t)K, (uint64_t)N};
+        uint64_t strides[1] = {(uint64_t)(B.row_stride * esz)};
+        uint32_t box[2] = {(uint32_t)bk, (uint32_t)bn};
+        if (wb_status st = encode_map(&plan->tma_b, B.ptr, 2, dims, strides, box, fp8)) return st;
+    }
+    plan->M_rows = A.rows;
+    plan->batches = A.batches;
+    plan->N = N;
+    plan->K = K;
+    plan->bn = bn;
+    plan->fp8 = fp8;
+    plan->ok = true;
+    return WB_OK;
+}
+
+wb_status gemm_run(const GemmPlan& p, const GemmEpi& epi, unsigned* err, cudaStream_t s, int max_ctas) {
+    if (!p.ok) return fail(WB_ERR_INVALID_ARG, "GEMM plan not built");
+    if (epi.out_type == OUT_BF16 && epi.mode == MODE_PLAIN && (epi.ldo % 8))
+        return fail(WB_ERR_ALIGN, "bf16 GEMM output stride must be a multiple of 8");
+    if (epi.out_type != OUT_BF16 && (epi.ldo % 4)) return fail(WB_ERR_ALIGN, "fp32 output stride % 4");
+    GemmArgs a;
+    a.rows = p.M_rows;
+    a.batches = p.batches;
+    a.N = p.N;
+    a.K = p.K;
+    a.mt_per_batch = (p.M_rows + kBM - 1) / kBM;
+    a.mt_total = a.mt_per_batch * p.batches;
+    a.nt_total = (p.N + p.bn - 1) / p.bn;
+    a.tiles = a.mt_total * a.nt_total;
+    a.kblocks = (int)(p.K / (p.fp8 ? 128 : 64));
+    a.epi = epi;
+    if (a.tiles == 0 || a.kblocks == 0) return WB_OK;
+    if (p.fp8) {
+        if (p.bn == 256) return launch_tc<256, true>(p, a, err, s, max_ctas);
+        if (p.bn == 128) return launch_tc<128, true>(p, a, err, s, max_ctas);
+        return launch_tc<64, true>(p, a, err, s, max_ctas);
+    }
+    if (p.bn == 256) return launch_tc<256, false>(p, a, err, s, max_ctas);
+    if (p.bn == 128) return launch_tc<128, false>(p, a, err, s, max_ctas);
+    return launch_tc<64, false>(p, a, err, s, max_ctas);
+}
+
+// ------------------------------------------------------------------ SIMT GEMM
+namespace {
+
+template <bool ABF, bool BBF>
+__global__ void __launch_bounds__(256)
+gemm_simt_kernel(const void* __restrict__ Ap, GemmOperand A, const void* __restrict__ Bp, int64_t ldb,
+                 GemmArgs args) {
+    // 64 x 64 output tile, 16-deep k-steps, 4 x 4 per thread.
+    __shared__ float As[16][64 + 4];
+    __shared__ float Bs[16][64 + 4];
+    const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;
+    const int64_t mt = blockIdx.y, nt = blockIdx.x;
+    const int64_t b = mt / args.mt_per_batch;
+    const int64_t r0 = (mt % args.mt_per_batch) * 64;
+    const int64_t n0 = nt * 64;
+    float acc[4][4] = {};
+    for (int64_t k0 = 0; k0 < args.K; k0 += 16) {
+        for (int i = threadIdx.x; i < 16 * 64; i += 256) {
+            const int kk = i % 16, rr = i / 16;
+            const int64_t r = r0 + rr, k = k0 + kk;
+            float va = 0.f;
+            if (r < args.rows && k < args.K) {
+                const int64_t idx = b * A.batch_stride + r * A.row_stride + k;
+                va = ABF ? bf2f(reinterpret_cast<const __nv_bfloat16*>(Ap)[idx])
+                         : reinterpret_cast<const float*>(Ap)[idx];
+            }
+            As[kk][rr] = va;
+            const int64_t n = n0 + rr;
+            float vb = 0.f;
+            if (n < args.N && k < args.K) {
+                const int64_t idx = n * ldb + k;
+                vb = BBF ? bf2f(reinterpret_cast<const __nv_bfloat16*>(Bp)[idx])
+                         : reinterpret_cast<const float*>(Bp)[idx];
+            }
+            Bs[kk][rr] = vb;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int kk = 0; kk < 16; ++kk) {
+            float a4[4], b4[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) { a4[i] = As[kk][ty * 4 + i]; b4[i] = Bs[kk][tx * 4 + i]; }
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a4[i], b4[j], acc[i][j]);
+        }
+        __syncthreads();
+    }
+    const GemmEpi& e = args.epi;
+    for (int i = 0; i < 4; ++i) {
+        const int64_t r = r0 + ty * 4 + i;
+        if (r >= args.rows) continue;
+        for (int j = 0; j < 4; ++j) {
+            const int64_t n = n0 + tx * 4 + j;
+            if (n >= args.N) continue;
+            float v = acc[i][j];
+            if (e.row_scale) v *= e.row_scale[b * args.rows + r];
+            if (e.col_scale) v *= e.col_scale[n];
+            if (e.bias) v += e.bias[n];
+            if (e.gelu) v = gelu_f(v);
+            if (e.add) v += e.add[r * e.ld_add + n];
+            if (e.mode == MODE_CROSS_KV) {
+                const int64_t m = b * args.rows + r;
+                const int64_t ch = m / kCtx, s = m % kCtx;
+                const int64_t two_d = 2 * (int64_t)e.ckv_d;
+                const int64_t l = n / two_d, rem = n % two_d;
+                const int64_t kv = rem / e.ckv_d, h = (rem % e.ckv_d) / 64, c = n % 64;
+                const int64_t off = ((((l * e.ckv_chunks + ch) * 2 + kv) * e.ckv_heads + h) * kCtx + s) * 64 + c;
+                if (e.out_type == OUT_BF16) reinterpret_cast<__nv_bfloat16*>(e.out)[off] = f2bf(v);
+                else reinterpret_cast<float*>(e.out)[off] = v;
+                continue;
+            }
+            const int64_t obr = e.out_batch_rows ? e.out_batch_rows : args.rows;
+            const int64_t orow = b * obr + e.out_row_offset + r;
+            if (e.out_type == OUT_BF16) reinterpret_cast<__nv_bfloat16*>(e.out)[orow * e.ldo + n] = f2bf(v);
+            else if (e.out_type == OUT_F32) reinterpret_cast<float*>(e.out)[orow * e.ldo + n] = v;
+            else reinterpret_cast<float*>(e.out)[orow * e.ldo + n] += v;
+        }
+    }
+}
+
+}  // namespace
+
+wb_status gemm_simt(const GemmOperand& A, bool a_bf16, const GemmOperand& B, bool b_bf16, int64_t N,
+                    int64_t K, const GemmEpi& epi, cudaStream_t s) {
+    GemmArgs a;
+    a.rows = A.rows;
+    a.batches = A.batches;
+    a.N = N;
+    a.K = K;
+    a.mt_per_batch = (A.rows + 63) / 64;
+    a.mt_total = a.mt_per_batch * A.batches;
+    a.nt_total = (N + 63) / 64;
+    a.tiles = a.mt_total * a.nt_total;
+    a.kblocks = 0;
+    a.epi = epi;
+    if (a.tiles == 0) return WB_OK;
+    if (a.mt_total > 65535) return fail(WB_ERR_SHAPE, "SIMT GEMM: too many row tiles");
+    dim3 grid((unsigned)a.nt_total, (unsigned)a.mt_total);
+    if (a_bf16 && b_bf16) gemm_simt_kernel<true, true><<<grid, 256, 0, s>>>(A.ptr, A, B.ptr, B.row_stride, a);
+    else if (!a_bf16 && b_bf16) gemm_simt_kernel<false, true><<<grid, 256, 0, s>>>(A.ptr, A, B.ptr, B.row_stride, a);
+    else if (a_bf16 && !b_bf16) gemm_simt_kernel<true, false><<<grid, 256, 0, s>>>(A.ptr, A, B.ptr, B.row_stride, a);
+    else gemm_simt_kernel<false, false><<<grid, 256, 0, s>>>(A.ptr, A, B.ptr, B.row_stride, a);
+    WB_CUDA(cudaGetLastError());
+    return WB_OK;
+}
+
+}  // namespace wb

@@ -1,0 +1,386 @@
+// Memory-bound kernels around the GEMMs and attention: LayerNorm (fused with
+// the FP8 per-row quantiser when the next GEMM runs in E4M3), token + position
+// embedding, the E4M3 KV-cache scale and append, the per-tensor quantiser,
+// greedy argmax with token bookkeeping, and weight re-layouts done once at
+// model creation.
+//
+// LayerNorm follows "whisper-blaze 0.1.8", "Direct Kernel API"
+// (layernorm_fused, eps 1e-5); FP8 quantisation follows the same page's
+// quantise_e4m3 (per-tensor scale, amax / 448) and the float8 KV cache of
+// "Blazingly fast whisper transcriptions with Inference Endpoints",
+// "Inference Stack"; greedy choice follows the "thewhisper-large-v3-turbo"
+// model card, "NVIDIA Usage" (no sampling, one beam).
+#include "common.cuh"
+#include "layers.cuh"
+
+namespace wb {
+namespace {
+
+constexpr int kMaxPerLane = 40;   // d <= 1280
+
+// One warp per row; the row lives in registers for the two-pass moments.
+template <int OUT>
+__global__ void __launch_bounds__(256)
+layernorm_kernel(const float* __restrict__ x, int64_t ld_x, int64_t rows, int d, const float* __restrict__ g,
+                 const float* __restrict__ b, void* __restrict__ out, int64_t ld_o, float* __restrict__ row_scale) {
+    const int64_t row = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (row >= rows) return;
+    const float* xr = x + row * ld_x;
+    const int per = d / 32;
+    float v[kMaxPerLane];
+    float s = 0.f;
+#pragma unroll
+    for (int i = 0; i < kMaxPerLane; ++i)
+        if (i < per) { v[i] = xr[i * 32 + lane]; s += v[i]; }
+    s = warp_sum(s);
+    const float mean = s / (float)d;
+    float q = 0.f;
+#pragma unroll
+    for (int i = 0; i < kMaxPerLane; ++i)
+        if (i < per) { const float t = v[i] - mean; q = fmaf(t, t, q); }
+    q = warp_sum(q);
+    const float rstd = rsqrtf(q / (float)d + 1e-5f);
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < kMaxPerLane; ++i)
+        if (i < per) {
+            const int c = i * 32 + lane;
+            v[i] = (v[i] - mean) * rstd * g[c] + b[c];
+            amax = fmaxf(amax, fabsf(v[i]));
+        }
+    if (OUT == LN_F32) {
+        float* o = reinterpret_cast<float*>(out) + row * ld_o;
+#pragma unroll
+        for (int i = 0; i < kMaxPerLane; ++i)
+            if (i < per) o[i * 32 + lane] = v[i];
+    } else if (OUT == LN_BF16) {
+        __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(out) + row * ld_o;
+#pragma unroll
+        for (int i = 0; i < kMaxPerLane; ++i)
+            if (i < per) o[i * 32 + lane] = f2bf(v[i]);
+    } else {   // LN_E4M3: per-row scale amax / 448
+        amax = warp_max(amax);
+        const float sc = amax > 0.f ? amax / 448.0f : 1.0f;
+        const float inv = 1.0f / sc;
+        uint8_t* o = reinterpret_cast<uint8_t*>(out) + row * ld_o;
+#pragma unroll
+        for (int i = 0; i < kMaxPerLane; ++i)
+            if (i < per) o[i * 32 + lane] = (uint8_t)(f2e4m3x2(v[i] * inv, 0.f) & 0xFF);
+        if (lane == 0) row_scale[row] = sc;
+    }
+}
+
+// x[r] = E[token] + P[pos] in fp32.  Row r is (chunk c = r / P, position
+// p0 + r % P); the token is tokens[c * 448 + pos].
+template <typename TW>
+__global__ void embed_kernel(const int32_t* __restrict__ tokens, int64_t rows, int P, int p0, int d,
+                             const TW* __restrict__ E, const TW* __restrict__ Pos, int vocab,
+                             float* __restrict__ x, unsigned* err) {
+    const int64_t r = blockIdx.x;
+    if (r >= rows) return;
+    const int64_t c = r / P;
+    const int pos = p0 + (int)(r % P);
+    int tok = tokens[c * kMaxPos + pos];
+    if (tok < 0 || tok >= vocab) {
+        if (threadIdx.x == 0) wb_set_error(err, WB_DEVERR_BOUNDS);
+        tok = 0;
+    }
+    for (int i = threadIdx.x; i < d; i += blockDim.x)
+        x[r * d + i] = (float)E[(int64_t)tok * d + i] + (float)Pos[(int64_t)pos * d + i];
+}
+
+// Per (chunk, K|V): s = 2 * max(amax over the chunk's P rows, 1e-12) / 448.
+__global__ void kv_scale_kernel(const float* __restrict__ qkv, int P, int d, float* __restrict__ k_scale,
+                                float* __restrict__ v_scale) {
+    const int64_t c = blockIdx.x;
+    const int which = blockIdx.y;   // 0: K, 1: V
+    float m = 0.f;
+    for (int i = threadIdx.x; i < P * d; i += blockDim.x) {
+        const int p = i / d, col = i % d;
+        m = fmaxf(m, fabsf(qkv[(c * P + p) * 3 * (int64_t)d + (1 + which) * d + col]));
+    }
+    m = warp_max(m);
+    __shared__ float red[8];
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float a = red[0];
+        for (int i = 1; i < (int)(blockDim.x >> 5); ++i) a = fmaxf(a, red[i]);
+        a = fmaxf(a, 1e-12f);
+        const float s = (2.0f * a) / 448.0f;
+        (which ? v_scale : k_scale)[c] = s;
+    }
+}
+
+// Append K/V rows (fp32 inputs from the QKV GEMM) into the cache at
+// positions p0 .. p0+P-1 of each chunk: E4M3 with the chunk's frozen scale,
+// or fp32.  Cache of chunk c, layer l: base + off[c] + ((2l + kv) H + h) L_c 64 + pos 64.
+template <bool FP8>
+__global__ void kv_append_kernel(const float* __restrict__ qkv, int64_t n_chunks, int P, int p0, int d, int H,
+                                 int layer, void* __restrict__ cache, const int64_t* __restrict__ off,
+                                 const int32_t* __restrict__ len, const float* __restrict__ k_scale,
+                                 const float* __restrict__ v_scale, unsigned* err) {
+    const int64_t r = blockIdx.x;   // row = c * P + p
+    const int64_t c = r / P;
+    const int pos = p0 + (int)(r % P);
+    if (c >= n_chunks) return;
+    const int L = len[c];
+    if (pos >= L) {
+        if (threadIdx.x == 0) wb_set_error(err, WB_DEVERR_BOUNDS);
+        return;
+    }
+    for (int i = threadIdx.x; i < 2 * d; i += blockDim.x) {
+        const int kv = i / d, col = i % d, h = col / 64, e = col % 64;
+        const float x = qkv[r * 3 * (int64_t)d + d + i];
+        const int64_t idx = off[c] + ((int64_t)(2 * layer + kv) * H + h) * L * 64 + (int64_t)pos * 64 + e;
+        if (FP8) {
+            const float s = kv ? v_scale[c] : k_scale[c];
+            const float inv = 1.0f / s;
+            reinterpret_cast<uint8_t*>(cache)[idx] = (uint8_t)(f2e4m3x2(x * inv, 0.f) & 0xFF);
+        } else {
+            reinterpret_cast<float*>(cache)[idx] = x;
+        }
+    }
+}
+
+// Per-row E4M3 quantisation of a bf16 matrix (FC2's input in mixed_fp8).
+__global__ void quant_rows_kernel(const __nv_bfloat16* __restrict__ x, int64_t rows, int K, uint8_t* __restrict__ q,
+                                  float* __restrict__ row_scale) {
+    const int64_t r = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (r >= rows) return;
+    const __nv_bfloat16* xr = x + r * K;
+    float m = 0.f;
+    for (int i = lane * 8; i < K; i += 256) {
+        float v[8];
+        const uint4 a = *reinterpret_cast<const uint4*>(xr + i);
+        const uint32_t w[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            v[2 * j] = __uint_as_float(w[j] << 16);
+            v[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) m = fmaxf(m, fabsf(v[j]));
+    }
+    m = warp_max(m);
+    const float sc = m > 0.f ? m / 448.0f : 1.0f;
+    const float inv = 1.0f / sc;
+    for (int i = lane * 8; i < K; i += 256) {
+        const uint4 a = *reinterpret_cast<const uint4*>(xr + i);
+        const uint32_t w[4] = {a.x, a.y, a.z, a.w};
+        uint32_t o[2];
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const float f0 = __uint_as_float(w[2 * j] << 16), f1 = __uint_as_float(w[2 * j] & 0xFFFF0000u);
+            const float f2 = __uint_as_float(w[2 * j + 1] << 16), f3 = __uint_as_float(w[2 * j + 1] & 0xFFFF0000u);
+            o[j] = (uint32_t)f2e4m3x2(f0 * inv, f1 * inv) | ((uint32_t)f2e4m3x2(f2 * inv, f3 * inv) << 16);
+        }
+        *reinterpret_cast<uint2*>(q + r * K + i) = make_uint2(o[0], o[1]);
+    }
+    if (lane == 0) row_scale[r] = sc;
+}
+
+// amax of a tensor (non-negative floats order like their bit patterns).
+template <typename T>
+__global__ void amax_kernel(const T* __restrict__ x, int64_t n, unsigned* __restrict__ out_bits) {
+    float m = 0.f;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
+        m = fmaxf(m, fabsf((float)x[i]));
+    m = warp_max(m);
+    if ((threadIdx.x & 31) == 0) atomicMax(out_bits, __float_as_uint(m));
+}
+
+__global__ void scale_from_amax_kernel(const unsigned* __restrict__ amax_bits, float* __restrict__ scale) {
+    const float a = __uint_as_float(*amax_bits);
+    *scale = a > 0.f ? a / 448.0f : 1.0f;
+}
+
+template <typename T>
+__global__ void quant_tensor_kernel(const T* __restrict__ x, int64_t n, const float* __restrict__ scale,
+                                    uint8_t* __restrict__ q) {
+    const float inv = 1.0f / *scale;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
+        q[i] = (uint8_t)(f2e4m3x2((float)x[i] * inv, 0.f) & 0xFF);
+}
+
+__global__ void dequant_kernel(const uint8_t* __restrict__ q, const float* __restrict__ scale, int64_t n,
+                               float* __restrict__ out) {
+    const float s = *scale;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
+        out[i] = e4m3_to_f(q[i]) * s;
+}
+
+__global__ void fill_kernel(float* __restrict__ x, int64_t n, float v) {
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
+        x[i] = v;
+}
+
+// Greedy token: lowest index of the row maximum.  Row r belongs to chunk
+// r (one row per chunk); the token goes to column pos+1 when pos+1 < len[c].
+__global__ void __launch_bounds__(256)
+argmax_kernel(const float* __restrict__ logits, int64_t ld, int64_t rows, int V, int32_t* __restrict__ tokens,
+              const int32_t* __restrict__ len, const int* __restrict__ pos_dev, int pos_host) {
+    const int64_t r = blockIdx.x;
+    if (r >= rows) return;
+    const float* lr = logits + r * ld;
+    float best = -INFINITY;
+    int bi = 0x7FFFFFFF;
+    for (int i = threadIdx.x; i < V; i += 256) {
+        const float v = lr[i];
+        if (v > best) { best = v; bi = i; }
+    }
+    __shared__ float sv[256];
+    __shared__ int si[256];
+    sv[threadIdx.x] = best;
+    si[threadIdx.x] = bi;
+    __syncthreads();
+    for (int s = 128; s > 0; s >>= 1) {
+        if (threadIdx.x < s) {
+            const float a = sv[threadIdx.x], b = sv[threadIdx.x + s];
+            const int ia = si[threadIdx.x], ib = si[threadIdx.x + s];
+            if (b > a || (b == a && ib < ia)) { sv[threadIdx.x] = b; si[threadIdx.x] = ib; }
+        }
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) {
+        const int pos = pos_dev ? *pos_dev : pos_host;
+        if (pos + 1 < len[r] && pos + 1 < kMaxPos) tokens[r * kMaxPos + pos + 1] = si[0] == 0x7FFFFFFF ? 0 : si[0];
+    }
+}
+
+// conv weight [O][C][3] -> GEMM operand [O][3][C] (k index = j * C + c)
+template <typename T>
+__global__ void conv_reorder_kernel(const T* __restrict__ w, int O, int C, T* __restrict__ out) {
+    const int64_t n = (int64_t)O * C * 3;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t o = i / (3 * C);
+        const int rem = (int)(i % (3 * C));
+        const int j = rem / C, c = rem % C;
+        out[i] = w[(o * C + c) * 3 + j];
+    }
+}
+
+__global__ void gather_rows_kernel(const float* __restrict__ x, int64_t rows, int d, int64_t stride_rows,
+                                   int64_t first, float* __restrict__ out) {
+    const int64_t r = blockIdx.x;
+    if (r >= rows) return;
+    for (int i = threadIdx.x; i < d; i += blockDim.x) out[r * d + i] = x[(r * stride_rows + first) * d + i];
+}
+
+int grid_for(int64_t n, int threads) {
+    int64_t g = (n + threads - 1) / threads;
+    if (g > 148 * 16) g = 148 * 16;
+    return (int)(g < 1 ? 1 : g);
+}
+
+}  // namespace
+
+wb_status layernorm(const float* x, int64_t ld_x, int64_t rows, int d, const float* g, const float* b, LnOut mode,
+                    void* out, int64_t ld_o, float* row_scale, cudaStream_t s) {
+    if (rows <= 0) return WB_OK;
+    if (d % 32 || d > 32 * kMaxPerLane) return fail(WB_ERR_SHAPE, "LayerNorm width must be a multiple of 32, <= 1280");
+    const unsigned grid = (unsigned)((rows + 7) / 8);
+    if (mode == LN_F32) layernorm_kernel<LN_F32><<<grid, 256, 0, s>>>(x, ld_x, rows, d, g, b, out, ld_o, row_scale);
+    else if (mode == LN_BF16) layernorm_kernel<LN_BF16><<<grid, 256, 0, s>>>(x, ld_x, rows, d, g, b, out, ld_o, row_scale);
+    else layernorm_kernel<LN_E4M3><<<grid, 256, 0, s>>>(x, ld_x, rows, d, g, b, out, ld_o, row_scale);
+    WB_CUDA(cudaGetLastError());
+    return WB_OK;
+}
+
+wb_status embed(const int32_t* tokens, int64_t rows, int P, int p0, int d, const void* E, const void* Pos,
+                bool bf16, int vocab, float* x, unsigned* err, cudaStream_t s) {
+    if (rows <= 0) return WB_OK;
+    if (bf16)
+        embed_kernel<__nv_bfloat16><<<(unsigned)rows, 256, 0, s>>>(tokens, rows, P, p0, d,
+            reinterpret_cast<const __nv_bfloat16*>(E), reinterpret_cast<const __nv_bfloat16*>(Pos), vocab, x, err);
+    else
+        embed_kernel<float><<<(unsigned)rows, 256, 0, s>>>(tokens, rows, P, p0, d, reinterpret_cast<const float*>(E),
+                                                           reinterpret_cast<const float*>(Pos), vocab, x, err);
+    WB_CUDA(cudaGetLastError());
+    return WB_OK;
+}
+
+wb_status kv_scales(const float* qkv, int64_t n_chunks, int P, int d, float* k_scale, float* v_scale, cudaStream_t s) {
+    if (n_chunks <= 0) return WB_OK;
+    kv_scale_kernel<<<dim3((unsigned)n_chunks, 2), 256, 0, s>>>(qkv, P, d, k_scale, v_scale);
+    WB_CUDA(cudaGetLastError());
+    return WB_OK;
+}
+
+wb_status kv_append(const float* qkv, int64_t n_chunks, int P, int p0, int d, int H, int layer, bool fp8, void* cache,
+                    const int64_t* off, const int32_t* len, const float* k_scale, const float* v_scale, unsigned* err,
+                    cudaStream_t s) {
+    if (n_chunks <= 0) return WB_OK;
+    const unsigned grid = (unsigned)(n_chunks * P);
+    if (fp8) kv_append_kernel<true><<<grid, 256, 0, s>>>(qkv, n_chunks, P, p0, d, H, layer, cache, off, len, k_scale, v_scale, err);
+    else kv_append_kernel<false><<<grid, 256, 0, s>>>(qkv, n_chunks, P, p0, d, H, layer, cache, off, len, k_scale, v_scale, err);
+    WB_CUDA(cudaGetLastError());
+    return WB_OK;
+}
+
+wb_status quant_rows(const void* x_bf16, int64_t rows, int K, uint8_t* q, float* row_scale, cudaStream_t s) {
+    if (rows <= 0) return WB_OK;
+    if (K % 256) return fail(WB_ERR_SHAPE, "row quantiser needs K % 256 == 0");
+    quant_rows_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(reinterpret_cast<const __nv_bfloat16*>(x_bf16), rows, K,
+                                                                   q, row_scale);
+    WB_CUDA(cudaGetLastError());
+    return WB_OK;
+}
+
+wb_status quant_tensor(const void* x, bool bf16, int64_t n, uint8_t* q, float* scale, unsigned* scratch_bits,
+                       cudaStream_t s) {
+    WB_CUDA(cudaMemsetAsync(scratch_bits, 0, sizeof(unsigned), s));
+    if (n > 0) {
+        if (bf16) amax_kernel<__nv_bfloat16><<<grid_for(n, 256), 256, 0, s>>>(reinterpret_cast<const __nv_bfloat16*>(x), n, scratch_bits);
+        else amax_kernel<float><<<grid_for(n, 256), 256, 0, s>>>(reinterpret_cast<const float*>(x), n, scratch_bits);
+    }
+    scale_from_amax_kernel<<<1, 1, 0, s>>>(scratch_bits, scale);
+    if (n > 0) {
+        if (bf16) quant_tensor_kernel<__nv_bfloat16><<<grid_for(n, 256), 256, 0, s>>>(reinterpret_cast<const __nv_bfloat16*>(x), n, scale, q);
+        else quant_tensor_kernel<float><<<grid_for(n, 256), 256, 0, s>>>(reinterpret_cast<const float*>(x), n, scale, q);
+    }
+    WB_CUDA(cudaGetLastError());
+    return WB_OK;
+}
+
+wb_status dequant_tensor(const uint8_t* q, const float* scale, int64_t n, float* out, cudaStream_t s) {
+    if (n <= 0) return WB_OK;
+    dequant_kernel<<<grid_for(n, 256), 256, 0, s>>>(q, scale, n, out);
+    WB_CUDA(cudaGetLastError());
+    return WB_OK;
+}
+
+wb_status fill(float* x, int64_t n, float v, cudaStream_t s) {
+    if (n <= 0) return WB_OK;
+    fill_kernel<<<grid_for(n, 256), 256, 0, s>>>(x, n, v);
+    WB_CUDA(cudaGetLastError());
+    return WB_OK;
+}
+
+wb_status argmax_tokens(const float* logits, int64_t ld, int64_t rows, int V, int32_t* tokens, const int32_t* len,
+                        const int* pos_dev, int pos_host, cudaStream_t s) {
+    if (rows <= 0) return WB_OK;
+    argmax_kernel<<<(unsigned)rows, 256, 0, s>>>(logits, ld, rows, V, tokens, len, pos_dev, pos_host);
+    WB_CUDA(cudaGetLastError());
+    return WB_OK;
+}
+
+wb_status conv_reorder(const void* w, int O, int C, bool bf16, void* out, cudaStream_t s) {
+    const int64_t n = (int64_t)O * C * 3;
+    if (bf16) conv_reorder_kernel<__nv_bfloat16><<<grid_for(n, 256), 256, 0, s>>>(reinterpret_cast<const __nv_bfloat16*>(w), O, C, reinterpret_cast<__nv_bfloat16*>(out));
+    else conv_reorder_kernel<float><<<grid_for(n, 256), 256, 0, s>>>(reinterpret_cast<const float*>(w), O, C, reinterpret_cast<float*>(out));
+    WB_CUDA(cudaGetLastError());
+    return WB_OK;
+}
+
+wb_status gather_rows(const float* x, int64_t rows, int d, int64_t stride_rows, int64_t first, float* out,
+                      cudaStream_t s) {
+    if (rows <= 0) return WB_OK;
+    gather_rows_kernel<<<(unsigned)rows, 256, 0, s>>>(x, rows, d, stride_rows, first, out);
+    WB_CUDA(cudaGetLastError());
+    return WB_OK;
+}
+
+}  // namespace wb

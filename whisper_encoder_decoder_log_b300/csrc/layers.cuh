@@ -1,0 +1,31 @@
+// Launchers of the memory-bound kernels (layers.cu).
+#pragma once
+
+#include <stdint.h>
+
+#include "internal.h"
+
+namespace wb {
+
+enum LnOut : int { LN_F32 = 0, LN_BF16 = 1, LN_E4M3 = 2 };
+
+wb_status layernorm(const float* x, int64_t ld_x, int64_t rows, int d, const float* g, const float* b, LnOut mode,
+                    void* out, int64_t ld_o, float* row_scale, cudaStream_t s);
+wb_status embed(const int32_t* tokens, int64_t rows, int P, int p0, int d, const void* E, const void* Pos, bool bf16,
+                int vocab, float* x, unsigned* err, cudaStream_t s);
+wb_status kv_scales(const float* qkv, int64_t n_chunks, int P, int d, float* k_scale, float* v_scale, cudaStream_t s);
+wb_status kv_append(const float* qkv, int64_t n_chunks, int P, int p0, int d, int H, int layer, bool fp8, void* cache,
+                    const int64_t* off, const int32_t* len, const float* k_scale, const float* v_scale, unsigned* err,
+                    cudaStream_t s);
+wb_status quant_rows(const void* x_bf16, int64_t rows, int K, uint8_t* q, float* row_scale, cudaStream_t s);
+wb_status quant_tensor(const void* x, bool bf16, int64_t n, uint8_t* q, float* scale, unsigned* scratch_bits,
+                       cudaStream_t s);
+wb_status dequant_tensor(const uint8_t* q, const float* scale, int64_t n, float* out, cudaStream_t s);
+wb_status fill(float* x, int64_t n, float v, cudaStream_t s);
+wb_status argmax_tokens(const float* logits, int64_t ld, int64_t rows, int V, int32_t* tokens, const int32_t* len,
+                        const int* pos_dev, int pos_host, cudaStream_t s);
+wb_status conv_reorder(const void* w, int O, int C, bool bf16, void* out, cudaStream_t s);
+wb_status gather_rows(const float* x, int64_t rows, int d, int64_t stride_rows, int64_t first, float* out,
+                      cudaStream_t s);
+
+}  // namespace wb

@@ -1,0 +1,363 @@
+// Log-Mel front end: one fused kernel from float32 audio to the normalised
+// [B, n_mels, 3000] log-Mel array ("whisper-blaze 0.1.8", "GPU Mel
+// Spectrogram"; "Unlocking the power of OpenAI's Whisper", section 2).
+//
+// Work split.  A cluster of kCluster CTAs owns one 30 s chunk; CTA r computes
+// frames [375 r, 375 r + 375).  Frames are processed 32 at a time: the audio
+// segment they cover (5360 samples, reflect-padded at the chunk edges) is
+// staged in shared memory, two real frames are packed into one complex
+// 400-point FFT (z = x_a + i x_b), split as 400 = 16 x 25:
+//   stage 1: per (pair, n2) a 16-point DFT over n1 of z[25 n1 + n2], times
+//            the twiddle W400^(n2 k1);
+//   stage 2: per (pair, k1) a 25-point DFT (as 5 x 5) over n2, in place, so
+//            slot k1 + 16 k2 ends up holding Z[k1 + 16 k2];
+// then X_a, X_b are separated from Z[k] and Z[400-k], the power of bins 0..200
+// goes through the sparse mel filterbank (each bin feeds at most two
+// filters), and log10 is taken.  The unfloored value (l + 4) / 4 is written
+// to HBM right away and the CTA's maximum is kept; the cluster then reduces
+// the chunk maximum through distributed shared memory, and each CTA re-reads
+// its own freshly written tile (resident in L2) to apply the max - 8 floor,
+// writing back only the values that change.
+#include <cooperative_groups.h>
+
+#include <cmath>
+#include <mutex>
+#include <vector>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace cg = cooperative_groups;
+
+namespace wb {
+namespace {
+
+constexpr int kCluster = 8;
+constexpr int kFramesPerCta = kFrames / kCluster;      // 375
+constexpr int kSub = 32;                               // frames per sub-block
+constexpr int kPairs = kSub / 2;
+constexpr int kSeg = kSub * kHop + (kNFFT - kHop);     // 5360 samples
+constexpr int kZStride = 425;                          // 400 slots + 25 pads
+constexpr int kPStride = kBins;                        // odd stride: no bank conflicts
+constexpr int kThreads = 256;
+constexpr int kMaxMels = 128;
+constexpr int kMaxFbNnz = 512;
+
+struct MelTables {
+    float2 tw[kNFFT];          // W400^j = exp(-2 pi i j / 400)
+    float win[kNFFT];          // periodic Hann
+    int kstart[kMaxMels];
+    int kcount[kMaxMels];
+    int woff[kMaxMels];
+    float w[kMaxFbNnz];
+};
+
+struct MelSmem {
+    MelTables t;
+    float seg[kSeg];
+    float2 z[kPairs * kZStride];
+    float p[kSub * kPStride];
+    float red[kThreads / 32];
+    float cmax;
+};
+
+__device__ __forceinline__ float2 cmul(float2 a, float2 b) {
+    return make_float2(a.x * b.x - a.y * b.y, a.x * b.y + a.y * b.x);
+}
+__device__ __forceinline__ float2 cadd(float2 a, float2 b) { return make_float2(a.x + b.x, a.y + b.y); }
+__device__ __forceinline__ float2 csub(float2 a, float2 b) { return make_float2(a.x - b.x, a.y - b.y); }
+// -i * a
+__device__ __forceinline__ float2 cmi(float2 a) { return make_float2(a.y, -a.x); }
+
+// 4-point DFT with W4 = -i, in place.
+__device__ __forceinline__ void dft4(float2& x0, float2& x1, float2& x2, float2& x3) {
+    float2 a = cadd(x0, x2), b = csub(x0, x2), c = cadd(x1, x3), d = cmi(csub(x1, x3));
+    x0 = cadd(a, c);
+    x2 = csub(a, c);
+    x1 = cadd(b, d);
+    x3 = csub(b, d);
+}
+
+// 5-point DFT with W5 = exp(-2 pi i / 5), in place.
+__device__ __forceinline__ void dft5(float2& x0, float2& x1, float2& x2, float2& x3, float2& x4) {
+    const float c1 = 0.30901699437494742f, c2 = -0.80901699437494742f;
+    const float s1 = 0.95105651629515357f, s2 = 0.58778525229247313f;
+    float2 t1 = cadd(x1, x4), t2 = cadd(x2, x3), t3 = csub(x1, x4), t4 = csub(x2, x3);
+    float2 a1 = make_float2(x0.x + c1 * t1.x + c2 * t2.x, x0.y + c1 * t1.y + c2 * t2.y);
+    float2 a2 = make_float2(x0.x + c2 * t1.x + c1 * t2.x, x0.y + c2 * t1.y + c1 * t2.y);
+    float2 b1 = make_float2(s1 * t3.x + s2 * t4.x, s1 * t3.y + s2 * t4.y);
+    float2 b2 = make_float2(s2 * t3.x - s1 * t4.x, s2 * t3.y - s1 * t4.y);
+    x0 = cadd(x0, cadd(t1, t2));
+    float2 ib1 = cmi(b1), ib2 = cmi(b2);                // -i b
+    x1 = cadd(a1, ib1);
+    x4 = csub(a1, ib1);
+    x2 = cadd(a2, ib2);
+    x3 = csub(a2, ib2);
+}
+
+__global__ void __launch_bounds__(kThreads, 2)
+mel_kernel(const float* __restrict__ audio, const MelTables* __restrict__ tables, int n_mels,
+           float* __restrict__ out) {
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    MelSmem& S = *reinterpret_cast<MelSmem*>(smem_raw);
+    cg::cluster_group cluster = cg::this_cluster();
+    const int tid = threadIdx.x;
+    const int rank = blockIdx.x % kCluster;
+    const int64_t chunk = blockIdx.x / kCluster;
+    const float* x = audio + chunk * (int64_t)kChunkSamples;
+    float* o = out + chunk * (int64_t)n_mels * kFrames;
+
+    {   // tables -> shared memory
+        const int4* src = reinterpret_cast<const int4*>(tables);
+        int4* dst = reinterpret_cast<int4*>(&S.t);
+        for (int i = tid; i < (int)(sizeof(MelTables) / 16); i += kThreads) dst[i] = src[i];
+    }
+
+    const int fbeg = rank * kFramesPerCta;
+    float tmax = -1e30f;
+
+    for (int f0 = fbeg; f0 < fbeg + kFramesPerCta; f0 += kSub) {
+        const int nf = min(kSub, fbeg + kFramesPerCta - f0);
+        __syncthreads();   // previous sub-block fully consumed (and tables ready)
+        // ---- audio segment: padded index 160 f0 + i maps to sample 160 f0 + i - 200
+        for (int i = tid; i < kSeg; i += kThreads) {
+            int q = kHop * f0 + i - kNFFT / 2;
+            if (q < 0) q = -q;
+            if (q >= kChunkSamples) q = 2 * (kChunkSamples - 1) - q;
+            q = max(0, min(q, kChunkSamples - 1));
+            S.seg[i] = __ldg(x + q);
+        }
+        __syncthreads();
+        // ---- stage 1: 16-point DFTs over n1, twiddle W400^(n2 k1)
+        for (int it = tid; it < kPairs * 25; it += kThreads) {
+            const int pr = it / 25, n2 = it % 25;
+            const float* fa = S.seg + kHop * (2 * pr);
+            const float* fb = fa + kHop;
+            float2 v[16];
+#pragma unroll
+            for (int n1 = 0; n1 < 16; ++n1) {
+                const int n = 25 * n1 + n2;
+                const float w = S.t.win[n];
+                v[n1] = make_float2(fa[n] * w, fb[n] * w);
+            }
+            // 16 = 4 x 4: n1 = 4 a + b, k1 = c + 4 d
+#pragma unroll
+            for (int b = 0; b < 4; ++b) dft4(v[b], v[4 + b], v[8 + b], v[12 + b]);   // over a -> c
+#pragma unroll
+            for (int b = 1; b < 4; ++b)
+#pragma unroll
+                for (int c = 1; c < 4; ++c) v[4 * c + b] = cmul(v[4 * c + b], S.t.tw[25 * b * c]);
+#pragma unroll
+            for (int c = 0; c < 4; ++c) dft4(v[4 * c + 0], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+            // v[4 c + d] now holds Y[k1 = c + 4 d]
+            float2* zp = S.z + pr * kZStride + n2 * 17;
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+#pragma unroll
+                for (int d = 0; d < 4; ++d) {
+                    const int k1 = c + 4 * d;
+                    zp[k1] = (n2 * k1 == 0) ? v[4 * c + d] : cmul(v[4 * c + d], S.t.tw[n2 * k1]);
+                }
+        }
+        __syncthreads();
+        // ---- stage 2: 25-point DFTs over n2 (5 x 5), in place
+        for (int it = tid; it < kPairs * 16; it += kThreads) {
+            const int pr = it / 16, k1 = it % 16;
+            float2* zp = S.z + pr * kZStride + k1;
+            float2 v[25];
+#pragma unroll
+            for (int n2 = 0; n2 < 25; ++n2) v[n2] = zp[17 * n2];
+            // n2 = 5 a + b; k2 = c + 5 d
+#pragma unroll
+            for (int b = 0; b < 5; ++b) dft5(v[b], v[5 + b], v[10 + b], v[15 + b], v[20 + b]);
+#pragma unroll
+            for (int b = 1; b < 5; ++b)
+#pragma unroll
+                for (int c = 1; c < 5; ++c) v[5 * c + b] = cmul(v[5 * c + b], S.t.tw[16 * b * c]);
+#pragma unroll
+            for (int c = 0; c < 5; ++c)
+                dft5(v[5 * c + 0], v[5 * c + 1], v[5 * c + 2], v[5 * c + 3], v[5 * c + 4]);
+            // v[5 c + d] holds Z[k1 + 16 (c + 5 d)]
+#pragma unroll
+            for (int c = 0; c < 5; ++c)
+#pragma unroll
+                for (int d = 0; d < 5; ++d) zp[17 * (c + 5 * d)] = v[5 * c + d];
+        }
+        __syncthreads();
+        // ---- separate the two real frames, power spectrum
+        for (int it = tid; it < kPairs * kBins; it += kThreads) {
+            const int pr = it / kBins, k = it % kBins;
+            const int kk = (kNFFT - k) % kNFFT;
+            const float2 zk = S.z[pr * kZStride + k + k / 16];
+            const float2 zn = S.z[pr * kZStride + kk + kk / 16];
+            const float ar = zk.x + zn.x, ai = zk.y - zn.y;     // 2 X_a
+            const float br = zk.y + zn.y, bi = zn.x - zk.x;     // 2 X_b
+            S.p[(2 * pr) * kPStride + k] = 0.25f * (ar * ar + ai * ai);
+            S.p[(2 * pr + 1) * kPStride + k] = 0.25f * (br * br + bi * bi);
+        }
+        __syncthreads();
+        // ---- mel filterbank, log10, unfloored output
+        for (int it = tid; it < n_mels * kSub; it += kThreads) {
+            const int m = it / kSub, f = it % kSub;
+            if (f >= nf) continue;
+            const float* pf = S.p + f * kPStride;
+            const int k0 = S.t.kstart[m], kc = S.t.kcount[m], wo = S.t.woff[m];
+            float e = 0.f;
+            for (int j = 0; j < kc; ++j) e = fmaf(S.t.w[wo + j], pf[k0 + j], e);
+            const float ell = __log2f(fmaxf(e, 1e-10f)) * 0.30102999566398120f;
+            tmax = fmaxf(tmax, ell);
+            o[(int64_t)m * kFrames + f0 + f] = (ell + 4.0f) * 0.25f;
+        }
+    }
+    // ---- chunk maximum across the cluster
+    tmax = warp_max(tmax);
+    if ((tid & 31) == 0) S.red[tid >> 5] = tmax;
+    __syncthreads();
+    if (tid == 0) {
+        float m = S.red[0];
+        for (int i = 1; i < kThreads / 32; ++i) m = fmaxf(m, S.red[i]);
+        S.cmax = m;
+    }
+    cluster.sync();   // releases this CTA's global writes and its cmax
+    float cm = -1e30f;
+#pragma unroll
+    for (int r = 0; r < kCluster; ++r) cm = fmaxf(cm, *cluster.map_shared_rank(&S.cmax, r));
+    const float floor_v = (cm - 8.0f + 4.0f) * 0.25f;
+    for (int it = tid; it < n_mels * kFramesPerCta; it += kThreads) {
+        const int m = it / kFramesPerCta, f = it % kFramesPerCta;
+        float* p = o + (int64_t)m * kFrames + fbeg + f;
+        const float v = *p;
+        if (v < floor_v) *p = floor_v;
+    }
+    cluster.sync();   // no CTA leaves while another may still read its cmax
+}
+
+// ------------------------------------------------------------------ host tables
+double hz_to_mel_slaney(double f) {
+    const double f_sp = 200.0 / 3.0, min_log_hz = 1000.0, min_log_mel = min_log_hz / f_sp;
+    const double logstep = std::log(6.4) / 27.0;
+    return f >= min_log_hz ? min_log_mel + std::log(f / min_log_hz) / logstep : f / f_sp;
+}
+double mel_to_hz_slaney(double m) {
+    const double f_sp = 200.0 / 3.0, min_log_hz = 1000.0, min_log_mel = min_log_hz / f_sp;
+    const double logstep = std::log(6.4) / 27.0;
+    return m >= min_log_mel ? min_log_hz * std::exp(logstep * (m - min_log_mel)) : f_sp * m;
+}
+
+bool build_tables(int n_mels, MelTables* t) {
+    const double pi = 3.14159265358979323846;
+    for (int j = 0; j < kNFFT; ++j) {
+        t->tw[j] = make_float2((float)std::cos(2 * pi * j / kNFFT), (float)-std::sin(2 * pi * j / kNFFT));
+        t->win[j] = (float)(0.5 - 0.5 * std::cos(2 * pi * j / kNFFT));
+    }
+    const double mlo = hz_to_mel_slaney(0.0), mhi = hz_to_mel_slaney(8000.0);
+    std::vector<double> pts(n_mels + 2);
+    for (int i = 0; i < n_mels + 2; ++i)
+        pts[i] = mel_to_hz_slaney(mlo + (mhi - mlo) * i / (n_mels + 1));
+    int nnz = 0;
+    for (int m = 0; m < n_mels; ++m) {
+        const double lo = pts[m], c = pts[m + 1], hi = pts[m + 2];
+        int first = -1, last = -1;
+        std::vector<float> ws;
+        for (int k = 0; k < kBins; ++k) {
+            const double f = 40.0 * k;
+            const double wv = std::fmax(0.0, std::fmin((f - lo) / (c - lo), (hi - f) / (hi - c))) *
+                              (2.0 / (hi - lo));
+            if (wv > 0) {
+                if (first < 0) first = k;
+                last = k;
+            }
+        }
+        if (first < 0) first = last = 0;
+        t->kstart[m] = first;
+        t->kcount[m] = last - first + 1;
+        t->woff[m] = nnz;
+        for (int k = first; k <= last; ++k) {
+            const double f = 40.0 * k;
+            const double wv = std::fmax(0.0, std::fmin((f - lo) / (c - lo), (hi - f) / (hi - c))) *
+                              (2.0 / (hi - lo));
+            if (nnz >= kMaxFbNnz) return false;
+            t->w[nnz++] = (float)wv;
+        }
+    }
+    return true;
+}
+
+struct DeviceTables {
+    MelTables* d80 = nullptr;
+    MelTables* d128 = nullptr;
+};
+std::mutex g_tab_mu;
+DeviceTables g_tabs[64];
+
+__global__ void transpose_pad_kernel(const float* __restrict__ mel, int C, void* __restrict__ out,
+                                     bool bf16) {
+    // grid: (ceil(3002 / 32), B); block 32 x 8.  Row r of the output is frame r - 1.
+    __shared__ float tile[32][129];
+    const int64_t b = blockIdx.y;
+    const int r0 = blockIdx.x * 32;
+    const float* src = mel + b * (int64_t)C * kFrames;
+    for (int c = threadIdx.y; c < C; c += 8) {
+        const int r = r0 + threadIdx.x;
+        const int f = r - 1;
+        tile[threadIdx.x][c] = (f >= 0 && f < kFrames) ? src[(int64_t)c * kFrames + f] : 0.f;
+    }
+    __syncthreads();
+    for (int rr = threadIdx.y; rr < 32; rr += 8) {
+        const int r = r0 + rr;
+        if (r >= kFrames + 2) break;
+        for (int c = threadIdx.x; c < C; c += 32) {
+            const int64_t idx = (b * (kFrames + 2) + r) * (int64_t)C + c;
+            if (bf16) reinterpret_cast<__nv_bfloat16*>(out)[idx] = __float2bfloat16_rn(tile[rr][c]);
+            else reinterpret_cast<float*>(out)[idx] = tile[rr][c];
+        }
+    }
+}
+
+}  // namespace
+
+wb_status mel_launch(const float* audio, int64_t B, int n_mels, float* mel, cudaStream_t s) {
+    int dev = 0;
+    WB_CUDA(cudaGetDevice(&dev));
+    if (dev < 0 || dev >= 64) return fail(WB_ERR_UNSUPPORTED, "device index out of range");
+    MelTables* tab = nullptr;
+    {
+        std::lock_guard<std::mutex> lk(g_tab_mu);
+        MelTables*& slot = n_mels == 80 ? g_tabs[dev].d80 : g_tabs[dev].d128;
+        if (!slot) {
+            MelTables h;
+            memset(&h, 0, sizeof(h));
+            if (!build_tables(n_mels, &h)) return fail(WB_ERR_SHAPE, "mel filterbank too large");
+            WB_CUDA(cudaMalloc(&slot, sizeof(MelTables)));
+            WB_CUDA(cudaMemcpy(slot, &h, sizeof(MelTables), cudaMemcpyHostToDevice));
+            WB_CUDA(cudaFuncSetAttribute(mel_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)sizeof(MelSmem)));
+        }
+        tab = slot;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(B * kCluster), 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = sizeof(MelSmem);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = kCluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    WB_CUDA(cudaLaunchKernelEx(&cfg, mel_kernel, audio, (const MelTables*)tab, n_mels, mel));
+    return WB_OK;
+}
+
+wb_status mel_transpose_pad(const float* mel, int64_t B, int C, void* out, bool bf16,
+                            cudaStream_t s) {
+    if (C > 128) return fail(WB_ERR_SHAPE, "n_mels > 128");
+    dim3 grid((kFrames + 2 + 31) / 32, (unsigned)B);
+    transpose_pad_kernel<<<grid, dim3(32, 8), 0, s>>>(mel, C, out, bf16);
+    WB_CUDA(cudaGetLastError());
+    return WB_OK;
+}
+
+}  // namespace wb
