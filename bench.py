@@ -1,0 +1,478 @@
+"""Benchmark of the Whisper transcription hot path on B300 GPUs.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config c4] [--impl ours|reference]
+
+One step is one pass of the whole hot path over one batch of seeded synthetic
+audio, through the library's public C ABI.  Workloads (random-init weights of
+the named shapes; synthetic audio standing in for the long-form recordings the
+pages measure on):
+
+  c1  tiny fp32: 1 chunk, mel + encoder + 32 teacher-forced decoder tokens
+  c2  mel front end: 64 chunks of 30 s, 128 mels
+  c3  large-v3 encoder, bf16: 16 chunks (mel + encoder)
+  c4  large-v3-turbo transcription (default): one 16-min recording = 32 chunks,
+      mel, encoder, cross-K/V, 4-token forced prefix + 224 greedy tokens with
+      the E4M3 self-attention cache
+  c5  large-v3 mixed serving batch: 48 requests of 2-15 min, FP8 QKV/FFN GEMMs,
+      E4M3 cache, 32-layer decoder, decode lengths 64-448, waves within 180 GB
+
+The metric is RTFx = audio seconds processed / wall seconds.  `value` is the
+device-resident throughput (audio already in HBM); `e2e` repeats the same work
+through the same C-ABI call with the audio copied from pinned host memory and
+the tokens copied back inside each timed step.  Multi-GPU runs are replicas
+(every rank transcribes its own batch; no collective on the data path) and
+report weak scaling.  `--impl reference` times the CPU oracle instead, on a
+bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+from synth import LARGE_V3, TINY, TURBO  # noqa: E402
+
+AUDIO_S_PER_CHUNK = 30.0
+L2_BYTES = 126 * 2 ** 20
+
+
+# ----------------------------------------------------------------- workloads
+
+class Workload:
+    name = ""
+    dims = None
+    precision = None
+    kv_fp8 = False
+    audio_s = 0.0
+    bound_kernel = None   # dominant kernel kind for the roofline object
+
+    def describe(self) -> dict:
+        return {"workload": self.name}
+
+
+def make_workload(cfg: str, seed: int):
+    import whisper_encoder_decoder_log_b300 as wb
+    if cfg == "c1":
+        w = Workload()
+        w.name = "tiny-fp32 1x30s chunk, mel+encoder+32 teacher-forced tokens"
+        w.dims, w.precision, w.kv_fp8 = TINY, wb.PREC_FP32, False
+        w.audio = synth.batch_audio("sine", 1, seed)
+        w.tokens = synth.random_tokens(seed, (1, 32), TINY.vocab)
+        w.audio_s = 30.0
+        w.kind = "teacher"
+        w.bound_kernel = wb.KERNEL_ENC_ATTN
+    elif cfg == "c2":
+        w = Workload()
+        w.name = "mel 64x30s chunks, 128 mels"
+        w.dims, w.precision, w.kv_fp8 = LARGE_V3, None, False
+        w.audio = synth.batch_audio("pink", 64, seed)
+        w.audio_s = 64 * 30.0
+        w.kind = "mel"
+        w.bound_kernel = wb.KERNEL_MEL
+    elif cfg == "c3":
+        w = Workload()
+        w.name = "large-v3 encoder bf16, 16x30s chunks"
+        w.dims = synth.ModelDims("large-v3-enc", 128, 1280, 20, 5120, 32, 0, 51866)
+        w.precision, w.kv_fp8 = wb.PREC_BF16, False
+        w.audio = synth.batch_audio("sine", 16, seed)
+        w.audio_s = 16 * 30.0
+        w.kind = "encode"
+        w.bound_kernel = wb.KERNEL_GEMM
+    elif cfg == "c4":
+        w = Workload()
+        w.name = "large-v3-turbo transcription, 16-min recording = 32x30s chunks, prefix 4 + 224 greedy tokens"
+        w.dims, w.precision, w.kv_fp8 = TURBO, wb.PREC_BF16, True
+        n = 32
+        w.audio_flat = synth.batch_audio("sine", n, seed).reshape(-1)
+        w.req_offsets = np.array([0], np.int64)
+        w.req_samples = np.array([w.audio_flat.size], np.int64)
+        w.chunk_len = np.full(n, 228, np.int32)
+        w.audio_s = w.audio_flat.size / 16000.0
+        w.kind = "batch"
+        w.budget = 180 * 10 ** 9
+        w.bound_kernel = wb.KERNEL_GEMM
+    elif cfg == "c5":
+        w = Workload()
+        w.name = "large-v3 mixed serving: 48 requests 2-15 min, mixed_fp8, E4M3 KV, lengths 64-448, waves <= 180 GB"
+        w.dims, w.precision, w.kv_fp8 = LARGE_V3, wb.PREC_MIXED_FP8, True
+        sb = synth.serving_requests(seed, n_req=48)
+        w.audio_flat = sb.audio
+        w.req_offsets = sb.req_offsets
+        w.req_samples = sb.req_samples
+        w.chunk_len = sb.chunk_len
+        w.audio_s = float(sb.req_samples.sum()) / 16000.0
+        w.kind = "batch"
+        w.budget = 180 * 10 ** 9
+        w.bound_kernel = wb.KERNEL_CROSS_ATTN
+    else:
+        raise SystemExit(f"unknown config {cfg}")
+    w.cfg = cfg
+    return w
+
+
+# ----------------------------------------------------------------- GPU runner
+
+class GpuRunner:
+    def __init__(self, w: Workload, seed: int):
+        import torch
+        import whisper_encoder_decoder_log_b300 as wb
+        self.torch, self.wb, self.w = torch, wb, w
+        self.stream = torch.cuda.current_stream()
+        self.model = None
+        if w.precision is not None:
+            desc = wb.make_desc(w.dims, w.precision, w.kv_fp8)
+            W = synth.make_weights(w.dims, seed, bf16=w.precision != wb.PREC_FP32)
+            self.wbuf = wb.pack_weights(desc, W)
+            del W
+            torch.cuda.synchronize()
+            self.model = wb.wb_model_create(desc, self.wbuf)
+        dev = "cuda"
+        if w.kind == "batch":
+            self.audio_host = torch.from_numpy(w.audio_flat).pin_memory()
+            self.audio = self.audio_host.to(dev)
+            n_chunks = w.chunk_len.size
+            self.tokens = torch.zeros(n_chunks, 448, dtype=torch.int32, device=dev)
+            self.tokens_host = torch.empty(n_chunks, 448, dtype=torch.int32).pin_memory()
+            self.prefix = synth.forced_prefix(seed, w.dims.vocab)
+            nbytes = wb.wb_transcribe_workspace_size(self.model, w.req_samples, w.chunk_len, w.budget)
+            self.ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+            self.h2d = int(w.audio_flat.nbytes)
+            self.d2h = int(self.tokens.numel() * 4)
+        else:
+            self.audio_host = torch.from_numpy(np.ascontiguousarray(w.audio)).pin_memory()
+            self.audio = self.audio_host.to(dev)
+            B = w.audio.shape[0]
+            self.mel = torch.empty(B, w.dims.n_mels, 3000, device=dev)
+            self.h2d = int(w.audio.nbytes)
+            if w.kind in ("encode", "teacher"):
+                act = torch.float32 if w.precision == wb.PREC_FP32 else torch.bfloat16
+                self.enc = torch.empty(B, 1500, w.dims.d_model, dtype=act, device=dev)
+                self.enc_host = torch.empty(self.enc.shape, dtype=act).pin_memory()
+                self.ews = torch.empty(wb.wb_encode_workspace_size(self.model, B), dtype=torch.uint8, device=dev)
+            if w.kind == "teacher":
+                P = w.tokens.shape[1]
+                self.chunk_len = np.full(B, P + 1, np.int32)
+                self.tok = torch.zeros(B, 448, dtype=torch.int32, device=dev)
+                self.tok[:, :P] = torch.from_numpy(w.tokens).to(dev)
+                self.logits = torch.empty(B, P, w.dims.vocab, device=dev)
+                self.logits_host = torch.empty(self.logits.shape).pin_memory()
+                self.dws = torch.empty(wb.wb_decoder_workspace_size(self.model, self.chunk_len), dtype=torch.uint8,
+                                       device=dev)
+                self.d2h = int(self.logits.numel() * 4)
+            elif w.kind == "encode":
+                self.d2h = int(self.enc.numel() * self.enc.element_size())
+            else:
+                self.mel_host = torch.empty(self.mel.shape).pin_memory()
+                self.d2h = int(self.mel.numel() * 4)
+        self.flush_buf = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def flush_l2(self):
+        self.flush_buf.fill_(1.0)
+
+    def step(self, host_io: bool = False):
+        wb, w = self.wb, self.w
+        if w.kind == "batch":
+            if host_io:
+                self.audio.copy_(self.audio_host, non_blocking=True)
+            wb.wb_transcribe_batch(self.model, self.audio, w.req_offsets, w.req_samples, self.prefix, w.chunk_len,
+                                   self.tokens, w.budget, self.ws)
+            if host_io:
+                self.tokens_host.copy_(self.tokens, non_blocking=True)
+            return
+        if host_io:
+            self.audio.copy_(self.audio_host, non_blocking=True)
+        wb.wb_mel(self.audio, w.dims.n_mels, self.mel)
+        if w.kind == "mel":
+            if host_io:
+                self.mel_host.copy_(self.mel, non_blocking=True)
+            return
+        wb.wb_encode(self.model, self.mel, self.enc, self.ews)
+        if w.kind == "encode":
+            if host_io:
+                self.enc_host.copy_(self.enc, non_blocking=True)
+            return
+        dec = wb.wb_decoder_init(self.model, self.chunk_len, self.enc, self.tok, self.dws)
+        wb.wb_decode_prefix(dec, w.tokens.shape[1], self.logits)
+        wb.wb_decoder_destroy(dec)
+        if host_io:
+            self.logits_host.copy_(self.logits, non_blocking=True)
+
+    def sync_check(self):
+        self.torch.cuda.synchronize()
+        self.wb.wb_sync_status(self.model)
+
+
+# ----------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------- CPU oracle sample
+
+def cpu_sample(w: Workload, seed: int):
+    """Time the oracle on a bounded sample of the workload; return
+    (RTFx estimate, seconds spent, description, threads)."""
+    from oracle import mel as omel
+    from oracle import model as omodel
+    try:
+        from threadpoolctl import threadpool_info
+        threads = max([t.get("num_threads", 1) for t in threadpool_info()] + [1])
+    except Exception:
+        threads = os.cpu_count() or 1
+    t0 = time.perf_counter()
+    if w.cfg == "c2":
+        omel.log_mel(w.audio[0].astype(np.float64), 128)
+        dt = time.perf_counter() - t0
+        return 30.0 / dt, dt, "oracle log-Mel of 1 of the 64 chunks, RTFx = 30 s / its time", threads
+    dims = w.dims
+    audio = w.audio[0] if hasattr(w, "audio") else w.audio_flat[:480000]
+    mel = omel.log_mel(audio.astype(np.float64), dims.n_mels)
+    t_mel = time.perf_counter() - t0
+    n_enc = min(2, dims.enc_layers)
+    fp8 = w.cfg == "c5"
+    W = synth.make_weights(dims, seed, bf16=w.precision != 0, enc_layers=range(n_enc),
+                           dec_layers=range(dims.dec_layers))
+    t1 = time.perf_counter()
+    h = omodel.conv_stem(mel, W)
+    for l in range(n_enc):
+        h = omodel.encoder_layer(h, W, l, dims.n_heads, fp8)
+    t_enc = time.perf_counter() - t1
+    est = t_mel + t_enc * (dims.enc_layers / max(1, n_enc))   # stem counted in the scale-up: an over-estimate
+    desc = f"oracle: log-Mel of 1 chunk, conv stem + {n_enc} of {dims.enc_layers} encoder layers (scaled)"
+    if dims.dec_layers and w.kind != "encode":
+        T = 16
+        toks = synth.random_tokens(seed, T, dims.vocab)
+        t2 = time.perf_counter()
+        omodel.decode_teacher_forced(toks, h, W, dims, kv_fp8=w.kv_fp8, fp8=fp8)
+        t_dec = time.perf_counter() - t2
+        L = 32 if w.cfg == "c1" else (228 if w.cfg == "c4" else int(np.mean(w.chunk_len)))
+        est += t_dec * (L / T)
+        desc += f", decoder over {T} teacher-forced positions (scaled to {L})"
+    spent = time.perf_counter() - t0
+    return 30.0 / est, spent, desc + "; RTFx = 30 s / estimated time for one 30 s chunk", threads
+
+
+# ----------------------------------------------------------------- main
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--config", default="c4", choices=["c1", "c2", "c3", "c4", "c5"])
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    metric, unit = "RTFx", "audio_s/wall_s"
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        w = make_workload(args.config, args.seed)
+        vals, spent = [], 0.0
+        desc, threads = "", 1
+        for i in range(args.warmup + args.steps):
+            v, s, desc, threads = cpu_sample(w, args.seed)
+            if i >= args.warmup:
+                vals.append(v)
+                spent += s
+        value = float(np.mean(vals))
+        line = {"impl": "reference", "metric": metric, "value": value, "unit": unit, "n_gpus": args.gpus,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * spent / max(1, args.steps),
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                "data": "synthetic", "config": w.describe(),
+                "cpu_baseline": {"value": value, "unit": unit, "cores": threads, "kind": "oracle", "sample": desc},
+                "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+
+    import torch
+    import whisper_encoder_decoder_log_b300 as wb
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local_rank)
+    w = make_workload(args.config, args.seed + rank)
+    run = GpuRunner(w, args.seed)
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+
+    for _ in range(max(3, args.warmup)):
+        run.step()
+    run.sync_check()
+
+    # which kernel kind dominates: one profiled step per kind
+    kinds = [wb.KERNEL_GEMM, wb.KERNEL_GEMM_SMALL, wb.KERNEL_ENC_ATTN, wb.KERNEL_CROSS_ATTN,
+             wb.KERNEL_SELF_ATTN, wb.KERNEL_MEL]
+    shares = {}
+    for k in kinds:
+        wb.wb_prof_start(k, 1 << 17)
+        run.step()
+        torch.cuda.synchronize()
+        n, ms, units = wb.wb_prof_stop()
+        if n:
+            shares[k] = ms
+    dom = max(shares, key=shares.get) if shares else w.bound_kernel
+
+    # ---- timed region: device-resident inputs
+    clocks = ClockSampler(local_rank)
+    barrier()
+    clocks.start()
+    launches0 = wb.wb_launch_count()
+    wb.wb_prof_start(dom, 1 << 17)
+    times = []
+    for i in range(args.steps):
+        run.flush_l2()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        run.step()
+        e1.record()
+        times.append((e0, e1))
+    torch.cuda.synchronize()
+    n_dom, ms_dom, units_dom = wb.wb_prof_stop()
+    launches = (wb.wb_launch_count() - launches0) // max(1, args.steps)
+    barrier()
+    clk = clocks.stop()
+    run.sync_check()
+    step_ms = [a.elapsed_time(b) for a, b in times]
+    local_ms = float(np.mean(step_ms))
+    if world > 1:
+        t = torch.tensor([local_ms], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        max_ms = float(t.item())
+    else:
+        max_ms = local_ms
+    value = w.audio_s * world / (max_ms / 1000.0)
+
+    # ---- end to end through the same C-ABI call with host buffers
+    barrier()
+    e2e_times = []
+    for i in range(args.steps):
+        run.flush_l2()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        run.step(host_io=True)
+        e1.record()
+        e2e_times.append((e0, e1))
+    torch.cuda.synchronize()
+    e2e_ms = float(np.mean([a.elapsed_time(b) for a, b in e2e_times]))
+    if world > 1:
+        t = torch.tensor([e2e_ms], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e = {"value": w.audio_s * world / (e2e_ms / 1000.0), "unit": unit, "h2d_bytes_per_step": run.h2d,
+           "d2h_bytes_per_step": run.d2h}
+
+    # ---- roofline of the dominant kernel
+    peaks = {}
+    try:
+        peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+        src = "measured"
+    except Exception:
+        src = "fallback"
+    tensor_kinds = (wb.KERNEL_GEMM, wb.KERNEL_ENC_ATTN)
+    if dom in tensor_kinds:
+        achieved = units_dom / (ms_dom / 1000.0) / 1e12 if ms_dom > 0 else 0.0
+        fp8_path = w.precision == wb.PREC_MIXED_FP8 and dom == wb.KERNEL_GEMM
+        peak = float(peaks.get("bf16_tflops_sustained", 1400.0))
+        if fp8_path:
+            peak *= 2.0   # mixed bf16/E4M3 GEMMs: E4M3 nominal rate is 2x bf16
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s"}
+    else:
+        achieved = units_dom / (ms_dom / 1000.0) / 1e9 if ms_dom > 0 else 0.0
+        peak = float(peaks.get("hbm_gbs", 6400.0))
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"] if roof["peak"] else None
+    roof["traffic"] = None
+    roof["kernel"] = wb.KERNEL_NAMES.get(dom, str(dom))
+    roof["launches_per_step"] = n_dom / max(1, args.steps)
+    roof["ms_per_step"] = ms_dom / max(1, args.steps)
+    roof["peak_source"] = src + (" bf16 sustained" if roof["bound"] == "tensor" else " copy bandwidth")
+    roof["kernel_ms_per_step"] = {wb.KERNEL_NAMES[k]: v for k, v in shares.items()}
+
+    if rank != 0:
+        return
+    cpu = None
+    if not args.no_cpu_baseline:
+        v, spent, desc, threads = cpu_sample(w, args.seed)
+        cpu = {"value": v, "unit": unit, "cores": threads, "kind": "oracle", "sample": desc}
+    dtype = {wb.PREC_FP32: "f32", wb.PREC_BF16: "bf16", wb.PREC_MIXED_FP8: "bf16+e4m3"}.get(w.precision, "f32")
+    cfg = w.describe()
+    cfg.update({"config": args.config, "audio_s_per_gpu": w.audio_s, "l2": "flushed between timed steps",
+                "parallelism": f"replicas x{world}"})
+    line = {"metric": metric, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
+            "warmup": max(3, args.warmup), "ms_per_step": max_ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": dtype, "data": "synthetic", "config": cfg, "roofline": roof,
+            "cpu_baseline": cpu, "e2e": e2e, "clocks": clk, "gpu_launches": int(launches)}
+    print(json.dumps(line))
+
+
+if __name__ == "__main__":
+    main()

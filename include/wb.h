@@ -303,6 +303,33 @@ WB_API wb_status wb_gemm(const void* A, const void* B, int64_t M, int64_t N, int
                          const float* bias, int32_t gelu, void* C, int32_t c_bf16,
                          wb_stream stream);
 
+/* ------------------------------------------------------------------ timing */
+
+/*
+ * Per-kernel timing for roofline reports (diagnostics; no counterpart on the
+ * pages).  After wb_prof_start(kind, max_launches), the library brackets every
+ * launch of that kernel kind with CUDA events recorded on the launch's own
+ * stream (up to max_launches launches; later ones are not timed) and sums
+ * each launch's algorithmic work: flops for WB_KERNEL_GEMM and
+ * WB_KERNEL_ENC_ATTN (2 M N K; 4 S^2 64 per chunk-head), bytes read and
+ * written once for the memory-bound kinds (mel: audio in + mel out; decoder
+ * attention: the K/V rows attended).  wb_prof_stop waits for the events and
+ * returns launches, their summed duration in ms, and the summed work; it ends
+ * the timing.  Not thread-safe against concurrent wb_prof_start calls.
+ */
+#define WB_KERNEL_GEMM        1
+#define WB_KERNEL_ENC_ATTN    2
+#define WB_KERNEL_CROSS_ATTN  3
+#define WB_KERNEL_SELF_ATTN   4
+#define WB_KERNEL_MEL         5
+#define WB_KERNEL_GEMM_SMALL  6   /* GEMMs with < 1024 rows: bytes of A, B, C */
+#define WB_KERNEL_MAX         6
+WB_API wb_status wb_prof_start(int32_t kind, int32_t max_launches);
+WB_API wb_status wb_prof_stop(int64_t* launches, double* total_ms, double* units);
+
+/* Number of kernels this library has launched in this process so far. */
+WB_API int64_t wb_launch_count(void);
+
 /* ------------------------------------------------------------------ status */
 
 /* Waits for the stream, then reports (and clears) the device error word of

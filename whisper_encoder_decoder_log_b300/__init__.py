@@ -59,7 +59,14 @@ _SIGS = {
     "wb_dequantise_e4m3": (ctypes.c_int, [_VP, _VP, _I64, _VP, _VP]),
     "wb_sync_status": (ctypes.c_int, [_VP, _VP]),
     "wb_gemm": (ctypes.c_int, [_VP, _VP, _I64, _I64, _I64, _I32, _VP, _VP, _VP, _I32, _VP, _I32, _VP]),
+    "wb_prof_start": (ctypes.c_int, [_I32, _I32]),
+    "wb_launch_count": (_I64, []),
+    "wb_prof_stop": (ctypes.c_int, [ctypes.POINTER(_I64), ctypes.POINTER(ctypes.c_double),
+                                    ctypes.POINTER(ctypes.c_double)]),
 }
+
+KERNEL_GEMM, KERNEL_ENC_ATTN, KERNEL_CROSS_ATTN, KERNEL_SELF_ATTN, KERNEL_MEL, KERNEL_GEMM_SMALL = 1, 2, 3, 4, 5, 6
+KERNEL_NAMES = {1: "gemm_tc", 2: "flash_enc", 3: "cross_attn", 4: "self_attn", 5: "mel", 6: "gemm_tc_small"}
 
 
 def lib():
@@ -221,6 +228,20 @@ def wb_gemm(A, B, C, bias=None, gelu=False, row_scale=None, col_scale=None, stre
     N = B.shape[0]
     _check(lib().wb_gemm(_p(A), _p(B), M, N, K, 1 if fp8 else 0, _p(row_scale), _p(col_scale), _p(bias),
                          1 if gelu else 0, _p(C), 1 if C.dtype == torch.bfloat16 else 0, _stream(stream)))
+
+
+def wb_launch_count() -> int:
+    return lib().wb_launch_count()
+
+
+def wb_prof_start(kind: int, max_launches: int = 1 << 16):
+    _check(lib().wb_prof_start(kind, max_launches))
+
+
+def wb_prof_stop():
+    n, ms, u = _I64(0), ctypes.c_double(0), ctypes.c_double(0)
+    _check(lib().wb_prof_stop(ctypes.byref(n), ctypes.byref(ms), ctypes.byref(u)))
+    return n.value, ms.value, u.value
 
 
 def wb_sync_status(model: Optional[int] = None, stream=None):

@@ -15,6 +15,7 @@
 #include "common.cuh"
 #include "gemm.cuh"
 #include "internal.h"
+#include "prof.cuh"
 #include "layers.cuh"
 
 namespace wb {
@@ -221,6 +222,7 @@ wb_status make_fp8(wb_model* m, const std::vector<std::string>& names, int64_t r
                                         m->scratch_bits, s))
             return st;
         expand_scale_kernel<<<1, 256, 0, s>>>(sc, rows_each);
+        count_launch();
     }
     WB_CUDA(cudaGetLastError());
     return WB_OK;
@@ -237,6 +239,7 @@ struct Lin {
     int64_t N = 0, K = 0;
     const FP8Weight* f8 = nullptr;
     const float* a_scale = nullptr;
+    bool split = false;           // a holds [hi | lo] bf16 halves: 2K columns, lda >= 2K
 };
 
 wb_status linear(const wb_model* m, const Lin& L, GemmEpi e, cudaStream_t s) {
@@ -257,13 +260,16 @@ wb_status linear(const wb_model* m, const Lin& L, GemmEpi e, cudaStream_t s) {
         e.row_scale = L.a_scale;
         e.col_scale = L.f8->col_scale;
     }
-    if (L.K % (f8 ? 128 : 64) != 0) return gemm_simt(A, true, B, true, L.N, L.K, e, s);
+    if (L.K % (f8 ? 128 : 64) != 0) {
+        if (L.split) return fail(WB_ERR_UNSUPPORTED, "split GEMM needs K % 64 == 0");
+        return gemm_simt(A, true, B, true, L.N, L.K, e, s);
+    }
     const int64_t tiles_m = ((L.rows + 127) / 128) * L.batches;
     int bn = 256;
     if (tiles_m * ((L.N + 255) / 256) < num_sms()) bn = 128;
     if (tiles_m * ((L.N + 127) / 128) < num_sms()) bn = 64;
     GemmPlan p;
-    if (wb_status st = gemm_plan(&p, A, B, L.N, L.K, f8, bn)) return st;
+    if (wb_status st = gemm_plan(&p, A, B, L.N, L.split ? 2 * L.K : L.K, f8, bn, L.split ? L.K : 0)) return st;
     return gemm_run(p, e, m->err, s);
 }
 
@@ -340,7 +346,7 @@ size_t carve_decoder(const wb_model* m, int64_t B, const int32_t* len, wb_decode
     void* f = c.take<uint8_t>((size_t)R * F * 4);
     uint8_t* fq = c.take<uint8_t>((size_t)R * F);
     float* f_scale = c.take<float>(R);
-    float* logits = c.take<float>((size_t)B * m->desc.vocab);
+    float* logits = c.take<float>((size_t)B * ((m->desc.vocab + 7) / 8 * 8));
     if (dec) {
         dec->crosskv = crosskv; dec->cache = cache; dec->kscale = kscale; dec->vscale = vscale;
         dec->off = off; dec->len_dev = lend; dec->h = h; dec->a = a; dec->a_scale = a_scale; dec->qkv = qkv;
@@ -384,25 +390,32 @@ size_t carve_encoder(const wb_model* m, int64_t B, EncBufs* eb, uint8_t* base, s
     return align_up(c.cur, 256);
 }
 
-// One decoder layer over R rows (rows_per_chunk per chunk, first position p0).
+// All decoder layers over R = n_chunks * rows_per_chunk rows (first position
+// p0).  With bf16 weights every activation that feeds a GEMM is carried as a
+// bf16 pair (hi, lo = bf16(x - hi)) and the GEMM runs over both halves against
+// the same weights: the step is bound by weight bandwidth, so the second half
+// costs no extra HBM traffic and the products keep ~16 mantissa bits of the
+// fp32 activation.  FP8 GEMMs quantise from fp32.
 wb_status decoder_layers(wb_decoder* dec, int64_t n_chunks, int rows_per_chunk, int p0, bool set_scales,
                          cudaStream_t s) {
     wb_model* m = dec->m;
     const int d = m->d(), H = m->H(), F = m->F();
     const int64_t R = n_chunks * rows_per_chunk;
     const bool f32 = m->fp32(), f8 = m->fp8();
-    const LnOut ln_plain = f32 ? LN_F32 : LN_BF16;
-    const DType act_dt = f32 ? DT_F32 : DT_BF16;
-    const int act_out = f32 ? OUT_F32 : OUT_BF16;
+    const bool sp = !f32;                              // split bf16 activations
+    const LnOut ln_act = f32 ? LN_F32 : LN_BF16X2;
+    const DType attn_dt = f32 ? DT_F32 : DT_BF16X2;
+    const int64_t lda = sp ? 2 * d : d;                // row stride of LN / attention outputs
     for (int l = 0; l < m->desc.dec_layers; ++l) {
         // ---- self-attention
         if (wb_status st = layernorm(dec->h, d, R, d, m->V(nm("dec.", l, "ln1.g")), m->V(nm("dec.", l, "ln1.b")),
-                                     f8 ? LN_E4M3 : ln_plain, dec->a, d, dec->a_scale, s))
+                                     f8 ? LN_E4M3 : ln_act, dec->a, f8 ? d : lda, dec->a_scale, s))
             return st;
         {
             Lin L;
-            L.a = dec->a; L.rows = R; L.lda = d; L.w = m->W(nm("dec.", l, "sq.w")); L.N = 3 * d; L.K = d;
-            if (f8) { L.f8 = &m->dec_qkv[l]; L.a_scale = dec->a_scale; }
+            L.a = dec->a; L.rows = R; L.w = m->W(nm("dec.", l, "sq.w")); L.N = 3 * d; L.K = d;
+            if (f8) { L.f8 = &m->dec_qkv[l]; L.a_scale = dec->a_scale; L.lda = d; }
+            else { L.lda = lda; L.split = sp; }
             if (wb_status st = linear(m, L, epi_out(dec->qkv, 3 * d, OUT_F32, m->V(nm("dec.", l, "sq.b"))), s)) return st;
         }
         const bool kv8 = m->desc.kv_fp8 != 0;
@@ -418,22 +431,23 @@ wb_status decoder_layers(wb_decoder* dec, int64_t n_chunks, int rows_per_chunk, 
             kv.ptr = dec->cache; kv.chunk_off = dec->off; kv.head_stride = 64; kv.chunk_len = dec->len_dev;
             kv.heads = H; kv.k_blk = 2 * l; kv.v_blk = 2 * l + 1; kv.row_stride = 64;
             if (kv8) { kv.k_scale = ks; kv.v_scale = vs; }
-            if (wb_status st = attn_rows(DT_F32, kv8 ? DT_E4M3 : DT_F32, act_dt, dec->qkv, 3 * d, n_chunks,
-                                         rows_per_chunk, H, kv, p0 + rows_per_chunk, true, p0, dec->attn, d, s))
+            if (wb_status st = attn_rows(DT_F32, kv8 ? DT_E4M3 : DT_F32, attn_dt, dec->qkv, 3 * d, n_chunks,
+                                         rows_per_chunk, H, kv, p0 + rows_per_chunk, true, p0, dec->attn, lda, s,
+                                         sp ? d : 0))
                 return st;
         }
         {
             Lin L;
-            L.a = dec->attn; L.rows = R; L.lda = d; L.w = m->W(nm("dec.", l, "so.w")); L.N = d; L.K = d;
+            L.a = dec->attn; L.rows = R; L.lda = lda; L.split = sp; L.w = m->W(nm("dec.", l, "so.w")); L.N = d; L.K = d;
             if (wb_status st = linear(m, L, epi_out(dec->h, d, OUT_F32_ACC, m->V(nm("dec.", l, "so.b"))), s)) return st;
         }
         // ---- cross-attention
         if (wb_status st = layernorm(dec->h, d, R, d, m->V(nm("dec.", l, "ln2.g")), m->V(nm("dec.", l, "ln2.b")),
-                                     ln_plain, dec->a, d, nullptr, s))
+                                     ln_act, dec->a, lda, nullptr, s))
             return st;
         {
             Lin L;
-            L.a = dec->a; L.rows = R; L.lda = d; L.w = m->W(nm("dec.", l, "cq.w")); L.N = d; L.K = d;
+            L.a = dec->a; L.rows = R; L.lda = lda; L.split = sp; L.w = m->W(nm("dec.", l, "cq.w")); L.N = d; L.K = d;
             if (wb_status st = linear(m, L, epi_out(dec->cq, d, OUT_F32, m->V(nm("dec.", l, "cq.b"))), s)) return st;
         }
         {
@@ -442,35 +456,38 @@ wb_status decoder_layers(wb_decoder* dec, int64_t n_chunks, int rows_per_chunk, 
             kv.ptr = reinterpret_cast<uint8_t*>(dec->crosskv) + (size_t)l * dec->B * 2 * H * kCtx * 64 * act;
             kv.chunk_stride = (int64_t)2 * H * kCtx * 64; kv.head_stride = (int64_t)kCtx * 64; kv.heads = H;
             kv.k_blk = 0; kv.v_blk = 1; kv.row_stride = 64;
-            if (wb_status st = attn_rows(DT_F32, act_dt, act_dt, dec->cq, d, n_chunks, rows_per_chunk, H, kv, kCtx,
-                                         false, 0, dec->attn, d, s))
+            if (wb_status st = attn_rows(DT_F32, f32 ? DT_F32 : DT_BF16, attn_dt, dec->cq, d, n_chunks, rows_per_chunk,
+                                         H, kv, kCtx, false, 0, dec->attn, lda, s, sp ? d : 0))
                 return st;
         }
         {
             Lin L;
-            L.a = dec->attn; L.rows = R; L.lda = d; L.w = m->W(nm("dec.", l, "co.w")); L.N = d; L.K = d;
+            L.a = dec->attn; L.rows = R; L.lda = lda; L.split = sp; L.w = m->W(nm("dec.", l, "co.w")); L.N = d; L.K = d;
             if (wb_status st = linear(m, L, epi_out(dec->h, d, OUT_F32_ACC, m->V(nm("dec.", l, "co.b"))), s)) return st;
         }
         // ---- FFN
         if (wb_status st = layernorm(dec->h, d, R, d, m->V(nm("dec.", l, "ln3.g")), m->V(nm("dec.", l, "ln3.b")),
-                                     f8 ? LN_E4M3 : ln_plain, dec->a, d, dec->a_scale, s))
+                                     f8 ? LN_E4M3 : ln_act, dec->a, f8 ? d : lda, dec->a_scale, s))
             return st;
-        {
-            Lin L;
-            L.a = dec->a; L.rows = R; L.lda = d; L.w = m->W(nm("dec.", l, "fc1.w")); L.N = F; L.K = d;
-            if (f8) { L.f8 = &m->dec_fc1[l]; L.a_scale = dec->a_scale; }
-            if (wb_status st = linear(m, L, epi_out(dec->f, F, act_out, m->V(nm("dec.", l, "fc1.b")), 1), s)) return st;
-        }
-        {
-            Lin L;
-            L.rows = R; L.w = m->W(nm("dec.", l, "fc2.w")); L.N = d; L.K = F;
-            if (f8) {
-                if (wb_status st = quant_rows(dec->f, R, F, dec->fq, dec->f_scale, s)) return st;
-                L.a = dec->fq; L.lda = F; L.f8 = &m->dec_fc2[l]; L.a_scale = dec->f_scale;
-            } else {
-                L.a = dec->f; L.lda = F;
-            }
-            if (wb_status st = linear(m, L, epi_out(dec->h, d, OUT_F32_ACC, m->V(nm("dec.", l, "fc2.b"))), s)) return st;
+        if (f8) {
+            Lin L1;
+            L1.a = dec->a; L1.rows = R; L1.lda = d; L1.w = m->W(nm("dec.", l, "fc1.w")); L1.N = F; L1.K = d;
+            L1.f8 = &m->dec_fc1[l]; L1.a_scale = dec->a_scale;
+            if (wb_status st = linear(m, L1, epi_out(dec->f, F, OUT_F32, m->V(nm("dec.", l, "fc1.b")), 1), s)) return st;
+            if (wb_status st = quant_rows_f32(reinterpret_cast<float*>(dec->f), R, F, dec->fq, dec->f_scale, s)) return st;
+            Lin L2;
+            L2.a = dec->fq; L2.rows = R; L2.lda = F; L2.w = m->W(nm("dec.", l, "fc2.w")); L2.N = d; L2.K = F;
+            L2.f8 = &m->dec_fc2[l]; L2.a_scale = dec->f_scale;
+            if (wb_status st = linear(m, L2, epi_out(dec->h, d, OUT_F32_ACC, m->V(nm("dec.", l, "fc2.b"))), s)) return st;
+        } else {
+            Lin L1;
+            L1.a = dec->a; L1.rows = R; L1.lda = lda; L1.split = sp; L1.w = m->W(nm("dec.", l, "fc1.w")); L1.N = F; L1.K = d;
+            const int fout = f32 ? OUT_F32 : OUT_BF16X2;
+            const int64_t ldf = sp ? 2 * F : F;
+            if (wb_status st = linear(m, L1, epi_out(dec->f, ldf, fout, m->V(nm("dec.", l, "fc1.b")), 1), s)) return st;
+            Lin L2;
+            L2.a = dec->f; L2.rows = R; L2.lda = ldf; L2.split = sp; L2.w = m->W(nm("dec.", l, "fc2.w")); L2.N = d; L2.K = F;
+            if (wb_status st = linear(m, L2, epi_out(dec->h, d, OUT_F32_ACC, m->V(nm("dec.", l, "fc2.b"))), s)) return st;
         }
     }
     return WB_OK;
@@ -481,12 +498,14 @@ wb_status decoder_head(wb_decoder* dec, int64_t n_chunks, int rows_per_chunk, in
                        cudaStream_t s) {
     wb_model* m = dec->m;
     const int d = m->d(), V = m->desc.vocab;
-    const LnOut ln_plain = m->fp32() ? LN_F32 : LN_BF16;
+    const bool sp = !m->fp32();
+    const LnOut ln_act = sp ? LN_BF16X2 : LN_F32;
+    const int64_t lda = sp ? 2 * d : d;
     const int64_t R = n_chunks * rows_per_chunk;
     Lin L;
-    L.w = m->W("dec.tok"); L.N = V; L.K = d; L.lda = d;
+    L.w = m->W("dec.tok"); L.N = V; L.K = d; L.lda = lda; L.split = sp;
     if (logits_all) {
-        if (wb_status st = layernorm(dec->h, d, R, d, m->V("dec.lnf.g"), m->V("dec.lnf.b"), ln_plain, dec->a, d,
+        if (wb_status st = layernorm(dec->h, d, R, d, m->V("dec.lnf.g"), m->V("dec.lnf.b"), ln_act, dec->a, lda,
                                      nullptr, s))
             return st;
         L.a = dec->a; L.rows = R;
@@ -496,11 +515,12 @@ wb_status decoder_head(wb_decoder* dec, int64_t n_chunks, int rows_per_chunk, in
     }
     // only the last row of each chunk matters
     if (wb_status st = layernorm(dec->h + (int64_t)(rows_per_chunk - 1) * d, (int64_t)rows_per_chunk * d, n_chunks, d,
-                                 m->V("dec.lnf.g"), m->V("dec.lnf.b"), ln_plain, dec->a, d, nullptr, s))
+                                 m->V("dec.lnf.g"), m->V("dec.lnf.b"), ln_act, dec->a, lda, nullptr, s))
         return st;
     L.a = dec->a; L.rows = n_chunks;
-    if (wb_status st = linear(m, L, epi_out(dec->logits, V, OUT_F32, nullptr), s)) return st;
-    return argmax_tokens(dec->logits, V, n_chunks, V, dec->tokens, dec->len_dev, nullptr, pos_last, s);
+    const int64_t ldl = (V + 7) / 8 * 8;
+    if (wb_status st = linear(m, L, epi_out(dec->logits, ldl, OUT_F32, nullptr), s)) return st;
+    return argmax_tokens(dec->logits, ldl, n_chunks, V, dec->tokens, dec->len_dev, nullptr, pos_last, s);
 }
 
 __global__ void gather_chunks_kernel(const float* __restrict__ audio, const int64_t* __restrict__ src,
@@ -1000,6 +1020,7 @@ wb_status wb_transcribe_batch(wb_model* m, const float* audio, const int64_t* re
         WB_CUDA(cudaStreamSynchronize(s));
         gather_chunks_kernel<<<dim3((kChunkSamples / 4 + 255) / 256, (unsigned)nw), 256, 0, s>>>(
             audio, tb.src, tb.valid, tb.chunk_audio);
+        count_launch();
         WB_CUDA(cudaGetLastError());
         if (wb_status st = wb_mel(tb.chunk_audio, nw, m->desc.n_mels, tb.mel, stream)) return st;
         for (int64_t i0 = 0; i0 < nw; i0 += kEncSubBatch) {
@@ -1010,6 +1031,7 @@ wb_status wb_transcribe_batch(wb_model* m, const float* audio, const int64_t* re
         }
         fill_prefix_kernel<<<(unsigned)((nw + 255) / 256), 256, 0, s>>>(tb.wave_tok, nw, prefix[0], prefix[1],
                                                                         prefix[2], prefix[3]);
+        count_launch();
         WB_CUDA(cudaGetLastError());
         wb_decoder* dec = nullptr;
         if (wb_status st = wb_decoder_init(m, nw, wl.data(), tb.enc, tb.wave_tok, tb.dec_ws, tb.dec_ws_bytes, stream,
@@ -1024,6 +1046,7 @@ wb_status wb_transcribe_batch(wb_model* m, const float* audio, const int64_t* re
         wb_decoder_destroy(dec);
         if (st) return st;
         scatter_tokens_kernel<<<(unsigned)nw, 128, 0, s>>>(tb.wave_tok, tb.dst_row, tb.wlen, tokens);
+        count_launch();
         WB_CUDA(cudaGetLastError());
     }
     if (n_waves_out) *n_waves_out = (int32_t)waves.size();

@@ -17,6 +17,7 @@
 //    p of a chunk sees cache rows 0..p.
 #include "attn.cuh"
 #include "common.cuh"
+#include "prof.cuh"
 
 namespace wb {
 namespace {
@@ -244,7 +245,8 @@ WB_DEV void load8<uint8_t>(const uint8_t* p, float (&v)[8]) {
 template <typename TQ, typename TKV, typename TO>
 __global__ void __launch_bounds__(kRowThreads)
 attn_rows_kernel(const TQ* __restrict__ q, int64_t q_ld, int rows_per_chunk, int n_rows_total,
-                 KVView kv, int kv_len, int causal, int q_pos0, TO* __restrict__ out, int64_t o_ld) {
+                 KVView kv, int kv_len, int causal, int q_pos0, TO* __restrict__ out, int64_t o_ld,
+                 int64_t o_split) {
     // scores for up to 4 query rows over up to kMaxKeys keys
     extern __shared__ float sm[];
     float* sq = sm;                              // [4][64]
@@ -358,14 +360,17 @@ attn_rows_kernel(const TQ* __restrict__ q, int64_t q_ld, int rows_per_chunk, int
         const int qi = i / 64, c = i % 64;
         float a = 0.f;
         for (int g = 0; g < kRowThreads / 8; ++g) a += sred[(g * kQGroup + qi) * 64 + c];
-        out[(row0 + qi) * o_ld + h * 64 + c] = (TO)(a * vs);
+        a *= vs;
+        const TO hi = (TO)a;
+        out[(row0 + qi) * o_ld + h * 64 + c] = hi;
+        if (o_split) out[(row0 + qi) * o_ld + o_split + h * 64 + c] = (TO)(a - (float)hi);
     }
 }
 
 template <typename TQ, typename TKV, typename TO>
 wb_status launch_rows(const void* q, int64_t q_ld, int64_t n_chunks, int rows_per_chunk, int heads,
                       const KVView& kv, int kv_len, bool causal, int q_pos0, void* out, int64_t o_ld,
-                      cudaStream_t s) {
+                      cudaStream_t s, int64_t o_split) {
     const size_t smem = sizeof(float) * (kQGroup * 64 + kQGroup * (size_t)kv_len + 32 * kQGroup * 64);
     static bool attr[64] = {};
     int dev = 0;
@@ -377,9 +382,19 @@ wb_status launch_rows(const void* q, int64_t q_ld, int64_t n_chunks, int rows_pe
     }
     if (smem > 200 * 1024) return fail(WB_ERR_SHAPE, "attention key length too large");
     dim3 grid((unsigned)n_chunks, (unsigned)heads, (unsigned)((rows_per_chunk + kQGroup - 1) / kQGroup));
+    const int kind = causal ? WB_KERNEL_SELF_ATTN : WB_KERNEL_CROSS_ATTN;
+    const int slot = prof_begin(kind, s);
     attn_rows_kernel<TQ, TKV, TO><<<grid, kRowThreads, smem, s>>>(
         reinterpret_cast<const TQ*>(q), q_ld, rows_per_chunk, (int)(n_chunks * rows_per_chunk), kv, kv_len,
-        causal ? 1 : 0, q_pos0, reinterpret_cast<TO*>(out), o_ld);
+        causal ? 1 : 0, q_pos0, reinterpret_cast<TO*>(out), o_ld, o_split);
+    count_launch();
+    if (slot >= 0) {
+        // K and V rows attended (each read once), queries in, outputs out
+        const double kv_rows = causal ? (double)(q_pos0 + rows_per_chunk) : (double)kv_len;
+        const double bytes = (double)n_chunks * heads *
+                             (2.0 * kv_rows * 64.0 * sizeof(TKV) + (double)rows_per_chunk * 64.0 * (sizeof(TQ) + sizeof(TO)));
+        prof_end(slot, s, bytes);
+    }
     WB_CUDA(cudaGetLastError());
     return WB_OK;
 }
@@ -390,19 +405,28 @@ wb_status attn_flash_enc_bf16(const void* qkv, int64_t n_chunks, int d, int head
                               cudaStream_t s) {
     if (n_chunks > 65535) return fail(WB_ERR_SHAPE, "too many chunks for one attention launch");
     dim3 grid((kCtx + kFaRows - 1) / kFaRows, heads, (unsigned)n_chunks);
+    const int slot = prof_begin(WB_KERNEL_ENC_ATTN, s);
     flash_enc_kernel<<<grid, 128, 0, s>>>(reinterpret_cast<const __nv_bfloat16*>(qkv), d, kCtx,
                                           reinterpret_cast<__nv_bfloat16*>(out));
+    count_launch();
+    prof_end(slot, s, 4.0 * (double)kCtx * kCtx * 64.0 * heads * (double)n_chunks);
     WB_CUDA(cudaGetLastError());
     return WB_OK;
 }
 
 wb_status attn_rows(DType tq, DType tkv, DType to, const void* q, int64_t q_ld, int64_t n_chunks,
                     int rows_per_chunk, int heads, const KVView& kv, int kv_len, bool causal, int q_pos0,
-                    void* out, int64_t o_ld, cudaStream_t s) {
+                    void* out, int64_t o_ld, cudaStream_t s, int64_t o_split) {
     if (n_chunks <= 0 || rows_per_chunk <= 0) return WB_OK;
+    if (to == DT_BF16X2) {
+        if (o_split <= 0) return fail(WB_ERR_INVALID_ARG, "split attention output needs an offset");
+        to = DT_BF16;
+    } else {
+        o_split = 0;
+    }
     if (n_chunks > 0x7FFFFFFF || heads > 65535) return fail(WB_ERR_SHAPE, "attention grid too large");
 #define WB_ROWS(TQ_, TKV_, TO_) \
-    return launch_rows<TQ_, TKV_, TO_>(q, q_ld, n_chunks, rows_per_chunk, heads, kv, kv_len, causal, q_pos0, out, o_ld, s)
+    return launch_rows<TQ_, TKV_, TO_>(q, q_ld, n_chunks, rows_per_chunk, heads, kv, kv_len, causal, q_pos0, out, o_ld, s, o_split)
     if (tq == DT_F32 && tkv == DT_F32 && to == DT_F32) WB_ROWS(float, float, float);
     if (tq == DT_F32 && tkv == DT_BF16 && to == DT_BF16) WB_ROWS(float, __nv_bfloat16, __nv_bfloat16);
     if (tq == DT_BF16 && tkv == DT_BF16 && to == DT_BF16) WB_ROWS(__nv_bfloat16, __nv_bfloat16, __nv_bfloat16);

@@ -7,7 +7,8 @@
 
 namespace wb {
 
-enum DType : int { DT_F32 = 0, DT_BF16 = 1, DT_E4M3 = 2 };
+// DT_BF16X2 (outputs only): hi = bf16(o) at column c, lo = bf16(o - hi) at c + o_split.
+enum DType : int { DT_F32 = 0, DT_BF16 = 1, DT_E4M3 = 2, DT_BF16X2 = 3 };
 
 // Where the keys/values of (chunk c, head h, key j) live (element offsets):
 //   hs(c)   = head_stride * (chunk_len ? chunk_len[c] : 1)
@@ -37,6 +38,6 @@ wb_status attn_flash_enc_bf16(const void* qkv, int64_t n_chunks, int d, int head
 // causal, over keys 0..q_pos0 + r.  Output row likewise with o_ld.
 wb_status attn_rows(DType tq, DType tkv, DType to, const void* q, int64_t q_ld, int64_t n_chunks,
                     int rows_per_chunk, int heads, const KVView& kv, int kv_len, bool causal, int q_pos0,
-                    void* out, int64_t o_ld, cudaStream_t s);
+                    void* out, int64_t o_ld, cudaStream_t s, int64_t o_split = 0);
 
 }  // namespace wb

@@ -23,6 +23,7 @@
 
 #include "common.cuh"
 #include "gemm.cuh"
+#include "prof.cuh"
 
 namespace wb {
 
@@ -48,6 +49,7 @@ struct GemmArgs {
     int64_t N, K;
     int64_t mt_per_batch, mt_total, nt_total, tiles;
     int kblocks;
+    int b_kwrap;
     GemmEpi epi;
 };
 
@@ -66,6 +68,7 @@ __device__ __forceinline__ void store_chunk(const GemmArgs& a, int64_t b, int64_
     const GemmEpi& e = a.epi;
     const int64_t N = a.N;
     const bool full = n0 + 32 <= N;
+    const bool vec = full && e.vec;
     // scale, bias, GELU, positional table
     if (e.row_scale || e.col_scale) {
         const float rs = e.row_scale ? e.row_scale[b * a.rows + r] : 1.f;
@@ -108,9 +111,27 @@ __device__ __forceinline__ void store_chunk(const GemmArgs& a, int64_t b, int64_
     const int64_t obr = e.out_batch_rows ? e.out_batch_rows : a.rows;
     orow = b * obr + e.out_row_offset + r;
     base = e.out;
-    if (e.out_type == OUT_BF16) {
+    if (e.out_type == OUT_BF16X2) {
         __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(base) + orow * e.ldo + n0;
-        if (full) {
+        float lo[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) lo[j] = v[j] - __bfloat162float(__float2bfloat16_rn(v[j]));
+        if (vec) {
+            uint4* d4 = reinterpret_cast<uint4*>(dst);
+            uint4* l4 = reinterpret_cast<uint4*>(dst + N);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                d4[q] = make_uint4(pack_bf16x2(v[8 * q + 0], v[8 * q + 1]), pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
+                                   pack_bf16x2(v[8 * q + 4], v[8 * q + 5]), pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
+                l4[q] = make_uint4(pack_bf16x2(lo[8 * q + 0], lo[8 * q + 1]), pack_bf16x2(lo[8 * q + 2], lo[8 * q + 3]),
+                                   pack_bf16x2(lo[8 * q + 4], lo[8 * q + 5]), pack_bf16x2(lo[8 * q + 6], lo[8 * q + 7]));
+            }
+        } else {
+            for (int j = 0; j < 32 && n0 + j < N; ++j) { dst[j] = f2bf(v[j]); dst[N + j] = f2bf(lo[j]); }
+        }
+    } else if (e.out_type == OUT_BF16) {
+        __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(base) + orow * e.ldo + n0;
+        if (vec) {
             uint4* d4 = reinterpret_cast<uint4*>(dst);
 #pragma unroll
             for (int q = 0; q < 4; ++q)
@@ -124,7 +145,7 @@ __device__ __forceinline__ void store_chunk(const GemmArgs& a, int64_t b, int64_
     } else {
         float* dst = reinterpret_cast<float*>(base) + orow * e.ldo + n0;
         const bool acc = e.out_type == OUT_F32_ACC;
-        if (full) {
+        if (vec) {
             float4* d4 = reinterpret_cast<float4*>(dst);
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
@@ -216,8 +237,9 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant_
                     unsigned char* sb = sa + C::A_BYTES;
                     mbar_arrive_expect_tx(&full_bar[stage], C::STAGE_BYTES);
                     const int kx = kb * (FP8 ? 128 : 64);
+                    const int kxb = args.b_kwrap ? kx % args.b_kwrap : kx;
                     tma_load_3d(sa, &tma_a, &full_bar[stage], kx, r0, b);
-                    tma_load_2d(sb, &tma_b, &full_bar[stage], kx, n0);
+                    tma_load_2d(sb, &tma_b, &full_bar[stage], kxb, n0);
                     issued[stage] = true;
                     last_parity[stage] = phase;
                     if (++stage == STAGES) { stage = 0; phase ^= 1; }
@@ -364,6 +386,7 @@ wb_status launch_tc(const GemmPlan& p, const GemmArgs& a, unsigned* err, cudaStr
     grid = (int)std::min<int64_t>(grid, a.tiles);
     if (grid <= 0) return WB_OK;
     gemm_tc_kernel<BN, FP8><<<grid, 192, C::SMEM, s>>>(p.tma_a, p.tma_b, a, err);
+    count_launch();
     WB_CUDA(cudaGetLastError());
     return WB_OK;
 }
@@ -381,7 +404,7 @@ int num_sms() {
 }
 
 wb_status gemm_plan(GemmPlan* plan, const GemmOperand& A, const GemmOperand& B, int64_t N, int64_t K,
-                    bool fp8, int bn) {
+                    bool fp8, int bn, int64_t b_kwrap) {
     if (wb_status st = get_encoder()) return st;
     const int esz = fp8 ? 1 : 2;
     const int bk = fp8 ? 128 : 64;
@@ -397,8 +420,9 @@ wb_status gemm_plan(GemmPlan* plan, const GemmOperand& A, const GemmOperand& B, 
         uint32_t box[3] = {(uint32_t)bk, (uint32_t)kBM, 1};
         if (wb_status st = encode_map(&plan->tma_a, A.ptr, 3, dims, strides, box, fp8)) return st;
     }
+    if (b_kwrap && (b_kwrap % bk || K % b_kwrap)) return fail(WB_ERR_SHAPE, "GEMM k-wrap must divide K");
     {
-        uint64_t dims[2] = {(uint64_t)K, (uint64_t)N};
+        uint64_t dims[2] = {(uint64_t)(b_kwrap ? b_kwrap : K), (uint64_t)N};
         uint64_t strides[1] = {(uint64_t)(B.row_stride * esz)};
         uint32_t box[2] = {(uint32_t)bk, (uint32_t)bn};
         if (wb_status st = encode_map(&plan->tma_b, B.ptr, 2, dims, strides, box, fp8)) return st;
@@ -408,6 +432,7 @@ wb_status gemm_plan(GemmPlan* plan, const GemmOperand& A, const GemmOperand& B, 
     plan->N = N;
     plan->K = K;
     plan->bn = bn;
+    plan->b_kwrap = b_kwrap;
     plan->fp8 = fp8;
     plan->ok = true;
     return WB_OK;
@@ -415,9 +440,6 @@ wb_status gemm_plan(GemmPlan* plan, const GemmOperand& A, const GemmOperand& B, 
 
 wb_status gemm_run(const GemmPlan& p, const GemmEpi& epi, unsigned* err, cudaStream_t s, int max_ctas) {
     if (!p.ok) return fail(WB_ERR_INVALID_ARG, "GEMM plan not built");
-    if (epi.out_type == OUT_BF16 && epi.mode == MODE_PLAIN && (epi.ldo % 8))
-        return fail(WB_ERR_ALIGN, "bf16 GEMM output stride must be a multiple of 8");
-    if (epi.out_type != OUT_BF16 && (epi.ldo % 4)) return fail(WB_ERR_ALIGN, "fp32 output stride % 4");
     GemmArgs a;
     a.rows = p.M_rows;
     a.batches = p.batches;
@@ -428,16 +450,31 @@ wb_status gemm_run(const GemmPlan& p, const GemmEpi& epi, unsigned* err, cudaStr
     a.nt_total = (p.N + p.bn - 1) / p.bn;
     a.tiles = a.mt_total * a.nt_total;
     a.kblocks = (int)(p.K / (p.fp8 ? 128 : 64));
+    a.b_kwrap = (int)p.b_kwrap;
     a.epi = epi;
+    const bool half = epi.out_type == OUT_BF16 || epi.out_type == OUT_BF16X2;
+    a.epi.vec = aligned16(epi.out) && (epi.mode == MODE_CROSS_KV || (epi.ldo * (half ? 2 : 4)) % 16 == 0) &&
+                (epi.out_type != OUT_BF16X2 || (p.N * 2) % 16 == 0);
+    if (epi.mode == MODE_CROSS_KV && !a.epi.vec) return fail(WB_ERR_ALIGN, "cross K/V output not 16-byte aligned");
     if (a.tiles == 0 || a.kblocks == 0) return WB_OK;
+    const bool small = p.M_rows * p.batches < 1024;
+    const int slot = prof_begin(small ? WB_KERNEL_GEMM_SMALL : WB_KERNEL_GEMM, s);
+    wb_status st;
     if (p.fp8) {
-        if (p.bn == 256) return launch_tc<256, true>(p, a, err, s, max_ctas);
-        if (p.bn == 128) return launch_tc<128, true>(p, a, err, s, max_ctas);
-        return launch_tc<64, true>(p, a, err, s, max_ctas);
+        if (p.bn == 256) st = launch_tc<256, true>(p, a, err, s, max_ctas);
+        else if (p.bn == 128) st = launch_tc<128, true>(p, a, err, s, max_ctas);
+        else st = launch_tc<64, true>(p, a, err, s, max_ctas);
+    } else {
+        if (p.bn == 256) st = launch_tc<256, false>(p, a, err, s, max_ctas);
+        else if (p.bn == 128) st = launch_tc<128, false>(p, a, err, s, max_ctas);
+        else st = launch_tc<64, false>(p, a, err, s, max_ctas);
     }
-    if (p.bn == 256) return launch_tc<256, false>(p, a, err, s, max_ctas);
-    if (p.bn == 128) return launch_tc<128, false>(p, a, err, s, max_ctas);
-    return launch_tc<64, false>(p, a, err, s, max_ctas);
+    const double k_alg = (double)(p.b_kwrap ? p.b_kwrap : p.K);
+    const double M = (double)(p.M_rows * p.batches), esz = p.fp8 ? 1.0 : 2.0;
+    const double osz = (epi.out_type == OUT_BF16) ? 2.0 : (epi.out_type == OUT_F32_ACC ? 8.0 : 4.0);
+    if (small) prof_end(slot, s, (double)p.N * k_alg * esz + M * (double)p.K * esz + M * (double)p.N * osz);
+    else prof_end(slot, s, 2.0 * M * (double)p.N * k_alg);
+    return st;
 }
 
 // ------------------------------------------------------------------ SIMT GEMM
@@ -536,7 +573,9 @@ wb_status gemm_simt(const GemmOperand& A, bool a_bf16, const GemmOperand& B, boo
     a.nt_total = (N + 63) / 64;
     a.tiles = a.mt_total * a.nt_total;
     a.kblocks = 0;
+    a.b_kwrap = 0;
     a.epi = epi;
+    if (epi.out_type == OUT_BF16X2) return fail(WB_ERR_UNSUPPORTED, "SIMT GEMM: no split output");
     if (a.tiles == 0) return WB_OK;
     if (a.mt_total > 65535) return fail(WB_ERR_SHAPE, "SIMT GEMM: too many row tiles");
     dim3 grid((unsigned)a.nt_total, (unsigned)a.mt_total);
@@ -544,6 +583,7 @@ wb_status gemm_simt(const GemmOperand& A, bool a_bf16, const GemmOperand& B, boo
     else if (!a_bf16 && b_bf16) gemm_simt_kernel<false, true><<<grid, 256, 0, s>>>(A.ptr, A, B.ptr, B.row_stride, a);
     else if (a_bf16 && !b_bf16) gemm_simt_kernel<true, false><<<grid, 256, 0, s>>>(A.ptr, A, B.ptr, B.row_stride, a);
     else gemm_simt_kernel<false, false><<<grid, 256, 0, s>>>(A.ptr, A, B.ptr, B.row_stride, a);
+    count_launch();
     WB_CUDA(cudaGetLastError());
     return WB_OK;
 }

@@ -8,7 +8,9 @@
 
 namespace wb {
 
-enum GemmOut : int { OUT_BF16 = 0, OUT_F32 = 1, OUT_F32_ACC = 2 };
+enum GemmOut : int { OUT_BF16 = 0, OUT_F32 = 1, OUT_F32_ACC = 2, OUT_BF16X2 = 3 };
+// OUT_BF16X2 writes v as a bf16 pair: hi = bf16(v) at column n and
+// lo = bf16(v - hi) at column N + n of the same row (ldo >= 2N).
 enum GemmMode : int { MODE_PLAIN = 0, MODE_CROSS_KV = 1 };
 
 // C = epilogue(A[M, K] . B[N, K]^T)
@@ -33,6 +35,7 @@ struct GemmEpi {
     int64_t ckv_chunks = 0;
     int64_t out_batch_rows = 0;      // 0: = rows_per_batch
     int out_row_offset = 0;
+    int vec = 1;                     // set by the launcher: 16-byte stores allowed
 };
 
 // Operand description.  A is either a plain [M, K] matrix (batches = 1,
@@ -51,6 +54,7 @@ struct GemmPlan {
     CUtensorMap tma_b;
     int64_t M_rows = 0, batches = 1;
     int64_t N = 0, K = 0;
+    int64_t b_kwrap = 0;   // A has K columns, B has b_kwrap: B is read at k mod b_kwrap
     int bn = 256;
     bool fp8 = false;
     bool ok = false;
@@ -59,7 +63,7 @@ struct GemmPlan {
 // Build the TMA descriptors (host only, no launch).  Element type bf16, or
 // E4M3 when fp8.  Returns WB_OK or an error code with the message set.
 wb_status gemm_plan(GemmPlan* plan, const GemmOperand& A, const GemmOperand& B, int64_t N,
-                    int64_t K, bool fp8, int bn);
+                    int64_t K, bool fp8, int bn, int64_t b_kwrap = 0);
 wb_status gemm_run(const GemmPlan& plan, const GemmEpi& epi, unsigned* err, cudaStream_t s,
                    int max_ctas = 0);
 

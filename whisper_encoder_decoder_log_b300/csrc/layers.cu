@@ -11,6 +11,7 @@
 // "Inference Stack"; greedy choice follows the "thewhisper-large-v3-turbo"
 // model card, "NVIDIA Usage" (no sampling, one beam).
 #include "common.cuh"
+#include "prof.cuh"
 #include "layers.cuh"
 
 namespace wb {
@@ -59,6 +60,15 @@ layernorm_kernel(const float* __restrict__ x, int64_t ld_x, int64_t rows, int d,
 #pragma unroll
         for (int i = 0; i < kMaxPerLane; ++i)
             if (i < per) o[i * 32 + lane] = f2bf(v[i]);
+    } else if (OUT == LN_BF16X2) {
+        __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(out) + row * ld_o;
+#pragma unroll
+        for (int i = 0; i < kMaxPerLane; ++i)
+            if (i < per) {
+                const __nv_bfloat16 hi = f2bf(v[i]);
+                o[i * 32 + lane] = hi;
+                o[d + i * 32 + lane] = f2bf(v[i] - bf2f(hi));
+            }
     } else {   // LN_E4M3: per-row scale amax / 448
         amax = warp_max(amax);
         const float sc = amax > 0.f ? amax / 448.0f : 1.0f;
@@ -182,6 +192,29 @@ __global__ void quant_rows_kernel(const __nv_bfloat16* __restrict__ x, int64_t r
     if (lane == 0) row_scale[r] = sc;
 }
 
+// Per-row E4M3 quantisation of an fp32 matrix.
+__global__ void quant_rows_f32_kernel(const float* __restrict__ x, int64_t rows, int K, uint8_t* __restrict__ q,
+                                      float* __restrict__ row_scale) {
+    const int64_t r = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (r >= rows) return;
+    const float* xr = x + r * K;
+    float m = 0.f;
+    for (int i = lane * 4; i < K; i += 128) {
+        const float4 a = *reinterpret_cast<const float4*>(xr + i);
+        m = fmaxf(m, fmaxf(fmaxf(fabsf(a.x), fabsf(a.y)), fmaxf(fabsf(a.z), fabsf(a.w))));
+    }
+    m = warp_max(m);
+    const float sc = m > 0.f ? m / 448.0f : 1.0f;
+    const float inv = 1.0f / sc;
+    for (int i = lane * 4; i < K; i += 128) {
+        const float4 a = *reinterpret_cast<const float4*>(xr + i);
+        const uint32_t o = (uint32_t)f2e4m3x2(a.x * inv, a.y * inv) | ((uint32_t)f2e4m3x2(a.z * inv, a.w * inv) << 16);
+        *reinterpret_cast<uint32_t*>(q + r * K + i) = o;
+    }
+    if (lane == 0) row_scale[r] = sc;
+}
+
 // amax of a tensor (non-negative floats order like their bit patterns).
 template <typename T>
 __global__ void amax_kernel(const T* __restrict__ x, int64_t n, unsigned* __restrict__ out_bits) {
@@ -284,7 +317,9 @@ wb_status layernorm(const float* x, int64_t ld_x, int64_t rows, int d, const flo
     const unsigned grid = (unsigned)((rows + 7) / 8);
     if (mode == LN_F32) layernorm_kernel<LN_F32><<<grid, 256, 0, s>>>(x, ld_x, rows, d, g, b, out, ld_o, row_scale);
     else if (mode == LN_BF16) layernorm_kernel<LN_BF16><<<grid, 256, 0, s>>>(x, ld_x, rows, d, g, b, out, ld_o, row_scale);
+    else if (mode == LN_BF16X2) layernorm_kernel<LN_BF16X2><<<grid, 256, 0, s>>>(x, ld_x, rows, d, g, b, out, ld_o, row_scale);
     else layernorm_kernel<LN_E4M3><<<grid, 256, 0, s>>>(x, ld_x, rows, d, g, b, out, ld_o, row_scale);
+    count_launch();
     WB_CUDA(cudaGetLastError());
     return WB_OK;
 }
@@ -298,6 +333,7 @@ wb_status embed(const int32_t* tokens, int64_t rows, int P, int p0, int d, const
     else
         embed_kernel<float><<<(unsigned)rows, 256, 0, s>>>(tokens, rows, P, p0, d, reinterpret_cast<const float*>(E),
                                                            reinterpret_cast<const float*>(Pos), vocab, x, err);
+    count_launch();
     WB_CUDA(cudaGetLastError());
     return WB_OK;
 }
@@ -305,6 +341,7 @@ wb_status embed(const int32_t* tokens, int64_t rows, int P, int p0, int d, const
 wb_status kv_scales(const float* qkv, int64_t n_chunks, int P, int d, float* k_scale, float* v_scale, cudaStream_t s) {
     if (n_chunks <= 0) return WB_OK;
     kv_scale_kernel<<<dim3((unsigned)n_chunks, 2), 256, 0, s>>>(qkv, P, d, k_scale, v_scale);
+    count_launch();
     WB_CUDA(cudaGetLastError());
     return WB_OK;
 }
@@ -316,6 +353,7 @@ wb_status kv_append(const float* qkv, int64_t n_chunks, int P, int p0, int d, in
     const unsigned grid = (unsigned)(n_chunks * P);
     if (fp8) kv_append_kernel<true><<<grid, 256, 0, s>>>(qkv, n_chunks, P, p0, d, H, layer, cache, off, len, k_scale, v_scale, err);
     else kv_append_kernel<false><<<grid, 256, 0, s>>>(qkv, n_chunks, P, p0, d, H, layer, cache, off, len, k_scale, v_scale, err);
+    count_launch();
     WB_CUDA(cudaGetLastError());
     return WB_OK;
 }
@@ -325,6 +363,16 @@ wb_status quant_rows(const void* x_bf16, int64_t rows, int K, uint8_t* q, float*
     if (K % 256) return fail(WB_ERR_SHAPE, "row quantiser needs K % 256 == 0");
     quant_rows_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(reinterpret_cast<const __nv_bfloat16*>(x_bf16), rows, K,
                                                                    q, row_scale);
+    count_launch();
+    WB_CUDA(cudaGetLastError());
+    return WB_OK;
+}
+
+wb_status quant_rows_f32(const float* x, int64_t rows, int K, uint8_t* q, float* row_scale, cudaStream_t s) {
+    if (rows <= 0) return WB_OK;
+    if (K % 128) return fail(WB_ERR_SHAPE, "row quantiser needs K % 128 == 0");
+    quant_rows_f32_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(x, rows, K, q, row_scale);
+    count_launch();
     WB_CUDA(cudaGetLastError());
     return WB_OK;
 }
@@ -335,11 +383,14 @@ wb_status quant_tensor(const void* x, bool bf16, int64_t n, uint8_t* q, float* s
     if (n > 0) {
         if (bf16) amax_kernel<__nv_bfloat16><<<grid_for(n, 256), 256, 0, s>>>(reinterpret_cast<const __nv_bfloat16*>(x), n, scratch_bits);
         else amax_kernel<float><<<grid_for(n, 256), 256, 0, s>>>(reinterpret_cast<const float*>(x), n, scratch_bits);
+        count_launch();
     }
     scale_from_amax_kernel<<<1, 1, 0, s>>>(scratch_bits, scale);
+    count_launch();
     if (n > 0) {
         if (bf16) quant_tensor_kernel<__nv_bfloat16><<<grid_for(n, 256), 256, 0, s>>>(reinterpret_cast<const __nv_bfloat16*>(x), n, scale, q);
         else quant_tensor_kernel<float><<<grid_for(n, 256), 256, 0, s>>>(reinterpret_cast<const float*>(x), n, scale, q);
+        count_launch();
     }
     WB_CUDA(cudaGetLastError());
     return WB_OK;
@@ -348,6 +399,7 @@ wb_status quant_tensor(const void* x, bool bf16, int64_t n, uint8_t* q, float* s
 wb_status dequant_tensor(const uint8_t* q, const float* scale, int64_t n, float* out, cudaStream_t s) {
     if (n <= 0) return WB_OK;
     dequant_kernel<<<grid_for(n, 256), 256, 0, s>>>(q, scale, n, out);
+    count_launch();
     WB_CUDA(cudaGetLastError());
     return WB_OK;
 }
@@ -355,6 +407,7 @@ wb_status dequant_tensor(const uint8_t* q, const float* scale, int64_t n, float*
 wb_status fill(float* x, int64_t n, float v, cudaStream_t s) {
     if (n <= 0) return WB_OK;
     fill_kernel<<<grid_for(n, 256), 256, 0, s>>>(x, n, v);
+    count_launch();
     WB_CUDA(cudaGetLastError());
     return WB_OK;
 }
@@ -363,6 +416,7 @@ wb_status argmax_tokens(const float* logits, int64_t ld, int64_t rows, int V, in
                         const int* pos_dev, int pos_host, cudaStream_t s) {
     if (rows <= 0) return WB_OK;
     argmax_kernel<<<(unsigned)rows, 256, 0, s>>>(logits, ld, rows, V, tokens, len, pos_dev, pos_host);
+    count_launch();
     WB_CUDA(cudaGetLastError());
     return WB_OK;
 }
@@ -371,6 +425,7 @@ wb_status conv_reorder(const void* w, int O, int C, bool bf16, void* out, cudaSt
     const int64_t n = (int64_t)O * C * 3;
     if (bf16) conv_reorder_kernel<__nv_bfloat16><<<grid_for(n, 256), 256, 0, s>>>(reinterpret_cast<const __nv_bfloat16*>(w), O, C, reinterpret_cast<__nv_bfloat16*>(out));
     else conv_reorder_kernel<float><<<grid_for(n, 256), 256, 0, s>>>(reinterpret_cast<const float*>(w), O, C, reinterpret_cast<float*>(out));
+    count_launch();
     WB_CUDA(cudaGetLastError());
     return WB_OK;
 }
@@ -379,6 +434,7 @@ wb_status gather_rows(const float* x, int64_t rows, int d, int64_t stride_rows, 
                       cudaStream_t s) {
     if (rows <= 0) return WB_OK;
     gather_rows_kernel<<<(unsigned)rows, 256, 0, s>>>(x, rows, d, stride_rows, first, out);
+    count_launch();
     WB_CUDA(cudaGetLastError());
     return WB_OK;
 }

@@ -7,7 +7,8 @@
 
 namespace wb {
 
-enum LnOut : int { LN_F32 = 0, LN_BF16 = 1, LN_E4M3 = 2 };
+// LN_BF16X2 writes hi = bf16(y) at column c and lo = bf16(y - hi) at d + c.
+enum LnOut : int { LN_F32 = 0, LN_BF16 = 1, LN_E4M3 = 2, LN_BF16X2 = 3 };
 
 wb_status layernorm(const float* x, int64_t ld_x, int64_t rows, int d, const float* g, const float* b, LnOut mode,
                     void* out, int64_t ld_o, float* row_scale, cudaStream_t s);
@@ -18,6 +19,8 @@ wb_status kv_append(const float* qkv, int64_t n_chunks, int P, int p0, int d, in
                     const int64_t* off, const int32_t* len, const float* k_scale, const float* v_scale, unsigned* err,
                     cudaStream_t s);
 wb_status quant_rows(const void* x_bf16, int64_t rows, int K, uint8_t* q, float* row_scale, cudaStream_t s);
+// Same from an fp32 matrix.
+wb_status quant_rows_f32(const float* x, int64_t rows, int K, uint8_t* q, float* row_scale, cudaStream_t s);
 wb_status quant_tensor(const void* x, bool bf16, int64_t n, uint8_t* q, float* scale, unsigned* scratch_bits,
                        cudaStream_t s);
 wb_status dequant_tensor(const uint8_t* q, const float* scale, int64_t n, float* out, cudaStream_t s);

@@ -26,6 +26,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "prof.cuh"
 
 namespace cg = cooperative_groups;
 
@@ -347,7 +348,10 @@ wb_status mel_launch(const float* audio, int64_t B, int n_mels, float* mel, cuda
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    const int slot = prof_begin(WB_KERNEL_MEL, s);
     WB_CUDA(cudaLaunchKernelEx(&cfg, mel_kernel, audio, (const MelTables*)tab, n_mels, mel));
+    count_launch();
+    prof_end(slot, s, (double)B * ((double)kChunkSamples * 4.0 + (double)n_mels * kFrames * 4.0));
     return WB_OK;
 }
 
@@ -356,6 +360,7 @@ wb_status mel_transpose_pad(const float* mel, int64_t B, int C, void* out, bool 
     if (C > 128) return fail(WB_ERR_SHAPE, "n_mels > 128");
     dim3 grid((kFrames + 2 + 31) / 32, (unsigned)B);
     transpose_pad_kernel<<<grid, dim3(32, 8), 0, s>>>(mel, C, out, bf16);
+    count_launch();
     WB_CUDA(cudaGetLastError());
     return WB_OK;
 }
