@@ -13,7 +13,6 @@ import torch.nn.functional as F
 from oracle import e4m3, model
 from synth import ModelDims, make_weights
 
-torch.set_default_dtype(torch.float64)
 MINI = ModelDims("mini", 8, 128, 2, 256, 2, 2, 97)
 
 
@@ -79,7 +78,7 @@ def test_attention_brute_force_and_torch(causal):
 
 def _torch_encoder_layer(W, l, d, H, f):
     layer = torch.nn.TransformerEncoderLayer(d, H, f, dropout=0.0, activation="gelu",
-                                             batch_first=True, norm_first=True)
+                                             batch_first=True, norm_first=True, dtype=torch.float64)
     p = f"enc.{l}."
     sd = {
         "self_attn.in_proj_weight": T(np.concatenate([W[p + "q.w"], W[p + "k.w"], W[p + "v.w"]])),
@@ -112,12 +111,12 @@ def test_decoder_matches_torch_pre_ln_decoder_layers():
     logits, info = model.decode_teacher_forced(tok, enc, W, MINI, return_hidden=True)
     d, H = MINI.d_model, MINI.n_heads
     x = (T(W["dec.tok"][tok]) + T(W["dec.pos"][:9]))[None]
-    mask = torch.nn.Transformer.generate_square_subsequent_mask(9)
+    mask = torch.nn.Transformer.generate_square_subsequent_mask(9, dtype=torch.float64)
     for l in range(MINI.dec_layers):
         p = f"dec.{l}."
         layer = torch.nn.TransformerDecoderLayer(d, H, MINI.d_ffn, dropout=0.0,
                                                  activation="gelu", batch_first=True,
-                                                 norm_first=True)
+                                                 norm_first=True, dtype=torch.float64)
         cat = lambda a, b, c: T(np.concatenate([W[p + a], W[p + b], W[p + c]]))  # noqa: E731
         sd = {"self_attn.in_proj_weight": cat("sq.w", "sk.w", "sv.w"),
               "self_attn.in_proj_bias": cat("sq.b", "sk.b", "sv.b"),

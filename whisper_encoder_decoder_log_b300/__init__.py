@@ -57,6 +57,7 @@ _SIGS = {
     "wb_plan_waves": (ctypes.c_int, [ctypes.POINTER(ModelDesc), _I32, _VP, _U64, _VP, _VP, _VP]),
     "wb_quantise_e4m3": (ctypes.c_int, [_VP, _I32, _I64, _VP, _VP, _VP]),
     "wb_dequantise_e4m3": (ctypes.c_int, [_VP, _VP, _I64, _VP, _VP]),
+    "wb_quantise_e4m3_static": (ctypes.c_int, [_VP, _I32, _I64, _VP, _VP, _VP]),
     "wb_sync_status": (ctypes.c_int, [_VP, _VP]),
     "wb_gemm": (ctypes.c_int, [_VP, _VP, _I64, _I64, _I64, _I32, _VP, _VP, _VP, _I32, _VP, _I32, _VP]),
     "wb_prof_start": (ctypes.c_int, [_I32, _I32]),
@@ -109,6 +110,14 @@ def _stream(stream=None) -> Optional[int]:
     return stream.cuda_stream
 
 
+def _need(t, dtype_name: str, what: str):
+    """Reject a tensor whose element type is not the one the C ABI expects."""
+    if t is not None and str(t.dtype) != "torch." + dtype_name:
+        raise TypeError(f"{what} must be torch.{dtype_name}, got {t.dtype}")
+    if t is not None and not t.is_contiguous():
+        raise ValueError(f"{what} must be contiguous")
+
+
 def _host_arr(a, dtype):
     a = np.ascontiguousarray(a, dtype=dtype)
     return a, a.ctypes.data
@@ -121,6 +130,8 @@ def wb_version() -> int:
 
 
 def wb_mel(audio, n_mels: int, mel, stream=None):
+    _need(audio, "float32", "audio")
+    _need(mel, "float32", "mel")
     _check(lib().wb_mel(_p(audio), audio.shape[0], n_mels, _p(mel), _stream(stream)))
 
 
@@ -149,6 +160,9 @@ def wb_encode_workspace_size(model: int, B: int) -> int:
 
 
 def wb_encode(model: int, mel, enc, workspace, stream=None):
+    _need(mel, "float32", "mel")
+    if str(enc.dtype) not in ("torch.float32", "torch.bfloat16"):
+        raise TypeError("enc must be float32 (fp32 model) or bfloat16")
     _check(lib().wb_encode(model, _p(mel), mel.shape[0], _p(enc), _p(workspace), workspace.numel() *
                            workspace.element_size(), _stream(stream)))
 
@@ -160,6 +174,7 @@ def wb_decoder_workspace_size(model: int, chunk_len) -> int:
 
 def wb_decoder_init(model: int, chunk_len, enc, tokens, workspace, stream=None) -> int:
     arr, ptr = _host_arr(chunk_len, np.int32)
+    _need(tokens, "int32", "tokens")
     h = _VP(0)
     _check(lib().wb_decoder_init(model, arr.size, ptr, _p(enc), _p(tokens), _p(workspace),
                                  workspace.numel() * workspace.element_size(), _stream(stream), ctypes.byref(h)))
@@ -167,10 +182,12 @@ def wb_decoder_init(model: int, chunk_len, enc, tokens, workspace, stream=None) 
 
 
 def wb_decode_prefix(dec: int, P: int, logits=None, stream=None):
+    _need(logits, "float32", "logits")
     _check(lib().wb_decode_prefix(dec, P, _p(logits), _stream(stream)))
 
 
 def wb_decode_step(dec: int, n_active: int, logits=None, stream=None):
+    _need(logits, "float32", "logits")
     _check(lib().wb_decode_step(dec, n_active, _p(logits), _stream(stream)))
 
 
@@ -194,6 +211,8 @@ def wb_transcribe_batch(model: int, audio, req_offset, req_samples, prefix, chun
     rs, rsp = _host_arr(req_samples, np.int64)
     pf, pfp = _host_arr(prefix, np.int32)
     cl, clp = _host_arr(chunk_len, np.int32)
+    _need(audio, "float32", "audio")
+    _need(tokens, "int32", "tokens")
     nw = _I32(0)
     _check(lib().wb_transcribe_batch(model, _p(audio), rop, rsp, rs.size, pfp, clp, _p(tokens), budget,
                                      _p(workspace), workspace.numel() * workspace.element_size(),
@@ -213,11 +232,23 @@ def wb_plan_waves(desc: ModelDesc, chunk_len, budget: int):
 
 def wb_quantise_e4m3(x, codes, scale, stream=None):
     import torch
+    _need(codes, "uint8", "codes")
+    _need(scale, "float32", "scale")
     _check(lib().wb_quantise_e4m3(_p(x), 1 if x.dtype == torch.bfloat16 else 0, x.numel(), _p(codes), _p(scale),
                                   _stream(stream)))
 
 
+def wb_quantise_e4m3_static(x, codes, scale, stream=None):
+    """wb_quantise_e4m3 without any device allocation (n <= 2^26)."""
+    import torch
+    _need(codes, "uint8", "codes")
+    _need(scale, "float32", "scale")
+    _check(lib().wb_quantise_e4m3_static(_p(x), 1 if x.dtype == torch.bfloat16 else 0, x.numel(), _p(codes),
+                                         _p(scale), _stream(stream)))
+
+
 def wb_dequantise_e4m3(codes, scale, out, stream=None):
+    _need(out, "float32", "out")
     _check(lib().wb_dequantise_e4m3(_p(codes), _p(scale), codes.numel(), _p(out), _stream(stream)))
 
 
