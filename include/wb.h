@@ -281,6 +281,24 @@ WB_API wb_status wb_plan_waves(const wb_model_desc* desc, int32_t n_chunks,
  */
 WB_API wb_status wb_quantise_e4m3(const void* x, int32_t x_is_bf16, int64_t n,
                            uint8_t* codes, float* scale, wb_stream stream);
+/*
+ * Same result as wb_quantise_e4m3 (identical codes and scale) for callers that
+ * cannot allocate device memory: applications whose allocator owns every byte
+ * of device memory, code paths where an implicit synchronisation from
+ * cudaMalloc/cudaFree is not acceptable, or hosts that forbid allocation after
+ * start-up.  The pages have no counterpart to this entry point.
+ * It allocates nothing: its reduction scratch (one partial maximum per block
+ * of 16384 elements) is a fixed 16 KB array in the library's device image,
+ * held by every GPU that loads the library until the process exits.
+ *   n <= 2^26 (67108864) elements; larger n returns WB_ERR_SHAPE.
+ * All calls share that array: calls whose kernels overlap on the GPU (e.g. on
+ * two unordered streams) race; calls ordered on one stream are safe.  The
+ * first call on a device looks the array's address up (cudaGetSymbolAddress);
+ * make that first call before any stream capture.
+ */
+WB_API wb_status wb_quantise_e4m3_static(const void* x, int32_t x_is_bf16, int64_t n,
+                                         uint8_t* codes, float* scale, wb_stream stream);
+
 /* out [dev] float32 [n] = value(codes) * scale[0]. */
 WB_API wb_status wb_dequantise_e4m3(const uint8_t* codes, const float* scale,
                              int64_t n, float* out, wb_stream stream);
