@@ -1,0 +1,63 @@
+"""End-to-end wb_transcribe_batch: chunking, wave packing, mel, encoder,
+cross-K/V, forced prefix, greedy steps replayed through captured CUDA graphs,
+ragged lengths and the token scatter back to request order -- checked against
+the oracle (its own chunking, mel, encoder and teacher-forced decoder)."""
+import numpy as np
+import pytest
+import torch
+
+import whisper_encoder_decoder_log_b300 as wb
+from oracle import mel as omel
+from oracle import model as omodel
+from oracle import plan as oplan
+from synth import TURBO, ModelDims, forced_prefix, sine_chunk_audio
+from tests.gpu_util import GpuModel
+
+pytestmark = pytest.mark.gpu
+
+
+def _requests(lengths_s, seed):
+    samples = np.array([int(s * 16000) for s in lengths_s], np.int64)
+    offs = np.zeros_like(samples)
+    offs[1:] = np.cumsum(samples)[:-1]
+    audio = np.concatenate([sine_chunk_audio(seed + i, int(n)) for i, n in enumerate(samples)])
+    return audio, offs, samples
+
+
+@pytest.mark.parametrize("prec", [wb.PREC_BF16, wb.PREC_MIXED_FP8])
+def test_transcribe_batch_matches_oracle(prec):
+    dims = ModelDims("turbo-2enc", 128, 1280, 20, 5120, 2, 4, TURBO.vocab)
+    m = GpuModel(dims, prec, True, seed=12)
+    audio, offs, samples = _requests([50.0, 70.5, 12.0], seed=40)
+    req, idx, valid = oplan.chunk_table(samples)
+    n = req.size
+    assert n == 6
+    lens = np.array([12, 20, 9, 30, 16, 7], np.int32)
+    prefix = forced_prefix(3, dims.vocab)
+    # a budget that holds about three chunks' decoder state forces several waves
+    budget = 3 * oplan.chunk_state_bytes(dims.d_model, dims.dec_layers, 30)
+    waves = oplan.plan_waves(lens, dims.d_model, dims.dec_layers, budget)
+    assert len(waves) >= 2
+    ws = torch.empty(wb.wb_transcribe_workspace_size(m.h, samples, lens, budget), dtype=torch.uint8, device="cuda")
+    tokens = torch.full((n, 448), -7, dtype=torch.int32, device="cuda")
+    nw = wb.wb_transcribe_batch(m.h, torch.from_numpy(audio).cuda(), offs, samples, prefix, lens, tokens, budget, ws)
+    assert nw == len(waves)
+    tok = tokens.cpu().numpy()
+    chunks, oreq, oidx, ovalid = omel.split_into_chunks(audio, offs, samples)
+    assert np.array_equal(oreq, req) and np.array_equal(ovalid, valid)
+    fp8 = prec == wb.PREC_MIXED_FP8
+    agree, total = 0, 0
+    for c in range(n):
+        L = int(lens[c])
+        assert np.array_equal(tok[c, :4], prefix)
+        assert (tok[c, L:] == -7).all()                      # untouched past the chunk's length
+        assert ((tok[c, :L] >= 0) & (tok[c, :L] < dims.vocab)).all()
+        enc = omodel.encode(omel.log_mel(chunks[c], 128), m.W, dims, fp8=fp8)
+        ref, _ = omodel.decode_teacher_forced(tok[c, :L - 1], enc, m.W, dims, kv_fp8=True, fp8=fp8)
+        pred = omodel.greedy(ref[3:L - 1])
+        agree += int((pred == tok[c, 4:L]).sum())
+        total += L - 4
+    # bf16: at least 99 % of greedy tokens agree; mixed_fp8 is bounded by how
+    # often FP8 rounding itself moves the argmax (about 5 % on random weights)
+    assert agree / total >= (0.99 if prec == wb.PREC_BF16 else 0.9), agree / total
+    m.close()

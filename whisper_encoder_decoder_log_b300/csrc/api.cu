@@ -231,6 +231,8 @@ wb_status make_fp8(wb_model* m, const std::vector<std::string>& names, int64_t r
 // ------------------------------------------------------------------ GEMM helper
 // y = x W^T (+ epilogue) with the model's arithmetic: SIMT fp32 for the fp32
 // model, tcgen05 otherwise (E4M3 when fp8 is given).
+constexpr int64_t kSwapRows = 256;   // GEMMs with at most this many rows use the swapped form
+
 struct Lin {
     const void* a = nullptr;      // activations
     int64_t rows = 0, lda = 0;
@@ -242,7 +244,7 @@ struct Lin {
     bool split = false;           // a holds [hi | lo] bf16 halves: 2K columns, lda >= 2K
 };
 
-wb_status linear(const wb_model* m, const Lin& L, GemmEpi e, cudaStream_t s) {
+wb_status linear_impl(const Lin& L, GemmEpi e, bool simt_fp32, unsigned* err, cudaStream_t s) {
     GemmOperand A;
     A.ptr = L.a;
     A.rows = L.rows;
@@ -254,7 +256,7 @@ wb_status linear(const wb_model* m, const Lin& L, GemmEpi e, cudaStream_t s) {
     B.rows = L.N;
     B.row_stride = L.K;
     if (L.rows <= 0 || L.N <= 0) return WB_OK;
-    if (m->fp32()) return gemm_simt(A, false, B, false, L.N, L.K, e, s);
+    if (simt_fp32) return gemm_simt(A, false, B, false, L.N, L.K, e, s);
     const bool f8 = L.f8 != nullptr;
     if (f8) {
         e.row_scale = L.a_scale;
@@ -264,13 +266,53 @@ wb_status linear(const wb_model* m, const Lin& L, GemmEpi e, cudaStream_t s) {
         if (L.split) return fail(WB_ERR_UNSUPPORTED, "split GEMM needs K % 64 == 0");
         return gemm_simt(A, true, B, true, L.N, L.K, e, s);
     }
+    const int sms = num_sms();
+    const bool linear_f32 = (e.out_type == OUT_F32 || e.out_type == OUT_F32_ACC) && !e.gelu && !e.add &&
+                            e.mode == MODE_PLAIN;
+    const int64_t kb_all = (L.split ? 2 * L.K : L.K) / (f8 ? 128 : 64);
+    if (linear_f32 && L.batches == 1 && L.rows <= kSwapRows && !e.out_batch_rows && !e.out_row_offset) {
+        // few rows: weights as the 128-row MMA operand, rows as the MMA N
+        const int bn = L.rows <= 32 ? 32 : (L.rows <= 64 ? 64 : 128);
+        const int64_t tiles = ((L.N + 127) / 128) * ((L.rows + bn - 1) / bn);
+        int ksplit = 1;
+        const int64_t want = (sms + tiles - 1) / tiles;
+        if (want > 1)
+            for (int64_t d = want; d <= kb_all / 2; ++d)
+                if (kb_all % d == 0) { ksplit = (int)d; break; }
+        if (ksplit > 1 && e.out_type == OUT_F32)
+            WB_CUDA(cudaMemsetAsync(e.out, 0, (size_t)L.rows * e.ldo * sizeof(float), s));
+        GemmPlan p;
+        if (wb_status st = gemm_plan_swap(&p, A, B, L.N, L.split ? 2 * L.K : L.K, f8, bn, L.split ? L.K : 0)) return st;
+        return gemm_run(p, e, err, s, 0, ksplit);
+    }
     const int64_t tiles_m = ((L.rows + 127) / 128) * L.batches;
+    auto tiles = [&](int bn) { return tiles_m * ((L.N + bn - 1) / bn); };
     int bn = 256;
-    if (tiles_m * ((L.N + 255) / 256) < num_sms()) bn = 128;
-    if (tiles_m * ((L.N + 127) / 128) < num_sms()) bn = 64;
+    if (tiles(256) < sms) bn = 128;
+    if (tiles(128) < sms) bn = 64;
+    // split-K applies to linear fp32 epilogues; otherwise narrow the tiles
+    const bool can_split = (e.out_type == OUT_F32 || e.out_type == OUT_F32_ACC) && !e.gelu && !e.add &&
+                           e.mode == MODE_PLAIN;
+    int ksplit = 1;
+    if (tiles(bn) < 2 * sms) {
+        if (can_split) {
+            ksplit = (int)std::min<int64_t>((2 * sms + tiles(bn) - 1) / tiles(bn), std::max<int64_t>(1, kb_all / 4));
+            while (ksplit > 1 && kb_all % ksplit) --ksplit;
+        } else if (tiles(32) <= 4 * sms) {
+            bn = 32;
+        }
+    }
+    if (ksplit > 1 && e.out_type == OUT_F32) {
+        const int64_t obr = e.out_batch_rows ? e.out_batch_rows : L.rows;
+        WB_CUDA(cudaMemsetAsync(e.out, 0, (size_t)(L.batches * obr) * e.ldo * sizeof(float), s));
+    }
     GemmPlan p;
     if (wb_status st = gemm_plan(&p, A, B, L.N, L.split ? 2 * L.K : L.K, f8, bn, L.split ? L.K : 0)) return st;
-    return gemm_run(p, e, m->err, s);
+    return gemm_run(p, e, err, s, 0, ksplit);
+}
+
+wb_status linear(const wb_model* m, const Lin& L, GemmEpi e, cudaStream_t s) {
+    return linear_impl(L, e, m->fp32(), m->err, s);
 }
 
 GemmEpi epi_out(void* out, int64_t ldo, int type, const float* bias, int gelu = 0) {
@@ -287,6 +329,12 @@ GemmEpi epi_out(void* out, int64_t ldo, int type, const float* bias, int gelu = 
 }  // namespace wb
 
 // ------------------------------------------------------------------ decoder state
+struct StepGraph {
+    int64_t rows = 0;
+    cudaGraphExec_t exec = nullptr;
+    int64_t kernels = 0;
+};
+
 struct wb_decoder {
     wb_model* m = nullptr;
     int64_t B = 0;
@@ -294,6 +342,10 @@ struct wb_decoder {
     int32_t* tokens = nullptr;
     int pos = 0;
     int P = 0;
+    int max_len = 0;
+    int* pos_dev = nullptr;            // position of the next step, on the device
+    std::vector<StepGraph> graphs;     // one captured step per active-row bucket
+    cudaStream_t cap_stream = nullptr; // graphs are captured here (capture runs nothing)
     // device buffers carved from the workspace
     void* crosskv = nullptr;
     void* cache = nullptr;
@@ -308,6 +360,7 @@ struct wb_decoder {
     void* attn = nullptr;
     float* cq = nullptr;
     void* f = nullptr;
+    void* f2 = nullptr;
     uint8_t* fq = nullptr;
     float* f_scale = nullptr;
     float* logits = nullptr;
@@ -344,13 +397,16 @@ size_t carve_decoder(const wb_model* m, int64_t B, const int32_t* len, wb_decode
     void* attn = c.take<uint8_t>((size_t)R * d * 4);
     float* cq = c.take<float>((size_t)R * d);
     void* f = c.take<uint8_t>((size_t)R * F * 4);
+    void* f2 = c.take<uint8_t>((size_t)R * F * 4);
     uint8_t* fq = c.take<uint8_t>((size_t)R * F);
     float* f_scale = c.take<float>(R);
     float* logits = c.take<float>((size_t)B * ((m->desc.vocab + 7) / 8 * 8));
+    int* pos_dev = c.take<int>(64);
     if (dec) {
+        dec->pos_dev = pos_dev;
         dec->crosskv = crosskv; dec->cache = cache; dec->kscale = kscale; dec->vscale = vscale;
         dec->off = off; dec->len_dev = lend; dec->h = h; dec->a = a; dec->a_scale = a_scale; dec->qkv = qkv;
-        dec->attn = attn; dec->cq = cq; dec->f = f; dec->fq = fq; dec->f_scale = f_scale; dec->logits = logits;
+        dec->attn = attn; dec->cq = cq; dec->f = f; dec->f2 = f2; dec->fq = fq; dec->f_scale = f_scale; dec->logits = logits;
     }
     if (overflow) *overflow = c.overflow;
     return align_up(c.cur, 256);
@@ -397,7 +453,7 @@ size_t carve_encoder(const wb_model* m, int64_t B, EncBufs* eb, uint8_t* base, s
 // costs no extra HBM traffic and the products keep ~16 mantissa bits of the
 // fp32 activation.  FP8 GEMMs quantise from fp32.
 wb_status decoder_layers(wb_decoder* dec, int64_t n_chunks, int rows_per_chunk, int p0, bool set_scales,
-                         cudaStream_t s) {
+                         cudaStream_t s, const int* pos_dev) {
     wb_model* m = dec->m;
     const int d = m->d(), H = m->H(), F = m->F();
     const int64_t R = n_chunks * rows_per_chunk;
@@ -424,16 +480,18 @@ wb_status decoder_layers(wb_decoder* dec, int64_t n_chunks, int rows_per_chunk, 
         if (kv8 && set_scales)
             if (wb_status st = kv_scales(dec->qkv, n_chunks, rows_per_chunk, d, ks, vs, s)) return st;
         if (wb_status st = kv_append(dec->qkv, n_chunks, rows_per_chunk, p0, d, H, l, kv8, dec->cache, dec->off,
-                                     dec->len_dev, ks, vs, m->err, s))
+                                     dec->len_dev, ks, vs, m->err, s, pos_dev))
             return st;
         {
             KVView kv;
             kv.ptr = dec->cache; kv.chunk_off = dec->off; kv.head_stride = 64; kv.chunk_len = dec->len_dev;
             kv.heads = H; kv.k_blk = 2 * l; kv.v_blk = 2 * l + 1; kv.row_stride = 64;
             if (kv8) { kv.k_scale = ks; kv.v_scale = vs; }
+            if (pos_dev) { kv.pos_dev = pos_dev; kv.active_len = dec->len_dev; }
+            // with a device-side position the score buffer is sized for the longest chunk
+            const int kv_len = pos_dev ? dec->max_len : p0 + rows_per_chunk;
             if (wb_status st = attn_rows(DT_F32, kv8 ? DT_E4M3 : DT_F32, attn_dt, dec->qkv, 3 * d, n_chunks,
-                                         rows_per_chunk, H, kv, p0 + rows_per_chunk, true, p0, dec->attn, lda, s,
-                                         sp ? d : 0))
+                                         rows_per_chunk, H, kv, kv_len, true, p0, dec->attn, lda, s, sp ? d : 0))
                 return st;
         }
         {
@@ -456,6 +514,7 @@ wb_status decoder_layers(wb_decoder* dec, int64_t n_chunks, int rows_per_chunk, 
             kv.ptr = reinterpret_cast<uint8_t*>(dec->crosskv) + (size_t)l * dec->B * 2 * H * kCtx * 64 * act;
             kv.chunk_stride = (int64_t)2 * H * kCtx * 64; kv.head_stride = (int64_t)kCtx * 64; kv.heads = H;
             kv.k_blk = 0; kv.v_blk = 1; kv.row_stride = 64;
+            if (pos_dev) { kv.pos_dev = pos_dev; kv.active_len = dec->len_dev; }
             if (wb_status st = attn_rows(DT_F32, f32 ? DT_F32 : DT_BF16, attn_dt, dec->cq, d, n_chunks, rows_per_chunk,
                                          H, kv, kCtx, false, 0, dec->attn, lda, s, sp ? d : 0))
                 return st;
@@ -469,12 +528,21 @@ wb_status decoder_layers(wb_decoder* dec, int64_t n_chunks, int rows_per_chunk, 
         if (wb_status st = layernorm(dec->h, d, R, d, m->V(nm("dec.", l, "ln3.g")), m->V(nm("dec.", l, "ln3.b")),
                                      f8 ? LN_E4M3 : ln_act, dec->a, f8 ? d : lda, dec->a_scale, s))
             return st;
+        // FC1 (+GELU): with few rows the swapped GEMM writes fp32 and a
+        // post-pass applies GELU (and the bf16 split); otherwise GELU is fused
+        const bool few = R <= kSwapRows && !f32;
         if (f8) {
             Lin L1;
             L1.a = dec->a; L1.rows = R; L1.lda = d; L1.w = m->W(nm("dec.", l, "fc1.w")); L1.N = F; L1.K = d;
             L1.f8 = &m->dec_fc1[l]; L1.a_scale = dec->a_scale;
-            if (wb_status st = linear(m, L1, epi_out(dec->f, F, OUT_F32, m->V(nm("dec.", l, "fc1.b")), 1), s)) return st;
-            if (wb_status st = quant_rows_f32(reinterpret_cast<float*>(dec->f), R, F, dec->fq, dec->f_scale, s)) return st;
+            float* f32buf = reinterpret_cast<float*>(dec->f);
+            if (few) {
+                if (wb_status st = linear(m, L1, epi_out(f32buf, F, OUT_F32, m->V(nm("dec.", l, "fc1.b"))), s)) return st;
+                if (wb_status st = gelu_post(f32buf, R, F, nullptr, s)) return st;
+            } else {
+                if (wb_status st = linear(m, L1, epi_out(f32buf, F, OUT_F32, m->V(nm("dec.", l, "fc1.b")), 1), s)) return st;
+            }
+            if (wb_status st = quant_rows_f32(f32buf, R, F, dec->fq, dec->f_scale, s)) return st;
             Lin L2;
             L2.a = dec->fq; L2.rows = R; L2.lda = F; L2.w = m->W(nm("dec.", l, "fc2.w")); L2.N = d; L2.K = F;
             L2.f8 = &m->dec_fc2[l]; L2.a_scale = dec->f_scale;
@@ -482,11 +550,18 @@ wb_status decoder_layers(wb_decoder* dec, int64_t n_chunks, int rows_per_chunk, 
         } else {
             Lin L1;
             L1.a = dec->a; L1.rows = R; L1.lda = lda; L1.split = sp; L1.w = m->W(nm("dec.", l, "fc1.w")); L1.N = F; L1.K = d;
-            const int fout = f32 ? OUT_F32 : OUT_BF16X2;
             const int64_t ldf = sp ? 2 * F : F;
-            if (wb_status st = linear(m, L1, epi_out(dec->f, ldf, fout, m->V(nm("dec.", l, "fc1.b")), 1), s)) return st;
+            void* fin = f32 ? dec->f : dec->f2;
+            if (few) {
+                float* f32buf = reinterpret_cast<float*>(dec->f);
+                if (wb_status st = linear(m, L1, epi_out(f32buf, F, OUT_F32, m->V(nm("dec.", l, "fc1.b"))), s)) return st;
+                if (wb_status st = gelu_post(f32buf, R, F, dec->f2, s)) return st;
+            } else {
+                const int fout = f32 ? OUT_F32 : OUT_BF16X2;
+                if (wb_status st = linear(m, L1, epi_out(fin, ldf, fout, m->V(nm("dec.", l, "fc1.b")), 1), s)) return st;
+            }
             Lin L2;
-            L2.a = dec->f; L2.rows = R; L2.lda = ldf; L2.split = sp; L2.w = m->W(nm("dec.", l, "fc2.w")); L2.N = d; L2.K = F;
+            L2.a = fin; L2.rows = R; L2.lda = ldf; L2.split = sp; L2.w = m->W(nm("dec.", l, "fc2.w")); L2.N = d; L2.K = F;
             if (wb_status st = linear(m, L2, epi_out(dec->h, d, OUT_F32_ACC, m->V(nm("dec.", l, "fc2.b"))), s)) return st;
         }
     }
@@ -495,7 +570,7 @@ wb_status decoder_layers(wb_decoder* dec, int64_t n_chunks, int rows_per_chunk, 
 
 // Final LayerNorm, logits = LN(h) E^T, greedy token into column pos+1.
 wb_status decoder_head(wb_decoder* dec, int64_t n_chunks, int rows_per_chunk, int pos_last, float* logits_all,
-                       cudaStream_t s) {
+                       cudaStream_t s, const int* pos_dev) {
     wb_model* m = dec->m;
     const int d = m->d(), V = m->desc.vocab;
     const bool sp = !m->fp32();
@@ -511,7 +586,7 @@ wb_status decoder_head(wb_decoder* dec, int64_t n_chunks, int rows_per_chunk, in
         L.a = dec->a; L.rows = R;
         if (wb_status st = linear(m, L, epi_out(logits_all, V, OUT_F32, nullptr), s)) return st;
         return argmax_tokens(logits_all + (int64_t)(rows_per_chunk - 1) * V, (int64_t)rows_per_chunk * V, n_chunks, V,
-                             dec->tokens, dec->len_dev, nullptr, pos_last, s);
+                             dec->tokens, dec->len_dev, pos_dev, pos_last, s);
     }
     // only the last row of each chunk matters
     if (wb_status st = layernorm(dec->h + (int64_t)(rows_per_chunk - 1) * d, (int64_t)rows_per_chunk * d, n_chunks, d,
@@ -520,7 +595,7 @@ wb_status decoder_head(wb_decoder* dec, int64_t n_chunks, int rows_per_chunk, in
     L.a = dec->a; L.rows = n_chunks;
     const int64_t ldl = (V + 7) / 8 * 8;
     if (wb_status st = linear(m, L, epi_out(dec->logits, ldl, OUT_F32, nullptr), s)) return st;
-    return argmax_tokens(dec->logits, ldl, n_chunks, V, dec->tokens, dec->len_dev, nullptr, pos_last, s);
+    return argmax_tokens(dec->logits, ldl, n_chunks, V, dec->tokens, dec->len_dev, pos_dev, pos_last, s);
 }
 
 __global__ void gather_chunks_kernel(const float* __restrict__ audio, const int64_t* __restrict__ src,
@@ -800,6 +875,7 @@ wb_status wb_decoder_init(wb_model* m, int64_t B, const int32_t* len, const void
     dec->B = B;
     dec->len.assign(len, len + B);
     dec->tokens = tokens;
+    dec->max_len = len[0];
     bool over = false;
     carve_decoder(m, B, len, dec, reinterpret_cast<uint8_t*>(workspace), ws_bytes, &over);
     if (over) {
@@ -844,11 +920,30 @@ wb_status wb_decode_prefix(wb_decoder* dec, int32_t P, float* logits, wb_stream 
     if (wb_status st = embed(dec->tokens, R, P, 0, m->d(), m->W("dec.tok"), m->W("dec.pos"), !m->fp32(),
                              m->desc.vocab, dec->h, m->err, s))
         return st;
-    if (wb_status st = decoder_layers(dec, dec->B, P, 0, true, s)) return st;
-    if (wb_status st = decoder_head(dec, dec->B, P, P - 1, logits, s)) return st;
+    if (wb_status st = decoder_layers(dec, dec->B, P, 0, true, s, nullptr)) return st;
+    if (wb_status st = decoder_head(dec, dec->B, P, P - 1, logits, s, nullptr)) return st;
+    if (wb_status st = set_pos(dec->pos_dev, P, false, s)) return st;
     dec->P = P;
     dec->pos = P;
     return WB_OK;
+}
+
+// One decode step over the first `rows` chunks; every position-dependent
+// kernel reads the position from dec->pos_dev, and chunks that have finished
+// are skipped on the device, so the same launch sequence serves every step.
+static wb_status run_step(wb_decoder* dec, int64_t rows, float* logits, cudaStream_t s) {
+    wb_model* m = dec->m;
+    if (wb_status st = embed(dec->tokens, rows, 1, dec->pos, m->d(), m->W("dec.tok"), m->W("dec.pos"), !m->fp32(),
+                             m->desc.vocab, dec->h, m->err, s, dec->pos_dev, dec->len_dev))
+        return st;
+    if (wb_status st = decoder_layers(dec, rows, 1, dec->pos, false, s, dec->pos_dev)) return st;
+    if (wb_status st = decoder_head(dec, rows, 1, dec->pos, logits, s, dec->pos_dev)) return st;
+    return set_pos(dec->pos_dev, 1, true, s);
+}
+
+static bool graphs_enabled() {
+    const char* e = getenv("WB_NO_GRAPHS");
+    return !(e && e[0] == '1');
 }
 
 wb_status wb_decode_step(wb_decoder* dec, int64_t n_active, float* logits, wb_stream stream) {
@@ -859,12 +954,43 @@ wb_status wb_decode_step(wb_decoder* dec, int64_t n_active, float* logits, wb_st
         return fail(WB_ERR_SHAPE, "wb_decode_step: an active chunk has reached its length");
     if (logits && !aligned16(logits)) return fail(WB_ERR_ALIGN, "wb_decode_step: logits alignment");
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    wb_model* m = dec->m;
-    if (wb_status st = embed(dec->tokens, n_active, 1, dec->pos, m->d(), m->W("dec.tok"), m->W("dec.pos"), !m->fp32(),
-                             m->desc.vocab, dec->h, m->err, s))
-        return st;
-    if (wb_status st = decoder_layers(dec, n_active, 1, dec->pos, false, s)) return st;
-    if (wb_status st = decoder_head(dec, n_active, 1, dec->pos, logits, s)) return st;
+    // logits for the caller, or per-kernel timing: launch directly with exactly n_active rows
+    if (logits || !graphs_enabled() || prof_any_active()) {
+        if (wb_status st = run_step(dec, n_active, logits, s)) return st;
+        dec->pos += 1;
+        return WB_OK;
+    }
+    // graph replay: rows rounded up to a 128-row bucket (finished chunks are masked)
+    const int64_t rows = std::min<int64_t>(dec->B, (n_active + 127) / 128 * 128);
+    StepGraph* g = nullptr;
+    for (auto& x : dec->graphs)
+        if (x.rows == rows) g = &x;
+    if (!g) {
+        StepGraph ng;
+        ng.rows = rows;
+        const int64_t k0 = wb_launch_count();
+        // the caller's stream may be the legacy default stream, which cannot be
+        // captured: record on a private stream, replay on the caller's
+        if (!dec->cap_stream) WB_CUDA(cudaStreamCreateWithFlags(&dec->cap_stream, cudaStreamNonBlocking));
+        WB_CUDA(cudaStreamBeginCapture(dec->cap_stream, cudaStreamCaptureModeThreadLocal));
+        wb_status st = run_step(dec, rows, nullptr, dec->cap_stream);
+        cudaGraph_t graph = nullptr;
+        const cudaError_t ce = cudaStreamEndCapture(dec->cap_stream, &graph);
+        if (st) {
+            if (graph) cudaGraphDestroy(graph);
+            return st;
+        }
+        if (ce != cudaSuccess) return cuda_fail(ce, "cudaStreamEndCapture(decode step)");
+        const cudaError_t ie = cudaGraphInstantiate(&ng.exec, graph, 0);
+        cudaGraphDestroy(graph);
+        if (ie != cudaSuccess) return cuda_fail(ie, "cudaGraphInstantiate(decode step)");
+        ng.kernels = wb_launch_count() - k0;
+        count_launch((int)-ng.kernels);    // captured, not launched
+        dec->graphs.push_back(ng);
+        g = &dec->graphs.back();
+    }
+    WB_CUDA(cudaGraphLaunch(g->exec, s));
+    count_launch((int)g->kernels);
     dec->pos += 1;
     return WB_OK;
 }
@@ -873,6 +999,9 @@ int32_t wb_decoder_position(const wb_decoder* dec) { return dec ? dec->pos : -1;
 
 wb_status wb_decoder_destroy(wb_decoder* dec) {
     if (!dec) return fail(WB_ERR_INVALID_ARG, "wb_decoder_destroy: null decoder");
+    for (auto& g : dec->graphs)
+        if (g.exec) cudaGraphExecDestroy(g.exec);
+    if (dec->cap_stream) cudaStreamDestroy(dec->cap_stream);
     delete dec;
     return WB_OK;
 }
@@ -1084,24 +1213,22 @@ wb_status wb_gemm(const void* A, const void* Bw, int64_t M, int64_t N, int64_t K
     if (K % (ab_type ? 128 : 64)) return fail(WB_ERR_SHAPE, "wb_gemm: K must be a multiple of 64 (bf16) / 128 (E4M3)");
     unsigned* err = lib_error_word();
     if (!err) return fail(WB_ERR_CUDA, "wb_gemm: no error word");
-    GemmOperand a;
-    a.ptr = A; a.rows = M; a.row_stride = K;
-    GemmOperand b;
-    b.ptr = Bw; b.rows = N; b.row_stride = K;
-    const int64_t tiles_m = (M + 127) / 128;
-    int bn = 256;
-    if (tiles_m * ((N + 255) / 256) < num_sms()) bn = 128;
-    if (tiles_m * ((N + 127) / 128) < num_sms()) bn = 64;
-    GemmPlan p;
-    if (wb_status st = gemm_plan(&p, a, b, N, K, ab_type == 1, bn)) return st;
+    Lin L;
+    L.a = A; L.rows = M; L.lda = K; L.w = Bw; L.N = N; L.K = K;
+    FP8Weight f8w;
+    if (ab_type == 1) {
+        f8w.w = reinterpret_cast<uint8_t*>(const_cast<void*>(Bw));
+        f8w.col_scale = const_cast<float*>(col_scale);
+        L.f8 = &f8w;
+        L.a_scale = row_scale;
+    }
     GemmEpi e;
     e.out = C;
     e.ldo = N;
     e.out_type = c_bf16 ? OUT_BF16 : OUT_F32;
     e.bias = bias;
     e.gelu = gelu;
-    if (ab_type == 1) { e.row_scale = row_scale; e.col_scale = col_scale; }
-    return gemm_run(p, e, err, reinterpret_cast<cudaStream_t>(stream));
+    return linear_impl(L, e, false, err, reinterpret_cast<cudaStream_t>(stream));
 }
 
 wb_status wb_sync_status(wb_model* m, wb_stream stream) {

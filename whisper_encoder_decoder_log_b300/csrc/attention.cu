@@ -209,20 +209,47 @@ flash_enc_kernel(const __nv_bfloat16* __restrict__ qkv, int d, int S, __nv_bfloa
 
 // ------------------------------------------------------------------ row attention
 constexpr int kRowThreads = 256;
-constexpr int kQGroup = 4;
+constexpr int kGroups = kRowThreads / 8;    // key rows handled per pass (8 lanes per row)
+constexpr int kUnroll = 4;                  // independent 16-byte loads in flight per thread
+
+// Streaming 16-byte load that does not allocate in L1 (every byte is read once).
+WB_DEV uint4 ld_stream(const void* p) {
+    uint4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
+    return r;
+}
+WB_DEV uint2 ld_stream8(const void* p) {
+    uint2 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];" : "=r"(r.x), "=r"(r.y) : "l"(p));
+    return r;
+}
+
+// Raw bytes of the 8 elements a lane owns in one key/value row.
+template <typename T>
+struct Raw8 { uint4 a, b; };
+template <typename T>
+WB_DEV Raw8<T> load_raw8(const T* p);
+template <>
+WB_DEV Raw8<float> load_raw8<float>(const float* p) { return {ld_stream(p), ld_stream(p + 4)}; }
+template <>
+WB_DEV Raw8<__nv_bfloat16> load_raw8<__nv_bfloat16>(const __nv_bfloat16* p) { return {ld_stream(p), make_uint4(0, 0, 0, 0)}; }
+template <>
+WB_DEV Raw8<uint8_t> load_raw8<uint8_t>(const uint8_t* p) {
+    const uint2 v = ld_stream8(p);
+    return {make_uint4(v.x, v.y, 0, 0), make_uint4(0, 0, 0, 0)};
+}
 
 template <typename T>
-WB_DEV void load8(const T* p, float (&v)[8]);
+WB_DEV void unpack8(const Raw8<T>& r, float (&v)[8]);
 template <>
-WB_DEV void load8<float>(const float* p, float (&v)[8]) {
-    const float4 a = *reinterpret_cast<const float4*>(p);
-    const float4 b = *reinterpret_cast<const float4*>(p + 4);
-    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+WB_DEV void unpack8<float>(const Raw8<float>& r, float (&v)[8]) {
+    v[0] = __uint_as_float(r.a.x); v[1] = __uint_as_float(r.a.y); v[2] = __uint_as_float(r.a.z); v[3] = __uint_as_float(r.a.w);
+    v[4] = __uint_as_float(r.b.x); v[5] = __uint_as_float(r.b.y); v[6] = __uint_as_float(r.b.z); v[7] = __uint_as_float(r.b.w);
 }
 template <>
-WB_DEV void load8<__nv_bfloat16>(const __nv_bfloat16* p, float (&v)[8]) {
-    const uint4 a = *reinterpret_cast<const uint4*>(p);
-    const uint32_t w[4] = {a.x, a.y, a.z, a.w};
+WB_DEV void unpack8<__nv_bfloat16>(const Raw8<__nv_bfloat16>& r, float (&v)[8]) {
+    const uint32_t w[4] = {r.a.x, r.a.y, r.a.z, r.a.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         v[2 * i] = __uint_as_float(w[i] << 16);
@@ -230,9 +257,8 @@ WB_DEV void load8<__nv_bfloat16>(const __nv_bfloat16* p, float (&v)[8]) {
     }
 }
 template <>
-WB_DEV void load8<uint8_t>(const uint8_t* p, float (&v)[8]) {
-    const uint2 a = *reinterpret_cast<const uint2*>(p);
-    const uint32_t w[2] = {a.x, a.y};
+WB_DEV void unpack8<uint8_t>(const Raw8<uint8_t>& r, float (&v)[8]) {
+    const uint32_t w[2] = {r.a.x, r.a.y};
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
         __nv_fp8x4_e4m3 q;
@@ -242,30 +268,33 @@ WB_DEV void load8<uint8_t>(const uint8_t* p, float (&v)[8]) {
     }
 }
 
-template <typename TQ, typename TKV, typename TO>
+template <int NQ, typename TQ, typename TKV, typename TO>
 __global__ void __launch_bounds__(kRowThreads)
 attn_rows_kernel(const TQ* __restrict__ q, int64_t q_ld, int rows_per_chunk, int n_rows_total,
                  KVView kv, int kv_len, int causal, int q_pos0, TO* __restrict__ out, int64_t o_ld,
                  int64_t o_split) {
-    // scores for up to 4 query rows over up to kMaxKeys keys
+    // scores for up to NQ query rows over up to kv_len keys
     extern __shared__ float sm[];
-    float* sq = sm;                              // [4][64]
-    float* ss = sq + kQGroup * 64;               // [4][kv_len]
-    float* sred = ss + kQGroup * kv_len;         // [32][4][64] partial outputs, reused for maxima
+    float* sq = sm;                              // [NQ][64], pre-scaled by 1/8
+    float* ss = sq + NQ * 64;                    // [NQ][kv_len]
+    float* sred = ss + NQ * kv_len;              // [kGroups][NQ][64] partial outputs
     const int64_t chunk = blockIdx.x;
     const int h = blockIdx.y;
     const int tid = threadIdx.x;
-    const int r_first = blockIdx.z * kQGroup;
-    const int nq = min(kQGroup, rows_per_chunk - r_first);
+    const int r_first = blockIdx.z * NQ;
+    const int nq = min(NQ, rows_per_chunk - r_first);
     if (nq <= 0) return;
     const int64_t row0 = chunk * rows_per_chunk + r_first;
     if (row0 >= n_rows_total) return;
+    if (kv.pos_dev) {
+        q_pos0 = *kv.pos_dev;
+        if (kv.active_len && kv.active_len[chunk] <= q_pos0 + 1) return;   // finished chunk
+    }
 
-    for (int i = tid; i < kQGroup * 64; i += kRowThreads) {
+    for (int i = tid; i < NQ * 64; i += kRowThreads) {
         const int qi = i / 64, c = i % 64;
         sq[i] = qi < nq ? (float)q[(row0 + qi) * q_ld + h * 64 + c] * 0.125f : 0.f;
     }
-    // key range
     const int64_t cb = kv.chunk_off ? kv.chunk_off[chunk] : chunk * kv.chunk_stride;
     const int64_t hs = kv.head_stride * (kv.chunk_len ? (int64_t)kv.chunk_len[chunk] : 1);
     const TKV* Kp = reinterpret_cast<const TKV*>(kv.ptr) + cb + ((int64_t)kv.k_blk * kv.heads + h) * hs;
@@ -276,42 +305,51 @@ attn_rows_kernel(const TQ* __restrict__ q, int64_t q_ld, int rows_per_chunk, int
     if (causal) nk = min(kv_len, q_pos0 + r_first + nq);
     __syncthreads();
 
-    // phase 1: scores, 8 lanes per key row (8 elements each); the trip count
-    // is uniform per warp so the 8-lane shuffles always see full warps
     const int sub = tid & 7;
     const int grp = tid >> 3;
-    for (int jb = 0; jb < nk; jb += kRowThreads / 8) {
-        const int j0 = jb + grp;
-        const bool valid = j0 < nk;
-        float kf[8];
-        if (valid) load8<TKV>(Kp + (int64_t)j0 * kv.row_stride + sub * 8, kf);
-        else {
+    float qv[NQ][8];
 #pragma unroll
-            for (int c = 0; c < 8; ++c) kf[c] = 0.f;
-        }
-        float acc[kQGroup];
+    for (int qi = 0; qi < NQ; ++qi)
 #pragma unroll
-        for (int qi = 0; qi < kQGroup; ++qi) {
-            float a = 0.f;
+        for (int c = 0; c < 8; ++c) qv[qi][c] = sq[qi * 64 + sub * 8 + c];
+
+    // phase 1: scores.  Trip count is uniform per warp (the 8-lane shuffles
+    // need full warps); kUnroll rows are loaded before any is used.
+    for (int jb = 0; jb < nk; jb += kGroups * kUnroll) {
+        Raw8<TKV> raw[kUnroll];
 #pragma unroll
-            for (int c = 0; c < 8; ++c) a = fmaf(sq[qi * 64 + sub * 8 + c], kf[c], a);
-            acc[qi] = a;
+        for (int u = 0; u < kUnroll; ++u) {
+            const int j = jb + u * kGroups + grp;
+            raw[u] = j < nk ? load_raw8<TKV>(Kp + (int64_t)j * kv.row_stride + sub * 8) : Raw8<TKV>{};
         }
 #pragma unroll
-        for (int qi = 0; qi < kQGroup; ++qi) {
-            acc[qi] += __shfl_xor_sync(0xffffffffu, acc[qi], 1);
-            acc[qi] += __shfl_xor_sync(0xffffffffu, acc[qi], 2);
-            acc[qi] += __shfl_xor_sync(0xffffffffu, acc[qi], 4);
-        }
-        if (valid && sub < nq) {
-            const int qi = sub;
-            float v = acc[0];
-            if (qi == 1) v = acc[1];
-            if (qi == 2) v = acc[2];
-            if (qi == 3) v = acc[3];
-            v *= ks;
-            if (causal && j0 > q_pos0 + r_first + qi) v = -INFINITY;
-            ss[qi * kv_len + j0] = v;
+        for (int u = 0; u < kUnroll; ++u) {
+            const int j = jb + u * kGroups + grp;
+            float kf[8];
+            unpack8<TKV>(raw[u], kf);
+            float acc[NQ];
+#pragma unroll
+            for (int qi = 0; qi < NQ; ++qi) {
+                float a = 0.f;
+#pragma unroll
+                for (int c = 0; c < 8; ++c) a = fmaf(qv[qi][c], kf[c], a);
+                acc[qi] = a;
+            }
+#pragma unroll
+            for (int qi = 0; qi < NQ; ++qi) {
+                acc[qi] += __shfl_xor_sync(0xffffffffu, acc[qi], 1);
+                acc[qi] += __shfl_xor_sync(0xffffffffu, acc[qi], 2);
+                acc[qi] += __shfl_xor_sync(0xffffffffu, acc[qi], 4);
+            }
+            if (j < nk && sub < nq) {
+                float v = acc[0];
+#pragma unroll
+                for (int qi = 1; qi < NQ; ++qi)
+                    if (sub == qi) v = acc[qi];
+                v *= ks;
+                if (causal && j > q_pos0 + r_first + sub) v = -INFINITY;
+                ss[sub * kv_len + j] = v;
+            }
         }
     }
     __syncthreads();
@@ -324,7 +362,7 @@ attn_rows_kernel(const TQ* __restrict__ q, int64_t q_ld, int rows_per_chunk, int
         m = warp_max(m);
         float sum = 0.f;
         for (int j = lane; j < nk; j += 32) {
-            const float e = __expf(sr[j] - m);   // fast exp: inputs <= 0, error ~2 ulp
+            const float e = __expf(sr[j] - m);   // inputs <= 0
             sr[j] = e;
             sum += e;
         }
@@ -333,33 +371,44 @@ attn_rows_kernel(const TQ* __restrict__ q, int64_t q_ld, int rows_per_chunk, int
         for (int j = lane; j < nk; j += 32) sr[j] *= inv;
     }
     __syncthreads();
-    // phase 2: o = p . V ; thread (row group rg = tid/8, dims 8*sub..)
-    const int rg = tid >> 3;
-    float o[kQGroup][8];
+    // phase 2: o = p . V ; thread (group grp, dims 8*sub..) over keys j = grp mod kGroups
+    float o[NQ][8];
 #pragma unroll
-    for (int qi = 0; qi < kQGroup; ++qi)
+    for (int qi = 0; qi < NQ; ++qi)
 #pragma unroll
         for (int c = 0; c < 8; ++c) o[qi][c] = 0.f;
-    for (int j = rg; j < nk; j += kRowThreads / 8) {
-        float vf[8];
-        load8<TKV>(Vp + (int64_t)j * kv.row_stride + sub * 8, vf);
+    for (int jb = 0; jb < nk; jb += kGroups * kUnroll) {
+        Raw8<TKV> raw[kUnroll];
 #pragma unroll
-        for (int qi = 0; qi < kQGroup; ++qi) {
-            const float p = ss[qi * kv_len + j];
+        for (int u = 0; u < kUnroll; ++u) {
+            const int j = jb + u * kGroups + grp;
+            raw[u] = j < nk ? load_raw8<TKV>(Vp + (int64_t)j * kv.row_stride + sub * 8) : Raw8<TKV>{};
+        }
 #pragma unroll
-            for (int c = 0; c < 8; ++c) o[qi][c] = fmaf(p, vf[c], o[qi][c]);
+        for (int u = 0; u < kUnroll; ++u) {
+            const int j = jb + u * kGroups + grp;
+            if (j < nk) {
+                float vf[8];
+                unpack8<TKV>(raw[u], vf);
+#pragma unroll
+                for (int qi = 0; qi < NQ; ++qi) {
+                    const float p = ss[qi * kv_len + j];
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) o[qi][c] = fmaf(p, vf[c], o[qi][c]);
+                }
+            }
         }
     }
-    // reduce the 32 row groups
+    // reduce the kGroups row groups
 #pragma unroll
-    for (int qi = 0; qi < kQGroup; ++qi)
+    for (int qi = 0; qi < NQ; ++qi)
 #pragma unroll
-        for (int c = 0; c < 8; ++c) sred[(rg * kQGroup + qi) * 64 + sub * 8 + c] = o[qi][c];
+        for (int c = 0; c < 8; ++c) sred[(grp * NQ + qi) * 64 + sub * 8 + c] = o[qi][c];
     __syncthreads();
     for (int i = tid; i < nq * 64; i += kRowThreads) {
         const int qi = i / 64, c = i % 64;
         float a = 0.f;
-        for (int g = 0; g < kRowThreads / 8; ++g) a += sred[(g * kQGroup + qi) * 64 + c];
+        for (int g = 0; g < kGroups; ++g) a += sred[(g * NQ + qi) * 64 + c];
         a *= vs;
         const TO hi = (TO)a;
         out[(row0 + qi) * o_ld + h * 64 + c] = hi;
@@ -367,24 +416,24 @@ attn_rows_kernel(const TQ* __restrict__ q, int64_t q_ld, int rows_per_chunk, int
     }
 }
 
-template <typename TQ, typename TKV, typename TO>
-wb_status launch_rows(const void* q, int64_t q_ld, int64_t n_chunks, int rows_per_chunk, int heads,
-                      const KVView& kv, int kv_len, bool causal, int q_pos0, void* out, int64_t o_ld,
-                      cudaStream_t s, int64_t o_split) {
-    const size_t smem = sizeof(float) * (kQGroup * 64 + kQGroup * (size_t)kv_len + 32 * kQGroup * 64);
+template <int NQ, typename TQ, typename TKV, typename TO>
+wb_status launch_rows_nq(const void* q, int64_t q_ld, int64_t n_chunks, int rows_per_chunk, int heads,
+                         const KVView& kv, int kv_len, bool causal, int q_pos0, void* out, int64_t o_ld,
+                         cudaStream_t s, int64_t o_split) {
+    const size_t smem = sizeof(float) * (NQ * 64 + NQ * (size_t)kv_len + (size_t)kGroups * NQ * 64);
     static bool attr[64] = {};
     int dev = 0;
     WB_CUDA(cudaGetDevice(&dev));
     if (!attr[dev & 63]) {
-        WB_CUDA(cudaFuncSetAttribute(attn_rows_kernel<TQ, TKV, TO>,
+        WB_CUDA(cudaFuncSetAttribute(attn_rows_kernel<NQ, TQ, TKV, TO>,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024));
         attr[dev & 63] = true;
     }
     if (smem > 200 * 1024) return fail(WB_ERR_SHAPE, "attention key length too large");
-    dim3 grid((unsigned)n_chunks, (unsigned)heads, (unsigned)((rows_per_chunk + kQGroup - 1) / kQGroup));
+    dim3 grid((unsigned)n_chunks, (unsigned)heads, (unsigned)((rows_per_chunk + NQ - 1) / NQ));
     const int kind = causal ? WB_KERNEL_SELF_ATTN : WB_KERNEL_CROSS_ATTN;
     const int slot = prof_begin(kind, s);
-    attn_rows_kernel<TQ, TKV, TO><<<grid, kRowThreads, smem, s>>>(
+    attn_rows_kernel<NQ, TQ, TKV, TO><<<grid, kRowThreads, smem, s>>>(
         reinterpret_cast<const TQ*>(q), q_ld, rows_per_chunk, (int)(n_chunks * rows_per_chunk), kv, kv_len,
         causal ? 1 : 0, q_pos0, reinterpret_cast<TO*>(out), o_ld, o_split);
     count_launch();
@@ -397,6 +446,17 @@ wb_status launch_rows(const void* q, int64_t q_ld, int64_t n_chunks, int rows_pe
     }
     WB_CUDA(cudaGetLastError());
     return WB_OK;
+}
+
+template <typename TQ, typename TKV, typename TO>
+wb_status launch_rows(const void* q, int64_t q_ld, int64_t n_chunks, int rows_per_chunk, int heads,
+                      const KVView& kv, int kv_len, bool causal, int q_pos0, void* out, int64_t o_ld,
+                      cudaStream_t s, int64_t o_split) {
+    if (rows_per_chunk == 1)
+        return launch_rows_nq<1, TQ, TKV, TO>(q, q_ld, n_chunks, rows_per_chunk, heads, kv, kv_len, causal, q_pos0,
+                                              out, o_ld, s, o_split);
+    return launch_rows_nq<4, TQ, TKV, TO>(q, q_ld, n_chunks, rows_per_chunk, heads, kv, kv_len, causal, q_pos0, out,
+                                          o_ld, s, o_split);
 }
 
 }  // namespace

@@ -27,6 +27,11 @@ struct KVView {
     int64_t row_stride = 64;
     const float* k_scale = nullptr;
     const float* v_scale = nullptr;
+    // Graph replay: when pos_dev is set, the first query row of each chunk
+    // sits at position *pos_dev (overrides q_pos0), and a chunk c with
+    // active_len[c] <= *pos_dev + 1 has finished and is skipped.
+    const int* pos_dev = nullptr;
+    const int32_t* active_len = nullptr;
 };
 
 // Encoder self-attention, bf16: qkv [n_chunks*1500, 3d] -> out [n_chunks*1500, d].

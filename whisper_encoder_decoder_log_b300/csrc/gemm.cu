@@ -48,12 +48,15 @@ struct GemmArgs {
     int64_t batches;
     int64_t N, K;
     int64_t mt_per_batch, mt_total, nt_total, tiles;
-    int kblocks;
+    int kblocks;            // k-blocks per split
+    int ksplit;             // K partitions; > 1 adds partial tiles atomically
+    int stages;             // smem ring depth (<= the compile-time maximum)
     int b_kwrap;
     GemmEpi epi;
 };
 
 __device__ __forceinline__ void tile_coords(const GemmArgs& a, int64_t t, int64_t& mt, int64_t& nt) {
+    t /= a.ksplit;
     const int64_t group = (int64_t)kGroupM * a.nt_total;
     const int64_t gid = t / group;
     const int64_t first_m = gid * kGroupM;
@@ -64,11 +67,34 @@ __device__ __forceinline__ void tile_coords(const GemmArgs& a, int64_t t, int64_
 }
 
 __device__ __forceinline__ void store_chunk(const GemmArgs& a, int64_t b, int64_t r, int64_t n0,
-                                            float (&v)[32]) {
+                                            float (&v)[32], int ks) {
     const GemmEpi& e = a.epi;
     const int64_t N = a.N;
     const bool full = n0 + 32 <= N;
     const bool vec = full && e.vec;
+    if (a.ksplit > 1) {
+        // split-K partial tile: fp32 output (zeroed beforehand unless it is a
+        // residual), bias from the first split only, no nonlinearity
+        const float rs = e.row_scale ? e.row_scale[b * a.rows + r] : 1.f;
+        const int64_t obr = e.out_batch_rows ? e.out_batch_rows : a.rows;
+        float* dst = reinterpret_cast<float*>(e.out) + (b * obr + e.out_row_offset + r) * e.ldo + n0;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            if (!full && n0 + j >= N) continue;
+            float x = v[j];
+            if (e.row_scale || e.col_scale) x *= rs * (e.col_scale ? e.col_scale[n0 + j] : 1.f);
+            if (e.bias && ks == 0) x += e.bias[n0 + j];
+            v[j] = x;
+        }
+        if (vec) {
+            float4* d4 = reinterpret_cast<float4*>(dst);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) atomicAdd(d4 + q, make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]));
+        } else {
+            for (int j = 0; j < 32 && n0 + j < N; ++j) atomicAdd(dst + j, v[j]);
+        }
+        return;
+    }
     // scale, bias, GELU, positional table
     if (e.row_scale || e.col_scale) {
         const float rs = e.row_scale ? e.row_scale[b * a.rows + r] : 1.f;
@@ -162,12 +188,34 @@ __device__ __forceinline__ void store_chunk(const GemmArgs& a, int64_t b, int64_
     }
 }
 
-template <int BN, bool FP8>
-__global__ void __launch_bounds__(192, 1)
+// Swapped operands (small M): TMEM lane = output feature n, column = row m.
+// One call stores 32 rows m0 .. m0+31 of feature n; lanes of a warp hold
+// consecutive n, so every store instruction is coalesced.
+__device__ __forceinline__ void store_swap(const GemmArgs& a, int64_t n, int64_t m0, const uint32_t (&raw)[32],
+                                           int ks) {
+    const GemmEpi& e = a.epi;
+    if (n >= a.N) return;
+    const float cs = e.col_scale ? e.col_scale[n] : 1.f;
+    const float bias = (e.bias && ks == 0) ? e.bias[n] : 0.f;
+    float* out = reinterpret_cast<float*>(e.out);
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+        const int64_t m = m0 + j;
+        if (m >= a.rows) break;
+        const float rs = e.row_scale ? e.row_scale[m] : 1.f;
+        const float v = __uint_as_float(raw[j]) * rs * cs + bias;
+        float* dst = out + m * e.ldo + n;
+        if (a.ksplit > 1 || e.out_type == OUT_F32_ACC) atomicAdd(dst, v);   // result unused: a reduction
+        else *dst = v;
+    }
+}
+
+template <int BN, bool FP8, bool SWAP>
+__global__ void __launch_bounds__(192)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUtensorMap tma_b,
                const GemmArgs args, unsigned* err) {
     using C = Cfg<BN>;
-    constexpr int STAGES = C::STAGES;
+    const int STAGES = args.stages;
     constexpr uint32_t IDESC = UmmaIdesc<kBM, BN, FP8 ? 0 : 1>::value;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>(
@@ -221,7 +269,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant_
                 const int b = (int)(mt / args.mt_per_batch);
                 const int r0 = (int)((mt % args.mt_per_batch) * kBM);
                 const int n0 = (int)(nt * BN);
-                for (int kb = 0; kb < args.kblocks; ++kb) {
+                const int kb0 = (int)(t % args.ksplit) * args.kblocks;
+                for (int kb = kb0; kb < kb0 + args.kblocks; ++kb) {
                     bool got = false;
                     for (WaitClock clk; !clk.expired();) {
                         if (mbar_try_wait(&empty_bar[stage], phase ^ 1)) { got = true; break; }
@@ -237,9 +286,16 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant_
                     unsigned char* sb = sa + C::A_BYTES;
                     mbar_arrive_expect_tx(&full_bar[stage], C::STAGE_BYTES);
                     const int kx = kb * (FP8 ? 128 : 64);
-                    const int kxb = args.b_kwrap ? kx % args.b_kwrap : kx;
-                    tma_load_3d(sa, &tma_a, &full_bar[stage], kx, r0, b);
-                    tma_load_2d(sb, &tma_b, &full_bar[stage], kxb, n0);
+                    if (SWAP) {
+                        // A: 128 weight rows (k wraps onto the weights), B: BN activation rows
+                        const int kxa = args.b_kwrap ? kx % args.b_kwrap : kx;
+                        tma_load_3d(sa, &tma_a, &full_bar[stage], kxa, (int)(mt * kBM), 0);
+                        tma_load_2d(sb, &tma_b, &full_bar[stage], kx, n0);
+                    } else {
+                        const int kxb = args.b_kwrap ? kx % args.b_kwrap : kx;
+                        tma_load_3d(sa, &tma_a, &full_bar[stage], kx, r0, b);
+                        tma_load_2d(sb, &tma_b, &full_bar[stage], kxb, n0);
+                    }
                     issued[stage] = true;
                     last_parity[stage] = phase;
                     if (++stage == STAGES) { stage = 0; phase ^= 1; }
@@ -281,8 +337,9 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant_
                     for (int k = 0; k < 4; ++k) {
                         const uint64_t ad = umma_desc_sw128(a_addr + 32 * k);
                         const uint64_t bd = umma_desc_sw128(b_addr + 32 * k);
-                        if (FP8) umma_fp8(d_tmem, ad, bd, IDESC, (kb | k) ? 1u : 0u);
-                        else umma_bf16(d_tmem, ad, bd, IDESC, (kb | k) ? 1u : 0u);
+                        const uint32_t accum = (kb | k) ? 1u : 0u;
+                        if (FP8) umma_fp8(d_tmem, ad, bd, IDESC, accum);
+                        else umma_bf16(d_tmem, ad, bd, IDESC, accum);
                     }
                     any = true;
                     umma_commit(&empty_bar[stage]);
@@ -317,6 +374,19 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant_
             const int64_t r = (mt % args.mt_per_batch) * kBM + g * 32 + lane;
             const bool row_ok = r < args.rows;
             const uint32_t taddr = tmem_base + ((uint32_t)(g * 32) << 16) + acc * BN;
+            if (SWAP) {
+                const int64_t n = mt * kBM + g * 32 + lane;      // output feature of this lane
+#pragma unroll 1
+                for (int c = 0; c < BN / 32; ++c) {
+                    uint32_t raw[32];
+                    tmem_ld32(taddr + c * 32, raw);
+                    tmem_wait_ld();
+                    store_swap(args, n, nt * BN + c * 32, raw, (int)(t % args.ksplit));
+                }
+                tc_fence_before();
+                mbar_arrive(&tempty_bar[acc]);
+                continue;
+            }
 #pragma unroll 1
             for (int c = 0; c < BN / 32; ++c) {
                 uint32_t raw[32];
@@ -327,7 +397,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant_
                     float v[32];
 #pragma unroll
                     for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(raw[j]);
-                    store_chunk(args, b, r, n0, v);
+                    store_chunk(args, b, r, n0, v, (int)(t % args.ksplit));
                 }
             }
             tc_fence_before();
@@ -370,22 +440,30 @@ wb_status encode_map(CUtensorMap* m, const void* ptr, int rank, const uint64_t* 
 
 int g_num_sms = 0;
 
-template <int BN, bool FP8>
-wb_status launch_tc(const GemmPlan& p, const GemmArgs& a, unsigned* err, cudaStream_t s, int max_ctas) {
+template <int BN, bool FP8, bool SWAP>
+wb_status launch_tc(const GemmPlan& p, GemmArgs a, unsigned* err, cudaStream_t s, int max_ctas) {
     using C = Cfg<BN>;
     static bool attr_set[64] = {};
     int dev = 0;
     WB_CUDA(cudaGetDevice(&dev));
     if (!attr_set[dev & 63]) {
-        WB_CUDA(cudaFuncSetAttribute(gemm_tc_kernel<BN, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        WB_CUDA(cudaFuncSetAttribute(gemm_tc_kernel<BN, FP8, SWAP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      C::SMEM));
         attr_set[dev & 63] = true;
     }
-    int grid = num_sms();
+    // A CTA that sees few k-blocks needs a shallow ring; the smaller footprint
+    // lets several CTAs share an SM (bounded by shared memory and TMEM).
+    const int64_t kb_per_cta = (int64_t)a.kblocks * ((a.tiles + num_sms() - 1) / num_sms());
+    a.stages = (int)std::max<int64_t>(2, std::min<int64_t>(C::STAGES, kb_per_cta));
+    const int smem = a.stages * C::STAGE_BYTES + 1024 + 256;
+    int occ = 1;
+    WB_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, gemm_tc_kernel<BN, FP8, SWAP>, 192, smem));
+    const int per_sm = std::max(1, std::min({occ, 512 / C::TMEM_COLS, 4}));
+    int grid = num_sms() * per_sm;
     if (max_ctas > 0) grid = std::min(grid, max_ctas);
     grid = (int)std::min<int64_t>(grid, a.tiles);
     if (grid <= 0) return WB_OK;
-    gemm_tc_kernel<BN, FP8><<<grid, 192, C::SMEM, s>>>(p.tma_a, p.tma_b, a, err);
+    gemm_tc_kernel<BN, FP8, SWAP><<<grid, 192, smem, s>>>(p.tma_a, p.tma_b, a, err);
     count_launch();
     WB_CUDA(cudaGetLastError());
     return WB_OK;
@@ -409,7 +487,7 @@ wb_status gemm_plan(GemmPlan* plan, const GemmOperand& A, const GemmOperand& B, 
     const int esz = fp8 ? 1 : 2;
     const int bk = fp8 ? 128 : 64;
     if (K % bk != 0) return fail(WB_ERR_SHAPE, "GEMM K must be a multiple of the k-block");
-    if (bn != 64 && bn != 128 && bn != 256) return fail(WB_ERR_SHAPE, "GEMM BN must be 64/128/256");
+    if (bn != 32 && bn != 64 && bn != 128 && bn != 256) return fail(WB_ERR_SHAPE, "GEMM BN must be 32/64/128/256");
     if (!aligned16(A.ptr) || !aligned16(B.ptr)) return fail(WB_ERR_ALIGN, "GEMM operand not 16-byte aligned");
     if ((A.row_stride * esz) % 16 || (B.row_stride * esz) % 16 || (A.batch_stride * esz) % 16)
         return fail(WB_ERR_ALIGN, "GEMM operand stride not a multiple of 16 bytes");
@@ -438,18 +516,71 @@ wb_status gemm_plan(GemmPlan* plan, const GemmOperand& A, const GemmOperand& B, 
     return WB_OK;
 }
 
-wb_status gemm_run(const GemmPlan& p, const GemmEpi& epi, unsigned* err, cudaStream_t s, int max_ctas) {
+wb_status gemm_plan_swap(GemmPlan* plan, const GemmOperand& X, const GemmOperand& W, int64_t N, int64_t K, bool fp8,
+                         int bn, int64_t w_kwrap) {
+    if (wb_status st = get_encoder()) return st;
+    const int esz = fp8 ? 1 : 2;
+    const int bk = fp8 ? 128 : 64;
+    if (K % bk != 0) return fail(WB_ERR_SHAPE, "GEMM K must be a multiple of the k-block");
+    if (bn != 32 && bn != 64 && bn != 128) return fail(WB_ERR_SHAPE, "swapped GEMM: activation tile 32/64/128");
+    if (X.batches != 1) return fail(WB_ERR_SHAPE, "swapped GEMM: no batched activations");
+    if (!aligned16(X.ptr) || !aligned16(W.ptr)) return fail(WB_ERR_ALIGN, "GEMM operand not 16-byte aligned");
+    if ((X.row_stride * esz) % 16 || (W.row_stride * esz) % 16) return fail(WB_ERR_ALIGN, "GEMM stride % 16 bytes");
+    if (w_kwrap && (w_kwrap % bk || K % w_kwrap)) return fail(WB_ERR_SHAPE, "GEMM k-wrap must divide K");
+    const int64_t kw = w_kwrap ? w_kwrap : K;
+    {   // A = weights [N, kw], 128-row boxes
+        uint64_t dims[3] = {(uint64_t)kw, (uint64_t)N, 1};
+        uint64_t strides[2] = {(uint64_t)(W.row_stride * esz), (uint64_t)(N * W.row_stride * esz)};
+        uint32_t box[3] = {(uint32_t)bk, (uint32_t)kBM, 1};
+        if (wb_status st = encode_map(&plan->tma_a, W.ptr, 3, dims, strides, box, fp8)) return st;
+    }
+    {   // B = activations [M, K], bn-row boxes
+        uint64_t dims[2] = {(uint64_t)K, (uint64_t)X.rows};
+        uint64_t strides[1] = {(uint64_t)(X.row_stride * esz)};
+        uint32_t box[2] = {(uint32_t)bk, (uint32_t)bn};
+        if (wb_status st = encode_map(&plan->tma_b, X.ptr, 2, dims, strides, box, fp8)) return st;
+    }
+    plan->M_rows = X.rows;
+    plan->batches = 1;
+    plan->N = N;
+    plan->K = K;
+    plan->bn = bn;
+    plan->b_kwrap = w_kwrap;
+    plan->fp8 = fp8;
+    plan->swap = true;
+    plan->ok = true;
+    return WB_OK;
+}
+
+wb_status gemm_run(const GemmPlan& p, const GemmEpi& epi, unsigned* err, cudaStream_t s, int max_ctas, int ksplit,
+                   int64_t rows_override) {
     if (!p.ok) return fail(WB_ERR_INVALID_ARG, "GEMM plan not built");
     GemmArgs a;
-    a.rows = p.M_rows;
+    a.rows = rows_override > 0 ? std::min<int64_t>(rows_override, p.M_rows) : p.M_rows;
     a.batches = p.batches;
     a.N = p.N;
     a.K = p.K;
-    a.mt_per_batch = (p.M_rows + kBM - 1) / kBM;
-    a.mt_total = a.mt_per_batch * p.batches;
-    a.nt_total = (p.N + p.bn - 1) / p.bn;
-    a.tiles = a.mt_total * a.nt_total;
-    a.kblocks = (int)(p.K / (p.fp8 ? 128 : 64));
+    if (p.swap) {
+        if (epi.out_type != OUT_F32 && epi.out_type != OUT_F32_ACC) return fail(WB_ERR_INVALID_ARG, "swapped GEMM: fp32 output only");
+        if (epi.gelu || epi.add || epi.mode != MODE_PLAIN) return fail(WB_ERR_INVALID_ARG, "swapped GEMM: linear epilogue only");
+        a.mt_per_batch = (p.N + kBM - 1) / kBM;        // weight-row tiles
+        a.mt_total = a.mt_per_batch;
+        a.nt_total = (a.rows + p.bn - 1) / p.bn;        // activation-row tiles
+    } else {
+        a.mt_per_batch = (a.rows + kBM - 1) / kBM;
+        a.mt_total = a.mt_per_batch * p.batches;
+        a.nt_total = (p.N + p.bn - 1) / p.bn;
+    }
+    const int kb_all = (int)(p.K / (p.fp8 ? 128 : 64));
+    if (ksplit < 1) ksplit = 1;
+    if (ksplit > 1) {
+        if (epi.out_type != OUT_F32 && epi.out_type != OUT_F32_ACC) return fail(WB_ERR_INVALID_ARG, "split-K needs fp32 output");
+        if (epi.gelu || epi.add || epi.mode != MODE_PLAIN) return fail(WB_ERR_INVALID_ARG, "split-K: linear epilogue only");
+        while (ksplit > 1 && kb_all % ksplit) --ksplit;
+    }
+    a.ksplit = ksplit;
+    a.tiles = a.mt_total * a.nt_total * ksplit;
+    a.kblocks = kb_all / ksplit;
     a.b_kwrap = (int)p.b_kwrap;
     a.epi = epi;
     const bool half = epi.out_type == OUT_BF16 || epi.out_type == OUT_BF16X2;
@@ -457,20 +588,33 @@ wb_status gemm_run(const GemmPlan& p, const GemmEpi& epi, unsigned* err, cudaStr
                 (epi.out_type != OUT_BF16X2 || (p.N * 2) % 16 == 0);
     if (epi.mode == MODE_CROSS_KV && !a.epi.vec) return fail(WB_ERR_ALIGN, "cross K/V output not 16-byte aligned");
     if (a.tiles == 0 || a.kblocks == 0) return WB_OK;
-    const bool small = p.M_rows * p.batches < 1024;
+    const bool small = a.rows * p.batches < 1024;
     const int slot = prof_begin(small ? WB_KERNEL_GEMM_SMALL : WB_KERNEL_GEMM, s);
     wb_status st;
-    if (p.fp8) {
-        if (p.bn == 256) st = launch_tc<256, true>(p, a, err, s, max_ctas);
-        else if (p.bn == 128) st = launch_tc<128, true>(p, a, err, s, max_ctas);
-        else st = launch_tc<64, true>(p, a, err, s, max_ctas);
+    if (p.swap) {
+        if (p.fp8) {
+            if (p.bn == 128) st = launch_tc<128, true, true>(p, a, err, s, max_ctas);
+            else if (p.bn == 64) st = launch_tc<64, true, true>(p, a, err, s, max_ctas);
+            else st = launch_tc<32, true, true>(p, a, err, s, max_ctas);
+        } else {
+            if (p.bn == 128) st = launch_tc<128, false, true>(p, a, err, s, max_ctas);
+            else if (p.bn == 64) st = launch_tc<64, false, true>(p, a, err, s, max_ctas);
+            else st = launch_tc<32, false, true>(p, a, err, s, max_ctas);
+        }
+    } else if (p.fp8) {
+        if (p.bn == 256) st = launch_tc<256, true, false>(p, a, err, s, max_ctas);
+        else if (p.bn == 128) st = launch_tc<128, true, false>(p, a, err, s, max_ctas);
+        else if (p.bn == 64) st = launch_tc<64, true, false>(p, a, err, s, max_ctas);
+        else st = launch_tc<32, true, false>(p, a, err, s, max_ctas);
     } else {
-        if (p.bn == 256) st = launch_tc<256, false>(p, a, err, s, max_ctas);
-        else if (p.bn == 128) st = launch_tc<128, false>(p, a, err, s, max_ctas);
-        else st = launch_tc<64, false>(p, a, err, s, max_ctas);
+        if (p.bn == 256) st = launch_tc<256, false, false>(p, a, err, s, max_ctas);
+        else if (p.bn == 128) st = launch_tc<128, false, false>(p, a, err, s, max_ctas);
+        else if (p.bn == 64) st = launch_tc<64, false, false>(p, a, err, s, max_ctas);
+        else st = launch_tc<32, false, false>(p, a, err, s, max_ctas);
     }
     const double k_alg = (double)(p.b_kwrap ? p.b_kwrap : p.K);
-    const double M = (double)(p.M_rows * p.batches), esz = p.fp8 ? 1.0 : 2.0;
+    const double M = (double)(a.rows * p.batches), esz = p.fp8 ? 1.0 : 2.0;
+    (void)M;
     const double osz = (epi.out_type == OUT_BF16) ? 2.0 : (epi.out_type == OUT_F32_ACC ? 8.0 : 4.0);
     if (small) prof_end(slot, s, (double)p.N * k_alg * esz + M * (double)p.K * esz + M * (double)p.N * osz);
     else prof_end(slot, s, 2.0 * M * (double)p.N * k_alg);

@@ -57,6 +57,7 @@ struct GemmPlan {
     int64_t b_kwrap = 0;   // A has K columns, B has b_kwrap: B is read at k mod b_kwrap
     int bn = 256;
     bool fp8 = false;
+    bool swap = false;     // small-M form: weights are the 128-row MMA operand
     bool ok = false;
 };
 
@@ -64,8 +65,16 @@ struct GemmPlan {
 // E4M3 when fp8.  Returns WB_OK or an error code with the message set.
 wb_status gemm_plan(GemmPlan* plan, const GemmOperand& A, const GemmOperand& B, int64_t N,
                     int64_t K, bool fp8, int bn, int64_t b_kwrap = 0);
+// Small-M form: C[M, N] = X[M, K] . W[N, K]^T computed as W . X^T, with the
+// weights as the 128-row MMA operand and bn (32/64/128) activation rows as the
+// MMA N dimension; fp32 output, linear epilogue; w_kwrap as b_kwrap above.
+wb_status gemm_plan_swap(GemmPlan* plan, const GemmOperand& X, const GemmOperand& W, int64_t N, int64_t K,
+                         bool fp8, int bn, int64_t w_kwrap = 0);
+// ksplit > 1 partitions K across CTAs and adds partial tiles with fp32
+// atomics (fp32 outputs only; the caller zeroes a non-residual output first).
+// rows_override < M_rows restricts the launch to the first rows.
 wb_status gemm_run(const GemmPlan& plan, const GemmEpi& epi, unsigned* err, cudaStream_t s,
-                   int max_ctas = 0);
+                   int max_ctas = 0, int ksplit = 1, int64_t rows_override = 0);
 
 // fp32 / bf16 CUDA-core GEMM with the same semantics (used by the fp32 model
 // and for small problems).  a_bf16 / b_bf16 select the operand types.

@@ -86,11 +86,16 @@ layernorm_kernel(const float* __restrict__ x, int64_t ld_x, int64_t rows, int d,
 template <typename TW>
 __global__ void embed_kernel(const int32_t* __restrict__ tokens, int64_t rows, int P, int p0, int d,
                              const TW* __restrict__ E, const TW* __restrict__ Pos, int vocab,
-                             float* __restrict__ x, unsigned* err) {
+                             float* __restrict__ x, unsigned* err, const int* __restrict__ pos_dev,
+                             const int32_t* __restrict__ len) {
     const int64_t r = blockIdx.x;
     if (r >= rows) return;
     const int64_t c = r / P;
-    const int pos = p0 + (int)(r % P);
+    const int pos = (pos_dev ? *pos_dev : p0) + (int)(r % P);
+    if (pos >= kMaxPos || (len && pos >= len[c])) {   // a finished chunk's row: nothing to embed
+        for (int i = threadIdx.x; i < d; i += blockDim.x) x[r * d + i] = 0.f;
+        return;
+    }
     int tok = tokens[c * kMaxPos + pos];
     if (tok < 0 || tok >= vocab) {
         if (threadIdx.x == 0) wb_set_error(err, WB_DEVERR_BOUNDS);
@@ -130,16 +135,13 @@ template <bool FP8>
 __global__ void kv_append_kernel(const float* __restrict__ qkv, int64_t n_chunks, int P, int p0, int d, int H,
                                  int layer, void* __restrict__ cache, const int64_t* __restrict__ off,
                                  const int32_t* __restrict__ len, const float* __restrict__ k_scale,
-                                 const float* __restrict__ v_scale, unsigned* err) {
+                                 const float* __restrict__ v_scale, unsigned* err, const int* __restrict__ pos_dev) {
     const int64_t r = blockIdx.x;   // row = c * P + p
     const int64_t c = r / P;
-    const int pos = p0 + (int)(r % P);
+    const int pos = (pos_dev ? *pos_dev : p0) + (int)(r % P);
     if (c >= n_chunks) return;
     const int L = len[c];
-    if (pos >= L) {
-        if (threadIdx.x == 0) wb_set_error(err, WB_DEVERR_BOUNDS);
-        return;
-    }
+    if (pos >= L) return;   // a chunk past its length keeps no more rows
     for (int i = threadIdx.x; i < 2 * d; i += blockDim.x) {
         const int kv = i / d, col = i % d, h = col / 64, e = col % 64;
         const float x = qkv[r * 3 * (int64_t)d + d + i];
@@ -302,6 +304,27 @@ __global__ void gather_rows_kernel(const float* __restrict__ x, int64_t rows, in
     for (int i = threadIdx.x; i < d; i += blockDim.x) out[r * d + i] = x[(r * stride_rows + first) * d + i];
 }
 
+__global__ void set_pos_kernel(int* pos, int value, int add) {
+    if (threadIdx.x == 0) *pos = add ? *pos + value : value;
+}
+
+// GELU after a linear GEMM: fp32 [rows, N] -> bf16 pair [rows, 2N] (hi | lo)
+// or fp32 in place.
+__global__ void gelu_post_kernel(float* __restrict__ x, int64_t rows, int N, __nv_bfloat16* __restrict__ out2) {
+    const int64_t total = rows * (int64_t)N;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+        const float v = gelu_f(x[i]);
+        if (out2) {
+            const int64_t r = i / N, c = i % N;
+            const __nv_bfloat16 hi = f2bf(v);
+            out2[r * 2 * N + c] = hi;
+            out2[r * 2 * N + N + c] = f2bf(v - bf2f(hi));
+        } else {
+            x[i] = v;
+        }
+    }
+}
+
 int grid_for(int64_t n, int threads) {
     int64_t g = (n + threads - 1) / threads;
     if (g > 148 * 16) g = 148 * 16;
@@ -325,14 +348,16 @@ wb_status layernorm(const float* x, int64_t ld_x, int64_t rows, int d, const flo
 }
 
 wb_status embed(const int32_t* tokens, int64_t rows, int P, int p0, int d, const void* E, const void* Pos,
-                bool bf16, int vocab, float* x, unsigned* err, cudaStream_t s) {
+                bool bf16, int vocab, float* x, unsigned* err, cudaStream_t s, const int* pos_dev,
+                const int32_t* len) {
     if (rows <= 0) return WB_OK;
     if (bf16)
         embed_kernel<__nv_bfloat16><<<(unsigned)rows, 256, 0, s>>>(tokens, rows, P, p0, d,
-            reinterpret_cast<const __nv_bfloat16*>(E), reinterpret_cast<const __nv_bfloat16*>(Pos), vocab, x, err);
+            reinterpret_cast<const __nv_bfloat16*>(E), reinterpret_cast<const __nv_bfloat16*>(Pos), vocab, x, err,
+            pos_dev, len);
     else
         embed_kernel<float><<<(unsigned)rows, 256, 0, s>>>(tokens, rows, P, p0, d, reinterpret_cast<const float*>(E),
-                                                           reinterpret_cast<const float*>(Pos), vocab, x, err);
+                                                           reinterpret_cast<const float*>(Pos), vocab, x, err, pos_dev, len);
     count_launch();
     WB_CUDA(cudaGetLastError());
     return WB_OK;
@@ -348,11 +373,11 @@ wb_status kv_scales(const float* qkv, int64_t n_chunks, int P, int d, float* k_s
 
 wb_status kv_append(const float* qkv, int64_t n_chunks, int P, int p0, int d, int H, int layer, bool fp8, void* cache,
                     const int64_t* off, const int32_t* len, const float* k_scale, const float* v_scale, unsigned* err,
-                    cudaStream_t s) {
+                    cudaStream_t s, const int* pos_dev) {
     if (n_chunks <= 0) return WB_OK;
     const unsigned grid = (unsigned)(n_chunks * P);
-    if (fp8) kv_append_kernel<true><<<grid, 256, 0, s>>>(qkv, n_chunks, P, p0, d, H, layer, cache, off, len, k_scale, v_scale, err);
-    else kv_append_kernel<false><<<grid, 256, 0, s>>>(qkv, n_chunks, P, p0, d, H, layer, cache, off, len, k_scale, v_scale, err);
+    if (fp8) kv_append_kernel<true><<<grid, 256, 0, s>>>(qkv, n_chunks, P, p0, d, H, layer, cache, off, len, k_scale, v_scale, err, pos_dev);
+    else kv_append_kernel<false><<<grid, 256, 0, s>>>(qkv, n_chunks, P, p0, d, H, layer, cache, off, len, k_scale, v_scale, err, pos_dev);
     count_launch();
     WB_CUDA(cudaGetLastError());
     return WB_OK;
@@ -399,6 +424,22 @@ wb_status quant_tensor(const void* x, bool bf16, int64_t n, uint8_t* q, float* s
 wb_status dequant_tensor(const uint8_t* q, const float* scale, int64_t n, float* out, cudaStream_t s) {
     if (n <= 0) return WB_OK;
     dequant_kernel<<<grid_for(n, 256), 256, 0, s>>>(q, scale, n, out);
+    count_launch();
+    WB_CUDA(cudaGetLastError());
+    return WB_OK;
+}
+
+wb_status gelu_post(float* x, int64_t rows, int N, void* out_bf16x2, cudaStream_t s) {
+    const int64_t n = rows * (int64_t)N;
+    if (n <= 0) return WB_OK;
+    gelu_post_kernel<<<grid_for(n, 256), 256, 0, s>>>(x, rows, N, reinterpret_cast<__nv_bfloat16*>(out_bf16x2));
+    count_launch();
+    WB_CUDA(cudaGetLastError());
+    return WB_OK;
+}
+
+wb_status set_pos(int* pos_dev, int value, bool add, cudaStream_t s) {
+    set_pos_kernel<<<1, 32, 0, s>>>(pos_dev, value, add ? 1 : 0);
     count_launch();
     WB_CUDA(cudaGetLastError());
     return WB_OK;

@@ -12,12 +12,18 @@ enum LnOut : int { LN_F32 = 0, LN_BF16 = 1, LN_E4M3 = 2, LN_BF16X2 = 3 };
 
 wb_status layernorm(const float* x, int64_t ld_x, int64_t rows, int d, const float* g, const float* b, LnOut mode,
                     void* out, int64_t ld_o, float* row_scale, cudaStream_t s);
+// Positions come from *pos_dev when it is non-null (graph replay), else p0.
 wb_status embed(const int32_t* tokens, int64_t rows, int P, int p0, int d, const void* E, const void* Pos, bool bf16,
-                int vocab, float* x, unsigned* err, cudaStream_t s);
+                int vocab, float* x, unsigned* err, cudaStream_t s, const int* pos_dev = nullptr,
+                const int32_t* len = nullptr);
 wb_status kv_scales(const float* qkv, int64_t n_chunks, int P, int d, float* k_scale, float* v_scale, cudaStream_t s);
 wb_status kv_append(const float* qkv, int64_t n_chunks, int P, int p0, int d, int H, int layer, bool fp8, void* cache,
                     const int64_t* off, const int32_t* len, const float* k_scale, const float* v_scale, unsigned* err,
-                    cudaStream_t s);
+                    cudaStream_t s, const int* pos_dev = nullptr);
+// x = GELU(x) in place, or GELU(x) as a bf16 (hi | lo) pair into out_bf16x2 [rows, 2N].
+wb_status gelu_post(float* x, int64_t rows, int N, void* out_bf16x2, cudaStream_t s);
+// *pos_dev = value, or += value when add.
+wb_status set_pos(int* pos_dev, int value, bool add, cudaStream_t s);
 wb_status quant_rows(const void* x_bf16, int64_t rows, int K, uint8_t* q, float* row_scale, cudaStream_t s);
 // Same from an fp32 matrix.
 wb_status quant_rows_f32(const float* x, int64_t rows, int K, uint8_t* q, float* row_scale, cudaStream_t s);

@@ -29,6 +29,7 @@ std::atomic<int64_t> g_launches{0};
 void count_launch(int n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
 
 bool prof_active(int kind) { return g_prof.kind != 0 && g_prof.kind == kind; }
+bool prof_any_active() { return g_prof.kind != 0; }
 
 int prof_begin(int kind, cudaStream_t s) {
     if (!prof_active(kind)) return -1;

@@ -8,6 +8,7 @@
 namespace wb {
 
 bool prof_active(int kind);
+bool prof_any_active();
 // Returns a slot (>= 0) when launches of `kind` are being timed.
 int prof_begin(int kind, cudaStream_t s);
 // Closes the slot; `units` is the launch's algorithmic bytes or flops.
