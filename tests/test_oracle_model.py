@@ -201,8 +201,8 @@ def test_fp8_row_scales_are_independent():
     x = rng.normal(size=(4, 16))
     lin = model.Linear(w, np.zeros(8), fp8=True)
     full = lin(x)
-    for i in range(4):
-        np.testing.assert_array_equal(lin(x[i:i + 1])[0], full[i])
+    for i in range(4):   # equal up to the summation order of one matrix product
+        np.testing.assert_allclose(lin(x[i:i + 1])[0], full[i], rtol=1e-13, atol=1e-15)
 
 
 def test_greedy_lowest_index_on_ties():
