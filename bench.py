@@ -10,11 +10,13 @@ pages measure on):
   c1  tiny fp32: 1 chunk, mel + encoder + 32 teacher-forced decoder tokens
   c2  mel front end: 64 chunks of 30 s, 128 mels
   c3  large-v3 encoder, bf16: 16 chunks (mel + encoder)
-  c4  large-v3-turbo transcription (default): one 16-min recording = 32 chunks,
+  c4  large-v3-turbo transcription: one 16-min recording = 32 chunks,
       mel, encoder, cross-K/V, 4-token forced prefix + 224 greedy tokens with
       the E4M3 self-attention cache
-  c5  large-v3 mixed serving batch: 48 requests of 2-15 min, FP8 QKV/FFN GEMMs,
-      E4M3 cache, 32-layer decoder, decode lengths 64-448, waves within 180 GB
+  c5  large-v3 mixed serving batch (default, the largest workload and the one
+      that runs every step of the path): 48 requests of 2-15 min, FP8 QKV/FFN
+      GEMMs, E4M3 cache, 32-layer decoder, decode lengths 64-448, waves within
+      180 GB
 
 The metric is RTFx = audio seconds processed / wall seconds.  `value` is the
 device-resident throughput (audio already in HBM); `e2e` repeats the same work
@@ -316,9 +318,9 @@ def cpu_sample(w: Workload, seed: int):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=3)
+    ap.add_argument("--steps", type=int, default=2)
     ap.add_argument("--warmup", type=int, default=3)
-    ap.add_argument("--config", default="c4", choices=["c1", "c2", "c3", "c4", "c5"])
+    ap.add_argument("--config", default="c5", choices=["c1", "c2", "c3", "c4", "c5"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -368,15 +370,14 @@ def main():
         run.step()
     run.sync_check()
 
-    # which kernel kind dominates: one profiled step per kind
-    kinds = [wb.KERNEL_GEMM, wb.KERNEL_GEMM_SMALL, wb.KERNEL_ENC_ATTN, wb.KERNEL_CROSS_ATTN,
-             wb.KERNEL_SELF_ATTN, wb.KERNEL_MEL]
+    # which kernel kind dominates: one step with every kind timed
+    wb.wb_prof_start(0, 1 << 20)
+    run.step()
+    torch.cuda.synchronize()
+    wb.wb_prof_stop()
     shares = {}
-    for k in kinds:
-        wb.wb_prof_start(k, 1 << 17)
-        run.step()
-        torch.cuda.synchronize()
-        n, ms, units = wb.wb_prof_stop()
+    for k in wb.KERNEL_NAMES:
+        n, ms, units = wb.wb_prof_result(k)
         if n:
             shares[k] = ms
     dom = max(shares, key=shares.get) if shares else w.bound_kernel

@@ -333,7 +333,9 @@ WB_API wb_status wb_gemm(const void* A, const void* B, int64_t M, int64_t N, int
  * written once for the memory-bound kinds (mel: audio in + mel out; decoder
  * attention: the K/V rows attended).  wb_prof_stop waits for the events and
  * returns launches, their summed duration in ms, and the summed work; it ends
- * the timing.  Not thread-safe against concurrent wb_prof_start calls.
+ * the timing.  kind 0 times every kind at once; wb_prof_result then returns
+ * one kind's share of the last timing.  Not thread-safe against concurrent
+ * wb_prof_start calls.
  */
 #define WB_KERNEL_GEMM        1
 #define WB_KERNEL_ENC_ATTN    2
@@ -344,6 +346,7 @@ WB_API wb_status wb_gemm(const void* A, const void* B, int64_t M, int64_t N, int
 #define WB_KERNEL_MAX         6
 WB_API wb_status wb_prof_start(int32_t kind, int32_t max_launches);
 WB_API wb_status wb_prof_stop(int64_t* launches, double* total_ms, double* units);
+WB_API wb_status wb_prof_result(int32_t kind, int64_t* launches, double* total_ms, double* units);
 
 /* Number of kernels this library has launched in this process so far. */
 WB_API int64_t wb_launch_count(void);

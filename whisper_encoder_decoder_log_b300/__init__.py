@@ -62,6 +62,8 @@ _SIGS = {
     "wb_gemm": (ctypes.c_int, [_VP, _VP, _I64, _I64, _I64, _I32, _VP, _VP, _VP, _I32, _VP, _I32, _VP]),
     "wb_prof_start": (ctypes.c_int, [_I32, _I32]),
     "wb_launch_count": (_I64, []),
+    "wb_prof_result": (ctypes.c_int, [_I32, ctypes.POINTER(_I64), ctypes.POINTER(ctypes.c_double),
+                                      ctypes.POINTER(ctypes.c_double)]),
     "wb_prof_stop": (ctypes.c_int, [ctypes.POINTER(_I64), ctypes.POINTER(ctypes.c_double),
                                     ctypes.POINTER(ctypes.c_double)]),
 }
@@ -272,6 +274,12 @@ def wb_prof_start(kind: int, max_launches: int = 1 << 16):
 def wb_prof_stop():
     n, ms, u = _I64(0), ctypes.c_double(0), ctypes.c_double(0)
     _check(lib().wb_prof_stop(ctypes.byref(n), ctypes.byref(ms), ctypes.byref(u)))
+    return n.value, ms.value, u.value
+
+
+def wb_prof_result(kind: int):
+    n, ms, u = _I64(0), ctypes.c_double(0), ctypes.c_double(0)
+    _check(lib().wb_prof_result(kind, ctypes.byref(n), ctypes.byref(ms), ctypes.byref(u)))
     return n.value, ms.value, u.value
 
 
