@@ -146,6 +146,8 @@ void sinusoids(int n_ctx, int d, std::vector<float>& out) {
 }
 
 __global__ void expand_scale_kernel(float* col_scale, int64_t rows_each) {
+    griddep_wait();
+    griddep_launch();
     const float s = col_scale[0];
     for (int64_t r = 1 + threadIdx.x; r < rows_each; r += blockDim.x) col_scale[r] = s;
 }
@@ -221,8 +223,7 @@ wb_status make_fp8(wb_model* m, const std::vector<std::string>& names, int64_t r
         if (wb_status st = quant_tensor(m->W(names[i]), true, rows_each * K, out->w + i * rows_each * K, sc,
                                         m->scratch_bits, s))
             return st;
-        expand_scale_kernel<<<1, 256, 0, s>>>(sc, rows_each);
-        count_launch();
+        WB_CUDA(launch_k(expand_scale_kernel, dim3(1), dim3(256), 0, s, sc, rows_each));
     }
     WB_CUDA(cudaGetLastError());
     return WB_OK;
@@ -280,7 +281,7 @@ wb_status linear_impl(const Lin& L, GemmEpi e, bool simt_fp32, unsigned* err, cu
             for (int64_t d = want; d <= kb_all / 2; ++d)
                 if (kb_all % d == 0) { ksplit = (int)d; break; }
         if (ksplit > 1 && e.out_type == OUT_F32)
-            WB_CUDA(cudaMemsetAsync(e.out, 0, (size_t)L.rows * e.ldo * sizeof(float), s));
+            if (wb_status st = fill(reinterpret_cast<float*>(e.out), L.rows * e.ldo, 0.f, s)) return st;
         GemmPlan p;
         if (wb_status st = gemm_plan_swap(&p, A, B, L.N, L.split ? 2 * L.K : L.K, f8, bn, L.split ? L.K : 0)) return st;
         return gemm_run(p, e, err, s, 0, ksplit);
@@ -304,7 +305,7 @@ wb_status linear_impl(const Lin& L, GemmEpi e, bool simt_fp32, unsigned* err, cu
     }
     if (ksplit > 1 && e.out_type == OUT_F32) {
         const int64_t obr = e.out_batch_rows ? e.out_batch_rows : L.rows;
-        WB_CUDA(cudaMemsetAsync(e.out, 0, (size_t)(L.batches * obr) * e.ldo * sizeof(float), s));
+        if (wb_status st = fill(reinterpret_cast<float*>(e.out), L.batches * obr * e.ldo, 0.f, s)) return st;
     }
     GemmPlan p;
     if (wb_status st = gemm_plan(&p, A, B, L.N, L.split ? 2 * L.K : L.K, f8, bn, L.split ? L.K : 0)) return st;
@@ -458,9 +459,11 @@ wb_status decoder_layers(wb_decoder* dec, int64_t n_chunks, int rows_per_chunk, 
     const int d = m->d(), H = m->H(), F = m->F();
     const int64_t R = n_chunks * rows_per_chunk;
     const bool f32 = m->fp32(), f8 = m->fp8();
-    const bool sp = !f32;                              // split bf16 activations
-    const LnOut ln_act = f32 ? LN_F32 : LN_BF16X2;
-    const DType attn_dt = f32 ? DT_F32 : DT_BF16X2;
+    // split bf16 activations for the bf16 model; under mixed_fp8 the FP8
+    // rounding of QKV/FFN inputs dominates and plain bf16 suffices
+    const bool sp = m->desc.precision == WB_PREC_BF16;
+    const LnOut ln_act = f32 ? LN_F32 : (sp ? LN_BF16X2 : LN_BF16);
+    const DType attn_dt = f32 ? DT_F32 : (sp ? DT_BF16X2 : DT_BF16);
     const int64_t lda = sp ? 2 * d : d;                // row stride of LN / attention outputs
     for (int l = 0; l < m->desc.dec_layers; ++l) {
         // ---- self-attention
@@ -573,8 +576,8 @@ wb_status decoder_head(wb_decoder* dec, int64_t n_chunks, int rows_per_chunk, in
                        cudaStream_t s, const int* pos_dev) {
     wb_model* m = dec->m;
     const int d = m->d(), V = m->desc.vocab;
-    const bool sp = !m->fp32();
-    const LnOut ln_act = sp ? LN_BF16X2 : LN_F32;
+    const bool sp = m->desc.precision == WB_PREC_BF16;
+    const LnOut ln_act = m->fp32() ? LN_F32 : (sp ? LN_BF16X2 : LN_BF16);
     const int64_t lda = sp ? 2 * d : d;
     const int64_t R = n_chunks * rows_per_chunk;
     Lin L;
@@ -600,6 +603,8 @@ wb_status decoder_head(wb_decoder* dec, int64_t n_chunks, int rows_per_chunk, in
 
 __global__ void gather_chunks_kernel(const float* __restrict__ audio, const int64_t* __restrict__ src,
                                      const int32_t* __restrict__ valid, float* __restrict__ out) {
+    griddep_wait();
+    griddep_launch();
     const int64_t c = blockIdx.y;
     const int64_t i0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * 4;
     if (i0 >= kChunkSamples) return;
@@ -612,6 +617,8 @@ __global__ void gather_chunks_kernel(const float* __restrict__ audio, const int6
 }
 
 __global__ void fill_prefix_kernel(int32_t* tokens, int64_t n, int32_t p0, int32_t p1, int32_t p2, int32_t p3) {
+    griddep_wait();
+    griddep_launch();
     const int64_t c = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (c >= n) return;
     tokens[c * kMaxPos + 0] = p0;
@@ -622,6 +629,8 @@ __global__ void fill_prefix_kernel(int32_t* tokens, int64_t n, int32_t p0, int32
 
 __global__ void scatter_tokens_kernel(const int32_t* __restrict__ wave_tok, const int32_t* __restrict__ dst_row,
                                       const int32_t* __restrict__ len, int32_t* __restrict__ out) {
+    griddep_wait();
+    griddep_launch();
     const int64_t c = blockIdx.x;
     const int64_t r = dst_row[c];
     for (int i = threadIdx.x; i < len[c]; i += blockDim.x) out[r * kMaxPos + i] = wave_tok[c * kMaxPos + i];
@@ -1147,9 +1156,8 @@ wb_status wb_transcribe_batch(wb_model* m, const float* audio, const int64_t* re
         WB_CUDA(cudaMemcpyAsync(tb.wlen, wl.data(), nw * 4, cudaMemcpyHostToDevice, s));
         // pageable host sources: make sure they are consumed before the vectors go away
         WB_CUDA(cudaStreamSynchronize(s));
-        gather_chunks_kernel<<<dim3((kChunkSamples / 4 + 255) / 256, (unsigned)nw), 256, 0, s>>>(
-            audio, tb.src, tb.valid, tb.chunk_audio);
-        count_launch();
+        WB_CUDA(launch_k(gather_chunks_kernel, dim3(dim3((kChunkSamples / 4 + 255) / 256, (unsigned)nw)), dim3(256), 0, s, 
+            audio, tb.src, tb.valid, tb.chunk_audio));
         WB_CUDA(cudaGetLastError());
         if (wb_status st = wb_mel(tb.chunk_audio, nw, m->desc.n_mels, tb.mel, stream)) return st;
         for (int64_t i0 = 0; i0 < nw; i0 += kEncSubBatch) {
@@ -1158,9 +1166,8 @@ wb_status wb_transcribe_batch(wb_model* m, const float* audio, const int64_t* re
                                          tb.enc + (size_t)i0 * kCtx * d * act, tb.enc_ws, tb.enc_ws_bytes, stream))
                 return st;
         }
-        fill_prefix_kernel<<<(unsigned)((nw + 255) / 256), 256, 0, s>>>(tb.wave_tok, nw, prefix[0], prefix[1],
-                                                                        prefix[2], prefix[3]);
-        count_launch();
+        WB_CUDA(launch_k(fill_prefix_kernel, dim3((unsigned)((nw + 255) / 256)), dim3(256), 0, s, tb.wave_tok, nw, prefix[0], prefix[1],
+                                                                        prefix[2], prefix[3]));
         WB_CUDA(cudaGetLastError());
         wb_decoder* dec = nullptr;
         if (wb_status st = wb_decoder_init(m, nw, wl.data(), tb.enc, tb.wave_tok, tb.dec_ws, tb.dec_ws_bytes, stream,
@@ -1174,8 +1181,7 @@ wb_status wb_transcribe_batch(wb_model* m, const float* audio, const int64_t* re
         }
         wb_decoder_destroy(dec);
         if (st) return st;
-        scatter_tokens_kernel<<<(unsigned)nw, 128, 0, s>>>(tb.wave_tok, tb.dst_row, tb.wlen, tokens);
-        count_launch();
+        WB_CUDA(launch_k(scatter_tokens_kernel, dim3((unsigned)nw), dim3(128), 0, s, tb.wave_tok, tb.dst_row, tb.wlen, tokens));
         WB_CUDA(cudaGetLastError());
     }
     if (n_waves_out) *n_waves_out = (int32_t)waves.size();

@@ -15,6 +15,8 @@
 //    decoder's cross-attention over the precomputed bf16 K/V, and the decoder's
 //    causal self-attention over the (E4M3 or fp32) KV cache, where query row
 //    p of a chunk sees cache rows 0..p.
+#include <type_traits>
+
 #include "attn.cuh"
 #include "common.cuh"
 #include "prof.cuh"
@@ -57,6 +59,8 @@ WB_DEV void mma16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_
 
 __global__ void __launch_bounds__(128)
 flash_enc_kernel(const __nv_bfloat16* __restrict__ qkv, int d, int S, __nv_bfloat16* __restrict__ out) {
+    griddep_wait();
+    griddep_launch();
     __shared__ __align__(128) __nv_bfloat16 sQ[kFaRows * 64];
     __shared__ __align__(128) __nv_bfloat16 sK[2][kFaKeys * 64];
     __shared__ __align__(128) __nv_bfloat16 sV[2][kFaKeys * 64];
@@ -273,6 +277,8 @@ __global__ void __launch_bounds__(kRowThreads)
 attn_rows_kernel(const TQ* __restrict__ q, int64_t q_ld, int rows_per_chunk, int n_rows_total,
                  KVView kv, int kv_len, int causal, int q_pos0, TO* __restrict__ out, int64_t o_ld,
                  int64_t o_split) {
+    griddep_wait();
+    griddep_launch();
     // scores for up to NQ query rows over up to kv_len keys
     extern __shared__ float sm[];
     float* sq = sm;                              // [NQ][64], pre-scaled by 1/8
@@ -416,6 +422,124 @@ attn_rows_kernel(const TQ* __restrict__ q, int64_t q_ld, int rows_per_chunk, int
     }
 }
 
+// Decode-step self-attention over the E4M3 cache: one CTA of 8 warps per
+// (chunk, head), one query row at the step's position, keys 0..pos.  Warp w
+// takes the 8-row passes w, w+8, ...; lane (r, sub) with r = lane / 4 and
+// sub = lane % 4 owns codes sub*16 .. sub*16+15 of row r of a pass.  K and V
+// of a pass are loaded together, scores are reduced over the 4 lanes of a
+// row, and each warp keeps an online softmax (running max, sum, output); the
+// 8 partial results are merged through shared memory at the end.
+template <typename TO>
+__global__ void __launch_bounds__(256)
+self_attn_e4m3_kernel(const float* __restrict__ q, int64_t q_ld, int heads, KVView kv, int q_pos_host,
+                      TO* __restrict__ out, int64_t o_ld, int64_t o_split) {
+    griddep_wait();
+    griddep_launch();
+    __shared__ float s_o[8][64];
+    __shared__ float s_m[8], s_l[8];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int h = blockIdx.x;
+    const int64_t chunk = blockIdx.y;
+    const int pos = kv.pos_dev ? *kv.pos_dev : q_pos_host;
+    if (kv.active_len && kv.active_len[chunk] <= pos + 1) return;   // finished chunk (uniform per CTA)
+    const int nk = pos + 1;
+    const int r = lane >> 2, sub = lane & 3;
+    const int64_t cb = kv.chunk_off ? kv.chunk_off[chunk] : chunk * kv.chunk_stride;
+    const int64_t hs = kv.head_stride * (kv.chunk_len ? (int64_t)kv.chunk_len[chunk] : 1);
+    const uint8_t* Kp = reinterpret_cast<const uint8_t*>(kv.ptr) + cb + ((int64_t)kv.k_blk * kv.heads + h) * hs;
+    const uint8_t* Vp = reinterpret_cast<const uint8_t*>(kv.ptr) + cb + ((int64_t)kv.v_blk * kv.heads + h) * hs;
+    const float ks = kv.k_scale ? kv.k_scale[chunk] : 1.f;
+    const float vs = kv.v_scale ? kv.v_scale[chunk] : 1.f;
+    float qv[16];
+    {
+        const float* qr = q + chunk * q_ld + h * 64 + sub * 16;
+#pragma unroll
+        for (int i = 0; i < 16; i += 4) {
+            const float4 t = *reinterpret_cast<const float4*>(qr + i);
+            // fold the 1/sqrt(64) and the K scale into q
+            qv[i] = t.x * 0.125f * ks; qv[i + 1] = t.y * 0.125f * ks; qv[i + 2] = t.z * 0.125f * ks; qv[i + 3] = t.w * 0.125f * ks;
+        }
+    }
+    float m = -INFINITY, l = 0.f, o[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) o[i] = 0.f;
+    for (int j0 = warp * 8; j0 < nk; j0 += 64) {
+        const int j = j0 + r;
+        const bool valid = j < nk;
+        uint4 kr = make_uint4(0, 0, 0, 0), vr = make_uint4(0, 0, 0, 0);
+        if (valid) {
+            kr = ld_stream(Kp + (int64_t)j * 64 + sub * 16);
+            vr = ld_stream(Vp + (int64_t)j * 64 + sub * 16);
+        }
+        float kf[16], vf[16];
+        {
+            const uint32_t w[4] = {kr.x, kr.y, kr.z, kr.w};
+            const uint32_t u[4] = {vr.x, vr.y, vr.z, vr.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                __nv_fp8x4_e4m3 a, b;
+                a.__x = w[i];
+                b.__x = u[i];
+                const float4 fa = static_cast<float4>(a), fb = static_cast<float4>(b);
+                kf[4 * i] = fa.x; kf[4 * i + 1] = fa.y; kf[4 * i + 2] = fa.z; kf[4 * i + 3] = fa.w;
+                vf[4 * i] = fb.x; vf[4 * i + 1] = fb.y; vf[4 * i + 2] = fb.z; vf[4 * i + 3] = fb.w;
+            }
+        }
+        float sc = 0.f;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) sc = fmaf(qv[i], kf[i], sc);
+        sc += __shfl_xor_sync(0xffffffffu, sc, 1);
+        sc += __shfl_xor_sync(0xffffffffu, sc, 2);
+        if (!valid) sc = -INFINITY;
+        float pm = sc;   // max over the 8 rows of the pass (lane bits 2-4)
+        pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 4));
+        pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 8));
+        pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 16));
+        const float mn = fmaxf(m, pm);
+        const float alpha = __expf(m - mn);        // 0 on a warp's first pass (m = -inf)
+        const float p = valid ? __expf(sc - mn) : 0.f;
+        float ps = p;                              // sum over the 8 rows
+        ps += __shfl_xor_sync(0xffffffffu, ps, 4);
+        ps += __shfl_xor_sync(0xffffffffu, ps, 8);
+        ps += __shfl_xor_sync(0xffffffffu, ps, 16);
+        l = l * alpha + ps;
+        m = mn;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) o[i] = fmaf(p, vf[i], o[i] * alpha);
+    }
+    // sum each warp's 8 row groups, then merge the 8 warps
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        o[i] += __shfl_xor_sync(0xffffffffu, o[i], 4);
+        o[i] += __shfl_xor_sync(0xffffffffu, o[i], 8);
+        o[i] += __shfl_xor_sync(0xffffffffu, o[i], 16);
+    }
+    if (r == 0) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) s_o[warp][sub * 16 + i] = o[i];
+    }
+    if (lane == 0) { s_m[warp] = m; s_l[warp] = l; }
+    __syncthreads();
+    if (threadIdx.x < 64) {
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < 8; ++w) M = fmaxf(M, s_m[w]);
+        float num = 0.f, den = 0.f;
+#pragma unroll
+        for (int w = 0; w < 8; ++w) {
+            if (s_m[w] == -INFINITY) continue;     // a warp that saw no rows
+            const float e = __expf(s_m[w] - M);
+            num = fmaf(e, s_o[w][threadIdx.x], num);
+            den = fmaf(e, s_l[w], den);
+        }
+        const float a = num / den * vs;
+        TO* orow = out + chunk * o_ld + h * 64;
+        const TO hi = (TO)a;
+        orow[threadIdx.x] = hi;
+        if (o_split) orow[o_split + threadIdx.x] = (TO)(a - (float)hi);
+    }
+}
+
 template <int NQ, typename TQ, typename TKV, typename TO>
 wb_status launch_rows_nq(const void* q, int64_t q_ld, int64_t n_chunks, int rows_per_chunk, int heads,
                          const KVView& kv, int kv_len, bool causal, int q_pos0, void* out, int64_t o_ld,
@@ -433,10 +557,9 @@ wb_status launch_rows_nq(const void* q, int64_t q_ld, int64_t n_chunks, int rows
     dim3 grid((unsigned)n_chunks, (unsigned)heads, (unsigned)((rows_per_chunk + NQ - 1) / NQ));
     const int kind = causal ? WB_KERNEL_SELF_ATTN : WB_KERNEL_CROSS_ATTN;
     const int slot = prof_begin(kind, s);
-    attn_rows_kernel<NQ, TQ, TKV, TO><<<grid, kRowThreads, smem, s>>>(
+    WB_CUDA(launch_k(attn_rows_kernel<NQ, TQ, TKV, TO>, dim3(grid), dim3(kRowThreads), smem, s, 
         reinterpret_cast<const TQ*>(q), q_ld, rows_per_chunk, (int)(n_chunks * rows_per_chunk), kv, kv_len,
-        causal ? 1 : 0, q_pos0, reinterpret_cast<TO*>(out), o_ld, o_split);
-    count_launch();
+        causal ? 1 : 0, q_pos0, reinterpret_cast<TO*>(out), o_ld, o_split));
     if (slot >= 0) {
         // K and V rows attended (each read once), queries in, outputs out
         const double kv_rows = causal ? (double)(q_pos0 + rows_per_chunk) : (double)kv_len;
@@ -452,6 +575,16 @@ template <typename TQ, typename TKV, typename TO>
 wb_status launch_rows(const void* q, int64_t q_ld, int64_t n_chunks, int rows_per_chunk, int heads,
                       const KVView& kv, int kv_len, bool causal, int q_pos0, void* out, int64_t o_ld,
                       cudaStream_t s, int64_t o_split) {
+    if (causal && rows_per_chunk == 1 && std::is_same<TKV, uint8_t>::value && std::is_same<TQ, float>::value &&
+        (q_ld % 4) == 0) {
+        dim3 grid((unsigned)heads, (unsigned)n_chunks);
+        const int slot = prof_begin(WB_KERNEL_SELF_ATTN, s);
+        WB_CUDA(launch_k(self_attn_e4m3_kernel<TO>, dim3(grid), dim3(256), 0, s, reinterpret_cast<const float*>(q), q_ld, heads, kv,
+                                                             q_pos0, reinterpret_cast<TO*>(out), o_ld, o_split));
+        prof_end(slot, s, (double)n_chunks * heads * (2.0 * (q_pos0 + 1) * 64.0 + 64.0 * (4 + sizeof(TO))));
+        WB_CUDA(cudaGetLastError());
+        return WB_OK;
+    }
     if (rows_per_chunk == 1)
         return launch_rows_nq<1, TQ, TKV, TO>(q, q_ld, n_chunks, rows_per_chunk, heads, kv, kv_len, causal, q_pos0,
                                               out, o_ld, s, o_split);
@@ -466,9 +599,8 @@ wb_status attn_flash_enc_bf16(const void* qkv, int64_t n_chunks, int d, int head
     if (n_chunks > 65535) return fail(WB_ERR_SHAPE, "too many chunks for one attention launch");
     dim3 grid((kCtx + kFaRows - 1) / kFaRows, heads, (unsigned)n_chunks);
     const int slot = prof_begin(WB_KERNEL_ENC_ATTN, s);
-    flash_enc_kernel<<<grid, 128, 0, s>>>(reinterpret_cast<const __nv_bfloat16*>(qkv), d, kCtx,
-                                          reinterpret_cast<__nv_bfloat16*>(out));
-    count_launch();
+    WB_CUDA(launch_k(flash_enc_kernel, dim3(grid), dim3(128), 0, s, reinterpret_cast<const __nv_bfloat16*>(qkv), d, kCtx,
+                                          reinterpret_cast<__nv_bfloat16*>(out)));
     prof_end(slot, s, 4.0 * (double)kCtx * kCtx * 64.0 * heads * (double)n_chunks);
     WB_CUDA(cudaGetLastError());
     return WB_OK;

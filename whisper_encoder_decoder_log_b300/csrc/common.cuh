@@ -25,6 +25,13 @@
 // gives up, records an error bit and lets its CTA wind down.
 #define WB_WAIT_NS 2000000000ull
 
+// Wait until the kernels this one depends on have completed and their writes
+// are visible (a no-op when the launch carried no programmatic dependency).
+WB_DEV void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Allow the next kernel in the stream to be scheduled (it still waits in its
+// own griddep_wait until this grid has completed).
+WB_DEV void griddep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 WB_DEV void wb_set_error(unsigned* err, unsigned bits) {
     if (err) atomicOr(err, bits);
 }

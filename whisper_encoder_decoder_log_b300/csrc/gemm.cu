@@ -3,15 +3,16 @@
 // the QKV, output and FFN projections; here they are tcgen05 with TMEM
 // accumulators for sm_103a).
 //
-// Kernel shape: persistent, one CTA per SM, 192 threads in three roles.
+// Kernel shape: persistent, 320 threads in three roles.
 //   warp 0      TMA producer: 128 x 128-byte A box and BN x 128-byte B box per
 //               k-block into a STAGES-deep ring (128-byte swizzle).
 //   warp 1      owns TMEM (2 x BN fp32 columns: a double-buffered accumulator)
 //               and, from one thread, issues tcgen05.mma (M 128, N BN, K 16
 //               for bf16 / 32 for E4M3) and tcgen05.commit to release stages
 //               and to hand a finished accumulator to the epilogue.
-//   warps 2-5   epilogue: tcgen05.ld 32 columns at a time, scale, bias, GELU,
-//               positional table, residual accumulate, store.
+//   warps 2-9   epilogue: two warps per TMEM lane quarter, alternate
+//               32-column chunks: tcgen05.ld, scale, bias, GELU, positional
+//               table, residual accumulate, store.
 // Tiles are visited in groups of 16 M-tiles so that the A panel of a group and
 // the whole B operand stay in L2.  Every mbarrier wait is bounded; a wait that
 // runs out records an error bit and the CTA winds down (waiting, bounded, for
@@ -210,8 +211,11 @@ __device__ __forceinline__ void store_swap(const GemmArgs& a, int64_t n, int64_t
     }
 }
 
+constexpr int kEpiWarps = 8;                       // two per TMEM lane quarter
+constexpr int kGemmThreads = 64 + 32 * kEpiWarps;  // producer + MMA + epilogue
+
 template <int BN, bool FP8, bool SWAP>
-__global__ void __launch_bounds__(192)
+__global__ void __launch_bounds__(kGemmThreads)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUtensorMap tma_b,
                const GemmArgs args, unsigned* err) {
     using C = Cfg<BN>;
@@ -238,7 +242,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant_
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&tfull_bar[i], 1);
-            mbar_init(&tempty_bar[i], 128);
+            mbar_init(&tempty_bar[i], 32 * kEpiWarps);
         }
         mbar_init(drain_bar, 1);
         *abort_flag = 0;
@@ -254,6 +258,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant_
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    griddep_wait();
+    griddep_launch();   // barriers and TMEM are set up; now wait for the producer kernels
 
     if (warp == 0) {
         if (lane == 0) {
@@ -355,8 +361,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant_
             }
         }
     } else {
-        // epilogue warps 2..5 -> TMEM lane groups 2,3,0,1
+        // epilogue warps 2..9: lane quarter g = warp % 4 (each quarter twice),
+        // the two warps of a quarter take alternate 32-column chunks
         const int g = warp & 3;
+        const int half = (warp - 2) >> 2;
         int local = 0;
         for (int64_t t = blockIdx.x; t < args.tiles; t += gridDim.x, ++local) {
             const int acc = local & 1;
@@ -377,7 +385,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant_
             if (SWAP) {
                 const int64_t n = mt * kBM + g * 32 + lane;      // output feature of this lane
 #pragma unroll 1
-                for (int c = 0; c < BN / 32; ++c) {
+                for (int c = half; c < BN / 32; c += 2) {
                     uint32_t raw[32];
                     tmem_ld32(taddr + c * 32, raw);
                     tmem_wait_ld();
@@ -388,7 +396,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant_
                 continue;
             }
 #pragma unroll 1
-            for (int c = 0; c < BN / 32; ++c) {
+            for (int c = half; c < BN / 32; c += 2) {
                 uint32_t raw[32];
                 tmem_ld32(taddr + c * 32, raw);
                 tmem_wait_ld();
@@ -457,14 +465,13 @@ wb_status launch_tc(const GemmPlan& p, GemmArgs a, unsigned* err, cudaStream_t s
     a.stages = (int)std::max<int64_t>(2, std::min<int64_t>(C::STAGES, kb_per_cta));
     const int smem = a.stages * C::STAGE_BYTES + 1024 + 256;
     int occ = 1;
-    WB_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, gemm_tc_kernel<BN, FP8, SWAP>, 192, smem));
+    WB_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, gemm_tc_kernel<BN, FP8, SWAP>, kGemmThreads, smem));
     const int per_sm = std::max(1, std::min({occ, 512 / C::TMEM_COLS, 4}));
     int grid = num_sms() * per_sm;
     if (max_ctas > 0) grid = std::min(grid, max_ctas);
     grid = (int)std::min<int64_t>(grid, a.tiles);
     if (grid <= 0) return WB_OK;
-    gemm_tc_kernel<BN, FP8, SWAP><<<grid, 192, smem, s>>>(p.tma_a, p.tma_b, a, err);
-    count_launch();
+    WB_CUDA(launch_k(gemm_tc_kernel<BN, FP8, SWAP>, dim3(grid), dim3(kGemmThreads), smem, s, p.tma_a, p.tma_b, a, err));
     WB_CUDA(cudaGetLastError());
     return WB_OK;
 }
@@ -628,6 +635,8 @@ template <bool ABF, bool BBF>
 __global__ void __launch_bounds__(256)
 gemm_simt_kernel(const void* __restrict__ Ap, GemmOperand A, const void* __restrict__ Bp, int64_t ldb,
                  GemmArgs args) {
+    griddep_wait();
+    griddep_launch();
     // 64 x 64 output tile, 16-deep k-steps, 4 x 4 per thread.
     __shared__ float As[16][64 + 4];
     __shared__ float Bs[16][64 + 4];
@@ -723,11 +732,10 @@ wb_status gemm_simt(const GemmOperand& A, bool a_bf16, const GemmOperand& B, boo
     if (a.tiles == 0) return WB_OK;
     if (a.mt_total > 65535) return fail(WB_ERR_SHAPE, "SIMT GEMM: too many row tiles");
     dim3 grid((unsigned)a.nt_total, (unsigned)a.mt_total);
-    if (a_bf16 && b_bf16) gemm_simt_kernel<true, true><<<grid, 256, 0, s>>>(A.ptr, A, B.ptr, B.row_stride, a);
-    else if (!a_bf16 && b_bf16) gemm_simt_kernel<false, true><<<grid, 256, 0, s>>>(A.ptr, A, B.ptr, B.row_stride, a);
-    else if (a_bf16 && !b_bf16) gemm_simt_kernel<true, false><<<grid, 256, 0, s>>>(A.ptr, A, B.ptr, B.row_stride, a);
-    else gemm_simt_kernel<false, false><<<grid, 256, 0, s>>>(A.ptr, A, B.ptr, B.row_stride, a);
-    count_launch();
+    if (a_bf16 && b_bf16) WB_CUDA(launch_k(gemm_simt_kernel<true, true>, dim3(grid), dim3(256), 0, s, A.ptr, A, B.ptr, B.row_stride, a));
+    else if (!a_bf16 && b_bf16) WB_CUDA(launch_k(gemm_simt_kernel<false, true>, dim3(grid), dim3(256), 0, s, A.ptr, A, B.ptr, B.row_stride, a));
+    else if (a_bf16 && !b_bf16) WB_CUDA(launch_k(gemm_simt_kernel<true, false>, dim3(grid), dim3(256), 0, s, A.ptr, A, B.ptr, B.row_stride, a));
+    else WB_CUDA(launch_k(gemm_simt_kernel<false, false>, dim3(grid), dim3(256), 0, s, A.ptr, A, B.ptr, B.row_stride, a));
     WB_CUDA(cudaGetLastError());
     return WB_OK;
 }

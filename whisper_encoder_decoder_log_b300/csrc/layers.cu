@@ -24,6 +24,8 @@ template <int OUT>
 __global__ void __launch_bounds__(256)
 layernorm_kernel(const float* __restrict__ x, int64_t ld_x, int64_t rows, int d, const float* __restrict__ g,
                  const float* __restrict__ b, void* __restrict__ out, int64_t ld_o, float* __restrict__ row_scale) {
+    griddep_wait();
+    griddep_launch();
     const int64_t row = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (row >= rows) return;
@@ -88,6 +90,8 @@ __global__ void embed_kernel(const int32_t* __restrict__ tokens, int64_t rows, i
                              const TW* __restrict__ E, const TW* __restrict__ Pos, int vocab,
                              float* __restrict__ x, unsigned* err, const int* __restrict__ pos_dev,
                              const int32_t* __restrict__ len) {
+    griddep_wait();
+    griddep_launch();
     const int64_t r = blockIdx.x;
     if (r >= rows) return;
     const int64_t c = r / P;
@@ -108,6 +112,8 @@ __global__ void embed_kernel(const int32_t* __restrict__ tokens, int64_t rows, i
 // Per (chunk, K|V): s = 2 * max(amax over the chunk's P rows, 1e-12) / 448.
 __global__ void kv_scale_kernel(const float* __restrict__ qkv, int P, int d, float* __restrict__ k_scale,
                                 float* __restrict__ v_scale) {
+    griddep_wait();
+    griddep_launch();
     const int64_t c = blockIdx.x;
     const int which = blockIdx.y;   // 0: K, 1: V
     float m = 0.f;
@@ -136,6 +142,8 @@ __global__ void kv_append_kernel(const float* __restrict__ qkv, int64_t n_chunks
                                  int layer, void* __restrict__ cache, const int64_t* __restrict__ off,
                                  const int32_t* __restrict__ len, const float* __restrict__ k_scale,
                                  const float* __restrict__ v_scale, unsigned* err, const int* __restrict__ pos_dev) {
+    griddep_wait();
+    griddep_launch();
     const int64_t r = blockIdx.x;   // row = c * P + p
     const int64_t c = r / P;
     const int pos = (pos_dev ? *pos_dev : p0) + (int)(r % P);
@@ -159,6 +167,8 @@ __global__ void kv_append_kernel(const float* __restrict__ qkv, int64_t n_chunks
 // Per-row E4M3 quantisation of a bf16 matrix (FC2's input in mixed_fp8).
 __global__ void quant_rows_kernel(const __nv_bfloat16* __restrict__ x, int64_t rows, int K, uint8_t* __restrict__ q,
                                   float* __restrict__ row_scale) {
+    griddep_wait();
+    griddep_launch();
     const int64_t r = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (r >= rows) return;
@@ -197,6 +207,8 @@ __global__ void quant_rows_kernel(const __nv_bfloat16* __restrict__ x, int64_t r
 // Per-row E4M3 quantisation of an fp32 matrix.
 __global__ void quant_rows_f32_kernel(const float* __restrict__ x, int64_t rows, int K, uint8_t* __restrict__ q,
                                       float* __restrict__ row_scale) {
+    griddep_wait();
+    griddep_launch();
     const int64_t r = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (r >= rows) return;
@@ -220,6 +232,8 @@ __global__ void quant_rows_f32_kernel(const float* __restrict__ x, int64_t rows,
 // amax of a tensor (non-negative floats order like their bit patterns).
 template <typename T>
 __global__ void amax_kernel(const T* __restrict__ x, int64_t n, unsigned* __restrict__ out_bits) {
+    griddep_wait();
+    griddep_launch();
     float m = 0.f;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
         m = fmaxf(m, fabsf((float)x[i]));
@@ -228,6 +242,8 @@ __global__ void amax_kernel(const T* __restrict__ x, int64_t n, unsigned* __rest
 }
 
 __global__ void scale_from_amax_kernel(const unsigned* __restrict__ amax_bits, float* __restrict__ scale) {
+    griddep_wait();
+    griddep_launch();
     const float a = __uint_as_float(*amax_bits);
     *scale = a > 0.f ? a / 448.0f : 1.0f;
 }
@@ -235,6 +251,8 @@ __global__ void scale_from_amax_kernel(const unsigned* __restrict__ amax_bits, f
 template <typename T>
 __global__ void quant_tensor_kernel(const T* __restrict__ x, int64_t n, const float* __restrict__ scale,
                                     uint8_t* __restrict__ q) {
+    griddep_wait();
+    griddep_launch();
     const float inv = 1.0f / *scale;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
         q[i] = (uint8_t)(f2e4m3x2((float)x[i] * inv, 0.f) & 0xFF);
@@ -242,12 +260,16 @@ __global__ void quant_tensor_kernel(const T* __restrict__ x, int64_t n, const fl
 
 __global__ void dequant_kernel(const uint8_t* __restrict__ q, const float* __restrict__ scale, int64_t n,
                                float* __restrict__ out) {
+    griddep_wait();
+    griddep_launch();
     const float s = *scale;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
         out[i] = e4m3_to_f(q[i]) * s;
 }
 
 __global__ void fill_kernel(float* __restrict__ x, int64_t n, float v) {
+    griddep_wait();
+    griddep_launch();
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
         x[i] = v;
 }
@@ -257,6 +279,8 @@ __global__ void fill_kernel(float* __restrict__ x, int64_t n, float v) {
 __global__ void __launch_bounds__(256)
 argmax_kernel(const float* __restrict__ logits, int64_t ld, int64_t rows, int V, int32_t* __restrict__ tokens,
               const int32_t* __restrict__ len, const int* __restrict__ pos_dev, int pos_host) {
+    griddep_wait();
+    griddep_launch();
     const int64_t r = blockIdx.x;
     if (r >= rows) return;
     const float* lr = logits + r * ld;
@@ -288,6 +312,8 @@ argmax_kernel(const float* __restrict__ logits, int64_t ld, int64_t rows, int V,
 // conv weight [O][C][3] -> GEMM operand [O][3][C] (k index = j * C + c)
 template <typename T>
 __global__ void conv_reorder_kernel(const T* __restrict__ w, int O, int C, T* __restrict__ out) {
+    griddep_wait();
+    griddep_launch();
     const int64_t n = (int64_t)O * C * 3;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
         const int64_t o = i / (3 * C);
@@ -299,18 +325,24 @@ __global__ void conv_reorder_kernel(const T* __restrict__ w, int O, int C, T* __
 
 __global__ void gather_rows_kernel(const float* __restrict__ x, int64_t rows, int d, int64_t stride_rows,
                                    int64_t first, float* __restrict__ out) {
+    griddep_wait();
+    griddep_launch();
     const int64_t r = blockIdx.x;
     if (r >= rows) return;
     for (int i = threadIdx.x; i < d; i += blockDim.x) out[r * d + i] = x[(r * stride_rows + first) * d + i];
 }
 
 __global__ void set_pos_kernel(int* pos, int value, int add) {
+    griddep_wait();
+    griddep_launch();
     if (threadIdx.x == 0) *pos = add ? *pos + value : value;
 }
 
 // GELU after a linear GEMM: fp32 [rows, N] -> bf16 pair [rows, 2N] (hi | lo)
 // or fp32 in place.
 __global__ void gelu_post_kernel(float* __restrict__ x, int64_t rows, int N, __nv_bfloat16* __restrict__ out2) {
+    griddep_wait();
+    griddep_launch();
     const int64_t total = rows * (int64_t)N;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
         const float v = gelu_f(x[i]);
@@ -338,11 +370,10 @@ wb_status layernorm(const float* x, int64_t ld_x, int64_t rows, int d, const flo
     if (rows <= 0) return WB_OK;
     if (d % 32 || d > 32 * kMaxPerLane) return fail(WB_ERR_SHAPE, "LayerNorm width must be a multiple of 32, <= 1280");
     const unsigned grid = (unsigned)((rows + 7) / 8);
-    if (mode == LN_F32) layernorm_kernel<LN_F32><<<grid, 256, 0, s>>>(x, ld_x, rows, d, g, b, out, ld_o, row_scale);
-    else if (mode == LN_BF16) layernorm_kernel<LN_BF16><<<grid, 256, 0, s>>>(x, ld_x, rows, d, g, b, out, ld_o, row_scale);
-    else if (mode == LN_BF16X2) layernorm_kernel<LN_BF16X2><<<grid, 256, 0, s>>>(x, ld_x, rows, d, g, b, out, ld_o, row_scale);
-    else layernorm_kernel<LN_E4M3><<<grid, 256, 0, s>>>(x, ld_x, rows, d, g, b, out, ld_o, row_scale);
-    count_launch();
+    if (mode == LN_F32) WB_CUDA(launch_k(layernorm_kernel<LN_F32>, dim3(grid), dim3(256), 0, s, x, ld_x, rows, d, g, b, out, ld_o, row_scale));
+    else if (mode == LN_BF16) WB_CUDA(launch_k(layernorm_kernel<LN_BF16>, dim3(grid), dim3(256), 0, s, x, ld_x, rows, d, g, b, out, ld_o, row_scale));
+    else if (mode == LN_BF16X2) WB_CUDA(launch_k(layernorm_kernel<LN_BF16X2>, dim3(grid), dim3(256), 0, s, x, ld_x, rows, d, g, b, out, ld_o, row_scale));
+    else WB_CUDA(launch_k(layernorm_kernel<LN_E4M3>, dim3(grid), dim3(256), 0, s, x, ld_x, rows, d, g, b, out, ld_o, row_scale));
     WB_CUDA(cudaGetLastError());
     return WB_OK;
 }
@@ -352,21 +383,19 @@ wb_status embed(const int32_t* tokens, int64_t rows, int P, int p0, int d, const
                 const int32_t* len) {
     if (rows <= 0) return WB_OK;
     if (bf16)
-        embed_kernel<__nv_bfloat16><<<(unsigned)rows, 256, 0, s>>>(tokens, rows, P, p0, d,
+        WB_CUDA(launch_k(embed_kernel<__nv_bfloat16>, dim3((unsigned)rows), dim3(256), 0, s, tokens, rows, P, p0, d,
             reinterpret_cast<const __nv_bfloat16*>(E), reinterpret_cast<const __nv_bfloat16*>(Pos), vocab, x, err,
-            pos_dev, len);
+            pos_dev, len));
     else
-        embed_kernel<float><<<(unsigned)rows, 256, 0, s>>>(tokens, rows, P, p0, d, reinterpret_cast<const float*>(E),
-                                                           reinterpret_cast<const float*>(Pos), vocab, x, err, pos_dev, len);
-    count_launch();
+        WB_CUDA(launch_k(embed_kernel<float>, dim3((unsigned)rows), dim3(256), 0, s, tokens, rows, P, p0, d, reinterpret_cast<const float*>(E),
+                                                           reinterpret_cast<const float*>(Pos), vocab, x, err, pos_dev, len));
     WB_CUDA(cudaGetLastError());
     return WB_OK;
 }
 
 wb_status kv_scales(const float* qkv, int64_t n_chunks, int P, int d, float* k_scale, float* v_scale, cudaStream_t s) {
     if (n_chunks <= 0) return WB_OK;
-    kv_scale_kernel<<<dim3((unsigned)n_chunks, 2), 256, 0, s>>>(qkv, P, d, k_scale, v_scale);
-    count_launch();
+    WB_CUDA(launch_k(kv_scale_kernel, dim3(dim3((unsigned)n_chunks, 2)), dim3(256), 0, s, qkv, P, d, k_scale, v_scale));
     WB_CUDA(cudaGetLastError());
     return WB_OK;
 }
@@ -376,9 +405,8 @@ wb_status kv_append(const float* qkv, int64_t n_chunks, int P, int p0, int d, in
                     cudaStream_t s, const int* pos_dev) {
     if (n_chunks <= 0) return WB_OK;
     const unsigned grid = (unsigned)(n_chunks * P);
-    if (fp8) kv_append_kernel<true><<<grid, 256, 0, s>>>(qkv, n_chunks, P, p0, d, H, layer, cache, off, len, k_scale, v_scale, err, pos_dev);
-    else kv_append_kernel<false><<<grid, 256, 0, s>>>(qkv, n_chunks, P, p0, d, H, layer, cache, off, len, k_scale, v_scale, err, pos_dev);
-    count_launch();
+    if (fp8) WB_CUDA(launch_k(kv_append_kernel<true>, dim3(grid), dim3(256), 0, s, qkv, n_chunks, P, p0, d, H, layer, cache, off, len, k_scale, v_scale, err, pos_dev));
+    else WB_CUDA(launch_k(kv_append_kernel<false>, dim3(grid), dim3(256), 0, s, qkv, n_chunks, P, p0, d, H, layer, cache, off, len, k_scale, v_scale, err, pos_dev));
     WB_CUDA(cudaGetLastError());
     return WB_OK;
 }
@@ -386,9 +414,8 @@ wb_status kv_append(const float* qkv, int64_t n_chunks, int P, int p0, int d, in
 wb_status quant_rows(const void* x_bf16, int64_t rows, int K, uint8_t* q, float* row_scale, cudaStream_t s) {
     if (rows <= 0) return WB_OK;
     if (K % 256) return fail(WB_ERR_SHAPE, "row quantiser needs K % 256 == 0");
-    quant_rows_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(reinterpret_cast<const __nv_bfloat16*>(x_bf16), rows, K,
-                                                                   q, row_scale);
-    count_launch();
+    WB_CUDA(launch_k(quant_rows_kernel, dim3((unsigned)((rows + 7) / 8)), dim3(256), 0, s, reinterpret_cast<const __nv_bfloat16*>(x_bf16), rows, K,
+                                                                   q, row_scale));
     WB_CUDA(cudaGetLastError());
     return WB_OK;
 }
@@ -396,8 +423,7 @@ wb_status quant_rows(const void* x_bf16, int64_t rows, int K, uint8_t* q, float*
 wb_status quant_rows_f32(const float* x, int64_t rows, int K, uint8_t* q, float* row_scale, cudaStream_t s) {
     if (rows <= 0) return WB_OK;
     if (K % 128) return fail(WB_ERR_SHAPE, "row quantiser needs K % 128 == 0");
-    quant_rows_f32_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(x, rows, K, q, row_scale);
-    count_launch();
+    WB_CUDA(launch_k(quant_rows_f32_kernel, dim3((unsigned)((rows + 7) / 8)), dim3(256), 0, s, x, rows, K, q, row_scale));
     WB_CUDA(cudaGetLastError());
     return WB_OK;
 }
@@ -406,16 +432,13 @@ wb_status quant_tensor(const void* x, bool bf16, int64_t n, uint8_t* q, float* s
                        cudaStream_t s) {
     WB_CUDA(cudaMemsetAsync(scratch_bits, 0, sizeof(unsigned), s));
     if (n > 0) {
-        if (bf16) amax_kernel<__nv_bfloat16><<<grid_for(n, 256), 256, 0, s>>>(reinterpret_cast<const __nv_bfloat16*>(x), n, scratch_bits);
-        else amax_kernel<float><<<grid_for(n, 256), 256, 0, s>>>(reinterpret_cast<const float*>(x), n, scratch_bits);
-        count_launch();
+        if (bf16) WB_CUDA(launch_k(amax_kernel<__nv_bfloat16>, dim3(grid_for(n, 256)), dim3(256), 0, s, reinterpret_cast<const __nv_bfloat16*>(x), n, scratch_bits));
+        else WB_CUDA(launch_k(amax_kernel<float>, dim3(grid_for(n, 256)), dim3(256), 0, s, reinterpret_cast<const float*>(x), n, scratch_bits));
     }
-    scale_from_amax_kernel<<<1, 1, 0, s>>>(scratch_bits, scale);
-    count_launch();
+    WB_CUDA(launch_k(scale_from_amax_kernel, dim3(1), dim3(1), 0, s, scratch_bits, scale));
     if (n > 0) {
-        if (bf16) quant_tensor_kernel<__nv_bfloat16><<<grid_for(n, 256), 256, 0, s>>>(reinterpret_cast<const __nv_bfloat16*>(x), n, scale, q);
-        else quant_tensor_kernel<float><<<grid_for(n, 256), 256, 0, s>>>(reinterpret_cast<const float*>(x), n, scale, q);
-        count_launch();
+        if (bf16) WB_CUDA(launch_k(quant_tensor_kernel<__nv_bfloat16>, dim3(grid_for(n, 256)), dim3(256), 0, s, reinterpret_cast<const __nv_bfloat16*>(x), n, scale, q));
+        else WB_CUDA(launch_k(quant_tensor_kernel<float>, dim3(grid_for(n, 256)), dim3(256), 0, s, reinterpret_cast<const float*>(x), n, scale, q));
     }
     WB_CUDA(cudaGetLastError());
     return WB_OK;
@@ -423,8 +446,7 @@ wb_status quant_tensor(const void* x, bool bf16, int64_t n, uint8_t* q, float* s
 
 wb_status dequant_tensor(const uint8_t* q, const float* scale, int64_t n, float* out, cudaStream_t s) {
     if (n <= 0) return WB_OK;
-    dequant_kernel<<<grid_for(n, 256), 256, 0, s>>>(q, scale, n, out);
-    count_launch();
+    WB_CUDA(launch_k(dequant_kernel, dim3(grid_for(n, 256)), dim3(256), 0, s, q, scale, n, out));
     WB_CUDA(cudaGetLastError());
     return WB_OK;
 }
@@ -432,23 +454,20 @@ wb_status dequant_tensor(const uint8_t* q, const float* scale, int64_t n, float*
 wb_status gelu_post(float* x, int64_t rows, int N, void* out_bf16x2, cudaStream_t s) {
     const int64_t n = rows * (int64_t)N;
     if (n <= 0) return WB_OK;
-    gelu_post_kernel<<<grid_for(n, 256), 256, 0, s>>>(x, rows, N, reinterpret_cast<__nv_bfloat16*>(out_bf16x2));
-    count_launch();
+    WB_CUDA(launch_k(gelu_post_kernel, dim3(grid_for(n, 256)), dim3(256), 0, s, x, rows, N, reinterpret_cast<__nv_bfloat16*>(out_bf16x2)));
     WB_CUDA(cudaGetLastError());
     return WB_OK;
 }
 
 wb_status set_pos(int* pos_dev, int value, bool add, cudaStream_t s) {
-    set_pos_kernel<<<1, 32, 0, s>>>(pos_dev, value, add ? 1 : 0);
-    count_launch();
+    WB_CUDA(launch_k(set_pos_kernel, dim3(1), dim3(32), 0, s, pos_dev, value, add ? 1 : 0));
     WB_CUDA(cudaGetLastError());
     return WB_OK;
 }
 
 wb_status fill(float* x, int64_t n, float v, cudaStream_t s) {
     if (n <= 0) return WB_OK;
-    fill_kernel<<<grid_for(n, 256), 256, 0, s>>>(x, n, v);
-    count_launch();
+    WB_CUDA(launch_k(fill_kernel, dim3(grid_for(n, 256)), dim3(256), 0, s, x, n, v));
     WB_CUDA(cudaGetLastError());
     return WB_OK;
 }
@@ -456,17 +475,15 @@ wb_status fill(float* x, int64_t n, float v, cudaStream_t s) {
 wb_status argmax_tokens(const float* logits, int64_t ld, int64_t rows, int V, int32_t* tokens, const int32_t* len,
                         const int* pos_dev, int pos_host, cudaStream_t s) {
     if (rows <= 0) return WB_OK;
-    argmax_kernel<<<(unsigned)rows, 256, 0, s>>>(logits, ld, rows, V, tokens, len, pos_dev, pos_host);
-    count_launch();
+    WB_CUDA(launch_k(argmax_kernel, dim3((unsigned)rows), dim3(256), 0, s, logits, ld, rows, V, tokens, len, pos_dev, pos_host));
     WB_CUDA(cudaGetLastError());
     return WB_OK;
 }
 
 wb_status conv_reorder(const void* w, int O, int C, bool bf16, void* out, cudaStream_t s) {
     const int64_t n = (int64_t)O * C * 3;
-    if (bf16) conv_reorder_kernel<__nv_bfloat16><<<grid_for(n, 256), 256, 0, s>>>(reinterpret_cast<const __nv_bfloat16*>(w), O, C, reinterpret_cast<__nv_bfloat16*>(out));
-    else conv_reorder_kernel<float><<<grid_for(n, 256), 256, 0, s>>>(reinterpret_cast<const float*>(w), O, C, reinterpret_cast<float*>(out));
-    count_launch();
+    if (bf16) WB_CUDA(launch_k(conv_reorder_kernel<__nv_bfloat16>, dim3(grid_for(n, 256)), dim3(256), 0, s, reinterpret_cast<const __nv_bfloat16*>(w), O, C, reinterpret_cast<__nv_bfloat16*>(out)));
+    else WB_CUDA(launch_k(conv_reorder_kernel<float>, dim3(grid_for(n, 256)), dim3(256), 0, s, reinterpret_cast<const float*>(w), O, C, reinterpret_cast<float*>(out)));
     WB_CUDA(cudaGetLastError());
     return WB_OK;
 }
@@ -474,8 +491,7 @@ wb_status conv_reorder(const void* w, int O, int C, bool bf16, void* out, cudaSt
 wb_status gather_rows(const float* x, int64_t rows, int d, int64_t stride_rows, int64_t first, float* out,
                       cudaStream_t s) {
     if (rows <= 0) return WB_OK;
-    gather_rows_kernel<<<(unsigned)rows, 256, 0, s>>>(x, rows, d, stride_rows, first, out);
-    count_launch();
+    WB_CUDA(launch_k(gather_rows_kernel, dim3((unsigned)rows), dim3(256), 0, s, x, rows, d, stride_rows, first, out));
     WB_CUDA(cudaGetLastError());
     return WB_OK;
 }

@@ -46,6 +46,7 @@ constexpr int kMaxFbNnz = 512;
 
 struct MelTables {
     float2 tw[kNFFT];          // W400^j = exp(-2 pi i j / 400)
+    float2 tw1[16 * 25];       // stage-1 twiddles W400^(n2 k1) at [k1][n2]
     float win[kNFFT];          // periodic Hann
     int kstart[kMaxMels];
     int kcount[kMaxMels];
@@ -99,6 +100,8 @@ __device__ __forceinline__ void dft5(float2& x0, float2& x1, float2& x2, float2&
 __global__ void __launch_bounds__(kThreads, 2)
 mel_kernel(const float* __restrict__ audio, const MelTables* __restrict__ tables, int n_mels,
            float* __restrict__ out) {
+    griddep_wait();
+    griddep_launch();
     extern __shared__ __align__(16) unsigned char smem_raw[];
     MelSmem& S = *reinterpret_cast<MelSmem*>(smem_raw);
     cg::cluster_group cluster = cg::this_cluster();
@@ -121,12 +124,19 @@ mel_kernel(const float* __restrict__ audio, const MelTables* __restrict__ tables
         const int nf = min(kSub, fbeg + kFramesPerCta - f0);
         __syncthreads();   // previous sub-block fully consumed (and tables ready)
         // ---- audio segment: padded index 160 f0 + i maps to sample 160 f0 + i - 200
-        for (int i = tid; i < kSeg; i += kThreads) {
-            int q = kHop * f0 + i - kNFFT / 2;
-            if (q < 0) q = -q;
-            if (q >= kChunkSamples) q = 2 * (kChunkSamples - 1) - q;
-            q = max(0, min(q, kChunkSamples - 1));
-            S.seg[i] = __ldg(x + q);
+        const int q0 = kHop * f0 - kNFFT / 2;            // a multiple of 4 samples
+        if (q0 >= 0 && q0 + kSeg <= kChunkSamples) {      // interior: 16-byte loads, all in flight
+            const float4* src = reinterpret_cast<const float4*>(x + q0);
+            float4* dst = reinterpret_cast<float4*>(S.seg);
+            for (int i = tid; i < kSeg / 4; i += kThreads) dst[i] = __ldg(src + i);
+        } else {                                          // chunk edges: reflect
+            for (int i = tid; i < kSeg; i += kThreads) {
+                int q = q0 + i;
+                if (q < 0) q = -q;
+                if (q >= kChunkSamples) q = 2 * (kChunkSamples - 1) - q;
+                q = max(0, min(q, kChunkSamples - 1));
+                S.seg[i] = __ldg(x + q);
+            }
         }
         __syncthreads();
         // ---- stage 1: 16-point DFTs over n1, twiddle W400^(n2 k1)
@@ -157,7 +167,7 @@ mel_kernel(const float* __restrict__ audio, const MelTables* __restrict__ tables
 #pragma unroll
                 for (int d = 0; d < 4; ++d) {
                     const int k1 = c + 4 * d;
-                    zp[k1] = (n2 * k1 == 0) ? v[4 * c + d] : cmul(v[4 * c + d], S.t.tw[n2 * k1]);
+                    zp[k1] = (k1 == 0) ? v[4 * c + d] : cmul(v[4 * c + d], S.t.tw1[k1 * 25 + n2]);
                 }
         }
         __syncthreads();
@@ -251,6 +261,8 @@ bool build_tables(int n_mels, MelTables* t) {
         t->tw[j] = make_float2((float)std::cos(2 * pi * j / kNFFT), (float)-std::sin(2 * pi * j / kNFFT));
         t->win[j] = (float)(0.5 - 0.5 * std::cos(2 * pi * j / kNFFT));
     }
+    for (int k1 = 0; k1 < 16; ++k1)
+        for (int n2 = 0; n2 < 25; ++n2) t->tw1[k1 * 25 + n2] = t->tw[(k1 * n2) % kNFFT];
     const double mlo = hz_to_mel_slaney(0.0), mhi = hz_to_mel_slaney(8000.0);
     std::vector<double> pts(n_mels + 2);
     for (int i = 0; i < n_mels + 2; ++i)
@@ -293,6 +305,8 @@ DeviceTables g_tabs[64];
 
 __global__ void transpose_pad_kernel(const float* __restrict__ mel, int C, void* __restrict__ out,
                                      bool bf16) {
+    griddep_wait();
+    griddep_launch();
     // grid: (ceil(3002 / 32), B); block 32 x 8.  Row r of the output is frame r - 1.
     __shared__ float tile[32][129];
     const int64_t b = blockIdx.y;
@@ -341,16 +355,18 @@ wb_status mel_launch(const float* audio, int64_t B, int n_mels, float* mel, cuda
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = sizeof(MelSmem);
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = kCluster;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = pdl_enabled() ? 2 : 1;
+    count_launch();
     const int slot = prof_begin(WB_KERNEL_MEL, s);
     WB_CUDA(cudaLaunchKernelEx(&cfg, mel_kernel, audio, (const MelTables*)tab, n_mels, mel));
-    count_launch();
     prof_end(slot, s, (double)B * ((double)kChunkSamples * 4.0 + (double)n_mels * kFrames * 4.0));
     return WB_OK;
 }
@@ -359,8 +375,7 @@ wb_status mel_transpose_pad(const float* mel, int64_t B, int C, void* out, bool 
                             cudaStream_t s) {
     if (C > 128) return fail(WB_ERR_SHAPE, "n_mels > 128");
     dim3 grid((kFrames + 2 + 31) / 32, (unsigned)B);
-    transpose_pad_kernel<<<grid, dim3(32, 8), 0, s>>>(mel, C, out, bf16);
-    count_launch();
+    WB_CUDA(launch_k(transpose_pad_kernel, dim3(grid), dim3(dim3(32, 8)), 0, s, mel, C, out, bf16));
     WB_CUDA(cudaGetLastError());
     return WB_OK;
 }

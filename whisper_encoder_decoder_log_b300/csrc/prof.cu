@@ -4,6 +4,7 @@
 // summed, so a caller can report achieved bandwidth or throughput of the kernel
 // inside a longer timed region.
 #include <atomic>
+#include <cstdlib>
 #include <mutex>
 #include <vector>
 
@@ -31,6 +32,14 @@ std::atomic<int64_t> g_launches{0};
 }  // namespace
 
 void count_launch(int n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+
+bool pdl_enabled() {
+    static const bool on = [] {
+        const char* e = getenv("WB_NO_PDL");
+        return !(e && e[0] == '1');
+    }();
+    return on;
+}
 
 bool prof_active(int kind) { return g_prof.kind != 0 && (g_prof.kind == kind || g_prof.kind == -1); }
 bool prof_any_active() { return g_prof.kind != 0; }

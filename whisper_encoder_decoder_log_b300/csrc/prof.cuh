@@ -3,6 +3,8 @@
 
 #include <cuda_runtime.h>
 
+#include <utility>
+
 #include "internal.h"
 
 namespace wb {
@@ -15,5 +17,27 @@ int prof_begin(int kind, cudaStream_t s);
 void prof_end(int slot, cudaStream_t s, double units);
 // Counts kernel launches (wb_launch_count).
 void count_launch(int n = 1);
+
+// Programmatic dependent launch: every kernel of the library begins with
+// griddep_wait() before it reads what an earlier kernel wrote, so the next
+// kernel's launch and prologue may overlap the tail of the previous one.
+// Off when the environment sets WB_NO_PDL=1.
+bool pdl_enabled();
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl_enabled() ? 1 : 0;
+    count_launch();
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 }  // namespace wb

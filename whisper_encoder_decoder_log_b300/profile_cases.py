@@ -1,0 +1,101 @@
+"""Small, self-contained runs of single kernel kinds for profiling.
+
+    python -m whisper_encoder_decoder_log_b300.profile_cases <case> [--iters N]
+
+Each case builds its inputs (seeded, synthetic), runs the kernel kind a few
+times through the C ABI and exits; a profiler can then select one launch of
+the kernel of interest.  Sizes are the workloads' own per-launch shapes with a
+small batch, so a capture holds well under a few GB of device memory.
+
+  mel     wb_mel on 64 chunks (the mel workload itself, 221 MB in + out)
+  gemm    encoder FC1-shaped bf16 GEMM, 24000 x 5120 x 1280 (16 chunks)
+  gemm8   the same GEMM in E4M3
+  decode  large-v3-turbo decoder over 32 chunks: prefix + 8 greedy steps
+          (cross-attention over 1500 bf16 rows per chunk and head, causal
+          self-attention over the E4M3 cache, few-row GEMMs)
+  flash   encoder self-attention over 16 chunks x 20 heads
+"""
+from __future__ import annotations
+
+import argparse
+import os
+import sys
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+
+def main():
+    import torch
+
+    import synth
+    import whisper_encoder_decoder_log_b300 as wb
+
+    ap = argparse.ArgumentParser()
+    ap.add_argument("case", choices=["mel", "gemm", "gemm8", "decode", "flash"])
+    ap.add_argument("--iters", type=int, default=3)
+    a = ap.parse_args()
+    dev = "cuda"
+    if a.case == "mel":
+        audio = torch.from_numpy(synth.batch_audio("pink", 64, 0)).to(dev)
+        mel = torch.empty(64, 128, 3000, device=dev)
+        for _ in range(a.iters):
+            wb.wb_mel(audio, 128, mel)
+    elif a.case in ("gemm", "gemm8"):
+        M, N, K = 24000, 5120, 1280
+        A = torch.randn(M, K, device=dev)
+        B = torch.randn(N, K, device=dev) * 0.02
+        C = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+        if a.case == "gemm":
+            A, B = A.to(torch.bfloat16), B.to(torch.bfloat16)
+            for _ in range(a.iters):
+                wb.wb_gemm(A, B, C)
+        else:
+            qa = torch.empty(M * K, dtype=torch.uint8, device=dev)
+            qb = torch.empty(N * K, dtype=torch.uint8, device=dev)
+            sa = torch.empty(1, device=dev)
+            sb = torch.empty(1, device=dev)
+            wb.wb_quantise_e4m3(A.reshape(-1), qa, sa)
+            wb.wb_quantise_e4m3(B.reshape(-1), qb, sb)
+            rs = sa.expand(M).contiguous()
+            cs = sb.expand(N).contiguous()
+            for _ in range(a.iters):
+                wb.wb_gemm(qa.view(M, K), qb.view(N, K), C, row_scale=rs, col_scale=cs)
+    else:
+        layers = (1, 4) if a.case == "decode" else (1, 0)
+        dims = synth.ModelDims("turbo", 128, 1280, 20, 5120, layers[0], layers[1], 51866)
+        desc = wb.make_desc(dims, wb.PREC_BF16, True)
+        buf = wb.pack_weights(desc, synth.make_weights(dims, 0, bf16=True))
+        torch.cuda.synchronize()
+        model = wb.wb_model_create(desc, buf)
+        B = 32 if a.case == "decode" else 16
+        audio = torch.from_numpy(synth.batch_audio("sine", B, 0)).to(dev)
+        mel = torch.empty(B, 128, 3000, device=dev)
+        wb.wb_mel(audio, 128, mel)
+        ws = torch.empty(wb.wb_encode_workspace_size(model, B), dtype=torch.uint8, device=dev)
+        enc = torch.empty(B, 1500, 1280, dtype=torch.bfloat16, device=dev)
+        for _ in range(a.iters if a.case == "flash" else 1):
+            wb.wb_encode(model, mel, enc, ws)
+        if a.case == "decode":
+            lens = np.full(B, 16, np.int32)
+            tok = torch.zeros(B, 448, dtype=torch.int32, device=dev)
+            tok[:, :4] = torch.from_numpy(synth.forced_prefix(0, dims.vocab)).to(dev)
+            dws = torch.empty(wb.wb_decoder_workspace_size(model, lens), dtype=torch.uint8, device=dev)
+            for _ in range(a.iters):
+                d = wb.wb_decoder_init(model, lens, enc, tok, dws)
+                wb.wb_decode_prefix(d, 4)
+                for _ in range(8):
+                    wb.wb_decode_step(d, B)
+                wb.wb_decoder_destroy(d)
+        wb.wb_sync_status(model)
+        wb.wb_model_destroy(model)
+    torch.cuda.synchronize()
+    wb.wb_sync_status()
+    print(f"profile case {a.case}: ok")
+
+
+if __name__ == "__main__":
+    main()
