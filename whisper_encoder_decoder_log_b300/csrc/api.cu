@@ -832,7 +832,10 @@ wb_status wb_encode(wb_model* m, const float* mel, int64_t B, void* enc, void* w
                                          d, s))
                 return st;
         } else {
-            if (wb_status st = attn_flash_enc_bf16(e.qkv, B, d, H, e.attn, s)) return st;
+            CUtensorMap tq;
+            if (wb_status st = make_tma_2d_bf16(&tq, e.qkv, 3 * (uint64_t)d, (uint64_t)M, 3 * (uint64_t)d * 2, 64, 128))
+                return st;
+            if (wb_status st = attn_flash_tc_bf16(&tq, B, d, H, e.attn, m->err, s)) return st;
         }
         {
             Lin L;

@@ -3,11 +3,7 @@
 // decoder_cross_attn without mask; "Unlocking the power of OpenAI's Whisper",
 // section 3).  Every head has width 64 and computes softmax(q k^T / 8) v.
 //
-//  * flash_enc_kernel: encoder self-attention in bf16.  One CTA = 64 query
-//    rows of one (chunk, head); 4 warps x 16 rows; K/V tiles of 64 keys are
-//    double-buffered in XOR-swizzled shared memory with cp.async; both
-//    products use the warp-level bf16 tensor-core MMA (m16n8k16) with the
-//    online softmax in fp32.
+//  * The bf16 encoder self-attention runs on tcgen05 (flash_tc.cu).
 //  * attn_rows_kernel: one CTA per (chunk, head, group of up to 4 query rows)
 //    streams the chunk's keys with 16-byte loads (8 lanes per bf16/fp32 key
 //    row, 4 lanes per E4M3 row), keeps the scores in shared memory, and
@@ -23,193 +19,6 @@
 
 namespace wb {
 namespace {
-
-// ------------------------------------------------------------------ flash (bf16)
-constexpr int kFaRows = 64;
-constexpr int kFaKeys = 64;
-
-WB_DEV uint32_t swz(int row, int chunk) {   // element offset in a [rows][64] bf16 tile
-    return (uint32_t)(row * 64 + ((chunk ^ (row & 7)) * 8));
-}
-
-WB_DEV void cp_async16(void* dst, const void* src, bool valid) {
-    const uint32_t d = smem_u32(dst);
-    const int n = valid ? 16 : 0;
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(d), "l"(src), "r"(n) : "memory");
-}
-WB_DEV void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-WB_DEV void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
-
-WB_DEV void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
-}
-WB_DEV void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
-}
-WB_DEV void mma16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-        "{%0,%1,%2,%3};"
-        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
-__global__ void __launch_bounds__(128)
-flash_enc_kernel(const __nv_bfloat16* __restrict__ qkv, int d, int S, __nv_bfloat16* __restrict__ out) {
-    griddep_wait();
-    griddep_launch();
-    __shared__ __align__(128) __nv_bfloat16 sQ[kFaRows * 64];
-    __shared__ __align__(128) __nv_bfloat16 sK[2][kFaKeys * 64];
-    __shared__ __align__(128) __nv_bfloat16 sV[2][kFaKeys * 64];
-    const int qb = blockIdx.x, h = blockIdx.y;
-    const int64_t chunk = blockIdx.z;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int64_t ld = 3 * (int64_t)d;
-    const __nv_bfloat16* base = qkv + chunk * S * ld;
-    const int q0 = qb * kFaRows;
-
-    // Q tile
-    for (int i = tid; i < kFaRows * 8; i += 128) {
-        const int r = i >> 3, c = i & 7;
-        const bool ok = q0 + r < S;
-        cp_async16(sQ + swz(r, c), base + (int64_t)(ok ? q0 + r : 0) * ld + h * 64 + c * 8, ok);
-    }
-    auto load_kv = [&](int buf, int k0) {
-        for (int i = tid; i < kFaKeys * 8; i += 128) {
-            const int r = i >> 3, c = i & 7;
-            const bool ok = k0 + r < S;
-            const __nv_bfloat16* src = base + (int64_t)(ok ? k0 + r : 0) * ld + h * 64 + c * 8;
-            cp_async16(sK[buf] + swz(r, c), src + d, ok);
-            cp_async16(sV[buf] + swz(r, c), src + 2 * d, ok);
-        }
-    };
-    load_kv(0, 0);
-    cp_async_commit();
-
-    const int nkb = (S + kFaKeys - 1) / kFaKeys;
-    uint32_t qf[4][4];
-    float o[8][4];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-    float m_r[2] = {-1e30f, -1e30f}, l_r[2] = {0.f, 0.f};
-    const float sc = 0.125f * 1.4426950408889634f;   // 1/sqrt(64) * log2(e)
-
-    for (int kb = 0; kb < nkb; ++kb) {
-        if (kb + 1 < nkb) load_kv((kb + 1) & 1, (kb + 1) * kFaKeys);
-        cp_async_commit();
-        cp_async_wait<1>();
-        __syncthreads();
-        if (kb == 0) {
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-                const int mi = lane >> 3, rr = lane & 7;
-                const int row = warp * 16 + rr + (mi & 1) * 8;
-                const int ch = kk * 2 + (mi >> 1);
-                ldsm_x4(smem_u32(sQ + swz(row, ch)), qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3]);
-            }
-        }
-        const __nv_bfloat16* k_t = sK[kb & 1];
-        const __nv_bfloat16* v_t = sV[kb & 1];
-        float s[8][4];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) s[j][0] = s[j][1] = s[j][2] = s[j][3] = 0.f;
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-#pragma unroll
-            for (int j = 0; j < 8; j += 2) {
-                const int mi = lane >> 3, rr = lane & 7;
-                const int key = 8 * (j + (mi >> 1)) + rr;
-                const int ch = kk * 2 + (mi & 1);
-                uint32_t b0, b1, b2, b3;
-                ldsm_x4(smem_u32(k_t + swz(key, ch)), b0, b1, b2, b3);
-                mma16816(s[j], qf[kk], b0, b1);
-                mma16816(s[j + 1], qf[kk], b2, b3);
-            }
-        }
-        // mask keys past S
-        const int k0 = kb * kFaKeys;
-        if (k0 + kFaKeys > S) {
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const int kc = k0 + 8 * j + 2 * (lane & 3);
-                if (kc >= S) { s[j][0] = -1e30f; s[j][2] = -1e30f; }
-                if (kc + 1 >= S) { s[j][1] = -1e30f; s[j][3] = -1e30f; }
-            }
-        }
-        // online softmax: rows g (c0,c1) and g+8 (c2,c3)
-        float mx[2] = {m_r[0], m_r[1]};
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            mx[0] = fmaxf(mx[0], fmaxf(s[j][0], s[j][1]));
-            mx[1] = fmaxf(mx[1], fmaxf(s[j][2], s[j][3]));
-        }
-#pragma unroll
-        for (int i = 0; i < 2; ++i) {
-            mx[i] = fmaxf(mx[i], __shfl_xor_sync(0xffffffffu, mx[i], 1));
-            mx[i] = fmaxf(mx[i], __shfl_xor_sync(0xffffffffu, mx[i], 2));
-        }
-        float alpha[2], rs[2] = {0.f, 0.f};
-#pragma unroll
-        for (int i = 0; i < 2; ++i) {
-            alpha[i] = exp2f((m_r[i] - mx[i]) * sc);
-            m_r[i] = mx[i];
-        }
-        uint32_t pf[4][4];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const float p0 = exp2f((s[j][0] - mx[0]) * sc), p1 = exp2f((s[j][1] - mx[0]) * sc);
-            const float p2 = exp2f((s[j][2] - mx[1]) * sc), p3 = exp2f((s[j][3] - mx[1]) * sc);
-            rs[0] += p0 + p1;
-            rs[1] += p2 + p3;
-            const int kt = j >> 1, hi = j & 1;
-            pf[kt][hi * 2 + 0] = pack_bf16x2(p0, p1);
-            pf[kt][hi * 2 + 1] = pack_bf16x2(p2, p3);
-        }
-#pragma unroll
-        for (int i = 0; i < 2; ++i) {
-            rs[i] += __shfl_xor_sync(0xffffffffu, rs[i], 1);
-            rs[i] += __shfl_xor_sync(0xffffffffu, rs[i], 2);
-            l_r[i] = l_r[i] * alpha[i] + rs[i];
-        }
-#pragma unroll
-        for (int dn = 0; dn < 8; ++dn) {
-            o[dn][0] *= alpha[0]; o[dn][1] *= alpha[0];
-            o[dn][2] *= alpha[1]; o[dn][3] *= alpha[1];
-        }
-#pragma unroll
-        for (int kt = 0; kt < 4; ++kt) {
-            // A fragment order: a0 (row g, keys lo), a1 (row g+8, lo), a2 (row g, hi), a3 (row g+8, hi)
-            const uint32_t a[4] = {pf[kt][0], pf[kt][1], pf[kt][2], pf[kt][3]};
-#pragma unroll
-            for (int dn = 0; dn < 8; dn += 2) {
-                const int mi = lane >> 3, rr = lane & 7;
-                const int key = 16 * kt + rr + (mi & 1) * 8;
-                const int ch = dn + (mi >> 1);
-                uint32_t b0, b1, b2, b3;
-                ldsm_x4_t(smem_u32(v_t + swz(key, ch)), b0, b1, b2, b3);
-                mma16816(o[dn], a, b0, b1);
-                mma16816(o[dn + 1], a, b2, b3);
-            }
-        }
-        __syncthreads();
-    }
-    // normalise and store
-    const int g = lane >> 2, t4 = lane & 3;
-    const float inv0 = 1.f / l_r[0], inv1 = 1.f / l_r[1];
-    const int r0 = q0 + warp * 16 + g, r1 = r0 + 8;
-    __nv_bfloat16* ob = out + chunk * S * (int64_t)d + h * 64;
-#pragma unroll
-    for (int dn = 0; dn < 8; ++dn) {
-        const int col = dn * 8 + 2 * t4;
-        if (r0 < S)
-            *reinterpret_cast<uint32_t*>(ob + (int64_t)r0 * d + col) = pack_bf16x2(o[dn][0] * inv0, o[dn][1] * inv0);
-        if (r1 < S)
-            *reinterpret_cast<uint32_t*>(ob + (int64_t)r1 * d + col) = pack_bf16x2(o[dn][2] * inv1, o[dn][3] * inv1);
-    }
-}
 
 // ------------------------------------------------------------------ row attention
 constexpr int kRowThreads = 256;
@@ -593,18 +402,6 @@ wb_status launch_rows(const void* q, int64_t q_ld, int64_t n_chunks, int rows_pe
 }
 
 }  // namespace
-
-wb_status attn_flash_enc_bf16(const void* qkv, int64_t n_chunks, int d, int heads, void* out,
-                              cudaStream_t s) {
-    if (n_chunks > 65535) return fail(WB_ERR_SHAPE, "too many chunks for one attention launch");
-    dim3 grid((kCtx + kFaRows - 1) / kFaRows, heads, (unsigned)n_chunks);
-    const int slot = prof_begin(WB_KERNEL_ENC_ATTN, s);
-    WB_CUDA(launch_k(flash_enc_kernel, dim3(grid), dim3(128), 0, s, reinterpret_cast<const __nv_bfloat16*>(qkv), d, kCtx,
-                                          reinterpret_cast<__nv_bfloat16*>(out)));
-    prof_end(slot, s, 4.0 * (double)kCtx * kCtx * 64.0 * heads * (double)n_chunks);
-    WB_CUDA(cudaGetLastError());
-    return WB_OK;
-}
 
 wb_status attn_rows(DType tq, DType tkv, DType to, const void* q, int64_t q_ld, int64_t n_chunks,
                     int rows_per_chunk, int heads, const KVView& kv, int kv_len, bool causal, int q_pos0,

@@ -3,6 +3,8 @@
 
 #include <stdint.h>
 
+#include <cuda.h>
+
 #include "internal.h"
 
 namespace wb {
@@ -34,9 +36,11 @@ struct KVView {
     const int32_t* active_len = nullptr;
 };
 
-// Encoder self-attention, bf16: qkv [n_chunks*1500, 3d] -> out [n_chunks*1500, d].
-wb_status attn_flash_enc_bf16(const void* qkv, int64_t n_chunks, int d, int heads, void* out,
-                              cudaStream_t s);
+// Encoder self-attention, bf16, on tcgen05 (TMEM accumulators, TMA-fed tiles):
+// qkv [n_chunks*1500, 3d] -> out [n_chunks*1500, d]; tma_qkv is a 2-D map over
+// the qkv buffer with 64 x 128 boxes.
+wb_status attn_flash_tc_bf16(const CUtensorMap* tma_qkv, int64_t n_chunks, int d, int heads, void* out,
+                             unsigned* err, cudaStream_t s);
 
 // Row attention: query row r of chunk c is q[(c*rows_per_chunk + r) * q_ld + h*64 ..]
 // (pre-scaling by 1/8 inside); it attends over keys 0..kv_len-1, or, when

@@ -448,6 +448,20 @@ wb_status encode_map(CUtensorMap* m, const void* ptr, int rank, const uint64_t* 
 
 int g_num_sms = 0;
 
+}  // namespace
+
+wb_status make_tma_2d_bf16(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, uint64_t row_stride_bytes,
+                           uint32_t box_inner, uint32_t box_outer) {
+    if (wb_status st = get_encoder()) return st;
+    if (!aligned16(ptr) || row_stride_bytes % 16) return fail(WB_ERR_ALIGN, "TMA operand alignment");
+    uint64_t dims[2] = {inner, outer};
+    uint64_t strides[1] = {row_stride_bytes};
+    uint32_t box[2] = {box_inner, box_outer};
+    return encode_map(m, ptr, 2, dims, strides, box, false);
+}
+
+namespace {
+
 template <int BN, bool FP8, bool SWAP>
 wb_status launch_tc(const GemmPlan& p, GemmArgs a, unsigned* err, cudaStream_t s, int max_ctas) {
     using C = Cfg<BN>;

@@ -83,4 +83,9 @@ wb_status gemm_simt(const GemmOperand& A, bool a_bf16, const GemmOperand& B, boo
 
 int num_sms();
 
+// 2-D bf16 TMA descriptor with the 128-byte swizzle: `outer` rows of
+// `inner` elements, rows `row_stride_bytes` apart, box box_inner x box_outer.
+wb_status make_tma_2d_bf16(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, uint64_t row_stride_bytes,
+                           uint32_t box_inner, uint32_t box_outer);
+
 }  // namespace wb
