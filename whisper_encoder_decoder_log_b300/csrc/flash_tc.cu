@@ -203,6 +203,7 @@ flash_tc_kernel(const __grid_constant__ CUtensorMap tma_qkv, int d, __nv_bfloat1
                 if (!wait_or_abort(&S.s_full[b], (j / kSBuf) & 1, abort_flag, err, WB_DEVERR_TIMEOUT_EPI)) { ok = false; break; }
                 tc_fence_after();
                 const int valid = min(kKeys, kCtx - j * kKeys);
+                const bool full = valid == kKeys;          // only the last tile is ragged
                 const uint32_t sa = tmem + lane_off + b * 128;
                 float mx = -INFINITY;
 #pragma unroll 1
@@ -210,13 +211,18 @@ flash_tc_kernel(const __grid_constant__ CUtensorMap tma_qkv, int d, __nv_bfloat1
                     uint32_t raw[32];
                     tmem_ld32(sa + cc * 32, raw);
                     tmem_wait_ld();
+                    if (full) {
 #pragma unroll
-                    for (int t = 0; t < 32; ++t)
-                        if (cc * 32 + t < valid) mx = fmaxf(mx, __uint_as_float(raw[t]));
+                        for (int t = 0; t < 32; ++t) mx = fmaxf(mx, __uint_as_float(raw[t]));
+                    } else {
+#pragma unroll
+                        for (int t = 0; t < 32; ++t)
+                            if (cc * 32 + t < valid) mx = fmaxf(mx, __uint_as_float(raw[t]));
+                    }
                 }
                 const float mn = fmaxf(m, mx * c);
-                const float alpha = exp2f(m - mn);          // 0 on the first tile
-                // P may be overwritten once PV_{j-2} has consumed it
+                const float alpha = ex2_fast(m - mn);      // 0 on the first tile (m = -inf)
+                // P may be overwritten once the previous PV has consumed it
                 if (!wait_or_abort(&S.p_empty[pbf], ((j / kPBuf) & 1) ^ 1, abort_flag, err, WB_DEVERR_TIMEOUT_EPI)) { ok = false; break; }
                 float sum = 0.f;
                 unsigned char* pb = S.p[pbf];
@@ -228,9 +234,13 @@ flash_tc_kernel(const __grid_constant__ CUtensorMap tma_qkv, int d, __nv_bfloat1
                     uint32_t pk[16];
 #pragma unroll
                     for (int t = 0; t < 32; t += 2) {
-                        const int col = cc * 32 + t;
-                        const float p0 = col < valid ? ex2_fast(__uint_as_float(raw[t]) * c - mn) : 0.f;
-                        const float p1 = col + 1 < valid ? ex2_fast(__uint_as_float(raw[t + 1]) * c - mn) : 0.f;
+                        float p0 = ex2_fast(fmaf(__uint_as_float(raw[t]), c, -mn));
+                        float p1 = ex2_fast(fmaf(__uint_as_float(raw[t + 1]), c, -mn));
+                        if (!full) {
+                            const int col = cc * 32 + t;
+                            if (col >= valid) p0 = 0.f;
+                            if (col + 1 >= valid) p1 = 0.f;
+                        }
                         sum += p0 + p1;
                         pk[t >> 1] = pack_bf16x2(p0, p1);
                     }
