@@ -243,7 +243,63 @@ struct Lin {
     const FP8Weight* f8 = nullptr;
     const float* a_scale = nullptr;
     bool split = false;           // a holds [hi | lo] bf16 halves: 2K columns, lda >= 2K
+    bool out_zeroed = false;      // the caller has zeroed a plain fp32 output already
 };
+
+// How linear_impl runs a GEMM: SIMT, swapped (few rows) or plain tcgen05, the
+// activation tile width and the K partitions.  Split-K adds fp32 partials
+// atomically, so a plain fp32 output must be zero before the launch.
+struct LinChoice {
+    bool simt = false, swap = false;
+    int bn = 0, ksplit = 1;
+    bool needs_zero = false;
+};
+
+LinChoice linear_choose(const Lin& L, const GemmEpi& e, bool simt_fp32) {
+    LinChoice c;
+    const bool f8 = L.f8 != nullptr;
+    if (simt_fp32 || L.K % (f8 ? 128 : 64) != 0) {
+        c.simt = true;
+        return c;
+    }
+    const int sms = num_sms();
+    const bool linear_f32 = (e.out_type == OUT_F32 || e.out_type == OUT_F32_ACC) && !e.gelu && !e.add &&
+                            e.mode == MODE_PLAIN;
+    const int64_t kb_all = (L.split ? 2 * L.K : L.K) / (f8 ? 128 : 64);
+    if (linear_f32 && L.batches == 1 && L.rows <= kSwapRows && !e.out_batch_rows && !e.out_row_offset) {
+        // few rows: weights as the 128-row MMA operand, rows as the MMA N
+        c.swap = true;
+        c.bn = L.rows <= 32 ? 32 : (L.rows <= 64 ? 64 : 128);
+        const int64_t tiles = ((L.N + 127) / 128) * ((L.rows + c.bn - 1) / c.bn);
+        // one CTA per SM, down to a single k-block per partition
+        const int64_t want = sms / tiles;
+        c.ksplit = (int)std::max<int64_t>(1, std::min<int64_t>(want, kb_all));
+    } else {
+        const int64_t tiles_m = ((L.rows + 127) / 128) * L.batches;
+        auto tiles = [&](int bn) { return tiles_m * ((L.N + bn - 1) / bn); };
+        c.bn = 256;
+        if (tiles(256) < sms) c.bn = 128;
+        if (tiles(128) < sms) c.bn = 64;
+        // split-K applies to linear fp32 epilogues; otherwise narrow the tiles
+        if (tiles(c.bn) < 2 * sms) {
+            if (linear_f32) {
+                c.ksplit = (int)std::min<int64_t>((2 * sms + tiles(c.bn) - 1) / tiles(c.bn),
+                                                  std::max<int64_t>(1, kb_all / 4));
+            } else if (tiles(32) <= 4 * sms) {
+                c.bn = 32;
+            }
+        }
+    }
+    c.needs_zero = c.ksplit > 1 && e.out_type == OUT_F32;
+    return c;
+}
+
+// Elements of the output that linear_impl zeroes (or that a caller zeroes
+// for it and flags with Lin::out_zeroed).
+int64_t linear_out_elems(const Lin& L, const GemmEpi& e) {
+    const int64_t obr = e.out_batch_rows ? e.out_batch_rows : L.rows;
+    return L.batches * obr * e.ldo;
+}
 
 wb_status linear_impl(const Lin& L, GemmEpi e, bool simt_fp32, unsigned* err, cudaStream_t s) {
     GemmOperand A;
@@ -257,59 +313,28 @@ wb_status linear_impl(const Lin& L, GemmEpi e, bool simt_fp32, unsigned* err, cu
     B.rows = L.N;
     B.row_stride = L.K;
     if (L.rows <= 0 || L.N <= 0) return WB_OK;
-    if (simt_fp32) return gemm_simt(A, false, B, false, L.N, L.K, e, s);
+    const LinChoice c = linear_choose(L, e, simt_fp32);
+    if (c.simt) {
+        if (simt_fp32) return gemm_simt(A, false, B, false, L.N, L.K, e, s);
+        if (L.f8) return fail(WB_ERR_UNSUPPORTED, "E4M3 GEMM needs K % 128 == 0");
+        if (L.split) return fail(WB_ERR_UNSUPPORTED, "split GEMM needs K % 64 == 0");
+        return gemm_simt(A, true, B, true, L.N, L.K, e, s);
+    }
     const bool f8 = L.f8 != nullptr;
     if (f8) {
         e.row_scale = L.a_scale;
         e.col_scale = L.f8->col_scale;
     }
-    if (L.K % (f8 ? 128 : 64) != 0) {
-        if (L.split) return fail(WB_ERR_UNSUPPORTED, "split GEMM needs K % 64 == 0");
-        return gemm_simt(A, true, B, true, L.N, L.K, e, s);
-    }
-    const int sms = num_sms();
-    const bool linear_f32 = (e.out_type == OUT_F32 || e.out_type == OUT_F32_ACC) && !e.gelu && !e.add &&
-                            e.mode == MODE_PLAIN;
-    const int64_t kb_all = (L.split ? 2 * L.K : L.K) / (f8 ? 128 : 64);
-    if (linear_f32 && L.batches == 1 && L.rows <= kSwapRows && !e.out_batch_rows && !e.out_row_offset) {
-        // few rows: weights as the 128-row MMA operand, rows as the MMA N
-        const int bn = L.rows <= 32 ? 32 : (L.rows <= 64 ? 64 : 128);
-        const int64_t tiles = ((L.N + 127) / 128) * ((L.rows + bn - 1) / bn);
-        int ksplit = 1;
-        const int64_t want = (sms + tiles - 1) / tiles;
-        if (want > 1)
-            for (int64_t d = want; d <= kb_all / 2; ++d)
-                if (kb_all % d == 0) { ksplit = (int)d; break; }
-        if (ksplit > 1 && e.out_type == OUT_F32)
-            if (wb_status st = fill(reinterpret_cast<float*>(e.out), L.rows * e.ldo, 0.f, s)) return st;
-        GemmPlan p;
-        if (wb_status st = gemm_plan_swap(&p, A, B, L.N, L.split ? 2 * L.K : L.K, f8, bn, L.split ? L.K : 0)) return st;
-        return gemm_run(p, e, err, s, 0, ksplit);
-    }
-    const int64_t tiles_m = ((L.rows + 127) / 128) * L.batches;
-    auto tiles = [&](int bn) { return tiles_m * ((L.N + bn - 1) / bn); };
-    int bn = 256;
-    if (tiles(256) < sms) bn = 128;
-    if (tiles(128) < sms) bn = 64;
-    // split-K applies to linear fp32 epilogues; otherwise narrow the tiles
-    const bool can_split = (e.out_type == OUT_F32 || e.out_type == OUT_F32_ACC) && !e.gelu && !e.add &&
-                           e.mode == MODE_PLAIN;
-    int ksplit = 1;
-    if (tiles(bn) < 2 * sms) {
-        if (can_split) {
-            ksplit = (int)std::min<int64_t>((2 * sms + tiles(bn) - 1) / tiles(bn), std::max<int64_t>(1, kb_all / 4));
-            while (ksplit > 1 && kb_all % ksplit) --ksplit;
-        } else if (tiles(32) <= 4 * sms) {
-            bn = 32;
-        }
-    }
-    if (ksplit > 1 && e.out_type == OUT_F32) {
-        const int64_t obr = e.out_batch_rows ? e.out_batch_rows : L.rows;
-        if (wb_status st = fill(reinterpret_cast<float*>(e.out), L.batches * obr * e.ldo, 0.f, s)) return st;
-    }
+    if (c.needs_zero && !L.out_zeroed)
+        if (wb_status st = fill(reinterpret_cast<float*>(e.out), linear_out_elems(L, e), 0.f, s)) return st;
     GemmPlan p;
-    if (wb_status st = gemm_plan(&p, A, B, L.N, L.split ? 2 * L.K : L.K, f8, bn, L.split ? L.K : 0)) return st;
-    return gemm_run(p, e, err, s, 0, ksplit);
+    if (c.swap) {
+        if (wb_status st = gemm_plan_swap(&p, A, B, L.N, L.split ? 2 * L.K : L.K, f8, c.bn, L.split ? L.K : 0))
+            return st;
+    } else {
+        if (wb_status st = gemm_plan(&p, A, B, L.N, L.split ? 2 * L.K : L.K, f8, c.bn, L.split ? L.K : 0)) return st;
+    }
+    return gemm_run(p, e, err, s, 0, c.ksplit);
 }
 
 wb_status linear(const wb_model* m, const Lin& L, GemmEpi e, cudaStream_t s) {
@@ -324,6 +349,26 @@ GemmEpi epi_out(void* out, int64_t ldo, int type, const float* bias, int gelu = 
     e.bias = bias;
     e.gelu = gelu;
     return e;
+}
+
+// LayerNorm of the residual into the GEMM input, then the GEMM; when the GEMM
+// splits K into an fp32 output, the LayerNorm launch zeroes that output too.
+wb_status ln_then_linear(const wb_model* m, const float* h, int64_t R, const std::string& ln, LnOut mode, void* a,
+                         int64_t lda, float* a_scale, Lin L, const GemmEpi& e, cudaStream_t s) {
+    const int d = m->d();
+    float* zero = nullptr;
+    int64_t zn = 0;
+    if (L.rows > 0 && L.N > 0) {
+        const LinChoice c = linear_choose(L, e, m->fp32());
+        if (c.needs_zero) {
+            zero = reinterpret_cast<float*>(e.out);
+            zn = linear_out_elems(L, e);
+            L.out_zeroed = true;
+        }
+    }
+    if (wb_status st = layernorm(h, d, R, d, m->V(ln + "g"), m->V(ln + "b"), mode, a, lda, a_scale, s, zero, zn))
+        return st;
+    return linear(m, L, e, s);
 }
 
 }  // namespace
@@ -467,35 +512,44 @@ wb_status decoder_layers(wb_decoder* dec, int64_t n_chunks, int rows_per_chunk, 
     const int64_t lda = sp ? 2 * d : d;                // row stride of LN / attention outputs
     for (int l = 0; l < m->desc.dec_layers; ++l) {
         // ---- self-attention
-        if (wb_status st = layernorm(dec->h, d, R, d, m->V(nm("dec.", l, "ln1.g")), m->V(nm("dec.", l, "ln1.b")),
-                                     f8 ? LN_E4M3 : ln_act, dec->a, f8 ? d : lda, dec->a_scale, s))
-            return st;
         {
             Lin L;
             L.a = dec->a; L.rows = R; L.w = m->W(nm("dec.", l, "sq.w")); L.N = 3 * d; L.K = d;
             if (f8) { L.f8 = &m->dec_qkv[l]; L.a_scale = dec->a_scale; L.lda = d; }
             else { L.lda = lda; L.split = sp; }
-            if (wb_status st = linear(m, L, epi_out(dec->qkv, 3 * d, OUT_F32, m->V(nm("dec.", l, "sq.b"))), s)) return st;
+            const GemmEpi e = epi_out(dec->qkv, 3 * d, OUT_F32, m->V(nm("dec.", l, "sq.b")));
+            if (wb_status st = ln_then_linear(m, dec->h, R, nm("dec.", l, "ln1."), f8 ? LN_E4M3 : ln_act, dec->a,
+                                              f8 ? d : lda, dec->a_scale, L, e, s))
+                return st;
         }
         const bool kv8 = m->desc.kv_fp8 != 0;
         float* ks = dec->kscale + (int64_t)l * dec->B;
         float* vs = dec->vscale + (int64_t)l * dec->B;
         if (kv8 && set_scales)
             if (wb_status st = kv_scales(dec->qkv, n_chunks, rows_per_chunk, d, ks, vs, s)) return st;
-        if (wb_status st = kv_append(dec->qkv, n_chunks, rows_per_chunk, p0, d, H, l, kv8, dec->cache, dec->off,
-                                     dec->len_dev, ks, vs, m->err, s, pos_dev))
-            return st;
+        // a decode step over the E4M3 cache appends inside the attention kernel
+        const bool fused_step = kv8 && rows_per_chunk == 1 && !f32;
+        if (!fused_step)
+            if (wb_status st = kv_append(dec->qkv, n_chunks, rows_per_chunk, p0, d, H, l, kv8, dec->cache, dec->off,
+                                         dec->len_dev, ks, vs, m->err, s, pos_dev))
+                return st;
         {
             KVView kv;
             kv.ptr = dec->cache; kv.chunk_off = dec->off; kv.head_stride = 64; kv.chunk_len = dec->len_dev;
             kv.heads = H; kv.k_blk = 2 * l; kv.v_blk = 2 * l + 1; kv.row_stride = 64;
             if (kv8) { kv.k_scale = ks; kv.v_scale = vs; }
             if (pos_dev) { kv.pos_dev = pos_dev; kv.active_len = dec->len_dev; }
+            if (fused_step) {
+                if (wb_status st = attn_self_step_e4m3(dec->qkv, 3 * d, n_chunks, H, kv, p0, dec->attn, lda, s,
+                                                       sp ? d : 0))
+                    return st;
+            } else {
             // with a device-side position the score buffer is sized for the longest chunk
             const int kv_len = pos_dev ? dec->max_len : p0 + rows_per_chunk;
             if (wb_status st = attn_rows(DT_F32, kv8 ? DT_E4M3 : DT_F32, attn_dt, dec->qkv, 3 * d, n_chunks,
                                          rows_per_chunk, H, kv, kv_len, true, p0, dec->attn, lda, s, sp ? d : 0))
                 return st;
+            }
         }
         {
             Lin L;
@@ -503,13 +557,12 @@ wb_status decoder_layers(wb_decoder* dec, int64_t n_chunks, int rows_per_chunk, 
             if (wb_status st = linear(m, L, epi_out(dec->h, d, OUT_F32_ACC, m->V(nm("dec.", l, "so.b"))), s)) return st;
         }
         // ---- cross-attention
-        if (wb_status st = layernorm(dec->h, d, R, d, m->V(nm("dec.", l, "ln2.g")), m->V(nm("dec.", l, "ln2.b")),
-                                     ln_act, dec->a, lda, nullptr, s))
-            return st;
         {
             Lin L;
             L.a = dec->a; L.rows = R; L.lda = lda; L.split = sp; L.w = m->W(nm("dec.", l, "cq.w")); L.N = d; L.K = d;
-            if (wb_status st = linear(m, L, epi_out(dec->cq, d, OUT_F32, m->V(nm("dec.", l, "cq.b"))), s)) return st;
+            const GemmEpi e = epi_out(dec->cq, d, OUT_F32, m->V(nm("dec.", l, "cq.b")));
+            if (wb_status st = ln_then_linear(m, dec->h, R, nm("dec.", l, "ln2."), ln_act, dec->a, lda, nullptr, L, e, s))
+                return st;
         }
         {
             const size_t act = f32 ? 4 : 2;
@@ -528,45 +581,33 @@ wb_status decoder_layers(wb_decoder* dec, int64_t n_chunks, int rows_per_chunk, 
             if (wb_status st = linear(m, L, epi_out(dec->h, d, OUT_F32_ACC, m->V(nm("dec.", l, "co.b"))), s)) return st;
         }
         // ---- FFN
-        if (wb_status st = layernorm(dec->h, d, R, d, m->V(nm("dec.", l, "ln3.g")), m->V(nm("dec.", l, "ln3.b")),
-                                     f8 ? LN_E4M3 : ln_act, dec->a, f8 ? d : lda, dec->a_scale, s))
-            return st;
         // FC1 (+GELU): with few rows the swapped GEMM writes fp32 and a
         // post-pass applies GELU (and the bf16 split); otherwise GELU is fused
         const bool few = R <= kSwapRows && !f32;
+        Lin L1;
+        L1.a = dec->a; L1.rows = R; L1.w = m->W(nm("dec.", l, "fc1.w")); L1.N = F; L1.K = d;
+        if (f8) { L1.lda = d; L1.f8 = &m->dec_fc1[l]; L1.a_scale = dec->a_scale; }
+        else { L1.lda = lda; L1.split = sp; }
+        const int64_t ldf = sp ? 2 * F : F;
+        void* fin = f32 ? dec->f : dec->f2;          // FC2 input (bf16 models)
+        float* f32buf = reinterpret_cast<float*>(dec->f);
+        const float* b1 = m->V(nm("dec.", l, "fc1.b"));
+        const GemmEpi e1 = (few || f8) ? epi_out(f32buf, F, OUT_F32, b1, few ? 0 : 1)
+                                       : epi_out(fin, ldf, f32 ? OUT_F32 : OUT_BF16X2, b1, 1);
+        if (wb_status st = ln_then_linear(m, dec->h, R, nm("dec.", l, "ln3."), f8 ? LN_E4M3 : ln_act, dec->a,
+                                          f8 ? d : lda, dec->a_scale, L1, e1, s))
+            return st;
+        if (few)
+            if (wb_status st = gelu_post(f32buf, R, F, f8 ? nullptr : dec->f2, s)) return st;
+        Lin L2;
+        L2.rows = R; L2.w = m->W(nm("dec.", l, "fc2.w")); L2.N = d; L2.K = F;
         if (f8) {
-            Lin L1;
-            L1.a = dec->a; L1.rows = R; L1.lda = d; L1.w = m->W(nm("dec.", l, "fc1.w")); L1.N = F; L1.K = d;
-            L1.f8 = &m->dec_fc1[l]; L1.a_scale = dec->a_scale;
-            float* f32buf = reinterpret_cast<float*>(dec->f);
-            if (few) {
-                if (wb_status st = linear(m, L1, epi_out(f32buf, F, OUT_F32, m->V(nm("dec.", l, "fc1.b"))), s)) return st;
-                if (wb_status st = gelu_post(f32buf, R, F, nullptr, s)) return st;
-            } else {
-                if (wb_status st = linear(m, L1, epi_out(f32buf, F, OUT_F32, m->V(nm("dec.", l, "fc1.b")), 1), s)) return st;
-            }
             if (wb_status st = quant_rows_f32(f32buf, R, F, dec->fq, dec->f_scale, s)) return st;
-            Lin L2;
-            L2.a = dec->fq; L2.rows = R; L2.lda = F; L2.w = m->W(nm("dec.", l, "fc2.w")); L2.N = d; L2.K = F;
-            L2.f8 = &m->dec_fc2[l]; L2.a_scale = dec->f_scale;
-            if (wb_status st = linear(m, L2, epi_out(dec->h, d, OUT_F32_ACC, m->V(nm("dec.", l, "fc2.b"))), s)) return st;
+            L2.a = dec->fq; L2.lda = F; L2.f8 = &m->dec_fc2[l]; L2.a_scale = dec->f_scale;
         } else {
-            Lin L1;
-            L1.a = dec->a; L1.rows = R; L1.lda = lda; L1.split = sp; L1.w = m->W(nm("dec.", l, "fc1.w")); L1.N = F; L1.K = d;
-            const int64_t ldf = sp ? 2 * F : F;
-            void* fin = f32 ? dec->f : dec->f2;
-            if (few) {
-                float* f32buf = reinterpret_cast<float*>(dec->f);
-                if (wb_status st = linear(m, L1, epi_out(f32buf, F, OUT_F32, m->V(nm("dec.", l, "fc1.b"))), s)) return st;
-                if (wb_status st = gelu_post(f32buf, R, F, dec->f2, s)) return st;
-            } else {
-                const int fout = f32 ? OUT_F32 : OUT_BF16X2;
-                if (wb_status st = linear(m, L1, epi_out(fin, ldf, fout, m->V(nm("dec.", l, "fc1.b")), 1), s)) return st;
-            }
-            Lin L2;
-            L2.a = fin; L2.rows = R; L2.lda = ldf; L2.split = sp; L2.w = m->W(nm("dec.", l, "fc2.w")); L2.N = d; L2.K = F;
-            if (wb_status st = linear(m, L2, epi_out(dec->h, d, OUT_F32_ACC, m->V(nm("dec.", l, "fc2.b"))), s)) return st;
+            L2.a = fin; L2.lda = ldf; L2.split = sp;
         }
+        if (wb_status st = linear(m, L2, epi_out(dec->h, d, OUT_F32_ACC, m->V(nm("dec.", l, "fc2.b"))), s)) return st;
     }
     return WB_OK;
 }

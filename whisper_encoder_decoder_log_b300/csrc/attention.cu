@@ -349,6 +349,147 @@ self_attn_e4m3_kernel(const float* __restrict__ q, int64_t q_ld, int heads, KVVi
     }
 }
 
+// Decode step, causal self-attention over the E4M3 cache, with the cache
+// append of the current token fused in.  One warp per (chunk, head), kStepHeads
+// heads per CTA.  Lane = (row r of 8, sub s of 4): a pass covers 8 cache rows
+// and each lane reads 16 bytes of K and of V; loads run kStepDepth passes
+// ahead of the arithmetic.  The current token's K and V rows (fp32 in the QKV
+// output) are quantised here with the chunk's scales, exactly as the append
+// kernel does, written to cache row pos, and used from registers at j = pos.
+constexpr int kStepHeads = 4;
+constexpr int kStepDepth = 4;
+
+WB_DEV void e4m3x16_to_f32(const uint4& w, float (&f)[16]) {
+    const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        __nv_fp8x4_e4m3 a;
+        a.__x = u[i];
+        const float4 fa = static_cast<float4>(a);
+        f[4 * i] = fa.x; f[4 * i + 1] = fa.y; f[4 * i + 2] = fa.z; f[4 * i + 3] = fa.w;
+    }
+}
+
+WB_DEV uint4 quant16(const float* x, float inv) {
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float4 t = *reinterpret_cast<const float4*>(x + 4 * i);
+        const uint32_t lo = f2e4m3x2(t.x * inv, t.y * inv), hi = f2e4m3x2(t.z * inv, t.w * inv);
+        w[i] = (lo & 0xFFFFu) | (hi << 16);
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+template <typename TO>
+__global__ void __launch_bounds__(32 * kStepHeads)
+self_attn_step_kernel(const float* __restrict__ qkv, int64_t q_ld, int heads, KVView kv, int q_pos_host,
+                      TO* __restrict__ out, int64_t o_ld, int64_t o_split) {
+    griddep_wait();
+    griddep_launch();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t chunk = blockIdx.x;
+    const int h = blockIdx.y * kStepHeads + warp;
+    if (h >= heads) return;
+    const int pos = kv.pos_dev ? *kv.pos_dev : q_pos_host;
+    if (kv.active_len && kv.active_len[chunk] <= pos + 1) return;   // finished chunk
+    const int L = kv.chunk_len[chunk];
+    if (pos >= L) return;                                          // no cache row for this position
+    const int r = lane >> 2, sub = lane & 3;
+    const int d = heads * 64;
+    const int64_t hs = kv.head_stride * (int64_t)L;
+    uint8_t* base = const_cast<uint8_t*>(reinterpret_cast<const uint8_t*>(kv.ptr)) + kv.chunk_off[chunk];
+    uint8_t* Kp = base + ((int64_t)kv.k_blk * kv.heads + h) * hs;
+    uint8_t* Vp = base + ((int64_t)kv.v_blk * kv.heads + h) * hs;
+    const float ks = kv.k_scale[chunk], vs = kv.v_scale[chunk];
+    const float* qr = qkv + chunk * q_ld + h * 64 + sub * 16;
+    // the current token's cache rows, quantised as the append kernel does
+    const uint4 kcur = quant16(qr + d, 1.0f / ks);
+    const uint4 vcur = quant16(qr + 2 * d, 1.0f / vs);
+    if (r == 0) {
+        *reinterpret_cast<uint4*>(Kp + (int64_t)pos * 64 + sub * 16) = kcur;
+        *reinterpret_cast<uint4*>(Vp + (int64_t)pos * 64 + sub * 16) = vcur;
+    }
+    float qv[16];
+#pragma unroll
+    for (int i = 0; i < 16; i += 4) {
+        const float4 t = *reinterpret_cast<const float4*>(qr + i);
+        // fold the 1/sqrt(64) and the K scale into q
+        qv[i] = t.x * 0.125f * ks; qv[i + 1] = t.y * 0.125f * ks; qv[i + 2] = t.z * 0.125f * ks; qv[i + 3] = t.w * 0.125f * ks;
+    }
+    const int nk = pos + 1;
+    const int npass = (nk + 7) >> 3;
+    auto load = [&](int pass, uint4& kr, uint4& vr) {
+        const int j = pass * 8 + r;
+        kr = make_uint4(0, 0, 0, 0);
+        vr = kr;
+        if (j < pos) {
+            kr = ld_stream(Kp + (int64_t)j * 64 + sub * 16);
+            vr = ld_stream(Vp + (int64_t)j * 64 + sub * 16);
+        } else if (j == pos) {
+            kr = kcur;
+            vr = vcur;
+        }
+    };
+    uint4 kb[kStepDepth], vb[kStepDepth];
+#pragma unroll
+    for (int u = 0; u < kStepDepth; ++u) load(u, kb[u], vb[u]);
+    float m = -INFINITY, l = 0.f, o[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) o[i] = 0.f;
+    for (int p0 = 0; p0 < npass; p0 += kStepDepth) {
+#pragma unroll
+        for (int u = 0; u < kStepDepth; ++u) {
+            const int pass = p0 + u;
+            if (pass < npass) {     // uniform across the warp
+                const bool valid = pass * 8 + r < nk;
+                float kf[16], vf[16];
+                e4m3x16_to_f32(kb[u], kf);
+                e4m3x16_to_f32(vb[u], vf);
+                load(pass + kStepDepth, kb[u], vb[u]);
+                float sc = 0.f;
+#pragma unroll
+                for (int i = 0; i < 16; ++i) sc = fmaf(qv[i], kf[i], sc);
+                sc += __shfl_xor_sync(0xffffffffu, sc, 1);
+                sc += __shfl_xor_sync(0xffffffffu, sc, 2);
+                if (!valid) sc = -INFINITY;
+                float pm = sc;     // max over the 8 rows of the pass
+                pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 4));
+                pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 8));
+                pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 16));
+                const float mn = fmaxf(m, pm);
+                const float alpha = __expf(m - mn);     // 0 on the first pass (m = -inf)
+                const float pr = valid ? __expf(sc - mn) : 0.f;
+                float ps = pr;
+                ps += __shfl_xor_sync(0xffffffffu, ps, 4);
+                ps += __shfl_xor_sync(0xffffffffu, ps, 8);
+                ps += __shfl_xor_sync(0xffffffffu, ps, 16);
+                l = l * alpha + ps;
+                m = mn;
+#pragma unroll
+                for (int i = 0; i < 16; ++i) o[i] = fmaf(pr, vf[i], o[i] * alpha);
+            }
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        o[i] += __shfl_xor_sync(0xffffffffu, o[i], 4);
+        o[i] += __shfl_xor_sync(0xffffffffu, o[i], 8);
+        o[i] += __shfl_xor_sync(0xffffffffu, o[i], 16);
+    }
+    if (r == 0) {
+        const float sc = vs / l;
+        TO* orow = out + chunk * o_ld + h * 64 + sub * 16;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const float a = o[i] * sc;
+            const TO hi = (TO)a;
+            orow[i] = hi;
+            if (o_split) orow[o_split + i] = (TO)(a - (float)hi);
+        }
+    }
+}
+
 template <int NQ, typename TQ, typename TKV, typename TO>
 wb_status launch_rows_nq(const void* q, int64_t q_ld, int64_t n_chunks, int rows_per_chunk, int heads,
                          const KVView& kv, int kv_len, bool causal, int q_pos0, void* out, int64_t o_ld,
@@ -402,6 +543,22 @@ wb_status launch_rows(const void* q, int64_t q_ld, int64_t n_chunks, int rows_pe
 }
 
 }  // namespace
+
+wb_status attn_self_step_e4m3(const float* qkv, int64_t q_ld, int64_t n_chunks, int heads, const KVView& kv,
+                              int q_pos, void* out, int64_t o_ld, cudaStream_t s, int64_t o_split) {
+    if (n_chunks <= 0) return WB_OK;
+    if (!kv.chunk_off || !kv.chunk_len || !kv.k_scale || !kv.v_scale || kv.head_stride != 64 || kv.row_stride != 64)
+        return fail(WB_ERR_INVALID_ARG, "step self-attention needs a ragged E4M3 cache with scales");
+    if ((q_ld % 4) || !aligned16(qkv) || !aligned16(kv.ptr)) return fail(WB_ERR_ALIGN, "step self-attention operands");
+    if (n_chunks > 0x7FFFFFFF || heads > 65535 * kStepHeads) return fail(WB_ERR_SHAPE, "attention grid too large");
+    const dim3 grid((unsigned)n_chunks, (unsigned)((heads + kStepHeads - 1) / kStepHeads));
+    const int slot = prof_begin(WB_KERNEL_SELF_ATTN, s);
+    WB_CUDA(launch_k(self_attn_step_kernel<__nv_bfloat16>, grid, dim3(32 * kStepHeads), 0, s, qkv, q_ld, heads, kv,
+                     q_pos, reinterpret_cast<__nv_bfloat16*>(out), o_ld, o_split));
+    prof_end(slot, s, (double)n_chunks * heads * (2.0 * q_pos * 64.0 + 2.0 * 64.0 * (4 + 1) + 64.0 * (4 + 2)));
+    WB_CUDA(cudaGetLastError());
+    return WB_OK;
+}
 
 wb_status attn_rows(DType tq, DType tkv, DType to, const void* q, int64_t q_ld, int64_t n_chunks,
                     int rows_per_chunk, int heads, const KVView& kv, int kv_len, bool causal, int q_pos0,

@@ -49,4 +49,12 @@ wb_status attn_rows(DType tq, DType tkv, DType to, const void* q, int64_t q_ld, 
                     int rows_per_chunk, int heads, const KVView& kv, int kv_len, bool causal, int q_pos0,
                     void* out, int64_t o_ld, cudaStream_t s, int64_t o_split = 0);
 
+// Decode step (one query row per chunk at position pos = *kv.pos_dev, else
+// q_pos): quantises the token's K and V rows of qkv [n_chunks, 3d] (fp32) to
+// E4M3 with the chunk's scales, writes them to cache row pos, and attends over
+// cache rows 0..pos; output bf16 (plus the bf16 remainder at o_split when
+// o_split > 0).  Needs a ragged cache view (chunk_off, chunk_len, scales).
+wb_status attn_self_step_e4m3(const float* qkv, int64_t q_ld, int64_t n_chunks, int heads, const KVView& kv,
+                              int q_pos, void* out, int64_t o_ld, cudaStream_t s, int64_t o_split);
+
 }  // namespace wb

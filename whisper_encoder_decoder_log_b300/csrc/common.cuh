@@ -114,13 +114,14 @@ WB_DEV uint64_t globaltimer_ns() {
     return t;
 }
 
-// Deadline helper: expired() is true once WB_WAIT_NS have passed since
-// construction (the clock is read every 64 polls).
+// Deadline helper: expired() is true once WB_WAIT_NS have passed since the
+// 64th poll.  The clock is read every 64 polls and never on the first one, so
+// a wait that is already satisfied costs no timer read.
 struct WaitClock {
     uint64_t t0 = 0;
     uint32_t n = 0;
     WB_DEV bool expired() {
-        if ((++n & 63u) != 1u) return false;
+        if ((++n & 63u) != 0u) return false;
         const uint64_t t = globaltimer_ns();
         if (t0 == 0) { t0 = t; return false; }
         return t - t0 > WB_WAIT_NS;

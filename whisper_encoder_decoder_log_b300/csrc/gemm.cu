@@ -49,7 +49,8 @@ struct GemmArgs {
     int64_t batches;
     int64_t N, K;
     int64_t mt_per_batch, mt_total, nt_total, tiles;
-    int kblocks;            // k-blocks per split
+    int kblocks;            // k-blocks of the longest split
+    int kb_all;             // k-blocks of the whole K
     int ksplit;             // K partitions; > 1 adds partial tiles atomically
     int stages;             // smem ring depth (<= the compile-time maximum)
     int b_kwrap;
@@ -211,6 +212,14 @@ __device__ __forceinline__ void store_swap(const GemmArgs& a, int64_t n, int64_t
     }
 }
 
+// K partition of tile t: k-blocks [kb0, kb1).  Partitions differ by at most
+// one k-block, so any ksplit <= kb_all spreads K evenly.
+__device__ __forceinline__ void split_range(const GemmArgs& a, int64_t t, int& kb0, int& kb1) {
+    const int ks = (int)(t % a.ksplit);
+    kb0 = (int)((int64_t)ks * a.kb_all / a.ksplit);
+    kb1 = (int)((int64_t)(ks + 1) * a.kb_all / a.ksplit);
+}
+
 constexpr int kEpiWarps = 8;                       // two per TMEM lane quarter
 constexpr int kGemmThreads = 64 + 32 * kEpiWarps;  // producer + MMA + epilogue
 
@@ -275,8 +284,9 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant_
                 const int b = (int)(mt / args.mt_per_batch);
                 const int r0 = (int)((mt % args.mt_per_batch) * kBM);
                 const int n0 = (int)(nt * BN);
-                const int kb0 = (int)(t % args.ksplit) * args.kblocks;
-                for (int kb = kb0; kb < kb0 + args.kblocks; ++kb) {
+                int kb0, kb1;
+                split_range(args, t, kb0, kb1);
+                for (int kb = kb0; kb < kb1; ++kb) {
                     bool got = false;
                     for (WaitClock clk; !clk.expired();) {
                         if (mbar_try_wait(&empty_bar[stage], phase ^ 1)) { got = true; break; }
@@ -329,7 +339,9 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant_
                 if (!got) { wb_set_error(err, WB_DEVERR_TIMEOUT_MMA); *abort_flag = 1; break; }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * BN;
-                for (int kb = 0; kb < args.kblocks; ++kb) {
+                int kb0, kb1;
+                split_range(args, t, kb0, kb1);
+                for (int kb = 0; kb < kb1 - kb0; ++kb) {
                     got = false;
                     for (WaitClock clk; !clk.expired();) {
                         if (mbar_try_wait(&full_bar[stage], phase)) { got = true; break; }
@@ -597,11 +609,12 @@ wb_status gemm_run(const GemmPlan& p, const GemmEpi& epi, unsigned* err, cudaStr
     if (ksplit > 1) {
         if (epi.out_type != OUT_F32 && epi.out_type != OUT_F32_ACC) return fail(WB_ERR_INVALID_ARG, "split-K needs fp32 output");
         if (epi.gelu || epi.add || epi.mode != MODE_PLAIN) return fail(WB_ERR_INVALID_ARG, "split-K: linear epilogue only");
-        while (ksplit > 1 && kb_all % ksplit) --ksplit;
+        if (ksplit > kb_all) ksplit = kb_all;
     }
     a.ksplit = ksplit;
     a.tiles = a.mt_total * a.nt_total * ksplit;
-    a.kblocks = kb_all / ksplit;
+    a.kb_all = kb_all;
+    a.kblocks = (kb_all + ksplit - 1) / ksplit;
     a.b_kwrap = (int)p.b_kwrap;
     a.epi = epi;
     const bool half = epi.out_type == OUT_BF16 || epi.out_type == OUT_BF16X2;
@@ -740,6 +753,7 @@ wb_status gemm_simt(const GemmOperand& A, bool a_bf16, const GemmOperand& B, boo
     a.nt_total = (N + 63) / 64;
     a.tiles = a.mt_total * a.nt_total;
     a.kblocks = 0;
+    a.kb_all = 0;
     a.b_kwrap = 0;
     a.epi = epi;
     if (epi.out_type == OUT_BF16X2) return fail(WB_ERR_UNSUPPORTED, "SIMT GEMM: no split output");

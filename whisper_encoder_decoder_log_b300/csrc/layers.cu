@@ -19,6 +19,88 @@ namespace {
 
 constexpr int kMaxPerLane = 40;   // d <= 1280
 
+// Vector form for d % 128 == 0: one warp per row, VPL float4 per lane, the
+// gain and shift fetched together with the row so that one memory round trip
+// covers all three.  Optionally zeroes `zero` (n4 float4) on the side: the
+// next GEMM's split-K output, which would otherwise need a launch of its own.
+template <int OUT, int VPL>
+__global__ void __launch_bounds__(128)
+layernorm_vec_kernel(const float* __restrict__ x, int64_t ld_x, int64_t rows, const float* __restrict__ g,
+                     const float* __restrict__ b, void* __restrict__ out, int64_t ld_o, float* __restrict__ row_scale,
+                     float4* __restrict__ zero, int64_t zero_n4) {
+    griddep_wait();
+    griddep_launch();
+    if (zero) {
+        const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < zero_n4; i += (int64_t)gridDim.x * blockDim.x)
+            zero[i] = z;
+    }
+    const int64_t row = (int64_t)blockIdx.x * 4 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (row >= rows) return;
+    constexpr int d = VPL * 128;
+    const float4* xr = reinterpret_cast<const float4*>(x + row * ld_x);
+    const float4* g4 = reinterpret_cast<const float4*>(g);
+    const float4* b4 = reinterpret_cast<const float4*>(b);
+    float4 v[VPL], gv[VPL], bv[VPL];
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) {
+        v[i] = xr[i * 32 + lane];
+        gv[i] = g4[i * 32 + lane];
+        bv[i] = b4[i * 32 + lane];
+    }
+    float s = 0.f;
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) s += (v[i].x + v[i].y) + (v[i].z + v[i].w);
+    const float mean = warp_sum(s) / (float)d;
+    float q = 0.f;
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) {
+        const float a = v[i].x - mean, c = v[i].y - mean, e = v[i].z - mean, f = v[i].w - mean;
+        q = fmaf(a, a, q); q = fmaf(c, c, q); q = fmaf(e, e, q); q = fmaf(f, f, q);
+    }
+    const float rstd = rsqrtf(warp_sum(q) / (float)d + 1e-5f);
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) {
+        v[i].x = (v[i].x - mean) * rstd * gv[i].x + bv[i].x;
+        v[i].y = (v[i].y - mean) * rstd * gv[i].y + bv[i].y;
+        v[i].z = (v[i].z - mean) * rstd * gv[i].z + bv[i].z;
+        v[i].w = (v[i].w - mean) * rstd * gv[i].w + bv[i].w;
+        amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v[i].x), fabsf(v[i].y)), fmaxf(fabsf(v[i].z), fabsf(v[i].w))));
+    }
+    if (OUT == LN_F32) {
+        float4* o = reinterpret_cast<float4*>(reinterpret_cast<float*>(out) + row * ld_o);
+#pragma unroll
+        for (int i = 0; i < VPL; ++i) o[i * 32 + lane] = v[i];
+    } else if (OUT == LN_BF16 || OUT == LN_BF16X2) {
+        __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(out) + row * ld_o;
+#pragma unroll
+        for (int i = 0; i < VPL; ++i) {
+            const int c = (i * 32 + lane) * 4;
+            const uint32_t h0 = pack_bf16x2(v[i].x, v[i].y), h1 = pack_bf16x2(v[i].z, v[i].w);
+            *reinterpret_cast<uint2*>(o + c) = make_uint2(h0, h1);
+            if (OUT == LN_BF16X2) {
+                const float r0 = v[i].x - __uint_as_float(h0 << 16), r1 = v[i].y - __uint_as_float(h0 & 0xFFFF0000u);
+                const float r2 = v[i].z - __uint_as_float(h1 << 16), r3 = v[i].w - __uint_as_float(h1 & 0xFFFF0000u);
+                *reinterpret_cast<uint2*>(o + d + c) = make_uint2(pack_bf16x2(r0, r1), pack_bf16x2(r2, r3));
+            }
+        }
+    } else {   // LN_E4M3: per-row scale amax / 448
+        amax = warp_max(amax);
+        const float sc = amax > 0.f ? amax / 448.0f : 1.0f;
+        const float inv = 1.0f / sc;
+        uint8_t* o = reinterpret_cast<uint8_t*>(out) + row * ld_o;
+#pragma unroll
+        for (int i = 0; i < VPL; ++i) {
+            const uint32_t lo = f2e4m3x2(v[i].x * inv, v[i].y * inv) & 0xFFFFu;
+            const uint32_t hi = f2e4m3x2(v[i].z * inv, v[i].w * inv) & 0xFFFFu;
+            *reinterpret_cast<uint32_t*>(o + (i * 32 + lane) * 4) = lo | (hi << 16);
+        }
+        if (lane == 0) row_scale[row] = sc;
+    }
+}
+
 // One warp per row; the row lives in registers for the two-pass moments.
 template <int OUT>
 __global__ void __launch_bounds__(256)
@@ -363,12 +445,52 @@ int grid_for(int64_t n, int threads) {
     return (int)(g < 1 ? 1 : g);
 }
 
+template <int OUT>
+wb_status launch_ln_vec(int vpl, const float* x, int64_t ld_x, int64_t rows, const float* g, const float* b, void* out,
+                        int64_t ld_o, float* row_scale, float* zero, int64_t zero_n, cudaStream_t s) {
+    const dim3 grid((unsigned)((rows + 3) / 4)), block(128);
+    float4* z = reinterpret_cast<float4*>(zero);
+    const int64_t z4 = zero ? zero_n / 4 : 0;
+    switch (vpl) {
+    case 1: return launch_k(layernorm_vec_kernel<OUT, 1>, grid, block, 0, s, x, ld_x, rows, g, b, out, ld_o, row_scale, z, z4) ? WB_ERR_CUDA : WB_OK;
+    case 2: return launch_k(layernorm_vec_kernel<OUT, 2>, grid, block, 0, s, x, ld_x, rows, g, b, out, ld_o, row_scale, z, z4) ? WB_ERR_CUDA : WB_OK;
+    case 3: return launch_k(layernorm_vec_kernel<OUT, 3>, grid, block, 0, s, x, ld_x, rows, g, b, out, ld_o, row_scale, z, z4) ? WB_ERR_CUDA : WB_OK;
+    case 4: return launch_k(layernorm_vec_kernel<OUT, 4>, grid, block, 0, s, x, ld_x, rows, g, b, out, ld_o, row_scale, z, z4) ? WB_ERR_CUDA : WB_OK;
+    case 5: return launch_k(layernorm_vec_kernel<OUT, 5>, grid, block, 0, s, x, ld_x, rows, g, b, out, ld_o, row_scale, z, z4) ? WB_ERR_CUDA : WB_OK;
+    case 6: return launch_k(layernorm_vec_kernel<OUT, 6>, grid, block, 0, s, x, ld_x, rows, g, b, out, ld_o, row_scale, z, z4) ? WB_ERR_CUDA : WB_OK;
+    case 8: return launch_k(layernorm_vec_kernel<OUT, 8>, grid, block, 0, s, x, ld_x, rows, g, b, out, ld_o, row_scale, z, z4) ? WB_ERR_CUDA : WB_OK;
+    case 10: return launch_k(layernorm_vec_kernel<OUT, 10>, grid, block, 0, s, x, ld_x, rows, g, b, out, ld_o, row_scale, z, z4) ? WB_ERR_CUDA : WB_OK;
+    default: return WB_ERR_UNSUPPORTED;
+    }
+}
+
+bool ln_vec_ok(int d) { return d % 128 == 0 && (d / 128 <= 6 || d / 128 == 8 || d / 128 == 10); }
+
 }  // namespace
 
 wb_status layernorm(const float* x, int64_t ld_x, int64_t rows, int d, const float* g, const float* b, LnOut mode,
-                    void* out, int64_t ld_o, float* row_scale, cudaStream_t s) {
-    if (rows <= 0) return WB_OK;
+                    void* out, int64_t ld_o, float* row_scale, cudaStream_t s, float* zero, int64_t zero_n) {
+    if (rows <= 0) {
+        if (zero && zero_n > 0) return fill(zero, zero_n, 0.f, s);
+        return WB_OK;
+    }
     if (d % 32 || d > 32 * kMaxPerLane) return fail(WB_ERR_SHAPE, "LayerNorm width must be a multiple of 32, <= 1280");
+    const int osz = mode == LN_F32 ? 4 : (mode == LN_E4M3 ? 1 : 2);
+    const bool vec = ln_vec_ok(d) && aligned16(x) && aligned16(g) && aligned16(b) && aligned16(out) && ld_x % 4 == 0 &&
+                     (ld_o * osz) % 16 == 0 && (!zero || (aligned16(zero) && zero_n % 4 == 0));
+    if (vec) {
+        wb_status st;
+        const int vpl = d / 128;
+        if (mode == LN_F32) st = launch_ln_vec<LN_F32>(vpl, x, ld_x, rows, g, b, out, ld_o, row_scale, zero, zero_n, s);
+        else if (mode == LN_BF16) st = launch_ln_vec<LN_BF16>(vpl, x, ld_x, rows, g, b, out, ld_o, row_scale, zero, zero_n, s);
+        else if (mode == LN_BF16X2) st = launch_ln_vec<LN_BF16X2>(vpl, x, ld_x, rows, g, b, out, ld_o, row_scale, zero, zero_n, s);
+        else st = launch_ln_vec<LN_E4M3>(vpl, x, ld_x, rows, g, b, out, ld_o, row_scale, zero, zero_n, s);
+        if (st) return fail(st, "LayerNorm launch failed");
+        WB_CUDA(cudaGetLastError());
+        return WB_OK;
+    }
+    if (zero && zero_n > 0)
+        if (wb_status st = fill(zero, zero_n, 0.f, s)) return st;
     const unsigned grid = (unsigned)((rows + 7) / 8);
     if (mode == LN_F32) WB_CUDA(launch_k(layernorm_kernel<LN_F32>, dim3(grid), dim3(256), 0, s, x, ld_x, rows, d, g, b, out, ld_o, row_scale));
     else if (mode == LN_BF16) WB_CUDA(launch_k(layernorm_kernel<LN_BF16>, dim3(grid), dim3(256), 0, s, x, ld_x, rows, d, g, b, out, ld_o, row_scale));

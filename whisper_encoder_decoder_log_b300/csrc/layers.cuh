@@ -10,8 +10,11 @@ namespace wb {
 // LN_BF16X2 writes hi = bf16(y) at column c and lo = bf16(y - hi) at d + c.
 enum LnOut : int { LN_F32 = 0, LN_BF16 = 1, LN_E4M3 = 2, LN_BF16X2 = 3 };
 
+// With zero set, zero[0 .. zero_n) is cleared by the same launch (the next
+// GEMM's split-K output).
 wb_status layernorm(const float* x, int64_t ld_x, int64_t rows, int d, const float* g, const float* b, LnOut mode,
-                    void* out, int64_t ld_o, float* row_scale, cudaStream_t s);
+                    void* out, int64_t ld_o, float* row_scale, cudaStream_t s, float* zero = nullptr,
+                    int64_t zero_n = 0);
 // Positions come from *pos_dev when it is non-null (graph replay), else p0.
 wb_status embed(const int32_t* tokens, int64_t rows, int P, int p0, int d, const void* E, const void* Pos, bool bf16,
                 int vocab, float* x, unsigned* err, cudaStream_t s, const int* pos_dev = nullptr,

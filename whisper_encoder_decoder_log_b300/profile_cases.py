@@ -13,6 +13,10 @@ small batch, so a capture holds well under a few GB of device memory.
   decode  large-v3-turbo decoder over 32 chunks: prefix + 8 greedy steps
           (cross-attention over 1500 bf16 rows per chunk and head, causal
           self-attention over the E4M3 cache, few-row GEMMs)
+  decode8 large-v3 decoder layers in mixed_fp8 (4 of the 32) over --chunks
+          chunks (default 512): prefix + --steps greedy steps through the
+          captured step graphs, the launch pattern of the serving batch's
+          decode; the encoder states are random
   flash   encoder self-attention over 16 chunks x 20 heads
 """
 from __future__ import annotations
@@ -35,8 +39,10 @@ def main():
     import whisper_encoder_decoder_log_b300 as wb
 
     ap = argparse.ArgumentParser()
-    ap.add_argument("case", choices=["mel", "gemm", "gemm8", "decode", "flash"])
+    ap.add_argument("case", choices=["mel", "gemm", "gemm8", "decode", "decode8", "flash"])
     ap.add_argument("--iters", type=int, default=3)
+    ap.add_argument("--chunks", type=int, default=512)
+    ap.add_argument("--steps", type=int, default=8)
     a = ap.parse_args()
     dev = "cuda"
     if a.case == "mel":
@@ -64,6 +70,28 @@ def main():
             cs = sb.expand(N).contiguous()
             for _ in range(a.iters):
                 wb.wb_gemm(qa.view(M, K), qb.view(N, K), C, row_scale=rs, col_scale=cs)
+    elif a.case == "decode8":
+        dims = synth.ModelDims("large-v3-dec4", 128, 1280, 20, 5120, 1, 4, 51866)
+        desc = wb.make_desc(dims, wb.PREC_MIXED_FP8, True)
+        buf = wb.pack_weights(desc, synth.make_weights(dims, 0, bf16=True))
+        torch.cuda.synchronize()
+        model = wb.wb_model_create(desc, buf)
+        B = a.chunks
+        g = torch.Generator(device=dev)
+        g.manual_seed(0)
+        enc = torch.randn(B, 1500, 1280, device=dev, generator=g).to(torch.bfloat16)
+        lens = np.full(B, 4 + a.steps + 1, np.int32)
+        tok = torch.zeros(B, 448, dtype=torch.int32, device=dev)
+        tok[:, :4] = torch.from_numpy(synth.forced_prefix(0, dims.vocab)).to(dev)
+        dws = torch.empty(wb.wb_decoder_workspace_size(model, lens), dtype=torch.uint8, device=dev)
+        for _ in range(a.iters):
+            d = wb.wb_decoder_init(model, lens, enc, tok, dws)
+            wb.wb_decode_prefix(d, 4)
+            for _ in range(a.steps):
+                wb.wb_decode_step(d, B)
+            wb.wb_decoder_destroy(d)
+        wb.wb_sync_status(model)
+        wb.wb_model_destroy(model)
     else:
         layers = (1, 4) if a.case == "decode" else (1, 0)
         dims = synth.ModelDims("turbo", 128, 1280, 20, 5120, layers[0], layers[1], 51866)
