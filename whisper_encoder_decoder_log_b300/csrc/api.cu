@@ -232,7 +232,10 @@ wb_status make_fp8(wb_model* m, const std::vector<std::string>& names, int64_t r
 // ------------------------------------------------------------------ GEMM helper
 // y = x W^T (+ epilogue) with the model's arithmetic: SIMT fp32 for the fp32
 // model, tcgen05 otherwise (E4M3 when fp8 is given).
-constexpr int64_t kSwapRows = 256;   // GEMMs with at most this many rows use the swapped form
+#ifndef WB_SWAP_ROWS
+#define WB_SWAP_ROWS 1024
+#endif
+constexpr int64_t kSwapRows = WB_SWAP_ROWS;   // GEMMs with at most this many rows use the swapped form
 
 struct Lin {
     const void* a = nullptr;      // activations
@@ -244,6 +247,7 @@ struct Lin {
     const float* a_scale = nullptr;
     bool split = false;           // a holds [hi | lo] bf16 halves: 2K columns, lda >= 2K
     bool out_zeroed = false;      // the caller has zeroed a plain fp32 output already
+    bool w_const = false;         // w is model data, written by no kernel this GEMM can overlap
 };
 
 // How linear_impl runs a GEMM: SIMT, swapped (few rows) or plain tcgen05, the
@@ -334,10 +338,13 @@ wb_status linear_impl(const Lin& L, GemmEpi e, bool simt_fp32, unsigned* err, cu
     } else {
         if (wb_status st = gemm_plan(&p, A, B, L.N, L.split ? 2 * L.K : L.K, f8, c.bn, L.split ? L.K : 0)) return st;
     }
+    p.w_const = L.w_const;
     return gemm_run(p, e, err, s, 0, c.ksplit);
 }
 
-wb_status linear(const wb_model* m, const Lin& L, GemmEpi e, cudaStream_t s) {
+wb_status linear(const wb_model* m, const Lin& L0, GemmEpi e, cudaStream_t s) {
+    Lin L = L0;
+    L.w_const = true;   // every model GEMM multiplies by model weights
     return linear_impl(L, e, m->fp32(), m->err, s);
 }
 

@@ -3,16 +3,21 @@
 // / 8) V per 64-wide head over the 1500 positions of a chunk, bf16 in, fp32
 // accumulation).
 //
-// One CTA = 128 query rows of one (chunk, head); 192 threads:
-//   warp 0      TMA: Q once, then K and V tiles of 128 keys into a 3-deep ring
+// One CTA = 128 query rows of one (chunk, head); 192 threads, two CTAs per SM:
+//   warp 0      TMA: Q once, then K and V tiles of 128 keys into a 2-deep ring
 //   warp 1      TMEM owner and MMA issuer (one thread):
-//                 S_j  = Q . K_j^T   M 128, N 128, K 64   -> TMEM S[j % 2]
-//                 PV_j = P_j . V_j   M 128, N 64,  K 128  -> TMEM PV[j % 2]
+//                 S_j  = Q . K_j^T          M 128, N 128, K 64   -> TMEM S
+//                 O   += P_j . V_j          M 128, N 64,  K 128  -> TMEM O
 //               V is read MN-major straight from its [key][dim] tile.
-//   warps 2-5   softmax, one query row per thread (TMEM lane = row): read the
-//               S row twice (maximum, then exp2 and sum), write P as bf16 into
-//               a 128-byte-swizzled shared tile (double buffered), and keep the
-//               fp32 output row in registers: O = O * exp2(m_old - m_new) + PV.
+//   warps 2-5   softmax, one query row per thread (TMEM lane = row): load the
+//               S row into registers once (S is then free for S_{j+1}), take
+//               its maximum, write P = exp2(S c - m) as bf16 into a
+//               128-byte-swizzled shared tile.
+// The output accumulates in TMEM across all key tiles.  The running maximum m
+// is only raised when a tile's maximum exceeds it by more than 2^8 (the
+// published "conditional rescaling" of FlashAttention-4): P stays <= 256, and
+// the rare raise rescales the row of O in TMEM once the previous P V product
+// has landed.  The final O / l equals softmax(S) V for any such m.
 // Keys past 1500 (the last tile reads into the next chunk or past the tensor,
 // where TMA fills zeros) are masked to -inf; query rows past 1500 are not
 // stored.  Every mbarrier wait is bounded by wall time.
@@ -26,9 +31,9 @@ namespace {
 constexpr int kRows = 128;          // query rows per CTA
 constexpr int kKeys = 128;          // keys per tile
 constexpr int kStages = 2;
-constexpr int kSBuf = 1;            // S buffers in TMEM
-constexpr int kPBuf = 1;            // P buffers in shared memory
-constexpr int kTmemCols = 256;      // S 0-127, PV[0] 128-191, PV[1] 192-255
+constexpr int kTmemCols = 256;      // S 0-127, O 128-191
+constexpr int kOCol = 128;
+constexpr float kRaise = 8.0f;      // log2 growth of a row maximum absorbed without rescaling O
 constexpr int kTileBytes = 128 * 128;            // 128 rows x 64 bf16
 constexpr int kSmemSlack = 256;     // alignment slack requested above sizeof(FlashSmem)
 constexpr uint32_t kIdescS = UmmaIdesc<128, 128, 1>::value;
@@ -38,19 +43,17 @@ struct FlashSmem {
     unsigned char q[kTileBytes];
     unsigned char k[kStages][kTileBytes];
     unsigned char v[kStages][kTileBytes];
-    unsigned char p[kPBuf][2 * kTileBytes];       // [buffer][key half]
+    unsigned char p[2 * kTileBytes];              // [key half]
     uint64_t q_full;
     uint64_t kv_full[kStages], kv_empty[kStages];
-    uint64_t s_full[kSBuf], s_empty[kSBuf];
-    uint64_t p_full[kPBuf], p_empty[kPBuf];
-    uint64_t pv_full[2], pv_empty[2];
+    uint64_t s_full, s_empty;
+    uint64_t p_full, p_empty;                     // p_empty completes when P_j . V_j has landed in O
     uint64_t drain;
     uint32_t tmem;
     int abort_flag;
 };
 
-// Hardware base-2 exponential (MUFU, ~2^-22 relative error; arguments here
-// are <= 0 so the result never overflows).
+// Hardware base-2 exponential (MUFU, ~2^-22 relative error).
 WB_DEV float ex2_fast(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -91,9 +94,10 @@ flash_tc_kernel(const __grid_constant__ CUtensorMap tma_qkv, int d, __nv_bfloat1
     if (threadIdx.x == 0) {
         mbar_init(&S.q_full, 1);
         for (int i = 0; i < kStages; ++i) { mbar_init(&S.kv_full[i], 1); mbar_init(&S.kv_empty[i], 1); }
-        for (int i = 0; i < kSBuf; ++i) { mbar_init(&S.s_full[i], 1); mbar_init(&S.s_empty[i], 128); }
-        for (int i = 0; i < kPBuf; ++i) { mbar_init(&S.p_full[i], 128); mbar_init(&S.p_empty[i], 1); }
-        for (int i = 0; i < 2; ++i) { mbar_init(&S.pv_full[i], 1); mbar_init(&S.pv_empty[i], 128); }
+        mbar_init(&S.s_full, 1);
+        mbar_init(&S.s_empty, 128);
+        mbar_init(&S.p_full, 128);
+        mbar_init(&S.p_empty, 1);
         mbar_init(&S.drain, 1);
         S.abort_flag = 0;
         fence_barrier_init();
@@ -142,9 +146,9 @@ flash_tc_kernel(const __grid_constant__ CUtensorMap tma_qkv, int d, __nv_bfloat1
             bool any = false;
             for (int j = 0; j <= n_tiles && ok; ++j) {
                 if (j < n_tiles) {   // S_j = Q K_j^T
-                    const int st = j % kStages, b = j % kSBuf;
+                    const int st = j % kStages;
                     if (!wait_or_abort(&S.kv_full[st], (j / kStages) & 1, abort_flag, err, WB_DEVERR_TIMEOUT_MMA) ||
-                        !wait_or_abort(&S.s_empty[b], ((j / kSBuf) & 1) ^ 1, abort_flag, err, WB_DEVERR_TIMEOUT_MMA)) {
+                        !wait_or_abort(&S.s_empty, (j & 1) ^ 1, abort_flag, err, WB_DEVERR_TIMEOUT_MMA)) {
                         ok = false;
                         break;
                     }
@@ -152,30 +156,28 @@ flash_tc_kernel(const __grid_constant__ CUtensorMap tma_qkv, int d, __nv_bfloat1
                     const uint32_t k_addr = smem_u32(S.k[st]);
 #pragma unroll
                     for (int k = 0; k < 4; ++k)
-                        umma_bf16(tmem + b * 128, umma_desc_sw128(q_addr + 32 * k), umma_desc_sw128(k_addr + 32 * k),
-                                  kIdescS, k ? 1u : 0u);
+                        umma_bf16(tmem, umma_desc_sw128(q_addr + 32 * k), umma_desc_sw128(k_addr + 32 * k), kIdescS,
+                                  k ? 1u : 0u);
                     any = true;
-                    umma_commit(&S.s_full[b]);
+                    umma_commit(&S.s_full);
                 }
-                if (j >= 1) {        // PV_{j-1} = P_{j-1} V_{j-1}
-                    const int i = j - 1, st = i % kStages, b = i & 1, pbf = i % kPBuf;
-                    if (!wait_or_abort(&S.p_full[pbf], (i / kPBuf) & 1, abort_flag, err, WB_DEVERR_TIMEOUT_MMA) ||
-                        !wait_or_abort(&S.pv_empty[b], ((i >> 1) & 1) ^ 1, abort_flag, err, WB_DEVERR_TIMEOUT_MMA)) {
+                if (j >= 1) {        // O += P_{j-1} V_{j-1}
+                    const int i = j - 1, st = i % kStages;
+                    if (!wait_or_abort(&S.p_full, i & 1, abort_flag, err, WB_DEVERR_TIMEOUT_MMA)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t p_addr = smem_u32(S.p[pbf]);
+                    const uint32_t p_addr = smem_u32(S.p);
                     const uint32_t v_addr = smem_u32(S.v[st]);
 #pragma unroll
                     for (int k = 0; k < 8; ++k) {
                         // A: P, K-major, 64-key halves of 16 KB; B: V rows (keys) of 128 B, MN-major
                         const uint64_t ad = umma_desc_sw128(p_addr + (k >> 2) * kTileBytes + 32 * (k & 3));
                         const uint64_t bd = umma_desc_sw128(v_addr + 2048 * k);
-                        umma_bf16(tmem + 128 + b * 64, ad, bd, kIdescPV, k ? 1u : 0u);
+                        umma_bf16(tmem + kOCol, ad, bd, kIdescPV, (i | k) ? 1u : 0u);
                     }
-                    umma_commit(&S.pv_full[b]);
-                    umma_commit(&S.p_empty[pbf]);
+                    umma_commit(&S.p_empty);
                     umma_commit(&S.kv_empty[st]);
                 }
             }
@@ -190,131 +192,127 @@ flash_tc_kernel(const __grid_constant__ CUtensorMap tma_qkv, int d, __nv_bfloat1
         const int r = g * 32 + lane;
         const uint32_t lane_off = (uint32_t)(g * 32) << 16;
         const float c = 0.125f * 1.4426950408889634f;   // 1/sqrt(64) * log2(e)
-        float m = -INFINITY, l = 0.f, o[64];
-#pragma unroll
-        for (int i = 0; i < 64; ++i) o[i] = 0.f;
-        float alpha_prev = 0.f;   // rescale belonging to the PV in flight
+        const uint64_t c2 = f32x2(c, c);
+        float m = -INFINITY, l = 0.f;                    // running maximum (log2 units) and sum
         bool ok = true;
         // row swizzle inside a 128-byte atom row
         const uint32_t row_off = (uint32_t)(r >> 3) * 1024 + (uint32_t)(r & 7) * 128;
-        for (int j = 0; j <= n_tiles && ok; ++j) {
-            if (j < n_tiles) {
-                const int b = j % kSBuf, pbf = j % kPBuf;
-                if (!wait_or_abort(&S.s_full[b], (j / kSBuf) & 1, abort_flag, err, WB_DEVERR_TIMEOUT_EPI)) { ok = false; break; }
-                tc_fence_after();
-                const int valid = min(kKeys, kCtx - j * kKeys);
-                const bool full = valid == kKeys;          // only the last tile is ragged
-                const uint32_t sa = tmem + lane_off + b * 128;
-                float mx = -INFINITY;
-#pragma unroll 1
-                for (int cc = 0; cc < 4; ++cc) {
-                    uint32_t raw[32];
-                    tmem_ld32(sa + cc * 32, raw);
-                    tmem_wait_ld();
-                    if (full) {
+        const uint32_t sa = tmem + lane_off;
+        const uint32_t oa = tmem + lane_off + kOCol;
+        for (int j = 0; j < n_tiles && ok; ++j) {
+            if (!wait_or_abort(&S.s_full, j & 1, abort_flag, err, WB_DEVERR_TIMEOUT_EPI)) { ok = false; break; }
+            tc_fence_after();
+            uint32_t s0[32], s1[32], s2[32], s3[32];
+            tmem_ld32(sa, s0);
+            tmem_ld32(sa + 32, s1);
+            tmem_ld32(sa + 64, s2);
+            tmem_ld32(sa + 96, s3);
+            tmem_wait_ld();
+            // S is in registers: the tensor core may compute S_{j+1}
+            tc_fence_before();
+            mbar_arrive(&S.s_empty);
+            const int valid = min(kKeys, kCtx - j * kKeys);
+            if (valid < kKeys) {                       // only the last tile is ragged
+                constexpr uint32_t kNegInf = 0xff800000u;
 #pragma unroll
-                        for (int t = 0; t < 32; ++t) mx = fmaxf(mx, __uint_as_float(raw[t]));
-                    } else {
-#pragma unroll
-                        for (int t = 0; t < 32; ++t)
-                            if (cc * 32 + t < valid) mx = fmaxf(mx, __uint_as_float(raw[t]));
-                    }
+                for (int t = 0; t < 32; ++t) {
+                    if (t >= valid) s0[t] = kNegInf;
+                    if (32 + t >= valid) s1[t] = kNegInf;
+                    if (64 + t >= valid) s2[t] = kNegInf;
+                    if (96 + t >= valid) s3[t] = kNegInf;
                 }
-                const float mn = fmaxf(m, mx * c);
-                const float alpha = ex2_fast(m - mn);      // 0 on the first tile (m = -inf)
-                // P may be overwritten once the previous PV has consumed it
-                if (!wait_or_abort(&S.p_empty[pbf], ((j / kPBuf) & 1) ^ 1, abort_flag, err, WB_DEVERR_TIMEOUT_EPI)) { ok = false; break; }
-                float sum = 0.f;
-                unsigned char* pb = S.p[pbf];
-#pragma unroll 1
-                for (int cc = 0; cc < 4; ++cc) {
-                    uint32_t raw[32];
-                    tmem_ld32(sa + cc * 32, raw);
-                    tmem_wait_ld();
-                    uint32_t pk[16];
+            }
+            float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
-                    for (int t = 0; t < 32; t += 2) {
-                        float p0 = ex2_fast(fmaf(__uint_as_float(raw[t]), c, -mn));
-                        float p1 = ex2_fast(fmaf(__uint_as_float(raw[t + 1]), c, -mn));
-                        if (!full) {
-                            const int col = cc * 32 + t;
-                            if (col >= valid) p0 = 0.f;
-                            if (col + 1 >= valid) p1 = 0.f;
-                        }
-                        sum += p0 + p1;
-                        pk[t >> 1] = pack_bf16x2(p0, p1);
-                    }
-                    // keys cc*32 .. cc*32+31: half = cc / 2, 16-byte chunks (cc % 2) * 4 .. +3
+            for (int t = 0; t < 32; t += 2) {
+                mx0 = fmax3(mx0, __uint_as_float(s0[t]), __uint_as_float(s0[t + 1]));
+                mx1 = fmax3(mx1, __uint_as_float(s1[t]), __uint_as_float(s1[t + 1]));
+                mx0 = fmax3(mx0, __uint_as_float(s2[t]), __uint_as_float(s2[t + 1]));
+                mx1 = fmax3(mx1, __uint_as_float(s3[t]), __uint_as_float(s3[t + 1]));
+            }
+            const float mt = fmaxf(mx0, mx1) * c;
+            const bool raise = mt > m + kRaise;          // always on the first tile (m = -inf)
+            const float m_use = raise ? mt : m;
+            const float alpha = raise ? ex2_fast(m - m_use) : 1.f;   // 0 when m = -inf
+            const bool warp_raise = __any_sync(0xffffffffu, raise) && j > 0;
+            // P and O may be touched once P_{j-1} V_{j-1} has landed
+            if (!wait_or_abort(&S.p_empty, (j & 1) ^ 1, abort_flag, err, WB_DEVERR_TIMEOUT_EPI)) { ok = false; break; }
+            tc_fence_after();
+            const uint64_t nm2 = f32x2(-m_use, -m_use);
+            uint64_t sum2 = f32x2(0.f, 0.f);
+            unsigned char* pb = S.p;
+            auto emit = [&](const uint32_t (&sv)[32], int cc) {
+                uint32_t pk[16];
 #pragma unroll
-                    for (int q4 = 0; q4 < 4; ++q4) {
-                        const int chunk16 = (cc & 1) * 4 + q4;
-                        const uint32_t off = (uint32_t)(cc >> 1) * kTileBytes + row_off +
-                                             (uint32_t)((chunk16 ^ (r & 7)) * 16);
-                        *reinterpret_cast<uint4*>(pb + off) =
-                            make_uint4(pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2], pk[4 * q4 + 3]);
-                    }
+                for (int t = 0; t < 32; t += 2) {
+                    float a0, a1;
+                    f32x2_split(fma_f32x2(f32x2(__uint_as_float(sv[t]), __uint_as_float(sv[t + 1])), c2, nm2), a0, a1);
+                    const float p0 = ex2_fast(a0), p1 = ex2_fast(a1);
+                    sum2 = add_f32x2(sum2, f32x2(p0, p1));
+                    pk[t >> 1] = pack_bf16x2(p0, p1);
                 }
-                // S[b] has been read; P[b] is ready for the tensor core
-                tc_fence_before();
-                mbar_arrive(&S.s_empty[b]);
-                fence_proxy_async();
-                mbar_arrive(&S.p_full[pbf]);
-                l = l * alpha + sum;
-                m = mn;
-                // O holds sum_{i < j-1} at the maximum of tile j-1; add PV_{j-1}
-                // (also at that maximum), then bring O to this tile's maximum
-                const float a_here = alpha;
-                if (j >= 1) {
-                    const int i = j - 1, bi = i & 1;
-                    if (!wait_or_abort(&S.pv_full[bi], (i >> 1) & 1, abort_flag, err, WB_DEVERR_TIMEOUT_EPI)) { ok = false; break; }
-                    tc_fence_after();
-                    const uint32_t pa = tmem + lane_off + 128 + bi * 64;
+                // keys cc*32 .. cc*32+31: half = cc / 2, 16-byte chunks (cc % 2) * 4 .. +3
 #pragma unroll
-                    for (int cc = 0; cc < 2; ++cc) {
-                        uint32_t raw[32];
-                        tmem_ld32(pa + cc * 32, raw);
-                        tmem_wait_ld();
-#pragma unroll
-                        for (int t = 0; t < 32; ++t) o[cc * 32 + t] = o[cc * 32 + t] * alpha_prev + __uint_as_float(raw[t]);
-                    }
-                    tc_fence_before();
-                    mbar_arrive(&S.pv_empty[bi]);
-                    // bring O to this tile's maximum
-#pragma unroll
-                    for (int t = 0; t < 64; ++t) o[t] *= a_here;
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    const int chunk16 = (cc & 1) * 4 + q4;
+                    const uint32_t off = (uint32_t)(cc >> 1) * kTileBytes + row_off +
+                                         (uint32_t)((chunk16 ^ (r & 7)) * 16);
+                    *reinterpret_cast<uint4*>(pb + off) =
+                        make_uint4(pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2], pk[4 * q4 + 3]);
                 }
-                else {
-#pragma unroll
-                    for (int t = 0; t < 64; ++t) o[t] *= a_here;   // first tile: O is zero
-                }
-                alpha_prev = 1.f;
-            } else {
-                // last PV
-                const int i = n_tiles - 1, bi = i & 1;
-                if (!wait_or_abort(&S.pv_full[bi], (i >> 1) & 1, abort_flag, err, WB_DEVERR_TIMEOUT_EPI)) { ok = false; break; }
-                tc_fence_after();
-                const uint32_t pa = tmem + lane_off + 128 + bi * 64;
+            };
+            emit(s0, 0);
+            emit(s1, 1);
+            emit(s2, 2);
+            emit(s3, 3);
+            // rescale O after P is out (the S registers are dead by now)
+            if (warp_raise) {                          // warp-uniform: tcgen05.ld/st are collective
+                const uint64_t a2 = f32x2(alpha, alpha);
 #pragma unroll
                 for (int cc = 0; cc < 2; ++cc) {
-                    uint32_t raw[32];
-                    tmem_ld32(pa + cc * 32, raw);
+                    uint32_t o[32];
+                    tmem_ld32(oa + cc * 32, o);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int t = 0; t < 32; ++t) o[cc * 32 + t] += __uint_as_float(raw[t]);
+                    for (int t = 0; t < 32; t += 2) {
+                        float x0, x1;
+                        f32x2_split(mul_f32x2(f32x2(__uint_as_float(o[t]), __uint_as_float(o[t + 1])), a2), x0, x1);
+                        o[t] = __float_as_uint(x0);
+                        o[t + 1] = __float_as_uint(x1);
+                    }
+                    tmem_st32(oa + cc * 32, o);
                 }
-                tc_fence_before();
-                mbar_arrive(&S.pv_empty[bi]);
+                tmem_wait_st();
             }
+            float sl, sh;
+            f32x2_split(sum2, sl, sh);
+            l = l * alpha + (sl + sh);
+            m = m_use;
+            // P_j is ready for the tensor core (and O's rescale has landed)
+            tc_fence_before();
+            fence_proxy_async();
+            mbar_arrive(&S.p_full);
         }
-        if (ok && q0 + r < kCtx) {
-            const float inv = 1.f / l;
-            __nv_bfloat16* dst = out + ((int64_t)row_base + q0 + r) * d + h * 64;
+        // the last P V product
+        if (ok && !wait_or_abort(&S.p_empty, (n_tiles - 1) & 1, abort_flag, err, WB_DEVERR_TIMEOUT_EPI)) ok = false;
+        if (ok) {
+            tc_fence_after();
+            uint32_t o0[32], o1[32];
+            tmem_ld32(oa, o0);
+            tmem_ld32(oa + 32, o1);
+            tmem_wait_ld();
+            if (q0 + r < kCtx) {
+                const float inv = 1.f / l;
+                __nv_bfloat16* dst = out + ((int64_t)row_base + q0 + r) * d + h * 64;
 #pragma unroll
-            for (int q8 = 0; q8 < 8; ++q8) {
-                const float* v = o + q8 * 8;
-                *reinterpret_cast<uint4*>(dst + q8 * 8) =
-                    make_uint4(pack_bf16x2(v[0] * inv, v[1] * inv), pack_bf16x2(v[2] * inv, v[3] * inv),
-                               pack_bf16x2(v[4] * inv, v[5] * inv), pack_bf16x2(v[6] * inv, v[7] * inv));
+                for (int q8 = 0; q8 < 8; ++q8) {
+                    const uint32_t* v = q8 < 4 ? o0 + q8 * 8 : o1 + (q8 - 4) * 8;
+                    *reinterpret_cast<uint4*>(dst + q8 * 8) = make_uint4(
+                        pack_bf16x2(__uint_as_float(v[0]) * inv, __uint_as_float(v[1]) * inv),
+                        pack_bf16x2(__uint_as_float(v[2]) * inv, __uint_as_float(v[3]) * inv),
+                        pack_bf16x2(__uint_as_float(v[4]) * inv, __uint_as_float(v[5]) * inv),
+                        pack_bf16x2(__uint_as_float(v[6]) * inv, __uint_as_float(v[7]) * inv));
+                }
             }
         }
     }

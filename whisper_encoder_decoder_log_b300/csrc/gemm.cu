@@ -34,14 +34,18 @@ constexpr int kBM = 128;
 constexpr int kRowBytes = 128;       // one k-block row: 64 bf16 or 128 E4M3
 constexpr int kGroupM = 16;
 
+// fp32 epilogue staging: one 32 x 32 fp32 block per epilogue warp, so that
+// global stores and reductions go out one 128-byte row segment at a time.
+constexpr int kEpiStageBytes = 8 * 32 * 32 * 4;
+
 template <int BN>
 struct Cfg {
     static constexpr int A_BYTES = kBM * kRowBytes;
     static constexpr int B_BYTES = BN * kRowBytes;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-    static constexpr int STAGES = (196 * 1024) / STAGE_BYTES > 8 ? 8 : (196 * 1024) / STAGE_BYTES;
+    static constexpr int STAGES = (192 * 1024) / STAGE_BYTES > 8 ? 8 : (192 * 1024) / STAGE_BYTES;
     static constexpr int TMEM_COLS = 2 * BN;
-    static constexpr int SMEM = STAGES * STAGE_BYTES + 1024 + 256;
+    static constexpr int SMEM = STAGES * STAGE_BYTES + kEpiStageBytes + 1024 + 256;
 };
 
 struct GemmArgs {
@@ -53,6 +57,7 @@ struct GemmArgs {
     int kb_all;             // k-blocks of the whole K
     int ksplit;             // K partitions; > 1 adds partial tiles atomically
     int stages;             // smem ring depth (<= the compile-time maximum)
+    int w_const;            // the weight operand is constant: load it before the grid dependency wait
     int b_kwrap;
     GemmEpi epi;
 };
@@ -66,6 +71,36 @@ __device__ __forceinline__ void tile_coords(const GemmArgs& a, int64_t t, int64_
     const int64_t local = t % group;
     mt = first_m + local % gsz;
     nt = local / gsz;
+}
+
+// Per-row epilogue arithmetic of an fp32 output (row r of batch b, columns
+// n0..n0+31): scales, bias (first K partition only), GELU, added matrix.
+__device__ __forceinline__ void transform_f32(const GemmArgs& a, int64_t b, int64_t r, int64_t n0, float (&v)[32],
+                                              int ks) {
+    const GemmEpi& e = a.epi;
+    const int64_t N = a.N;
+    const bool full = n0 + 32 <= N;
+    if (e.row_scale || e.col_scale) {
+        const float rs = e.row_scale ? e.row_scale[b * a.rows + r] : 1.f;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            const float cs = (e.col_scale && (full || n0 + j < N)) ? e.col_scale[n0 + j] : 1.f;
+            v[j] *= rs * cs;
+        }
+    }
+    if (e.bias && ks == 0) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] += (full || n0 + j < N) ? e.bias[n0 + j] : 0.f;
+    }
+    if (e.gelu) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = gelu_f(v[j]);
+    }
+    if (e.add) {
+        const float* ap = e.add + r * e.ld_add + n0;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] += (full || n0 + j < N) ? ap[j] : 0.f;
+    }
 }
 
 __device__ __forceinline__ void store_chunk(const GemmArgs& a, int64_t b, int64_t r, int64_t n0,
@@ -93,7 +128,9 @@ __device__ __forceinline__ void store_chunk(const GemmArgs& a, int64_t b, int64_
 #pragma unroll
             for (int q = 0; q < 8; ++q) atomicAdd(d4 + q, make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]));
         } else {
-            for (int j = 0; j < 32 && n0 + j < N; ++j) atomicAdd(dst + j, v[j]);
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+                if (n0 + j < N) atomicAdd(dst + j, v[j]);
         }
         return;
     }
@@ -155,7 +192,9 @@ __device__ __forceinline__ void store_chunk(const GemmArgs& a, int64_t b, int64_
                                    pack_bf16x2(lo[8 * q + 4], lo[8 * q + 5]), pack_bf16x2(lo[8 * q + 6], lo[8 * q + 7]));
             }
         } else {
-            for (int j = 0; j < 32 && n0 + j < N; ++j) { dst[j] = f2bf(v[j]); dst[N + j] = f2bf(lo[j]); }
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+                if (n0 + j < N) { dst[j] = f2bf(v[j]); dst[N + j] = f2bf(lo[j]); }
         }
     } else if (e.out_type == OUT_BF16) {
         __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(base) + orow * e.ldo + n0;
@@ -168,7 +207,9 @@ __device__ __forceinline__ void store_chunk(const GemmArgs& a, int64_t b, int64_
                                    pack_bf16x2(v[8 * q + 4], v[8 * q + 5]),
                                    pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
         } else {
-            for (int j = 0; j < 32 && n0 + j < N; ++j) dst[j] = f2bf(v[j]);
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+                if (n0 + j < N) dst[j] = f2bf(v[j]);
         }
     } else {
         float* dst = reinterpret_cast<float*>(base) + orow * e.ldo + n0;
@@ -185,7 +226,9 @@ __device__ __forceinline__ void store_chunk(const GemmArgs& a, int64_t b, int64_
                 d4[q] = w;
             }
         } else {
-            for (int j = 0; j < 32 && n0 + j < N; ++j) dst[j] = acc ? dst[j] + v[j] : v[j];
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+                if (n0 + j < N) dst[j] = acc ? dst[j] + v[j] : v[j];
         }
     }
 }
@@ -224,7 +267,7 @@ constexpr int kEpiWarps = 8;                       // two per TMEM lane quarter
 constexpr int kGemmThreads = 64 + 32 * kEpiWarps;  // producer + MMA + epilogue
 
 template <int BN, bool FP8, bool SWAP>
-__global__ void __launch_bounds__(kGemmThreads)
+__global__ void __launch_bounds__(kGemmThreads, SWAP ? 2 : 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUtensorMap tma_b,
                const GemmArgs args, unsigned* err) {
     using C = Cfg<BN>;
@@ -233,7 +276,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant_
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + STAGES * C::STAGE_BYTES);
+    float* epi_stage = reinterpret_cast<float*>(smem + STAGES * C::STAGE_BYTES);
+    uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + STAGES * C::STAGE_BYTES + kEpiStageBytes);
     uint64_t* empty_bar = full_bar + STAGES;
     uint64_t* tfull_bar = empty_bar + STAGES;     // [2]
     uint64_t* tempty_bar = tfull_bar + 2;         // [2]
@@ -267,17 +311,43 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant_
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
-    griddep_wait();
-    griddep_launch();   // barriers and TMEM are set up; now wait for the producer kernels
+    const bool producer = warp == 0 && lane == 0;
+    if (!producer) {
+        griddep_wait();
+        griddep_launch();   // barriers and TMEM are set up; now wait for the producer kernels
+    }
 
     if (warp == 0) {
         if (lane == 0) {
+            // Weight half of one stage (swapped: A holds the weights, else B).
+            auto load_w = [&](int stage, int64_t mt, int n0, int kx) {
+                unsigned char* sa = smem + stage * C::STAGE_BYTES;
+                if (SWAP) tma_load_3d(sa, &tma_a, &full_bar[stage], args.b_kwrap ? kx % args.b_kwrap : kx, (int)(mt * kBM), 0);
+                else tma_load_2d(sa + C::A_BYTES, &tma_b, &full_bar[stage], args.b_kwrap ? kx % args.b_kwrap : kx, n0);
+            };
+            // Constant weights do not depend on the kernels this one waits
+            // for: the first ring stages fetch them before the wait, which
+            // overlaps the previous kernel's tail (programmatic launch).
+            int pre = 0;
+            if (args.w_const) {
+                for (int64_t t = blockIdx.x; t < args.tiles && pre < STAGES; t += gridDim.x) {
+                    int64_t mt, nt;
+                    tile_coords(args, t, mt, nt);
+                    int kb0, kb1;
+                    split_range(args, t, kb0, kb1);
+                    for (int kb = kb0; kb < kb1 && pre < STAGES; ++kb, ++pre) {
+                        mbar_arrive_expect_tx(&full_bar[pre], C::STAGE_BYTES);
+                        load_w(pre, mt, (int)(nt * BN), kb * (FP8 ? 128 : 64));
+                    }
+                }
+            }
+            griddep_wait();
+            griddep_launch();
             int stage = 0;
             uint32_t phase = 0;
-            uint32_t last_parity[8];
-            bool issued[8];
-            for (int s = 0; s < 8; ++s) { issued[s] = false; last_parity[s] = 0; }
+            uint32_t issued = 0, last_parity = 0;      // bit s: stage s was loaded / its last phase
             bool ok = true;
+            int it = 0;
             for (int64_t t = blockIdx.x; t < args.tiles && ok; t += gridDim.x) {
                 int64_t mt, nt;
                 tile_coords(args, t, mt, nt);
@@ -286,40 +356,36 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant_
                 const int n0 = (int)(nt * BN);
                 int kb0, kb1;
                 split_range(args, t, kb0, kb1);
-                for (int kb = kb0; kb < kb1; ++kb) {
-                    bool got = false;
-                    for (WaitClock clk; !clk.expired();) {
-                        if (mbar_try_wait(&empty_bar[stage], phase ^ 1)) { got = true; break; }
-                        if (*abort_flag) break;
-                    }
-                    if (!got) {
-                        wb_set_error(err, WB_DEVERR_TIMEOUT_TMA);
-                        *abort_flag = 1;
-                        ok = false;
-                        break;
-                    }
-                    unsigned char* sa = smem + stage * C::STAGE_BYTES;
-                    unsigned char* sb = sa + C::A_BYTES;
-                    mbar_arrive_expect_tx(&full_bar[stage], C::STAGE_BYTES);
+                for (int kb = kb0; kb < kb1; ++kb, ++it) {
                     const int kx = kb * (FP8 ? 128 : 64);
-                    if (SWAP) {
-                        // A: 128 weight rows (k wraps onto the weights), B: BN activation rows
-                        const int kxa = args.b_kwrap ? kx % args.b_kwrap : kx;
-                        tma_load_3d(sa, &tma_a, &full_bar[stage], kxa, (int)(mt * kBM), 0);
-                        tma_load_2d(sb, &tma_b, &full_bar[stage], kx, n0);
-                    } else {
-                        const int kxb = args.b_kwrap ? kx % args.b_kwrap : kx;
-                        tma_load_3d(sa, &tma_a, &full_bar[stage], kx, r0, b);
-                        tma_load_2d(sb, &tma_b, &full_bar[stage], kxb, n0);
+                    if (it >= pre) {
+                        bool got = false;
+                        for (WaitClock clk; !clk.expired();) {
+                            if (mbar_try_wait(&empty_bar[stage], phase ^ 1)) { got = true; break; }
+                            if (*abort_flag) break;
+                        }
+                        if (!got) {
+                            wb_set_error(err, WB_DEVERR_TIMEOUT_TMA);
+                            *abort_flag = 1;
+                            ok = false;
+                            break;
+                        }
+                        mbar_arrive_expect_tx(&full_bar[stage], C::STAGE_BYTES);
+                        load_w(stage, mt, n0, kx);
                     }
-                    issued[stage] = true;
-                    last_parity[stage] = phase;
+                    // activation half: swapped -> B (BN activation rows), else A
+                    unsigned char* sa = smem + stage * C::STAGE_BYTES;
+                    if (SWAP) tma_load_2d(sa + C::A_BYTES, &tma_b, &full_bar[stage], kx, n0);
+                    else tma_load_3d(sa, &tma_a, &full_bar[stage], kx, r0, b);
+                    issued |= 1u << stage;
+                    last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
                     if (++stage == STAGES) { stage = 0; phase ^= 1; }
                 }
             }
+
             // never leave TMA writes in flight into this CTA's shared memory
             for (int s = 0; s < STAGES; ++s)
-                if (issued[s]) mbar_wait(&full_bar[s], last_parity[s], err, WB_DEVERR_TIMEOUT_TMA);
+                if ((issued >> s) & 1u) mbar_wait(&full_bar[s], (last_parity >> s) & 1u, err, WB_DEVERR_TIMEOUT_TMA);
         }
     } else if (warp == 1) {
         if (lane == 0) {
@@ -407,18 +473,50 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant_
                 mbar_arrive(&tempty_bar[acc]);
                 continue;
             }
+            const GemmEpi& e = args.epi;
+            // stores and reductions are staged; a residual update without
+            // split-K reads its destination and stays in the thread's row
+            const bool staged = e.mode == MODE_PLAIN &&
+                                (e.out_type == OUT_F32 || (e.out_type == OUT_F32_ACC && args.ksplit > 1));
+            float* stg = epi_stage + (warp - 2) * 32 * 32;
 #pragma unroll 1
             for (int c = half; c < BN / 32; c += 2) {
                 uint32_t raw[32];
                 tmem_ld32(taddr + c * 32, raw);
                 tmem_wait_ld();
                 const int64_t n0 = nt * BN + c * 32;
-                if (row_ok && n0 < args.N) {
-                    float v[32];
+                float v[32];
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(raw[j]);
-                    store_chunk(args, b, r, n0, v, (int)(t % args.ksplit));
+                for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(raw[j]);
+                if (!staged) {
+                    if (row_ok && n0 < args.N) store_chunk(args, b, r, n0, v, (int)(t % args.ksplit));
+                    continue;
                 }
+                // fp32 output: transform in the thread's row, then transpose the
+                // 32 x 32 block through shared memory (16-byte chunks XOR-swizzled
+                // by row) and write one 128-byte row segment per instruction
+                if (row_ok && n0 < args.N) transform_f32(args, b, r, n0, v, (int)(t % args.ksplit));
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    *reinterpret_cast<float4*>(stg + lane * 32 + ((q ^ (lane & 7)) << 2)) =
+                        make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+                __syncwarp();
+                const int64_t col = n0 + lane;
+                const int64_t rq = (mt % args.mt_per_batch) * kBM + g * 32;   // first row of the quarter
+                const int64_t obr = e.out_batch_rows ? e.out_batch_rows : args.rows;
+                const bool reduce = args.ksplit > 1;             // partial tiles of one output
+                float* ob = reinterpret_cast<float*>(e.out) + (b * obr + e.out_row_offset) * e.ldo + col;
+                if (col < args.N) {
+#pragma unroll 4
+                    for (int rr = 0; rr < 32; ++rr) {
+                        if (rq + rr >= args.rows) break;
+                        const float x = stg[rr * 32 + ((((lane >> 2) ^ (rr & 7))) << 2) + (lane & 3)];
+                        float* dst = ob + (rq + rr) * e.ldo;
+                        if (reduce) atomicAdd(dst, x);   // result unused: a reduction
+                        else *dst = x;
+                    }
+                }
+                __syncwarp();
             }
             tc_fence_before();
             mbar_arrive(&tempty_bar[acc]);
@@ -489,7 +587,7 @@ wb_status launch_tc(const GemmPlan& p, GemmArgs a, unsigned* err, cudaStream_t s
     // lets several CTAs share an SM (bounded by shared memory and TMEM).
     const int64_t kb_per_cta = (int64_t)a.kblocks * ((a.tiles + num_sms() - 1) / num_sms());
     a.stages = (int)std::max<int64_t>(2, std::min<int64_t>(C::STAGES, kb_per_cta));
-    const int smem = a.stages * C::STAGE_BYTES + 1024 + 256;
+    const int smem = a.stages * C::STAGE_BYTES + kEpiStageBytes + 1024 + 256;
     int occ = 1;
     WB_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, gemm_tc_kernel<BN, FP8, SWAP>, kGemmThreads, smem));
     const int per_sm = std::max(1, std::min({occ, 512 / C::TMEM_COLS, 4}));
@@ -616,6 +714,7 @@ wb_status gemm_run(const GemmPlan& p, const GemmEpi& epi, unsigned* err, cudaStr
     a.kb_all = kb_all;
     a.kblocks = (kb_all + ksplit - 1) / ksplit;
     a.b_kwrap = (int)p.b_kwrap;
+    a.w_const = p.w_const ? 1 : 0;
     a.epi = epi;
     const bool half = epi.out_type == OUT_BF16 || epi.out_type == OUT_BF16X2;
     a.epi.vec = aligned16(epi.out) && (epi.mode == MODE_CROSS_KV || (epi.ldo * (half ? 2 : 4)) % 16 == 0) &&

@@ -58,6 +58,7 @@ struct GemmPlan {
     int bn = 256;
     bool fp8 = false;
     bool swap = false;     // small-M form: weights are the 128-row MMA operand
+    bool w_const = false;  // the weight operand is not written by kernels this GEMM may overlap
     bool ok = false;
 };
 
