@@ -352,21 +352,46 @@ self_attn_e4m3_kernel(const float* __restrict__ q, int64_t q_ld, int heads, KVVi
 // Decode step, causal self-attention over the E4M3 cache, with the cache
 // append of the current token fused in.  One warp per (chunk, head), kStepHeads
 // heads per CTA.  Lane = (row r of 8, sub s of 4): a pass covers 8 cache rows
-// and each lane reads 16 bytes of K and of V; loads run kStepDepth passes
-// ahead of the arithmetic.  The current token's K and V rows (fp32 in the QKV
-// output) are quantised here with the chunk's scales, exactly as the append
-// kernel does, written to cache row pos, and used from registers at j = pos.
+// and each lane owns 16 bytes of the K row and of the V row.  Every lane
+// streams its own pieces into a kStepDepth-deep shared-memory ring with
+// cp.async (16 bytes, L2 only), so the data in flight costs no registers and
+// a lane only ever reads back what it copied itself.  The current token's K
+// and V rows (fp32 in the QKV output) are quantised here with the chunk's
+// scales, exactly as the append kernel does, written to cache row pos, and
+// used from registers at j = pos.
 constexpr int kStepHeads = 4;
-constexpr int kStepDepth = 4;
+constexpr int kStepDepth = 8;
 
-WB_DEV void e4m3x16_to_f32(const uint4& w, float (&f)[16]) {
+WB_DEV void cp_async16(void* smem, const void* gmem) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem)), "l"(gmem) : "memory");
+}
+WB_DEV void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+WB_DEV void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+// dot(q[0..15], E4M3 codes w) and o = o * alpha + p * E4M3 codes v
+WB_DEV float dot16_e4m3(const float (&q)[16], const uint4& w) {
+    const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+    float s = 0.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        __nv_fp8x4_e4m3 a;
+        a.__x = u[i];
+        const float4 f = static_cast<float4>(a);
+        s = fmaf(q[4 * i], f.x, s); s = fmaf(q[4 * i + 1], f.y, s);
+        s = fmaf(q[4 * i + 2], f.z, s); s = fmaf(q[4 * i + 3], f.w, s);
+    }
+    return s;
+}
+WB_DEV void axpy16_e4m3(float (&o)[16], float alpha, float p, const uint4& w) {
     const uint32_t u[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         __nv_fp8x4_e4m3 a;
         a.__x = u[i];
-        const float4 fa = static_cast<float4>(a);
-        f[4 * i] = fa.x; f[4 * i + 1] = fa.y; f[4 * i + 2] = fa.z; f[4 * i + 3] = fa.w;
+        const float4 f = static_cast<float4>(a);
+        o[4 * i] = fmaf(p, f.x, o[4 * i] * alpha); o[4 * i + 1] = fmaf(p, f.y, o[4 * i + 1] * alpha);
+        o[4 * i + 2] = fmaf(p, f.z, o[4 * i + 2] * alpha); o[4 * i + 3] = fmaf(p, f.w, o[4 * i + 3] * alpha);
     }
 }
 
@@ -382,9 +407,10 @@ WB_DEV uint4 quant16(const float* x, float inv) {
 }
 
 template <typename TO>
-__global__ void __launch_bounds__(32 * kStepHeads)
+__global__ void __launch_bounds__(32 * kStepHeads, 6)
 self_attn_step_kernel(const float* __restrict__ qkv, int64_t q_ld, int heads, KVView kv, int q_pos_host,
                       TO* __restrict__ out, int64_t o_ld, int64_t o_split) {
+    __shared__ uint4 ring[kStepHeads][kStepDepth][2][32];   // [warp][stage][K|V][lane]
     griddep_wait();
     griddep_launch();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -401,6 +427,20 @@ self_attn_step_kernel(const float* __restrict__ qkv, int64_t q_ld, int heads, KV
     uint8_t* base = const_cast<uint8_t*>(reinterpret_cast<const uint8_t*>(kv.ptr)) + kv.chunk_off[chunk];
     uint8_t* Kp = base + ((int64_t)kv.k_blk * kv.heads + h) * hs;
     uint8_t* Vp = base + ((int64_t)kv.v_blk * kv.heads + h) * hs;
+    const int npass = (pos + 8) >> 3;                              // passes over rows 0..pos
+    uint4 (*rg)[2][32] = ring[warp];
+    // rows below pos stream in while the current row is quantised
+    auto issue = [&](int pass) {
+        const int j = pass * 8 + r;
+        if (pass < npass && j < pos) {
+            const int st = pass % kStepDepth;
+            cp_async16(&rg[st][0][lane], Kp + (int64_t)j * 64 + sub * 16);
+            cp_async16(&rg[st][1][lane], Vp + (int64_t)j * 64 + sub * 16);
+        }
+        cp_async_commit();      // one group per pass, empty or not
+    };
+#pragma unroll
+    for (int u = 0; u < kStepDepth; ++u) issue(u);
     const float ks = kv.k_scale[chunk], vs = kv.v_scale[chunk];
     const float* qr = qkv + chunk * q_ld + h * 64 + sub * 16;
     // the current token's cache rows, quantised as the append kernel does
@@ -417,60 +457,38 @@ self_attn_step_kernel(const float* __restrict__ qkv, int64_t q_ld, int heads, KV
         // fold the 1/sqrt(64) and the K scale into q
         qv[i] = t.x * 0.125f * ks; qv[i + 1] = t.y * 0.125f * ks; qv[i + 2] = t.z * 0.125f * ks; qv[i + 3] = t.w * 0.125f * ks;
     }
-    const int nk = pos + 1;
-    const int npass = (nk + 7) >> 3;
-    auto load = [&](int pass, uint4& kr, uint4& vr) {
-        const int j = pass * 8 + r;
-        kr = make_uint4(0, 0, 0, 0);
-        vr = kr;
-        if (j < pos) {
-            kr = ld_stream(Kp + (int64_t)j * 64 + sub * 16);
-            vr = ld_stream(Vp + (int64_t)j * 64 + sub * 16);
-        } else if (j == pos) {
-            kr = kcur;
-            vr = vcur;
-        }
-    };
-    uint4 kb[kStepDepth], vb[kStepDepth];
-#pragma unroll
-    for (int u = 0; u < kStepDepth; ++u) load(u, kb[u], vb[u]);
     float m = -INFINITY, l = 0.f, o[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) o[i] = 0.f;
-    for (int p0 = 0; p0 < npass; p0 += kStepDepth) {
-#pragma unroll
-        for (int u = 0; u < kStepDepth; ++u) {
-            const int pass = p0 + u;
-            if (pass < npass) {     // uniform across the warp
-                const bool valid = pass * 8 + r < nk;
-                float kf[16], vf[16];
-                e4m3x16_to_f32(kb[u], kf);
-                e4m3x16_to_f32(vb[u], vf);
-                load(pass + kStepDepth, kb[u], vb[u]);
-                float sc = 0.f;
-#pragma unroll
-                for (int i = 0; i < 16; ++i) sc = fmaf(qv[i], kf[i], sc);
-                sc += __shfl_xor_sync(0xffffffffu, sc, 1);
-                sc += __shfl_xor_sync(0xffffffffu, sc, 2);
-                if (!valid) sc = -INFINITY;
-                float pm = sc;     // max over the 8 rows of the pass
-                pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 4));
-                pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 8));
-                pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 16));
-                const float mn = fmaxf(m, pm);
-                const float alpha = __expf(m - mn);     // 0 on the first pass (m = -inf)
-                const float pr = valid ? __expf(sc - mn) : 0.f;
-                float ps = pr;
-                ps += __shfl_xor_sync(0xffffffffu, ps, 4);
-                ps += __shfl_xor_sync(0xffffffffu, ps, 8);
-                ps += __shfl_xor_sync(0xffffffffu, ps, 16);
-                l = l * alpha + ps;
-                m = mn;
-#pragma unroll
-                for (int i = 0; i < 16; ++i) o[i] = fmaf(pr, vf[i], o[i] * alpha);
-            }
-        }
+    for (int pass = 0; pass < npass; ++pass) {
+        cp_async_wait<kStepDepth - 1>();                           // this pass's group has landed
+        const int j = pass * 8 + r;
+        const int st = pass % kStepDepth;
+        uint4 kr = make_uint4(0, 0, 0, 0), vr = kr;
+        if (j < pos) { kr = rg[st][0][lane]; vr = rg[st][1][lane]; }
+        else if (j == pos) { kr = kcur; vr = vcur; }
+        const bool valid = j <= pos;
+        float sc = dot16_e4m3(qv, kr);
+        sc += __shfl_xor_sync(0xffffffffu, sc, 1);
+        sc += __shfl_xor_sync(0xffffffffu, sc, 2);
+        if (!valid) sc = -INFINITY;
+        float pm = sc;     // max over the 8 rows of the pass
+        pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 4));
+        pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 8));
+        pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 16));
+        const float mn = fmaxf(m, pm);
+        const float alpha = __expf(m - mn);     // 0 on the first pass (m = -inf)
+        const float pr = valid ? __expf(sc - mn) : 0.f;
+        float ps = pr;
+        ps += __shfl_xor_sync(0xffffffffu, ps, 4);
+        ps += __shfl_xor_sync(0xffffffffu, ps, 8);
+        ps += __shfl_xor_sync(0xffffffffu, ps, 16);
+        l = l * alpha + ps;
+        m = mn;
+        axpy16_e4m3(o, alpha, pr, vr);
+        issue(pass + kStepDepth);                                  // refill the stage just consumed
     }
+    cp_async_wait<0>();
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
         o[i] += __shfl_xor_sync(0xffffffffu, o[i], 4);
