@@ -112,6 +112,66 @@ def test_gemm_e4m3_matches_oracle(M, N, K):
     assert np.abs(got - ref).max() <= 1e-5 * np.abs(ref).max() * np.sqrt(K / 64) + 1e-7
 
 
+def _sample_rows(M, seed):
+    rng = np.random.default_rng(seed)
+    # both ends of every 256-row pair, the ragged last tile, and random rows
+    rows = {0, 127, 128, 255, M - 1, M - 2, (M // 128) * 128, max(0, (M // 128) * 128 - 1)}
+    rows.update(rng.integers(0, M, 40).tolist())
+    return np.array(sorted(r for r in rows if 0 <= r < M))
+
+
+@pytest.mark.parametrize("M,N,K", [(9000, 5120, 1280), (4100, 3840, 640)])
+def test_gemm_pair_bf16_matches_oracle(M, N, K):
+    """Large plain GEMMs run on CTA pairs sharing each B tile (odd M-tile count: the last pair has an empty half)."""
+    rng = np.random.default_rng(M + N)
+    a = _bf16(rng.normal(size=(M, K)))
+    b = _bf16(rng.normal(size=(N, K)) * 0.05)
+    bias = rng.normal(size=N).astype(np.float32)
+    C = torch.empty(M, N, device="cuda")
+    wb.wb_gemm(torch.from_numpy(a).to(torch.bfloat16).cuda(), torch.from_numpy(b).to(torch.bfloat16).cuda(), C,
+               bias=torch.from_numpy(bias).cuda())
+    wb.wb_sync_status()
+    rows = _sample_rows(M, 1)
+    ref = omodel.Linear(b, bias)(a[rows])
+    got = C.cpu().numpy()[rows]
+    scale = np.abs(a).max() * np.abs(b).max() * np.sqrt(K)
+    assert np.abs(got - ref).max() <= 1e-5 * scale + 1e-6
+
+
+def test_gemm_pair_e4m3_matches_oracle():
+    M, N, K = 9000, 3840, 1280
+    rng = np.random.default_rng(11)
+    x = rng.normal(size=(M, K)).astype(np.float32)
+    w = (rng.normal(size=(N, K)) * 0.02).astype(np.float32)
+    lin = omodel.Linear(w, np.zeros(N), fp8=True)
+    rows = _sample_rows(M, 2)
+    ref = lin(x[rows])
+    amax = np.abs(x).max(axis=1)
+    sx = np.array([oe4m3.scale_of(v) for v in amax], np.float32)
+    qx = oe4m3.encode((x * (np.float32(1.0) / sx)[:, None]).astype(np.float32))
+    C = torch.empty(M, N, device="cuda")
+    wb.wb_gemm(torch.from_numpy(qx).cuda(), torch.from_numpy(lin.w_codes).cuda(), C,
+               row_scale=torch.from_numpy(sx).cuda(), col_scale=torch.full((N,), float(lin.w_scale), device="cuda"))
+    wb.wb_sync_status()
+    got = C.cpu().numpy()[rows]
+    assert np.abs(got - ref).max() <= 1e-5 * np.abs(ref).max() * np.sqrt(K / 64) + 1e-7
+
+
+def test_gemm_pair_gelu_bf16_out_ragged_n():
+    M, N, K = 12000, 1000, 256
+    rng = np.random.default_rng(5)
+    a, b = _bf16(rng.normal(size=(M, K))), _bf16(rng.normal(size=(N, K)) * 0.05)
+    bias = rng.normal(size=N).astype(np.float32)
+    C = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+    wb.wb_gemm(torch.from_numpy(a).to(torch.bfloat16).cuda(), torch.from_numpy(b).to(torch.bfloat16).cuda(), C,
+               bias=torch.from_numpy(bias).cuda(), gelu=True)
+    wb.wb_sync_status()
+    rows = _sample_rows(M, 3)
+    ref = omodel.gelu(omodel.Linear(b, bias)(a[rows]))
+    got = C.float().cpu().numpy()[rows]
+    assert np.abs(got - ref).max() <= 2 ** -8 * np.abs(ref).max() + 1e-3
+
+
 @pytest.mark.parametrize("bf16", [False, True])
 @pytest.mark.parametrize("n", [1, 1000, 1 << 20])
 def test_quantiser_codes_bit_exact(bf16, n):

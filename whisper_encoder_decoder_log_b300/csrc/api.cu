@@ -256,6 +256,7 @@ struct Lin {
 struct LinChoice {
     bool simt = false, swap = false;
     int bn = 0, ksplit = 1;
+    bool pair = false;            // CTA pairs share B tiles (large plain GEMMs)
     bool needs_zero = false;
 };
 
@@ -294,6 +295,10 @@ LinChoice linear_choose(const Lin& L, const GemmEpi& e, bool simt_fp32) {
             }
         }
     }
+    // enough M-tile pairs x N tiles for every SM pair: share B across a CTA pair
+    if (!c.swap && c.ksplit == 1 && c.bn == 256 && L.batches == 1 &&
+        ((L.rows + 255) / 256) * ((L.N + 255) / 256) >= sms)
+        c.pair = true;
     c.needs_zero = c.ksplit > 1 && e.out_type == OUT_F32;
     return c;
 }
@@ -336,7 +341,8 @@ wb_status linear_impl(const Lin& L, GemmEpi e, bool simt_fp32, unsigned* err, cu
         if (wb_status st = gemm_plan_swap(&p, A, B, L.N, L.split ? 2 * L.K : L.K, f8, c.bn, L.split ? L.K : 0))
             return st;
     } else {
-        if (wb_status st = gemm_plan(&p, A, B, L.N, L.split ? 2 * L.K : L.K, f8, c.bn, L.split ? L.K : 0)) return st;
+        if (wb_status st = gemm_plan(&p, A, B, L.N, L.split ? 2 * L.K : L.K, f8, c.bn, L.split ? L.K : 0, c.pair))
+            return st;
     }
     p.w_const = L.w_const;
     return gemm_run(p, e, err, s, 0, c.ksplit);

@@ -153,6 +153,27 @@ WB_DEV void tma_load_2d(void* dst, const CUtensorMap* m, uint64_t* bar, int x, i
           "r"(x), "r"(y) : "memory");
 }
 
+// Same box into this CTA and every CTA of the cluster in cta_mask (same
+// shared-memory offsets); each destination's mbarrier at `bar`'s offset
+// receives the byte count.
+WB_DEV void tma_load_2d_mc(void* dst, const CUtensorMap* m, uint64_t* bar, int x, int y, uint16_t cta_mask) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
+        " [%0], [%1, {%3, %4}], [%2], %5;"
+        ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(m)), "r"(smem_u32(bar)),
+          "r"(x), "r"(y), "h"(cta_mask) : "memory");
+}
+
+WB_DEV uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+// All threads of every CTA of the cluster (release / acquire).
+WB_DEV void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 WB_DEV void tma_load_3d(void* dst, const CUtensorMap* m, uint64_t* bar, int x, int y, int z) {
     asm volatile(
         "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
@@ -222,6 +243,14 @@ WB_DEV void umma_commit(uint64_t* bar) {
     asm volatile(
         "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
         ::"r"(smem_u32(bar)) : "memory");
+}
+
+// Arrive on the mbarrier at `bar`'s offset in every CTA of cta_mask once all
+// earlier tcgen05 operations of this thread have completed.
+WB_DEV void umma_commit_mc(uint64_t* bar, uint16_t cta_mask) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;"
+        ::"r"(smem_u32(bar)), "h"(cta_mask) : "memory");
 }
 
 WB_DEV void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }

@@ -266,7 +266,11 @@ __device__ __forceinline__ void split_range(const GemmArgs& a, int64_t t, int& k
 constexpr int kEpiWarps = 8;                       // two per TMEM lane quarter
 constexpr int kGemmThreads = 64 + 32 * kEpiWarps;  // producer + MMA + epilogue
 
-template <int BN, bool FP8, bool SWAP>
+// PAIR: a cluster of two CTAs computes M tiles 2p and 2p+1 of the same N
+// tile in lockstep; each CTA loads half of the B tile and multicasts it to
+// both, so a k-block costs each SM's L2 feed A + B/2 instead of A + B.  The
+// stage's empty barrier then waits for both CTAs' MMAs.
+template <int BN, bool FP8, bool SWAP, bool PAIR = false>
 __global__ void __launch_bounds__(kGemmThreads, SWAP ? 2 : 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUtensorMap tma_b,
                const GemmArgs args, unsigned* err) {
@@ -287,11 +291,16 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant_
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    const int rank = PAIR ? (int)cluster_ctarank() : 0;
+    const int64_t t_first = PAIR ? blockIdx.x / 2 : blockIdx.x;      // first tile (pair of M tiles) of this CTA
+    const int64_t t_step = PAIR ? gridDim.x / 2 : gridDim.x;
+    // M tile of this CTA within tile t (a pair index when PAIR)
+    auto my_mt = [&](int64_t mt) { return PAIR ? 2 * mt + rank : mt; };
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&full_bar[s], 1);
-            mbar_init(&empty_bar[s], 1);
+            mbar_init(&empty_bar[s], PAIR ? 2 : 1);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&tfull_bar[i], 1);
@@ -309,6 +318,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant_
     }
     tc_fence_before();
     __syncthreads();
+    if (PAIR) cluster_sync_all();    // the peer's barriers exist before anything is multicast to them
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     const bool producer = warp == 0 && lane == 0;
@@ -322,15 +332,19 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant_
             // Weight half of one stage (swapped: A holds the weights, else B).
             auto load_w = [&](int stage, int64_t mt, int n0, int kx) {
                 unsigned char* sa = smem + stage * C::STAGE_BYTES;
-                if (SWAP) tma_load_3d(sa, &tma_a, &full_bar[stage], args.b_kwrap ? kx % args.b_kwrap : kx, (int)(mt * kBM), 0);
-                else tma_load_2d(sa + C::A_BYTES, &tma_b, &full_bar[stage], args.b_kwrap ? kx % args.b_kwrap : kx, n0);
+                const int kw = args.b_kwrap ? kx % args.b_kwrap : kx;
+                if (SWAP) tma_load_3d(sa, &tma_a, &full_bar[stage], kw, (int)(mt * kBM), 0);
+                else if (PAIR)   // this CTA's half of the B tile, into both CTAs
+                    tma_load_2d_mc(sa + C::A_BYTES + rank * (BN / 2) * kRowBytes, &tma_b, &full_bar[stage], kw,
+                                   n0 + rank * (BN / 2), (uint16_t)3);
+                else tma_load_2d(sa + C::A_BYTES, &tma_b, &full_bar[stage], kw, n0);
             };
             // Constant weights do not depend on the kernels this one waits
             // for: the first ring stages fetch them before the wait, which
             // overlaps the previous kernel's tail (programmatic launch).
             int pre = 0;
             if (args.w_const) {
-                for (int64_t t = blockIdx.x; t < args.tiles && pre < STAGES; t += gridDim.x) {
+                for (int64_t t = t_first; t < args.tiles && pre < STAGES; t += t_step) {
                     int64_t mt, nt;
                     tile_coords(args, t, mt, nt);
                     int kb0, kb1;
@@ -348,11 +362,11 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant_
             uint32_t issued = 0, last_parity = 0;      // bit s: stage s was loaded / its last phase
             bool ok = true;
             int it = 0;
-            for (int64_t t = blockIdx.x; t < args.tiles && ok; t += gridDim.x) {
+            for (int64_t t = t_first; t < args.tiles && ok; t += t_step) {
                 int64_t mt, nt;
                 tile_coords(args, t, mt, nt);
-                const int b = (int)(mt / args.mt_per_batch);
-                const int r0 = (int)((mt % args.mt_per_batch) * kBM);
+                const int b = PAIR ? 0 : (int)(mt / args.mt_per_batch);
+                const int r0 = PAIR ? (int)(my_mt(mt) * kBM) : (int)((mt % args.mt_per_batch) * kBM);
                 const int n0 = (int)(nt * BN);
                 int kb0, kb1;
                 split_range(args, t, kb0, kb1);
@@ -394,7 +408,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant_
             int local = 0;
             bool ok = true;
             bool any = false;
-            for (int64_t t = blockIdx.x; t < args.tiles && ok; t += gridDim.x, ++local) {
+            for (int64_t t = t_first; t < args.tiles && ok; t += t_step, ++local) {
                 const int acc = local & 1;
                 const uint32_t aphase = (local >> 1) & 1;
                 bool got = false;
@@ -426,7 +440,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant_
                         else umma_bf16(d_tmem, ad, bd, IDESC, accum);
                     }
                     any = true;
-                    umma_commit(&empty_bar[stage]);
+                    if (PAIR) umma_commit_mc(&empty_bar[stage], (uint16_t)3);   // both CTAs' copies of the stage
+                    else umma_commit(&empty_bar[stage]);
                     if (++stage == STAGES) { stage = 0; phase ^= 1; }
                 }
                 if (!ok) break;
@@ -444,7 +459,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant_
         const int g = warp & 3;
         const int half = (warp - 2) >> 2;
         int local = 0;
-        for (int64_t t = blockIdx.x; t < args.tiles; t += gridDim.x, ++local) {
+        for (int64_t t = t_first; t < args.tiles; t += t_step, ++local) {
             const int acc = local & 1;
             const uint32_t aphase = (local >> 1) & 1;
             bool got = false;
@@ -456,8 +471,9 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant_
             tc_fence_after();
             int64_t mt, nt;
             tile_coords(args, t, mt, nt);
-            const int64_t b = mt / args.mt_per_batch;
-            const int64_t r = (mt % args.mt_per_batch) * kBM + g * 32 + lane;
+            if (PAIR) mt = my_mt(mt);     // one batch: M tile index = row tile
+            const int64_t b = PAIR ? 0 : mt / args.mt_per_batch;
+            const int64_t r = (PAIR ? mt : mt % args.mt_per_batch) * kBM + g * 32 + lane;
             const bool row_ok = r < args.rows;
             const uint32_t taddr = tmem_base + ((uint32_t)(g * 32) << 16) + acc * BN;
             if (SWAP) {
@@ -476,8 +492,13 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant_
             const GemmEpi& e = args.epi;
             // stores and reductions are staged; a residual update without
             // split-K reads its destination and stays in the thread's row
+            // a residual update without split-K reads its destination: it
+            // stays in the thread's row, where 8 float4 loads go out at once
             const bool staged = e.mode == MODE_PLAIN &&
                                 (e.out_type == OUT_F32 || (e.out_type == OUT_F32_ACC && args.ksplit > 1));
+            // bf16 rows go out as full 64-byte segments (8 rows per instruction)
+            const bool staged16 = e.mode == MODE_PLAIN && e.out_type == OUT_BF16 && e.vec && args.ksplit == 1 &&
+                                  (args.N & 7) == 0;
             float* stg = epi_stage + (warp - 2) * 32 * 32;
 #pragma unroll 1
             for (int c = half; c < BN / 32; c += 2) {
@@ -488,6 +509,31 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant_
                 float v[32];
 #pragma unroll
                 for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(raw[j]);
+                if (staged16) {
+                    if (row_ok && n0 < args.N) transform_f32(args, b, r, n0, v, 0);
+                    uint4* s4 = reinterpret_cast<uint4*>(stg);        // [32 rows][4 x 16 B]
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        s4[lane * 4 + (q ^ ((lane >> 1) & 3))] =
+                            make_uint4(pack_bf16x2(v[8 * q + 0], v[8 * q + 1]), pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
+                                       pack_bf16x2(v[8 * q + 4], v[8 * q + 5]), pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
+                    __syncwarp();
+                    const int pq = lane & 3;                          // 16-byte piece of the row segment
+                    const int64_t col = n0 + pq * 8;
+                    const int64_t rq = (PAIR ? mt : mt % args.mt_per_batch) * kBM + g * 32;
+                    const int64_t obr = e.out_batch_rows ? e.out_batch_rows : args.rows;
+                    __nv_bfloat16* ob = reinterpret_cast<__nv_bfloat16*>(e.out) + (b * obr + e.out_row_offset) * e.ldo + col;
+                    if (col < args.N) {
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const int rr = (lane >> 2) + 8 * i;
+                            if (rq + rr < args.rows)
+                                *reinterpret_cast<uint4*>(ob + (rq + rr) * e.ldo) = s4[rr * 4 + (pq ^ ((rr >> 1) & 3))];
+                        }
+                    }
+                    __syncwarp();
+                    continue;
+                }
                 if (!staged) {
                     if (row_ok && n0 < args.N) store_chunk(args, b, r, n0, v, (int)(t % args.ksplit));
                     continue;
@@ -502,18 +548,20 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant_
                         make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
                 __syncwarp();
                 const int64_t col = n0 + lane;
-                const int64_t rq = (mt % args.mt_per_batch) * kBM + g * 32;   // first row of the quarter
+                const int64_t rq = (PAIR ? mt : mt % args.mt_per_batch) * kBM + g * 32;   // first row of the quarter
                 const int64_t obr = e.out_batch_rows ? e.out_batch_rows : args.rows;
                 const bool reduce = args.ksplit > 1;             // partial tiles of one output
                 float* ob = reinterpret_cast<float*>(e.out) + (b * obr + e.out_row_offset) * e.ldo + col;
                 if (col < args.N) {
+                    {
 #pragma unroll 4
-                    for (int rr = 0; rr < 32; ++rr) {
-                        if (rq + rr >= args.rows) break;
-                        const float x = stg[rr * 32 + ((((lane >> 2) ^ (rr & 7))) << 2) + (lane & 3)];
-                        float* dst = ob + (rq + rr) * e.ldo;
-                        if (reduce) atomicAdd(dst, x);   // result unused: a reduction
-                        else *dst = x;
+                        for (int rr = 0; rr < 32; ++rr) {
+                            if (rq + rr >= args.rows) break;
+                            const float x = stg[rr * 32 + ((((lane >> 2) ^ (rr & 7))) << 2) + (lane & 3)];
+                            float* dst = ob + (rq + rr) * e.ldo;
+                            if (reduce) atomicAdd(dst, x);   // result unused: a reduction
+                            else *dst = x;
+                        }
                     }
                 }
                 __syncwarp();
@@ -524,6 +572,9 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant_
     }
     tc_fence_before();
     __syncthreads();
+    // neither CTA of a pair leaves while the other may still multicast into
+    // its shared memory or arrive on its barriers
+    if (PAIR) cluster_sync_all();
     tc_fence_after();
     if (warp == 1) tmem_dealloc(tmem_base, C::TMEM_COLS);
 }
@@ -600,6 +651,43 @@ wb_status launch_tc(const GemmPlan& p, GemmArgs a, unsigned* err, cudaStream_t s
     return WB_OK;
 }
 
+// CTA pairs (clusters of two) sharing each B tile; a.tiles counts M-tile pairs.
+template <int BN, bool FP8>
+wb_status launch_tc_pair(const GemmPlan& p, GemmArgs a, unsigned* err, cudaStream_t s) {
+    using C = Cfg<BN>;
+    auto kern = gemm_tc_kernel<BN, FP8, false, true>;
+    static bool attr_set[64] = {};
+    int dev = 0;
+    WB_CUDA(cudaGetDevice(&dev));
+    if (!attr_set[dev & 63]) {
+        WB_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM));
+        attr_set[dev & 63] = true;
+    }
+    const int64_t pairs_per_wave = num_sms() / 2;
+    const int64_t kb_per_cta = (int64_t)a.kblocks * ((a.tiles + pairs_per_wave - 1) / pairs_per_wave);
+    a.stages = (int)std::max<int64_t>(2, std::min<int64_t>(C::STAGES, kb_per_cta));
+    const int smem = a.stages * C::STAGE_BYTES + kEpiStageBytes + 1024 + 256;
+    // as many clusters as can be resident at once (persistent)
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(2 * pairs_per_wave));
+    cfg.blockDim = dim3(kGemmThreads);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int clusters = 0;
+    WB_CUDA(cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg));
+    if (clusters <= 0) return fail(WB_ERR_CUDA, "no resident CTA pair for the paired GEMM");
+    clusters = (int)std::min<int64_t>(clusters, a.tiles);
+    WB_CUDA(launch_k_cluster(kern, dim3(2 * clusters), dim3(kGemmThreads), smem, s, 2, p.tma_a, p.tma_b, a, err));
+    WB_CUDA(cudaGetLastError());
+    return WB_OK;
+}
+
 }  // namespace
 
 int num_sms() {
@@ -613,7 +701,7 @@ int num_sms() {
 }
 
 wb_status gemm_plan(GemmPlan* plan, const GemmOperand& A, const GemmOperand& B, int64_t N, int64_t K,
-                    bool fp8, int bn, int64_t b_kwrap) {
+                    bool fp8, int bn, int64_t b_kwrap, bool pair) {
     if (wb_status st = get_encoder()) return st;
     const int esz = fp8 ? 1 : 2;
     const int bk = fp8 ? 128 : 64;
@@ -633,9 +721,12 @@ wb_status gemm_plan(GemmPlan* plan, const GemmOperand& A, const GemmOperand& B, 
     {
         uint64_t dims[2] = {(uint64_t)(b_kwrap ? b_kwrap : K), (uint64_t)N};
         uint64_t strides[1] = {(uint64_t)(B.row_stride * esz)};
-        uint32_t box[2] = {(uint32_t)bk, (uint32_t)bn};
+        // a CTA pair loads the B tile as two halves, one per CTA
+        uint32_t box[2] = {(uint32_t)bk, (uint32_t)(pair ? bn / 2 : bn)};
         if (wb_status st = encode_map(&plan->tma_b, B.ptr, 2, dims, strides, box, fp8)) return st;
     }
+    if (pair && (A.batches != 1 || bn != 256)) return fail(WB_ERR_INVALID_ARG, "paired GEMM: one batch, 256-wide tiles");
+    plan->pair = pair;
     plan->M_rows = A.rows;
     plan->batches = A.batches;
     plan->N = N;
@@ -697,6 +788,10 @@ wb_status gemm_run(const GemmPlan& p, const GemmEpi& epi, unsigned* err, cudaStr
         a.mt_per_batch = (p.N + kBM - 1) / kBM;        // weight-row tiles
         a.mt_total = a.mt_per_batch;
         a.nt_total = (a.rows + p.bn - 1) / p.bn;        // activation-row tiles
+    } else if (p.pair) {
+        a.mt_per_batch = ((a.rows + kBM - 1) / kBM + 1) / 2;   // M-tile pairs
+        a.mt_total = a.mt_per_batch;
+        a.nt_total = (p.N + p.bn - 1) / p.bn;
     } else {
         a.mt_per_batch = (a.rows + kBM - 1) / kBM;
         a.mt_total = a.mt_per_batch * p.batches;
@@ -734,6 +829,9 @@ wb_status gemm_run(const GemmPlan& p, const GemmEpi& epi, unsigned* err, cudaStr
             else if (p.bn == 64) st = launch_tc<64, false, true>(p, a, err, s, max_ctas);
             else st = launch_tc<32, false, true>(p, a, err, s, max_ctas);
         }
+    } else if (p.pair) {
+        if (a.ksplit != 1) return fail(WB_ERR_INVALID_ARG, "paired GEMM: no split-K");
+        st = p.fp8 ? launch_tc_pair<256, true>(p, a, err, s) : launch_tc_pair<256, false>(p, a, err, s);
     } else if (p.fp8) {
         if (p.bn == 256) st = launch_tc<256, true, false>(p, a, err, s, max_ctas);
         else if (p.bn == 128) st = launch_tc<128, true, false>(p, a, err, s, max_ctas);

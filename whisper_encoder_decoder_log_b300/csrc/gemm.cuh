@@ -59,13 +59,14 @@ struct GemmPlan {
     bool fp8 = false;
     bool swap = false;     // small-M form: weights are the 128-row MMA operand
     bool w_const = false;  // the weight operand is not written by kernels this GEMM may overlap
+    bool pair = false;     // clusters of two CTAs share each B tile (TMA multicast)
     bool ok = false;
 };
 
 // Build the TMA descriptors (host only, no launch).  Element type bf16, or
 // E4M3 when fp8.  Returns WB_OK or an error code with the message set.
 wb_status gemm_plan(GemmPlan* plan, const GemmOperand& A, const GemmOperand& B, int64_t N,
-                    int64_t K, bool fp8, int bn, int64_t b_kwrap = 0);
+                    int64_t K, bool fp8, int bn, int64_t b_kwrap = 0, bool pair = false);
 // Small-M form: C[M, N] = X[M, K] . W[N, K]^T computed as W . X^T, with the
 // weights as the 128-row MMA operand and bn (32/64/128) activation rows as the
 // MMA N dimension; fp32 output, linear epilogue; w_kwrap as b_kwrap above.
