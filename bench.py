@@ -473,7 +473,19 @@ def main():
         peak = float(peaks.get("hbm_gbs", 6400.0))
         roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s"}
     roof["frac"] = roof["achieved"] / roof["peak"] if roof["peak"] else None
-    roof["traffic"] = None
+    # DRAM bytes per launch from the committed ncu captures (profiles/) of
+    # kernels unchanged since: the capture's read + write bytes over its
+    # algorithmic bytes, applied to this launch's algorithmic bytes (the
+    # captures ran smaller batches of the same per-unit work).
+    traffic_ratio = {
+        wb.KERNEL_CROSS_ATTN: (245.95e6 + 3.16e6) / (32 * 20 * (2 * 1500 * 64 * 2 + 64 * 4 + 64 * 2)),
+        wb.KERNEL_MEL: (139.39e6 + 63.99e6) / (64 * (480000 * 4 + 128 * 3000 * 4)),
+    }
+    if dom in traffic_ratio and roof["bound"] == "hbm" and n_dom:
+        roof["traffic"] = units_dom / n_dom * traffic_ratio[dom]
+        roof["traffic_unit"] = "bytes per launch"
+    else:
+        roof["traffic"] = None
     roof["kernel"] = wb.KERNEL_NAMES.get(dom, str(dom))
     roof["launches_per_step"] = n_dom / max(1, args.steps)
     roof["ms_per_step"] = ms_dom / max(1, args.steps)

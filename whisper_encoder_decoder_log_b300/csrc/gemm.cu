@@ -80,17 +80,37 @@ __device__ __forceinline__ void transform_f32(const GemmArgs& a, int64_t b, int6
     const GemmEpi& e = a.epi;
     const int64_t N = a.N;
     const bool full = n0 + 32 <= N;
+    // column vectors as 16-byte loads when the chunk is whole and aligned
+    const bool v4 = full && (n0 & 3) == 0;
     if (e.row_scale || e.col_scale) {
         const float rs = e.row_scale ? e.row_scale[b * a.rows + r] : 1.f;
+        if (e.col_scale && v4 && (reinterpret_cast<uintptr_t>(e.col_scale) & 15) == 0) {
+            const float4* c4 = reinterpret_cast<const float4*>(e.col_scale + n0);
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-            const float cs = (e.col_scale && (full || n0 + j < N)) ? e.col_scale[n0 + j] : 1.f;
-            v[j] *= rs * cs;
+            for (int q = 0; q < 8; ++q) {
+                const float4 c = c4[q];
+                v[4 * q] *= rs * c.x; v[4 * q + 1] *= rs * c.y; v[4 * q + 2] *= rs * c.z; v[4 * q + 3] *= rs * c.w;
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                const float cs = (e.col_scale && (full || n0 + j < N)) ? e.col_scale[n0 + j] : 1.f;
+                v[j] *= rs * cs;
+            }
         }
     }
     if (e.bias && ks == 0) {
+        if (v4 && (reinterpret_cast<uintptr_t>(e.bias) & 15) == 0) {
+            const float4* b4 = reinterpret_cast<const float4*>(e.bias + n0);
 #pragma unroll
-        for (int j = 0; j < 32; ++j) v[j] += (full || n0 + j < N) ? e.bias[n0 + j] : 0.f;
+            for (int q = 0; q < 8; ++q) {
+                const float4 c = b4[q];
+                v[4 * q] += c.x; v[4 * q + 1] += c.y; v[4 * q + 2] += c.z; v[4 * q + 3] += c.w;
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] += (full || n0 + j < N) ? e.bias[n0 + j] : 0.f;
+        }
     }
     if (e.gelu) {
 #pragma unroll
