@@ -32,7 +32,13 @@ Readings taken where the pages are silent or contradict one another:
     product of scales multiplies the exact product of the decoded codes;
   * FP8 self-attention cache: one scale per (layer, K or V) of each chunk,
     taken from the forced-prefix rows (oracle.e4m3.kv_scale_of); attention
-    reads the dequantised cache, the current token's own row included.
+    reads the dequantised cache, the current token's own row included;
+  * FP8 cross-attention K/V (the float8 KV cache of [BFW] "Inference Stack"
+    extended to the cross-attention, as [WB] "Precision Presets" does for
+    attention under aggressive_fp8): one scale per (layer, K or V) of each
+    chunk, amax / 448 over all 1500 x d values of that tensor (all of them
+    are known when it is precomputed, so no headroom factor), applied to the
+    fp32 projection before rounding; attention reads the dequantised values.
 """
 from __future__ import annotations
 
@@ -182,6 +188,17 @@ def cross_kv(enc, W, l: int):
             Linear(W[p + "cv.w"], W[p + "cv.b"])(enc))
 
 
+def cross_kv_fp8(k, v):
+    """E4M3 round trip of one chunk's cross K and V of one layer, each with its
+    own per-tensor scale amax / 448 (returned with the dequantised values)."""
+    out = []
+    for x in (k, v):
+        x32 = np.asarray(x, np.float32)
+        s = e4m3.scale_of(float(np.max(np.abs(x32))))
+        out.append((e4m3.dequantise(e4m3.quantise(x32, s), s), s))
+    return out
+
+
 def _kv_fp8(x, prefix_len: int):
     s = e4m3.kv_scale_of(np.max(np.abs(np.asarray(x[:prefix_len], np.float32))))
     return e4m3.dequantise(e4m3.quantise(x, s), s), s
@@ -189,7 +206,7 @@ def _kv_fp8(x, prefix_len: int):
 
 def decode_teacher_forced(tokens, enc, W, dims, kv_fp8: bool = False,
                           prefix_len: int = 4, fp8: bool = False,
-                          return_hidden: bool = False):
+                          return_hidden: bool = False, cross_fp8: bool = False):
     """Logits [T, V] for a token sequence run through the decoder in one causal pass.
 
     Equivalent to stepping token by token with a KV cache: every position only
@@ -214,6 +231,9 @@ def decode_teacher_forced(tokens, enc, W, dims, kv_fp8: bool = False,
         a = layer_norm(h, W[p + "ln2.g"], W[p + "ln2.b"])
         q = Linear(W[p + "cq.w"], W[p + "cq.b"])(a)
         ck, cv = cross_kv(enc, W, l)
+        if cross_fp8:
+            (ck, sck), (cv, scv) = cross_kv_fp8(ck, cv)
+            info.setdefault("cross_scales", []).append((sck, scv))
         h = h + Linear(W[p + "co.w"], W[p + "co.b"])(multi_head(q, ck, cv, dims.n_heads))
         a = layer_norm(h, W[p + "ln3.g"], W[p + "ln3.b"])
         f = gelu(Linear(W[p + "fc1.w"], W[p + "fc1.b"], fp8)(a))

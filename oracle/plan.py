@@ -9,9 +9,10 @@ batches.
 Readings:
   * chunk c of the batch is (request r, index k) in request order, then index
     order; it holds min(480000, samples_r - 480000 k) real samples;
-  * a chunk's decode state costs, per decoder layer, the bf16 cross-attention
-    K and V over 1500 encoder positions plus its float8 self-attention K and V
-    over its own decode length L_c, plus its token row (448 int32);
+  * a chunk's decode state costs, per decoder layer, the cross-attention K
+    and V over 1500 encoder positions (bf16, or float8 when the cross K/V are
+    stored as E4M3) plus its float8 self-attention K and V over its own decode
+    length L_c, plus its token row (448 int32);
   * waves: chunks sorted by decode length, longest first (ties by chunk
     index), are packed greedily in that order; a new wave opens when the next
     chunk would push the running total of per-chunk bytes past the budget.
@@ -39,19 +40,19 @@ def chunk_table(req_samples):
     return (np.array(req, np.int32), np.array(idx, np.int32), np.array(valid, np.int32))
 
 
-def chunk_state_bytes(d_model: int, dec_layers: int, length: int) -> int:
-    cross = dec_layers * 2 * N_CTX * d_model * 2
+def chunk_state_bytes(d_model: int, dec_layers: int, length: int, cross_bytes: int = 2) -> int:
+    cross = dec_layers * 2 * N_CTX * d_model * cross_bytes
     self_kv = dec_layers * 2 * int(length) * d_model
     return cross + self_kv + MAX_POS * 4
 
 
-def plan_waves(chunk_len, d_model: int, dec_layers: int, budget_bytes: int):
+def plan_waves(chunk_len, d_model: int, dec_layers: int, budget_bytes: int, cross_bytes: int = 2):
     """List of waves, each an int32 array of chunk indices in decode order."""
     chunk_len = np.asarray(chunk_len, dtype=np.int64)
     order = sorted(range(chunk_len.size), key=lambda c: (-int(chunk_len[c]), c))
     waves, cur, used = [], [], 0
     for c in order:
-        b = chunk_state_bytes(d_model, dec_layers, int(chunk_len[c]))
+        b = chunk_state_bytes(d_model, dec_layers, int(chunk_len[c]), cross_bytes)
         if b > budget_bytes:
             raise ValueError("one chunk exceeds the wave budget")
         if cur and used + b > budget_bytes:

@@ -148,20 +148,61 @@ def test_encoder_permutation_equivariance_without_positions():
     np.testing.assert_allclose(a[perm], b, atol=1e-12)
 
 
-@pytest.mark.parametrize("kv_fp8", [False, True])
-def test_decoder_causality_and_prefix_consistency(kv_fp8):
+@pytest.mark.parametrize("kv_fp8,cross_fp8", [(False, False), (True, False), (True, True)])
+def test_decoder_causality_and_prefix_consistency(kv_fp8, cross_fp8):
     W = make_weights(MINI, 7, bf16=True)
     rng = np.random.default_rng(7)
     enc = rng.normal(size=(20, MINI.d_model))
     tok = rng.integers(0, MINI.vocab, size=12)
-    full, _ = model.decode_teacher_forced(tok, enc, W, MINI, kv_fp8=kv_fp8)
+    full, _ = model.decode_teacher_forced(tok, enc, W, MINI, kv_fp8=kv_fp8, cross_fp8=cross_fp8)
     tok2 = tok.copy()
     tok2[8:] = rng.integers(0, MINI.vocab, size=4)
-    alt, _ = model.decode_teacher_forced(tok2, enc, W, MINI, kv_fp8=kv_fp8)
+    alt, _ = model.decode_teacher_forced(tok2, enc, W, MINI, kv_fp8=kv_fp8, cross_fp8=cross_fp8)
     np.testing.assert_array_equal(full[:8], alt[:8])          # future tokens are invisible
     for t in (4, 6, 11):                                      # cache-append == full pass
-        part, _ = model.decode_teacher_forced(tok[:t + 1], enc, W, MINI, kv_fp8=kv_fp8)
+        part, _ = model.decode_teacher_forced(tok[:t + 1], enc, W, MINI, kv_fp8=kv_fp8, cross_fp8=cross_fp8)
         np.testing.assert_allclose(part[t], full[t], atol=1e-12)
+
+
+def test_cross_kv_fp8_round_trip_bounds():
+    """Per-tensor E4M3 of a cross K/V: the largest magnitude maps to the top code
+    (448 x scale = amax up to fp32 rounding of the scale), normal values keep a
+    relative error <= 2^-4 (3 mantissa bits, round to nearest), values below
+    the normal range an absolute error <= 2^-10 x scale, and an all-zero
+    tensor stays zero."""
+    rng = np.random.default_rng(21)
+    k = rng.normal(size=(1500, 64)) * 0.7
+    k[123, 45] = -3.25                                        # the largest magnitude
+    v = rng.standard_t(3, size=(1500, 64))
+    (kq, sk), (vq, sv) = model.cross_kv_fp8(k, v)
+    for x, xq, s in ((k, kq, sk), (v, vq, sv)):
+        x32 = np.asarray(x, np.float32).astype(np.float64)
+        amax = np.abs(x32).max()
+        assert s == np.float32(np.float32(amax) / np.float32(448.0))
+        i = np.unravel_index(np.argmax(np.abs(x32)), x32.shape)
+        assert abs(abs(xq[i]) - amax) <= amax * 2.0 ** -23
+        assert np.sign(xq[i]) == np.sign(x32[i])
+        normal = np.abs(x32) >= 2.0 ** -6 * float(s)
+        assert np.all(np.abs(xq - x32)[normal] <= 2.0 ** -4 * np.abs(x32)[normal] * (1 + 1e-6))
+        assert np.all(np.abs(xq - x32)[~normal] <= 2.0 ** -10 * float(s) * (1 + 1e-6))
+    (zq, sz), _ = model.cross_kv_fp8(np.zeros((4, 64)), v)
+    assert sz == 1.0 and not zq.any()
+
+
+def test_cross_fp8_decoder_close_to_exact_and_scales_per_layer():
+    W = make_weights(MINI, 12, bf16=True)
+    rng = np.random.default_rng(12)
+    enc = rng.normal(size=(30, MINI.d_model))
+    tok = rng.integers(0, MINI.vocab, size=10)
+    ref, _ = model.decode_teacher_forced(tok, enc, W, MINI, kv_fp8=True)
+    got, info = model.decode_teacher_forced(tok, enc, W, MINI, kv_fp8=True, cross_fp8=True)
+    assert len(info["cross_scales"]) == MINI.dec_layers
+    for l, (sk, sv) in enumerate(info["cross_scales"]):
+        ck, cv = model.cross_kv(enc, W, l)
+        assert sk == e4m3.scale_of(np.abs(np.asarray(ck, np.float32)).max())
+        assert sv == e4m3.scale_of(np.abs(np.asarray(cv, np.float32)).max())
+    # E4M3 rounding of K and V moves the logits, but by much less than their spread
+    assert 0 < np.sqrt(np.mean((got - ref) ** 2)) < 0.1 * ref.std()
 
 
 def test_key_bias_does_not_change_attention():

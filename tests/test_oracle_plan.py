@@ -52,3 +52,16 @@ def test_serving_batch_waves():
 def test_oversize_chunk_rejected():
     with pytest.raises(ValueError):
         plan.plan_waves([448], 1280, 32, 10**6)
+
+
+def test_fp8_cross_kv_halves_the_cross_bytes_and_fits_more_per_wave():
+    d, L, n = 1280, 32, 200
+    bf = plan.chunk_state_bytes(d, L, n)
+    f8 = plan.chunk_state_bytes(d, L, n, cross_bytes=1)
+    assert bf - f8 == L * 2 * 1500 * d                      # exactly half of the bf16 cross K/V
+    lens = np.full(900, 448, np.int32)
+    budget = 180 * 10 ** 9
+    w_bf = plan.plan_waves(lens, d, L, budget)
+    w_f8 = plan.plan_waves(lens, d, L, budget, cross_bytes=1)
+    assert len(w_f8) < len(w_bf)
+    assert sorted(np.concatenate(w_f8).tolist()) == list(range(900))
