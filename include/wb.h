@@ -100,8 +100,22 @@ typedef struct wb_model_desc {
     int32_t dec_layers;   /* >= 0                                           */
     int32_t vocab;        /* >= 1                                           */
     int32_t precision;    /* WB_PREC_*                                      */
-    int32_t kv_fp8;       /* 1: self-attention cache in E4M3 (not with FP32) */
+    int32_t kv_fp8;       /* WB_KV_*: 0 none; 1 self-attention cache in E4M3;
+                             2 also the cross-attention K/V (not with FP32)  */
 } wb_model_desc;
+
+/*
+ * kv_fp8 values.  WB_KV_FP8_CROSS additionally stores each chunk's
+ * precomputed cross-attention K and V in E4M3 with one scale per (chunk,
+ * decoder layer, K or V): amax / 448 over that 1500 x d tensor (the float8
+ * KV cache of "Blazingly fast whisper transcriptions with Inference
+ * Endpoints", "Inference Stack", applied to the cross-attention as
+ * "whisper-blaze 0.1.8", "Precision Presets" does for attention under
+ * aggressive_fp8).  It halves the bytes the decode step streams per chunk.
+ */
+#define WB_KV_NONE 0
+#define WB_KV_FP8_SELF 1
+#define WB_KV_FP8_CROSS 2
 
 typedef struct wb_model wb_model;
 

@@ -79,12 +79,14 @@ def test_unknown_weight_name_is_an_error():
     assert e.value.status == -1
 
 
+@pytest.mark.parametrize("kv", [1, 2])
 @pytest.mark.parametrize("budget", [2 * 10**9, 50 * 10**9, 180 * 10**9])
-def test_wave_plan_matches_oracle_bit_exact(budget):
+def test_wave_plan_matches_oracle_bit_exact(budget, kv):
     sb = serving_requests(0, n_req=48, with_audio=False)
-    desc = wb.make_desc(LARGE_V3, wb.PREC_MIXED_FP8, True)
+    desc = wb.make_desc(LARGE_V3, wb.PREC_MIXED_FP8, kv)
     wave, order, nw = wb.wb_plan_waves(desc, sb.chunk_len, budget)
-    ref = oplan.plan_waves(sb.chunk_len, LARGE_V3.d_model, LARGE_V3.dec_layers, budget)
+    # float8 cross K/V (kv = 2) halve the per-chunk cross bytes
+    ref = oplan.plan_waves(sb.chunk_len, LARGE_V3.d_model, LARGE_V3.dec_layers, budget, 1 if kv == 2 else 2)
     assert nw == len(ref)
     assert np.array_equal(order, np.concatenate(ref))
     for w, chunks in enumerate(ref):

@@ -24,10 +24,13 @@ def _requests(lengths_s, seed):
     return audio, offs, samples
 
 
-@pytest.mark.parametrize("prec", [wb.PREC_BF16, wb.PREC_MIXED_FP8])
-def test_transcribe_batch_matches_oracle(prec):
+@pytest.mark.parametrize("prec,kv", [(wb.PREC_BF16, wb.KV_FP8_SELF), (wb.PREC_MIXED_FP8, wb.KV_FP8_SELF),
+                                     (wb.PREC_MIXED_FP8, wb.KV_FP8_CROSS)])
+def test_transcribe_batch_matches_oracle(prec, kv):
     dims = ModelDims("turbo-2enc", 128, 1280, 20, 5120, 2, 4, TURBO.vocab)
-    m = GpuModel(dims, prec, True, seed=12)
+    m = GpuModel(dims, prec, kv, seed=12)
+    cross = kv == wb.KV_FP8_CROSS
+    cb = 1 if cross else 2
     audio, offs, samples = _requests([50.0, 70.5, 12.0], seed=40)
     req, idx, valid = oplan.chunk_table(samples)
     n = req.size
@@ -35,8 +38,8 @@ def test_transcribe_batch_matches_oracle(prec):
     lens = np.array([12, 20, 9, 30, 16, 7], np.int32)
     prefix = forced_prefix(3, dims.vocab)
     # a budget that holds about three chunks' decoder state forces several waves
-    budget = 3 * oplan.chunk_state_bytes(dims.d_model, dims.dec_layers, 30)
-    waves = oplan.plan_waves(lens, dims.d_model, dims.dec_layers, budget)
+    budget = 3 * oplan.chunk_state_bytes(dims.d_model, dims.dec_layers, 30, cb)
+    waves = oplan.plan_waves(lens, dims.d_model, dims.dec_layers, budget, cb)
     assert len(waves) >= 2
     ws = torch.empty(wb.wb_transcribe_workspace_size(m.h, samples, lens, budget), dtype=torch.uint8, device="cuda")
     tokens = torch.full((n, 448), -7, dtype=torch.int32, device="cuda")
@@ -53,7 +56,7 @@ def test_transcribe_batch_matches_oracle(prec):
         assert (tok[c, L:] == -7).all()                      # untouched past the chunk's length
         assert ((tok[c, :L] >= 0) & (tok[c, :L] < dims.vocab)).all()
         enc = omodel.encode(omel.log_mel(chunks[c], 128), m.W, dims, fp8=fp8)
-        ref, _ = omodel.decode_teacher_forced(tok[c, :L - 1], enc, m.W, dims, kv_fp8=True, fp8=fp8)
+        ref, _ = omodel.decode_teacher_forced(tok[c, :L - 1], enc, m.W, dims, kv_fp8=True, fp8=fp8, cross_fp8=cross)
         pred = omodel.greedy(ref[3:L - 1])
         agree += int((pred == tok[c, 4:L]).sum())
         total += L - 4

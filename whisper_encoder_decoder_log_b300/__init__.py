@@ -289,9 +289,15 @@ def wb_sync_status(model: Optional[int] = None, stream=None):
 
 # ----------------------------------------------------------------- marshalling helpers
 
-def make_desc(dims, precision: int, kv_fp8: bool) -> ModelDesc:
+KV_NONE, KV_FP8_SELF, KV_FP8_CROSS = 0, 1, 2
+
+
+def make_desc(dims, precision: int, kv_fp8) -> ModelDesc:
+    """kv_fp8: False/True (E4M3 self-attention cache) or one of KV_* (KV_FP8_CROSS
+    also stores the cross-attention K/V in E4M3)."""
+    kv = int(kv_fp8) if not isinstance(kv_fp8, bool) else (KV_FP8_SELF if kv_fp8 else KV_NONE)
     return ModelDesc(dims.n_mels, dims.d_model, dims.n_heads, dims.d_ffn, dims.enc_layers, dims.dec_layers,
-                     dims.vocab, precision, 1 if kv_fp8 else 0)
+                     dims.vocab, precision, kv)
 
 
 def pack_weights(desc: ModelDesc, tensors: Dict[str, np.ndarray], device="cuda"):

@@ -79,6 +79,7 @@ bool valid_desc(const wb_model_desc* d, std::string* why) {
     if (d->vocab <= 0) { *why = "vocab must be positive"; return false; }
     if (d->precision < WB_PREC_FP32 || d->precision > WB_PREC_MIXED_FP8) { *why = "bad precision"; return false; }
     if (d->kv_fp8 && d->precision == WB_PREC_FP32) { *why = "kv_fp8 needs a bf16 precision"; return false; }
+    if (d->kv_fp8 < WB_KV_NONE || d->kv_fp8 > WB_KV_FP8_CROSS) { *why = "kv_fp8 must be 0, 1 or 2"; return false; }
     return true;
 }
 
@@ -407,6 +408,8 @@ struct wb_decoder {
     cudaStream_t cap_stream = nullptr; // graphs are captured here (capture runs nothing)
     // device buffers carved from the workspace
     void* crosskv = nullptr;
+    void* ckv_tmp = nullptr;           // bf16 cross K/V of one chunk group before E4M3 rounding
+    float* cscale = nullptr;           // E4M3 cross K/V scales [layer][K|V][chunk]
     void* cache = nullptr;
     float* kscale = nullptr;
     float* vscale = nullptr;
@@ -429,6 +432,7 @@ namespace wb {
 namespace {
 
 constexpr int kMaxPrefix = 32;
+constexpr int64_t kCrossGroup = 32;   // chunks per E4M3 cross K/V precompute group
 
 struct DecLayout {
     size_t total = 0;
@@ -441,7 +445,10 @@ size_t carve_decoder(const wb_model* m, int64_t B, const int32_t* len, wb_decode
     const int Ld = m->desc.dec_layers, d = m->d(), H = m->H(), F = m->F();
     const size_t act = m->fp32() ? 4 : 2;
     const int64_t R = B * kMaxPrefix;
-    void* crosskv = c.take<uint8_t>((size_t)Ld * B * 2 * kCtx * d * act);
+    const bool c8 = m->desc.kv_fp8 == WB_KV_FP8_CROSS;
+    void* crosskv = c.take<uint8_t>((size_t)Ld * B * 2 * kCtx * d * (c8 ? 1 : act));
+    void* ckv_tmp = c8 ? c.take<uint8_t>((size_t)Ld * std::min<int64_t>(B, kCrossGroup) * 2 * kCtx * d * 2) : nullptr;
+    float* cscale = c8 ? c.take<float>((size_t)std::max(1, Ld) * 2 * B) : nullptr;
     int64_t cache_elems = 0;
     for (int64_t i = 0; i < B; ++i) cache_elems += (int64_t)Ld * 2 * H * len[i] * 64;
     void* cache = c.take<uint8_t>((size_t)cache_elems * (m->desc.kv_fp8 ? 1 : 4));
@@ -463,7 +470,8 @@ size_t carve_decoder(const wb_model* m, int64_t B, const int32_t* len, wb_decode
     int* pos_dev = c.take<int>(64);
     if (dec) {
         dec->pos_dev = pos_dev;
-        dec->crosskv = crosskv; dec->cache = cache; dec->kscale = kscale; dec->vscale = vscale;
+        dec->crosskv = crosskv; dec->ckv_tmp = ckv_tmp; dec->cscale = cscale;
+        dec->cache = cache; dec->kscale = kscale; dec->vscale = vscale;
         dec->off = off; dec->len_dev = lend; dec->h = h; dec->a = a; dec->a_scale = a_scale; dec->qkv = qkv;
         dec->attn = attn; dec->cq = cq; dec->f = f; dec->f2 = f2; dec->fq = fq; dec->f_scale = f_scale; dec->logits = logits;
     }
@@ -578,14 +586,16 @@ wb_status decoder_layers(wb_decoder* dec, int64_t n_chunks, int rows_per_chunk, 
                 return st;
         }
         {
-            const size_t act = f32 ? 4 : 2;
+            const bool c8 = m->desc.kv_fp8 == WB_KV_FP8_CROSS;
+            const size_t act = c8 ? 1 : (f32 ? 4 : 2);
             KVView kv;
             kv.ptr = reinterpret_cast<uint8_t*>(dec->crosskv) + (size_t)l * dec->B * 2 * H * kCtx * 64 * act;
             kv.chunk_stride = (int64_t)2 * H * kCtx * 64; kv.head_stride = (int64_t)kCtx * 64; kv.heads = H;
             kv.k_blk = 0; kv.v_blk = 1; kv.row_stride = 64;
+            if (c8) { kv.k_scale = dec->cscale + (size_t)(2 * l) * dec->B; kv.v_scale = dec->cscale + (size_t)(2 * l + 1) * dec->B; }
             if (pos_dev) { kv.pos_dev = pos_dev; kv.active_len = dec->len_dev; }
-            if (wb_status st = attn_rows(DT_F32, f32 ? DT_F32 : DT_BF16, attn_dt, dec->cq, d, n_chunks, rows_per_chunk,
-                                         H, kv, kCtx, false, 0, dec->attn, lda, s, sp ? d : 0))
+            if (wb_status st = attn_rows(DT_F32, c8 ? DT_E4M3 : (f32 ? DT_F32 : DT_BF16), attn_dt, dec->cq, d, n_chunks,
+                                         rows_per_chunk, H, kv, kCtx, false, 0, dec->attn, lda, s, sp ? d : 0))
                 return st;
         }
         {
@@ -695,8 +705,9 @@ void plan_waves_host(const wb_model_desc& d, int32_t n, const int32_t* len, uint
     std::vector<int32_t> order(n);
     for (int32_t i = 0; i < n; ++i) order[i] = i;
     std::stable_sort(order.begin(), order.end(), [&](int32_t a, int32_t b) { return len[a] > len[b]; });
+    const uint64_t cross_elt = d.kv_fp8 == WB_KV_FP8_CROSS ? 1 : 2;
     auto bytes = [&](int32_t L) {
-        return (uint64_t)d.dec_layers * 2 * kCtx * d.d_model * 2 + (uint64_t)d.dec_layers * 2 * L * d.d_model +
+        return (uint64_t)d.dec_layers * 2 * kCtx * d.d_model * cross_elt + (uint64_t)d.dec_layers * 2 * L * d.d_model +
                (uint64_t)kMaxPos * 4;
     };
     *too_big = false;
@@ -962,7 +973,7 @@ wb_status wb_decoder_init(wb_model* m, int64_t B, const int32_t* len, const void
         cudaMemcpyAsync(dec->len_dev, len, B * 4, cudaMemcpyHostToDevice, s) != cudaSuccess ||
         cudaStreamSynchronize(s) != cudaSuccess)
         return fail_free(fail(WB_ERR_CUDA, "wb_decoder_init: upload"));
-    if (Ld > 0) {
+    if (Ld > 0 && m->desc.kv_fp8 != WB_KV_FP8_CROSS) {
         Lin L;
         L.a = enc; L.rows = B * kCtx; L.lda = d; L.w = m->W("dec.0.ck.w"); L.N = (int64_t)Ld * 2 * d; L.K = d;
         GemmEpi ep = epi_out(dec->crosskv, 0, m->fp32() ? OUT_F32 : OUT_BF16, m->V("dec.0.ck.b"));
@@ -971,6 +982,25 @@ wb_status wb_decoder_init(wb_model* m, int64_t B, const int32_t* len, const void
         ep.ckv_heads = H;
         ep.ckv_chunks = B;
         if (wb_status st = linear(m, L, ep, s)) return fail_free(st);
+    } else if (Ld > 0) {
+        // E4M3 cross K/V: per group of chunks, the bf16 projection into a
+        // scratch area, then one amax / 448 scale and the codes per (chunk,
+        // layer, K|V) tensor
+        for (int64_t g0 = 0; g0 < B; g0 += kCrossGroup) {
+            const int64_t gB = std::min<int64_t>(kCrossGroup, B - g0);
+            Lin L;
+            L.a = reinterpret_cast<const __nv_bfloat16*>(enc) + g0 * kCtx * d;
+            L.rows = gB * kCtx; L.lda = d; L.w = m->W("dec.0.ck.w"); L.N = (int64_t)Ld * 2 * d; L.K = d;
+            GemmEpi ep = epi_out(dec->ckv_tmp, 0, OUT_BF16, m->V("dec.0.ck.b"));
+            ep.mode = MODE_CROSS_KV;
+            ep.ckv_d = d;
+            ep.ckv_heads = H;
+            ep.ckv_chunks = gB;
+            if (wb_status st = linear(m, L, ep, s)) return fail_free(st);
+            if (wb_status st = cross_kv_quant(dec->ckv_tmp, gB, B, g0, Ld, (int64_t)H * kCtx * 64,
+                                              reinterpret_cast<uint8_t*>(dec->crosskv), dec->cscale, s))
+                return fail_free(st);
+        }
     }
     *out = dec;
     return WB_OK;
