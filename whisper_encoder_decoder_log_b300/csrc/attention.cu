@@ -5,12 +5,14 @@
 //
 //  * The bf16 encoder self-attention runs on tcgen05 (flash_tc.cu).
 //  * attn_rows_kernel: one CTA per (chunk, head, group of up to 4 query rows)
-//    streams the chunk's keys with 16-byte loads (8 lanes per bf16/fp32 key
-//    row, 4 lanes per E4M3 row), keeps the scores in shared memory, and
-//    reduces p . V across the CTA.  It serves the fp32 model's encoder, the
-//    decoder's cross-attention over the precomputed bf16 K/V, and the decoder's
-//    causal self-attention over the (E4M3 or fp32) KV cache, where query row
-//    p of a chunk sees cache rows 0..p.
+//    streams the chunk's keys with 16-byte loads (8 lanes per key row),
+//    keeps the scores in shared memory, and reduces p . V across the CTA.  It
+//    serves the fp32 model's encoder, the decoder's cross-attention over the
+//    precomputed bf16 K/V, and the prefix pass's causal self-attention over
+//    the (E4M3 or fp32) KV cache, where query row p sees cache rows 0..p.
+//  * self_attn_step_kernel: one warp per (chunk, head) for a decode step over
+//    E4M3 rows -- the causal self-attention (appending the token's own K/V
+//    row) and the cross-attention over E4M3 cross K/V.
 #include <type_traits>
 
 #include "attn.cuh"
@@ -231,124 +233,6 @@ attn_rows_kernel(const TQ* __restrict__ q, int64_t q_ld, int rows_per_chunk, int
     }
 }
 
-// Decode-step self-attention over the E4M3 cache: one CTA of 8 warps per
-// (chunk, head), one query row at the step's position, keys 0..pos.  Warp w
-// takes the 8-row passes w, w+8, ...; lane (r, sub) with r = lane / 4 and
-// sub = lane % 4 owns codes sub*16 .. sub*16+15 of row r of a pass.  K and V
-// of a pass are loaded together, scores are reduced over the 4 lanes of a
-// row, and each warp keeps an online softmax (running max, sum, output); the
-// 8 partial results are merged through shared memory at the end.
-template <typename TO>
-__global__ void __launch_bounds__(256)
-self_attn_e4m3_kernel(const float* __restrict__ q, int64_t q_ld, int heads, KVView kv, int q_pos_host,
-                      TO* __restrict__ out, int64_t o_ld, int64_t o_split) {
-    griddep_wait();
-    griddep_launch();
-    __shared__ float s_o[8][64];
-    __shared__ float s_m[8], s_l[8];
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int h = blockIdx.x;
-    const int64_t chunk = blockIdx.y;
-    const int pos = kv.pos_dev ? *kv.pos_dev : q_pos_host;
-    if (kv.active_len && kv.active_len[chunk] <= pos + 1) return;   // finished chunk (uniform per CTA)
-    const int nk = pos + 1;
-    const int r = lane >> 2, sub = lane & 3;
-    const int64_t cb = kv.chunk_off ? kv.chunk_off[chunk] : chunk * kv.chunk_stride;
-    const int64_t hs = kv.head_stride * (kv.chunk_len ? (int64_t)kv.chunk_len[chunk] : 1);
-    const uint8_t* Kp = reinterpret_cast<const uint8_t*>(kv.ptr) + cb + ((int64_t)kv.k_blk * kv.heads + h) * hs;
-    const uint8_t* Vp = reinterpret_cast<const uint8_t*>(kv.ptr) + cb + ((int64_t)kv.v_blk * kv.heads + h) * hs;
-    const float ks = kv.k_scale ? kv.k_scale[chunk] : 1.f;
-    const float vs = kv.v_scale ? kv.v_scale[chunk] : 1.f;
-    float qv[16];
-    {
-        const float* qr = q + chunk * q_ld + h * 64 + sub * 16;
-#pragma unroll
-        for (int i = 0; i < 16; i += 4) {
-            const float4 t = *reinterpret_cast<const float4*>(qr + i);
-            // fold the 1/sqrt(64) and the K scale into q
-            qv[i] = t.x * 0.125f * ks; qv[i + 1] = t.y * 0.125f * ks; qv[i + 2] = t.z * 0.125f * ks; qv[i + 3] = t.w * 0.125f * ks;
-        }
-    }
-    float m = -INFINITY, l = 0.f, o[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) o[i] = 0.f;
-    for (int j0 = warp * 8; j0 < nk; j0 += 64) {
-        const int j = j0 + r;
-        const bool valid = j < nk;
-        uint4 kr = make_uint4(0, 0, 0, 0), vr = make_uint4(0, 0, 0, 0);
-        if (valid) {
-            kr = ld_stream(Kp + (int64_t)j * 64 + sub * 16);
-            vr = ld_stream(Vp + (int64_t)j * 64 + sub * 16);
-        }
-        float kf[16], vf[16];
-        {
-            const uint32_t w[4] = {kr.x, kr.y, kr.z, kr.w};
-            const uint32_t u[4] = {vr.x, vr.y, vr.z, vr.w};
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                __nv_fp8x4_e4m3 a, b;
-                a.__x = w[i];
-                b.__x = u[i];
-                const float4 fa = static_cast<float4>(a), fb = static_cast<float4>(b);
-                kf[4 * i] = fa.x; kf[4 * i + 1] = fa.y; kf[4 * i + 2] = fa.z; kf[4 * i + 3] = fa.w;
-                vf[4 * i] = fb.x; vf[4 * i + 1] = fb.y; vf[4 * i + 2] = fb.z; vf[4 * i + 3] = fb.w;
-            }
-        }
-        float sc = 0.f;
-#pragma unroll
-        for (int i = 0; i < 16; ++i) sc = fmaf(qv[i], kf[i], sc);
-        sc += __shfl_xor_sync(0xffffffffu, sc, 1);
-        sc += __shfl_xor_sync(0xffffffffu, sc, 2);
-        if (!valid) sc = -INFINITY;
-        float pm = sc;   // max over the 8 rows of the pass (lane bits 2-4)
-        pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 4));
-        pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 8));
-        pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 16));
-        const float mn = fmaxf(m, pm);
-        const float alpha = __expf(m - mn);        // 0 on a warp's first pass (m = -inf)
-        const float p = valid ? __expf(sc - mn) : 0.f;
-        float ps = p;                              // sum over the 8 rows
-        ps += __shfl_xor_sync(0xffffffffu, ps, 4);
-        ps += __shfl_xor_sync(0xffffffffu, ps, 8);
-        ps += __shfl_xor_sync(0xffffffffu, ps, 16);
-        l = l * alpha + ps;
-        m = mn;
-#pragma unroll
-        for (int i = 0; i < 16; ++i) o[i] = fmaf(p, vf[i], o[i] * alpha);
-    }
-    // sum each warp's 8 row groups, then merge the 8 warps
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-        o[i] += __shfl_xor_sync(0xffffffffu, o[i], 4);
-        o[i] += __shfl_xor_sync(0xffffffffu, o[i], 8);
-        o[i] += __shfl_xor_sync(0xffffffffu, o[i], 16);
-    }
-    if (r == 0) {
-#pragma unroll
-        for (int i = 0; i < 16; ++i) s_o[warp][sub * 16 + i] = o[i];
-    }
-    if (lane == 0) { s_m[warp] = m; s_l[warp] = l; }
-    __syncthreads();
-    if (threadIdx.x < 64) {
-        float M = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < 8; ++w) M = fmaxf(M, s_m[w]);
-        float num = 0.f, den = 0.f;
-#pragma unroll
-        for (int w = 0; w < 8; ++w) {
-            if (s_m[w] == -INFINITY) continue;     // a warp that saw no rows
-            const float e = __expf(s_m[w] - M);
-            num = fmaf(e, s_o[w][threadIdx.x], num);
-            den = fmaf(e, s_l[w], den);
-        }
-        const float a = num / den * vs;
-        TO* orow = out + chunk * o_ld + h * 64;
-        const TO hi = (TO)a;
-        orow[threadIdx.x] = hi;
-        if (o_split) orow[o_split + threadIdx.x] = (TO)(a - (float)hi);
-    }
-}
-
 // Decode step, causal self-attention over the E4M3 cache, with the cache
 // append of the current token fused in.  One warp per (chunk, head), kStepHeads
 // heads per CTA.  Lane = (row r of 8, sub s of 4): a pass covers 8 cache rows
@@ -406,7 +290,9 @@ WB_DEV uint4 quant16(const float* x, float inv) {
     return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
-template <typename TO>
+// CROSS: the same stream over a chunk's 1500 precomputed E4M3 cross K/V rows
+// (q is the cross-attention query row, nothing is appended).
+template <typename TO, bool CROSS>
 __global__ void __launch_bounds__(32 * kStepHeads, 6)
 self_attn_step_kernel(const float* __restrict__ qkv, int64_t q_ld, int heads, KVView kv, int q_pos_host,
                       TO* __restrict__ out, int64_t o_ld, int64_t o_split) {
@@ -419,20 +305,23 @@ self_attn_step_kernel(const float* __restrict__ qkv, int64_t q_ld, int heads, KV
     if (h >= heads) return;
     const int pos = kv.pos_dev ? *kv.pos_dev : q_pos_host;
     if (kv.active_len && kv.active_len[chunk] <= pos + 1) return;   // finished chunk
-    const int L = kv.chunk_len[chunk];
-    if (pos >= L) return;                                          // no cache row for this position
+    const int L = CROSS ? kCtx : kv.chunk_len[chunk];
+    if (!CROSS && pos >= L) return;                                // no cache row for this position
     const int r = lane >> 2, sub = lane & 3;
     const int d = heads * 64;
-    const int64_t hs = kv.head_stride * (int64_t)L;
-    uint8_t* base = const_cast<uint8_t*>(reinterpret_cast<const uint8_t*>(kv.ptr)) + kv.chunk_off[chunk];
+    const int64_t hs = kv.head_stride * (CROSS ? 1 : (int64_t)L);
+    uint8_t* base = const_cast<uint8_t*>(reinterpret_cast<const uint8_t*>(kv.ptr)) +
+                    (CROSS ? chunk * kv.chunk_stride : kv.chunk_off[chunk]);
     uint8_t* Kp = base + ((int64_t)kv.k_blk * kv.heads + h) * hs;
     uint8_t* Vp = base + ((int64_t)kv.v_blk * kv.heads + h) * hs;
-    const int npass = (pos + 8) >> 3;                              // passes over rows 0..pos
+    const int nk = CROSS ? kCtx : pos + 1;                         // rows attended
+    const int nmem = CROSS ? kCtx : pos;                           // rows read from memory
+    const int npass = (nk + 7) >> 3;
     uint4 (*rg)[2][32] = ring[warp];
     // rows below pos stream in while the current row is quantised
     auto issue = [&](int pass) {
         const int j = pass * 8 + r;
-        if (pass < npass && j < pos) {
+        if (pass < npass && j < nmem) {
             const int st = pass % kStepDepth;
             cp_async16(&rg[st][0][lane], Kp + (int64_t)j * 64 + sub * 16);
             cp_async16(&rg[st][1][lane], Vp + (int64_t)j * 64 + sub * 16);
@@ -444,11 +333,14 @@ self_attn_step_kernel(const float* __restrict__ qkv, int64_t q_ld, int heads, KV
     const float ks = kv.k_scale[chunk], vs = kv.v_scale[chunk];
     const float* qr = qkv + chunk * q_ld + h * 64 + sub * 16;
     // the current token's cache rows, quantised as the append kernel does
-    const uint4 kcur = quant16(qr + d, 1.0f / ks);
-    const uint4 vcur = quant16(qr + 2 * d, 1.0f / vs);
-    if (r == 0) {
-        *reinterpret_cast<uint4*>(Kp + (int64_t)pos * 64 + sub * 16) = kcur;
-        *reinterpret_cast<uint4*>(Vp + (int64_t)pos * 64 + sub * 16) = vcur;
+    uint4 kcur = make_uint4(0, 0, 0, 0), vcur = kcur;
+    if (!CROSS) {
+        kcur = quant16(qr + d, 1.0f / ks);
+        vcur = quant16(qr + 2 * d, 1.0f / vs);
+        if (r == 0) {
+            *reinterpret_cast<uint4*>(Kp + (int64_t)pos * 64 + sub * 16) = kcur;
+            *reinterpret_cast<uint4*>(Vp + (int64_t)pos * 64 + sub * 16) = vcur;
+        }
     }
     float qv[16];
 #pragma unroll
@@ -465,9 +357,9 @@ self_attn_step_kernel(const float* __restrict__ qkv, int64_t q_ld, int heads, KV
         const int j = pass * 8 + r;
         const int st = pass % kStepDepth;
         uint4 kr = make_uint4(0, 0, 0, 0), vr = kr;
-        if (j < pos) { kr = rg[st][0][lane]; vr = rg[st][1][lane]; }
-        else if (j == pos) { kr = kcur; vr = vcur; }
-        const bool valid = j <= pos;
+        if (j < nmem) { kr = rg[st][0][lane]; vr = rg[st][1][lane]; }
+        else if (!CROSS && j == pos) { kr = kcur; vr = vcur; }
+        const bool valid = j < nk;
         float sc = dot16_e4m3(qv, kr);
         sc += __shfl_xor_sync(0xffffffffu, sc, 1);
         sc += __shfl_xor_sync(0xffffffffu, sc, 2);
@@ -543,13 +435,18 @@ template <typename TQ, typename TKV, typename TO>
 wb_status launch_rows(const void* q, int64_t q_ld, int64_t n_chunks, int rows_per_chunk, int heads,
                       const KVView& kv, int kv_len, bool causal, int q_pos0, void* out, int64_t o_ld,
                       cudaStream_t s, int64_t o_split) {
-    if (causal && rows_per_chunk == 1 && std::is_same<TKV, uint8_t>::value && std::is_same<TQ, float>::value &&
-        (q_ld % 4) == 0) {
-        dim3 grid((unsigned)heads, (unsigned)n_chunks);
-        const int slot = prof_begin(WB_KERNEL_SELF_ATTN, s);
-        WB_CUDA(launch_k(self_attn_e4m3_kernel<TO>, dim3(grid), dim3(256), 0, s, reinterpret_cast<const float*>(q), q_ld, heads, kv,
-                                                             q_pos0, reinterpret_cast<TO*>(out), o_ld, o_split));
-        prof_end(slot, s, (double)n_chunks * heads * (2.0 * (q_pos0 + 1) * 64.0 + 64.0 * (4 + sizeof(TO))));
+    if (!causal && rows_per_chunk == 1 && kv_len == kCtx && std::is_same<TKV, uint8_t>::value &&
+        std::is_same<TQ, float>::value && std::is_same<TO, __nv_bfloat16>::value && (q_ld % 4) == 0 &&
+        kv.k_scale && kv.v_scale && !kv.chunk_off && kv.head_stride == (int64_t)kCtx * 64 && kv.row_stride == 64 &&
+        aligned16(q) && aligned16(kv.ptr) && (kv.chunk_stride % 16) == 0) {
+        // decode step over E4M3 cross K/V: one warp per (chunk, head), cp.async ring
+        if (n_chunks > 0x7FFFFFFF || heads > 65535 * kStepHeads) return fail(WB_ERR_SHAPE, "attention grid too large");
+        const dim3 grid((unsigned)n_chunks, (unsigned)((heads + kStepHeads - 1) / kStepHeads));
+        const int slot = prof_begin(WB_KERNEL_CROSS_ATTN, s);
+        WB_CUDA(launch_k(self_attn_step_kernel<__nv_bfloat16, true>, grid, dim3(32 * kStepHeads), 0, s,
+                         reinterpret_cast<const float*>(q), q_ld, heads, kv, q_pos0,
+                         reinterpret_cast<__nv_bfloat16*>(out), o_ld, o_split));
+        prof_end(slot, s, (double)n_chunks * heads * (2.0 * kCtx * 64.0 + 64.0 * (4 + 2)));
         WB_CUDA(cudaGetLastError());
         return WB_OK;
     }
@@ -571,8 +468,8 @@ wb_status attn_self_step_e4m3(const float* qkv, int64_t q_ld, int64_t n_chunks, 
     if (n_chunks > 0x7FFFFFFF || heads > 65535 * kStepHeads) return fail(WB_ERR_SHAPE, "attention grid too large");
     const dim3 grid((unsigned)n_chunks, (unsigned)((heads + kStepHeads - 1) / kStepHeads));
     const int slot = prof_begin(WB_KERNEL_SELF_ATTN, s);
-    WB_CUDA(launch_k(self_attn_step_kernel<__nv_bfloat16>, grid, dim3(32 * kStepHeads), 0, s, qkv, q_ld, heads, kv,
-                     q_pos, reinterpret_cast<__nv_bfloat16*>(out), o_ld, o_split));
+    WB_CUDA(launch_k(self_attn_step_kernel<__nv_bfloat16, false>, grid, dim3(32 * kStepHeads), 0, s, qkv, q_ld, heads,
+                     kv, q_pos, reinterpret_cast<__nv_bfloat16*>(out), o_ld, o_split));
     prof_end(slot, s, (double)n_chunks * heads * (2.0 * q_pos * 64.0 + 2.0 * 64.0 * (4 + 1) + 64.0 * (4 + 2)));
     WB_CUDA(cudaGetLastError());
     return WB_OK;
