@@ -16,7 +16,8 @@ small batch, so a capture holds well under a few GB of device memory.
   decode8 large-v3 decoder layers in mixed_fp8 (4 of the 32) over --chunks
           chunks (default 512): prefix + --steps greedy steps through the
           captured step graphs, the launch pattern of the serving batch's
-          decode; the encoder states are random
+          decode; the encoder states are random; --kv 2 stores the cross
+          K/V in E4M3 as well
   flash   encoder self-attention over 16 chunks x 20 heads
 """
 from __future__ import annotations
@@ -43,6 +44,7 @@ def main():
     ap.add_argument("--iters", type=int, default=3)
     ap.add_argument("--chunks", type=int, default=512)
     ap.add_argument("--steps", type=int, default=8)
+    ap.add_argument("--kv", type=int, default=1, choices=[1, 2])
     a = ap.parse_args()
     dev = "cuda"
     if a.case == "mel":
@@ -72,7 +74,7 @@ def main():
                 wb.wb_gemm(qa.view(M, K), qb.view(N, K), C, row_scale=rs, col_scale=cs)
     elif a.case == "decode8":
         dims = synth.ModelDims("large-v3-dec4", 128, 1280, 20, 5120, 1, 4, 51866)
-        desc = wb.make_desc(dims, wb.PREC_MIXED_FP8, True)
+        desc = wb.make_desc(dims, wb.PREC_MIXED_FP8, a.kv)
         buf = wb.pack_weights(desc, synth.make_weights(dims, 0, bf16=True))
         torch.cuda.synchronize()
         model = wb.wb_model_create(desc, buf)
