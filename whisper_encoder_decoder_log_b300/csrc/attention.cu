@@ -253,7 +253,7 @@ WB_DEV void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memor
 template <int N>
 WB_DEV void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
-// dot(q[0..15], E4M3 codes w) and o = o * alpha + p * E4M3 codes v
+// dot(q[0..15], E4M3 codes w) and o += p * E4M3 codes v
 WB_DEV float dot16_e4m3(const float (&q)[16], const uint4& w) {
     const uint32_t u[4] = {w.x, w.y, w.z, w.w};
     float s = 0.f;
@@ -267,15 +267,15 @@ WB_DEV float dot16_e4m3(const float (&q)[16], const uint4& w) {
     }
     return s;
 }
-WB_DEV void axpy16_e4m3(float (&o)[16], float alpha, float p, const uint4& w) {
+WB_DEV void axpy16_e4m3(float (&o)[16], float p, const uint4& w) {
     const uint32_t u[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         __nv_fp8x4_e4m3 a;
         a.__x = u[i];
         const float4 f = static_cast<float4>(a);
-        o[4 * i] = fmaf(p, f.x, o[4 * i] * alpha); o[4 * i + 1] = fmaf(p, f.y, o[4 * i + 1] * alpha);
-        o[4 * i + 2] = fmaf(p, f.z, o[4 * i + 2] * alpha); o[4 * i + 3] = fmaf(p, f.w, o[4 * i + 3] * alpha);
+        o[4 * i] = fmaf(p, f.x, o[4 * i]); o[4 * i + 1] = fmaf(p, f.y, o[4 * i + 1]);
+        o[4 * i + 2] = fmaf(p, f.z, o[4 * i + 2]); o[4 * i + 3] = fmaf(p, f.w, o[4 * i + 3]);
     }
 }
 
@@ -368,16 +368,24 @@ self_attn_step_kernel(const float* __restrict__ qkv, int64_t q_ld, int heads, KV
         pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 4));
         pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 8));
         pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 16));
-        const float mn = fmaxf(m, pm);
-        const float alpha = __expf(m - mn);     // 0 on the first pass (m = -inf)
-        const float pr = valid ? __expf(sc - mn) : 0.f;
+        // the running maximum is raised only when a pass exceeds it by more
+        // than 8 (natural log): otherwise p <= e^8 and o, l keep their scale,
+        // which saves the per-pass correction multiply (pm and m are the same
+        // in every lane, so the branch is warp-uniform)
+        if (pm > m + 8.f) {
+            const float alpha = __expf(m - pm);   // 0 on the first pass (m = -inf)
+            l *= alpha;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) o[i] *= alpha;
+            m = pm;
+        }
+        const float pr = valid ? __expf(sc - m) : 0.f;
         float ps = pr;
         ps += __shfl_xor_sync(0xffffffffu, ps, 4);
         ps += __shfl_xor_sync(0xffffffffu, ps, 8);
         ps += __shfl_xor_sync(0xffffffffu, ps, 16);
-        l = l * alpha + ps;
-        m = mn;
-        axpy16_e4m3(o, alpha, pr, vr);
+        l += ps;
+        axpy16_e4m3(o, pr, vr);
         issue(pass + kStepDepth);                                  // refill the stage just consumed
     }
     cp_async_wait<0>();
