@@ -195,7 +195,10 @@ WB_API size_t wb_decoder_workspace_size(const wb_model* model, int64_t B,
  * Set up a decoder over B chunks: computes cross-attention K and V of every
  * decoder layer from enc ([dev] [B, 1500, d], wb_encode's output) into the
  * workspace ("whisper-blaze 0.1.8", "Direct Kernel API", decoder_cross_attn:
- * K/V come from the encoder and are computed once per chunk).
+ * K/V come from the encoder and are computed once per chunk).  With
+ * kv_fp8 = WB_KV_FP8_CROSS they are computed 32 chunks at a time into a bf16
+ * scratch area of the workspace and stored as E4M3 with one scale per
+ * (chunk, layer, K|V); wb_decoder_workspace_size includes that scratch.
  *   tokens [dev] int32 [B, 448]  token matrix the decoder reads and writes
  *     (kept by reference).  Row c receives chunk c's tokens, position p in
  *     column p.
