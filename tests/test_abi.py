@@ -113,3 +113,17 @@ def test_host_side_argument_checks_need_no_gpu():
     assert L.wb_gemm(16, 16, 1, 8, 63, 0, None, None, None, 0, 16, 0, None) == -2
     assert L.wb_decode_step(None, 1, None, None) == -1
     assert L.wb_weights_bytes(ctypes.byref(bad)) == 0
+
+
+def test_kv_modes_are_validated_on_the_host():
+    L = wb.lib()
+    from synth import TURBO
+    for prec, kv, ok in [(wb.PREC_BF16, wb.KV_NONE, True), (wb.PREC_BF16, wb.KV_FP8_SELF, True),
+                         (wb.PREC_MIXED_FP8, wb.KV_FP8_CROSS, True), (wb.PREC_FP32, wb.KV_FP8_CROSS, False),
+                         (wb.PREC_BF16, 3, False), (wb.PREC_BF16, -1, False)]:
+        desc = wb.make_desc(TURBO, prec, kv)
+        assert (L.wb_weights_bytes(ctypes.byref(desc)) > 0) == ok, (prec, kv)
+    # the E4M3 cross K/V do not change the weight layout
+    a = L.wb_weights_bytes(ctypes.byref(wb.make_desc(TURBO, wb.PREC_MIXED_FP8, wb.KV_FP8_SELF)))
+    b = L.wb_weights_bytes(ctypes.byref(wb.make_desc(TURBO, wb.PREC_MIXED_FP8, wb.KV_FP8_CROSS)))
+    assert a == b
