@@ -27,9 +27,17 @@ Readings taken where the pages are silent or contradict one another:
     final LayerNorm precedes it; the encoder ends with its own LayerNorm;
   * greedy choice = lowest index among the maximal logits; no token is
     suppressed and decoding runs to the requested length (no end token);
-  * FP8 GEMMs (``mixed_fp8``): weights get one scale per weight matrix, each
-    activation row (one token) gets its own scale, both amax / 448; the
-    product of scales multiplies the exact product of the decoded codes;
+  * FP8 GEMMs (``mixed_fp8``): every E4M3 operand is a tensor with one scale
+    amax / 448 ([WB] "Direct Kernel API": ``quantise_e4m3(x) -> (fp8,
+    scale)``, one scale per call).  Weights: one scale per weight matrix.
+    Activations: one scale per (chunk, GEMM input) -- in the encoder the
+    1500 x K input one chunk feeds a GEMM; in the decoder the one-token input
+    a decode step feeds per chunk, so a teacher-forced pass quantises each
+    position as its own step would (the forced prefix counts as one step per
+    token) and incremental decoding equals the full pass.  Scales are per
+    chunk, never per batch, so a chunk's result does not depend on what it is
+    batched with.  The product of the two scales multiplies the exact product
+    of the decoded codes;
   * FP8 self-attention cache: one scale per (layer, K or V) of each chunk,
     taken from the forced-prefix rows (oracle.e4m3.kv_scale_of); attention
     reads the dequantised cache, the current token's own row included;
@@ -77,12 +85,20 @@ def sinusoids(n_ctx: int, d: int) -> np.ndarray:
 # ------------------------------------------------------------------ GEMM forms
 
 class Linear:
-    """y = x W^T + b, optionally through E4M3 codes (``mixed_fp8``)."""
+    """y = x W^T + b, optionally through E4M3 codes (``mixed_fp8``).
 
-    def __init__(self, w, b, fp8: bool = False):
+    ``act_scale`` says what one activation scale covers: ``"tensor"`` -- the
+    whole input x (the encoder calls this once per chunk), ``"row"`` -- each
+    row of x on its own (a decoder row is one decode step's input).
+    """
+
+    def __init__(self, w, b, fp8: bool = False, act_scale: str = "row"):
+        if act_scale not in ("row", "tensor"):
+            raise ValueError(act_scale)
         self.w = np.asarray(w, dtype=np.float64)
         self.b = np.asarray(b, dtype=np.float64)
         self.fp8 = fp8
+        self.act_scale = act_scale
         if fp8:
             codes, s = e4m3.quantise_tensor(np.asarray(w, np.float32))
             self.w_codes, self.w_scale = codes, s
@@ -92,10 +108,13 @@ class Linear:
         x = np.asarray(x, dtype=np.float64)
         if not self.fp8:
             return x @ self.w.T + self.b
-        # every row (token) is quantised with its own scale amax / 448
         x32 = x.astype(np.float32).reshape(-1, x.shape[-1])
-        amax = np.max(np.abs(x32), axis=-1)
-        s_x = np.array([e4m3.scale_of(a) for a in amax], dtype=np.float32)
+        if self.act_scale == "tensor":   # one scale amax / 448 over the whole input
+            s_t = e4m3.scale_of(float(np.max(np.abs(x32))) if x32.size else 0.0)
+            s_x = np.full(x32.shape[0], s_t, dtype=np.float32)
+        else:                            # every row (one step's token) has its own
+            amax = np.max(np.abs(x32), axis=-1)
+            s_x = np.array([e4m3.scale_of(a) for a in amax], dtype=np.float32)
         inv = (np.float32(1.0) / s_x).astype(np.float32)
         qx = e4m3.decode(e4m3.encode((x32 * inv[:, None]).astype(np.float32)))
         acc = qx @ self.w_deq.T
@@ -161,15 +180,18 @@ def conv_stem(mel, W):
 
 
 def encoder_layer(h, W, l: int, n_heads: int, fp8: bool = False):
+    """One pre-LN layer over one chunk's [1500, d] states; under ``mixed_fp8``
+    each E4M3 GEMM input (LN1 output, LN2 output, GELU output) is one tensor
+    with one scale."""
     p = f"enc.{l}."
     a = layer_norm(h, W[p + "ln1.g"], W[p + "ln1.b"])
-    q = Linear(W[p + "q.w"], W[p + "q.b"], fp8)(a)
-    k = Linear(W[p + "k.w"], W[p + "k.b"], fp8)(a)
-    v = Linear(W[p + "v.w"], W[p + "v.b"], fp8)(a)
+    q = Linear(W[p + "q.w"], W[p + "q.b"], fp8, "tensor")(a)
+    k = Linear(W[p + "k.w"], W[p + "k.b"], fp8, "tensor")(a)
+    v = Linear(W[p + "v.w"], W[p + "v.b"], fp8, "tensor")(a)
     h = h + Linear(W[p + "o.w"], W[p + "o.b"])(multi_head(q, k, v, n_heads))
     a = layer_norm(h, W[p + "ln2.g"], W[p + "ln2.b"])
-    f = gelu(Linear(W[p + "fc1.w"], W[p + "fc1.b"], fp8)(a))
-    return h + Linear(W[p + "fc2.w"], W[p + "fc2.b"], fp8)(f)
+    f = gelu(Linear(W[p + "fc1.w"], W[p + "fc1.b"], fp8, "tensor")(a))
+    return h + Linear(W[p + "fc2.w"], W[p + "fc2.b"], fp8, "tensor")(f)
 
 
 def encode(mel, W, dims, fp8: bool = False, layers=None):

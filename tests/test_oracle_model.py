@@ -246,6 +246,61 @@ def test_fp8_row_scales_are_independent():
         np.testing.assert_allclose(lin(x[i:i + 1])[0], full[i], rtol=1e-13, atol=1e-15)
 
 
+def test_fp8_tensor_scale_is_one_amax_over_all_rows():
+    """One scale amax / 448 over the whole input: inputs on that grid pass
+    through E4M3 losslessly, while per-row scales (finer grids on the small
+    rows) would round them."""
+    rng = np.random.default_rng(12)
+    vals = e4m3.decode_table()[1:0x7F]
+    w = rng.choice(vals, size=(8, 32)) * rng.choice([-1, 1], size=(8, 32))
+    s = 0.125                                  # the tensor's scale: amax = 448 s
+    x = rng.choice(vals[:40], size=(6, 32)) * s  # small rows: codes of at most 0.3 ...
+    x[2, 5] = 448.0 * s                          # ... and one element that sets amax
+    x = x.astype(np.float32).astype(np.float64)
+    lin_t = model.Linear(w, np.zeros(8), fp8=True, act_scale="tensor")
+    s32 = e4m3.scale_of(448.0 * np.float32(s))
+    exact = (x.astype(np.float32) * (np.float32(1) / s32)).astype(np.float64)
+    assert np.array_equal(e4m3.decode(e4m3.encode(exact)), exact)      # on the tensor grid
+    np.testing.assert_allclose(lin_t(x), (exact * np.float64(s32)) @ w.T, rtol=1e-14)
+    lin_r = model.Linear(w, np.zeros(8), fp8=True, act_scale="row")
+    assert np.abs(lin_r(x) - lin_t(x)).max() > 1e-6 * np.abs(lin_t(x)).max()
+
+
+def test_fp8_tensor_scale_couples_rows_and_scales_by_powers_of_two():
+    rng = np.random.default_rng(13)
+    w = rng.normal(size=(8, 16)) * 0.1
+    x = rng.normal(size=(5, 16))
+    lin = model.Linear(w, np.zeros(8), fp8=True, act_scale="tensor")
+    base = lin(x)
+    # a power of two moves amax, the scale and every product by the same
+    # factor: the codes do not change, the result scales exactly
+    np.testing.assert_array_equal(lin(x * 8.0), base * 8.0)
+    np.testing.assert_array_equal(lin(x / 4.0), base / 4.0)
+    # permuting rows permutes the result (the scale is a function of the set)
+    perm = rng.permutation(5)
+    np.testing.assert_allclose(lin(x[perm]), base[perm], rtol=1e-13, atol=1e-15)
+    # raising one row's amax re-grids every other row; per-row scales would not
+    y = x.copy()
+    y[0] *= 10.0
+    assert np.abs(lin(y)[1:] - base[1:]).max() > 0
+    lin_r = model.Linear(w, np.zeros(8), fp8=True, act_scale="row")
+    np.testing.assert_allclose(lin_r(y)[1:], lin_r(x)[1:], rtol=1e-13, atol=1e-15)
+    # equal row amax: per-tensor and per-row scales coincide
+    z = x / np.abs(x).max(axis=1, keepdims=True)
+    np.testing.assert_allclose(lin(z), lin_r(z), rtol=1e-13, atol=1e-15)
+
+
+def test_fp8_encoder_layer_permutation_equivariant():
+    """A per-chunk tensor scale keeps the encoder layer (no positions) equivariant
+    under a permutation of positions."""
+    W = make_weights(MINI, 14, bf16=False)
+    h = np.random.default_rng(15).normal(size=(24, MINI.d_model))
+    perm = np.random.default_rng(16).permutation(24)
+    a = model.encoder_layer(h, W, 0, MINI.n_heads, fp8=True)
+    b = model.encoder_layer(h[perm], W, 0, MINI.n_heads, fp8=True)
+    np.testing.assert_allclose(b, a[perm], rtol=1e-11, atol=1e-11)
+
+
 def test_greedy_lowest_index_on_ties():
     logits = np.array([[0.0, 3.0, 3.0, 1.0], [5.0, 5.0, 5.0, 5.0]])
     assert list(model.greedy(logits)) == [1, 0]
