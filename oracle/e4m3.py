@@ -70,6 +70,23 @@ def encode(x) -> np.ndarray:
     return code
 
 
+def round_values(x) -> np.ndarray:
+    """E4M3 rounding as values: the same result as decode(encode(x)) for
+    finite x, written as rounding onto the format's grid.  Inside binade
+    [2^e, 2^(e+1)) E4M3 has 8 values 2^(e-3) apart (e >= -6; below 2^-6 the
+    subnormals keep the spacing 2^-9), so the nearest value is rint(|x| /
+    2^(e-3)) * 2^(e-3), rint rounding ties to even, which is the even code
+    (the code's last bit is the last mantissa bit); magnitudes above 448 take
+    448 (satfinite); the sign is kept."""
+    x = np.asarray(x, dtype=np.float64)
+    mag = np.abs(x)
+    _, ex = np.frexp(mag)                      # mag = f 2^ex, f in [0.5, 1)
+    e = np.maximum(ex - 1, -6)
+    step = np.ldexp(1.0, e - 3)
+    q = np.minimum(np.rint(mag / step) * step, E4M3_MAX)
+    return np.copysign(q, x)
+
+
 def scale_of(amax: float) -> np.float32:
     """Per-tensor scale of a weight or GEMM activation: amax / 448 in fp32.
 

@@ -51,6 +51,7 @@ Readings taken where the pages are silent or contradict one another:
 from __future__ import annotations
 
 import math
+import weakref
 
 import numpy as np
 from scipy.special import erf
@@ -84,6 +85,28 @@ def sinusoids(n_ctx: int, d: int) -> np.ndarray:
 
 # ------------------------------------------------------------------ GEMM forms
 
+_W8_CACHE = {}
+
+
+def _fp8_weight(w):
+    """(scale, fp32 products w * fp32(1/scale), their E4M3 values) of one weight
+    matrix, one scale amax / 448 over it; memoised per array object (the
+    weights of a model are quantised once, as a deployed model would be)."""
+    key = id(w)
+    hit = _W8_CACHE.get(key)
+    if hit is not None and hit[0]() is w:
+        return hit[1]
+    w32 = np.asarray(w, np.float32)
+    s = e4m3.scale_of(float(np.max(np.abs(w32))) if w32.size else 0.0)
+    q = (w32 * np.float32(np.float32(1.0) / s)).astype(np.float32)
+    res = (s, q, e4m3.round_values(q))
+    try:
+        _W8_CACHE[key] = (weakref.ref(w), res)
+    except TypeError:          # not weak-referenceable (a list): no memo
+        pass
+    return res
+
+
 class Linear:
     """y = x W^T + b, optionally through E4M3 codes (``mixed_fp8``).
 
@@ -100,9 +123,12 @@ class Linear:
         self.fp8 = fp8
         self.act_scale = act_scale
         if fp8:
-            codes, s = e4m3.quantise_tensor(np.asarray(w, np.float32))
-            self.w_codes, self.w_scale = codes, s
-            self.w_deq = e4m3.decode(codes)
+            self.w_scale, self._w_q, self.w_deq = _fp8_weight(w)
+
+    @property
+    def w_codes(self):
+        """E4M3 codes of the weights (the values w_deq holds)."""
+        return e4m3.encode(self._w_q)
 
     def __call__(self, x):
         x = np.asarray(x, dtype=np.float64)
@@ -116,7 +142,7 @@ class Linear:
             amax = np.max(np.abs(x32), axis=-1)
             s_x = np.array([e4m3.scale_of(a) for a in amax], dtype=np.float32)
         inv = (np.float32(1.0) / s_x).astype(np.float32)
-        qx = e4m3.decode(e4m3.encode((x32 * inv[:, None]).astype(np.float32)))
+        qx = e4m3.round_values((x32 * inv[:, None]).astype(np.float32))
         acc = qx @ self.w_deq.T
         out = acc * (s_x.astype(np.float64)[:, None] * np.float64(self.w_scale))
         return out.reshape(x.shape[:-1] + (self.w.shape[0],)) + self.b

@@ -74,3 +74,19 @@ def test_quantise_is_one_fp32_product(s):
     inv = np.float32(1) / s
     ref = torch.from_numpy(np.clip(x * inv, -448, 448)).to(torch.float8_e4m3fn)
     assert np.array_equal(e4m3.quantise(x, s), ref.view(torch.uint8).numpy())
+
+
+def test_grid_rounding_equals_code_rounding():
+    """round_values (rounding onto the 2^(e-3) grid) is the same map as
+    decode(encode(x)) (nearest of the 253 finite values, ties to the even
+    code): on every value, every tie between neighbours, just either side of
+    each tie, past the top, and over random magnitudes 2^-14 .. 2^10."""
+    vals = e4m3.decode_table()[:0x7F]
+    mids = (vals[:-1] + vals[1:]) / 2
+    near = np.concatenate([np.nextafter(mids, 0), np.nextafter(mids, np.inf)])
+    rng = np.random.default_rng(5)
+    rand = np.ldexp(rng.uniform(1, 2, 400000), rng.integers(-14, 11, 400000))
+    x = np.concatenate([vals, mids, near, [0.0, 448.0, 449.0, 463.9, 464.0, 465.0, 1e9, np.inf], rand])
+    x = np.concatenate([x, -x])
+    assert np.array_equal(e4m3.round_values(x), e4m3.decode(e4m3.encode(x)))
+    assert np.array_equal(np.signbit(e4m3.round_values(np.array([-0.0, -1e-30]))), [True, True])
