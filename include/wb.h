@@ -285,6 +285,32 @@ WB_API wb_status wb_plan_waves(const wb_model_desc* desc, int32_t n_chunks,
                         int32_t* wave_of_chunk, int32_t* order,
                         int32_t* n_waves_out);
 
+/*
+ * One batch over several GPUs (host only; one process per GPU, each calling
+ * wb_transcribe_batch on its share).  Chunks are independent from the mel to
+ * the last decode step ("whisper-blaze 0.1.8", "Batch Transcription": every
+ * 30 s chunk of every request is its own unit of the batch), so the split
+ * needs no data from other GPUs.  The chunks, in request order, are cut into
+ * `world` contiguous ranges balanced on their work: chunk c weighs
+ * chunk_len[c] + 48 (its decode positions, plus the mel and encoder, which
+ * cost about as much as 48 positions of the large-v3 decoder); range r begins
+ * at the first chunk whose preceding work w satisfies w * world >= r * total.
+ * For rank `rank` this returns its range as a request list -- every request
+ * that overlaps the range, cut at chunk boundaries, with offsets into the
+ * same audio buffer -- so that
+ *   wb_transcribe_batch(model, audio, out_req_offset, out_req_samples,
+ *                       *out_n_req, prefix, chunk_len + *out_chunk_first, ...)
+ * transcribes exactly chunks [*out_chunk_first, *out_chunk_first +
+ * *out_chunk_count) and writes their token rows in the same order.  A rank
+ * may get no chunk (*out_chunk_count == 0, *out_n_req == 0).
+ *   req_offset, req_samples [host] int64 [n_req]; chunk_len [host] int32 [n_chunks]
+ *   out_req_offset, out_req_samples [host] int64 [n_req] (the first *out_n_req used)
+ */
+WB_API wb_status wb_shard_batch(int32_t n_req, const int64_t* req_offset, const int64_t* req_samples,
+                                const int32_t* chunk_len, int32_t world, int32_t rank,
+                                int64_t* out_req_offset, int64_t* out_req_samples, int32_t* out_n_req,
+                                int32_t* out_chunk_first, int32_t* out_chunk_count);
+
 /* ------------------------------------------------------------------ FP8 */
 
 /*
@@ -315,6 +341,22 @@ WB_API wb_status wb_quantise_e4m3(const void* x, int32_t x_is_bf16, int64_t n,
  */
 WB_API wb_status wb_quantise_e4m3_static(const void* x, int32_t x_is_bf16, int64_t n,
                                          uint8_t* codes, float* scale, wb_stream stream);
+
+/*
+ * The same quantisation over n_groups tensors at once, one scale each: group
+ * g is x[g * group_elems .. (g + 1) * group_elems).  This is how the
+ * WB_PREC_MIXED_FP8 encoder rounds each chunk's E4M3 GEMM input (one
+ * 1500 x K tensor per chunk, "whisper-blaze 0.1.8", "Direct Kernel API",
+ * quantise_e4m3: one scale per tensor).
+ *   x      [dev] float32 [n_groups * group_elems], 16-byte aligned
+ *   codes  [dev] uint8 [n_groups * group_elems] output, 16-byte aligned
+ *   scales [dev] float32 [n_groups] output: amax_g / 448 (1 when amax_g is 0)
+ * 1 <= n_groups <= 65535; group_elems a positive multiple of 4.  Codes are as
+ * in wb_quantise_e4m3 with the group's scale.  Scratch: none (scales doubles
+ * as the amax accumulator).
+ */
+WB_API wb_status wb_quantise_e4m3_groups(const float* x, int64_t n_groups, int64_t group_elems,
+                                         uint8_t* codes, float* scales, wb_stream stream);
 
 /* out [dev] float32 [n] = value(codes) * scale[0]. */
 WB_API wb_status wb_dequantise_e4m3(const uint8_t* codes, const float* scale,
@@ -373,6 +415,18 @@ WB_API int64_t wb_launch_count(void);
 /* Waits for the stream, then reports (and clears) the device error word of
  * the model (or of the library's mel kernels when model is null). */
 WB_API wb_status wb_sync_status(wb_model* model, wb_stream stream);
+
+/*
+ * Failure-detection test hook (no counterpart on the pages).  The next
+ * tensor-core GEMM the library launches in this process (any entry point)
+ * first waits limit_ns on a device barrier that nothing arrives on, then takes
+ * the path of a pipeline wait that ran out: it records a timeout in the error
+ * word it was given, stops issuing copies and MMAs, waits for the copies it
+ * already issued, releases its tensor memory and exits.  That call's output
+ * is unspecified; wb_sync_status reports WB_ERR_TIMEOUT and clears the word,
+ * and later calls run normally.  0 < limit_ns <= 1e9, else WB_ERR_INVALID_ARG.
+ */
+WB_API wb_status wb_debug_stall_next_gemm(uint64_t limit_ns);
 
 #ifdef __cplusplus
 }

@@ -38,6 +38,15 @@ Readings taken where the pages are silent or contradict one another:
     chunk, never per batch, so a chunk's result does not depend on what it is
     batched with.  The product of the two scales multiplies the exact product
     of the decoded codes;
+  * 16-bit storage ([BFW] "Inference Stack": the arithmetic is bfloat16;
+    [WB] "Precision Presets": mixed_fp8 keeps attention in 16 bits): with
+    ``act16`` the tensors the method holds in bf16 between its steps are
+    rounded to bf16 (nearest, ties to even) where it holds them -- the
+    encoder's attention operands Q, K, V and its attention output, the
+    encoder states handed to the decoder, and the cross-attention K/V cache
+    -- and every other value stays float64.  Under FP8 this matters: a bf16
+    rounding upstream of an E4M3 quantiser moves some codes to a neighbour,
+    and those moves compound through the layers;
   * FP8 self-attention cache: one scale per (layer, K or V) of each chunk,
     taken from the forced-prefix rows (oracle.e4m3.kv_scale_of); attention
     reads the dequantised cache, the current token's own row included;
@@ -74,6 +83,17 @@ def layer_norm(x, g, b, eps=EPS):
     mu = x.mean(axis=-1, keepdims=True)
     var = ((x - mu) ** 2).mean(axis=-1, keepdims=True)
     return (x - mu) / np.sqrt(var + eps) * np.asarray(g, np.float64) + np.asarray(b, np.float64)
+
+
+def bf16(x) -> np.ndarray:
+    """Nearest bfloat16 value of each entry (8 significant bits, ties to
+    even), returned as float64: inside binade [2^e, 2^(e+1)) the bf16 values
+    are 2^(e-7) apart, so the nearest is rint(x / 2^(e-7)) * 2^(e-7) (rint
+    rounds ties to even, the even significand)."""
+    x = np.asarray(x, dtype=np.float64)
+    _, ex = np.frexp(x)                        # |x| = f 2^ex, f in [0.5, 1)
+    step = np.ldexp(1.0, ex - 8)
+    return np.where(x == 0, x, np.rint(x / step) * step)
 
 
 def sinusoids(n_ctx: int, d: int) -> np.ndarray:
@@ -205,27 +225,35 @@ def conv_stem(mel, W):
     return x + sinusoids(x.shape[0], x.shape[1])
 
 
-def encoder_layer(h, W, l: int, n_heads: int, fp8: bool = False):
+def encoder_layer(h, W, l: int, n_heads: int, fp8: bool = False, act16: bool = False):
     """One pre-LN layer over one chunk's [1500, d] states; under ``mixed_fp8``
     each E4M3 GEMM input (LN1 output, LN2 output, GELU output) is one tensor
-    with one scale."""
+    with one scale; with ``act16`` attention reads bf16 Q, K, V and hands on a
+    bf16 result."""
     p = f"enc.{l}."
     a = layer_norm(h, W[p + "ln1.g"], W[p + "ln1.b"])
     q = Linear(W[p + "q.w"], W[p + "q.b"], fp8, "tensor")(a)
     k = Linear(W[p + "k.w"], W[p + "k.b"], fp8, "tensor")(a)
     v = Linear(W[p + "v.w"], W[p + "v.b"], fp8, "tensor")(a)
-    h = h + Linear(W[p + "o.w"], W[p + "o.b"])(multi_head(q, k, v, n_heads))
+    if act16:
+        q, k, v = bf16(q), bf16(k), bf16(v)
+    att = multi_head(q, k, v, n_heads)
+    if act16:
+        att = bf16(att)
+    h = h + Linear(W[p + "o.w"], W[p + "o.b"])(att)
     a = layer_norm(h, W[p + "ln2.g"], W[p + "ln2.b"])
     f = gelu(Linear(W[p + "fc1.w"], W[p + "fc1.b"], fp8, "tensor")(a))
     return h + Linear(W[p + "fc2.w"], W[p + "fc2.b"], fp8, "tensor")(f)
 
 
-def encode(mel, W, dims, fp8: bool = False, layers=None):
-    """[n_mels, 3000] -> [1500, d] encoder states (after the final LayerNorm)."""
+def encode(mel, W, dims, fp8: bool = False, layers=None, act16: bool = False):
+    """[n_mels, 3000] -> [1500, d] encoder states (after the final LayerNorm;
+    bf16 values with ``act16``, the form the decoder receives them in)."""
     h = conv_stem(mel, W)
     for l in range(dims.enc_layers if layers is None else layers):
-        h = encoder_layer(h, W, l, dims.n_heads, fp8)
-    return layer_norm(h, W["enc.lnp.g"], W["enc.lnp.b"])
+        h = encoder_layer(h, W, l, dims.n_heads, fp8, act16)
+    out = layer_norm(h, W["enc.lnp.g"], W["enc.lnp.b"])
+    return bf16(out) if act16 else out
 
 
 # ------------------------------------------------------------------ decoder
@@ -254,12 +282,14 @@ def _kv_fp8(x, prefix_len: int):
 
 def decode_teacher_forced(tokens, enc, W, dims, kv_fp8: bool = False,
                           prefix_len: int = 4, fp8: bool = False,
-                          return_hidden: bool = False, cross_fp8: bool = False):
+                          return_hidden: bool = False, cross_fp8: bool = False, act16: bool = False):
     """Logits [T, V] for a token sequence run through the decoder in one causal pass.
 
     Equivalent to stepping token by token with a KV cache: every position only
     sees earlier positions, and the FP8 cache scale depends on the prefix rows
-    alone.  Returns (logits, info) with the per-layer KV scales in ``info``.
+    alone.  With ``act16`` the cross-attention K/V cache holds bf16 values
+    (E4M3 ones with ``cross_fp8``, rounded from the float64 projection).
+    Returns (logits, info) with the per-layer KV scales in ``info``.
     """
     tokens = np.asarray(tokens)
     T = tokens.shape[0]
@@ -282,6 +312,8 @@ def decode_teacher_forced(tokens, enc, W, dims, kv_fp8: bool = False,
         if cross_fp8:
             (ck, sck), (cv, scv) = cross_kv_fp8(ck, cv)
             info.setdefault("cross_scales", []).append((sck, scv))
+        elif act16:
+            ck, cv = bf16(ck), bf16(cv)
         h = h + Linear(W[p + "co.w"], W[p + "co.b"])(multi_head(q, ck, cv, dims.n_heads))
         a = layer_norm(h, W[p + "ln3.g"], W[p + "ln3.b"])
         f = gelu(Linear(W[p + "fc1.w"], W[p + "fc1.b"], fp8)(a))

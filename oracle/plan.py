@@ -13,6 +13,9 @@ Readings:
     and V over 1500 encoder positions (bf16, or float8 when the cross K/V are
     stored as E4M3) plus its float8 self-attention K and V over its own decode
     length L_c, plus its token row (448 int32);
+  * several GPUs: contiguous ranges of chunks in request order, balanced on
+    decode length plus a fixed per-chunk share for the mel and encoder (each
+    chunk is transcribed on exactly one GPU; no step needs another GPU's data);
   * waves: chunks sorted by decode length, longest first (ties by chunk
     index), are packed greedily in that order; a new wave opens when the next
     chunk would push the running total of per-chunk bytes past the budget.
@@ -63,3 +66,45 @@ def plan_waves(chunk_len, d_model: int, dec_layers: int, budget_bytes: int, cros
     if cur:
         waves.append(np.array(cur, np.int32))
     return waves
+
+
+SHARD_CHUNK_BASE = 48
+
+
+def shard_ranges(chunk_len, world: int):
+    """Contiguous chunk ranges of one batch for ``world`` GPUs, balanced on
+    work: chunk c weighs chunk_len[c] + 48 (its decode positions plus the mel
+    and encoder, about 48 positions' worth); range r starts at the first chunk
+    whose preceding work w has w * world >= r * total.  Returns first[0..world]
+    with first[0] = 0 and first[world] = n_chunks."""
+    w = [int(x) + SHARD_CHUNK_BASE for x in np.asarray(chunk_len)]
+    total = sum(w)
+    first = [0]
+    for r in range(1, world):
+        acc, pick = 0, len(w)
+        for c in range(len(w)):
+            if acc * world >= r * total:
+                pick = c
+                break
+            acc += w[c]
+        first.append(pick)
+    first.append(len(w))
+    return first
+
+
+def shard_requests(req_offsets, req_samples, c0: int, c1: int):
+    """The requests overlapping chunks [c0, c1), cut at chunk boundaries:
+    (offsets, samples) into the same audio buffer."""
+    req, idx, valid = chunk_table(req_samples)
+    offs, samples = [], []
+    c = c0
+    while c < c1:
+        r, e = int(req[c]), c
+        while e < c1 and req[e] == r:
+            e += 1
+        s0 = int(idx[c]) * CHUNK
+        s1 = s0 + sum(int(v) for v in valid[c:e])
+        offs.append(int(req_offsets[r]) + s0)
+        samples.append(s1 - s0)
+        c = e
+    return np.array(offs, np.int64), np.array(samples, np.int64)

@@ -113,6 +113,15 @@ def test_host_side_argument_checks_need_no_gpu():
     assert L.wb_gemm(16, 16, 1, 8, 63, 0, None, None, None, 0, 16, 0, None) == -2
     assert L.wb_decode_step(None, 1, None, None) == -1
     assert L.wb_weights_bytes(ctypes.byref(bad)) == 0
+    # grouped quantiser: group count, group size and alignment are checked first
+    assert L.wb_quantise_e4m3_groups(None, 1, 4, 16, 16, None) == -1
+    assert L.wb_quantise_e4m3_groups(16, 0, 4, 16, 16, None) == -2
+    assert L.wb_quantise_e4m3_groups(16, 1, 6, 16, 16, None) == -2
+    assert L.wb_quantise_e4m3_groups(16, 65536, 4, 16, 16, None) == -2
+    assert L.wb_quantise_e4m3_groups(8, 1, 4, 16, 16, None) == -3
+    # the failure-detection hook rejects limits outside (0, 1 s] without arming
+    assert L.wb_debug_stall_next_gemm(0) == -1
+    assert L.wb_debug_stall_next_gemm(2 * 10**9) == -1
 
 
 def test_kv_modes_are_validated_on_the_host():
@@ -127,3 +136,23 @@ def test_kv_modes_are_validated_on_the_host():
     a = L.wb_weights_bytes(ctypes.byref(wb.make_desc(TURBO, wb.PREC_MIXED_FP8, wb.KV_FP8_SELF)))
     b = L.wb_weights_bytes(ctypes.byref(wb.make_desc(TURBO, wb.PREC_MIXED_FP8, wb.KV_FP8_CROSS)))
     assert a == b
+
+
+@pytest.mark.parametrize("world", [1, 2, 3, 8, 2000])
+def test_shard_batch_matches_oracle_bit_exact(world):
+    sb = serving_requests(0, n_req=48, with_audio=False)
+    first = oplan.shard_ranges(sb.chunk_len, world)
+    seen = 0
+    for rank in range(min(world, 9)):
+        offs, samples, c0, cn = wb.wb_shard_batch(sb.req_offsets, sb.req_samples, sb.chunk_len, world, rank)
+        assert (c0, cn) == (first[rank], first[rank + 1] - first[rank])
+        ro, rs = oplan.shard_requests(sb.req_offsets, sb.req_samples, c0, c0 + cn)
+        assert np.array_equal(offs, ro) and np.array_equal(samples, rs)
+        seen += cn
+    if world <= 9:
+        assert seen == sb.chunk_len.size
+
+
+def test_shard_batch_rejects_bad_rank():
+    with pytest.raises(wb.WBError):
+        wb.wb_shard_batch(np.zeros(1, np.int64), np.ones(1, np.int64), np.ones(1, np.int32), 2, 2)

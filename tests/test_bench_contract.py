@@ -25,3 +25,17 @@ def test_reference_arm_json_line():
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
     assert "workload" in d["config"]
+
+
+def test_reference_arm_finishes_the_serving_workload_at_driver_step_counts():
+    """The serving-batch reference arm with 20 timed and 5 warm-up steps ends
+    well inside the driver's limit: every step is one bounded oracle sample of
+    a few seconds, and only the sampled chunk's weights are generated."""
+    env = dict(os.environ)
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--config", "c5",
+                          "--steps", "20", "--warmup", "5"], capture_output=True, text=True, timeout=600, cwd=ROOT,
+                         env=env)
+    assert out.returncode == 0, out.stderr[-2000:]
+    d = json.loads([l for l in out.stdout.splitlines() if l.startswith("{")][0])
+    assert d["impl"] == "reference" and d["steps"] == 20 and d["warmup"] == 5 and d["value"] > 0
+    assert "extrapolated" in d["cpu_baseline"]["sample"]

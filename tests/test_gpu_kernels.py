@@ -122,7 +122,9 @@ def _sample_rows(M, seed):
 
 @pytest.mark.parametrize("M,N,K", [(9000, 5120, 1280), (4100, 3840, 640)])
 def test_gemm_pair_bf16_matches_oracle(M, N, K):
-    """Large plain GEMMs run on CTA pairs sharing each B tile (odd M-tile count: the last pair has an empty half)."""
+    """Large plain GEMMs run on CTA pairs (cta_group::2 MMAs over 256-row
+    tiles, each CTA loading its own half of A and of B): an odd number of
+    128-row tiles leaves the last pair's second half empty."""
     rng = np.random.default_rng(M + N)
     a = _bf16(rng.normal(size=(M, K)))
     b = _bf16(rng.normal(size=(N, K)) * 0.05)
@@ -192,3 +194,54 @@ def test_quantiser_codes_bit_exact(bf16, n):
     assert np.float32(scale.item()) == ref_scale
     assert np.array_equal(codes.cpu().numpy(), ref_codes)
     assert np.array_equal(out.cpu().numpy(), (oe4m3.decode(ref_codes) * np.float64(ref_scale)).astype(np.float32))
+
+
+@pytest.mark.parametrize("n_groups,group_elems", [(5, 1500 * 64), (3, 4), (2, 1500 * 1284), (1, 1 << 20)])
+def test_group_quantiser_bit_exact(n_groups, group_elems):
+    """One E4M3 scale per group (the mixed_fp8 encoder's per-chunk tensors):
+    codes and scales bit-exact against the oracle's per-tensor quantiser on
+    each group, including an all-zero group and a group whose amax is one
+    outlier."""
+    rng = np.random.default_rng(n_groups * 31 + group_elems % 997)
+    x = rng.normal(0, 2.0, size=(n_groups, group_elems)).astype(np.float32)
+    if n_groups > 1:
+        x[1] = 0.0
+    if n_groups > 2:
+        x[2] *= 1e-3
+        x[2, group_elems // 2] = -300.0
+    X = torch.from_numpy(x.reshape(-1)).cuda()
+    codes = torch.full((x.size,), 0xAA, dtype=torch.uint8, device="cuda")
+    scales = torch.full((n_groups,), -1.0, device="cuda")
+    wb.wb_quantise_e4m3_groups(X, n_groups, codes, scales)
+    wb.wb_sync_status()
+    got_c = codes.cpu().numpy().reshape(n_groups, group_elems)
+    got_s = scales.cpu().numpy()
+    for g in range(n_groups):
+        ref_c, ref_s = oe4m3.quantise_tensor(x[g])
+        assert np.float32(got_s[g]) == ref_s, g
+        assert np.array_equal(got_c[g], ref_c), g
+
+
+def test_gemm_bounded_wait_runs_out_and_recovers():
+    """Failure detection without a fault: the GEMM's first pipeline wait is
+    made to run out (a 1 ms wait on a barrier nothing arrives on).  The kernel
+    records a timeout, drains its own copies, frees its tensor memory and
+    exits; wb_sync_status reports WB_ERR_TIMEOUT, and the next call on the
+    same context computes the right product."""
+    rng = np.random.default_rng(77)
+    M, N, K = 256, 512, 256
+    a, b = _bf16(rng.normal(size=(M, K))), _bf16(rng.normal(size=(N, K)) * 0.05)
+    A = torch.from_numpy(a).to(torch.bfloat16).cuda()
+    B = torch.from_numpy(b).to(torch.bfloat16).cuda()
+    C = torch.zeros(M, N, dtype=torch.bfloat16, device="cuda")
+    wb.wb_sync_status()
+    wb.wb_debug_stall_next_gemm(1_000_000)
+    wb.wb_gemm(A, B, C, gelu=True)
+    with pytest.raises(wb.WBError) as err:
+        wb.wb_sync_status()
+    assert err.value.status == -6, err.value
+    wb.wb_sync_status()                     # the error word was cleared
+    wb.wb_gemm(A, B, C, gelu=True)
+    wb.wb_sync_status()
+    ref = omodel.gelu(omodel.Linear(b, np.zeros(N))(a))
+    assert np.abs(C.float().cpu().numpy() - ref).max() <= 2 ** -8 * np.abs(ref).max() + 1e-3

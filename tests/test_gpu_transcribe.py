@@ -60,7 +60,8 @@ def test_transcribe_batch_matches_oracle(prec, kv):
         pred = omodel.greedy(ref[3:L - 1])
         agree += int((pred == tok[c, 4:L]).sum())
         total += L - 4
-    # bf16: at least 99 % of greedy tokens agree; mixed_fp8 is bounded by how
-    # often FP8 rounding itself moves the argmax (about 5 % on random weights)
-    assert agree / total >= (0.99 if prec == wb.PREC_BF16 else 0.9), agree / total
+    # at least 99 % of greedy tokens agree with the oracle's argmax, in every
+    # precision (mixed_fp8 included: the oracle applies the same E4M3 rules)
+    print(f"precision {prec}, kv {kv}: greedy agreement {agree / total:.4f}")
+    assert agree / total >= 0.99, agree / total
     m.close()

@@ -148,19 +148,20 @@ def test_encoder_permutation_equivariance_without_positions():
     np.testing.assert_allclose(a[perm], b, atol=1e-12)
 
 
-@pytest.mark.parametrize("kv_fp8,cross_fp8", [(False, False), (True, False), (True, True)])
-def test_decoder_causality_and_prefix_consistency(kv_fp8, cross_fp8):
+@pytest.mark.parametrize("kv_fp8,cross_fp8,act16", [(False, False, False), (True, False, False),
+                                                      (True, True, False), (True, False, True)])
+def test_decoder_causality_and_prefix_consistency(kv_fp8, cross_fp8, act16):
     W = make_weights(MINI, 7, bf16=True)
     rng = np.random.default_rng(7)
     enc = rng.normal(size=(20, MINI.d_model))
     tok = rng.integers(0, MINI.vocab, size=12)
-    full, _ = model.decode_teacher_forced(tok, enc, W, MINI, kv_fp8=kv_fp8, cross_fp8=cross_fp8)
+    full, _ = model.decode_teacher_forced(tok, enc, W, MINI, kv_fp8=kv_fp8, cross_fp8=cross_fp8, act16=act16)
     tok2 = tok.copy()
     tok2[8:] = rng.integers(0, MINI.vocab, size=4)
-    alt, _ = model.decode_teacher_forced(tok2, enc, W, MINI, kv_fp8=kv_fp8, cross_fp8=cross_fp8)
+    alt, _ = model.decode_teacher_forced(tok2, enc, W, MINI, kv_fp8=kv_fp8, cross_fp8=cross_fp8, act16=act16)
     np.testing.assert_array_equal(full[:8], alt[:8])          # future tokens are invisible
     for t in (4, 6, 11):                                      # cache-append == full pass
-        part, _ = model.decode_teacher_forced(tok[:t + 1], enc, W, MINI, kv_fp8=kv_fp8, cross_fp8=cross_fp8)
+        part, _ = model.decode_teacher_forced(tok[:t + 1], enc, W, MINI, kv_fp8=kv_fp8, cross_fp8=cross_fp8, act16=act16)
         np.testing.assert_allclose(part[t], full[t], atol=1e-12)
 
 
@@ -299,6 +300,34 @@ def test_fp8_encoder_layer_permutation_equivariant():
     a = model.encoder_layer(h, W, 0, MINI.n_heads, fp8=True)
     b = model.encoder_layer(h[perm], W, 0, MINI.n_heads, fp8=True)
     np.testing.assert_allclose(b, a[perm], rtol=1e-11, atol=1e-11)
+
+
+def test_bf16_rounding_matches_torch_and_ties_to_even():
+    rng = np.random.default_rng(17)
+    x = np.concatenate([rng.normal(0, 1, 200000), rng.normal(0, 1e-3, 50000), rng.normal(0, 300, 50000)])
+    x = x.astype(np.float32)
+    # exact ties: a bf16 value plus half its spacing (low 16 bits 0x8000)
+    ties = (x[:1000].view(np.uint32) & np.uint32(0xFFFF0000)) | np.uint32(0x8000)
+    x = np.concatenate([x, ties.view(np.float32), np.float32([0.0, -0.0, 1.0, -2.5])])
+    ref = torch.from_numpy(x).to(torch.bfloat16).to(torch.float64).numpy()
+    assert np.array_equal(model.bf16(x.astype(np.float64)), ref)
+
+
+def test_act16_states_are_bf16_and_close_to_float64():
+    """The encoder states handed to the decoder are bf16 values; one layer
+    with bf16 attention operands stays within the bf16 rounding bound of the
+    float64 layer."""
+    W = make_weights(MINI, 18, bf16=False)
+    h = np.random.default_rng(19).normal(size=(40, MINI.d_model))
+    a = model.encoder_layer(h, W, 0, MINI.n_heads)
+    b = model.encoder_layer(h, W, 0, MINI.n_heads, act16=True)
+    assert np.abs(a - b).max() <= 2.0 ** -7 * np.abs(a).max()
+    assert 0 < np.abs(a - b).max()
+    enc = model.encode(np.random.default_rng(20).normal(size=(MINI.n_mels, 3000)), W, MINI, layers=1, act16=True)
+    assert np.array_equal(model.bf16(enc), enc)
+    perm = np.random.default_rng(21).permutation(40)    # elementwise rounding keeps the equivariance
+    c = model.encoder_layer(h[perm], W, 0, MINI.n_heads, act16=True)
+    np.testing.assert_allclose(c, b[perm], rtol=1e-11, atol=1e-11)
 
 
 def test_greedy_lowest_index_on_ties():

@@ -65,3 +65,42 @@ def test_fp8_cross_kv_halves_the_cross_bytes_and_fits_more_per_wave():
     w_f8 = plan.plan_waves(lens, d, L, budget, cross_bytes=1)
     assert len(w_f8) < len(w_bf)
     assert sorted(np.concatenate(w_f8).tolist()) == list(range(900))
+
+
+@pytest.mark.parametrize("world", [1, 2, 3, 8])
+def test_shard_ranges_cover_every_chunk_once_and_balance(world):
+    sb = serving_requests(3, n_req=20, with_audio=False)
+    lens = sb.chunk_len
+    first = plan.shard_ranges(lens, world)
+    assert first[0] == 0 and first[-1] == lens.size and len(first) == world + 1
+    assert all(a <= b for a, b in zip(first, first[1:]))
+    owner = np.concatenate([np.full(b - a, r) for r, (a, b) in enumerate(zip(first, first[1:]))])
+    assert owner.size == lens.size                      # each chunk on exactly one rank, in order
+    w = lens.astype(np.int64) + plan.SHARD_CHUNK_BASE
+    total = int(w.sum())
+    for r in range(world):                               # greedy prefix cut: within one chunk of the mean
+        got = int(w[first[r]:first[r + 1]].sum())
+        assert abs(got - total / world) <= w.max(), (r, got, total / world)
+
+
+def test_shard_ranges_more_ranks_than_chunks():
+    first = plan.shard_ranges(np.array([100, 200], np.int32), 5)
+    assert first[0] == 0 and first[-1] == 2
+    sizes = np.diff(first)
+    assert sizes.sum() == 2 and (sizes >= 0).all()
+
+
+def test_shard_requests_rechunk_to_the_same_chunks():
+    """A rank's trimmed requests, cut into chunks again, are exactly its chunk
+    range: same audio start and same valid samples, in the same order."""
+    sb = serving_requests(4, n_req=12, with_audio=False)
+    req, idx, valid = plan.chunk_table(sb.req_samples)
+    start = sb.req_offsets[req] + idx.astype(np.int64) * plan.CHUNK
+    first = plan.shard_ranges(sb.chunk_len, 3)
+    for r in range(3):
+        c0, c1 = first[r], first[r + 1]
+        offs, samples = plan.shard_requests(sb.req_offsets, sb.req_samples, c0, c1)
+        rreq, ridx, rvalid = plan.chunk_table(samples)
+        assert rreq.size == c1 - c0
+        assert np.array_equal(rvalid, valid[c0:c1])
+        assert np.array_equal(offs[rreq] + ridx.astype(np.int64) * plan.CHUNK, start[c0:c1])

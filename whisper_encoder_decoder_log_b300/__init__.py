@@ -55,10 +55,13 @@ _SIGS = {
     "wb_transcribe_workspace_size": (_SZ, [_VP, _I32, _VP, _VP, _U64]),
     "wb_transcribe_batch": (ctypes.c_int, [_VP, _VP, _VP, _VP, _I32, _VP, _VP, _VP, _U64, _VP, _SZ, _VP, _VP]),
     "wb_plan_waves": (ctypes.c_int, [ctypes.POINTER(ModelDesc), _I32, _VP, _U64, _VP, _VP, _VP]),
+    "wb_shard_batch": (ctypes.c_int, [_I32, _VP, _VP, _VP, _I32, _I32, _VP, _VP, _VP, _VP, _VP]),
     "wb_quantise_e4m3": (ctypes.c_int, [_VP, _I32, _I64, _VP, _VP, _VP]),
     "wb_dequantise_e4m3": (ctypes.c_int, [_VP, _VP, _I64, _VP, _VP]),
     "wb_quantise_e4m3_static": (ctypes.c_int, [_VP, _I32, _I64, _VP, _VP, _VP]),
+    "wb_quantise_e4m3_groups": (ctypes.c_int, [_VP, _I64, _I64, _VP, _VP, _VP]),
     "wb_sync_status": (ctypes.c_int, [_VP, _VP]),
+    "wb_debug_stall_next_gemm": (ctypes.c_int, [_U64]),
     "wb_gemm": (ctypes.c_int, [_VP, _VP, _I64, _I64, _I64, _I32, _VP, _VP, _VP, _I32, _VP, _I32, _VP]),
     "wb_prof_start": (ctypes.c_int, [_I32, _I32]),
     "wb_launch_count": (_I64, []),
@@ -232,6 +235,20 @@ def wb_plan_waves(desc: ModelDesc, chunk_len, budget: int):
     return wave, order, nw.value
 
 
+def wb_shard_batch(req_offset, req_samples, chunk_len, world: int, rank: int):
+    """This rank's share of one batch: (req_offset, req_samples, chunk_first,
+    chunk_count), the requests cut at chunk boundaries (host only)."""
+    ro, rop = _host_arr(req_offset, np.int64)
+    rs, rsp = _host_arr(req_samples, np.int64)
+    cl, clp = _host_arr(chunk_len, np.int32)
+    oo = np.zeros(rs.size, np.int64)
+    os_ = np.zeros(rs.size, np.int64)
+    nr, c0, cn = _I32(0), _I32(0), _I32(0)
+    _check(lib().wb_shard_batch(rs.size, rop, rsp, clp, world, rank, oo.ctypes.data, os_.ctypes.data,
+                                ctypes.addressof(nr), ctypes.addressof(c0), ctypes.addressof(cn)))
+    return oo[:nr.value].copy(), os_[:nr.value].copy(), c0.value, cn.value
+
+
 def wb_quantise_e4m3(x, codes, scale, stream=None):
     import torch
     _need(codes, "uint8", "codes")
@@ -247,6 +264,17 @@ def wb_quantise_e4m3_static(x, codes, scale, stream=None):
     _need(scale, "float32", "scale")
     _check(lib().wb_quantise_e4m3_static(_p(x), 1 if x.dtype == torch.bfloat16 else 0, x.numel(), _p(codes),
                                          _p(scale), _stream(stream)))
+
+
+def wb_quantise_e4m3_groups(x, n_groups: int, codes, scales, stream=None):
+    """One E4M3 scale per group of x.numel() // n_groups consecutive fp32 values."""
+    _need(x, "float32", "x")
+    _need(codes, "uint8", "codes")
+    _need(scales, "float32", "scales")
+    if x.numel() % n_groups:
+        raise ValueError("x.numel() must be a multiple of n_groups")
+    _check(lib().wb_quantise_e4m3_groups(_p(x), n_groups, x.numel() // n_groups, _p(codes), _p(scales),
+                                         _stream(stream)))
 
 
 def wb_dequantise_e4m3(codes, scale, out, stream=None):
@@ -285,6 +313,11 @@ def wb_prof_result(kind: int):
 
 def wb_sync_status(model: Optional[int] = None, stream=None):
     _check(lib().wb_sync_status(model, _stream(stream)))
+
+
+def wb_debug_stall_next_gemm(limit_ns: int):
+    """Make the next tensor-core GEMM give up after a bounded wait (test hook)."""
+    _check(lib().wb_debug_stall_next_gemm(limit_ns))
 
 
 # ----------------------------------------------------------------- marshalling helpers

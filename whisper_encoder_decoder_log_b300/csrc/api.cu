@@ -490,6 +490,7 @@ struct EncBufs {
     void* f;
     uint8_t* fq;
     float* f_scale;
+    unsigned* amax;     // mixed_fp8: [layer][LN1 | LN2 | GELU][chunk] E4M3 tensor amax
 };
 
 size_t carve_encoder(const wb_model* m, int64_t B, EncBufs* eb, uint8_t* base, size_t cap, bool* overflow) {
@@ -498,16 +499,20 @@ size_t carve_encoder(const wb_model* m, int64_t B, EncBufs* eb, uint8_t* base, s
     const size_t act = m->fp32() ? 4 : 2;
     const int64_t M = B * kCtx;
     EncBufs e;
-    e.melT = c.take<uint8_t>((size_t)B * (kFrames + 2) * C * act);
-    e.x1 = c.take<uint8_t>((size_t)B * (kFrames + 2) * d * act);
+    // bf16 models: stem rows hold (hi | lo) bf16 pairs, the size of fp32
+    e.melT = c.take<uint8_t>((size_t)B * (kFrames + 2) * C * 4);
+    e.x1 = c.take<uint8_t>((size_t)B * (kFrames + 2) * d * 4);
     e.h = c.take<float>((size_t)M * d);
     e.a = c.take<uint8_t>((size_t)M * d * act);
     e.a_scale = c.take<float>(M);
     e.qkv = c.take<uint8_t>((size_t)M * 3 * d * act);
     e.attn = c.take<uint8_t>((size_t)M * d * act);
-    e.f = c.take<uint8_t>((size_t)M * F * act);
+    // mixed_fp8 keeps the GELU output in fp32: FC2's E4M3 input is rounded
+    // once, from fp32, with the chunk's scale
+    e.f = c.take<uint8_t>((size_t)M * F * (m->fp8() ? 4 : act));
     e.fq = m->fp8() ? c.take<uint8_t>((size_t)M * F) : nullptr;
     e.f_scale = c.take<float>(M);
+    e.amax = m->fp8() ? c.take<unsigned>((size_t)std::max(1, m->desc.enc_layers) * 3 * B) : nullptr;
     if (eb) *eb = e;
     if (overflow) *overflow = c.overflow;
     return align_up(c.cur, 256);
@@ -525,9 +530,10 @@ wb_status decoder_layers(wb_decoder* dec, int64_t n_chunks, int rows_per_chunk, 
     const int d = m->d(), H = m->H(), F = m->F();
     const int64_t R = n_chunks * rows_per_chunk;
     const bool f32 = m->fp32(), f8 = m->fp8();
-    // split bf16 activations for the bf16 model; under mixed_fp8 the FP8
-    // rounding of QKV/FFN inputs dominates and plain bf16 suffices
-    const bool sp = m->desc.precision == WB_PREC_BF16;
+    // split bf16 activations for every bf16 GEMM input (mixed_fp8 included:
+    // there the E4M3 codes of the next QKV/FFN inputs depend on these values,
+    // and a bf16 rounding upstream would move some of them to the next code)
+    const bool sp = !f32;
     const LnOut ln_act = f32 ? LN_F32 : (sp ? LN_BF16X2 : LN_BF16);
     const DType attn_dt = f32 ? DT_F32 : (sp ? DT_BF16X2 : DT_BF16);
     const int64_t lda = sp ? 2 * d : d;                // row stride of LN / attention outputs
@@ -640,7 +646,7 @@ wb_status decoder_head(wb_decoder* dec, int64_t n_chunks, int rows_per_chunk, in
                        cudaStream_t s, const int* pos_dev) {
     wb_model* m = dec->m;
     const int d = m->d(), V = m->desc.vocab;
-    const bool sp = m->desc.precision == WB_PREC_BF16;
+    const bool sp = !m->fp32();
     const LnOut ln_act = m->fp32() ? LN_F32 : (sp ? LN_BF16X2 : LN_BF16);
     const int64_t lda = sp ? 2 * d : d;
     const int64_t R = n_chunks * rows_per_chunk;
@@ -792,10 +798,13 @@ wb_status wb_model_create(const wb_model_desc* desc, const void* weights, wb_mod
     if (wb_status st = dev_alloc(m, (void**)&m->err, 16)) return bail(st);
     m->scratch_bits = m->err + 1;
     if (cudaMemset(m->err, 0, 16) != cudaSuccess) return bail(fail(WB_ERR_CUDA, "memset"));
-    if (wb_status st = dev_alloc(m, &m->conv1_w, (size_t)d * C * 3 * m->wsz())) return bail(st);
-    if (wb_status st = dev_alloc(m, &m->conv2_w, (size_t)d * d * 3 * m->wsz())) return bail(st);
-    if (wb_status st = conv_reorder(m->W("enc.conv1.w"), d, C, bf, m->conv1_w, s)) return bail(st);
-    if (wb_status st = conv_reorder(m->W("enc.conv2.w"), d, d, bf, m->conv2_w, s)) return bail(st);
+    // bf16 models feed the stem GEMMs bf16 pairs (hi | lo) of every value:
+    // each conv tap is stored twice to multiply both halves
+    const size_t taps = bf ? 6 : 3;
+    if (wb_status st = dev_alloc(m, &m->conv1_w, (size_t)d * C * taps * m->wsz())) return bail(st);
+    if (wb_status st = dev_alloc(m, &m->conv2_w, (size_t)d * d * taps * m->wsz())) return bail(st);
+    if (wb_status st = conv_reorder(m->W("enc.conv1.w"), d, C, bf, m->conv1_w, s, bf)) return bail(st);
+    if (wb_status st = conv_reorder(m->W("enc.conv2.w"), d, d, bf, m->conv2_w, s, bf)) return bail(st);
     {
         std::vector<float> pe;
         sinusoids(kCtx, d, pe);
@@ -855,23 +864,29 @@ wb_status wb_encode(wb_model* m, const float* mel, int64_t B, void* enc, void* w
     const int act_out = f32 ? OUT_F32 : OUT_BF16;
     const LnOut ln_plain = f32 ? LN_F32 : LN_BF16;
     // ---- stem: mel -> [B, 3002, C] -> conv1 (+GELU) -> padded [B, 3002, d] -> conv2 (+GELU, +PE)
+    // bf16 models carry every stem value as a bf16 pair (hi | lo) and multiply
+    // both halves by the same (duplicated) conv taps: the stem output enters
+    // the fp32 residual with ~16 bits instead of bf16's 8
+    const int64_t pw = f32 ? 1 : 2;    // stored values per mel / conv1 value
     if (wb_status st = mel_transpose_pad(mel, B, C, e.melT, !f32, s)) return st;
-    WB_CUDA(cudaMemset2DAsync(e.x1, (size_t)(kFrames + 2) * d * act, 0, (size_t)d * act, (size_t)B, s));
-    WB_CUDA(cudaMemset2DAsync(reinterpret_cast<uint8_t*>(e.x1) + (size_t)(kFrames + 1) * d * act,
-                              (size_t)(kFrames + 2) * d * act, 0, (size_t)d * act, (size_t)B, s));
+    WB_CUDA(cudaMemset2DAsync(e.x1, (size_t)(kFrames + 2) * pw * d * act, 0, (size_t)pw * d * act, (size_t)B, s));
+    WB_CUDA(cudaMemset2DAsync(reinterpret_cast<uint8_t*>(e.x1) + (size_t)(kFrames + 1) * pw * d * act,
+                              (size_t)(kFrames + 2) * pw * d * act, 0, (size_t)pw * d * act, (size_t)B, s));
     {
         Lin L;
-        L.a = e.melT; L.rows = kFrames; L.lda = C; L.batches = B; L.batch_stride = (int64_t)(kFrames + 2) * C;
-        L.w = m->conv1_w; L.N = d; L.K = 3 * C;
-        GemmEpi ep = epi_out(e.x1, d, act_out, m->V("enc.conv1.b"), 1);
+        L.a = e.melT; L.rows = kFrames; L.lda = pw * C; L.batches = B;
+        L.batch_stride = (int64_t)(kFrames + 2) * pw * C;
+        L.w = m->conv1_w; L.N = d; L.K = 3 * pw * C;
+        GemmEpi ep = epi_out(e.x1, pw * d, f32 ? OUT_F32 : OUT_BF16X2, m->V("enc.conv1.b"), 1);
         ep.out_batch_rows = kFrames + 2;
         ep.out_row_offset = 1;
         if (wb_status st = linear(m, L, ep, s)) return st;
     }
     {
         Lin L;
-        L.a = e.x1; L.rows = kCtx; L.lda = 2 * d; L.batches = B; L.batch_stride = (int64_t)(kFrames + 2) * d;
-        L.w = m->conv2_w; L.N = d; L.K = 3 * d;
+        L.a = e.x1; L.rows = kCtx; L.lda = 2 * pw * d; L.batches = B;
+        L.batch_stride = (int64_t)(kFrames + 2) * pw * d;
+        L.w = m->conv2_w; L.N = d; L.K = 3 * pw * d;
         GemmEpi ep = epi_out(e.h, d, OUT_F32, m->V("enc.conv2.b"), 1);
         ep.add = m->pe;
         ep.ld_add = d;
@@ -879,10 +894,22 @@ wb_status wb_encode(wb_model* m, const float* mel, int64_t B, void* enc, void* w
         if (wb_status st = linear(m, L, ep, s)) return st;
     }
     // ---- layers
+    // mixed_fp8: every E4M3 GEMM input is one tensor per chunk (1500 rows)
+    // with one scale amax / 448 ("whisper-blaze 0.1.8", "Direct Kernel API",
+    // quantise_e4m3 returns one scale per tensor)
+    if (f8 && m->desc.enc_layers > 0)
+        WB_CUDA(cudaMemsetAsync(e.amax, 0, sizeof(unsigned) * (size_t)m->desc.enc_layers * 3 * B, s));
+    auto amax_of = [&](int l, int which) { return e.amax + ((int64_t)l * 3 + which) * B; };
     for (int l = 0; l < m->desc.enc_layers; ++l) {
-        if (wb_status st = layernorm(e.h, d, M, d, m->V(nm("enc.", l, "ln1.g")), m->V(nm("enc.", l, "ln1.b")),
-                                     f8 ? LN_E4M3 : ln_plain, e.a, d, e.a_scale, s))
+        if (f8) {
+            if (wb_status st = layernorm_group_e4m3(e.h, d, M, d, m->V(nm("enc.", l, "ln1.g")),
+                                                    m->V(nm("enc.", l, "ln1.b")), kCtx, amax_of(l, 0),
+                                                    reinterpret_cast<uint8_t*>(e.a), d, e.a_scale, s))
+                return st;
+        } else if (wb_status st = layernorm(e.h, d, M, d, m->V(nm("enc.", l, "ln1.g")), m->V(nm("enc.", l, "ln1.b")),
+                                            ln_plain, e.a, d, e.a_scale, s)) {
             return st;
+        }
         {
             Lin L;
             L.a = e.a; L.rows = M; L.lda = d; L.w = m->W(nm("enc.", l, "q.w")); L.N = 3 * d; L.K = d;
@@ -907,20 +934,35 @@ wb_status wb_encode(wb_model* m, const float* mel, int64_t B, void* enc, void* w
             L.a = e.attn; L.rows = M; L.lda = d; L.w = m->W(nm("enc.", l, "o.w")); L.N = d; L.K = d;
             if (wb_status st = linear(m, L, epi_out(e.h, d, OUT_F32_ACC, m->V(nm("enc.", l, "o.b"))), s)) return st;
         }
-        if (wb_status st = layernorm(e.h, d, M, d, m->V(nm("enc.", l, "ln2.g")), m->V(nm("enc.", l, "ln2.b")),
-                                     f8 ? LN_E4M3 : ln_plain, e.a, d, e.a_scale, s))
+        if (f8) {
+            if (wb_status st = layernorm_group_e4m3(e.h, d, M, d, m->V(nm("enc.", l, "ln2.g")),
+                                                    m->V(nm("enc.", l, "ln2.b")), kCtx, amax_of(l, 1),
+                                                    reinterpret_cast<uint8_t*>(e.a), d, e.a_scale, s))
+                return st;
+        } else if (wb_status st = layernorm(e.h, d, M, d, m->V(nm("enc.", l, "ln2.g")), m->V(nm("enc.", l, "ln2.b")),
+                                            ln_plain, e.a, d, e.a_scale, s)) {
             return st;
+        }
         {
             Lin L;
             L.a = e.a; L.rows = M; L.lda = d; L.w = m->W(nm("enc.", l, "fc1.w")); L.N = F; L.K = d;
-            if (f8) { L.f8 = &m->enc_fc1[l]; L.a_scale = e.a_scale; }
-            if (wb_status st = linear(m, L, epi_out(e.f, F, act_out, m->V(nm("enc.", l, "fc1.b")), 1), s)) return st;
+            GemmEpi ep = epi_out(e.f, F, act_out, m->V(nm("enc.", l, "fc1.b")), 1);
+            if (f8) {
+                // fp32 GELU output and each chunk's amax of it, taken in the epilogue
+                L.f8 = &m->enc_fc1[l]; L.a_scale = e.a_scale;
+                ep.out_type = OUT_F32;
+                ep.amax = amax_of(l, 2);
+                ep.amax_rows = kCtx;
+            }
+            if (wb_status st = linear(m, L, ep, s)) return st;
         }
         {
             Lin L;
             L.rows = M; L.w = m->W(nm("enc.", l, "fc2.w")); L.N = d; L.K = F;
             if (f8) {
-                if (wb_status st = quant_rows(e.f, M, F, e.fq, e.f_scale, s)) return st;
+                if (wb_status st = quant_groups(reinterpret_cast<const float*>(e.f), M, F, kCtx, amax_of(l, 2), e.fq,
+                                                e.f_scale, s))
+                    return st;
                 L.a = e.fq; L.lda = F; L.f8 = &m->enc_fc2[l]; L.a_scale = e.f_scale;
             } else {
                 L.a = e.f; L.lda = F;
@@ -1121,6 +1163,68 @@ wb_status wb_plan_waves(const wb_model_desc* desc, int32_t n, const int32_t* len
     return WB_OK;
 }
 
+// Work of one chunk for the split across GPUs, in decode positions: its own
+// decode length plus the mel and encoder, which cost about as much as 48
+// decode positions of the 32-layer large-v3 decoder.
+constexpr int64_t kShardChunkBase = 48;
+
+wb_status wb_shard_batch(int32_t n_req, const int64_t* req_offset, const int64_t* req_samples,
+                         const int32_t* chunk_len, int32_t world, int32_t rank, int64_t* out_req_offset,
+                         int64_t* out_req_samples, int32_t* out_n_req, int32_t* out_chunk_first,
+                         int32_t* out_chunk_count) {
+    if (n_req < 1 || !req_offset || !req_samples || !chunk_len || !out_req_offset || !out_req_samples || !out_n_req ||
+        !out_chunk_first || !out_chunk_count)
+        return fail(WB_ERR_INVALID_ARG, "wb_shard_batch: null argument or n_req < 1");
+    if (world < 1 || rank < 0 || rank >= world) return fail(WB_ERR_INVALID_ARG, "wb_shard_batch: bad world/rank");
+    // chunks in request order: (request, index), as the chunk table of wb_transcribe_batch
+    std::vector<int32_t> creq;
+    std::vector<int64_t> cidx;
+    for (int32_t r = 0; r < n_req; ++r) {
+        if (req_samples[r] < 1) return fail(WB_ERR_SHAPE, "wb_shard_batch: empty request");
+        const int64_t n = (req_samples[r] + kChunkSamples - 1) / kChunkSamples;
+        for (int64_t k = 0; k < n; ++k) {
+            creq.push_back(r);
+            cidx.push_back(k);
+        }
+    }
+    const int64_t n = (int64_t)creq.size();
+    if (n > INT32_MAX) return fail(WB_ERR_SHAPE, "wb_shard_batch: too many chunks");
+    int64_t total = 0;
+    for (int64_t c = 0; c < n; ++c) {
+        if (chunk_len[c] < 1) return fail(WB_ERR_SHAPE, "wb_shard_batch: chunk_len < 1");
+        total += chunk_len[c] + kShardChunkBase;
+    }
+    // range r = [first(r), first(r + 1)), first(r) = the first chunk whose
+    // preceding work w satisfies w * world >= r * total
+    auto first_of = [&](int64_t r) -> int64_t {
+        if (r <= 0) return 0;
+        if (r >= world) return n;
+        int64_t w = 0;
+        for (int64_t c = 0; c < n; ++c) {
+            if (w * world >= r * total) return c;
+            w += chunk_len[c] + kShardChunkBase;
+        }
+        return n;
+    };
+    const int64_t c0 = first_of(rank), c1 = first_of((int64_t)rank + 1);
+    *out_chunk_first = (int32_t)c0;
+    *out_chunk_count = (int32_t)(c1 - c0);
+    int32_t k = 0;
+    for (int64_t c = c0; c < c1;) {
+        const int32_t r = creq[c];
+        int64_t e = c;   // chunks of request r inside the range
+        while (e < c1 && creq[e] == r) ++e;
+        const int64_t s0 = cidx[c] * kChunkSamples;
+        const int64_t s1 = std::min<int64_t>(req_samples[r], (cidx[e - 1] + 1) * kChunkSamples);
+        out_req_offset[k] = req_offset[r] + s0;
+        out_req_samples[k] = s1 - s0;
+        ++k;
+        c = e;
+    }
+    *out_n_req = k;
+    return WB_OK;
+}
+
 struct TranscribeBufs {
     float* chunk_audio = nullptr;
     float* mel = nullptr;
@@ -1288,6 +1392,28 @@ wb_status wb_quantise_e4m3(const void* x, int32_t x_is_bf16, int64_t n, uint8_t*
         if (!bits[dev & 63]) WB_CUDA(cudaMalloc(&bits[dev & 63], 16));
     }
     return quant_tensor(x, x_is_bf16 != 0, n, codes, scale, bits[dev & 63], reinterpret_cast<cudaStream_t>(stream));
+}
+
+wb_status wb_quantise_e4m3_groups(const float* x, int64_t n_groups, int64_t group_elems, uint8_t* codes,
+                                  float* scales, wb_stream stream) {
+    if (!x || !codes || !scales) return fail(WB_ERR_INVALID_ARG, "wb_quantise_e4m3_groups: null argument");
+    if (n_groups < 1 || n_groups > 65535 || group_elems < 4 || group_elems % 4 || group_elems > ((int64_t)1 << 34))
+        return fail(WB_ERR_SHAPE, "wb_quantise_e4m3_groups: 1 <= n_groups <= 65535, group_elems a positive multiple of 4");
+    if (!aligned16(x) || !aligned16(codes)) return fail(WB_ERR_ALIGN, "wb_quantise_e4m3_groups: x and codes 16-byte aligned");
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    // scales[] first accumulates each group's amax (as bit patterns)
+    WB_CUDA(cudaMemsetAsync(scales, 0, sizeof(float) * (size_t)n_groups, s));
+    unsigned* amax = reinterpret_cast<unsigned*>(scales);
+    if (wb_status st = group_amax(x, n_groups, group_elems, amax, s)) return st;
+    // codes row by row, a group split into rows of at most 8192 values
+    int64_t R = group_elems;
+    if (R > 8192) {
+        R = 8192;
+        while (group_elems % R) R -= 4;
+    }
+    if (wb_status st = quant_groups(x, n_groups * (group_elems / R), R, group_elems / R, amax, codes, nullptr, s))
+        return st;
+    return scales_from_amax(scales, n_groups, s);
 }
 
 wb_status wb_dequantise_e4m3(const uint8_t* codes, const float* scale, int64_t n, float* out, wb_stream stream) {

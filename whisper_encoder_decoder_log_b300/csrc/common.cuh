@@ -114,17 +114,21 @@ WB_DEV uint64_t globaltimer_ns() {
     return t;
 }
 
-// Deadline helper: expired() is true once WB_WAIT_NS have passed since the
-// 64th poll.  The clock is read every 64 polls and never on the first one, so
-// a wait that is already satisfied costs no timer read.
+// Deadline helper: expired() is true once `limit` ns (WB_WAIT_NS unless
+// given) have passed since the 64th poll.  The clock is read every 64 polls
+// and never on the first one, so a wait that is already satisfied costs no
+// timer read.
 struct WaitClock {
     uint64_t t0 = 0;
     uint32_t n = 0;
+    uint64_t limit = WB_WAIT_NS;
+    WaitClock() = default;
+    WB_DEV explicit WaitClock(uint64_t ns) : limit(ns) {}
     WB_DEV bool expired() {
         if ((++n & 63u) != 0u) return false;
         const uint64_t t = globaltimer_ns();
         if (t0 == 0) { t0 = t; return false; }
-        return t - t0 > WB_WAIT_NS;
+        return t - t0 > limit;
     }
 };
 
@@ -153,15 +157,30 @@ WB_DEV void tma_load_2d(void* dst, const CUtensorMap* m, uint64_t* bar, int x, i
           "r"(x), "r"(y) : "memory");
 }
 
-// Same box into this CTA and every CTA of the cluster in cta_mask (same
-// shared-memory offsets); each destination's mbarrier at `bar`'s offset
-// receives the byte count.
-WB_DEV void tma_load_2d_mc(void* dst, const CUtensorMap* m, uint64_t* bar, int x, int y, uint16_t cta_mask) {
+// shared::cluster address of the object at `p`'s offset in CTA `rank` of the
+// cluster.
+WB_DEV uint32_t mapa_shared(const void* p, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
+    return r;
+}
+
+// Arrive (release at cluster scope) on an mbarrier given by its
+// shared::cluster address, possibly in another CTA of the cluster.
+WB_DEV void mbar_arrive_cluster(uint32_t bar_cluster) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster) : "memory");
+}
+
+// try_wait with acquire at cluster scope: for barriers that threads or the
+// tensor core of the peer CTA arrive on.
+WB_DEV bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
     asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
-        " [%0], [%1, {%3, %4}], [%2], %5;"
-        ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(m)), "r"(smem_u32(bar)),
-          "r"(x), "r"(y), "h"(cta_mask) : "memory");
+        "{\n .reg .pred p;\n"
+        " mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
+    return ok != 0;
 }
 
 WB_DEV uint32_t cluster_ctarank() {
@@ -245,12 +264,44 @@ WB_DEV void umma_commit(uint64_t* bar) {
         ::"r"(smem_u32(bar)) : "memory");
 }
 
-// Arrive on the mbarrier at `bar`'s offset in every CTA of cta_mask once all
-// earlier tcgen05 operations of this thread have completed.
-WB_DEV void umma_commit_mc(uint64_t* bar, uint16_t cta_mask) {
+// ---- CTA pairs (cta_group::2): one MMA spans the two CTAs of a cluster.
+// Allocation and release are collective: one warp of EACH CTA of the pair
+// executes them with the same column count; the returned address is the same
+// in both CTAs.
+WB_DEV void tmem_alloc_pair(uint32_t* dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;"
+                 ::"r"(smem_u32(dst_smem)), "r"(ncols) : "memory");
+}
+WB_DEV void tmem_relinquish_pair() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+WB_DEV void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;"
+                 ::"r"(taddr), "r"(ncols) : "memory");
+}
+// D[256 x N] (+)= A . B^T over the pair: each CTA holds 128 rows of A and N/2
+// rows of B at the same shared-memory offsets, and 128 lanes of D in its own
+// TMEM.  Issued by one thread of the leader CTA (rank 0).
+WB_DEV void umma_bf16_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                           uint32_t accumulate) {
     asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;"
-        ::"r"(smem_u32(bar)), "h"(cta_mask) : "memory");
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n}\n"
+        ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate) : "memory");
+}
+WB_DEV void umma_fp8_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                          uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n}\n"
+        ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate) : "memory");
+}
+// Arrive on the mbarrier at shared::cluster address `bar_cluster` (this CTA's
+// or the peer's) once all earlier pair MMAs of this thread have completed.
+WB_DEV void umma_commit_pair(uint32_t bar_cluster) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+        ::"r"(bar_cluster) : "memory");
 }
 
 WB_DEV void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }

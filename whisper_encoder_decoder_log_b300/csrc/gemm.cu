@@ -10,6 +10,8 @@
 //               and, from one thread, issues tcgen05.mma (M 128, N BN, K 16
 //               for bf16 / 32 for E4M3) and tcgen05.commit to release stages
 //               and to hand a finished accumulator to the epilogue.
+//               Large GEMMs run on CTA pairs (cta_group::2, M 256 over two
+//               SMs, each SM loading half of the B tile): see gemm_tc_kernel.
 //   warps 2-9   epilogue: two warps per TMEM lane quarter, alternate
 //               32-column chunks: tcgen05.ld, scale, bias, GELU, positional
 //               table, residual accumulate, store.
@@ -20,6 +22,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <atomic>
 #include <mutex>
 
 #include "common.cuh"
@@ -38,10 +41,11 @@ constexpr int kGroupM = 16;
 // global stores and reductions go out one 128-byte row segment at a time.
 constexpr int kEpiStageBytes = 8 * 32 * 32 * 4;
 
-template <int BN>
+// PAIR: each CTA of a pair holds half of the BN rows of B.
+template <int BN, bool PAIR = false>
 struct Cfg {
     static constexpr int A_BYTES = kBM * kRowBytes;
-    static constexpr int B_BYTES = BN * kRowBytes;
+    static constexpr int B_BYTES = (PAIR ? BN / 2 : BN) * kRowBytes;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int STAGES = (192 * 1024) / STAGE_BYTES > 8 ? 8 : (192 * 1024) / STAGE_BYTES;
     static constexpr int TMEM_COLS = 2 * BN;
@@ -59,6 +63,10 @@ struct GemmArgs {
     int stages;             // smem ring depth (<= the compile-time maximum)
     int w_const;            // the weight operand is constant: load it before the grid dependency wait
     int b_kwrap;
+    // Failure-detection test hook: when non-zero, the MMA issuer first waits
+    // this many ns on a barrier nothing arrives on, and takes the same
+    // give-up path as a pipeline wait that ran out.
+    uint64_t stall_ns;
     GemmEpi epi;
 };
 
@@ -283,62 +291,104 @@ __device__ __forceinline__ void split_range(const GemmArgs& a, int64_t t, int& k
     kb1 = (int)((int64_t)(ks + 1) * a.kb_all / a.ksplit);
 }
 
+// Fold the per-thread maxima of one warp's 32 consecutive rows into the
+// group maxima: the rows span at most two groups (amax_rows >= 32), so two
+// warp reductions and at most two atomics per warp and tile.
+__device__ __forceinline__ void epi_group_amax(unsigned* amax, int64_t group_rows, int64_t row, bool row_ok, float m) {
+    const int64_t grp = row_ok ? row / group_rows : -1;
+    const long long g0 = __shfl_sync(0xffffffffu, (long long)grp, 0);
+    if (g0 < 0) return;                       // lane 0 holds the warp's first row
+    const float m0 = warp_max(grp == g0 ? m : 0.f);
+    const float m1 = warp_max(grp == g0 + 1 ? m : 0.f);
+    if ((threadIdx.x & 31) == 0) {
+        atomicMax(amax + g0, __float_as_uint(m0));
+        if (m1 > 0.f) atomicMax(amax + g0 + 1, __float_as_uint(m1));
+    }
+}
+
 constexpr int kEpiWarps = 8;                       // two per TMEM lane quarter
 constexpr int kGemmThreads = 64 + 32 * kEpiWarps;  // producer + MMA + epilogue
 
-// PAIR: a cluster of two CTAs computes M tiles 2p and 2p+1 of the same N
-// tile in lockstep; each CTA loads half of the B tile and multicasts it to
-// both, so a k-block costs each SM's L2 feed A + B/2 instead of A + B.  The
-// stage's empty barrier then waits for both CTAs' MMAs.
+// PAIR: a cluster of two CTAs computes a 256 x BN tile with cta_group::2 MMAs:
+// CTA r of the pair holds rows [128 r, 128 r + 128) of A and rows
+// [BN/2 r, BN/2 r + BN/2) of B in its shared memory (each loaded by its own,
+// ordinary TMA copies) and the accumulator of its 128 rows in its TMEM.  One
+// thread of the leader CTA (rank 0) issues the MMAs, which read both CTAs'
+// shared memory, so a k-block costs each SM's L2 feed A + B/2 instead of
+// A + B.  Hand-offs across the pair:
+//   stage loaded   the peer's MMA warp waits on its own full barrier and
+//                  arrives on the leader's peer_full barrier;
+//   stage free     the leader's MMA commit arrives on both CTAs' empty
+//                  barriers (one commit per barrier);
+//   tile ready     likewise on both CTAs' accumulator-full barriers;
+//   tile drained   each peer epilogue warp arrives on the leader's
+//                  accumulator-empty barrier.
+// Every wait stays bounded; a CTA that gives up leaves its peer to time out
+// in turn, and both meet at the final cluster barrier before TMEM is released.
 template <int BN, bool FP8, bool SWAP, bool PAIR = false>
 __global__ void __launch_bounds__(kGemmThreads, SWAP ? 2 : 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUtensorMap tma_b,
                const GemmArgs args, unsigned* err) {
-    using C = Cfg<BN>;
+    using C = Cfg<BN, PAIR>;
     const int STAGES = args.stages;
-    constexpr uint32_t IDESC = UmmaIdesc<kBM, BN, FP8 ? 0 : 1>::value;
+    constexpr uint32_t IDESC = UmmaIdesc<PAIR ? 2 * kBM : kBM, BN, FP8 ? 0 : 1>::value;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     float* epi_stage = reinterpret_cast<float*>(smem + STAGES * C::STAGE_BYTES);
     uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + STAGES * C::STAGE_BYTES + kEpiStageBytes);
     uint64_t* empty_bar = full_bar + STAGES;
-    uint64_t* tfull_bar = empty_bar + STAGES;     // [2]
+    uint64_t* pfull_bar = empty_bar + STAGES;     // [STAGES] leader: the peer's half of a stage has landed
+    uint64_t* tfull_bar = pfull_bar + STAGES;     // [2]
     uint64_t* tempty_bar = tfull_bar + 2;         // [2]
     uint64_t* drain_bar = tempty_bar + 2;         // [1]
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain_bar + 1);
+    uint64_t* stall_bar = drain_bar + 1;          // [1] never arrived on (stall_ns)
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(stall_bar + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int rank = PAIR ? (int)cluster_ctarank() : 0;
-    const int64_t t_first = PAIR ? blockIdx.x / 2 : blockIdx.x;      // first tile (pair of M tiles) of this CTA
+    const bool leader = rank == 0;
+    const int64_t t_first = PAIR ? blockIdx.x / 2 : blockIdx.x;      // first tile (256-row tile when PAIR)
     const int64_t t_step = PAIR ? gridDim.x / 2 : gridDim.x;
-    // M tile of this CTA within tile t (a pair index when PAIR)
+    // M tile (128 rows) of this CTA within tile index mt
     auto my_mt = [&](int64_t mt) { return PAIR ? 2 * mt + rank : mt; };
+    // try_wait at cluster scope where the peer (or its tensor core) arrives
+    auto try_wait = [&](uint64_t* bar, uint32_t parity) {
+        return PAIR ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity);
+    };
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&full_bar[s], 1);
-            mbar_init(&empty_bar[s], PAIR ? 2 : 1);
+            mbar_init(&empty_bar[s], 1);
+            mbar_init(&pfull_bar[s], 1);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&tfull_bar[i], 1);
-            mbar_init(&tempty_bar[i], 32 * kEpiWarps);
+            // local epilogue threads, plus one arrival per peer epilogue warp
+            mbar_init(&tempty_bar[i], 32 * kEpiWarps + (PAIR ? kEpiWarps : 0));
         }
         mbar_init(drain_bar, 1);
+        mbar_init(stall_bar, 1);
         *abort_flag = 0;
         fence_barrier_init();
         tma_prefetch_desc(&tma_a);
         tma_prefetch_desc(&tma_b);
     }
     if (warp == 1) {
-        tmem_alloc(tmem_slot, C::TMEM_COLS);
-        tmem_relinquish();
+        if (PAIR) {
+            tmem_alloc_pair(tmem_slot, C::TMEM_COLS);
+            tmem_relinquish_pair();
+        } else {
+            tmem_alloc(tmem_slot, C::TMEM_COLS);
+            tmem_relinquish();
+        }
     }
     tc_fence_before();
     __syncthreads();
-    if (PAIR) cluster_sync_all();    // the peer's barriers exist before anything is multicast to them
+    if (PAIR) cluster_sync_all();    // both CTAs' barriers exist before either arrives on the other's
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     const bool producer = warp == 0 && lane == 0;
@@ -354,10 +404,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant_
                 unsigned char* sa = smem + stage * C::STAGE_BYTES;
                 const int kw = args.b_kwrap ? kx % args.b_kwrap : kx;
                 if (SWAP) tma_load_3d(sa, &tma_a, &full_bar[stage], kw, (int)(mt * kBM), 0);
-                else if (PAIR)   // this CTA's half of the B tile, into both CTAs
-                    tma_load_2d_mc(sa + C::A_BYTES + rank * (BN / 2) * kRowBytes, &tma_b, &full_bar[stage], kw,
-                                   n0 + rank * (BN / 2), (uint16_t)3);
-                else tma_load_2d(sa + C::A_BYTES, &tma_b, &full_bar[stage], kw, n0);
+                else tma_load_2d(sa + C::A_BYTES, &tma_b, &full_bar[stage], kw, n0 + (PAIR ? rank * (BN / 2) : 0));
             };
             // Constant weights do not depend on the kernels this one waits
             // for: the first ring stages fetch them before the wait, which
@@ -395,7 +442,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant_
                     if (it >= pre) {
                         bool got = false;
                         for (WaitClock clk; !clk.expired();) {
-                            if (mbar_try_wait(&empty_bar[stage], phase ^ 1)) { got = true; break; }
+                            if (try_wait(&empty_bar[stage], phase ^ 1)) { got = true; break; }
                             if (*abort_flag) break;
                         }
                         if (!got) {
@@ -422,18 +469,48 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant_
                 if ((issued >> s) & 1u) mbar_wait(&full_bar[s], (last_parity >> s) & 1u, err, WB_DEVERR_TIMEOUT_TMA);
         }
     } else if (warp == 1) {
-        if (lane == 0) {
+        if (lane == 0 && PAIR && !leader) {
+            // Peer: forward "stage landed" to the leader, stage by stage, in
+            // the producer's order.
+            const uint32_t pfull_leader = mapa_shared(pfull_bar, 0);
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            for (int64_t t = t_first; t < args.tiles && ok; t += t_step) {
+                int kb0, kb1;
+                split_range(args, t, kb0, kb1);
+                for (int kb = kb0; kb < kb1; ++kb) {
+                    bool got = false;
+                    for (WaitClock clk; !clk.expired();) {
+                        if (mbar_try_wait(&full_bar[stage], phase)) { got = true; break; }
+                        if (*abort_flag) break;
+                    }
+                    if (!got) { wb_set_error(err, WB_DEVERR_TIMEOUT_MMA); *abort_flag = 1; ok = false; break; }
+                    mbar_arrive_cluster(pfull_leader + 8u * (uint32_t)stage);
+                    if (++stage == STAGES) { stage = 0; phase ^= 1; }
+                }
+            }
+        } else if (lane == 0) {
+            // shared::cluster addresses of both CTAs' barriers (PAIR)
+            const uint32_t empty_c[2] = {PAIR ? mapa_shared(empty_bar, 0) : 0u, PAIR ? mapa_shared(empty_bar, 1) : 0u};
+            const uint32_t tfull_c[2] = {PAIR ? mapa_shared(tfull_bar, 0) : 0u, PAIR ? mapa_shared(tfull_bar, 1) : 0u};
             int stage = 0;
             uint32_t phase = 0;
             int local = 0;
             bool ok = true;
             bool any = false;
+            if (args.stall_ns) {
+                bool got = false;
+                for (WaitClock clk(args.stall_ns); !clk.expired();)
+                    if (mbar_try_wait(stall_bar, 0)) { got = true; break; }
+                if (!got) { wb_set_error(err, WB_DEVERR_TIMEOUT_MMA); *abort_flag = 1; ok = false; }
+            }
             for (int64_t t = t_first; t < args.tiles && ok; t += t_step, ++local) {
                 const int acc = local & 1;
                 const uint32_t aphase = (local >> 1) & 1;
                 bool got = false;
                 for (WaitClock clk; !clk.expired();) {
-                    if (mbar_try_wait(&tempty_bar[acc], aphase ^ 1)) { got = true; break; }
+                    if (try_wait(&tempty_bar[acc], aphase ^ 1)) { got = true; break; }
                     if (*abort_flag) break;
                 }
                 if (!got) { wb_set_error(err, WB_DEVERR_TIMEOUT_MMA); *abort_flag = 1; break; }
@@ -444,7 +521,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant_
                 for (int kb = 0; kb < kb1 - kb0; ++kb) {
                     got = false;
                     for (WaitClock clk; !clk.expired();) {
-                        if (mbar_try_wait(&full_bar[stage], phase)) { got = true; break; }
+                        if (mbar_try_wait(&full_bar[stage], phase) &&
+                            (!PAIR || mbar_try_wait_cluster(&pfull_bar[stage], phase))) { got = true; break; }
                         if (*abort_flag) break;
                     }
                     if (!got) { wb_set_error(err, WB_DEVERR_TIMEOUT_MMA); *abort_flag = 1; ok = false; break; }
@@ -456,20 +534,35 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant_
                         const uint64_t ad = umma_desc_sw128(a_addr + 32 * k);
                         const uint64_t bd = umma_desc_sw128(b_addr + 32 * k);
                         const uint32_t accum = (kb | k) ? 1u : 0u;
-                        if (FP8) umma_fp8(d_tmem, ad, bd, IDESC, accum);
-                        else umma_bf16(d_tmem, ad, bd, IDESC, accum);
+                        if (PAIR) {
+                            if (FP8) umma_fp8_pair(d_tmem, ad, bd, IDESC, accum);
+                            else umma_bf16_pair(d_tmem, ad, bd, IDESC, accum);
+                        } else {
+                            if (FP8) umma_fp8(d_tmem, ad, bd, IDESC, accum);
+                            else umma_bf16(d_tmem, ad, bd, IDESC, accum);
+                        }
                     }
                     any = true;
-                    if (PAIR) umma_commit_mc(&empty_bar[stage], (uint16_t)3);   // both CTAs' copies of the stage
-                    else umma_commit(&empty_bar[stage]);
+                    if (PAIR) {   // both CTAs' copies of the stage are free
+                        umma_commit_pair(empty_c[0] + 8u * (uint32_t)stage);
+                        umma_commit_pair(empty_c[1] + 8u * (uint32_t)stage);
+                    } else {
+                        umma_commit(&empty_bar[stage]);
+                    }
                     if (++stage == STAGES) { stage = 0; phase ^= 1; }
                 }
                 if (!ok) break;
-                umma_commit(&tfull_bar[acc]);
+                if (PAIR) {
+                    umma_commit_pair(tfull_c[0] + 8u * (uint32_t)acc);
+                    umma_commit_pair(tfull_c[1] + 8u * (uint32_t)acc);
+                } else {
+                    umma_commit(&tfull_bar[acc]);
+                }
             }
             // all issued MMAs complete before TMEM can be released
             if (any) {
-                umma_commit(drain_bar);
+                if (PAIR) umma_commit_pair(mapa_shared(drain_bar, 0));
+                else umma_commit(drain_bar);
                 mbar_wait(drain_bar, 0, err, WB_DEVERR_TIMEOUT_MMA);
             }
         }
@@ -478,13 +571,14 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant_
         // the two warps of a quarter take alternate 32-column chunks
         const int g = warp & 3;
         const int half = (warp - 2) >> 2;
+        const uint32_t tempty_leader = PAIR ? mapa_shared(tempty_bar, 0) : 0u;
         int local = 0;
         for (int64_t t = t_first; t < args.tiles; t += t_step, ++local) {
             const int acc = local & 1;
             const uint32_t aphase = (local >> 1) & 1;
             bool got = false;
             for (WaitClock clk; !clk.expired();) {
-                if (mbar_try_wait(&tfull_bar[acc], aphase)) { got = true; break; }
+                if (try_wait(&tfull_bar[acc], aphase)) { got = true; break; }
                 if (*abort_flag) break;
             }
             if (!got) { wb_set_error(err, WB_DEVERR_TIMEOUT_EPI); *abort_flag = 1; break; }
@@ -510,16 +604,16 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant_
                 continue;
             }
             const GemmEpi& e = args.epi;
-            // stores and reductions are staged; a residual update without
-            // split-K reads its destination and stays in the thread's row
-            // a residual update without split-K reads its destination: it
-            // stays in the thread's row, where 8 float4 loads go out at once
+            // fp32 stores and split-K reductions are staged; a residual update
+            // without split-K reads its destination: it stays in the thread's
+            // row, where 8 float4 loads go out at once
             const bool staged = e.mode == MODE_PLAIN &&
                                 (e.out_type == OUT_F32 || (e.out_type == OUT_F32_ACC && args.ksplit > 1));
             // bf16 rows go out as full 64-byte segments (8 rows per instruction)
             const bool staged16 = e.mode == MODE_PLAIN && e.out_type == OUT_BF16 && e.vec && args.ksplit == 1 &&
                                   (args.N & 7) == 0;
             float* stg = epi_stage + (warp - 2) * 32 * 32;
+            float tmax = 0.f;     // largest |v| of this thread's row in the tile (e.amax)
 #pragma unroll 1
             for (int c = half; c < BN / 32; c += 2) {
                 uint32_t raw[32];
@@ -561,7 +655,14 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant_
                 // fp32 output: transform in the thread's row, then transpose the
                 // 32 x 32 block through shared memory (16-byte chunks XOR-swizzled
                 // by row) and write one 128-byte row segment per instruction
-                if (row_ok && n0 < args.N) transform_f32(args, b, r, n0, v, (int)(t % args.ksplit));
+                if (row_ok && n0 < args.N) {
+                    transform_f32(args, b, r, n0, v, (int)(t % args.ksplit));
+                    if (e.amax) {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            if (n0 + j < args.N) tmax = fmaxf(tmax, fabsf(v[j]));
+                    }
+                }
 #pragma unroll
                 for (int q = 0; q < 8; ++q)
                     *reinterpret_cast<float4*>(stg + lane * 32 + ((q ^ (lane & 7)) << 2)) =
@@ -573,30 +674,38 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant_
                 const bool reduce = args.ksplit > 1;             // partial tiles of one output
                 float* ob = reinterpret_cast<float*>(e.out) + (b * obr + e.out_row_offset) * e.ldo + col;
                 if (col < args.N) {
-                    {
 #pragma unroll 4
-                        for (int rr = 0; rr < 32; ++rr) {
-                            if (rq + rr >= args.rows) break;
-                            const float x = stg[rr * 32 + ((((lane >> 2) ^ (rr & 7))) << 2) + (lane & 3)];
-                            float* dst = ob + (rq + rr) * e.ldo;
-                            if (reduce) atomicAdd(dst, x);   // result unused: a reduction
-                            else *dst = x;
-                        }
+                    for (int rr = 0; rr < 32; ++rr) {
+                        if (rq + rr >= args.rows) break;
+                        const float x = stg[rr * 32 + ((((lane >> 2) ^ (rr & 7))) << 2) + (lane & 3)];
+                        float* dst = ob + (rq + rr) * e.ldo;
+                        if (reduce) atomicAdd(dst, x);   // result unused: a reduction
+                        else *dst = x;
                     }
                 }
                 __syncwarp();
             }
+            if (e.amax) epi_group_amax(e.amax, e.amax_rows, b * args.rows + r, row_ok, tmax);
             tc_fence_before();
-            mbar_arrive(&tempty_bar[acc]);
+            if (!PAIR || leader) {
+                mbar_arrive(&tempty_bar[acc]);
+            } else {   // one arrival per peer warp on the leader's barrier, after all its lanes' loads
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cluster(tempty_leader + 8u * (uint32_t)acc);
+            }
         }
     }
     tc_fence_before();
     __syncthreads();
-    // neither CTA of a pair leaves while the other may still multicast into
-    // its shared memory or arrive on its barriers
+    // neither CTA of a pair releases TMEM (or leaves) while the leader's MMAs
+    // may still write the peer's TMEM or either CTA may arrive on the other's
+    // barriers
     if (PAIR) cluster_sync_all();
     tc_fence_after();
-    if (warp == 1) tmem_dealloc(tmem_base, C::TMEM_COLS);
+    if (warp == 1) {
+        if (PAIR) tmem_dealloc_pair(tmem_base, C::TMEM_COLS);
+        else tmem_dealloc(tmem_base, C::TMEM_COLS);
+    }
 }
 
 // ------------------------------------------------------------------ host: TMA
@@ -628,6 +737,9 @@ wb_status encode_map(CUtensorMap* m, const void* ptr, int rank, const uint64_t* 
 }
 
 int g_num_sms = 0;
+
+// One-shot failure-detection hook (wb_debug_stall_next_gemm).
+std::atomic<uint64_t> g_stall_next{0};
 
 }  // namespace
 
@@ -671,10 +783,11 @@ wb_status launch_tc(const GemmPlan& p, GemmArgs a, unsigned* err, cudaStream_t s
     return WB_OK;
 }
 
-// CTA pairs (clusters of two) sharing each B tile; a.tiles counts M-tile pairs.
+// CTA pairs (clusters of two, cta_group::2 MMAs over 256-row tiles); a.tiles
+// counts 256-row tiles.
 template <int BN, bool FP8>
 wb_status launch_tc_pair(const GemmPlan& p, GemmArgs a, unsigned* err, cudaStream_t s) {
-    using C = Cfg<BN>;
+    using C = Cfg<BN, true>;
     auto kern = gemm_tc_kernel<BN, FP8, false, true>;
     static bool attr_set[64] = {};
     int dev = 0;
@@ -809,7 +922,7 @@ wb_status gemm_run(const GemmPlan& p, const GemmEpi& epi, unsigned* err, cudaStr
         a.mt_total = a.mt_per_batch;
         a.nt_total = (a.rows + p.bn - 1) / p.bn;        // activation-row tiles
     } else if (p.pair) {
-        a.mt_per_batch = ((a.rows + kBM - 1) / kBM + 1) / 2;   // M-tile pairs
+        a.mt_per_batch = ((a.rows + kBM - 1) / kBM + 1) / 2;   // 256-row tiles
         a.mt_total = a.mt_per_batch;
         a.nt_total = (p.N + p.bn - 1) / p.bn;
     } else {
@@ -830,11 +943,14 @@ wb_status gemm_run(const GemmPlan& p, const GemmEpi& epi, unsigned* err, cudaStr
     a.kblocks = (kb_all + ksplit - 1) / ksplit;
     a.b_kwrap = (int)p.b_kwrap;
     a.w_const = p.w_const ? 1 : 0;
+    a.stall_ns = g_stall_next.exchange(0);
     a.epi = epi;
     const bool half = epi.out_type == OUT_BF16 || epi.out_type == OUT_BF16X2;
     a.epi.vec = aligned16(epi.out) && (epi.mode == MODE_CROSS_KV || (epi.ldo * (half ? 2 : 4)) % 16 == 0) &&
                 (epi.out_type != OUT_BF16X2 || (p.N * 2) % 16 == 0);
     if (epi.mode == MODE_CROSS_KV && !a.epi.vec) return fail(WB_ERR_ALIGN, "cross K/V output not 16-byte aligned");
+    if (epi.amax && (p.swap || epi.out_type != OUT_F32 || ksplit != 1 || epi.mode != MODE_PLAIN || epi.amax_rows < 32))
+        return fail(WB_ERR_INVALID_ARG, "GEMM group amax: fp32 output, no split-K, groups of >= 32 rows");
     if (a.tiles == 0 || a.kblocks == 0) return WB_OK;
     const bool small = a.rows * p.batches < 1024;
     const int slot = prof_begin(small ? WB_KERNEL_GEMM_SMALL : WB_KERNEL_GEMM, s);
@@ -986,3 +1102,10 @@ wb_status gemm_simt(const GemmOperand& A, bool a_bf16, const GemmOperand& B, boo
 }
 
 }  // namespace wb
+
+extern "C" wb_status wb_debug_stall_next_gemm(uint64_t limit_ns) {
+    if (limit_ns == 0 || limit_ns > 1000000000ull)
+        return wb::fail(WB_ERR_INVALID_ARG, "wb_debug_stall_next_gemm: limit must be in (0, 1e9] ns");
+    wb::g_stall_next.store(limit_ns);
+    return WB_OK;
+}

@@ -35,6 +35,11 @@ struct GemmEpi {
     int64_t ckv_chunks = 0;
     int64_t out_batch_rows = 0;      // 0: = rows_per_batch
     int out_row_offset = 0;
+    // With amax set (fp32 output, no split-K, tcgen05 path): the largest |v|
+    // of every group of amax_rows output rows (>= 32) is folded into
+    // amax[group] by atomic max over the bit patterns (zero it beforehand).
+    unsigned* amax = nullptr;
+    int64_t amax_rows = 0;
     int vec = 1;                     // set by the launcher: 16-byte stores allowed
 };
 
@@ -59,7 +64,7 @@ struct GemmPlan {
     bool fp8 = false;
     bool swap = false;     // small-M form: weights are the 128-row MMA operand
     bool w_const = false;  // the weight operand is not written by kernels this GEMM may overlap
-    bool pair = false;     // clusters of two CTAs share each B tile (TMA multicast)
+    bool pair = false;     // CTA pairs: cta_group::2 MMAs over 256-row tiles, each CTA loads half of B
     bool ok = false;
 };
 

@@ -39,8 +39,9 @@ constexpr int kMaxPos = 448;
 
 wb_status mel_launch(const float* audio, int64_t B, int n_mels, float* mel, cudaStream_t s);
 
-// mel [B, C, 3000] fp32 -> [B, 3002, C] (bf16 or fp32) with a zero row at
-// both ends of each chunk: the conv1 implicit-GEMM operand.
+// mel [B, C, 3000] fp32 -> [B, 3002, C] fp32, or [B, 3002, 2C] bf16 pairs
+// (hi | lo per row), with a zero row at both ends of each chunk: the conv1
+// implicit-GEMM operand.
 wb_status mel_transpose_pad(const float* mel, int64_t B, int C, void* out, bool bf16,
                             cudaStream_t s);
 

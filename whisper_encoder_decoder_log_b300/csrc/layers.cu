@@ -10,6 +10,8 @@
 // "Blazingly fast whisper transcriptions with Inference Endpoints",
 // "Inference Stack"; greedy choice follows the "thewhisper-large-v3-turbo"
 // model card, "NVIDIA Usage" (no sampling, one beam).
+#include <algorithm>
+
 #include "common.cuh"
 #include "prof.cuh"
 #include "layers.cuh"
@@ -23,11 +25,15 @@ constexpr int kMaxPerLane = 40;   // d <= 1280
 // gain and shift fetched together with the row so that one memory round trip
 // covers all three.  Optionally zeroes `zero` (n4 float4) on the side: the
 // next GEMM's split-K output, which would otherwise need a launch of its own.
+// LN_AMAX / LN_E4M3_GROUP: amax of every group of group_rows rows (one
+// chunk's GEMM input) in amax_bits; the first pass takes it, the second
+// quantises with it, both from the same arithmetic on the same row.
 template <int OUT, int VPL>
 __global__ void __launch_bounds__(128)
 layernorm_vec_kernel(const float* __restrict__ x, int64_t ld_x, int64_t rows, const float* __restrict__ g,
                      const float* __restrict__ b, void* __restrict__ out, int64_t ld_o, float* __restrict__ row_scale,
-                     float4* __restrict__ zero, int64_t zero_n4) {
+                     float4* __restrict__ zero, int64_t zero_n4, unsigned* __restrict__ amax_bits,
+                     int64_t group_rows) {
     griddep_wait();
     griddep_launch();
     if (zero) {
@@ -86,9 +92,18 @@ layernorm_vec_kernel(const float* __restrict__ x, int64_t ld_x, int64_t rows, co
                 *reinterpret_cast<uint2*>(o + d + c) = make_uint2(pack_bf16x2(r0, r1), pack_bf16x2(r2, r3));
             }
         }
-    } else {   // LN_E4M3: per-row scale amax / 448
+    } else if (OUT == LN_AMAX) {
         amax = warp_max(amax);
-        const float sc = amax > 0.f ? amax / 448.0f : 1.0f;
+        if (lane == 0) atomicMax(amax_bits + row / group_rows, __float_as_uint(amax));
+    } else {   // LN_E4M3: per-row scale amax / 448; LN_E4M3_GROUP: the group's
+        float sc;
+        if (OUT == LN_E4M3_GROUP) {
+            const float a = __uint_as_float(amax_bits[row / group_rows]);
+            sc = a > 0.f ? a / 448.0f : 1.0f;
+        } else {
+            amax = warp_max(amax);
+            sc = amax > 0.f ? amax / 448.0f : 1.0f;
+        }
         const float inv = 1.0f / sc;
         uint8_t* o = reinterpret_cast<uint8_t*>(out) + row * ld_o;
 #pragma unroll
@@ -246,46 +261,6 @@ __global__ void kv_append_kernel(const float* __restrict__ qkv, int64_t n_chunks
     }
 }
 
-// Per-row E4M3 quantisation of a bf16 matrix (FC2's input in mixed_fp8).
-__global__ void quant_rows_kernel(const __nv_bfloat16* __restrict__ x, int64_t rows, int K, uint8_t* __restrict__ q,
-                                  float* __restrict__ row_scale) {
-    griddep_wait();
-    griddep_launch();
-    const int64_t r = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
-    const int lane = threadIdx.x & 31;
-    if (r >= rows) return;
-    const __nv_bfloat16* xr = x + r * K;
-    float m = 0.f;
-    for (int i = lane * 8; i < K; i += 256) {
-        float v[8];
-        const uint4 a = *reinterpret_cast<const uint4*>(xr + i);
-        const uint32_t w[4] = {a.x, a.y, a.z, a.w};
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            v[2 * j] = __uint_as_float(w[j] << 16);
-            v[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
-        }
-#pragma unroll
-        for (int j = 0; j < 8; ++j) m = fmaxf(m, fabsf(v[j]));
-    }
-    m = warp_max(m);
-    const float sc = m > 0.f ? m / 448.0f : 1.0f;
-    const float inv = 1.0f / sc;
-    for (int i = lane * 8; i < K; i += 256) {
-        const uint4 a = *reinterpret_cast<const uint4*>(xr + i);
-        const uint32_t w[4] = {a.x, a.y, a.z, a.w};
-        uint32_t o[2];
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-            const float f0 = __uint_as_float(w[2 * j] << 16), f1 = __uint_as_float(w[2 * j] & 0xFFFF0000u);
-            const float f2 = __uint_as_float(w[2 * j + 1] << 16), f3 = __uint_as_float(w[2 * j + 1] & 0xFFFF0000u);
-            o[j] = (uint32_t)f2e4m3x2(f0 * inv, f1 * inv) | ((uint32_t)f2e4m3x2(f2 * inv, f3 * inv) << 16);
-        }
-        *reinterpret_cast<uint2*>(q + r * K + i) = make_uint2(o[0], o[1]);
-    }
-    if (lane == 0) row_scale[r] = sc;
-}
-
 // Per-row E4M3 quantisation of an fp32 matrix.
 __global__ void quant_rows_f32_kernel(const float* __restrict__ x, int64_t rows, int K, uint8_t* __restrict__ q,
                                       float* __restrict__ row_scale) {
@@ -309,6 +284,61 @@ __global__ void quant_rows_f32_kernel(const float* __restrict__ x, int64_t rows,
         *reinterpret_cast<uint32_t*>(q + r * K + i) = o;
     }
     if (lane == 0) row_scale[r] = sc;
+}
+
+// amax of each group of group_elems consecutive fp32 values: grid (slices,
+// groups), one atomic max per block.
+__global__ void __launch_bounds__(256)
+group_amax_kernel(const float* __restrict__ x, int64_t group_elems, unsigned* __restrict__ amax_bits) {
+    griddep_wait();
+    griddep_launch();
+    const int64_t grp = blockIdx.y;
+    const float4* p = reinterpret_cast<const float4*>(x + grp * group_elems);
+    const int64_t n4 = group_elems / 4;
+    float m = 0.f;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += (int64_t)gridDim.x * blockDim.x) {
+        const float4 a = p[i];
+        m = fmaxf(m, fmaxf(fmaxf(fabsf(a.x), fabsf(a.y)), fmaxf(fabsf(a.z), fabsf(a.w))));
+    }
+    m = warp_max(m);
+    __shared__ float red[8];
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float a = red[0];
+        for (int i = 1; i < 8; ++i) a = fmaxf(a, red[i]);
+        atomicMax(amax_bits + grp, __float_as_uint(a));
+    }
+}
+
+// E4M3 codes of fp32 rows with one scale per group of rows: one warp per row.
+__global__ void __launch_bounds__(256)
+quant_groups_kernel(const float* __restrict__ x, int64_t rows, int64_t K, int64_t group_rows,
+                    const unsigned* __restrict__ amax_bits, uint8_t* __restrict__ q, float* __restrict__ row_scale) {
+    griddep_wait();
+    griddep_launch();
+    const int64_t r = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (r >= rows) return;
+    const float a = __uint_as_float(amax_bits[r / group_rows]);
+    const float sc = a > 0.f ? a / 448.0f : 1.0f;
+    const float inv = 1.0f / sc;
+    const float4* xr = reinterpret_cast<const float4*>(x + r * K);
+    uint32_t* qr = reinterpret_cast<uint32_t*>(q + r * K);
+    for (int64_t i = lane; i < K / 4; i += 32) {
+        const float4 v = xr[i];
+        qr[i] = (uint32_t)f2e4m3x2(v.x * inv, v.y * inv) | ((uint32_t)f2e4m3x2(v.z * inv, v.w * inv) << 16);
+    }
+    if (row_scale && lane == 0) row_scale[r] = sc;
+}
+
+__global__ void scales_from_amax_kernel(float* __restrict__ a, int64_t n) {
+    griddep_wait();
+    griddep_launch();
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+        const float m = a[i];
+        a[i] = m > 0.f ? m / 448.0f : 1.0f;
+    }
 }
 
 // amax of a tensor (non-negative floats order like their bit patterns).
@@ -391,16 +421,21 @@ argmax_kernel(const float* __restrict__ logits, int64_t ld, int64_t rows, int V,
     }
 }
 
-// conv weight [O][C][3] -> GEMM operand [O][3][C] (k index = j * C + c)
+// conv weight [O][C][3] -> GEMM operand [O][3][C] (k index = j * C + c).
+// With dup, every tap j is stored twice ([o][j][hi | lo][c], k index
+// (2 j + half) C + c): the weights of a stem GEMM whose input rows carry each
+// frame as a bf16 pair (hi | lo).
 template <typename T>
-__global__ void conv_reorder_kernel(const T* __restrict__ w, int O, int C, T* __restrict__ out) {
+__global__ void conv_reorder_kernel(const T* __restrict__ w, int O, int C, int dup, T* __restrict__ out) {
     griddep_wait();
     griddep_launch();
-    const int64_t n = (int64_t)O * C * 3;
+    const int reps = dup ? 2 : 1;
+    const int64_t kk = (int64_t)3 * reps * C;
+    const int64_t n = (int64_t)O * kk;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t o = i / (3 * C);
-        const int rem = (int)(i % (3 * C));
-        const int j = rem / C, c = rem % C;
+        const int64_t o = i / kk;
+        const int rem = (int)(i % kk);
+        const int j = rem / (reps * C), c = rem % C;
         out[i] = w[(o * C + c) * 3 + j];
     }
 }
@@ -491,21 +526,24 @@ int grid_for(int64_t n, int threads) {
 
 template <int OUT>
 wb_status launch_ln_vec(int vpl, const float* x, int64_t ld_x, int64_t rows, const float* g, const float* b, void* out,
-                        int64_t ld_o, float* row_scale, float* zero, int64_t zero_n, cudaStream_t s) {
+                        int64_t ld_o, float* row_scale, float* zero, int64_t zero_n, cudaStream_t s,
+                        unsigned* amax_bits = nullptr, int64_t group_rows = 1) {
     const dim3 grid((unsigned)((rows + 3) / 4)), block(128);
     float4* z = reinterpret_cast<float4*>(zero);
     const int64_t z4 = zero ? zero_n / 4 : 0;
+#define WB_LN_ARGS x, ld_x, rows, g, b, out, ld_o, row_scale, z, z4, amax_bits, group_rows
     switch (vpl) {
-    case 1: return launch_k(layernorm_vec_kernel<OUT, 1>, grid, block, 0, s, x, ld_x, rows, g, b, out, ld_o, row_scale, z, z4) ? WB_ERR_CUDA : WB_OK;
-    case 2: return launch_k(layernorm_vec_kernel<OUT, 2>, grid, block, 0, s, x, ld_x, rows, g, b, out, ld_o, row_scale, z, z4) ? WB_ERR_CUDA : WB_OK;
-    case 3: return launch_k(layernorm_vec_kernel<OUT, 3>, grid, block, 0, s, x, ld_x, rows, g, b, out, ld_o, row_scale, z, z4) ? WB_ERR_CUDA : WB_OK;
-    case 4: return launch_k(layernorm_vec_kernel<OUT, 4>, grid, block, 0, s, x, ld_x, rows, g, b, out, ld_o, row_scale, z, z4) ? WB_ERR_CUDA : WB_OK;
-    case 5: return launch_k(layernorm_vec_kernel<OUT, 5>, grid, block, 0, s, x, ld_x, rows, g, b, out, ld_o, row_scale, z, z4) ? WB_ERR_CUDA : WB_OK;
-    case 6: return launch_k(layernorm_vec_kernel<OUT, 6>, grid, block, 0, s, x, ld_x, rows, g, b, out, ld_o, row_scale, z, z4) ? WB_ERR_CUDA : WB_OK;
-    case 8: return launch_k(layernorm_vec_kernel<OUT, 8>, grid, block, 0, s, x, ld_x, rows, g, b, out, ld_o, row_scale, z, z4) ? WB_ERR_CUDA : WB_OK;
-    case 10: return launch_k(layernorm_vec_kernel<OUT, 10>, grid, block, 0, s, x, ld_x, rows, g, b, out, ld_o, row_scale, z, z4) ? WB_ERR_CUDA : WB_OK;
+    case 1: return launch_k(layernorm_vec_kernel<OUT, 1>, grid, block, 0, s, WB_LN_ARGS) ? WB_ERR_CUDA : WB_OK;
+    case 2: return launch_k(layernorm_vec_kernel<OUT, 2>, grid, block, 0, s, WB_LN_ARGS) ? WB_ERR_CUDA : WB_OK;
+    case 3: return launch_k(layernorm_vec_kernel<OUT, 3>, grid, block, 0, s, WB_LN_ARGS) ? WB_ERR_CUDA : WB_OK;
+    case 4: return launch_k(layernorm_vec_kernel<OUT, 4>, grid, block, 0, s, WB_LN_ARGS) ? WB_ERR_CUDA : WB_OK;
+    case 5: return launch_k(layernorm_vec_kernel<OUT, 5>, grid, block, 0, s, WB_LN_ARGS) ? WB_ERR_CUDA : WB_OK;
+    case 6: return launch_k(layernorm_vec_kernel<OUT, 6>, grid, block, 0, s, WB_LN_ARGS) ? WB_ERR_CUDA : WB_OK;
+    case 8: return launch_k(layernorm_vec_kernel<OUT, 8>, grid, block, 0, s, WB_LN_ARGS) ? WB_ERR_CUDA : WB_OK;
+    case 10: return launch_k(layernorm_vec_kernel<OUT, 10>, grid, block, 0, s, WB_LN_ARGS) ? WB_ERR_CUDA : WB_OK;
     default: return WB_ERR_UNSUPPORTED;
     }
+#undef WB_LN_ARGS
 }
 
 bool ln_vec_ok(int d) { return d % 128 == 0 && (d / 128 <= 6 || d / 128 == 8 || d / 128 == 10); }
@@ -540,6 +578,55 @@ wb_status layernorm(const float* x, int64_t ld_x, int64_t rows, int d, const flo
     else if (mode == LN_BF16) WB_CUDA(launch_k(layernorm_kernel<LN_BF16>, dim3(grid), dim3(256), 0, s, x, ld_x, rows, d, g, b, out, ld_o, row_scale));
     else if (mode == LN_BF16X2) WB_CUDA(launch_k(layernorm_kernel<LN_BF16X2>, dim3(grid), dim3(256), 0, s, x, ld_x, rows, d, g, b, out, ld_o, row_scale));
     else WB_CUDA(launch_k(layernorm_kernel<LN_E4M3>, dim3(grid), dim3(256), 0, s, x, ld_x, rows, d, g, b, out, ld_o, row_scale));
+    WB_CUDA(cudaGetLastError());
+    return WB_OK;
+}
+
+wb_status layernorm_group_e4m3(const float* x, int64_t ld_x, int64_t rows, int d, const float* g, const float* b,
+                               int64_t group_rows, unsigned* amax_bits, uint8_t* out, int64_t ld_o, float* row_scale,
+                               cudaStream_t s) {
+    if (rows <= 0) return WB_OK;
+    if (!ln_vec_ok(d) || !aligned16(x) || !aligned16(g) || !aligned16(b) || !aligned16(out) || ld_x % 4 || ld_o % 16)
+        return fail(WB_ERR_UNSUPPORTED, "grouped E4M3 LayerNorm needs d % 128 == 0 and 16-byte aligned rows");
+    if (group_rows < 1) return fail(WB_ERR_SHAPE, "grouped E4M3 LayerNorm: group_rows < 1");
+    const int vpl = d / 128;
+    wb_status st = launch_ln_vec<LN_AMAX>(vpl, x, ld_x, rows, g, b, nullptr, 0, nullptr, nullptr, 0, s, amax_bits,
+                                          group_rows);
+    if (!st)
+        st = launch_ln_vec<LN_E4M3_GROUP>(vpl, x, ld_x, rows, g, b, out, ld_o, row_scale, nullptr, 0, s, amax_bits,
+                                          group_rows);
+    if (st) return fail(st, "grouped LayerNorm launch failed");
+    WB_CUDA(cudaGetLastError());
+    return WB_OK;
+}
+
+wb_status group_amax(const float* x, int64_t n_groups, int64_t group_elems, unsigned* amax_bits, cudaStream_t s) {
+    if (n_groups <= 0 || group_elems <= 0) return WB_OK;
+    if (group_elems % 4 || !aligned16(x)) return fail(WB_ERR_ALIGN, "group amax: groups of whole 16-byte vectors");
+    if (n_groups > 65535) return fail(WB_ERR_SHAPE, "group amax: at most 65535 groups");
+    // enough blocks to fill the SMs, at most one per 256 vectors of a group
+    const int64_t want = std::max<int64_t>(1, (148 * 8 + n_groups - 1) / n_groups);
+    const int64_t slices = std::max<int64_t>(1, std::min<int64_t>(want, (group_elems / 4 + 255) / 256));
+    WB_CUDA(launch_k(group_amax_kernel, dim3((unsigned)slices, (unsigned)n_groups), dim3(256), 0, s, x, group_elems,
+                     amax_bits));
+    WB_CUDA(cudaGetLastError());
+    return WB_OK;
+}
+
+wb_status quant_groups(const float* x, int64_t rows, int64_t K, int64_t group_rows, const unsigned* amax_bits,
+                       uint8_t* q, float* row_scale, cudaStream_t s) {
+    if (rows <= 0 || K <= 0) return WB_OK;
+    if (K % 4 || !aligned16(x) || !aligned16(q)) return fail(WB_ERR_ALIGN, "group quantiser: rows of 16-byte vectors");
+    if (group_rows < 1) return fail(WB_ERR_SHAPE, "group quantiser: group_rows < 1");
+    WB_CUDA(launch_k(quant_groups_kernel, dim3((unsigned)((rows + 7) / 8)), dim3(256), 0, s, x, rows, K, group_rows,
+                     amax_bits, q, row_scale));
+    WB_CUDA(cudaGetLastError());
+    return WB_OK;
+}
+
+wb_status scales_from_amax(float* a, int64_t n, cudaStream_t s) {
+    if (n <= 0) return WB_OK;
+    WB_CUDA(launch_k(scales_from_amax_kernel, dim3(grid_for(n, 256)), dim3(256), 0, s, a, n));
     WB_CUDA(cudaGetLastError());
     return WB_OK;
 }
@@ -584,15 +671,6 @@ wb_status kv_append(const float* qkv, int64_t n_chunks, int P, int p0, int d, in
     const unsigned grid = (unsigned)(n_chunks * P);
     if (fp8) WB_CUDA(launch_k(kv_append_kernel<true>, dim3(grid), dim3(256), 0, s, qkv, n_chunks, P, p0, d, H, layer, cache, off, len, k_scale, v_scale, err, pos_dev));
     else WB_CUDA(launch_k(kv_append_kernel<false>, dim3(grid), dim3(256), 0, s, qkv, n_chunks, P, p0, d, H, layer, cache, off, len, k_scale, v_scale, err, pos_dev));
-    WB_CUDA(cudaGetLastError());
-    return WB_OK;
-}
-
-wb_status quant_rows(const void* x_bf16, int64_t rows, int K, uint8_t* q, float* row_scale, cudaStream_t s) {
-    if (rows <= 0) return WB_OK;
-    if (K % 256) return fail(WB_ERR_SHAPE, "row quantiser needs K % 256 == 0");
-    WB_CUDA(launch_k(quant_rows_kernel, dim3((unsigned)((rows + 7) / 8)), dim3(256), 0, s, reinterpret_cast<const __nv_bfloat16*>(x_bf16), rows, K,
-                                                                   q, row_scale));
     WB_CUDA(cudaGetLastError());
     return WB_OK;
 }
@@ -657,10 +735,10 @@ wb_status argmax_tokens(const float* logits, int64_t ld, int64_t rows, int V, in
     return WB_OK;
 }
 
-wb_status conv_reorder(const void* w, int O, int C, bool bf16, void* out, cudaStream_t s) {
-    const int64_t n = (int64_t)O * C * 3;
-    if (bf16) WB_CUDA(launch_k(conv_reorder_kernel<__nv_bfloat16>, dim3(grid_for(n, 256)), dim3(256), 0, s, reinterpret_cast<const __nv_bfloat16*>(w), O, C, reinterpret_cast<__nv_bfloat16*>(out)));
-    else WB_CUDA(launch_k(conv_reorder_kernel<float>, dim3(grid_for(n, 256)), dim3(256), 0, s, reinterpret_cast<const float*>(w), O, C, reinterpret_cast<float*>(out)));
+wb_status conv_reorder(const void* w, int O, int C, bool bf16, void* out, cudaStream_t s, bool dup) {
+    const int64_t n = (int64_t)O * C * 3 * (dup ? 2 : 1);
+    if (bf16) WB_CUDA(launch_k(conv_reorder_kernel<__nv_bfloat16>, dim3(grid_for(n, 256)), dim3(256), 0, s, reinterpret_cast<const __nv_bfloat16*>(w), O, C, dup ? 1 : 0, reinterpret_cast<__nv_bfloat16*>(out)));
+    else WB_CUDA(launch_k(conv_reorder_kernel<float>, dim3(grid_for(n, 256)), dim3(256), 0, s, reinterpret_cast<const float*>(w), O, C, dup ? 1 : 0, reinterpret_cast<float*>(out)));
     WB_CUDA(cudaGetLastError());
     return WB_OK;
 }

@@ -8,13 +8,34 @@
 namespace wb {
 
 // LN_BF16X2 writes hi = bf16(y) at column c and lo = bf16(y - hi) at d + c.
-enum LnOut : int { LN_F32 = 0, LN_BF16 = 1, LN_E4M3 = 2, LN_BF16X2 = 3 };
+// LN_AMAX writes nothing but the amax of every group of rows (see
+// layernorm_group_e4m3); LN_E4M3_GROUP quantises with that group's scale.
+enum LnOut : int { LN_F32 = 0, LN_BF16 = 1, LN_E4M3 = 2, LN_BF16X2 = 3, LN_AMAX = 4, LN_E4M3_GROUP = 5 };
 
 // With zero set, zero[0 .. zero_n) is cleared by the same launch (the next
 // GEMM's split-K output).
 wb_status layernorm(const float* x, int64_t ld_x, int64_t rows, int d, const float* g, const float* b, LnOut mode,
                     void* out, int64_t ld_o, float* row_scale, cudaStream_t s, float* zero = nullptr,
                     int64_t zero_n = 0);
+// LayerNorm into E4M3 with one scale per group of group_rows consecutive rows
+// (one chunk's GEMM input): a first pass takes each group's amax of the
+// normalised values into amax_bits[group] (zero beforehand; non-negative
+// floats as their bit patterns), a second recomputes the rows and writes
+// codes of y * fp32(1 / s), s = amax / 448 (1 when amax is 0), and
+// row_scale[row] = s.  Needs d % 128 == 0.
+wb_status layernorm_group_e4m3(const float* x, int64_t ld_x, int64_t rows, int d, const float* g, const float* b,
+                               int64_t group_rows, unsigned* amax_bits, uint8_t* out, int64_t ld_o, float* row_scale,
+                               cudaStream_t s);
+// amax of each group of group_elems consecutive fp32 values (group_elems % 4
+// == 0, x 16-byte aligned) into amax_bits[group] (atomic max: zero before).
+wb_status group_amax(const float* x, int64_t n_groups, int64_t group_elems, unsigned* amax_bits, cudaStream_t s);
+// E4M3 codes of fp32 rows x [rows, K] (K % 4 == 0) with one scale per group of
+// group_rows rows, s = amax_bits[group] / 448 (1 when 0); row_scale[row] = s
+// when row_scale is non-null.
+wb_status quant_groups(const float* x, int64_t rows, int64_t K, int64_t group_rows, const unsigned* amax_bits,
+                       uint8_t* q, float* row_scale, cudaStream_t s);
+// scale[g] = amax / 448 (1 when 0) in place over an array that holds amax bits.
+wb_status scales_from_amax(float* amax_then_scale, int64_t n, cudaStream_t s);
 // Positions come from *pos_dev when it is non-null (graph replay), else p0.
 wb_status embed(const int32_t* tokens, int64_t rows, int P, int p0, int d, const void* E, const void* Pos, bool bf16,
                 int vocab, float* x, unsigned* err, cudaStream_t s, const int* pos_dev = nullptr,
@@ -27,8 +48,7 @@ wb_status kv_append(const float* qkv, int64_t n_chunks, int P, int p0, int d, in
 wb_status gelu_post(float* x, int64_t rows, int N, void* out_bf16x2, cudaStream_t s);
 // *pos_dev = value, or += value when add.
 wb_status set_pos(int* pos_dev, int value, bool add, cudaStream_t s);
-wb_status quant_rows(const void* x_bf16, int64_t rows, int K, uint8_t* q, float* row_scale, cudaStream_t s);
-// Same from an fp32 matrix.
+// E4M3 codes of an fp32 matrix with one scale amax / 448 per row.
 wb_status quant_rows_f32(const float* x, int64_t rows, int K, uint8_t* q, float* row_scale, cudaStream_t s);
 wb_status quant_tensor(const void* x, bool bf16, int64_t n, uint8_t* q, float* scale, unsigned* scratch_bits,
                        cudaStream_t s);
@@ -40,7 +60,9 @@ wb_status cross_kv_quant(const void* tmp, int64_t gB, int64_t B, int64_t g0, int
                          float* scale, cudaStream_t s);
 wb_status argmax_tokens(const float* logits, int64_t ld, int64_t rows, int V, int32_t* tokens, const int32_t* len,
                         const int* pos_dev, int pos_host, cudaStream_t s);
-wb_status conv_reorder(const void* w, int O, int C, bool bf16, void* out, cudaStream_t s);
+// conv weight [O][C][3] -> [O][3][C]; dup: [O][3][2][C] (each tap twice, for
+// stem inputs that carry a bf16 pair per value)
+wb_status conv_reorder(const void* w, int O, int C, bool bf16, void* out, cudaStream_t s, bool dup = false);
 wb_status gather_rows(const float* x, int64_t rows, int d, int64_t stride_rows, int64_t first, float* out,
                       cudaStream_t s);
 

@@ -303,6 +303,9 @@ struct DeviceTables {
 std::mutex g_tab_mu;
 DeviceTables g_tabs[64];
 
+// bf16 output rows carry each value as a pair: [hi (C) | lo (C)] with
+// hi = bf16(x), lo = bf16(x - hi), so the stem GEMM keeps ~16 bits of the
+// fp32 mel.
 __global__ void transpose_pad_kernel(const float* __restrict__ mel, int C, void* __restrict__ out,
                                      bool bf16) {
     griddep_wait();
@@ -322,9 +325,15 @@ __global__ void transpose_pad_kernel(const float* __restrict__ mel, int C, void*
         const int r = r0 + rr;
         if (r >= kFrames + 2) break;
         for (int c = threadIdx.x; c < C; c += 32) {
-            const int64_t idx = (b * (kFrames + 2) + r) * (int64_t)C + c;
-            if (bf16) reinterpret_cast<__nv_bfloat16*>(out)[idx] = __float2bfloat16_rn(tile[rr][c]);
-            else reinterpret_cast<float*>(out)[idx] = tile[rr][c];
+            if (bf16) {
+                const int64_t idx = (b * (kFrames + 2) + r) * (int64_t)(2 * C) + c;
+                const float x = tile[rr][c];
+                const __nv_bfloat16 hi = __float2bfloat16_rn(x);
+                reinterpret_cast<__nv_bfloat16*>(out)[idx] = hi;
+                reinterpret_cast<__nv_bfloat16*>(out)[idx + C] = __float2bfloat16_rn(x - __bfloat162float(hi));
+            } else {
+                reinterpret_cast<float*>(out)[(b * (kFrames + 2) + r) * (int64_t)C + c] = tile[rr][c];
+            }
         }
     }
 }
