@@ -32,21 +32,29 @@ N_FRAMES = 3000
 
 # ------------------------------------------------------------------ chunking
 
-def split_into_chunks(audio: np.ndarray, offsets, samples):
+def split_into_chunks(audio: np.ndarray, offsets, samples, overlap: int = 0):
     """Cut each request into 30 s chunks, zero-padding its last chunk.
 
     [WB] "Batch Transcription": every input is split into 30-second chunks and
-    all chunks go through one generate pass.  Chunk k of a request holds
-    samples [480000 k, 480000 (k+1)) of that request; the samples past its end
-    are zero.  Returns (chunks [n,480000] float64, req_of_chunk int32,
+    all chunks go through one generate pass.  With ``overlap`` samples
+    ([WB] "GPU Mel Spectrogram", ``process_chunks(..., overlap_s)``;
+    [TWT] ``overlap_seconds``), consecutive chunks of a request start
+    480000 - overlap samples apart and share ``overlap`` samples; the last
+    chunk is the first that reaches the request's end.  Chunk k holds samples
+    [k stride, k stride + 480000) of its request; samples past the end are
+    zero.  Returns (chunks [n,480000] float64, req_of_chunk int32,
     index_in_req int32, valid_samples int32).
     """
+    stride = CHUNK - int(overlap)
+    if not 0 <= int(overlap) < CHUNK:
+        raise ValueError("overlap must be in [0, 480000)")
     chunks, req, idx, valid = [], [], [], []
     for r, (o, s) in enumerate(zip(offsets, samples)):
-        n = (int(s) + CHUNK - 1) // CHUNK
+        s = int(s)
+        n = 1 + (max(0, s - CHUNK) + stride - 1) // stride
         for k in range(n):
-            lo = k * CHUNK
-            hi = min(int(s), lo + CHUNK)
+            lo = k * stride
+            hi = min(s, lo + CHUNK)
             c = np.zeros(CHUNK, dtype=np.float64)
             c[: hi - lo] = audio[int(o) + lo: int(o) + hi]
             chunks.append(c)

@@ -13,6 +13,9 @@ Readings:
     and V over 1500 encoder positions (bf16, or float8 when the cross K/V are
     stored as E4M3) plus its float8 self-attention K and V over its own decode
     length L_c, plus its token row (448 int32);
+  * overlapping windows: chunk k of a request starts k (480000 - overlap)
+    samples in; a request's transcript joins its chunks' tokens, dropping the
+    longest prefix of each chunk that repeats the end of the text so far;
   * several GPUs: contiguous ranges of chunks in request order, balanced on
     decode length plus a fixed per-chunk share for the mel and encoder (each
     chunk is transcribed on exactly one GPU; no step needs another GPU's data);
@@ -31,16 +34,34 @@ N_CTX = 1500
 MAX_POS = 448
 
 
-def chunk_table(req_samples):
-    """(req_of_chunk, index_in_req, valid_samples) as int32 arrays."""
+def chunk_table(req_samples, overlap: int = 0):
+    """(req_of_chunk, index_in_req, valid_samples) as int32 arrays; chunk k of
+    a request starts at k (480000 - overlap) (see oracle.mel.split_into_chunks)."""
+    stride = CHUNK - int(overlap)
     req, idx, valid = [], [], []
     for r, s in enumerate(np.asarray(req_samples, dtype=np.int64)):
-        n = int((s + CHUNK - 1) // CHUNK)
+        n = 1 + (max(0, int(s) - CHUNK) + stride - 1) // stride
         for k in range(n):
             req.append(r)
             idx.append(k)
-            valid.append(int(min(CHUNK, s - CHUNK * k)))
+            valid.append(int(min(CHUNK, s - stride * k)))
     return (np.array(req, np.int32), np.array(idx, np.int32), np.array(valid, np.int32))
+
+
+def stitch(rows):
+    """One request's transcript (token ids) from its chunks' generated tokens,
+    in chunk order.  Overlapping windows transcribe the shared audio twice, so
+    the next chunk's tokens are joined after removing the longest prefix of
+    them that equals a suffix of the transcript so far; with no such prefix
+    the tokens are simply appended (token ids only: no timestamps)."""
+    out = []
+    for row in rows:
+        row = [int(t) for t in row]
+        k = min(len(out), len(row))
+        while k > 0 and out[len(out) - k:] != row[:k]:
+            k -= 1
+        out.extend(row[k:])
+    return np.array(out, np.int32)
 
 
 def chunk_state_bytes(d_model: int, dec_layers: int, length: int, cross_bytes: int = 2) -> int:

@@ -104,3 +104,53 @@ def test_shard_requests_rechunk_to_the_same_chunks():
         assert rreq.size == c1 - c0
         assert np.array_equal(rvalid, valid[c0:c1])
         assert np.array_equal(offs[rreq] + ridx.astype(np.int64) * plan.CHUNK, start[c0:c1])
+
+
+@pytest.mark.parametrize("overlap", [0, 16000, 160000, 479999])
+def test_overlapping_chunk_table_covers_each_request(overlap):
+    samples = np.array([1, 480000, 480001, 960000 - overlap, 2_345_678, 31 * 16000], np.int64)
+    req, idx, valid = plan.chunk_table(samples, overlap)
+    stride = plan.CHUNK - overlap
+    for r, s in enumerate(samples):
+        ks = idx[req == r]
+        n = ks.size
+        assert np.array_equal(ks, np.arange(n))
+        # brute force: the fewest windows of 480000 samples, stride apart, reaching the end
+        m = 1
+        while (m - 1) * stride + plan.CHUNK < s:
+            m += 1
+        assert n == m
+        v = valid[req == r]
+        assert np.array_equal(v, np.minimum(plan.CHUNK, s - stride * ks))
+        assert (v > 0).all()
+
+
+def test_overlapping_chunks_share_their_samples():
+    from oracle import mel as omel
+    rng = np.random.default_rng(8)
+    samples = np.array([1_000_000, 700_000], np.int64)
+    offs = np.array([0, 1_000_000], np.int64)
+    audio = rng.normal(size=int(samples.sum()))
+    ov = 16000
+    chunks, req, idx, valid = omel.split_into_chunks(audio, offs, samples, overlap=ov)
+    for c in range(len(req) - 1):
+        if req[c] == req[c + 1]:
+            assert np.array_equal(chunks[c][plan.CHUNK - ov:], chunks[c + 1][:ov])
+    assert np.array_equal(chunks[0], audio[:plan.CHUNK])
+
+
+def test_stitch_removes_the_repeated_overlap_once():
+    a, b, c = [5, 6, 7, 8], [7, 8, 9, 10], [1, 2]
+    assert plan.stitch([a, b]).tolist() == [5, 6, 7, 8, 9, 10]       # suffix [7, 8] = prefix of b
+    assert plan.stitch([a, c]).tolist() == a + c                     # no overlap: concatenation
+    assert plan.stitch([a, [6, 7, 8]]).tolist() == a                 # fully repeated: nothing new
+    assert plan.stitch([[], a, []]).tolist() == a
+    assert plan.stitch([[3, 3, 3], [3, 3, 4]]).tolist() == [3, 3, 3, 4]   # the longest overlap wins
+    rng = np.random.default_rng(9)
+    for _ in range(200):                     # planted overlaps on random rows
+        x = rng.integers(0, 5, size=rng.integers(0, 12)).tolist()
+        k = int(rng.integers(0, len(x) + 1))
+        y = x[len(x) - k:] + rng.integers(0, 5, size=rng.integers(0, 6)).tolist()
+        out = plan.stitch([x, y]).tolist()
+        best = max(j for j in range(min(len(x), len(y)) + 1) if x[len(x) - j:] == y[:j])
+        assert out == x + y[best:]
