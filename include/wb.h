@@ -196,9 +196,10 @@ WB_API size_t wb_decoder_workspace_size(const wb_model* model, int64_t B,
  * decoder layer from enc ([dev] [B, 1500, d], wb_encode's output) into the
  * workspace ("whisper-blaze 0.1.8", "Direct Kernel API", decoder_cross_attn:
  * K/V come from the encoder and are computed once per chunk).  With
- * kv_fp8 = WB_KV_FP8_CROSS they are computed 32 chunks at a time into a bf16
- * scratch area of the workspace and stored as E4M3 with one scale per
- * (chunk, layer, K|V); wb_decoder_workspace_size includes that scratch.
+ * kv_fp8 = WB_KV_FP8_CROSS they are computed 16 chunks at a time into an
+ * fp32 scratch area of the workspace and stored as E4M3 with one scale per
+ * (chunk, layer, K|V), each value rounded once from fp32;
+ * wb_decoder_workspace_size includes that scratch.
  *   tokens [dev] int32 [B, 448]  token matrix the decoder reads and writes
  *     (kept by reference).  Row c receives chunk c's tokens, position p in
  *     column p.
@@ -278,6 +279,47 @@ WB_API wb_status wb_transcribe_batch(wb_model* model, const float* audio,
                               void* workspace, size_t workspace_bytes,
                               int32_t* n_waves_out, wb_stream stream);
 
+/*
+ * Overlapping windows ("whisper-blaze 0.1.8", "GPU Mel Spectrogram":
+ * process_chunks(..., overlap_s); "thewhisper-large-v3-turbo": overlap_seconds
+ * when long audio is split into windows).  With overlap_samples in
+ * [0, 480000), chunk k of a request starts k * (480000 - overlap_samples)
+ * samples in and holds the next 480000 samples (zero past the request's
+ * end); a request of s samples has 1 + ceil(max(0, s - 480000) / stride)
+ * chunks.  overlap_samples = 0 is the plain chunking of wb_transcribe_batch.
+ *
+ * wb_chunk_count: number of chunks of the batch (host only), -1 on bad input.
+ * wb_transcribe_workspace_size_overlap / wb_transcribe_batch_overlap: as the
+ *   calls without _overlap, on that chunking (chunk_len and the token rows
+ *   follow the same chunk order).
+ */
+WB_API int64_t wb_chunk_count(int32_t n_req, const int64_t* req_samples, int64_t overlap_samples);
+WB_API size_t wb_transcribe_workspace_size_overlap(const wb_model* model, int32_t n_req,
+                                                   const int64_t* req_samples, const int32_t* chunk_len,
+                                                   uint64_t wave_budget_bytes, int64_t overlap_samples);
+WB_API wb_status wb_transcribe_batch_overlap(wb_model* model, const float* audio, const int64_t* req_offset,
+                                             const int64_t* req_samples, int32_t n_req, int64_t overlap_samples,
+                                             const int32_t* prefix, const int32_t* chunk_len, int32_t* tokens,
+                                             uint64_t wave_budget_bytes, void* workspace, size_t workspace_bytes,
+                                             int32_t* n_waves_out, wb_stream stream);
+
+/*
+ * One transcript per request from its chunks' token rows (host only).
+ * Overlapping windows transcribe their shared audio twice, so each chunk's
+ * generated tokens (columns prefix_len .. chunk_len - 1 of its row) are joined
+ * to the request's text after dropping the longest prefix of them that
+ * repeats the end of the text so far; with no such prefix they are appended
+ * whole.  Token ids only: there are no timestamps to align on.
+ *   tokens [host] int32 [n_chunks, 448] (wb_transcribe_batch_overlap's rows,
+ *          copied to the host), chunk_len [host] int32 [n_chunks]
+ *   out [host] int32 [out_cap]: request r's text is
+ *          out[out_offset[r] .. out_offset[r + 1]); out_offset [host] int64
+ *          [n_req + 1].  WB_ERR_SHAPE when out_cap is too small.
+ */
+WB_API wb_status wb_stitch_tokens(int32_t n_req, const int64_t* req_samples, int64_t overlap_samples,
+                                  const int32_t* tokens, const int32_t* chunk_len, int32_t prefix_len,
+                                  int32_t* out, int64_t out_cap, int64_t* out_offset);
+
 /* Wave plan alone (host only): wave_of_chunk[host] int32 [n_chunks],
  * order[host] int32 [n_chunks] chunk indices in decode order. */
 WB_API wb_status wb_plan_waves(const wb_model_desc* desc, int32_t n_chunks,
@@ -331,13 +373,17 @@ WB_API wb_status wb_quantise_e4m3(const void* x, int32_t x_is_bf16, int64_t n,
  * cudaMalloc/cudaFree is not acceptable, or hosts that forbid allocation after
  * start-up.  The pages have no counterpart to this entry point.
  * It allocates nothing: its reduction scratch (one partial maximum per block
- * of 16384 elements) is a fixed 16 KB array in the library's device image,
- * held by every GPU that loads the library until the process exits.
- *   n <= 2^26 (67108864) elements; larger n returns WB_ERR_SHAPE.
+ * of 16384 elements) is a fixed array of 4160 floats (16.6 KB) in the
+ * library's device image, held by every GPU that loads the library until the
+ * process exits.
+ *   n <= 2^26 (67108864) elements; larger n returns WB_ERR_SHAPE; n == 0
+ *   writes scale 1 (x and codes may then be null).
  * All calls share that array: calls whose kernels overlap on the GPU (e.g. on
  * two unordered streams) race; calls ordered on one stream are safe.  The
- * first call on a device looks the array's address up (cudaGetSymbolAddress);
- * make that first call before any stream capture.
+ * first call in a CUDA context looks the array's address up
+ * (cudaGetSymbolAddress) and keeps it for that context; make that first call
+ * before any stream capture.  After cudaDeviceReset (a new context on the
+ * device) the next call looks it up again, so the same rule applies to it.
  */
 WB_API wb_status wb_quantise_e4m3_static(const void* x, int32_t x_is_bf16, int64_t n,
                                          uint8_t* codes, float* scale, wb_stream stream);

@@ -55,6 +55,11 @@ _SIGS = {
     "wb_transcribe_workspace_size": (_SZ, [_VP, _I32, _VP, _VP, _U64]),
     "wb_transcribe_batch": (ctypes.c_int, [_VP, _VP, _VP, _VP, _I32, _VP, _VP, _VP, _U64, _VP, _SZ, _VP, _VP]),
     "wb_plan_waves": (ctypes.c_int, [ctypes.POINTER(ModelDesc), _I32, _VP, _U64, _VP, _VP, _VP]),
+    "wb_chunk_count": (_I64, [_I32, _VP, _I64]),
+    "wb_transcribe_workspace_size_overlap": (_SZ, [_VP, _I32, _VP, _VP, _U64, _I64]),
+    "wb_transcribe_batch_overlap": (ctypes.c_int, [_VP, _VP, _VP, _VP, _I32, _I64, _VP, _VP, _VP, _U64, _VP, _SZ,
+                                                   _VP, _VP]),
+    "wb_stitch_tokens": (ctypes.c_int, [_I32, _VP, _I64, _VP, _VP, _I32, _VP, _I64, _VP]),
     "wb_shard_batch": (ctypes.c_int, [_I32, _VP, _VP, _VP, _I32, _I32, _VP, _VP, _VP, _VP, _VP]),
     "wb_quantise_e4m3": (ctypes.c_int, [_VP, _I32, _I64, _VP, _VP, _VP]),
     "wb_dequantise_e4m3": (ctypes.c_int, [_VP, _VP, _I64, _VP, _VP]),
@@ -223,6 +228,47 @@ def wb_transcribe_batch(model: int, audio, req_offset, req_samples, prefix, chun
                                      _p(workspace), workspace.numel() * workspace.element_size(),
                                      ctypes.addressof(nw), _stream(stream)))
     return nw.value
+
+
+def wb_chunk_count(req_samples, overlap: int = 0) -> int:
+    rs, rsp = _host_arr(req_samples, np.int64)
+    n = lib().wb_chunk_count(rs.size, rsp, overlap)
+    if n < 0:
+        raise WBError(-2, "bad requests or overlap")
+    return n
+
+
+def wb_transcribe_workspace_size_overlap(model: int, req_samples, chunk_len, budget: int, overlap: int) -> int:
+    rs, rsp = _host_arr(req_samples, np.int64)
+    cl, clp = _host_arr(chunk_len, np.int32)
+    return lib().wb_transcribe_workspace_size_overlap(model, rs.size, rsp, clp, budget, overlap)
+
+
+def wb_transcribe_batch_overlap(model: int, audio, req_offset, req_samples, overlap: int, prefix, chunk_len, tokens,
+                                budget: int, workspace, stream=None) -> int:
+    ro, rop = _host_arr(req_offset, np.int64)
+    rs, rsp = _host_arr(req_samples, np.int64)
+    pf, pfp = _host_arr(prefix, np.int32)
+    cl, clp = _host_arr(chunk_len, np.int32)
+    _need(audio, "float32", "audio")
+    _need(tokens, "int32", "tokens")
+    nw = _I32(0)
+    _check(lib().wb_transcribe_batch_overlap(model, _p(audio), rop, rsp, rs.size, overlap, pfp, clp, _p(tokens), budget,
+                                             _p(workspace), workspace.numel() * workspace.element_size(),
+                                             ctypes.addressof(nw), _stream(stream)))
+    return nw.value
+
+
+def wb_stitch_tokens(req_samples, overlap: int, tokens, chunk_len, prefix_len: int = 4):
+    """Per-request transcripts (list of int32 arrays) from host token rows [n_chunks, 448]."""
+    rs, rsp = _host_arr(req_samples, np.int64)
+    tk, tkp = _host_arr(tokens, np.int32)
+    cl, clp = _host_arr(chunk_len, np.int32)
+    cap = int(np.maximum(cl - prefix_len, 0).sum())
+    out = np.zeros(max(cap, 1), np.int32)
+    off = np.zeros(rs.size + 1, np.int64)
+    _check(lib().wb_stitch_tokens(rs.size, rsp, overlap, tkp, clp, prefix_len, out.ctypes.data, cap, off.ctypes.data))
+    return [out[off[r]:off[r + 1]].copy() for r in range(rs.size)]
 
 
 def wb_plan_waves(desc: ModelDesc, chunk_len, budget: int):

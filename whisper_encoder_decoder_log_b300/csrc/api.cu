@@ -408,7 +408,7 @@ struct wb_decoder {
     cudaStream_t cap_stream = nullptr; // graphs are captured here (capture runs nothing)
     // device buffers carved from the workspace
     void* crosskv = nullptr;
-    void* ckv_tmp = nullptr;           // bf16 cross K/V of one chunk group before E4M3 rounding
+    void* ckv_tmp = nullptr;           // fp32 cross K/V of one chunk group before E4M3 rounding
     float* cscale = nullptr;           // E4M3 cross K/V scales [layer][K|V][chunk]
     void* cache = nullptr;
     float* kscale = nullptr;
@@ -432,7 +432,7 @@ namespace wb {
 namespace {
 
 constexpr int kMaxPrefix = 32;
-constexpr int64_t kCrossGroup = 32;   // chunks per E4M3 cross K/V precompute group
+constexpr int64_t kCrossGroup = 16;   // chunks per E4M3 cross K/V precompute group
 
 struct DecLayout {
     size_t total = 0;
@@ -447,7 +447,7 @@ size_t carve_decoder(const wb_model* m, int64_t B, const int32_t* len, wb_decode
     const int64_t R = B * kMaxPrefix;
     const bool c8 = m->desc.kv_fp8 == WB_KV_FP8_CROSS;
     void* crosskv = c.take<uint8_t>((size_t)Ld * B * 2 * kCtx * d * (c8 ? 1 : act));
-    void* ckv_tmp = c8 ? c.take<uint8_t>((size_t)Ld * std::min<int64_t>(B, kCrossGroup) * 2 * kCtx * d * 2) : nullptr;
+    void* ckv_tmp = c8 ? c.take<float>((size_t)Ld * std::min<int64_t>(B, kCrossGroup) * 2 * kCtx * d) : nullptr;
     float* cscale = c8 ? c.take<float>((size_t)std::max(1, Ld) * 2 * B) : nullptr;
     int64_t cache_elems = 0;
     for (int64_t i = 0; i < B; ++i) cache_elems += (int64_t)Ld * 2 * H * len[i] * 64;
@@ -1025,15 +1025,15 @@ wb_status wb_decoder_init(wb_model* m, int64_t B, const int32_t* len, const void
         ep.ckv_chunks = B;
         if (wb_status st = linear(m, L, ep, s)) return fail_free(st);
     } else if (Ld > 0) {
-        // E4M3 cross K/V: per group of chunks, the bf16 projection into a
+        // E4M3 cross K/V: per group of chunks, the fp32 projection into a
         // scratch area, then one amax / 448 scale and the codes per (chunk,
-        // layer, K|V) tensor
+        // layer, K|V) tensor, rounded once from fp32
         for (int64_t g0 = 0; g0 < B; g0 += kCrossGroup) {
             const int64_t gB = std::min<int64_t>(kCrossGroup, B - g0);
             Lin L;
             L.a = reinterpret_cast<const __nv_bfloat16*>(enc) + g0 * kCtx * d;
             L.rows = gB * kCtx; L.lda = d; L.w = m->W("dec.0.ck.w"); L.N = (int64_t)Ld * 2 * d; L.K = d;
-            GemmEpi ep = epi_out(dec->ckv_tmp, 0, OUT_BF16, m->V("dec.0.ck.b"));
+            GemmEpi ep = epi_out(dec->ckv_tmp, 0, OUT_F32, m->V("dec.0.ck.b"));
             ep.mode = MODE_CROSS_KV;
             ep.ckv_d = d;
             ep.ckv_heads = H;
@@ -1269,26 +1269,52 @@ static size_t transcribe_ws(const wb_model* m, int64_t max_wave, const std::vect
     return align_up(c.cur, 256);
 }
 
+// Chunk k of request r starts k * stride samples in (stride = 480000 -
+// overlap) and holds min(480000, samples_r - k * stride) real samples; a
+// request has 1 + ceil(max(0, samples_r - 480000) / stride) chunks.
 static bool chunk_table(int32_t n_req, const int64_t* req_samples, std::vector<int32_t>& req, std::vector<int64_t>& idx,
-                        std::vector<int32_t>& valid) {
+                        std::vector<int32_t>& valid, int64_t overlap = 0) {
+    const int64_t stride = kChunkSamples - overlap;
+    if (overlap < 0 || stride < 1) return false;
     for (int32_t r = 0; r < n_req; ++r) {
         if (req_samples[r] < 1) return false;
-        const int64_t n = (req_samples[r] + kChunkSamples - 1) / kChunkSamples;
+        const int64_t n = 1 + (std::max<int64_t>(0, req_samples[r] - kChunkSamples) + stride - 1) / stride;
         for (int64_t k = 0; k < n; ++k) {
             req.push_back(r);
             idx.push_back(k);
-            valid.push_back((int32_t)std::min<int64_t>(kChunkSamples, req_samples[r] - k * kChunkSamples));
+            valid.push_back((int32_t)std::min<int64_t>(kChunkSamples, req_samples[r] - k * stride));
         }
     }
     return true;
 }
 
+int64_t wb_chunk_count(int32_t n_req, const int64_t* req_samples, int64_t overlap_samples) {
+    if (n_req < 1 || !req_samples) return -1;
+    std::vector<int32_t> req, valid;
+    std::vector<int64_t> idx;
+    if (!chunk_table(n_req, req_samples, req, idx, valid, overlap_samples)) return -1;
+    return (int64_t)req.size();
+}
+
+static size_t transcribe_ws_size(const wb_model* m, int32_t n_req, const int64_t* req_samples, const int32_t* chunk_len,
+                                 uint64_t budget, int64_t overlap);
+
 size_t wb_transcribe_workspace_size(const wb_model* m, int32_t n_req, const int64_t* req_samples,
                                     const int32_t* chunk_len, uint64_t budget) {
+    return transcribe_ws_size(m, n_req, req_samples, chunk_len, budget, 0);
+}
+
+size_t wb_transcribe_workspace_size_overlap(const wb_model* m, int32_t n_req, const int64_t* req_samples,
+                                            const int32_t* chunk_len, uint64_t budget, int64_t overlap_samples) {
+    return transcribe_ws_size(m, n_req, req_samples, chunk_len, budget, overlap_samples);
+}
+
+static size_t transcribe_ws_size(const wb_model* m, int32_t n_req, const int64_t* req_samples, const int32_t* chunk_len,
+                                 uint64_t budget, int64_t overlap) {
     if (!m || n_req < 1 || !req_samples || !chunk_len) return 0;
     std::vector<int32_t> req, valid;
     std::vector<int64_t> idx;
-    if (!chunk_table(n_req, req_samples, req, idx, valid)) return 0;
+    if (!chunk_table(n_req, req_samples, req, idx, valid, overlap)) return 0;
     std::vector<int32_t> lens(chunk_len, chunk_len + req.size());
     std::vector<std::vector<int32_t>> waves;
     bool too_big = false;
@@ -1299,10 +1325,33 @@ size_t wb_transcribe_workspace_size(const wb_model* m, int32_t n_req, const int6
     return transcribe_ws(m, mw, waves, lens, nullptr, 0, nullptr, nullptr);
 }
 
+static wb_status transcribe_impl(wb_model* m, const float* audio, const int64_t* req_offset, const int64_t* req_samples,
+                                 int32_t n_req, const int32_t* prefix, const int32_t* chunk_len, int32_t* tokens,
+                                 uint64_t budget, void* workspace, size_t ws_bytes, int32_t* n_waves_out,
+                                 wb_stream stream, int64_t overlap);
+
 wb_status wb_transcribe_batch(wb_model* m, const float* audio, const int64_t* req_offset, const int64_t* req_samples,
                               int32_t n_req, const int32_t* prefix, const int32_t* chunk_len, int32_t* tokens,
                               uint64_t budget, void* workspace, size_t ws_bytes, int32_t* n_waves_out,
                               wb_stream stream) {
+    return transcribe_impl(m, audio, req_offset, req_samples, n_req, prefix, chunk_len, tokens, budget, workspace,
+                           ws_bytes, n_waves_out, stream, 0);
+}
+
+wb_status wb_transcribe_batch_overlap(wb_model* m, const float* audio, const int64_t* req_offset,
+                                      const int64_t* req_samples, int32_t n_req, int64_t overlap_samples,
+                                      const int32_t* prefix, const int32_t* chunk_len, int32_t* tokens, uint64_t budget,
+                                      void* workspace, size_t ws_bytes, int32_t* n_waves_out, wb_stream stream) {
+    if (overlap_samples < 0 || overlap_samples >= kChunkSamples)
+        return fail(WB_ERR_SHAPE, "wb_transcribe_batch_overlap: overlap must be in [0, 480000)");
+    return transcribe_impl(m, audio, req_offset, req_samples, n_req, prefix, chunk_len, tokens, budget, workspace,
+                           ws_bytes, n_waves_out, stream, overlap_samples);
+}
+
+static wb_status transcribe_impl(wb_model* m, const float* audio, const int64_t* req_offset, const int64_t* req_samples,
+                                 int32_t n_req, const int32_t* prefix, const int32_t* chunk_len, int32_t* tokens,
+                                 uint64_t budget, void* workspace, size_t ws_bytes, int32_t* n_waves_out,
+                                 wb_stream stream, int64_t overlap) {
     if (!m || !audio || !req_offset || !req_samples || !prefix || !chunk_len || !tokens || !workspace)
         return fail(WB_ERR_INVALID_ARG, "wb_transcribe_batch: null argument");
     if (n_req < 1) return fail(WB_ERR_SHAPE, "wb_transcribe_batch: n_req < 1");
@@ -1312,7 +1361,9 @@ wb_status wb_transcribe_batch(wb_model* m, const float* audio, const int64_t* re
         if (prefix[i] < 0 || prefix[i] >= m->desc.vocab) return fail(WB_ERR_SHAPE, "wb_transcribe_batch: prefix id");
     std::vector<int32_t> req, valid;
     std::vector<int64_t> idx;
-    if (!chunk_table(n_req, req_samples, req, idx, valid)) return fail(WB_ERR_SHAPE, "wb_transcribe_batch: empty request");
+    if (!chunk_table(n_req, req_samples, req, idx, valid, overlap))
+        return fail(WB_ERR_SHAPE, "wb_transcribe_batch: empty request");
+    const int64_t stride = kChunkSamples - overlap;
     const int32_t n = (int32_t)req.size();
     std::vector<int32_t> lens(chunk_len, chunk_len + n);
     for (int32_t c = 0; c < n; ++c)
@@ -1336,7 +1387,7 @@ wb_status wb_transcribe_batch(wb_model* m, const float* audio, const int64_t* re
         std::vector<int32_t> hvalid(nw), hdst(nw), wl(nw);
         for (int64_t i = 0; i < nw; ++i) {
             const int32_t c = w[i];
-            hsrc[i] = req_offset[req[c]] + idx[c] * kChunkSamples;
+            hsrc[i] = req_offset[req[c]] + idx[c] * stride;
             hvalid[i] = valid[c];
             hdst[i] = c;
             wl[i] = lens[c];
@@ -1377,6 +1428,39 @@ wb_status wb_transcribe_batch(wb_model* m, const float* audio, const int64_t* re
     }
     if (n_waves_out) *n_waves_out = (int32_t)waves.size();
     return wb_sync_status(m, stream);
+}
+
+wb_status wb_stitch_tokens(int32_t n_req, const int64_t* req_samples, int64_t overlap_samples, const int32_t* tokens,
+                           const int32_t* chunk_len, int32_t prefix_len, int32_t* out, int64_t out_cap,
+                           int64_t* out_offset) {
+    if (n_req < 1 || !req_samples || !tokens || !chunk_len || !out || !out_offset)
+        return fail(WB_ERR_INVALID_ARG, "wb_stitch_tokens: null argument");
+    if (prefix_len < 0 || prefix_len > kMaxPos) return fail(WB_ERR_SHAPE, "wb_stitch_tokens: bad prefix_len");
+    std::vector<int32_t> req, valid;
+    std::vector<int64_t> idx;
+    if (!chunk_table(n_req, req_samples, req, idx, valid, overlap_samples))
+        return fail(WB_ERR_SHAPE, "wb_stitch_tokens: bad requests or overlap");
+    int64_t pos = 0;
+    size_t c = 0;
+    for (int32_t r = 0; r < n_req; ++r) {
+        out_offset[r] = pos;
+        const int64_t start = pos;
+        for (; c < req.size() && req[c] == r; ++c) {
+            const int32_t L = chunk_len[c];
+            if (L < prefix_len || L > kMaxPos) return fail(WB_ERR_SHAPE, "wb_stitch_tokens: chunk_len out of range");
+            const int32_t* row = tokens + (int64_t)c * kMaxPos + prefix_len;
+            const int64_t n = L - prefix_len;
+            // longest prefix of this row that repeats the end of the text so far
+            int64_t k = std::min<int64_t>(pos - start, n);
+            for (; k > 0; --k)
+                if (std::equal(row, row + k, out + pos - k)) break;
+            if (pos + (n - k) > out_cap) return fail(WB_ERR_SHAPE, "wb_stitch_tokens: out_cap too small");
+            std::copy(row + k, row + n, out + pos);
+            pos += n - k;
+        }
+    }
+    out_offset[n_req] = pos;
+    return WB_OK;
 }
 
 wb_status wb_quantise_e4m3(const void* x, int32_t x_is_bf16, int64_t n, uint8_t* codes, float* scale, wb_stream stream) {

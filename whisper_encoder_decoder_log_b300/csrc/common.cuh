@@ -157,6 +157,25 @@ WB_DEV void tma_load_2d(void* dst, const CUtensorMap* m, uint64_t* bar, int x, i
           "r"(x), "r"(y) : "memory");
 }
 
+// CTA-pair forms (cta_group::2): the box lands in this CTA's shared memory
+// and its byte count goes to the mbarrier at shared::cluster address
+// `bar_cluster`, which may lie in the peer CTA of the pair (the pair's MMA
+// issuer waits on one barrier for both CTAs' halves of a stage).
+WB_DEV void tma_load_2d_pair(void* dst, const CUtensorMap* m, uint32_t bar_cluster, int x, int y) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
+        " [%0], [%1, {%3, %4}], [%2];"
+        ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(m)), "r"(bar_cluster),
+          "r"(x), "r"(y) : "memory");
+}
+WB_DEV void tma_load_3d_pair(void* dst, const CUtensorMap* m, uint32_t bar_cluster, int x, int y, int z) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
+        " [%0], [%1, {%3, %4, %5}], [%2];"
+        ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(m)), "r"(bar_cluster),
+          "r"(x), "r"(y), "r"(z) : "memory");
+}
+
 // shared::cluster address of the object at `p`'s offset in CTA `rank` of the
 // cluster.
 WB_DEV uint32_t mapa_shared(const void* p, uint32_t rank) {

@@ -193,6 +193,12 @@ __device__ __forceinline__ void store_chunk(const GemmArgs& a, int64_t b, int64_
         const int64_t l = n0 / two_d, rem = n0 % two_d;
         const int64_t kv = rem / e.ckv_d, h = (rem % e.ckv_d) / 64, c0 = n0 % 64;
         const int64_t off = ((((l * e.ckv_chunks + ch) * 2 + kv) * e.ckv_heads + h) * kCtx + s) * 64 + c0;
+        if (e.out_type == OUT_F32) {
+            float4* d4 = reinterpret_cast<float4*>(reinterpret_cast<float*>(e.out) + off);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) d4[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+            return;
+        }
         __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(e.out) + off;
         uint4* d4 = reinterpret_cast<uint4*>(dst);
 #pragma unroll
@@ -311,13 +317,14 @@ constexpr int kGemmThreads = 64 + 32 * kEpiWarps;  // producer + MMA + epilogue
 
 // PAIR: a cluster of two CTAs computes a 256 x BN tile with cta_group::2 MMAs:
 // CTA r of the pair holds rows [128 r, 128 r + 128) of A and rows
-// [BN/2 r, BN/2 r + BN/2) of B in its shared memory (each loaded by its own,
-// ordinary TMA copies) and the accumulator of its 128 rows in its TMEM.  One
-// thread of the leader CTA (rank 0) issues the MMAs, which read both CTAs'
-// shared memory, so a k-block costs each SM's L2 feed A + B/2 instead of
-// A + B.  Hand-offs across the pair:
-//   stage loaded   the peer's MMA warp waits on its own full barrier and
-//                  arrives on the leader's peer_full barrier;
+// [BN/2 r, BN/2 r + BN/2) of B in its shared memory (each CTA's own TMA
+// copies, not shared with the other) and the accumulator of its 128 rows in
+// its TMEM.  One thread of the leader CTA (rank 0) issues the MMAs, which
+// read both CTAs' shared memory, so a k-block costs each SM's L2 feed
+// A + B/2 instead of A + B.  Hand-offs across the pair:
+//   stage loaded   both CTAs' copies of a stage count their bytes on the
+//                  leader's full barrier (cta_group::2 copies), which the
+//                  leader arms for both halves;
 //   stage free     the leader's MMA commit arrives on both CTAs' empty
 //                  barriers (one commit per barrier);
 //   tile ready     likewise on both CTAs' accumulator-full barriers;
@@ -338,8 +345,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant_
     float* epi_stage = reinterpret_cast<float*>(smem + STAGES * C::STAGE_BYTES);
     uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + STAGES * C::STAGE_BYTES + kEpiStageBytes);
     uint64_t* empty_bar = full_bar + STAGES;
-    uint64_t* pfull_bar = empty_bar + STAGES;     // [STAGES] leader: the peer's half of a stage has landed
-    uint64_t* tfull_bar = pfull_bar + STAGES;     // [2]
+    uint64_t* tfull_bar = empty_bar + STAGES;     // [2]
     uint64_t* tempty_bar = tfull_bar + 2;         // [2]
     uint64_t* drain_bar = tempty_bar + 2;         // [1]
     uint64_t* stall_bar = drain_bar + 1;          // [1] never arrived on (stall_ns)
@@ -363,7 +369,6 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant_
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&full_bar[s], 1);
             mbar_init(&empty_bar[s], 1);
-            mbar_init(&pfull_bar[s], 1);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&tfull_bar[i], 1);
@@ -399,12 +404,20 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant_
 
     if (warp == 0) {
         if (lane == 0) {
+            // PAIR: every copy of the pair counts on the leader's full barrier
+            const uint32_t full_leader = PAIR ? mapa_shared(full_bar, 0) : 0u;
+            // Arm a stage: the leader expects both CTAs' bytes.
+            auto arm = [&](int stage) {
+                if (!PAIR || leader) mbar_arrive_expect_tx(&full_bar[stage], (PAIR ? 2 : 1) * C::STAGE_BYTES);
+            };
             // Weight half of one stage (swapped: A holds the weights, else B).
             auto load_w = [&](int stage, int64_t mt, int n0, int kx) {
                 unsigned char* sa = smem + stage * C::STAGE_BYTES;
                 const int kw = args.b_kwrap ? kx % args.b_kwrap : kx;
                 if (SWAP) tma_load_3d(sa, &tma_a, &full_bar[stage], kw, (int)(mt * kBM), 0);
-                else tma_load_2d(sa + C::A_BYTES, &tma_b, &full_bar[stage], kw, n0 + (PAIR ? rank * (BN / 2) : 0));
+                else if (PAIR) tma_load_2d_pair(sa + C::A_BYTES, &tma_b, full_leader + 8u * (uint32_t)stage, kw,
+                                                n0 + rank * (BN / 2));
+                else tma_load_2d(sa + C::A_BYTES, &tma_b, &full_bar[stage], kw, n0);
             };
             // Constant weights do not depend on the kernels this one waits
             // for: the first ring stages fetch them before the wait, which
@@ -417,7 +430,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant_
                     int kb0, kb1;
                     split_range(args, t, kb0, kb1);
                     for (int kb = kb0; kb < kb1 && pre < STAGES; ++kb, ++pre) {
-                        mbar_arrive_expect_tx(&full_bar[pre], C::STAGE_BYTES);
+                        arm(pre);
                         load_w(pre, mt, (int)(nt * BN), kb * (FP8 ? 128 : 64));
                     }
                 }
@@ -451,12 +464,13 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant_
                             ok = false;
                             break;
                         }
-                        mbar_arrive_expect_tx(&full_bar[stage], C::STAGE_BYTES);
+                        arm(stage);
                         load_w(stage, mt, n0, kx);
                     }
                     // activation half: swapped -> B (BN activation rows), else A
                     unsigned char* sa = smem + stage * C::STAGE_BYTES;
                     if (SWAP) tma_load_2d(sa + C::A_BYTES, &tma_b, &full_bar[stage], kx, n0);
+                    else if (PAIR) tma_load_3d_pair(sa, &tma_a, full_leader + 8u * (uint32_t)stage, kx, r0, b);
                     else tma_load_3d(sa, &tma_a, &full_bar[stage], kx, r0, b);
                     issued |= 1u << stage;
                     last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
@@ -464,33 +478,16 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant_
                 }
             }
 
-            // never leave TMA writes in flight into this CTA's shared memory
-            for (int s = 0; s < STAGES; ++s)
-                if ((issued >> s) & 1u) mbar_wait(&full_bar[s], (last_parity >> s) & 1u, err, WB_DEVERR_TIMEOUT_TMA);
+            // never leave TMA writes in flight into shared memory: the leader's
+            // full barriers count both CTAs' copies (the peer leaves only
+            // after the leader, at the final cluster barrier)
+            if (!PAIR || leader)
+                for (int s = 0; s < STAGES; ++s)
+                    if ((issued >> s) & 1u)
+                        mbar_wait(&full_bar[s], (last_parity >> s) & 1u, err, WB_DEVERR_TIMEOUT_TMA);
         }
     } else if (warp == 1) {
-        if (lane == 0 && PAIR && !leader) {
-            // Peer: forward "stage landed" to the leader, stage by stage, in
-            // the producer's order.
-            const uint32_t pfull_leader = mapa_shared(pfull_bar, 0);
-            int stage = 0;
-            uint32_t phase = 0;
-            bool ok = true;
-            for (int64_t t = t_first; t < args.tiles && ok; t += t_step) {
-                int kb0, kb1;
-                split_range(args, t, kb0, kb1);
-                for (int kb = kb0; kb < kb1; ++kb) {
-                    bool got = false;
-                    for (WaitClock clk; !clk.expired();) {
-                        if (mbar_try_wait(&full_bar[stage], phase)) { got = true; break; }
-                        if (*abort_flag) break;
-                    }
-                    if (!got) { wb_set_error(err, WB_DEVERR_TIMEOUT_MMA); *abort_flag = 1; ok = false; break; }
-                    mbar_arrive_cluster(pfull_leader + 8u * (uint32_t)stage);
-                    if (++stage == STAGES) { stage = 0; phase ^= 1; }
-                }
-            }
-        } else if (lane == 0) {
+        if (lane == 0 && (!PAIR || leader)) {
             // shared::cluster addresses of both CTAs' barriers (PAIR)
             const uint32_t empty_c[2] = {PAIR ? mapa_shared(empty_bar, 0) : 0u, PAIR ? mapa_shared(empty_bar, 1) : 0u};
             const uint32_t tfull_c[2] = {PAIR ? mapa_shared(tfull_bar, 0) : 0u, PAIR ? mapa_shared(tfull_bar, 1) : 0u};
@@ -521,8 +518,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant_
                 for (int kb = 0; kb < kb1 - kb0; ++kb) {
                     got = false;
                     for (WaitClock clk; !clk.expired();) {
-                        if (mbar_try_wait(&full_bar[stage], phase) &&
-                            (!PAIR || mbar_try_wait_cluster(&pfull_bar[stage], phase))) { got = true; break; }
+                        if (try_wait(&full_bar[stage], phase)) { got = true; break; }
                         if (*abort_flag) break;
                     }
                     if (!got) { wb_set_error(err, WB_DEVERR_TIMEOUT_MMA); *abort_flag = 1; ok = false; break; }

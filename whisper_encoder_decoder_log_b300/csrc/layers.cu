@@ -475,25 +475,22 @@ __global__ void gelu_post_kernel(float* __restrict__ x, int64_t rows, int N, __n
 }
 
 // E4M3 cross-attention K/V: one CTA per (chunk of the group, K|V, layer)
-// tensor of n bf16 values (contiguous in both layouts): amax over the tensor,
+// tensor of n fp32 values (contiguous in both layouts): amax over the tensor,
 // scale = amax / 448 (1 for an all-zero tensor), then codes of x * (1 / scale).
 __global__ void __launch_bounds__(512)
-cross_kv_quant_kernel(const __nv_bfloat16* __restrict__ tmp, int64_t n, int gB, int64_t B, int64_t g0,
+cross_kv_quant_kernel(const float* __restrict__ tmp, int64_t n, int gB, int64_t B, int64_t g0,
                       uint8_t* __restrict__ out, float* __restrict__ scale) {
     griddep_wait();
     griddep_launch();
     __shared__ float red[16];
     const int64_t c = blockIdx.x, kv = blockIdx.y, l = blockIdx.z;
-    const uint4* src = reinterpret_cast<const uint4*>(tmp + ((l * gB + c) * 2 + kv) * n);
-    uint2* dst = reinterpret_cast<uint2*>(out + ((l * B + g0 + c) * 2 + kv) * n);
-    const int64_t n8 = n / 8;
+    const float4* src = reinterpret_cast<const float4*>(tmp + ((l * gB + c) * 2 + kv) * n);
+    uint32_t* dst = reinterpret_cast<uint32_t*>(out + ((l * B + g0 + c) * 2 + kv) * n);
+    const int64_t n4 = n / 4;
     float m = 0.f;
-    for (int64_t i = threadIdx.x; i < n8; i += blockDim.x) {
-        const uint4 w = src[i];
-        const uint32_t u[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-            m = fmaxf(m, fmaxf(fabsf(__uint_as_float(u[j] << 16)), fabsf(__uint_as_float(u[j] & 0xFFFF0000u))));
+    for (int64_t i = threadIdx.x; i < n4; i += blockDim.x) {
+        const float4 w = src[i];
+        m = fmaxf(m, fmaxf(fmaxf(fabsf(w.x), fabsf(w.y)), fmaxf(fabsf(w.z), fabsf(w.w))));
     }
     m = warp_max(m);
     if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
@@ -503,18 +500,9 @@ cross_kv_quant_kernel(const __nv_bfloat16* __restrict__ tmp, int64_t n, int gB, 
     const float sc = amax > 0.f ? amax / 448.0f : 1.0f;
     const float inv = 1.0f / sc;
     if (threadIdx.x == 0) scale[(l * 2 + kv) * B + g0 + c] = sc;
-    for (int64_t i = threadIdx.x; i < n8; i += blockDim.x) {
-        const uint4 w = src[i];
-        const uint32_t u[4] = {w.x, w.y, w.z, w.w};
-        uint32_t q[2];
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-            const uint32_t a = u[2 * j], b = u[2 * j + 1];
-            const uint32_t lo = f2e4m3x2(__uint_as_float(a << 16) * inv, __uint_as_float(a & 0xFFFF0000u) * inv);
-            const uint32_t hi = f2e4m3x2(__uint_as_float(b << 16) * inv, __uint_as_float(b & 0xFFFF0000u) * inv);
-            q[j] = (lo & 0xFFFFu) | (hi << 16);
-        }
-        dst[i] = make_uint2(q[0], q[1]);
+    for (int64_t i = threadIdx.x; i < n4; i += blockDim.x) {
+        const float4 w = src[i];
+        dst[i] = (uint32_t)f2e4m3x2(w.x * inv, w.y * inv) | ((uint32_t)f2e4m3x2(w.z * inv, w.w * inv) << 16);
     }
 }
 
@@ -634,10 +622,10 @@ wb_status scales_from_amax(float* a, int64_t n, cudaStream_t s) {
 wb_status cross_kv_quant(const void* tmp, int64_t gB, int64_t B, int64_t g0, int layers, int64_t n, uint8_t* out,
                          float* scale, cudaStream_t s) {
     if (gB <= 0 || layers <= 0) return WB_OK;
-    if (n % 8 || !aligned16(tmp) || !aligned16(out)) return fail(WB_ERR_ALIGN, "cross K/V quantiser layout");
+    if (n % 16 || !aligned16(tmp) || !aligned16(out)) return fail(WB_ERR_ALIGN, "cross K/V quantiser layout");
     if (gB > 65535 || layers > 65535) return fail(WB_ERR_SHAPE, "cross K/V quantiser grid");
     WB_CUDA(launch_k(cross_kv_quant_kernel, dim3((unsigned)gB, 2, (unsigned)layers), dim3(512), 0, s,
-                     reinterpret_cast<const __nv_bfloat16*>(tmp), n, (int)gB, B, g0, out, scale));
+                     reinterpret_cast<const float*>(tmp), n, (int)gB, B, g0, out, scale));
     WB_CUDA(cudaGetLastError());
     return WB_OK;
 }

@@ -54,7 +54,7 @@ wb_status quant_tensor(const void* x, bool bf16, int64_t n, uint8_t* q, float* s
                        cudaStream_t s);
 wb_status dequant_tensor(const uint8_t* q, const float* scale, int64_t n, float* out, cudaStream_t s);
 wb_status fill(float* x, int64_t n, float v, cudaStream_t s);
-// E4M3 cross K/V of chunks g0 .. g0+gB-1 from their bf16 projection tmp
+// E4M3 cross K/V of chunks g0 .. g0+gB-1 from their fp32 projection tmp
 // [layers][gB][K|V][n] into out [layers][B][K|V][n], scale [layers][K|V][B].
 wb_status cross_kv_quant(const void* tmp, int64_t gB, int64_t B, int64_t g0, int layers, int64_t n, uint8_t* out,
                          float* scale, cudaStream_t s);

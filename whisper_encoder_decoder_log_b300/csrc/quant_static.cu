@@ -12,11 +12,16 @@
 // kMaxBlocks * kPerBlock = 2^26 elements.
 //
 // The array is static device memory of the library: every GPU that loads the
-// library holds it (16 KB) until the process exits.  All calls share it, so
-// calls whose kernels overlap on the GPU (different streams without ordering)
-// race on it; calls on one stream, or otherwise ordered, are safe.  The first
-// call on a device looks up the array's device address (cudaGetSymbolAddress)
-// and caches it; make that first call before any stream capture.
+// library holds it (4160 floats, 16.6 KB) until the process exits.  All calls
+// share it, so calls whose kernels overlap on the GPU (different streams
+// without ordering) race on it; calls on one stream, or otherwise ordered, are
+// safe.  The first call in a CUDA context looks up the array's device address
+// (cudaGetSymbolAddress) with that context current and keeps it for that
+// context; a new context on the device (after cudaDeviceReset, say) is looked
+// up again on its first call.  Make that first call before any stream
+// capture.
+#include <cudaTypedefs.h>
+
 #include <mutex>
 
 #include "common.cuh"
@@ -79,20 +84,37 @@ quant_codes_kernel(const T* __restrict__ x, int64_t n, const float* __restrict__
 }
 
 std::mutex g_mu;
+// Per device: the context the address was looked up in, and the address.
+CUcontext g_scratch_ctx[64] = {};
 float* g_scratch_ptr[64] = {};
+PFN_cuCtxGetCurrent_v4000 g_ctx_current = nullptr;
+std::once_flag g_ctx_once;
 
-// Device address of the static scratch on the current device (looked up once
-// per device, with that device current).
+// Device address of the static scratch in the current context (looked up
+// with that context current, again whenever the device's context changes).
 wb_status scratch_ptr(float** out) {
     int dev = 0;
     WB_CUDA(cudaGetDevice(&dev));
     if (dev < 0 || dev >= 64) return fail(WB_ERR_UNSUPPORTED, "device index out of range");
+    std::call_once(g_ctx_once, [] {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_ctx_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(fn);
+    });
+    if (!g_ctx_current) return fail(WB_ERR_CUDA, "cuCtxGetCurrent unavailable");
+    // null before the runtime has made a context current on this thread
+    CUcontext ctx = nullptr;
+    if (g_ctx_current(&ctx) != CUDA_SUCCESS) return fail(WB_ERR_CUDA, "cuCtxGetCurrent failed");
     std::lock_guard<std::mutex> lk(g_mu);
-    if (!g_scratch_ptr[dev]) {
-        void* p = nullptr;
+    if (!ctx || !g_scratch_ptr[dev] || g_scratch_ctx[dev] != ctx) {
+        void* p = nullptr;   // the lookup also brings up the device's primary context
         const cudaError_t e = cudaGetSymbolAddress(&p, g_quant_scratch);
         if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(quantiser scratch)");
+        if (g_ctx_current(&ctx) != CUDA_SUCCESS || !ctx) return fail(WB_ERR_CUDA, "no current CUDA context");
         g_scratch_ptr[dev] = reinterpret_cast<float*>(p);
+        g_scratch_ctx[dev] = ctx;
     }
     *out = g_scratch_ptr[dev];
     return WB_OK;
@@ -105,7 +127,8 @@ using namespace wb;
 
 extern "C" wb_status wb_quantise_e4m3_static(const void* x, int32_t x_is_bf16, int64_t n, uint8_t* codes,
                                              float* scale, wb_stream stream) {
-    if (!x || !codes || !scale) return fail(WB_ERR_INVALID_ARG, "wb_quantise_e4m3_static: null argument");
+    if (!scale || (n > 0 && (!x || !codes)))
+        return fail(WB_ERR_INVALID_ARG, "wb_quantise_e4m3_static: null argument");
     if (n < 0) return fail(WB_ERR_SHAPE, "wb_quantise_e4m3_static: n < 0");
     if (n > kMaxN)
         return fail(WB_ERR_SHAPE, "wb_quantise_e4m3_static: n exceeds the static scratch limit of 2^26 elements");
