@@ -156,3 +156,19 @@ def test_shard_batch_matches_oracle_bit_exact(world):
 def test_shard_batch_rejects_bad_rank():
     with pytest.raises(wb.WBError):
         wb.wb_shard_batch(np.zeros(1, np.int64), np.ones(1, np.int64), np.ones(1, np.int32), 2, 2)
+
+
+@pytest.mark.parametrize("overlap", [0, 16000, 320000])
+def test_overlap_chunk_count_and_stitching_match_oracle(overlap):
+    rng = np.random.default_rng(overlap % 97)
+    samples = np.array([1, 480000, 480001, 1_234_567, 5_000_000], np.int64)
+    req, idx, valid = oplan.chunk_table(samples, overlap)
+    assert wb.wb_chunk_count(samples, overlap) == req.size
+    n = req.size
+    lens = rng.integers(5, 40, size=n).astype(np.int32)
+    tok = rng.integers(0, 4, size=(n, 448)).astype(np.int32)   # a small alphabet makes overlaps common
+    got = wb.wb_stitch_tokens(samples, overlap, tok, lens, 4)
+    for r in range(samples.size):
+        rows = [tok[c, 4:lens[c]] for c in range(n) if req[c] == r]
+        assert np.array_equal(got[r], oplan.stitch(rows)), r
+    assert wb.lib().wb_chunk_count(1, samples.ctypes.data, 480000) == -1

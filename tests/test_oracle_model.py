@@ -347,3 +347,34 @@ def test_conv_stem_shape_and_positions():
     # zero conv1 -> conv2 sees zeros -> GELU(b2) + PE on every row
     np.testing.assert_allclose(out, model.gelu(W["enc.conv2.b"])[None, :] + model.sinusoids(1500, 64),
                                atol=1e-12)
+
+
+def test_fp8_decoder_moves_with_float32_level_perturbations():
+    """Why the FP8 (mixed_fp8) logits cannot sit within 6e-2 of a float64
+    oracle for any implementation that computes in float32: perturbing every
+    LayerNorm output of the oracle itself by a relative 1e-7 (float32 rounding
+    size) leaves the bf16 decoder within 2e-3 but moves the FP8 decoder's
+    logits by more than 6e-2 -- a value near an E4M3 rounding boundary moves
+    to the next code, and the change grows through the layers."""
+    from synth import TURBO, ModelDims, forced_prefix, random_tokens, round_to_bf16
+    dims = ModelDims("turbo-dec", 128, 1280, 20, 5120, 0, 4, TURBO.vocab)
+    W = make_weights(dims, 6, bf16=True)
+    enc = round_to_bf16(np.random.default_rng(61).normal(size=(1500, 1280)).astype(np.float32)).astype(np.float64)
+    toks = np.concatenate([forced_prefix(2, dims.vocab), random_tokens(5, 28, dims.vocab)])
+    orig = model.layer_norm
+    moved = {}
+    for fp8 in (False, True):
+        ref, _ = model.decode_teacher_forced(toks, enc, W, dims, kv_fp8=True, fp8=fp8, act16=True)
+        prng = np.random.default_rng(1)
+
+        def perturbed(x, g, b, eps=1e-5):
+            y = orig(x, g, b, eps)
+            return y * (1.0 + 1e-7 * prng.standard_normal(y.shape))
+        model.layer_norm = perturbed
+        try:
+            alt, _ = model.decode_teacher_forced(toks, enc, W, dims, kv_fp8=True, fp8=fp8, act16=True)
+        finally:
+            model.layer_norm = orig
+        moved[fp8] = float(np.abs(alt - ref).max())
+    assert moved[False] < 2e-3, moved
+    assert moved[True] > 6e-2, moved

@@ -53,6 +53,30 @@ def test_static_quantiser_matches_regular_twice_in_a_row():
     wb.wb_sync_status()
 
 
+def test_static_quantiser_at_its_limit_matches_the_oracle():
+    """n = 2^26, the largest size the fixed scratch covers: codes and scale
+    bit-exact against the oracle's per-tensor quantiser (scale amax / 448,
+    codes of x * fp32(1 / scale)), compared piecewise; and n = 0 writes scale 1."""
+    from oracle import e4m3 as oe4m3
+    n = 1 << 26
+    rng = np.random.default_rng(321)
+    x = rng.normal(0, 3.0, size=n).astype(np.float32)
+    x[n - 5] = -1234.5                       # the amax sits in the last block
+    c_got, s_got = _static_via_cabi(torch.from_numpy(x).cuda())
+    torch.cuda.synchronize()
+    s_ref = oe4m3.scale_of(float(np.max(np.abs(x))))
+    assert np.float32(s_got.item()) == s_ref
+    got = c_got.cpu().numpy()
+    step = 1 << 23
+    for i in range(0, n, step):
+        assert np.array_equal(got[i:i + step], oe4m3.quantise(x[i:i + step], s_ref)), i
+    empty = torch.empty(0, device="cuda")
+    c0, s0 = _static_via_cabi(empty)
+    torch.cuda.synchronize()
+    assert s0.item() == 1.0 and c0.numel() == 0
+    wb.wb_sync_status()
+
+
 def test_static_quantiser_rejects_oversize_input():
     L = wb.lib()
     n = (1 << 26) + 1
