@@ -370,6 +370,7 @@ class OracleSample:
         self.W = synth.make_weights(dims, seed, bf16=w.precision != PREC_FP32, enc_layers=range(self.n_enc),
                                     dec_layers=range(self.n_dec))
         self.fp8 = w.cfg in ("c5", "c5x")
+        self.act16 = w.precision != PREC_FP32
         self.cross8 = w.cfg == "c5x"
         if w.kind == "teacher":
             self.L = int(w.tokens.shape[1])
@@ -401,7 +402,7 @@ class OracleSample:
         t_stem = time.perf_counter() - t1
         t1 = time.perf_counter()
         for l in range(self.n_enc):
-            h = om.encoder_layer(h, W, l, dims.n_heads, self.fp8)
+            h = om.encoder_layer(h, W, l, dims.n_heads, self.fp8, self.act16)
         t_enc = time.perf_counter() - t1
         est = t_mel + t_stem + t_enc * dims.enc_layers / max(1, self.n_enc)
         desc = (f"oracle on one 30 s chunk: log-Mel, conv stem, {self.n_enc} of {dims.enc_layers} encoder layers "
@@ -419,7 +420,7 @@ class OracleSample:
                 for T in (T1, T2):
                     t1 = time.perf_counter()
                     om.decode_teacher_forced(self.tokens[:T], enc, W, self.sub, kv_fp8=bool(w.kv_fp8), fp8=self.fp8,
-                                             cross_fp8=self.cross8)
+                                             cross_fp8=self.cross8, act16=self.act16)
                     tt[T] = time.perf_counter() - t1
                 # the output head (final LayerNorm, tied-embedding logits) on its own
                 hh = np.random.default_rng(0).normal(size=(T2, dims.d_model))
@@ -502,7 +503,7 @@ def main():
     # which kernel kind dominates: one step with every kind timed (launched
     # directly, since events cannot bracket single kernels inside a replayed
     # graph); this also counts each kind's launches per step
-    wb.wb_prof_start(0, 1 << 21)
+    wb.wb_prof_start(0, 1 << 20)
     run.step()
     torch.cuda.synchronize()
     wb.wb_prof_stop()
@@ -537,7 +538,7 @@ def main():
     # ---- kernel timing: one more step with every launch of the dominant kind
     # bracketed by CUDA events on its own stream (event pool sized to the step)
     n_dom_step = per_step.get(dom, 0)
-    wb.wb_prof_start(dom, max(1024, 2 * n_dom_step + 64))
+    wb.wb_prof_start(dom, min(1 << 20, max(1024, 2 * n_dom_step + 64)))
     run.flush_l2()
     run.step()
     torch.cuda.synchronize()
