@@ -27,6 +27,9 @@ Readings taken where the pages are silent or contradict one another:
     final LayerNorm precedes it; the encoder ends with its own LayerNorm;
   * greedy choice = lowest index among the maximal logits; no token is
     suppressed and decoding runs to the requested length (no end token);
+  * beam search (the beam size of [TWT] / [BFW]): hypotheses ranked by the
+    sum of their tokens' log-softmax probabilities, ties to the lower beam
+    then the lower token id, no length penalty (see beam_search);
   * FP8 GEMMs (``mixed_fp8``): every E4M3 operand is a tensor with one scale
     amax / 448 ([WB] "Direct Kernel API": ``quantise_e4m3(x) -> (fp8,
     scale)``, one scale per call).  Weights: one scale per weight matrix.
@@ -328,3 +331,51 @@ def decode_teacher_forced(tokens, enc, W, dims, kv_fp8: bool = False,
 def greedy(logits) -> np.ndarray:
     """Lowest index of the maximum of each row."""
     return np.argmax(np.asarray(logits), axis=-1).astype(np.int32)
+
+
+# ------------------------------------------------------------------ beam search
+
+def log_softmax(x):
+    """log p_v = x_v - max - log sum_u exp(x_u - max), float64."""
+    x = np.asarray(x, dtype=np.float64)
+    m = x.max(axis=-1, keepdims=True)
+    return x - m - np.log(np.exp(x - m).sum(axis=-1, keepdims=True))
+
+
+def beam_candidates(scores, logits, beams: int):
+    """One beam-search step.  ``scores`` [n] are the running sums of the live
+    hypotheses' token log-probabilities, ``logits`` [n, V] their next-token
+    logits.  Every continuation (b, v) scores scores[b] + log_softmax(logits[b])[v];
+    the ``beams`` best continue, ranked by score, ties to the lower beam then
+    the lower token id.  Returns (new scores, parent beams, tokens)."""
+    lp = log_softmax(logits)
+    cand = np.asarray(scores, np.float64)[:, None] + lp
+    n, V = cand.shape
+    b_idx = np.repeat(np.arange(n), V)
+    v_idx = np.tile(np.arange(V), n)
+    order = np.lexsort((v_idx, b_idx, -cand.reshape(-1)))[:beams]
+    return cand.reshape(-1)[order], b_idx[order].astype(np.int32), v_idx[order].astype(np.int32)
+
+
+def beam_search(prefix, length: int, beams: int, enc, W, dims, **decode_kw):
+    """Beam search over one chunk ([TWT] "NVIDIA Usage": ``num_beams``; [BFW]
+    "Benchmarks": a fixed beam size).  Readings: a hypothesis is scored by the
+    sum of its generated tokens' log-probabilities; there is no length penalty
+    and no end token, so every hypothesis reaches ``length`` positions
+    (prefix included) and the answer is the best-scoring one (ties: the lower
+    beam); the first step expands the forced prefix alone.  Each hypothesis's
+    logits come from the teacher-forced decoder over its own tokens.
+    Returns (tokens [length] of the best hypothesis, its score, the per-step
+    list of (scores, parents, tokens))."""
+    hyps = [list(np.asarray(prefix, np.int64))]
+    scores = np.zeros(1)
+    trace = []
+    P = len(hyps[0])
+    for t in range(P - 1, length - 1):
+        logits = np.stack([decode_teacher_forced(np.array(h), enc, W, dims, prefix_len=P, **decode_kw)[0][-1]
+                           for h in hyps])
+        scores, parents, toks = beam_candidates(scores, logits, beams)
+        hyps = [hyps[p] + [int(v)] for p, v in zip(parents, toks)]
+        trace.append((scores.copy(), parents, toks))
+    best = int(np.argmax(scores))          # lowest index among the maxima
+    return np.array(hyps[best], np.int32), float(scores[best]), trace

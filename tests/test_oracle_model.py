@@ -378,3 +378,47 @@ def test_fp8_decoder_moves_with_float32_level_perturbations():
         moved[fp8] = float(np.abs(alt - ref).max())
     assert moved[False] < 2e-3, moved
     assert moved[True] > 6e-2, moved
+
+
+def test_beam_candidates_rank_by_score_then_beam_then_token():
+    logits = np.log(np.array([[0.5, 0.25, 0.25], [0.25, 0.5, 0.25]]))
+    s, p, v = model.beam_candidates(np.array([0.0, 0.0]), logits, 4)
+    assert p.tolist() == [0, 1, 0, 0] and v.tolist() == [0, 1, 1, 2]      # ties: lower beam, then lower token
+    np.testing.assert_allclose(s, np.log([0.5, 0.5, 0.25, 0.25]), atol=1e-15)
+    np.testing.assert_allclose(model.log_softmax(np.array([1.0, 2.0, 3.0])),
+                               np.log(np.exp([1.0, 2.0, 3.0]) / np.exp([1.0, 2.0, 3.0]).sum()), atol=1e-15)
+
+
+TINYV = ModelDims("tinyv", 8, 64, 1, 128, 0, 1, 6)
+
+
+def _seq_logprob(tokens, P, enc, W):
+    logits, _ = model.decode_teacher_forced(np.array(tokens), enc, W, TINYV)
+    lp = model.log_softmax(logits)
+    return sum(lp[t, tokens[t + 1]] for t in range(P - 1, len(tokens) - 1))
+
+
+def test_beam_search_without_pruning_finds_the_best_sequence():
+    """With as many beams as continuations (V^2 for 3 generated tokens) nothing
+    is pruned before the last step, so beam search must return the best of
+    all V^3 sequences found by brute force."""
+    import itertools
+    W = make_weights(TINYV, 23, bf16=False)
+    enc = np.random.default_rng(24).normal(size=(10, TINYV.d_model))
+    prefix = [1, 4]
+    best, score, trace = model.beam_search(prefix, 5, 36, enc, W, TINYV)
+    brute = max((_seq_logprob(prefix + list(c), 2, enc, W), list(c)) for c in itertools.product(range(6), repeat=3))
+    assert best.tolist() == prefix + brute[1]
+    np.testing.assert_allclose(score, brute[0], atol=1e-12)
+    np.testing.assert_allclose(score, _seq_logprob(best.tolist(), 2, enc, W), atol=1e-12)
+
+
+def test_beam_search_with_one_beam_is_greedy():
+    W = make_weights(TINYV, 25, bf16=False)
+    enc = np.random.default_rng(26).normal(size=(10, TINYV.d_model))
+    tok = [2, 3]
+    for _ in range(5):
+        logits, _ = model.decode_teacher_forced(np.array(tok), enc, W, TINYV)
+        tok.append(int(model.greedy(logits[-1])))
+    best, _, _ = model.beam_search([2, 3], 7, 1, enc, W, TINYV)
+    assert best.tolist() == tok
