@@ -238,6 +238,41 @@ WB_API wb_status wb_decode_prefix(wb_decoder* dec, int32_t P, float* logits,
 WB_API wb_status wb_decode_step(wb_decoder* dec, int64_t n_active, float* logits,
                          wb_stream stream);
 
+/*
+ * Beam search ("thewhisper-large-v3-turbo" model card, "NVIDIA Usage":
+ * generate_kwargs with num_beams; "Blazingly fast whisper transcriptions",
+ * "Benchmarks": a fixed beam size).  A beam decoder over B chunks keeps
+ * `beams` (2..8) hypotheses per chunk: token rows c*beams .. c*beams+beams-1
+ * of `tokens` ([dev] int32 [B*beams, 448], every row holding the forced
+ * prefix) belong to chunk c; the cross-attention K/V are computed once per
+ * chunk and shared by its hypotheses.  wb_decode_prefix runs the prefix and
+ * the first selection.  A hypothesis scores the sum of its generated tokens'
+ * log-probabilities (log-softmax of its logits); every step ranks all
+ * beams x vocab continuations of a chunk by that sum (ties: the lower beam,
+ * then the lower token id) and keeps the best `beams`; their token rows and
+ * cache histories are their parents' (a hypothesis reads the cached K/V rows
+ * its ancestors wrote; no cache row is copied), with the chosen token in
+ * column t + 1.  No length penalty, no end token: every chunk decodes to its
+ * chunk_len.
+ *   wb_decode_step_beams: one step for the first n_active chunks (launched
+ *     directly, not through a captured graph); scores_out [dev] float32
+ *     [B*beams] and parents_out [dev] int32 [B*beams] (beam index within its
+ *     chunk) receive the new hypotheses' scores and parents, or are null.
+ *   wb_decoder_best_beams: each chunk's best hypothesis (lowest beam among
+ *     the maximal scores) into out_tokens [dev] int32 [B, 448] (columns 0 ..
+ *     chunk_len - 1) and its score into out_scores [dev] float32 [B] or null.
+ */
+WB_API size_t wb_decoder_workspace_size_beams(const wb_model* model, int64_t B, const int32_t* chunk_len,
+                                              int32_t beams);
+WB_API wb_status wb_decoder_init_beams(wb_model* model, int64_t B, const int32_t* chunk_len, int32_t beams,
+                                       const void* enc, int32_t* tokens, void* workspace, size_t workspace_bytes,
+                                       wb_stream stream, wb_decoder** out);
+WB_API wb_status wb_decode_step_beams(wb_decoder* dec, int64_t n_active, float* scores_out, int32_t* parents_out,
+                                      wb_stream stream);
+WB_API wb_status wb_decoder_best_beams(wb_decoder* dec, int32_t* out_tokens, float* out_scores, wb_stream stream);
+/* The current running scores of every hypothesis into out [dev] float32 [B*beams]. */
+WB_API wb_status wb_decoder_beam_scores(wb_decoder* dec, float* out, wb_stream stream);
+
 /* Position the next wb_decode_step will process. */
 WB_API int32_t wb_decoder_position(const wb_decoder* dec);
 WB_API wb_status wb_decoder_destroy(wb_decoder* dec);

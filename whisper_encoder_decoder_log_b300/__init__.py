@@ -51,6 +51,11 @@ _SIGS = {
     "wb_decode_prefix": (ctypes.c_int, [_VP, _I32, _VP, _VP]),
     "wb_decode_step": (ctypes.c_int, [_VP, _I64, _VP, _VP]),
     "wb_decoder_position": (_I32, [_VP]),
+    "wb_decoder_workspace_size_beams": (_SZ, [_VP, _I64, _VP, _I32]),
+    "wb_decoder_init_beams": (ctypes.c_int, [_VP, _I64, _VP, _I32, _VP, _VP, _VP, _SZ, _VP, ctypes.POINTER(_VP)]),
+    "wb_decode_step_beams": (ctypes.c_int, [_VP, _I64, _VP, _VP, _VP]),
+    "wb_decoder_best_beams": (ctypes.c_int, [_VP, _VP, _VP, _VP]),
+    "wb_decoder_beam_scores": (ctypes.c_int, [_VP, _VP, _VP]),
     "wb_decoder_destroy": (ctypes.c_int, [_VP]),
     "wb_transcribe_workspace_size": (_SZ, [_VP, _I32, _VP, _VP, _U64]),
     "wb_transcribe_batch": (ctypes.c_int, [_VP, _VP, _VP, _VP, _I32, _VP, _VP, _VP, _U64, _VP, _SZ, _VP, _VP]),
@@ -199,6 +204,37 @@ def wb_decode_prefix(dec: int, P: int, logits=None, stream=None):
 def wb_decode_step(dec: int, n_active: int, logits=None, stream=None):
     _need(logits, "float32", "logits")
     _check(lib().wb_decode_step(dec, n_active, _p(logits), _stream(stream)))
+
+
+def wb_decoder_workspace_size_beams(model: int, chunk_len, beams: int) -> int:
+    arr, ptr = _host_arr(chunk_len, np.int32)
+    return lib().wb_decoder_workspace_size_beams(model, arr.size, ptr, beams)
+
+
+def wb_decoder_init_beams(model: int, chunk_len, beams: int, enc, tokens, workspace, stream=None) -> int:
+    arr, ptr = _host_arr(chunk_len, np.int32)
+    _need(tokens, "int32", "tokens")
+    h = _VP(0)
+    _check(lib().wb_decoder_init_beams(model, arr.size, ptr, beams, _p(enc), _p(tokens), _p(workspace),
+                                       workspace.numel() * workspace.element_size(), _stream(stream), ctypes.byref(h)))
+    return h.value
+
+
+def wb_decode_step_beams(dec: int, n_active: int, scores_out=None, parents_out=None, stream=None):
+    _need(scores_out, "float32", "scores_out")
+    _need(parents_out, "int32", "parents_out")
+    _check(lib().wb_decode_step_beams(dec, n_active, _p(scores_out), _p(parents_out), _stream(stream)))
+
+
+def wb_decoder_best_beams(dec: int, out_tokens, out_scores=None, stream=None):
+    _need(out_tokens, "int32", "out_tokens")
+    _need(out_scores, "float32", "out_scores")
+    _check(lib().wb_decoder_best_beams(dec, _p(out_tokens), _p(out_scores), _stream(stream)))
+
+
+def wb_decoder_beam_scores(dec: int, out, stream=None):
+    _need(out, "float32", "out")
+    _check(lib().wb_decoder_beam_scores(dec, _p(out), _stream(stream)))
 
 
 def wb_decoder_position(dec: int) -> int:

@@ -426,6 +426,14 @@ struct wb_decoder {
     uint8_t* fq = nullptr;
     float* f_scale = nullptr;
     float* logits = nullptr;
+    // beam search: rows = chunks x beams (chunk c owns rows c*beams ..);
+    // cross K/V are held once per chunk (n_cross chunks)
+    int beams = 1;
+    int64_t n_cross = 0;
+    int32_t* hist = nullptr;           // [rows][448] row whose cache holds each position
+    float* scores = nullptr;           // [rows] running log-probability sums
+    int32_t* step_parents = nullptr;   // caller buffers of the current step (or null)
+    float* step_scores = nullptr;
 };
 
 namespace wb {
@@ -439,16 +447,20 @@ struct DecLayout {
 };
 
 // Carve (or size, with base == nullptr) the decoder workspace.
+// B rows (chunks x beams); the cross K/V are held once per chunk.
 size_t carve_decoder(const wb_model* m, int64_t B, const int32_t* len, wb_decoder* dec, uint8_t* base, size_t cap,
-                     bool* overflow) {
+                     bool* overflow, int beams = 1) {
     Carve c{base, cap};
     const int Ld = m->desc.dec_layers, d = m->d(), H = m->H(), F = m->F();
     const size_t act = m->fp32() ? 4 : 2;
     const int64_t R = B * kMaxPrefix;
+    const int64_t NC = B / beams;
     const bool c8 = m->desc.kv_fp8 == WB_KV_FP8_CROSS;
-    void* crosskv = c.take<uint8_t>((size_t)Ld * B * 2 * kCtx * d * (c8 ? 1 : act));
-    void* ckv_tmp = c8 ? c.take<float>((size_t)Ld * std::min<int64_t>(B, kCrossGroup) * 2 * kCtx * d) : nullptr;
-    float* cscale = c8 ? c.take<float>((size_t)std::max(1, Ld) * 2 * B) : nullptr;
+    void* crosskv = c.take<uint8_t>((size_t)Ld * NC * 2 * kCtx * d * (c8 ? 1 : act));
+    void* ckv_tmp = c8 ? c.take<float>((size_t)Ld * std::min<int64_t>(NC, kCrossGroup) * 2 * kCtx * d) : nullptr;
+    float* cscale = c8 ? c.take<float>((size_t)std::max(1, Ld) * 2 * NC) : nullptr;
+    int32_t* hist = beams > 1 ? c.take<int32_t>((size_t)B * kMaxPos) : nullptr;
+    float* scores = beams > 1 ? c.take<float>(B) : nullptr;
     int64_t cache_elems = 0;
     for (int64_t i = 0; i < B; ++i) cache_elems += (int64_t)Ld * 2 * H * len[i] * 64;
     void* cache = c.take<uint8_t>((size_t)cache_elems * (m->desc.kv_fp8 ? 1 : 4));
@@ -469,6 +481,10 @@ size_t carve_decoder(const wb_model* m, int64_t B, const int32_t* len, wb_decode
     float* logits = c.take<float>((size_t)B * ((m->desc.vocab + 7) / 8 * 8));
     int* pos_dev = c.take<int>(64);
     if (dec) {
+        dec->beams = beams;
+        dec->n_cross = NC;
+        dec->hist = hist;
+        dec->scores = scores;
         dec->pos_dev = pos_dev;
         dec->crosskv = crosskv; dec->ckv_tmp = ckv_tmp; dec->cscale = cscale;
         dec->cache = cache; dec->kscale = kscale; dec->vscale = vscale;
@@ -566,6 +582,7 @@ wb_status decoder_layers(wb_decoder* dec, int64_t n_chunks, int rows_per_chunk, 
             kv.heads = H; kv.k_blk = 2 * l; kv.v_blk = 2 * l + 1; kv.row_stride = 64;
             if (kv8) { kv.k_scale = ks; kv.v_scale = vs; }
             if (pos_dev) { kv.pos_dev = pos_dev; kv.active_len = dec->len_dev; }
+            if (dec->beams > 1 && rows_per_chunk == 1) kv.hist = dec->hist;
             if (fused_step) {
                 if (wb_status st = attn_self_step_e4m3(dec->qkv, 3 * d, n_chunks, H, kv, p0, dec->attn, lda, s,
                                                        sp ? d : 0))
@@ -595,10 +612,14 @@ wb_status decoder_layers(wb_decoder* dec, int64_t n_chunks, int rows_per_chunk, 
             const bool c8 = m->desc.kv_fp8 == WB_KV_FP8_CROSS;
             const size_t act = c8 ? 1 : (f32 ? 4 : 2);
             KVView kv;
-            kv.ptr = reinterpret_cast<uint8_t*>(dec->crosskv) + (size_t)l * dec->B * 2 * H * kCtx * 64 * act;
+            kv.ptr = reinterpret_cast<uint8_t*>(dec->crosskv) + (size_t)l * dec->n_cross * 2 * H * kCtx * 64 * act;
             kv.chunk_stride = (int64_t)2 * H * kCtx * 64; kv.head_stride = (int64_t)kCtx * 64; kv.heads = H;
             kv.k_blk = 0; kv.v_blk = 1; kv.row_stride = 64;
-            if (c8) { kv.k_scale = dec->cscale + (size_t)(2 * l) * dec->B; kv.v_scale = dec->cscale + (size_t)(2 * l + 1) * dec->B; }
+            kv.beam_div = dec->beams;
+            if (c8) {
+                kv.k_scale = dec->cscale + (size_t)(2 * l) * dec->n_cross;
+                kv.v_scale = dec->cscale + (size_t)(2 * l + 1) * dec->n_cross;
+            }
             if (pos_dev) { kv.pos_dev = pos_dev; kv.active_len = dec->len_dev; }
             if (wb_status st = attn_rows(DT_F32, c8 ? DT_E4M3 : (f32 ? DT_F32 : DT_BF16), attn_dt, dec->cq, d, n_chunks,
                                          rows_per_chunk, H, kv, kCtx, false, 0, dec->attn, lda, s, sp ? d : 0))
@@ -658,6 +679,10 @@ wb_status decoder_head(wb_decoder* dec, int64_t n_chunks, int rows_per_chunk, in
             return st;
         L.a = dec->a; L.rows = R;
         if (wb_status st = linear(m, L, epi_out(logits_all, V, OUT_F32, nullptr), s)) return st;
+        if (dec->beams > 1)
+            return beam_select(logits_all + (int64_t)(rows_per_chunk - 1) * V, (int64_t)rows_per_chunk * V,
+                               n_chunks / dec->beams, dec->beams, V, dec->scores, dec->tokens, dec->hist, dec->len_dev,
+                               pos_dev, pos_last, dec->step_parents, dec->step_scores, s);
         return argmax_tokens(logits_all + (int64_t)(rows_per_chunk - 1) * V, (int64_t)rows_per_chunk * V, n_chunks, V,
                              dec->tokens, dec->len_dev, pos_dev, pos_last, s);
     }
@@ -668,6 +693,9 @@ wb_status decoder_head(wb_decoder* dec, int64_t n_chunks, int rows_per_chunk, in
     L.a = dec->a; L.rows = n_chunks;
     const int64_t ldl = (V + 7) / 8 * 8;
     if (wb_status st = linear(m, L, epi_out(dec->logits, ldl, OUT_F32, nullptr), s)) return st;
+    if (dec->beams > 1)
+        return beam_select(dec->logits, ldl, n_chunks / dec->beams, dec->beams, V, dec->scores, dec->tokens, dec->hist,
+                           dec->len_dev, pos_dev, pos_last, dec->step_parents, dec->step_scores, s);
     return argmax_tokens(dec->logits, ldl, n_chunks, V, dec->tokens, dec->len_dev, pos_dev, pos_last, s);
 }
 
@@ -978,32 +1006,38 @@ size_t wb_decoder_workspace_size(const wb_model* m, int64_t B, const int32_t* le
     return carve_decoder(m, B, len, nullptr, nullptr, 0, nullptr);
 }
 
-wb_status wb_decoder_init(wb_model* m, int64_t B, const int32_t* len, const void* enc, int32_t* tokens,
-                          void* workspace, size_t ws_bytes, wb_stream stream, wb_decoder** out) {
+// A decoder over n_chunks chunks with `beams` hypotheses each (rows c*beams
+// .. c*beams + beams - 1 belong to chunk c); the cross K/V are computed once
+// per chunk.
+static wb_status decoder_init(wb_model* m, int64_t n_chunks, const int32_t* chunk_len, int beams, const void* enc,
+                              int32_t* tokens, void* workspace, size_t ws_bytes, wb_stream stream, wb_decoder** out) {
     if (!out) return fail(WB_ERR_INVALID_ARG, "wb_decoder_init: null out");
     *out = nullptr;
-    if (!m || !len || !enc || !tokens || !workspace) return fail(WB_ERR_INVALID_ARG, "wb_decoder_init: null argument");
-    if (B < 1 || B > 65535) return fail(WB_ERR_SHAPE, "wb_decoder_init: B must be in [1, 65535]");
+    if (!m || !chunk_len || !enc || !tokens || !workspace) return fail(WB_ERR_INVALID_ARG, "wb_decoder_init: null argument");
+    if (n_chunks < 1 || n_chunks * beams > 65535) return fail(WB_ERR_SHAPE, "wb_decoder_init: B * beams must be in [1, 65535]");
     if (!aligned16(enc) || !aligned16(tokens) || !aligned16(workspace)) return fail(WB_ERR_ALIGN, "wb_decoder_init: alignment");
-    for (int64_t i = 0; i < B; ++i) {
-        if (len[i] < 1 || len[i] > kMaxPos) return fail(WB_ERR_SHAPE, "wb_decoder_init: chunk_len must be in [1, 448]");
-        if (i && len[i] > len[i - 1]) return fail(WB_ERR_SHAPE, "wb_decoder_init: chunk_len must be non-increasing");
+    for (int64_t i = 0; i < n_chunks; ++i) {
+        if (chunk_len[i] < 1 || chunk_len[i] > kMaxPos) return fail(WB_ERR_SHAPE, "wb_decoder_init: chunk_len must be in [1, 448]");
+        if (i && chunk_len[i] > chunk_len[i - 1]) return fail(WB_ERR_SHAPE, "wb_decoder_init: chunk_len must be non-increasing");
     }
+    const int64_t B = n_chunks * beams;          // rows
+    std::vector<int32_t> len(B);
+    for (int64_t r = 0; r < B; ++r) len[r] = chunk_len[r / beams];
     wb_decoder* dec = new wb_decoder();
     dec->m = m;
     dec->B = B;
-    dec->len.assign(len, len + B);
+    dec->len = len;
     dec->tokens = tokens;
     dec->max_len = len[0];
     bool over = false;
-    carve_decoder(m, B, len, dec, reinterpret_cast<uint8_t*>(workspace), ws_bytes, &over);
+    carve_decoder(m, B, len.data(), dec, reinterpret_cast<uint8_t*>(workspace), ws_bytes, &over, beams);
     if (over) {
         delete dec;
         return fail(WB_ERR_SHAPE, "wb_decoder_init: workspace too small");
     }
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const int d = m->d(), H = m->H(), Ld = m->desc.dec_layers;
-    // per-chunk cache offsets (elements) and lengths
+    // per-row cache offsets (elements) and lengths
     std::vector<int64_t> off(B);
     int64_t acc = 0;
     for (int64_t i = 0; i < B; ++i) {
@@ -1012,24 +1046,27 @@ wb_status wb_decoder_init(wb_model* m, int64_t B, const int32_t* len, const void
     }
     auto fail_free = [&](wb_status st) { delete dec; return st; };
     if (cudaMemcpyAsync(dec->off, off.data(), B * 8, cudaMemcpyHostToDevice, s) != cudaSuccess ||
-        cudaMemcpyAsync(dec->len_dev, len, B * 4, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+        cudaMemcpyAsync(dec->len_dev, len.data(), B * 4, cudaMemcpyHostToDevice, s) != cudaSuccess ||
         cudaStreamSynchronize(s) != cudaSuccess)
         return fail_free(fail(WB_ERR_CUDA, "wb_decoder_init: upload"));
+    if (beams > 1)
+        if (wb_status st = beam_init(dec->hist, dec->scores, B, beams, s)) return fail_free(st);
+    const int64_t NC = n_chunks;
     if (Ld > 0 && m->desc.kv_fp8 != WB_KV_FP8_CROSS) {
         Lin L;
-        L.a = enc; L.rows = B * kCtx; L.lda = d; L.w = m->W("dec.0.ck.w"); L.N = (int64_t)Ld * 2 * d; L.K = d;
+        L.a = enc; L.rows = NC * kCtx; L.lda = d; L.w = m->W("dec.0.ck.w"); L.N = (int64_t)Ld * 2 * d; L.K = d;
         GemmEpi ep = epi_out(dec->crosskv, 0, m->fp32() ? OUT_F32 : OUT_BF16, m->V("dec.0.ck.b"));
         ep.mode = MODE_CROSS_KV;
         ep.ckv_d = d;
         ep.ckv_heads = H;
-        ep.ckv_chunks = B;
+        ep.ckv_chunks = NC;
         if (wb_status st = linear(m, L, ep, s)) return fail_free(st);
     } else if (Ld > 0) {
         // E4M3 cross K/V: per group of chunks, the fp32 projection into a
         // scratch area, then one amax / 448 scale and the codes per (chunk,
         // layer, K|V) tensor, rounded once from fp32
-        for (int64_t g0 = 0; g0 < B; g0 += kCrossGroup) {
-            const int64_t gB = std::min<int64_t>(kCrossGroup, B - g0);
+        for (int64_t g0 = 0; g0 < NC; g0 += kCrossGroup) {
+            const int64_t gB = std::min<int64_t>(kCrossGroup, NC - g0);
             Lin L;
             L.a = reinterpret_cast<const __nv_bfloat16*>(enc) + g0 * kCtx * d;
             L.rows = gB * kCtx; L.lda = d; L.w = m->W("dec.0.ck.w"); L.N = (int64_t)Ld * 2 * d; L.K = d;
@@ -1039,13 +1076,31 @@ wb_status wb_decoder_init(wb_model* m, int64_t B, const int32_t* len, const void
             ep.ckv_heads = H;
             ep.ckv_chunks = gB;
             if (wb_status st = linear(m, L, ep, s)) return fail_free(st);
-            if (wb_status st = cross_kv_quant(dec->ckv_tmp, gB, B, g0, Ld, (int64_t)H * kCtx * 64,
+            if (wb_status st = cross_kv_quant(dec->ckv_tmp, gB, NC, g0, Ld, (int64_t)H * kCtx * 64,
                                               reinterpret_cast<uint8_t*>(dec->crosskv), dec->cscale, s))
                 return fail_free(st);
         }
     }
     *out = dec;
     return WB_OK;
+}
+
+wb_status wb_decoder_init(wb_model* m, int64_t B, const int32_t* len, const void* enc, int32_t* tokens,
+                          void* workspace, size_t ws_bytes, wb_stream stream, wb_decoder** out) {
+    return decoder_init(m, B, len, 1, enc, tokens, workspace, ws_bytes, stream, out);
+}
+
+size_t wb_decoder_workspace_size_beams(const wb_model* m, int64_t B, const int32_t* chunk_len, int32_t beams) {
+    if (!m || B < 1 || !chunk_len || beams < 1 || beams > kBeamMax) return 0;
+    std::vector<int32_t> len((size_t)(B * beams));
+    for (int64_t r = 0; r < B * beams; ++r) len[r] = chunk_len[r / beams];
+    return carve_decoder(m, B * beams, len.data(), nullptr, nullptr, 0, nullptr, beams);
+}
+
+wb_status wb_decoder_init_beams(wb_model* m, int64_t B, const int32_t* chunk_len, int32_t beams, const void* enc,
+                                int32_t* tokens, void* workspace, size_t ws_bytes, wb_stream stream, wb_decoder** out) {
+    if (beams < 2 || beams > kBeamMax) return fail(WB_ERR_SHAPE, "wb_decoder_init_beams: beams must be in [2, 8]");
+    return decoder_init(m, B, chunk_len, beams, enc, tokens, workspace, ws_bytes, stream, out);
 }
 
 wb_status wb_decode_prefix(wb_decoder* dec, int32_t P, float* logits, wb_stream stream) {
@@ -1086,6 +1141,7 @@ static bool graphs_enabled() {
 
 wb_status wb_decode_step(wb_decoder* dec, int64_t n_active, float* logits, wb_stream stream) {
     if (!dec) return fail(WB_ERR_INVALID_ARG, "wb_decode_step: null decoder");
+    if (dec->beams > 1) return fail(WB_ERR_INVALID_ARG, "wb_decode_step: a beam decoder steps with wb_decode_step_beams");
     if (dec->P == 0) return fail(WB_ERR_INVALID_ARG, "wb_decode_step: run wb_decode_prefix first");
     if (n_active < 1 || n_active > dec->B) return fail(WB_ERR_SHAPE, "wb_decode_step: bad n_active");
     if (dec->len[n_active - 1] <= dec->pos + 1)
@@ -1131,6 +1187,41 @@ wb_status wb_decode_step(wb_decoder* dec, int64_t n_active, float* logits, wb_st
     count_launch((int)g->kernels);
     dec->pos += 1;
     return WB_OK;
+}
+
+wb_status wb_decode_step_beams(wb_decoder* dec, int64_t n_active, float* scores_out, int32_t* parents_out,
+                               wb_stream stream) {
+    if (!dec) return fail(WB_ERR_INVALID_ARG, "wb_decode_step_beams: null decoder");
+    if (dec->beams < 2) return fail(WB_ERR_INVALID_ARG, "wb_decode_step_beams: not a beam decoder");
+    if (dec->P == 0) return fail(WB_ERR_INVALID_ARG, "wb_decode_step_beams: run wb_decode_prefix first");
+    const int64_t rows = n_active * dec->beams;
+    if (n_active < 1 || rows > dec->B) return fail(WB_ERR_SHAPE, "wb_decode_step_beams: bad n_active");
+    if (dec->len[rows - 1] <= dec->pos + 1)
+        return fail(WB_ERR_SHAPE, "wb_decode_step_beams: an active chunk has reached its length");
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    dec->step_scores = scores_out;
+    dec->step_parents = parents_out;
+    const wb_status st = run_step(dec, rows, nullptr, s);
+    dec->step_scores = nullptr;
+    dec->step_parents = nullptr;
+    if (st) return st;
+    dec->pos += 1;
+    return WB_OK;
+}
+
+wb_status wb_decoder_beam_scores(wb_decoder* dec, float* out, wb_stream stream) {
+    if (!dec || !out) return fail(WB_ERR_INVALID_ARG, "wb_decoder_beam_scores: null argument");
+    if (dec->beams < 2) return fail(WB_ERR_INVALID_ARG, "wb_decoder_beam_scores: not a beam decoder");
+    WB_CUDA(cudaMemcpyAsync(out, dec->scores, sizeof(float) * (size_t)dec->B, cudaMemcpyDeviceToDevice,
+                            reinterpret_cast<cudaStream_t>(stream)));
+    return WB_OK;
+}
+
+wb_status wb_decoder_best_beams(wb_decoder* dec, int32_t* out_tokens, float* out_scores, wb_stream stream) {
+    if (!dec || !out_tokens) return fail(WB_ERR_INVALID_ARG, "wb_decoder_best_beams: null argument");
+    if (dec->beams < 2) return fail(WB_ERR_INVALID_ARG, "wb_decoder_best_beams: not a beam decoder");
+    return beam_best(dec->scores, dec->tokens, dec->B / dec->beams, dec->beams, dec->len_dev, out_tokens, out_scores,
+                     reinterpret_cast<cudaStream_t>(stream));
 }
 
 int32_t wb_decoder_position(const wb_decoder* dec) { return dec ? dec->pos : -1; }

@@ -112,12 +112,13 @@ attn_rows_kernel(const TQ* __restrict__ q, int64_t q_ld, int rows_per_chunk, int
         const int qi = i / 64, c = i % 64;
         sq[i] = qi < nq ? (float)q[(row0 + qi) * q_ld + h * 64 + c] * 0.125f : 0.f;
     }
-    const int64_t cb = kv.chunk_off ? kv.chunk_off[chunk] : chunk * kv.chunk_stride;
-    const int64_t hs = kv.head_stride * (kv.chunk_len ? (int64_t)kv.chunk_len[chunk] : 1);
+    const int64_t kc = chunk / kv.beam_div;       // the chunk whose keys this row reads
+    const int64_t cb = kv.chunk_off ? kv.chunk_off[kc] : kc * kv.chunk_stride;
+    const int64_t hs = kv.head_stride * (kv.chunk_len ? (int64_t)kv.chunk_len[kc] : 1);
     const TKV* Kp = reinterpret_cast<const TKV*>(kv.ptr) + cb + ((int64_t)kv.k_blk * kv.heads + h) * hs;
     const TKV* Vp = reinterpret_cast<const TKV*>(kv.ptr) + cb + ((int64_t)kv.v_blk * kv.heads + h) * hs;
-    const float ks = kv.k_scale ? kv.k_scale[chunk] : 1.f;
-    const float vs = kv.v_scale ? kv.v_scale[chunk] : 1.f;
+    const float ks = kv.k_scale ? kv.k_scale[kc] : 1.f;
+    const float vs = kv.v_scale ? kv.v_scale[kc] : 1.f;
     int nk = kv_len;
     if (causal) nk = min(kv_len, q_pos0 + r_first + nq);
     __syncthreads();
@@ -297,23 +298,31 @@ __global__ void __launch_bounds__(32 * kStepHeads, 6)
 self_attn_step_kernel(const float* __restrict__ qkv, int64_t q_ld, int heads, KVView kv, int q_pos_host,
                       TO* __restrict__ out, int64_t o_ld, int64_t o_split) {
     __shared__ uint4 ring[kStepHeads][kStepDepth][2][32];   // [warp][stage][K|V][lane]
+    __shared__ int64_t shist[CROSS ? 1 : kMaxPos];          // beam search: cache base of each row j
     griddep_wait();
     griddep_launch();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t chunk = blockIdx.x;
     const int h = blockIdx.y * kStepHeads + warp;
-    if (h >= heads) return;
     const int pos = kv.pos_dev ? *kv.pos_dev : q_pos_host;
-    if (kv.active_len && kv.active_len[chunk] <= pos + 1) return;   // finished chunk
+    if (kv.active_len && kv.active_len[chunk] <= pos + 1) return;   // finished chunk (uniform per CTA)
+    const int64_t kc = CROSS ? chunk / kv.beam_div : chunk;         // whose cross K/V / scales
     const int L = CROSS ? kCtx : kv.chunk_len[chunk];
     if (!CROSS && pos >= L) return;                                // no cache row for this position
+    if (!CROSS && kv.hist) {   // hypothesis history: row j of this row's cache sits in row hist[j]'s cache
+        for (int j = threadIdx.x; j < pos; j += blockDim.x) shist[j] = kv.chunk_off[kv.hist[chunk * kMaxPos + j]];
+        __syncthreads();
+    }
+    if (h >= heads) return;
     const int r = lane >> 2, sub = lane & 3;
     const int d = heads * 64;
     const int64_t hs = kv.head_stride * (CROSS ? 1 : (int64_t)L);
-    uint8_t* base = const_cast<uint8_t*>(reinterpret_cast<const uint8_t*>(kv.ptr)) +
-                    (CROSS ? chunk * kv.chunk_stride : kv.chunk_off[chunk]);
-    uint8_t* Kp = base + ((int64_t)kv.k_blk * kv.heads + h) * hs;
-    uint8_t* Vp = base + ((int64_t)kv.v_blk * kv.heads + h) * hs;
+    uint8_t* const kvb = const_cast<uint8_t*>(reinterpret_cast<const uint8_t*>(kv.ptr));
+    uint8_t* base = kvb + (CROSS ? kc * kv.chunk_stride : kv.chunk_off[chunk]);
+    const int64_t koff = ((int64_t)kv.k_blk * kv.heads + h) * hs, voff = ((int64_t)kv.v_blk * kv.heads + h) * hs;
+    uint8_t* Kp = base + koff;
+    uint8_t* Vp = base + voff;
+    const bool hist = !CROSS && kv.hist != nullptr;
     const int nk = CROSS ? kCtx : pos + 1;                         // rows attended
     const int nmem = CROSS ? kCtx : pos;                           // rows read from memory
     const int npass = (nk + 7) >> 3;
@@ -323,14 +332,15 @@ self_attn_step_kernel(const float* __restrict__ qkv, int64_t q_ld, int heads, KV
         const int j = pass * 8 + r;
         if (pass < npass && j < nmem) {
             const int st = pass % kStepDepth;
-            cp_async16(&rg[st][0][lane], Kp + (int64_t)j * 64 + sub * 16);
-            cp_async16(&rg[st][1][lane], Vp + (int64_t)j * 64 + sub * 16);
+            const uint8_t* rb = hist ? kvb + shist[j] : base;      // the cache that holds row j
+            cp_async16(&rg[st][0][lane], rb + koff + (int64_t)j * 64 + sub * 16);
+            cp_async16(&rg[st][1][lane], rb + voff + (int64_t)j * 64 + sub * 16);
         }
         cp_async_commit();      // one group per pass, empty or not
     };
 #pragma unroll
     for (int u = 0; u < kStepDepth; ++u) issue(u);
-    const float ks = kv.k_scale[chunk], vs = kv.v_scale[chunk];
+    const float ks = kv.k_scale[kc], vs = kv.v_scale[kc];
     const float* qr = qkv + chunk * q_ld + h * 64 + sub * 16;
     // the current token's cache rows, quantised as the append kernel does
     uint4 kcur = make_uint4(0, 0, 0, 0), vcur = kcur;

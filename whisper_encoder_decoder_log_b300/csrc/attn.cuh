@@ -34,6 +34,12 @@ struct KVView {
     // active_len[c] <= *pos_dev + 1 has finished and is skipped.
     const int* pos_dev = nullptr;
     const int32_t* active_len = nullptr;
+    // Beam search: query row c reads the cross K/V (and their scales) of
+    // chunk c / beam_div; and, when hist is set, cache row j of row c (j <
+    // the current position) lives in the cache of row hist[c * 448 + j] (the
+    // row whose hypothesis wrote it).
+    int beam_div = 1;
+    const int32_t* hist = nullptr;
 };
 
 // Encoder self-attention, bf16, on tcgen05 (TMEM accumulators, TMA-fed tiles):

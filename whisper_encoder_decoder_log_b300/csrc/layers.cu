@@ -421,6 +421,157 @@ argmax_kernel(const float* __restrict__ logits, int64_t ld, int64_t rows, int V,
     }
 }
 
+// ------------------------------------------------------------------ beam search
+// One beam-search step for one chunk (K rows r0 .. r0+K-1, one hypothesis
+// each; "thewhisper-large-v3-turbo", "NVIDIA Usage": num_beams): every
+// continuation (b, v) scores scores[b] + (logit[b][v] - logZ_b), logZ_b the
+// log-sum-exp of row b; the K best (ties: lower beam, then lower token) become
+// the new hypotheses: their token rows and cache histories are the parents'
+// up to position pos, the chosen token goes to column pos + 1 and the cache
+// row the next step appends (pos + 1) is the new row's own.
+constexpr int kSelThreads = 512;
+
+__device__ __forceinline__ bool cand_better(float s1, int b1, int v1, float s2, int b2, int v2) {
+    return s1 > s2 || (s1 == s2 && (b1 < b2 || (b1 == b2 && v1 < v2)));
+}
+
+__global__ void __launch_bounds__(kSelThreads)
+beam_select_kernel(const float* __restrict__ logits, int64_t ld, int K, int V, float* __restrict__ scores,
+                   int32_t* __restrict__ tokens, int32_t* __restrict__ hist, const int32_t* __restrict__ len,
+                   const int* __restrict__ pos_dev, int pos_host, int32_t* __restrict__ parents_out,
+                   float* __restrict__ scores_out) {
+    griddep_wait();
+    griddep_launch();
+    __shared__ float logz[kBeamMax];
+    __shared__ float rf[kSelThreads / 32];
+    __shared__ int rb[kSelThreads / 32], rv[kSelThreads / 32], rt[kSelThreads / 32];
+    __shared__ float sel_s[kBeamMax];
+    __shared__ int sel_b[kBeamMax], sel_v[kBeamMax];
+    __shared__ int32_t stok[kBeamMax][kMaxPos], shis[kBeamMax][kMaxPos];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int64_t r0 = (int64_t)blockIdx.x * K;
+    const int pos = pos_dev ? *pos_dev : pos_host;
+    if (len[r0] <= pos + 1) return;                 // this chunk has reached its length (uniform)
+    // log-sum-exp of every hypothesis's logits
+    for (int b = 0; b < K; ++b) {
+        const float* x = logits + (r0 + b) * ld;
+        float m = -INFINITY;
+        for (int v = tid; v < V; v += kSelThreads) m = fmaxf(m, x[v]);
+        m = warp_max(m);
+        if (lane == 0) rf[warp] = m;
+        __syncthreads();
+        m = rf[0];
+        for (int w = 1; w < kSelThreads / 32; ++w) m = fmaxf(m, rf[w]);
+        __syncthreads();
+        float sum = 0.f;
+        for (int v = tid; v < V; v += kSelThreads) sum += expf(x[v] - m);
+        sum = warp_sum(sum);
+        if (lane == 0) rf[warp] = sum;
+        __syncthreads();
+        if (tid == 0) {
+            float t = 0.f;
+            for (int w = 0; w < kSelThreads / 32; ++w) t += rf[w];
+            logz[b] = m + logf(t);
+        }
+        __syncthreads();
+    }
+    // each thread's K best continuations, sorted
+    float ls[kBeamMax];
+    int lb[kBeamMax], lv[kBeamMax];
+    int n = 0;
+    for (int b = 0; b < K; ++b) {
+        const float base = scores[r0 + b], lz = logz[b];
+        const float* x = logits + (r0 + b) * ld;
+        for (int v = tid; v < V; v += kSelThreads) {
+            const float sc = base + (x[v] - lz);
+            if (n == K && !cand_better(sc, b, v, ls[K - 1], lb[K - 1], lv[K - 1])) continue;
+            int i = n < K ? n++ : K - 1;
+            while (i > 0 && cand_better(sc, b, v, ls[i - 1], lb[i - 1], lv[i - 1])) {
+                ls[i] = ls[i - 1]; lb[i] = lb[i - 1]; lv[i] = lv[i - 1];
+                --i;
+            }
+            ls[i] = sc; lb[i] = b; lv[i] = v;
+        }
+    }
+    // K rounds: the best head among all threads' lists wins and is popped
+    int head = 0;
+    for (int k = 0; k < K; ++k) {
+        float s = head < n ? ls[head] : -INFINITY;
+        int b = head < n ? lb[head] : 0x7FFFFFFF, v = head < n ? lv[head] : 0x7FFFFFFF, t = tid;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
+            const int b2 = __shfl_xor_sync(0xffffffffu, b, o), v2 = __shfl_xor_sync(0xffffffffu, v, o);
+            const int t2 = __shfl_xor_sync(0xffffffffu, t, o);
+            if (cand_better(s2, b2, v2, s, b, v) || (s2 == s && b2 == b && v2 == v && t2 < t)) {
+                s = s2; b = b2; v = v2; t = t2;
+            }
+        }
+        if (lane == 0) { rf[warp] = s; rb[warp] = b; rv[warp] = v; rt[warp] = t; }
+        __syncthreads();
+        if (tid == 0) {
+            int w0 = 0;
+            for (int w = 1; w < kSelThreads / 32; ++w)
+                if (cand_better(rf[w], rb[w], rv[w], rf[w0], rb[w0], rv[w0])) w0 = w;
+            sel_s[k] = rf[w0]; sel_b[k] = rb[w0]; sel_v[k] = rv[w0];
+            rt[0] = rt[w0];
+        }
+        __syncthreads();
+        if (tid == rt[0]) ++head;
+        __syncthreads();
+    }
+    // gather the parents' token rows and cache histories (positions 0 .. pos)
+    for (int i = tid; i < K * (pos + 1); i += kSelThreads) {
+        const int b = i / (pos + 1), q = i % (pos + 1);
+        stok[b][q] = tokens[(r0 + b) * kMaxPos + q];
+        shis[b][q] = hist[(r0 + b) * kMaxPos + q];
+    }
+    __syncthreads();
+    for (int i = tid; i < K * (pos + 1); i += kSelThreads) {
+        const int j = i / (pos + 1), q = i % (pos + 1);
+        const int p = sel_b[j];
+        tokens[(r0 + j) * kMaxPos + q] = stok[p][q];
+        hist[(r0 + j) * kMaxPos + q] = shis[p][q];
+    }
+    if (tid < K) {
+        const int j = tid;
+        if (pos + 1 < kMaxPos) {
+            tokens[(r0 + j) * kMaxPos + pos + 1] = sel_v[j];
+            hist[(r0 + j) * kMaxPos + pos + 1] = (int32_t)(r0 + j);
+        }
+        scores[r0 + j] = sel_s[j];
+        if (parents_out) parents_out[r0 + j] = sel_b[j];
+        if (scores_out) scores_out[r0 + j] = sel_s[j];
+    }
+}
+
+// The best hypothesis of each chunk (lowest beam index among the maximal
+// scores): its token row (positions 0 .. len - 1) into out[c].
+__global__ void beam_best_kernel(const float* __restrict__ scores, const int32_t* __restrict__ tokens, int K,
+                                 const int32_t* __restrict__ len, int32_t* __restrict__ out,
+                                 float* __restrict__ score_out) {
+    griddep_wait();
+    griddep_launch();
+    const int64_t c = blockIdx.x, r0 = c * K;
+    int best = 0;
+    for (int b = 1; b < K; ++b)
+        if (scores[r0 + b] > scores[r0 + best]) best = b;
+    const int L = len[r0];
+    for (int q = threadIdx.x; q < L; q += blockDim.x) out[c * kMaxPos + q] = tokens[(r0 + best) * kMaxPos + q];
+    if (threadIdx.x == 0 && score_out) score_out[c] = scores[r0 + best];
+}
+
+// hist[r][q] = r (every row starts with its own cache rows); scores: 0 for
+// the first row of each chunk, -inf for the others (one live hypothesis).
+__global__ void beam_init_kernel(int32_t* __restrict__ hist, float* __restrict__ scores, int64_t rows, int K) {
+    griddep_wait();
+    griddep_launch();
+    const int64_t r = blockIdx.x;
+    if (r >= rows) return;
+    for (int q = threadIdx.x; q < kMaxPos; q += blockDim.x) hist[r * kMaxPos + q] = (int32_t)r;
+    if (threadIdx.x == 0) scores[r] = (r % K == 0) ? 0.f : -INFINITY;
+}
+
 // conv weight [O][C][3] -> GEMM operand [O][3][C] (k index = j * C + c).
 // With dup, every tap j is stored twice ([o][j][hi | lo][c], k index
 // (2 j + half) C + c): the weights of a stem GEMM whose input rows carry each
@@ -719,6 +870,33 @@ wb_status argmax_tokens(const float* logits, int64_t ld, int64_t rows, int V, in
                         const int* pos_dev, int pos_host, cudaStream_t s) {
     if (rows <= 0) return WB_OK;
     WB_CUDA(launch_k(argmax_kernel, dim3((unsigned)rows), dim3(256), 0, s, logits, ld, rows, V, tokens, len, pos_dev, pos_host));
+    WB_CUDA(cudaGetLastError());
+    return WB_OK;
+}
+
+wb_status beam_select(const float* logits, int64_t ld, int64_t n_chunks, int K, int V, float* scores, int32_t* tokens,
+                      int32_t* hist, const int32_t* len, const int* pos_dev, int pos_host, int32_t* parents_out,
+                      float* scores_out, cudaStream_t s) {
+    if (n_chunks <= 0) return WB_OK;
+    if (K < 1 || K > kBeamMax) return fail(WB_ERR_SHAPE, "beam search: 1 <= beams <= 8");
+    WB_CUDA(launch_k(beam_select_kernel, dim3((unsigned)n_chunks), dim3(kSelThreads), 0, s, logits, ld, K, V, scores,
+                     tokens, hist, len, pos_dev, pos_host, parents_out, scores_out));
+    WB_CUDA(cudaGetLastError());
+    return WB_OK;
+}
+
+wb_status beam_best(const float* scores, const int32_t* tokens, int64_t n_chunks, int K, const int32_t* len,
+                    int32_t* out, float* score_out, cudaStream_t s) {
+    if (n_chunks <= 0) return WB_OK;
+    WB_CUDA(launch_k(beam_best_kernel, dim3((unsigned)n_chunks), dim3(128), 0, s, scores, tokens, K, len, out,
+                     score_out));
+    WB_CUDA(cudaGetLastError());
+    return WB_OK;
+}
+
+wb_status beam_init(int32_t* hist, float* scores, int64_t rows, int K, cudaStream_t s) {
+    if (rows <= 0) return WB_OK;
+    WB_CUDA(launch_k(beam_init_kernel, dim3((unsigned)rows), dim3(128), 0, s, hist, scores, rows, K));
     WB_CUDA(cudaGetLastError());
     return WB_OK;
 }

@@ -58,6 +58,18 @@ wb_status fill(float* x, int64_t n, float v, cudaStream_t s);
 // [layers][gB][K|V][n] into out [layers][B][K|V][n], scale [layers][K|V][B].
 wb_status cross_kv_quant(const void* tmp, int64_t gB, int64_t B, int64_t g0, int layers, int64_t n, uint8_t* out,
                          float* scale, cudaStream_t s);
+// Beam search (at most kBeamMax hypotheses per chunk; rows r0 = c K .. c K +
+// K - 1 are chunk c's): one selection step over the logits of the first
+// n_chunks chunks' rows at position pos (= *pos_dev when set), updating
+// scores, token rows and cache histories [rows][448]; the best hypothesis
+// per chunk; the initial histories and scores.
+constexpr int kBeamMax = 8;
+wb_status beam_select(const float* logits, int64_t ld, int64_t n_chunks, int K, int V, float* scores, int32_t* tokens,
+                      int32_t* hist, const int32_t* len, const int* pos_dev, int pos_host, int32_t* parents_out,
+                      float* scores_out, cudaStream_t s);
+wb_status beam_best(const float* scores, const int32_t* tokens, int64_t n_chunks, int K, const int32_t* len,
+                    int32_t* out, float* score_out, cudaStream_t s);
+wb_status beam_init(int32_t* hist, float* scores, int64_t rows, int K, cudaStream_t s);
 wb_status argmax_tokens(const float* logits, int64_t ld, int64_t rows, int V, int32_t* tokens, const int32_t* len,
                         const int* pos_dev, int pos_host, cudaStream_t s);
 // conv weight [O][C][3] -> [O][3][C]; dup: [O][3][2][C] (each tap twice, for
