@@ -355,6 +355,29 @@ WB_API wb_status wb_stitch_tokens(int32_t n_req, const int64_t* req_samples, int
                                   const int32_t* tokens, const int32_t* chunk_len, int32_t prefix_len,
                                   int32_t* out, int64_t out_cap, int64_t* out_offset);
 
+/*
+ * Continuous batching ("whisper-blaze 0.1.8", "Serving at Scale": requests of
+ * mixed lengths batched together).  The same transcription as
+ * wb_transcribe_batch, but instead of fixed waves the decoder keeps S slots
+ * busy: S = min(n_chunks, wave_budget_bytes / per-slot bytes), a slot holding
+ * one chunk's cross-attention K/V, a 448-row E4M3 cache and a token row.
+ * Every chunk first goes through the mel and the encoder; then chunks,
+ * longest first, enter free slots in groups of up to R = clamp(S / 8, 1, 32)
+ * (their cross K/V and forced prefix are computed in a staging decoder and
+ * moved into the slots), and each step -- one CUDA graph over all S slots --
+ * advances every slot at its own position; a slot whose chunk has reached its
+ * length is masked until it is refilled.  A chunk's tokens do not depend on
+ * the slot it ran in or on the other chunks.  Needs a bf16 or mixed_fp8
+ * model with kv_fp8 != 0.  n_slots_out [host] optional: S.
+ */
+WB_API size_t wb_transcribe_workspace_size_continuous(const wb_model* model, int32_t n_req,
+                                                      const int64_t* req_samples, uint64_t wave_budget_bytes);
+WB_API wb_status wb_transcribe_batch_continuous(wb_model* model, const float* audio, const int64_t* req_offset,
+                                                const int64_t* req_samples, int32_t n_req, const int32_t* prefix,
+                                                const int32_t* chunk_len, int32_t* tokens,
+                                                uint64_t wave_budget_bytes, void* workspace,
+                                                size_t workspace_bytes, int32_t* n_slots_out, wb_stream stream);
+
 /* Wave plan alone (host only): wave_of_chunk[host] int32 [n_chunks],
  * order[host] int32 [n_chunks] chunk indices in decode order. */
 WB_API wb_status wb_plan_waves(const wb_model_desc* desc, int32_t n_chunks,

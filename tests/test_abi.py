@@ -122,6 +122,9 @@ def test_host_side_argument_checks_need_no_gpu():
     # the failure-detection hook rejects limits outside (0, 1 s] without arming
     assert L.wb_debug_stall_next_gemm(0) == -1
     assert L.wb_debug_stall_next_gemm(2 * 10**9) == -1
+    # continuous batching: null arguments and an empty request list
+    assert L.wb_transcribe_batch_continuous(None, 16, 16, 16, 1, 16, 16, 16, 1 << 30, 16, 1 << 30, None, None) == -1
+    assert L.wb_transcribe_workspace_size_continuous(None, 1, None, 1 << 30) == 0
 
 
 def test_kv_modes_are_validated_on_the_host():

@@ -61,6 +61,9 @@ _SIGS = {
     "wb_transcribe_batch": (ctypes.c_int, [_VP, _VP, _VP, _VP, _I32, _VP, _VP, _VP, _U64, _VP, _SZ, _VP, _VP]),
     "wb_plan_waves": (ctypes.c_int, [ctypes.POINTER(ModelDesc), _I32, _VP, _U64, _VP, _VP, _VP]),
     "wb_chunk_count": (_I64, [_I32, _VP, _I64]),
+    "wb_transcribe_workspace_size_continuous": (_SZ, [_VP, _I32, _VP, _U64]),
+    "wb_transcribe_batch_continuous": (ctypes.c_int, [_VP, _VP, _VP, _VP, _I32, _VP, _VP, _VP, _U64, _VP, _SZ, _VP,
+                                                      _VP]),
     "wb_transcribe_workspace_size_overlap": (_SZ, [_VP, _I32, _VP, _VP, _U64, _I64]),
     "wb_transcribe_batch_overlap": (ctypes.c_int, [_VP, _VP, _VP, _VP, _I32, _I64, _VP, _VP, _VP, _U64, _VP, _SZ,
                                                    _VP, _VP]),
@@ -264,6 +267,27 @@ def wb_transcribe_batch(model: int, audio, req_offset, req_samples, prefix, chun
                                      _p(workspace), workspace.numel() * workspace.element_size(),
                                      ctypes.addressof(nw), _stream(stream)))
     return nw.value
+
+
+def wb_transcribe_workspace_size_continuous(model: int, req_samples, budget: int) -> int:
+    rs, rsp = _host_arr(req_samples, np.int64)
+    return lib().wb_transcribe_workspace_size_continuous(model, rs.size, rsp, budget)
+
+
+def wb_transcribe_batch_continuous(model: int, audio, req_offset, req_samples, prefix, chunk_len, tokens, budget: int,
+                                   workspace, stream=None) -> int:
+    """Transcribe with continuous batching; returns the number of slots."""
+    ro, rop = _host_arr(req_offset, np.int64)
+    rs, rsp = _host_arr(req_samples, np.int64)
+    pf, pfp = _host_arr(prefix, np.int32)
+    cl, clp = _host_arr(chunk_len, np.int32)
+    _need(audio, "float32", "audio")
+    _need(tokens, "int32", "tokens")
+    ns = _I32(0)
+    _check(lib().wb_transcribe_batch_continuous(model, _p(audio), rop, rsp, rs.size, pfp, clp, _p(tokens), budget,
+                                                _p(workspace), workspace.numel() * workspace.element_size(),
+                                                ctypes.addressof(ns), _stream(stream)))
+    return ns.value
 
 
 def wb_chunk_count(req_samples, overlap: int = 0) -> int:

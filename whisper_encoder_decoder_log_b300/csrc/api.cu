@@ -434,6 +434,11 @@ struct wb_decoder {
     float* scores = nullptr;           // [rows] running log-probability sums
     int32_t* step_parents = nullptr;   // caller buffers of the current step (or null)
     float* step_scores = nullptr;
+    // continuous batching: one position per row (pos_dev[row]) and cache
+    // layout lengths (448 per slot) apart from the rows' decode lengths
+    int pos_stride = 0;
+    int32_t* lay_dev = nullptr;
+    int32_t* lay_buf = nullptr;
 };
 
 namespace wb {
@@ -479,13 +484,16 @@ size_t carve_decoder(const wb_model* m, int64_t B, const int32_t* len, wb_decode
     uint8_t* fq = c.take<uint8_t>((size_t)R * F);
     float* f_scale = c.take<float>(R);
     float* logits = c.take<float>((size_t)B * ((m->desc.vocab + 7) / 8 * 8));
-    int* pos_dev = c.take<int>(64);
+    int* pos_dev = c.take<int>((size_t)std::max<int64_t>(64, B));   // one per row with per-row positions
+    int32_t* lay = c.take<int32_t>(B);
     if (dec) {
         dec->beams = beams;
         dec->n_cross = NC;
         dec->hist = hist;
         dec->scores = scores;
         dec->pos_dev = pos_dev;
+        dec->lay_dev = nullptr;     // set (to lay_buf) by decoders whose layout differs from their lengths
+        dec->lay_buf = lay;
         dec->crosskv = crosskv; dec->ckv_tmp = ckv_tmp; dec->cscale = cscale;
         dec->cache = cache; dec->kscale = kscale; dec->vscale = vscale;
         dec->off = off; dec->len_dev = lend; dec->h = h; dec->a = a; dec->a_scale = a_scale; dec->qkv = qkv;
@@ -581,7 +589,8 @@ wb_status decoder_layers(wb_decoder* dec, int64_t n_chunks, int rows_per_chunk, 
             kv.ptr = dec->cache; kv.chunk_off = dec->off; kv.head_stride = 64; kv.chunk_len = dec->len_dev;
             kv.heads = H; kv.k_blk = 2 * l; kv.v_blk = 2 * l + 1; kv.row_stride = 64;
             if (kv8) { kv.k_scale = ks; kv.v_scale = vs; }
-            if (pos_dev) { kv.pos_dev = pos_dev; kv.active_len = dec->len_dev; }
+            if (pos_dev) { kv.pos_dev = pos_dev; kv.active_len = dec->len_dev; kv.pos_stride = dec->pos_stride; }
+            if (dec->lay_dev) kv.chunk_len = dec->lay_dev;
             if (dec->beams > 1 && rows_per_chunk == 1) kv.hist = dec->hist;
             if (fused_step) {
                 if (wb_status st = attn_self_step_e4m3(dec->qkv, 3 * d, n_chunks, H, kv, p0, dec->attn, lda, s,
@@ -616,6 +625,7 @@ wb_status decoder_layers(wb_decoder* dec, int64_t n_chunks, int rows_per_chunk, 
             kv.chunk_stride = (int64_t)2 * H * kCtx * 64; kv.head_stride = (int64_t)kCtx * 64; kv.heads = H;
             kv.k_blk = 0; kv.v_blk = 1; kv.row_stride = 64;
             kv.beam_div = dec->beams;
+            kv.pos_stride = dec->pos_stride;
             if (c8) {
                 kv.k_scale = dec->cscale + (size_t)(2 * l) * dec->n_cross;
                 kv.v_scale = dec->cscale + (size_t)(2 * l + 1) * dec->n_cross;
@@ -696,7 +706,8 @@ wb_status decoder_head(wb_decoder* dec, int64_t n_chunks, int rows_per_chunk, in
     if (dec->beams > 1)
         return beam_select(dec->logits, ldl, n_chunks / dec->beams, dec->beams, V, dec->scores, dec->tokens, dec->hist,
                            dec->len_dev, pos_dev, pos_last, dec->step_parents, dec->step_scores, s);
-    return argmax_tokens(dec->logits, ldl, n_chunks, V, dec->tokens, dec->len_dev, pos_dev, pos_last, s);
+    return argmax_tokens(dec->logits, ldl, n_chunks, V, dec->tokens, dec->len_dev, pos_dev, pos_last, s,
+                         dec->pos_stride);
 }
 
 __global__ void gather_chunks_kernel(const float* __restrict__ audio, const int64_t* __restrict__ src,
@@ -1007,15 +1018,14 @@ size_t wb_decoder_workspace_size(const wb_model* m, int64_t B, const int32_t* le
 }
 
 // A decoder over n_chunks chunks with `beams` hypotheses each (rows c*beams
-// .. c*beams + beams - 1 belong to chunk c); the cross K/V are computed once
-// per chunk.
-static wb_status decoder_init(wb_model* m, int64_t n_chunks, const int32_t* chunk_len, int beams, const void* enc,
-                              int32_t* tokens, void* workspace, size_t ws_bytes, wb_stream stream, wb_decoder** out) {
+// .. c*beams + beams - 1 belong to chunk c), without its cross K/V yet.
+static wb_status decoder_setup(wb_model* m, int64_t n_chunks, const int32_t* chunk_len, int beams, int32_t* tokens,
+                               void* workspace, size_t ws_bytes, wb_stream stream, wb_decoder** out) {
     if (!out) return fail(WB_ERR_INVALID_ARG, "wb_decoder_init: null out");
     *out = nullptr;
-    if (!m || !chunk_len || !enc || !tokens || !workspace) return fail(WB_ERR_INVALID_ARG, "wb_decoder_init: null argument");
+    if (!m || !chunk_len || !tokens || !workspace) return fail(WB_ERR_INVALID_ARG, "wb_decoder_init: null argument");
     if (n_chunks < 1 || n_chunks * beams > 65535) return fail(WB_ERR_SHAPE, "wb_decoder_init: B * beams must be in [1, 65535]");
-    if (!aligned16(enc) || !aligned16(tokens) || !aligned16(workspace)) return fail(WB_ERR_ALIGN, "wb_decoder_init: alignment");
+    if (!aligned16(tokens) || !aligned16(workspace)) return fail(WB_ERR_ALIGN, "wb_decoder_init: alignment");
     for (int64_t i = 0; i < n_chunks; ++i) {
         if (chunk_len[i] < 1 || chunk_len[i] > kMaxPos) return fail(WB_ERR_SHAPE, "wb_decoder_init: chunk_len must be in [1, 448]");
         if (i && chunk_len[i] > chunk_len[i - 1]) return fail(WB_ERR_SHAPE, "wb_decoder_init: chunk_len must be non-increasing");
@@ -1036,7 +1046,7 @@ static wb_status decoder_init(wb_model* m, int64_t n_chunks, const int32_t* chun
         return fail(WB_ERR_SHAPE, "wb_decoder_init: workspace too small");
     }
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    const int d = m->d(), H = m->H(), Ld = m->desc.dec_layers;
+    const int H = m->H(), Ld = m->desc.dec_layers;
     // per-row cache offsets (elements) and lengths
     std::vector<int64_t> off(B);
     int64_t acc = 0;
@@ -1051,35 +1061,57 @@ static wb_status decoder_init(wb_model* m, int64_t n_chunks, const int32_t* chun
         return fail_free(fail(WB_ERR_CUDA, "wb_decoder_init: upload"));
     if (beams > 1)
         if (wb_status st = beam_init(dec->hist, dec->scores, B, beams, s)) return fail_free(st);
-    const int64_t NC = n_chunks;
-    if (Ld > 0 && m->desc.kv_fp8 != WB_KV_FP8_CROSS) {
+    *out = dec;
+    return WB_OK;
+}
+
+// Cross-attention K/V of every decoder layer for the first NC chunks of the
+// decoder from their encoder states enc [NC, 1500, d].
+static wb_status compute_cross_kv(wb_decoder* dec, const void* enc, int64_t NC, cudaStream_t s) {
+    wb_model* m = dec->m;
+    const int d = m->d(), H = m->H(), Ld = m->desc.dec_layers;
+    if (Ld <= 0 || NC <= 0) return WB_OK;
+    if (m->desc.kv_fp8 != WB_KV_FP8_CROSS) {
         Lin L;
         L.a = enc; L.rows = NC * kCtx; L.lda = d; L.w = m->W("dec.0.ck.w"); L.N = (int64_t)Ld * 2 * d; L.K = d;
         GemmEpi ep = epi_out(dec->crosskv, 0, m->fp32() ? OUT_F32 : OUT_BF16, m->V("dec.0.ck.b"));
         ep.mode = MODE_CROSS_KV;
         ep.ckv_d = d;
         ep.ckv_heads = H;
-        ep.ckv_chunks = NC;
-        if (wb_status st = linear(m, L, ep, s)) return fail_free(st);
-    } else if (Ld > 0) {
-        // E4M3 cross K/V: per group of chunks, the fp32 projection into a
-        // scratch area, then one amax / 448 scale and the codes per (chunk,
-        // layer, K|V) tensor, rounded once from fp32
-        for (int64_t g0 = 0; g0 < NC; g0 += kCrossGroup) {
-            const int64_t gB = std::min<int64_t>(kCrossGroup, NC - g0);
-            Lin L;
-            L.a = reinterpret_cast<const __nv_bfloat16*>(enc) + g0 * kCtx * d;
-            L.rows = gB * kCtx; L.lda = d; L.w = m->W("dec.0.ck.w"); L.N = (int64_t)Ld * 2 * d; L.K = d;
-            GemmEpi ep = epi_out(dec->ckv_tmp, 0, OUT_F32, m->V("dec.0.ck.b"));
-            ep.mode = MODE_CROSS_KV;
-            ep.ckv_d = d;
-            ep.ckv_heads = H;
-            ep.ckv_chunks = gB;
-            if (wb_status st = linear(m, L, ep, s)) return fail_free(st);
-            if (wb_status st = cross_kv_quant(dec->ckv_tmp, gB, NC, g0, Ld, (int64_t)H * kCtx * 64,
-                                              reinterpret_cast<uint8_t*>(dec->crosskv), dec->cscale, s))
-                return fail_free(st);
-        }
+        ep.ckv_chunks = dec->n_cross;
+        return linear(m, L, ep, s);
+    }
+    // E4M3 cross K/V: per group of chunks, the fp32 projection into a scratch
+    // area, then one amax / 448 scale and the codes per (chunk, layer, K|V)
+    // tensor, rounded once from fp32
+    for (int64_t g0 = 0; g0 < NC; g0 += kCrossGroup) {
+        const int64_t gB = std::min<int64_t>(kCrossGroup, NC - g0);
+        Lin L;
+        L.a = reinterpret_cast<const __nv_bfloat16*>(enc) + g0 * kCtx * d;
+        L.rows = gB * kCtx; L.lda = d; L.w = m->W("dec.0.ck.w"); L.N = (int64_t)Ld * 2 * d; L.K = d;
+        GemmEpi ep = epi_out(dec->ckv_tmp, 0, OUT_F32, m->V("dec.0.ck.b"));
+        ep.mode = MODE_CROSS_KV;
+        ep.ckv_d = d;
+        ep.ckv_heads = H;
+        ep.ckv_chunks = gB;
+        if (wb_status st = linear(m, L, ep, s)) return st;
+        if (wb_status st = cross_kv_quant(dec->ckv_tmp, gB, dec->n_cross, g0, Ld, (int64_t)H * kCtx * 64,
+                                          reinterpret_cast<uint8_t*>(dec->crosskv), dec->cscale, s))
+            return st;
+    }
+    return WB_OK;
+}
+
+static wb_status decoder_init(wb_model* m, int64_t n_chunks, const int32_t* chunk_len, int beams, const void* enc,
+                              int32_t* tokens, void* workspace, size_t ws_bytes, wb_stream stream, wb_decoder** out) {
+    if (!enc) return fail(WB_ERR_INVALID_ARG, "wb_decoder_init: null argument");
+    if (!aligned16(enc)) return fail(WB_ERR_ALIGN, "wb_decoder_init: alignment");
+    wb_decoder* dec = nullptr;
+    if (wb_status st = decoder_setup(m, n_chunks, chunk_len, beams, tokens, workspace, ws_bytes, stream, &dec))
+        return st;
+    if (wb_status st = compute_cross_kv(dec, enc, n_chunks, reinterpret_cast<cudaStream_t>(stream))) {
+        delete dec;
+        return st;
     }
     *out = dec;
     return WB_OK;
@@ -1127,11 +1159,11 @@ wb_status wb_decode_prefix(wb_decoder* dec, int32_t P, float* logits, wb_stream 
 static wb_status run_step(wb_decoder* dec, int64_t rows, float* logits, cudaStream_t s) {
     wb_model* m = dec->m;
     if (wb_status st = embed(dec->tokens, rows, 1, dec->pos, m->d(), m->W("dec.tok"), m->W("dec.pos"), !m->fp32(),
-                             m->desc.vocab, dec->h, m->err, s, dec->pos_dev, dec->len_dev))
+                             m->desc.vocab, dec->h, m->err, s, dec->pos_dev, dec->len_dev, dec->pos_stride))
         return st;
     if (wb_status st = decoder_layers(dec, rows, 1, dec->pos, false, s, dec->pos_dev)) return st;
     if (wb_status st = decoder_head(dec, rows, 1, dec->pos, logits, s, dec->pos_dev)) return st;
-    return set_pos(dec->pos_dev, 1, true, s);
+    return set_pos(dec->pos_dev, 1, true, s, dec->pos_stride ? (int)rows : 1);
 }
 
 static bool graphs_enabled() {
@@ -1139,23 +1171,10 @@ static bool graphs_enabled() {
     return !(e && e[0] == '1');
 }
 
-wb_status wb_decode_step(wb_decoder* dec, int64_t n_active, float* logits, wb_stream stream) {
-    if (!dec) return fail(WB_ERR_INVALID_ARG, "wb_decode_step: null decoder");
-    if (dec->beams > 1) return fail(WB_ERR_INVALID_ARG, "wb_decode_step: a beam decoder steps with wb_decode_step_beams");
-    if (dec->P == 0) return fail(WB_ERR_INVALID_ARG, "wb_decode_step: run wb_decode_prefix first");
-    if (n_active < 1 || n_active > dec->B) return fail(WB_ERR_SHAPE, "wb_decode_step: bad n_active");
-    if (dec->len[n_active - 1] <= dec->pos + 1)
-        return fail(WB_ERR_SHAPE, "wb_decode_step: an active chunk has reached its length");
-    if (logits && !aligned16(logits)) return fail(WB_ERR_ALIGN, "wb_decode_step: logits alignment");
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    // logits for the caller, or per-kernel timing: launch directly with exactly n_active rows
-    if (logits || !graphs_enabled() || prof_any_active()) {
-        if (wb_status st = run_step(dec, n_active, logits, s)) return st;
-        dec->pos += 1;
-        return WB_OK;
-    }
-    // graph replay: rows rounded up to a 128-row bucket (finished chunks are masked)
-    const int64_t rows = std::min<int64_t>(dec->B, (n_active + 127) / 128 * 128);
+// One decode step over `rows` rows, replayed from a CUDA graph captured the
+// first time this row count is used (the step reads its positions from the
+// device, so the same graph serves every step).
+static wb_status replay_step(wb_decoder* dec, int64_t rows, cudaStream_t s) {
     StepGraph* g = nullptr;
     for (auto& x : dec->graphs)
         if (x.rows == rows) g = &x;
@@ -1185,6 +1204,27 @@ wb_status wb_decode_step(wb_decoder* dec, int64_t n_active, float* logits, wb_st
     }
     WB_CUDA(cudaGraphLaunch(g->exec, s));
     count_launch((int)g->kernels);
+    return WB_OK;
+}
+
+wb_status wb_decode_step(wb_decoder* dec, int64_t n_active, float* logits, wb_stream stream) {
+    if (!dec) return fail(WB_ERR_INVALID_ARG, "wb_decode_step: null decoder");
+    if (dec->beams > 1) return fail(WB_ERR_INVALID_ARG, "wb_decode_step: a beam decoder steps with wb_decode_step_beams");
+    if (dec->P == 0) return fail(WB_ERR_INVALID_ARG, "wb_decode_step: run wb_decode_prefix first");
+    if (n_active < 1 || n_active > dec->B) return fail(WB_ERR_SHAPE, "wb_decode_step: bad n_active");
+    if (dec->len[n_active - 1] <= dec->pos + 1)
+        return fail(WB_ERR_SHAPE, "wb_decode_step: an active chunk has reached its length");
+    if (logits && !aligned16(logits)) return fail(WB_ERR_ALIGN, "wb_decode_step: logits alignment");
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    // logits for the caller, or per-kernel timing: launch directly with exactly n_active rows
+    if (logits || !graphs_enabled() || prof_any_active()) {
+        if (wb_status st = run_step(dec, n_active, logits, s)) return st;
+        dec->pos += 1;
+        return WB_OK;
+    }
+    // graph replay: rows rounded up to a 128-row bucket (finished chunks are masked)
+    const int64_t rows = std::min<int64_t>(dec->B, (n_active + 127) / 128 * 128);
+    if (wb_status st = replay_step(dec, rows, s)) return st;
     dec->pos += 1;
     return WB_OK;
 }
@@ -1518,6 +1558,253 @@ static wb_status transcribe_impl(wb_model* m, const float* audio, const int64_t*
         WB_CUDA(cudaGetLastError());
     }
     if (n_waves_out) *n_waves_out = (int32_t)waves.size();
+    return wb_sync_status(m, stream);
+}
+
+// ------------------------------------------------------------------ continuous batching
+// Slots of a decoder that stays full: chunks (longest first) enter free
+// slots in groups of up to R as earlier chunks finish, every slot at its own
+// position ("whisper-blaze 0.1.8", "Serving at Scale": requests of mixed
+// lengths are batched together).  Per-slot state: cross K/V, an E4M3 cache of
+// 448 rows, the token row.
+struct ContPlan {
+    int64_t S = 0, R = 0;
+};
+
+static uint64_t slot_bytes(const wb_model_desc& d) {
+    const uint64_t cross_elt = d.kv_fp8 == WB_KV_FP8_CROSS ? 1 : 2;
+    return (uint64_t)d.dec_layers * 2 * kCtx * d.d_model * cross_elt + (uint64_t)d.dec_layers * 2 * kMaxPos * d.d_model +
+           (uint64_t)kMaxPos * 4;
+}
+
+static ContPlan cont_plan(const wb_model_desc& d, int64_t n_chunks, uint64_t budget) {
+    ContPlan p;
+    p.S = std::min<int64_t>(n_chunks, (int64_t)(budget / std::max<uint64_t>(1, slot_bytes(d))));
+    p.S = std::min<int64_t>(p.S, 65535);
+    p.R = std::max<int64_t>(1, std::min<int64_t>({p.S, 32, p.S / 8}));
+    return p;
+}
+
+struct ContBufs {
+    float* chunk_audio = nullptr;
+    float* mel = nullptr;
+    uint8_t* enc_ws = nullptr;
+    size_t enc_ws_bytes = 0;
+    uint8_t* enc_all = nullptr;      // [n_chunks, 1500, d] encoder states
+    uint8_t* st_enc = nullptr;       // [R, 1500, d] states of the chunks entering slots
+    int32_t* st_tok = nullptr;       // [R, 448]
+    int32_t* sl_tok = nullptr;       // [S, 448]
+    int64_t* src = nullptr;
+    int32_t* valid = nullptr;
+    int32_t* slot_of = nullptr;      // [R]
+    int32_t* new_len = nullptr;      // [R]
+    int32_t* out_slot = nullptr;     // [S]
+    int32_t* out_chunk = nullptr;    // [S]
+    int32_t* out_len = nullptr;      // [S]
+    uint8_t* sl_ws = nullptr;
+    size_t sl_ws_bytes = 0;
+    uint8_t* st_ws = nullptr;
+    size_t st_ws_bytes = 0;
+};
+
+static size_t cont_ws(const wb_model* m, int64_t n_chunks, const ContPlan& p, uint8_t* base, size_t cap, ContBufs* cb,
+                      bool* overflow) {
+    Carve c{base, cap};
+    const int d = m->d();
+    const size_t act = m->fp32() ? 4 : 2;
+    const int64_t EB = std::min<int64_t>(kEncSubBatch, n_chunks);
+    ContBufs b;
+    b.chunk_audio = c.take<float>((size_t)EB * kChunkSamples);
+    b.mel = c.take<float>((size_t)EB * m->desc.n_mels * kFrames);
+    b.enc_ws_bytes = carve_encoder(m, EB, nullptr, nullptr, 0, nullptr);
+    b.enc_ws = c.take<uint8_t>(b.enc_ws_bytes);
+    b.enc_all = c.take<uint8_t>((size_t)n_chunks * kCtx * d * act);
+    b.st_enc = c.take<uint8_t>((size_t)p.R * kCtx * d * act);
+    b.st_tok = c.take<int32_t>((size_t)p.R * kMaxPos);
+    b.sl_tok = c.take<int32_t>((size_t)p.S * kMaxPos);
+    b.src = c.take<int64_t>(EB);
+    b.valid = c.take<int32_t>(EB);
+    b.slot_of = c.take<int32_t>(p.R);
+    b.new_len = c.take<int32_t>(p.R);
+    b.out_slot = c.take<int32_t>(p.S);
+    b.out_chunk = c.take<int32_t>(p.S);
+    b.out_len = c.take<int32_t>(p.S);
+    std::vector<int32_t> lay_s((size_t)p.S, kMaxPos), lay_r((size_t)p.R, kMaxPos);
+    b.sl_ws_bytes = carve_decoder(m, p.S, lay_s.data(), nullptr, nullptr, 0, nullptr);
+    b.sl_ws = c.take<uint8_t>(b.sl_ws_bytes);
+    b.st_ws_bytes = carve_decoder(m, p.R, lay_r.data(), nullptr, nullptr, 0, nullptr);
+    b.st_ws = c.take<uint8_t>(b.st_ws_bytes);
+    if (cb) *cb = b;
+    if (overflow) *overflow = c.overflow;
+    return align_up(c.cur, 256);
+}
+
+size_t wb_transcribe_workspace_size_continuous(const wb_model* m, int32_t n_req, const int64_t* req_samples,
+                                               uint64_t budget) {
+    if (!m || n_req < 1 || !req_samples) return 0;
+    std::vector<int32_t> req, valid;
+    std::vector<int64_t> idx;
+    if (!chunk_table(n_req, req_samples, req, idx, valid)) return 0;
+    const ContPlan p = cont_plan(m->desc, (int64_t)req.size(), budget);
+    if (p.S < 1) return 0;
+    return cont_ws(m, (int64_t)req.size(), p, nullptr, 0, nullptr, nullptr);
+}
+
+wb_status wb_transcribe_batch_continuous(wb_model* m, const float* audio, const int64_t* req_offset,
+                                         const int64_t* req_samples, int32_t n_req, const int32_t* prefix,
+                                         const int32_t* chunk_len, int32_t* tokens, uint64_t budget, void* workspace,
+                                         size_t ws_bytes, int32_t* n_slots_out, wb_stream stream) {
+    if (!m || !audio || !req_offset || !req_samples || !prefix || !chunk_len || !tokens || !workspace)
+        return fail(WB_ERR_INVALID_ARG, "wb_transcribe_batch_continuous: null argument");
+    if (n_req < 1) return fail(WB_ERR_SHAPE, "wb_transcribe_batch_continuous: n_req < 1");
+    if (!aligned16(audio) || !aligned16(tokens) || !aligned16(workspace))
+        return fail(WB_ERR_ALIGN, "wb_transcribe_batch_continuous: alignment");
+    if (m->fp32() || !m->desc.kv_fp8)
+        return fail(WB_ERR_UNSUPPORTED, "wb_transcribe_batch_continuous: needs a bf16 model with the E4M3 cache");
+    for (int i = 0; i < 4; ++i)
+        if (prefix[i] < 0 || prefix[i] >= m->desc.vocab)
+            return fail(WB_ERR_SHAPE, "wb_transcribe_batch_continuous: prefix id");
+    std::vector<int32_t> req, valid;
+    std::vector<int64_t> idx;
+    if (!chunk_table(n_req, req_samples, req, idx, valid))
+        return fail(WB_ERR_SHAPE, "wb_transcribe_batch_continuous: empty request");
+    const int64_t n = (int64_t)req.size();
+    for (int64_t c = 0; c < n; ++c)
+        if (chunk_len[c] < 5 || chunk_len[c] > kMaxPos)
+            return fail(WB_ERR_SHAPE, "wb_transcribe_batch_continuous: chunk_len must be in [5, 448]");
+    const ContPlan p = cont_plan(m->desc, n, budget);
+    if (p.S < 1) return fail(WB_ERR_SHAPE, "wb_transcribe_batch_continuous: the budget holds no slot");
+    ContBufs cb;
+    bool over = false;
+    cont_ws(m, n, p, reinterpret_cast<uint8_t*>(workspace), ws_bytes, &cb, &over);
+    if (over) return fail(WB_ERR_SHAPE, "wb_transcribe_batch_continuous: workspace too small");
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const int d = m->d(), H = m->H(), Ld = m->desc.dec_layers;
+    const size_t act = 2;
+    const size_t enc_bytes = (size_t)kCtx * d * act;
+    // ---- every chunk through mel and the encoder, in groups
+    for (int64_t c0 = 0; c0 < n; c0 += kEncSubBatch) {
+        const int64_t nb = std::min<int64_t>(kEncSubBatch, n - c0);
+        std::vector<int64_t> hsrc(nb);
+        std::vector<int32_t> hval(nb);
+        for (int64_t i = 0; i < nb; ++i) {
+            hsrc[i] = req_offset[req[c0 + i]] + idx[c0 + i] * kChunkSamples;
+            hval[i] = valid[c0 + i];
+        }
+        WB_CUDA(cudaMemcpyAsync(cb.src, hsrc.data(), nb * 8, cudaMemcpyHostToDevice, s));
+        WB_CUDA(cudaMemcpyAsync(cb.valid, hval.data(), nb * 4, cudaMemcpyHostToDevice, s));
+        WB_CUDA(cudaStreamSynchronize(s));    // pageable sources are consumed before the vectors go away
+        WB_CUDA(launch_k(gather_chunks_kernel, dim3((kChunkSamples / 4 + 255) / 256, (unsigned)nb), dim3(256), 0, s,
+                         audio, cb.src, cb.valid, cb.chunk_audio));
+        WB_CUDA(cudaGetLastError());
+        if (wb_status st = wb_mel(cb.chunk_audio, nb, m->desc.n_mels, cb.mel, stream)) return st;
+        if (wb_status st = wb_encode(m, cb.mel, nb, cb.enc_all + (size_t)c0 * enc_bytes, cb.enc_ws, cb.enc_ws_bytes,
+                                     stream))
+            return st;
+    }
+    // ---- the slot decoder (S rows, one position each) and the staging decoder (R rows)
+    std::vector<int32_t> lay_s((size_t)p.S, kMaxPos), lay_r((size_t)p.R, kMaxPos);
+    wb_decoder* sl = nullptr;
+    wb_decoder* stg = nullptr;
+    if (wb_status st = decoder_setup(m, p.S, lay_s.data(), 1, cb.sl_tok, cb.sl_ws, cb.sl_ws_bytes, stream, &sl)) return st;
+    auto done = [&](wb_status st) {
+        if (sl) wb_decoder_destroy(sl);
+        if (stg) wb_decoder_destroy(stg);
+        return st;
+    };
+    if (wb_status st = decoder_setup(m, p.R, lay_r.data(), 1, cb.st_tok, cb.st_ws, cb.st_ws_bytes, stream, &stg))
+        return done(st);
+    sl->pos_stride = 1;
+    sl->lay_dev = sl->lay_buf;
+    sl->P = 4;
+    WB_CUDA(cudaMemcpyAsync(sl->lay_dev, lay_s.data(), p.S * 4, cudaMemcpyHostToDevice, s));
+    WB_CUDA(cudaMemsetAsync(sl->len_dev, 0, p.S * 4, s));       // every slot starts empty (masked)
+    WB_CUDA(cudaMemsetAsync(sl->pos_dev, 0, p.S * 4, s));
+    WB_CUDA(cudaMemsetAsync(sl->attn, 0, (size_t)p.S * kMaxPrefix * d * 4, s));
+    WB_CUDA(cudaStreamSynchronize(s));                          // lay_s is pageable
+    // ---- schedule: longest chunks first, refills of up to R slots
+    std::vector<int32_t> order((size_t)n);
+    for (int64_t i = 0; i < n; ++i) order[i] = (int32_t)i;
+    std::stable_sort(order.begin(), order.end(), [&](int32_t a, int32_t b) { return chunk_len[a] > chunk_len[b]; });
+    std::vector<int32_t> slot_chunk((size_t)p.S, -1);     // chunk held (finished or not), -1: empty
+    std::vector<int32_t> remaining((size_t)p.S, 0);       // steps the slot's chunk still needs
+    const int64_t cross_blk = (int64_t)2 * H * kCtx * 64 * (m->desc.kv_fp8 == WB_KV_FP8_CROSS ? 1 : 2);
+    // finished chunks' token rows to the output (the listed slots)
+    auto flush = [&](const std::vector<int32_t>& slots) -> wb_status {
+        std::vector<int32_t> os, oc, ol;
+        for (int32_t q : slots)
+            if (slot_chunk[q] >= 0) {
+                os.push_back(q);
+                oc.push_back(slot_chunk[q]);
+                ol.push_back(chunk_len[slot_chunk[q]]);
+                slot_chunk[q] = -1;
+            }
+        if (os.empty()) return WB_OK;
+        const size_t k = os.size();
+        WB_CUDA(cudaMemcpyAsync(cb.out_slot, os.data(), k * 4, cudaMemcpyHostToDevice, s));
+        WB_CUDA(cudaMemcpyAsync(cb.out_chunk, oc.data(), k * 4, cudaMemcpyHostToDevice, s));
+        WB_CUDA(cudaMemcpyAsync(cb.out_len, ol.data(), k * 4, cudaMemcpyHostToDevice, s));
+        return slot_out(cb.sl_tok, cb.out_slot, cb.out_chunk, cb.out_len, (int)k, tokens, s);
+    };
+    size_t qi = 0;
+    int64_t refills = 0;
+    while (true) {
+        std::vector<int32_t> free_slots;
+        int64_t active = 0;
+        for (int64_t q = 0; q < p.S; ++q) {
+            if (remaining[q] > 0) ++active;
+            else free_slots.push_back((int32_t)q);
+        }
+        if (qi < order.size() && ((int64_t)free_slots.size() >= p.R || active == 0)) {
+            const int64_t k = std::min<int64_t>({(int64_t)free_slots.size(), p.R, (int64_t)(order.size() - qi)});
+            std::vector<int32_t> slots(free_slots.begin(), free_slots.begin() + k), chunks(k), lens(k);
+            if (wb_status st = flush(slots)) return done(st);
+            for (int64_t i = 0; i < k; ++i) {
+                chunks[i] = order[qi + i];
+                lens[i] = chunk_len[chunks[i]];
+                WB_CUDA(cudaMemcpyAsync(cb.st_enc + (size_t)i * enc_bytes, cb.enc_all + (size_t)chunks[i] * enc_bytes,
+                                        enc_bytes, cudaMemcpyDeviceToDevice, s));
+            }
+            qi += (size_t)k;
+            // the entering chunks' prefix pass in the staging decoder
+            WB_CUDA(launch_k(fill_prefix_kernel, dim3((unsigned)((p.R + 255) / 256)), dim3(256), 0, s, cb.st_tok,
+                             (int64_t)p.R, prefix[0], prefix[1], prefix[2], prefix[3]));
+            if (wb_status st = compute_cross_kv(stg, cb.st_enc, k, s)) return done(st);
+            if (wb_status st = wb_decode_prefix(stg, 4, nullptr, stream)) return done(st);
+            WB_CUDA(cudaMemcpyAsync(cb.slot_of, slots.data(), k * 4, cudaMemcpyHostToDevice, s));
+            WB_CUDA(cudaMemcpyAsync(cb.new_len, lens.data(), k * 4, cudaMemcpyHostToDevice, s));
+            if (wb_status st = slot_cross_copy(stg->crosskv, sl->crosskv, cb.slot_of, (int)k, p.R, p.S, Ld, cross_blk, s))
+                return done(st);
+            if (m->desc.kv_fp8 == WB_KV_FP8_CROSS)
+                for (int l = 0; l < Ld; ++l)
+                    for (int kv = 0; kv < 2; ++kv)
+                        for (int64_t i = 0; i < k; ++i)
+                            WB_CUDA(cudaMemcpyAsync(sl->cscale + (size_t)(2 * l + kv) * p.S + slots[i],
+                                                    stg->cscale + (size_t)(2 * l + kv) * p.R + i, 4,
+                                                    cudaMemcpyDeviceToDevice, s));
+            if (wb_status st = slot_state(reinterpret_cast<const uint8_t*>(stg->cache), reinterpret_cast<uint8_t*>(sl->cache),
+                                          stg->kscale, stg->vscale, sl->kscale, sl->vscale, cb.st_tok, cb.sl_tok,
+                                          sl->pos_dev, sl->len_dev, cb.slot_of, cb.new_len, (int)k, (int)p.R,
+                                          (int)p.S, Ld, H, kMaxPos, 4, s))
+                return done(st);
+            for (int64_t i = 0; i < k; ++i) {
+                slot_chunk[slots[i]] = chunks[i];
+                remaining[slots[i]] = lens[i] - 5;       // steps at positions 4 .. len - 2
+            }
+            ++refills;
+            continue;
+        }
+        if (active == 0) break;
+        if (wb_status st = replay_step(sl, p.S, s)) return done(st);
+        for (int64_t q = 0; q < p.S; ++q)
+            if (remaining[q] > 0) --remaining[q];
+    }
+    std::vector<int32_t> all((size_t)p.S);
+    for (int64_t q = 0; q < p.S; ++q) all[q] = (int32_t)q;
+    if (wb_status st = flush(all)) return done(st);
+    if (n_slots_out) *n_slots_out = (int32_t)p.S;
+    (void)refills;
+    done(WB_OK);
     return wb_sync_status(m, stream);
 }
 

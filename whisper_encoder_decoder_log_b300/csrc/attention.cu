@@ -104,7 +104,7 @@ attn_rows_kernel(const TQ* __restrict__ q, int64_t q_ld, int rows_per_chunk, int
     const int64_t row0 = chunk * rows_per_chunk + r_first;
     if (row0 >= n_rows_total) return;
     if (kv.pos_dev) {
-        q_pos0 = *kv.pos_dev;
+        q_pos0 = kv.pos_dev[chunk * kv.pos_stride];
         if (kv.active_len && kv.active_len[chunk] <= q_pos0 + 1) return;   // finished chunk
     }
 
@@ -304,7 +304,7 @@ self_attn_step_kernel(const float* __restrict__ qkv, int64_t q_ld, int heads, KV
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t chunk = blockIdx.x;
     const int h = blockIdx.y * kStepHeads + warp;
-    const int pos = kv.pos_dev ? *kv.pos_dev : q_pos_host;
+    const int pos = kv.pos_dev ? kv.pos_dev[chunk * kv.pos_stride] : q_pos_host;
     if (kv.active_len && kv.active_len[chunk] <= pos + 1) return;   // finished chunk (uniform per CTA)
     const int64_t kc = CROSS ? chunk / kv.beam_div : chunk;         // whose cross K/V / scales
     const int L = CROSS ? kCtx : kv.chunk_len[chunk];

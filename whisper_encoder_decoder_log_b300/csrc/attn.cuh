@@ -40,6 +40,8 @@ struct KVView {
     // row whose hypothesis wrote it).
     int beam_div = 1;
     const int32_t* hist = nullptr;
+    // with pos_dev: row c's position is pos_dev[c * pos_stride] (0: one for all)
+    int pos_stride = 0;
 };
 
 // Encoder self-attention, bf16, on tcgen05 (TMEM accumulators, TMA-fed tiles):

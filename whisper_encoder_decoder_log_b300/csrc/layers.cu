@@ -185,14 +185,14 @@ layernorm_kernel(const float* __restrict__ x, int64_t ld_x, int64_t rows, int d,
 template <typename TW>
 __global__ void embed_kernel(const int32_t* __restrict__ tokens, int64_t rows, int P, int p0, int d,
                              const TW* __restrict__ E, const TW* __restrict__ Pos, int vocab,
-                             float* __restrict__ x, unsigned* err, const int* __restrict__ pos_dev,
+                             float* __restrict__ x, unsigned* err, const int* __restrict__ pos_dev, int pos_stride,
                              const int32_t* __restrict__ len) {
     griddep_wait();
     griddep_launch();
     const int64_t r = blockIdx.x;
     if (r >= rows) return;
     const int64_t c = r / P;
-    const int pos = (pos_dev ? *pos_dev : p0) + (int)(r % P);
+    const int pos = (pos_dev ? pos_dev[c * pos_stride] : p0) + (int)(r % P);
     if (pos >= kMaxPos || (len && pos >= len[c])) {   // a finished chunk's row: nothing to embed
         for (int i = threadIdx.x; i < d; i += blockDim.x) x[r * d + i] = 0.f;
         return;
@@ -390,7 +390,7 @@ __global__ void fill_kernel(float* __restrict__ x, int64_t n, float v) {
 // r (one row per chunk); the token goes to column pos+1 when pos+1 < len[c].
 __global__ void __launch_bounds__(256)
 argmax_kernel(const float* __restrict__ logits, int64_t ld, int64_t rows, int V, int32_t* __restrict__ tokens,
-              const int32_t* __restrict__ len, const int* __restrict__ pos_dev, int pos_host) {
+              const int32_t* __restrict__ len, const int* __restrict__ pos_dev, int pos_host, int pos_stride) {
     griddep_wait();
     griddep_launch();
     const int64_t r = blockIdx.x;
@@ -416,7 +416,7 @@ argmax_kernel(const float* __restrict__ logits, int64_t ld, int64_t rows, int V,
         __syncthreads();
     }
     if (threadIdx.x == 0) {
-        const int pos = pos_dev ? *pos_dev : pos_host;
+        const int pos = pos_dev ? pos_dev[r * pos_stride] : pos_host;
         if (pos + 1 < len[r] && pos + 1 < kMaxPos) tokens[r * kMaxPos + pos + 1] = si[0] == 0x7FFFFFFF ? 0 : si[0];
     }
 }
@@ -572,6 +572,65 @@ __global__ void beam_init_kernel(int32_t* __restrict__ hist, float* __restrict__
     if (threadIdx.x == 0) scores[r] = (r % K == 0) ? 0.f : -INFINITY;
 }
 
+// ------------------------------------------------------------------ continuous batching
+// The cross K/V of n new chunks, computed into a staging decoder ([layer][R]
+// blocks of blk16 16-byte words), copied into the blocks of their slots
+// ([layer][S] blocks).  grid (x, n, layers).
+__global__ void slot_cross_copy_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst,
+                                       const int32_t* __restrict__ slot_of, int64_t R, int64_t S, int64_t blk16) {
+    griddep_wait();
+    griddep_launch();
+    const int64_t i = blockIdx.y, l = blockIdx.z;
+    const uint4* a = src + (l * R + i) * blk16;
+    uint4* b = dst + (l * S + slot_of[i]) * blk16;
+    for (int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; k < blk16; k += (int64_t)gridDim.x * blockDim.x)
+        b[k] = a[k];
+}
+
+// The rest of a new chunk's decode state into its slot (one CTA per chunk):
+// the first P rows of every (layer, K|V, head) cache block (E4M3, blocks of
+// lay x 64 bytes in both decoders), the per-layer cache scales ([layer][rows]),
+// the token row up to position P (the prefix and the first generated token),
+// the slot's position (P) and decode length.
+__global__ void slot_state_kernel(const uint8_t* __restrict__ st_cache, uint8_t* __restrict__ sl_cache,
+                                  const float* __restrict__ st_ks, const float* __restrict__ st_vs,
+                                  float* __restrict__ sl_ks, float* __restrict__ sl_vs,
+                                  const int32_t* __restrict__ st_tok, int32_t* __restrict__ sl_tok,
+                                  int* __restrict__ pos, int32_t* __restrict__ len, const int32_t* __restrict__ slot_of,
+                                  const int32_t* __restrict__ new_len, int R, int S, int layers, int heads, int lay,
+                                  int P) {
+    griddep_wait();
+    griddep_launch();
+    const int i = blockIdx.x, sl = slot_of[i];
+    const int64_t per_row = (int64_t)layers * 2 * heads * lay * 64;
+    const uint8_t* a = st_cache + (int64_t)i * per_row;
+    uint8_t* b = sl_cache + (int64_t)sl * per_row;
+    const int nblk = layers * 2 * heads, w16 = P * 4;      // 16-byte words per block prefix
+    for (int k = threadIdx.x; k < nblk * w16; k += blockDim.x) {
+        const int64_t blk = k / w16, w = k % w16;
+        reinterpret_cast<uint4*>(b + blk * lay * 64)[w] = reinterpret_cast<const uint4*>(a + blk * lay * 64)[w];
+    }
+    for (int l = threadIdx.x; l < layers; l += blockDim.x) {
+        sl_ks[(int64_t)l * S + sl] = st_ks[(int64_t)l * R + i];
+        sl_vs[(int64_t)l * S + sl] = st_vs[(int64_t)l * R + i];
+    }
+    for (int q = threadIdx.x; q <= P; q += blockDim.x) sl_tok[(int64_t)sl * kMaxPos + q] = st_tok[(int64_t)i * kMaxPos + q];
+    if (threadIdx.x == 0) {
+        pos[sl] = P;
+        len[sl] = new_len[i];
+    }
+}
+
+// Finished chunks: out[chunk][0 .. len) = slot token row (one CTA per pair).
+__global__ void slot_out_kernel(const int32_t* __restrict__ sl_tok, const int32_t* __restrict__ slot, const int32_t* __restrict__ chunk,
+                                const int32_t* __restrict__ n_len, int32_t* __restrict__ out) {
+    griddep_wait();
+    griddep_launch();
+    const int i = blockIdx.x;
+    for (int q = threadIdx.x; q < n_len[i]; q += blockDim.x)
+        out[(int64_t)chunk[i] * kMaxPos + q] = sl_tok[(int64_t)slot[i] * kMaxPos + q];
+}
+
 // conv weight [O][C][3] -> GEMM operand [O][3][C] (k index = j * C + c).
 // With dup, every tap j is stored twice ([o][j][hi | lo][c], k index
 // (2 j + half) C + c): the weights of a stem GEMM whose input rows carry each
@@ -600,10 +659,11 @@ __global__ void gather_rows_kernel(const float* __restrict__ x, int64_t rows, in
     for (int i = threadIdx.x; i < d; i += blockDim.x) out[r * d + i] = x[(r * stride_rows + first) * d + i];
 }
 
-__global__ void set_pos_kernel(int* pos, int value, int add) {
+__global__ void set_pos_kernel(int* pos, int value, int add, int n) {
     griddep_wait();
     griddep_launch();
-    if (threadIdx.x == 0) *pos = add ? *pos + value : value;
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x)
+        pos[i] = add ? pos[i] + value : value;
 }
 
 // GELU after a linear GEMM: fp32 [rows, N] -> bf16 pair [rows, 2N] (hi | lo)
@@ -783,15 +843,15 @@ wb_status cross_kv_quant(const void* tmp, int64_t gB, int64_t B, int64_t g0, int
 
 wb_status embed(const int32_t* tokens, int64_t rows, int P, int p0, int d, const void* E, const void* Pos,
                 bool bf16, int vocab, float* x, unsigned* err, cudaStream_t s, const int* pos_dev,
-                const int32_t* len) {
+                const int32_t* len, int pos_stride) {
     if (rows <= 0) return WB_OK;
     if (bf16)
         WB_CUDA(launch_k(embed_kernel<__nv_bfloat16>, dim3((unsigned)rows), dim3(256), 0, s, tokens, rows, P, p0, d,
             reinterpret_cast<const __nv_bfloat16*>(E), reinterpret_cast<const __nv_bfloat16*>(Pos), vocab, x, err,
-            pos_dev, len));
+            pos_dev, pos_stride, len));
     else
         WB_CUDA(launch_k(embed_kernel<float>, dim3((unsigned)rows), dim3(256), 0, s, tokens, rows, P, p0, d, reinterpret_cast<const float*>(E),
-                                                           reinterpret_cast<const float*>(Pos), vocab, x, err, pos_dev, len));
+                                                           reinterpret_cast<const float*>(Pos), vocab, x, err, pos_dev, pos_stride, len));
     WB_CUDA(cudaGetLastError());
     return WB_OK;
 }
@@ -853,8 +913,9 @@ wb_status gelu_post(float* x, int64_t rows, int N, void* out_bf16x2, cudaStream_
     return WB_OK;
 }
 
-wb_status set_pos(int* pos_dev, int value, bool add, cudaStream_t s) {
-    WB_CUDA(launch_k(set_pos_kernel, dim3(1), dim3(32), 0, s, pos_dev, value, add ? 1 : 0));
+wb_status set_pos(int* pos_dev, int value, bool add, cudaStream_t s, int n) {
+    WB_CUDA(launch_k(set_pos_kernel, dim3((unsigned)std::max(1, std::min((n + 255) / 256, 148))), dim3(256), 0, s,
+                     pos_dev, value, add ? 1 : 0, n));
     WB_CUDA(cudaGetLastError());
     return WB_OK;
 }
@@ -867,9 +928,9 @@ wb_status fill(float* x, int64_t n, float v, cudaStream_t s) {
 }
 
 wb_status argmax_tokens(const float* logits, int64_t ld, int64_t rows, int V, int32_t* tokens, const int32_t* len,
-                        const int* pos_dev, int pos_host, cudaStream_t s) {
+                        const int* pos_dev, int pos_host, cudaStream_t s, int pos_stride) {
     if (rows <= 0) return WB_OK;
-    WB_CUDA(launch_k(argmax_kernel, dim3((unsigned)rows), dim3(256), 0, s, logits, ld, rows, V, tokens, len, pos_dev, pos_host));
+    WB_CUDA(launch_k(argmax_kernel, dim3((unsigned)rows), dim3(256), 0, s, logits, ld, rows, V, tokens, len, pos_dev, pos_host, pos_stride));
     WB_CUDA(cudaGetLastError());
     return WB_OK;
 }
@@ -897,6 +958,36 @@ wb_status beam_best(const float* scores, const int32_t* tokens, int64_t n_chunks
 wb_status beam_init(int32_t* hist, float* scores, int64_t rows, int K, cudaStream_t s) {
     if (rows <= 0) return WB_OK;
     WB_CUDA(launch_k(beam_init_kernel, dim3((unsigned)rows), dim3(128), 0, s, hist, scores, rows, K));
+    WB_CUDA(cudaGetLastError());
+    return WB_OK;
+}
+
+wb_status slot_cross_copy(const void* src, void* dst, const int32_t* slot_of, int n, int64_t R, int64_t S, int layers,
+                          int64_t blk_bytes, cudaStream_t s) {
+    if (n <= 0 || layers <= 0) return WB_OK;
+    if (blk_bytes % 16) return fail(WB_ERR_ALIGN, "slot cross copy: blocks of whole 16-byte words");
+    const int64_t blk16 = blk_bytes / 16;
+    const unsigned gx = (unsigned)std::max<int64_t>(1, std::min<int64_t>(64, (blk16 + 1023) / 1024));
+    WB_CUDA(launch_k(slot_cross_copy_kernel, dim3(gx, (unsigned)n, (unsigned)layers), dim3(256), 0, s,
+                     reinterpret_cast<const uint4*>(src), reinterpret_cast<uint4*>(dst), slot_of, R, S, blk16));
+    WB_CUDA(cudaGetLastError());
+    return WB_OK;
+}
+
+wb_status slot_state(const uint8_t* st_cache, uint8_t* sl_cache, const float* st_ks, const float* st_vs, float* sl_ks,
+                     float* sl_vs, const int32_t* st_tok, int32_t* sl_tok, int* pos, int32_t* len, const int32_t* slot_of,
+                     const int32_t* new_len, int n, int R, int S, int layers, int heads, int lay, int P, cudaStream_t s) {
+    if (n <= 0) return WB_OK;
+    WB_CUDA(launch_k(slot_state_kernel, dim3((unsigned)n), dim3(256), 0, s, st_cache, sl_cache, st_ks, st_vs, sl_ks,
+                     sl_vs, st_tok, sl_tok, pos, len, slot_of, new_len, R, S, layers, heads, lay, P));
+    WB_CUDA(cudaGetLastError());
+    return WB_OK;
+}
+
+wb_status slot_out(const int32_t* sl_tok, const int32_t* slot, const int32_t* chunk, const int32_t* n_len, int n,
+                   int32_t* out, cudaStream_t s) {
+    if (n <= 0) return WB_OK;
+    WB_CUDA(launch_k(slot_out_kernel, dim3((unsigned)n), dim3(128), 0, s, sl_tok, slot, chunk, n_len, out));
     WB_CUDA(cudaGetLastError());
     return WB_OK;
 }

@@ -36,18 +36,19 @@ wb_status quant_groups(const float* x, int64_t rows, int64_t K, int64_t group_ro
                        uint8_t* q, float* row_scale, cudaStream_t s);
 // scale[g] = amax / 448 (1 when 0) in place over an array that holds amax bits.
 wb_status scales_from_amax(float* amax_then_scale, int64_t n, cudaStream_t s);
-// Positions come from *pos_dev when it is non-null (graph replay), else p0.
+// Positions come from pos_dev[c * pos_stride] when pos_dev is non-null (graph
+// replay; pos_stride 0: one position for all, 1: one per chunk), else p0.
 wb_status embed(const int32_t* tokens, int64_t rows, int P, int p0, int d, const void* E, const void* Pos, bool bf16,
                 int vocab, float* x, unsigned* err, cudaStream_t s, const int* pos_dev = nullptr,
-                const int32_t* len = nullptr);
+                const int32_t* len = nullptr, int pos_stride = 0);
 wb_status kv_scales(const float* qkv, int64_t n_chunks, int P, int d, float* k_scale, float* v_scale, cudaStream_t s);
 wb_status kv_append(const float* qkv, int64_t n_chunks, int P, int p0, int d, int H, int layer, bool fp8, void* cache,
                     const int64_t* off, const int32_t* len, const float* k_scale, const float* v_scale, unsigned* err,
                     cudaStream_t s, const int* pos_dev = nullptr);
 // x = GELU(x) in place, or GELU(x) as a bf16 (hi | lo) pair into out_bf16x2 [rows, 2N].
 wb_status gelu_post(float* x, int64_t rows, int N, void* out_bf16x2, cudaStream_t s);
-// *pos_dev = value, or += value when add.
-wb_status set_pos(int* pos_dev, int value, bool add, cudaStream_t s);
+// pos_dev[0 .. n) = value, or += value when add.
+wb_status set_pos(int* pos_dev, int value, bool add, cudaStream_t s, int n = 1);
 // E4M3 codes of an fp32 matrix with one scale amax / 448 per row.
 wb_status quant_rows_f32(const float* x, int64_t rows, int K, uint8_t* q, float* row_scale, cudaStream_t s);
 wb_status quant_tensor(const void* x, bool bf16, int64_t n, uint8_t* q, float* scale, unsigned* scratch_bits,
@@ -70,8 +71,20 @@ wb_status beam_select(const float* logits, int64_t ld, int64_t n_chunks, int K, 
 wb_status beam_best(const float* scores, const int32_t* tokens, int64_t n_chunks, int K, const int32_t* len,
                     int32_t* out, float* score_out, cudaStream_t s);
 wb_status beam_init(int32_t* hist, float* scores, int64_t rows, int K, cudaStream_t s);
+// Continuous batching: move the decode state of n chunks prepared in a
+// staging decoder of R rows into their slots of an S-row decoder (cross K/V
+// blocks of blk_bytes per layer and chunk; the first P cache rows of each
+// (layer, K|V, head) block of lay rows, cache scales, token rows, position P,
+// decode length), and copy finished slots' token rows to the output.
+wb_status slot_cross_copy(const void* src, void* dst, const int32_t* slot_of, int n, int64_t R, int64_t S, int layers,
+                          int64_t blk_bytes, cudaStream_t s);
+wb_status slot_state(const uint8_t* st_cache, uint8_t* sl_cache, const float* st_ks, const float* st_vs, float* sl_ks,
+                     float* sl_vs, const int32_t* st_tok, int32_t* sl_tok, int* pos, int32_t* len, const int32_t* slot_of,
+                     const int32_t* new_len, int n, int R, int S, int layers, int heads, int lay, int P, cudaStream_t s);
+wb_status slot_out(const int32_t* sl_tok, const int32_t* slot, const int32_t* chunk, const int32_t* n_len, int n,
+                   int32_t* out, cudaStream_t s);
 wb_status argmax_tokens(const float* logits, int64_t ld, int64_t rows, int V, int32_t* tokens, const int32_t* len,
-                        const int* pos_dev, int pos_host, cudaStream_t s);
+                        const int* pos_dev, int pos_host, cudaStream_t s, int pos_stride = 0);
 // conv weight [O][C][3] -> [O][3][C]; dup: [O][3][2][C] (each tap twice, for
 // stem inputs that carry a bf16 pair per value)
 wb_status conv_reorder(const void* w, int O, int C, bool bf16, void* out, cudaStream_t s, bool dup = false);
