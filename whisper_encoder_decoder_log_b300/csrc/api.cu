@@ -657,12 +657,13 @@ wb_status decoder_layers(wb_decoder* dec, int64_t n_chunks, int rows_per_chunk, 
         if (wb_status st = ln_then_linear(m, dec->h, R, nm("dec.", l, "ln3."), f8 ? LN_E4M3 : ln_act, dec->a,
                                           f8 ? d : lda, dec->a_scale, L1, e1, s))
             return st;
-        if (few)
-            if (wb_status st = gelu_post(f32buf, R, F, f8 ? nullptr : dec->f2, s)) return st;
+        // few rows, E4M3: GELU goes into the FC2 input quantiser
+        if (few && !f8)
+            if (wb_status st = gelu_post(f32buf, R, F, dec->f2, s)) return st;
         Lin L2;
         L2.rows = R; L2.w = m->W(nm("dec.", l, "fc2.w")); L2.N = d; L2.K = F;
         if (f8) {
-            if (wb_status st = quant_rows_f32(f32buf, R, F, dec->fq, dec->f_scale, s)) return st;
+            if (wb_status st = quant_rows_f32(f32buf, R, F, dec->fq, dec->f_scale, s, few)) return st;
             L2.a = dec->fq; L2.lda = F; L2.f8 = &m->dec_fc2[l]; L2.a_scale = dec->f_scale;
         } else {
             L2.a = fin; L2.lda = ldf; L2.split = sp;

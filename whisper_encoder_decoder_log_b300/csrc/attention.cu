@@ -247,13 +247,6 @@ attn_rows_kernel(const TQ* __restrict__ q, int64_t q_ld, int rows_per_chunk, int
 constexpr int kStepHeads = 4;
 constexpr int kStepDepth = 8;
 
-WB_DEV void cp_async16(void* smem, const void* gmem) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem)), "l"(gmem) : "memory");
-}
-WB_DEV void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-WB_DEV void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
-
 // dot(q[0..15], E4M3 codes w) and o += p * E4M3 codes v
 WB_DEV float dot16_e4m3(const float (&q)[16], const uint4& w) {
     const uint32_t u[4] = {w.x, w.y, w.z, w.w};

@@ -270,22 +270,28 @@ __device__ __forceinline__ void store_chunk(const GemmArgs& a, int64_t b, int64_
 // Swapped operands (small M): TMEM lane = output feature n, column = row m.
 // One call stores 32 rows m0 .. m0+31 of feature n; lanes of a warp hold
 // consecutive n, so every store instruction is coalesced.
+// Swapped form: lane = output feature n (cs, bias: its column scale and bias,
+// the bias only on the first K partition), the 32 values = rows m0..m0+31.
+// The rows' scales arrive as one coalesced load and are broadcast by
+// shuffles, so no store waits on a load.
 __device__ __forceinline__ void store_swap(const GemmArgs& a, int64_t n, int64_t m0, const uint32_t (&raw)[32],
-                                           int ks) {
+                                           float cs, float bias) {
     const GemmEpi& e = a.epi;
-    if (n >= a.N) return;
-    const float cs = e.col_scale ? e.col_scale[n] : 1.f;
-    const float bias = (e.bias && ks == 0) ? e.bias[n] : 0.f;
-    float* out = reinterpret_cast<float*>(e.out);
+    const int lane = threadIdx.x & 31;
+    const float rs_lane = (e.row_scale && m0 + lane < a.rows) ? e.row_scale[m0 + lane] : 1.f;
+    const int64_t left = a.rows - m0;
+    const int nrow = left < 32 ? (int)left : 32;
+    const bool nok = n < a.N;
+    const bool red = a.ksplit > 1 || e.out_type == OUT_F32_ACC;
+    float* dst = reinterpret_cast<float*>(e.out) + m0 * e.ldo + n;
 #pragma unroll
     for (int j = 0; j < 32; ++j) {
-        const int64_t m = m0 + j;
-        if (m >= a.rows) break;
-        const float rs = e.row_scale ? e.row_scale[m] : 1.f;
-        const float v = __uint_as_float(raw[j]) * rs * cs + bias;
-        float* dst = out + m * e.ldo + n;
-        if (a.ksplit > 1 || e.out_type == OUT_F32_ACC) atomicAdd(dst, v);   // result unused: a reduction
-        else *dst = v;
+        const float rs = __shfl_sync(0xffffffffu, rs_lane, j);
+        if (nok && j < nrow) {
+            const float v = __uint_as_float(raw[j]) * rs * cs + bias;
+            if (red) atomicAdd(dst + j * e.ldo, v);    // result unused: a reduction
+            else dst[j * e.ldo] = v;
+        }
     }
 }
 
@@ -588,12 +594,16 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant_
             const uint32_t taddr = tmem_base + ((uint32_t)(g * 32) << 16) + acc * BN;
             if (SWAP) {
                 const int64_t n = mt * kBM + g * 32 + lane;      // output feature of this lane
+                const bool nok = n < args.N;
+                const float cs = (args.epi.col_scale && nok) ? args.epi.col_scale[n] : 1.f;
+                const float bias = (args.epi.bias && nok && t % args.ksplit == 0) ? args.epi.bias[n] : 0.f;
 #pragma unroll 1
                 for (int c = half; c < BN / 32; c += 2) {
+                    if (nt * BN + c * 32 >= args.rows) break;    // no rows left in this tile (warp-uniform)
                     uint32_t raw[32];
                     tmem_ld32(taddr + c * 32, raw);
                     tmem_wait_ld();
-                    store_swap(args, n, nt * BN + c * 32, raw, (int)(t % args.ksplit));
+                    store_swap(args, n, nt * BN + c * 32, raw, cs, bias);
                 }
                 tc_fence_before();
                 mbar_arrive(&tempty_bar[acc]);

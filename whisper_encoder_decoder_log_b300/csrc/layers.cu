@@ -261,7 +261,9 @@ __global__ void kv_append_kernel(const float* __restrict__ qkv, int64_t n_chunks
     }
 }
 
-// Per-row E4M3 quantisation of an fp32 matrix.
+// Per-row E4M3 quantisation of an fp32 matrix; with GELU, of GELU(x) (the
+// value is recomputed in both passes instead of being stored).
+template <bool GELU>
 __global__ void quant_rows_f32_kernel(const float* __restrict__ x, int64_t rows, int K, uint8_t* __restrict__ q,
                                       float* __restrict__ row_scale) {
     griddep_wait();
@@ -271,15 +273,20 @@ __global__ void quant_rows_f32_kernel(const float* __restrict__ x, int64_t rows,
     if (r >= rows) return;
     const float* xr = x + r * K;
     float m = 0.f;
+    auto load = [&](int i) {
+        float4 a = *reinterpret_cast<const float4*>(xr + i);
+        if (GELU) { a.x = gelu_f(a.x); a.y = gelu_f(a.y); a.z = gelu_f(a.z); a.w = gelu_f(a.w); }
+        return a;
+    };
     for (int i = lane * 4; i < K; i += 128) {
-        const float4 a = *reinterpret_cast<const float4*>(xr + i);
+        const float4 a = load(i);
         m = fmaxf(m, fmaxf(fmaxf(fabsf(a.x), fabsf(a.y)), fmaxf(fabsf(a.z), fabsf(a.w))));
     }
     m = warp_max(m);
     const float sc = m > 0.f ? m / 448.0f : 1.0f;
     const float inv = 1.0f / sc;
     for (int i = lane * 4; i < K; i += 128) {
-        const float4 a = *reinterpret_cast<const float4*>(xr + i);
+        const float4 a = load(i);
         const uint32_t o = (uint32_t)f2e4m3x2(a.x * inv, a.y * inv) | ((uint32_t)f2e4m3x2(a.z * inv, a.w * inv) << 16);
         *reinterpret_cast<uint32_t*>(q + r * K + i) = o;
     }
@@ -874,10 +881,16 @@ wb_status kv_append(const float* qkv, int64_t n_chunks, int P, int p0, int d, in
     return WB_OK;
 }
 
-wb_status quant_rows_f32(const float* x, int64_t rows, int K, uint8_t* q, float* row_scale, cudaStream_t s) {
+wb_status quant_rows_f32(const float* x, int64_t rows, int K, uint8_t* q, float* row_scale, cudaStream_t s,
+                         bool gelu) {
     if (rows <= 0) return WB_OK;
     if (K % 128) return fail(WB_ERR_SHAPE, "row quantiser needs K % 128 == 0");
-    WB_CUDA(launch_k(quant_rows_f32_kernel, dim3((unsigned)((rows + 7) / 8)), dim3(256), 0, s, x, rows, K, q, row_scale));
+    if (gelu)
+        WB_CUDA(launch_k(quant_rows_f32_kernel<true>, dim3((unsigned)((rows + 7) / 8)), dim3(256), 0, s, x, rows, K, q,
+                         row_scale));
+    else
+        WB_CUDA(launch_k(quant_rows_f32_kernel<false>, dim3((unsigned)((rows + 7) / 8)), dim3(256), 0, s, x, rows, K,
+                         q, row_scale));
     WB_CUDA(cudaGetLastError());
     return WB_OK;
 }

@@ -50,7 +50,8 @@ wb_status gelu_post(float* x, int64_t rows, int N, void* out_bf16x2, cudaStream_
 // pos_dev[0 .. n) = value, or += value when add.
 wb_status set_pos(int* pos_dev, int value, bool add, cudaStream_t s, int n = 1);
 // E4M3 codes of an fp32 matrix with one scale amax / 448 per row.
-wb_status quant_rows_f32(const float* x, int64_t rows, int K, uint8_t* q, float* row_scale, cudaStream_t s);
+wb_status quant_rows_f32(const float* x, int64_t rows, int K, uint8_t* q, float* row_scale, cudaStream_t s,
+                         bool gelu = false);
 wb_status quant_tensor(const void* x, bool bf16, int64_t n, uint8_t* q, float* scale, unsigned* scratch_bits,
                        cudaStream_t s);
 wb_status dequant_tensor(const uint8_t* q, const float* scale, int64_t n, float* out, cudaStream_t s);

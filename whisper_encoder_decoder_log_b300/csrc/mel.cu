@@ -3,9 +3,12 @@
 // Spectrogram"; "Unlocking the power of OpenAI's Whisper", section 2).
 //
 // Work split.  A cluster of kCluster CTAs owns one 30 s chunk; CTA r computes
-// frames [375 r, 375 r + 375).  Frames are processed 32 at a time: the audio
-// segment they cover (5360 samples, reflect-padded at the chunk edges) is
-// staged in shared memory, two real frames are packed into one complex
+// frames [376 r, min(376 r + 376, 3000)) (a multiple of 4 frames, so rows of
+// its output tile start on 16-byte boundaries).  Frames are processed 32 at a
+// time: the audio segment they cover (5360 samples, reflect-padded at the
+// chunk edges) is staged in shared memory -- the next sub-block's segment is
+// copied asynchronously (cp.async) while the current one is transformed --
+// and two real frames are packed into one complex
 // 400-point FFT (z = x_a + i x_b), split as 400 = 16 x 25:
 //   stage 1: per (pair, n2) a 16-point DFT over n1 of z[25 n1 + n2], times
 //            the twiddle W400^(n2 k1);
@@ -14,10 +17,11 @@
 // then X_a, X_b are separated from Z[k] and Z[400-k], the power of bins 0..200
 // goes through the sparse mel filterbank (each bin feeds at most two
 // filters), and log10 is taken.  The unfloored value (l + 4) / 4 is written
-// to HBM right away and the CTA's maximum is kept; the cluster then reduces
-// the chunk maximum through distributed shared memory, and each CTA re-reads
-// its own freshly written tile (resident in L2) to apply the max - 8 floor,
-// writing back only the values that change.
+// to HBM right away, and the CTA keeps its maximum and each sub-block's
+// minimum; the cluster then reduces the chunk maximum through distributed
+// shared memory, and each CTA re-reads (from L2, 16 bytes at a time) only
+// the sub-blocks whose minimum lies below the max - 8 floor, writing back the
+// values that change.
 #include <cooperative_groups.h>
 
 #include <cmath>
@@ -34,7 +38,7 @@ namespace wb {
 namespace {
 
 constexpr int kCluster = 8;
-constexpr int kFramesPerCta = kFrames / kCluster;      // 375
+constexpr int kFramesPerCta = 376;                     // the last CTA of a chunk: 368
 constexpr int kSub = 32;                               // frames per sub-block
 constexpr int kPairs = kSub / 2;
 constexpr int kSeg = kSub * kHop + (kNFFT - kHop);     // 5360 samples
@@ -43,14 +47,22 @@ constexpr int kPStride = kBins;                        // odd stride: no bank co
 constexpr int kThreads = 256;
 constexpr int kMaxMels = 128;
 constexpr int kMaxFbNnz = 512;
+constexpr int kSubBlocks = (kFramesPerCta + kSub - 1) / kSub;   // 12
+
+// float -> unsigned key with the same order (for atomicMin on shared memory)
+__device__ __forceinline__ unsigned order_key(float f) {
+    const unsigned b = __float_as_uint(f);
+    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+__device__ __forceinline__ float key_value(unsigned k) {
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
 
 struct MelTables {
     float2 tw[kNFFT];          // W400^j = exp(-2 pi i j / 400)
     float2 tw1[16 * 25];       // stage-1 twiddles W400^(n2 k1) at [k1][n2]
     float win[kNFFT];          // periodic Hann
-    int kstart[kMaxMels];
-    int kcount[kMaxMels];
-    int woff[kMaxMels];
+    int4 meta[kMaxMels];       // filter m: first bin, bin count, weight offset
     float w[kMaxFbNnz];
 };
 
@@ -61,6 +73,7 @@ struct MelSmem {
     float p[kSub * kPStride];
     float red[kThreads / 32];
     float cmax;
+    unsigned smin[kSubBlocks];   // per sub-block minimum of log10(mel), order-preserving keys
 };
 
 __device__ __forceinline__ float2 cmul(float2 a, float2 b) {
@@ -118,18 +131,29 @@ mel_kernel(const float* __restrict__ audio, const MelTables* __restrict__ tables
     }
 
     const int fbeg = rank * kFramesPerCta;
+    const int fend = min(kFrames, fbeg + kFramesPerCta);
+    const int nsb = (fend - fbeg + kSub - 1) / kSub;
+    if (tid < kSubBlocks) S.smin[tid] = 0xFFFFFFFFu;
     float tmax = -1e30f;
 
-    for (int f0 = fbeg; f0 < fbeg + kFramesPerCta; f0 += kSub) {
-        const int nf = min(kSub, fbeg + kFramesPerCta - f0);
-        __syncthreads();   // previous sub-block fully consumed (and tables ready)
-        // ---- audio segment: padded index 160 f0 + i maps to sample 160 f0 + i - 200
-        const int q0 = kHop * f0 - kNFFT / 2;            // a multiple of 4 samples
-        if (q0 >= 0 && q0 + kSeg <= kChunkSamples) {      // interior: 16-byte loads, all in flight
-            const float4* src = reinterpret_cast<const float4*>(x + q0);
-            float4* dst = reinterpret_cast<float4*>(S.seg);
-            for (int i = tid; i < kSeg / 4; i += kThreads) dst[i] = __ldg(src + i);
-        } else {                                          // chunk edges: reflect
+    // audio segment of the sub-block at frame f0: padded index 160 f0 + i is
+    // sample 160 f0 + i - 200 (a multiple of 4 samples, so 16-byte aligned)
+    auto interior = [](int f0) {
+        const int q0 = kHop * f0 - kNFFT / 2;
+        return q0 >= 0 && q0 + kSeg <= kChunkSamples;
+    };
+    auto load_async = [&](int f0) {
+        const float* src = x + (kHop * f0 - kNFFT / 2);
+        for (int i = tid; i < kSeg / 4; i += kThreads) cp_async16(S.seg + 4 * i, src + 4 * i);
+        cp_async_commit();
+    };
+    if (interior(fbeg)) load_async(fbeg);
+
+    for (int sb = 0; sb < nsb; ++sb) {
+        const int f0 = fbeg + sb * kSub;
+        const int nf = min(kSub, fend - f0);
+        if (!interior(f0)) {   // chunk edges: reflect (the segment buffer is free here)
+            const int q0 = kHop * f0 - kNFFT / 2;
             for (int i = tid; i < kSeg; i += kThreads) {
                 int q = q0 + i;
                 if (q < 0) q = -q;
@@ -138,7 +162,8 @@ mel_kernel(const float* __restrict__ audio, const MelTables* __restrict__ tables
                 S.seg[i] = __ldg(x + q);
             }
         }
-        __syncthreads();
+        cp_async_wait<0>();
+        __syncthreads();   // segment (and, the first time, tables) ready; previous sub-block consumed
         // ---- stage 1: 16-point DFTs over n1, twiddle W400^(n2 k1)
         for (int it = tid; it < kPairs * 25; it += kThreads) {
             const int pr = it / 25, n2 = it % 25;
@@ -171,6 +196,8 @@ mel_kernel(const float* __restrict__ audio, const MelTables* __restrict__ tables
                 }
         }
         __syncthreads();
+        // the segment is consumed: the next sub-block's copy overlaps the rest
+        if (sb + 1 < nsb && interior(f0 + kSub)) load_async(f0 + kSub);
         // ---- stage 2: 25-point DFTs over n2 (5 x 5), in place
         for (int it = tid; it < kPairs * 16; it += kThreads) {
             const int pr = it / 16, k1 = it % 16;
@@ -208,17 +235,21 @@ mel_kernel(const float* __restrict__ audio, const MelTables* __restrict__ tables
         }
         __syncthreads();
         // ---- mel filterbank, log10, unfloored output
+        float smin = 1e30f;
         for (int it = tid; it < n_mels * kSub; it += kThreads) {
             const int m = it / kSub, f = it % kSub;
             if (f >= nf) continue;
             const float* pf = S.p + f * kPStride;
-            const int k0 = S.t.kstart[m], kc = S.t.kcount[m], wo = S.t.woff[m];
+            const int4 mt = S.t.meta[m];
             float e = 0.f;
-            for (int j = 0; j < kc; ++j) e = fmaf(S.t.w[wo + j], pf[k0 + j], e);
+            for (int j = 0; j < mt.y; ++j) e = fmaf(S.t.w[mt.z + j], pf[mt.x + j], e);
             const float ell = __log2f(fmaxf(e, 1e-10f)) * 0.30102999566398120f;
             tmax = fmaxf(tmax, ell);
+            smin = fminf(smin, ell);
             o[(int64_t)m * kFrames + f0 + f] = (ell + 4.0f) * 0.25f;
         }
+        smin = warp_min(smin);
+        if ((tid & 31) == 0) atomicMin(&S.smin[sb], order_key(smin));
     }
     // ---- chunk maximum across the cluster
     tmax = warp_max(tmax);
@@ -233,12 +264,25 @@ mel_kernel(const float* __restrict__ audio, const MelTables* __restrict__ tables
     float cm = -1e30f;
 #pragma unroll
     for (int r = 0; r < kCluster; ++r) cm = fmaxf(cm, *cluster.map_shared_rank(&S.cmax, r));
-    const float floor_v = (cm - 8.0f + 4.0f) * 0.25f;
-    for (int it = tid; it < n_mels * kFramesPerCta; it += kThreads) {
-        const int m = it / kFramesPerCta, f = it % kFramesPerCta;
-        float* p = o + (int64_t)m * kFrames + fbeg + f;
-        const float v = *p;
-        if (v < floor_v) *p = floor_v;
+    const float floor_log = cm - 8.0f;
+    const float floor_v = (floor_log + 4.0f) * 0.25f;
+    // ---- the floor, on the sub-blocks that hold a value below it; a value
+    // at or above floor_log maps to an output at or above floor_v, so the
+    // skipped sub-blocks are unchanged
+    for (int sb = 0; sb < nsb; ++sb) {
+        if (!(key_value(S.smin[sb]) < floor_log)) continue;
+        const int f0 = fbeg + sb * kSub;
+        const int q4 = min(kSub, fend - f0) / 4;       // 16-byte pieces per mel row
+        for (int it = tid; it < n_mels * q4; it += kThreads) {
+            const int m = it / q4, q = it % q4;
+            float4* p = reinterpret_cast<float4*>(o + (int64_t)m * kFrames + f0) + q;
+            float4 v = *p;
+            if (v.x < floor_v || v.y < floor_v || v.z < floor_v || v.w < floor_v) {
+                v.x = fmaxf(v.x, floor_v); v.y = fmaxf(v.y, floor_v);
+                v.z = fmaxf(v.z, floor_v); v.w = fmaxf(v.w, floor_v);
+                *p = v;
+            }
+        }
     }
     cluster.sync();   // no CTA leaves while another may still read its cmax
 }
@@ -282,9 +326,7 @@ bool build_tables(int n_mels, MelTables* t) {
             }
         }
         if (first < 0) first = last = 0;
-        t->kstart[m] = first;
-        t->kcount[m] = last - first + 1;
-        t->woff[m] = nnz;
+        t->meta[m] = make_int4(first, last - first + 1, nnz, 0);
         for (int k = first; k <= last; ++k) {
             const double f = 40.0 * k;
             const double wv = std::fmax(0.0, std::fmin((f - lo) / (c - lo), (hi - f) / (hi - c))) *
