@@ -60,6 +60,7 @@ struct GemmArgs {
     int kblocks;            // k-blocks of the longest split
     int kb_all;             // k-blocks of the whole K
     int ksplit;             // K partitions; > 1 adds partial tiles atomically
+    int stream_k;           // the CTAs split the flattened (tile, k-block) sequence evenly (swapped form)
     int stages;             // smem ring depth (<= the compile-time maximum)
     int w_const;            // the weight operand is constant: load it before the grid dependency wait
     int b_kwrap;
@@ -272,17 +273,15 @@ __device__ __forceinline__ void store_chunk(const GemmArgs& a, int64_t b, int64_
 // consecutive n, so every store instruction is coalesced.
 // Swapped form: lane = output feature n (cs, bias: its column scale and bias,
 // the bias only on the first K partition), the 32 values = rows m0..m0+31.
-// The rows' scales arrive as one coalesced load and are broadcast by
-// shuffles, so no store waits on a load.
+// rs_lane is row m0 + lane's scale, loaded before the accumulator was ready
+// and broadcast by shuffles, so no store waits on a load.
 __device__ __forceinline__ void store_swap(const GemmArgs& a, int64_t n, int64_t m0, const uint32_t (&raw)[32],
-                                           float cs, float bias) {
+                                           float cs, float bias, float rs_lane) {
     const GemmEpi& e = a.epi;
-    const int lane = threadIdx.x & 31;
-    const float rs_lane = (e.row_scale && m0 + lane < a.rows) ? e.row_scale[m0 + lane] : 1.f;
     const int64_t left = a.rows - m0;
     const int nrow = left < 32 ? (int)left : 32;
     const bool nok = n < a.N;
-    const bool red = a.ksplit > 1 || e.out_type == OUT_F32_ACC;
+    const bool red = a.ksplit > 1 || a.stream_k || e.out_type == OUT_F32_ACC;
     float* dst = reinterpret_cast<float*>(e.out) + m0 * e.ldo + n;
 #pragma unroll
     for (int j = 0; j < 32; ++j) {
@@ -301,6 +300,49 @@ __device__ __forceinline__ void split_range(const GemmArgs& a, int64_t t, int& k
     const int ks = (int)(t % a.ksplit);
     kb0 = (int)((int64_t)ks * a.kb_all / a.ksplit);
     kb1 = (int)((int64_t)(ks + 1) * a.kb_all / a.ksplit);
+}
+
+// One CTA's work: with stream_k, the k-blocks [c T / G, (c + 1) T / G) of
+// the flattened sequence of T = tiles x kb_all (tile-major) k-blocks, cut
+// into one segment per tile it touches (every segment's partial sum is added
+// atomically; the segment that holds k-block 0 adds the bias); otherwise
+// tiles c, c + G, c + 2 G, ... with their K partitions (split_range).
+struct WorkIter {
+    int64_t cur, end, step;
+};
+__device__ __forceinline__ WorkIter work_begin(const GemmArgs& a, int64_t c, int64_t g) {
+    WorkIter w;
+    if (a.stream_k) {
+        const int64_t T = a.tiles * (int64_t)a.kb_all;
+        w.cur = c * T / g;
+        w.end = (c + 1) * T / g;
+        w.step = 0;
+    } else {
+        w.cur = c;
+        w.end = a.tiles;
+        w.step = g;
+    }
+    return w;
+}
+// Next work item: tile (mt, nt), k-blocks [kb0, kb1); first: kb0 is the
+// tile's first k-block (the bias goes with it).
+__device__ __forceinline__ bool work_next(const GemmArgs& a, WorkIter& w, int64_t& mt, int64_t& nt, int& kb0,
+                                          int& kb1) {
+    if (w.cur >= w.end) return false;
+    if (a.stream_k) {
+        const int64_t u = w.cur / a.kb_all;
+        kb0 = (int)(w.cur - u * a.kb_all);
+        const int64_t left = w.end - w.cur;
+        kb1 = (int)min((int64_t)a.kb_all, (int64_t)kb0 + left);
+        mt = u / a.nt_total;
+        nt = u - mt * a.nt_total;
+        w.cur += kb1 - kb0;
+    } else {
+        tile_coords(a, w.cur, mt, nt);
+        split_range(a, w.cur, kb0, kb1);
+        w.cur += w.step;
+    }
+    return true;
 }
 
 // Fold the per-thread maxima of one warp's 32 consecutive rows into the
@@ -362,8 +404,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant_
     const int lane = threadIdx.x & 31;
     const int rank = PAIR ? (int)cluster_ctarank() : 0;
     const bool leader = rank == 0;
-    const int64_t t_first = PAIR ? blockIdx.x / 2 : blockIdx.x;      // first tile (256-row tile when PAIR)
-    const int64_t t_step = PAIR ? gridDim.x / 2 : gridDim.x;
+    const int64_t cta_id = PAIR ? blockIdx.x / 2 : blockIdx.x;      // CTA (pair) index: 256-row tiles when PAIR
+    const int64_t n_ctas = PAIR ? gridDim.x / 2 : gridDim.x;
     // M tile (128 rows) of this CTA within tile index mt
     auto my_mt = [&](int64_t mt) { return PAIR ? 2 * mt + rank : mt; };
     // try_wait at cluster scope where the peer (or its tensor core) arrives
@@ -430,11 +472,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant_
             // overlaps the previous kernel's tail (programmatic launch).
             int pre = 0;
             if (args.w_const) {
-                for (int64_t t = t_first; t < args.tiles && pre < STAGES; t += t_step) {
-                    int64_t mt, nt;
-                    tile_coords(args, t, mt, nt);
-                    int kb0, kb1;
-                    split_range(args, t, kb0, kb1);
+                WorkIter wi = work_begin(args, cta_id, n_ctas);
+                int64_t mt, nt;
+                int kb0, kb1;
+                while (pre < STAGES && work_next(args, wi, mt, nt, kb0, kb1)) {
                     for (int kb = kb0; kb < kb1 && pre < STAGES; ++kb, ++pre) {
                         arm(pre);
                         load_w(pre, mt, (int)(nt * BN), kb * (FP8 ? 128 : 64));
@@ -448,14 +489,13 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant_
             uint32_t issued = 0, last_parity = 0;      // bit s: stage s was loaded / its last phase
             bool ok = true;
             int it = 0;
-            for (int64_t t = t_first; t < args.tiles && ok; t += t_step) {
-                int64_t mt, nt;
-                tile_coords(args, t, mt, nt);
+            WorkIter wi = work_begin(args, cta_id, n_ctas);
+            int64_t mt, nt;
+            int kb0, kb1;
+            while (ok && work_next(args, wi, mt, nt, kb0, kb1)) {
                 const int b = PAIR ? 0 : (int)(mt / args.mt_per_batch);
                 const int r0 = PAIR ? (int)(my_mt(mt) * kBM) : (int)((mt % args.mt_per_batch) * kBM);
                 const int n0 = (int)(nt * BN);
-                int kb0, kb1;
-                split_range(args, t, kb0, kb1);
                 for (int kb = kb0; kb < kb1; ++kb, ++it) {
                     const int kx = kb * (FP8 ? 128 : 64);
                     if (it >= pre) {
@@ -508,7 +548,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant_
                     if (mbar_try_wait(stall_bar, 0)) { got = true; break; }
                 if (!got) { wb_set_error(err, WB_DEVERR_TIMEOUT_MMA); *abort_flag = 1; ok = false; }
             }
-            for (int64_t t = t_first; t < args.tiles && ok; t += t_step, ++local) {
+            WorkIter wi = work_begin(args, cta_id, n_ctas);
+            int64_t mt_w, nt_w;
+            int kb0, kb1;
+            for (; ok && work_next(args, wi, mt_w, nt_w, kb0, kb1); ++local) {
                 const int acc = local & 1;
                 const uint32_t aphase = (local >> 1) & 1;
                 bool got = false;
@@ -519,8 +562,6 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant_
                 if (!got) { wb_set_error(err, WB_DEVERR_TIMEOUT_MMA); *abort_flag = 1; break; }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * BN;
-                int kb0, kb1;
-                split_range(args, t, kb0, kb1);
                 for (int kb = 0; kb < kb1 - kb0; ++kb) {
                     got = false;
                     for (WaitClock clk; !clk.expired();) {
@@ -575,9 +616,28 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant_
         const int half = (warp - 2) >> 2;
         const uint32_t tempty_leader = PAIR ? mapa_shared(tempty_bar, 0) : 0u;
         int local = 0;
-        for (int64_t t = t_first; t < args.tiles; t += t_step, ++local) {
+        WorkIter wi = work_begin(args, cta_id, n_ctas);
+        int64_t mt, nt;
+        int kb0, kb1;
+        for (; work_next(args, wi, mt, nt, kb0, kb1); ++local) {
             const int acc = local & 1;
             const uint32_t aphase = (local >> 1) & 1;
+            const int ks = kb0 == 0 ? 0 : 1;     // 0: the tile's first K part (bias, plain stores)
+            // swapped form: this lane's column scale and bias and its rows'
+            // scales (chunks c = half, half + 2, ...) go out before the wait
+            constexpr int kSwapChunks = (BN / 32 + 1) / 2;
+            float sw_cs = 1.f, sw_bias = 0.f, sw_rs[kSwapChunks];
+            if (SWAP) {
+                const int64_t n = mt * kBM + g * 32 + lane;
+                const bool nok = n < args.N;
+                if (args.epi.col_scale && nok) sw_cs = args.epi.col_scale[n];
+                if (args.epi.bias && nok && ks == 0) sw_bias = args.epi.bias[n];
+#pragma unroll
+                for (int i = 0; i < kSwapChunks; ++i) {
+                    const int64_t m = nt * BN + (half + 2 * i) * 32 + lane;
+                    sw_rs[i] = (args.epi.row_scale && m < args.rows) ? args.epi.row_scale[m] : 1.f;
+                }
+            }
             bool got = false;
             for (WaitClock clk; !clk.expired();) {
                 if (try_wait(&tfull_bar[acc], aphase)) { got = true; break; }
@@ -585,8 +645,6 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant_
             }
             if (!got) { wb_set_error(err, WB_DEVERR_TIMEOUT_EPI); *abort_flag = 1; break; }
             tc_fence_after();
-            int64_t mt, nt;
-            tile_coords(args, t, mt, nt);
             if (PAIR) mt = my_mt(mt);     // one batch: M tile index = row tile
             const int64_t b = PAIR ? 0 : mt / args.mt_per_batch;
             const int64_t r = (PAIR ? mt : mt % args.mt_per_batch) * kBM + g * 32 + lane;
@@ -594,16 +652,14 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant_
             const uint32_t taddr = tmem_base + ((uint32_t)(g * 32) << 16) + acc * BN;
             if (SWAP) {
                 const int64_t n = mt * kBM + g * 32 + lane;      // output feature of this lane
-                const bool nok = n < args.N;
-                const float cs = (args.epi.col_scale && nok) ? args.epi.col_scale[n] : 1.f;
-                const float bias = (args.epi.bias && nok && t % args.ksplit == 0) ? args.epi.bias[n] : 0.f;
-#pragma unroll 1
-                for (int c = half; c < BN / 32; c += 2) {
-                    if (nt * BN + c * 32 >= args.rows) break;    // no rows left in this tile (warp-uniform)
+#pragma unroll
+                for (int i = 0; i < kSwapChunks; ++i) {
+                    const int c = half + 2 * i;
+                    if (c >= BN / 32 || nt * BN + c * 32 >= args.rows) break;   // warp-uniform
                     uint32_t raw[32];
                     tmem_ld32(taddr + c * 32, raw);
                     tmem_wait_ld();
-                    store_swap(args, n, nt * BN + c * 32, raw, cs, bias);
+                    store_swap(args, n, nt * BN + c * 32, raw, sw_cs, sw_bias, sw_rs[i]);
                 }
                 tc_fence_before();
                 mbar_arrive(&tempty_bar[acc]);
@@ -655,14 +711,14 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant_
                     continue;
                 }
                 if (!staged) {
-                    if (row_ok && n0 < args.N) store_chunk(args, b, r, n0, v, (int)(t % args.ksplit));
+                    if (row_ok && n0 < args.N) store_chunk(args, b, r, n0, v, ks);
                     continue;
                 }
                 // fp32 output: transform in the thread's row, then transpose the
                 // 32 x 32 block through shared memory (16-byte chunks XOR-swizzled
                 // by row) and write one 128-byte row segment per instruction
                 if (row_ok && n0 < args.N) {
-                    transform_f32(args, b, r, n0, v, (int)(t % args.ksplit));
+                    transform_f32(args, b, r, n0, v, ks);
                     if (e.amax) {
 #pragma unroll
                         for (int j = 0; j < 32; ++j)
@@ -774,15 +830,16 @@ wb_status launch_tc(const GemmPlan& p, GemmArgs a, unsigned* err, cudaStream_t s
     }
     // A CTA that sees few k-blocks needs a shallow ring; the smaller footprint
     // lets several CTAs share an SM (bounded by shared memory and TMEM).
-    const int64_t kb_per_cta = (int64_t)a.kblocks * ((a.tiles + num_sms() - 1) / num_sms());
+    const int64_t kb_per_cta = a.stream_k ? (a.tiles * a.kb_all + num_sms() - 1) / num_sms()
+                                          : (int64_t)a.kblocks * ((a.tiles + num_sms() - 1) / num_sms());
     a.stages = (int)std::max<int64_t>(2, std::min<int64_t>(C::STAGES, kb_per_cta));
     const int smem = a.stages * C::STAGE_BYTES + kEpiStageBytes + 1024 + 256;
     int occ = 1;
     WB_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, gemm_tc_kernel<BN, FP8, SWAP>, kGemmThreads, smem));
     const int per_sm = std::max(1, std::min({occ, 512 / C::TMEM_COLS, 4}));
-    int grid = num_sms() * per_sm;
+    int grid = a.stream_k ? num_sms() : num_sms() * per_sm;
     if (max_ctas > 0) grid = std::min(grid, max_ctas);
-    grid = (int)std::min<int64_t>(grid, a.tiles);
+    grid = (int)std::min<int64_t>(grid, a.stream_k ? a.tiles * a.kb_all : a.tiles);
     if (grid <= 0) return WB_OK;
     WB_CUDA(launch_k(gemm_tc_kernel<BN, FP8, SWAP>, dim3(grid), dim3(kGemmThreads), smem, s, p.tma_a, p.tma_b, a, err));
     WB_CUDA(cudaGetLastError());
@@ -942,6 +999,11 @@ wb_status gemm_run(const GemmPlan& p, const GemmEpi& epi, unsigned* err, cudaStr
         if (epi.out_type != OUT_F32 && epi.out_type != OUT_F32_ACC) return fail(WB_ERR_INVALID_ARG, "split-K needs fp32 output");
         if (epi.gelu || epi.add || epi.mode != MODE_PLAIN) return fail(WB_ERR_INVALID_ARG, "split-K: linear epilogue only");
         if (ksplit > kb_all) ksplit = kb_all;
+    }
+    a.stream_k = (p.swap && p.stream_k) ? 1 : 0;
+    if (a.stream_k) {
+        if (epi.out_type != OUT_F32 && epi.out_type != OUT_F32_ACC) return fail(WB_ERR_INVALID_ARG, "stream-K needs fp32 output");
+        ksplit = 1;
     }
     a.ksplit = ksplit;
     a.tiles = a.mt_total * a.nt_total * ksplit;
