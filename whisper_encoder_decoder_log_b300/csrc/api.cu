@@ -258,7 +258,6 @@ struct LinChoice {
     bool simt = false, swap = false;
     int bn = 0, ksplit = 1;
     bool pair = false;            // CTA pairs share B tiles (large plain GEMMs)
-    bool stream_k = false;        // swapped form with few tiles: even k-block shares, one CTA per SM
     bool needs_zero = false;
 };
 
@@ -278,15 +277,9 @@ LinChoice linear_choose(const Lin& L, const GemmEpi& e, bool simt_fp32) {
         c.swap = true;
         c.bn = L.rows <= 32 ? 32 : (L.rows <= 64 ? 64 : 128);
         const int64_t tiles = ((L.N + 127) / 128) * ((L.rows + c.bn - 1) / c.bn);
-        if (tiles < 2 * sms && tiles * kb_all >= sms) {
-            // at most two waves of tiles: an even share of all k-blocks per SM
-            // instead (no CTA runs a second tile while others idle)
-            c.stream_k = true;
-        } else {
-            // one CTA per SM, down to a single k-block per partition
-            const int64_t want = sms / tiles;
-            c.ksplit = (int)std::max<int64_t>(1, std::min<int64_t>(want, kb_all));
-        }
+        // one CTA per SM, down to a single k-block per partition
+        const int64_t want = sms / tiles;
+        c.ksplit = (int)std::max<int64_t>(1, std::min<int64_t>(want, kb_all));
     } else {
         const int64_t tiles_m = ((L.rows + 127) / 128) * L.batches;
         auto tiles = [&](int bn) { return tiles_m * ((L.N + bn - 1) / bn); };
@@ -307,7 +300,7 @@ LinChoice linear_choose(const Lin& L, const GemmEpi& e, bool simt_fp32) {
     if (!c.swap && c.ksplit == 1 && c.bn == 256 && L.batches == 1 &&
         ((L.rows + 255) / 256) * ((L.N + 255) / 256) >= sms)
         c.pair = true;
-    c.needs_zero = (c.ksplit > 1 || c.stream_k) && e.out_type == OUT_F32;
+    c.needs_zero = c.ksplit > 1 && e.out_type == OUT_F32;
     return c;
 }
 
@@ -353,7 +346,6 @@ wb_status linear_impl(const Lin& L, GemmEpi e, bool simt_fp32, unsigned* err, cu
             return st;
     }
     p.w_const = L.w_const;
-    p.stream_k = c.stream_k;
     return gemm_run(p, e, err, s, 0, c.ksplit);
 }
 

@@ -83,8 +83,10 @@ WB_DEV void unpack8<uint8_t>(const Raw8<uint8_t>& r, float (&v)[8]) {
     }
 }
 
+// One query row per CTA over 16-bit or 8-bit K/V (decode steps) keeps 6 CTAs
+// resident per SM: the K/V stream needs the loads of many CTAs in flight.
 template <int NQ, typename TQ, typename TKV, typename TO>
-__global__ void __launch_bounds__(kRowThreads)
+__global__ void __launch_bounds__(kRowThreads, (NQ == 1 && sizeof(TKV) < 4) ? 6 : 1)
 attn_rows_kernel(const TQ* __restrict__ q, int64_t q_ld, int rows_per_chunk, int n_rows_total,
                  KVView kv, int kv_len, int causal, int q_pos0, TO* __restrict__ out, int64_t o_ld,
                  int64_t o_split) {
@@ -112,7 +114,7 @@ attn_rows_kernel(const TQ* __restrict__ q, int64_t q_ld, int rows_per_chunk, int
         const int qi = i / 64, c = i % 64;
         sq[i] = qi < nq ? (float)q[(row0 + qi) * q_ld + h * 64 + c] * 0.125f : 0.f;
     }
-    const int64_t kc = chunk / kv.beam_div;       // the chunk whose keys this row reads
+    const int64_t kc = kv.beam_div > 1 ? chunk / kv.beam_div : chunk;   // the chunk whose keys this row reads
     const int64_t cb = kv.chunk_off ? kv.chunk_off[kc] : kc * kv.chunk_stride;
     const int64_t hs = kv.head_stride * (kv.chunk_len ? (int64_t)kv.chunk_len[kc] : 1);
     const TKV* Kp = reinterpret_cast<const TKV*>(kv.ptr) + cb + ((int64_t)kv.k_blk * kv.heads + h) * hs;

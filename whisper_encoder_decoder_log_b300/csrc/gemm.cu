@@ -60,7 +60,6 @@ struct GemmArgs {
     int kblocks;            // k-blocks of the longest split
     int kb_all;             // k-blocks of the whole K
     int ksplit;             // K partitions; > 1 adds partial tiles atomically
-    int stream_k;           // the CTAs split the flattened (tile, k-block) sequence evenly (swapped form)
     int stages;             // smem ring depth (<= the compile-time maximum)
     int w_const;            // the weight operand is constant: load it before the grid dependency wait
     int b_kwrap;
@@ -281,7 +280,7 @@ __device__ __forceinline__ void store_swap(const GemmArgs& a, int64_t n, int64_t
     const int64_t left = a.rows - m0;
     const int nrow = left < 32 ? (int)left : 32;
     const bool nok = n < a.N;
-    const bool red = a.ksplit > 1 || a.stream_k || e.out_type == OUT_F32_ACC;
+    const bool red = a.ksplit > 1 || e.out_type == OUT_F32_ACC;
     float* dst = reinterpret_cast<float*>(e.out) + m0 * e.ldo + n;
 #pragma unroll
     for (int j = 0; j < 32; ++j) {
@@ -302,46 +301,25 @@ __device__ __forceinline__ void split_range(const GemmArgs& a, int64_t t, int& k
     kb1 = (int)((int64_t)(ks + 1) * a.kb_all / a.ksplit);
 }
 
-// One CTA's work: with stream_k, the k-blocks [c T / G, (c + 1) T / G) of
-// the flattened sequence of T = tiles x kb_all (tile-major) k-blocks, cut
-// into one segment per tile it touches (every segment's partial sum is added
-// atomically; the segment that holds k-block 0 adds the bias); otherwise
-// tiles c, c + G, c + 2 G, ... with their K partitions (split_range).
+// One CTA's work: tiles c, c + G, c + 2 G, ... (G CTAs or CTA pairs), each
+// with its K partition [kb0, kb1) (split_range); kb0 == 0 marks the part
+// that adds the bias.
 struct WorkIter {
     int64_t cur, end, step;
 };
 __device__ __forceinline__ WorkIter work_begin(const GemmArgs& a, int64_t c, int64_t g) {
     WorkIter w;
-    if (a.stream_k) {
-        const int64_t T = a.tiles * (int64_t)a.kb_all;
-        w.cur = c * T / g;
-        w.end = (c + 1) * T / g;
-        w.step = 0;
-    } else {
-        w.cur = c;
-        w.end = a.tiles;
-        w.step = g;
-    }
+    w.cur = c;
+    w.end = a.tiles;
+    w.step = g;
     return w;
 }
-// Next work item: tile (mt, nt), k-blocks [kb0, kb1); first: kb0 is the
-// tile's first k-block (the bias goes with it).
 __device__ __forceinline__ bool work_next(const GemmArgs& a, WorkIter& w, int64_t& mt, int64_t& nt, int& kb0,
                                           int& kb1) {
     if (w.cur >= w.end) return false;
-    if (a.stream_k) {
-        const int64_t u = w.cur / a.kb_all;
-        kb0 = (int)(w.cur - u * a.kb_all);
-        const int64_t left = w.end - w.cur;
-        kb1 = (int)min((int64_t)a.kb_all, (int64_t)kb0 + left);
-        mt = u / a.nt_total;
-        nt = u - mt * a.nt_total;
-        w.cur += kb1 - kb0;
-    } else {
-        tile_coords(a, w.cur, mt, nt);
-        split_range(a, w.cur, kb0, kb1);
-        w.cur += w.step;
-    }
+    tile_coords(a, w.cur, mt, nt);
+    split_range(a, w.cur, kb0, kb1);
+    w.cur += w.step;
     return true;
 }
 
@@ -730,19 +708,45 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant_
                     *reinterpret_cast<float4*>(stg + lane * 32 + ((q ^ (lane & 7)) << 2)) =
                         make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
                 __syncwarp();
-                const int64_t col = n0 + lane;
                 const int64_t rq = (PAIR ? mt : mt % args.mt_per_batch) * kBM + g * 32;   // first row of the quarter
                 const int64_t obr = e.out_batch_rows ? e.out_batch_rows : args.rows;
                 const bool reduce = args.ksplit > 1;             // partial tiles of one output
-                float* ob = reinterpret_cast<float*>(e.out) + (b * obr + e.out_row_offset) * e.ldo + col;
-                if (col < args.N) {
-#pragma unroll 4
-                    for (int rr = 0; rr < 32; ++rr) {
+                float* obase = reinterpret_cast<float*>(e.out) + (b * obr + e.out_row_offset) * e.ldo;
+                if (e.vec) {
+                    // lane = (row i4 of 4, 16-byte piece q of 8): one instruction
+                    // writes 4 rows x 128 bytes
+                    const int i4 = lane >> 3, q = lane & 7;
+                    const int64_t col = n0 + 4 * q;
+#pragma unroll 2
+                    for (int pp = 0; pp < 8; ++pp) {
+                        const int rr = 4 * pp + i4;
                         if (rq + rr >= args.rows) break;
-                        const float x = stg[rr * 32 + ((((lane >> 2) ^ (rr & 7))) << 2) + (lane & 3)];
-                        float* dst = ob + (rq + rr) * e.ldo;
-                        if (reduce) atomicAdd(dst, x);   // result unused: a reduction
-                        else *dst = x;
+                        const float4 x = *reinterpret_cast<const float4*>(stg + rr * 32 + ((q ^ (rr & 7)) << 2));
+                        float* dst = obase + (rq + rr) * e.ldo + col;
+                        if (col + 3 < args.N) {
+                            if (reduce) atomicAdd(reinterpret_cast<float4*>(dst), x);   // a reduction
+                            else *reinterpret_cast<float4*>(dst) = x;
+                        } else {
+                            const float xs[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+                            for (int j = 0; j < 4; ++j)
+                                if (col + j < args.N) {
+                                    if (reduce) atomicAdd(dst + j, xs[j]);
+                                    else dst[j] = xs[j];
+                                }
+                        }
+                    }
+                } else {
+                    const int64_t col = n0 + lane;
+                    if (col < args.N) {
+#pragma unroll 4
+                        for (int rr = 0; rr < 32; ++rr) {
+                            if (rq + rr >= args.rows) break;
+                            const float x = stg[rr * 32 + ((((lane >> 2) ^ (rr & 7))) << 2) + (lane & 3)];
+                            float* dst = obase + (rq + rr) * e.ldo + col;
+                            if (reduce) atomicAdd(dst, x);   // result unused: a reduction
+                            else *dst = x;
+                        }
                     }
                 }
                 __syncwarp();
@@ -830,16 +834,15 @@ wb_status launch_tc(const GemmPlan& p, GemmArgs a, unsigned* err, cudaStream_t s
     }
     // A CTA that sees few k-blocks needs a shallow ring; the smaller footprint
     // lets several CTAs share an SM (bounded by shared memory and TMEM).
-    const int64_t kb_per_cta = a.stream_k ? (a.tiles * a.kb_all + num_sms() - 1) / num_sms()
-                                          : (int64_t)a.kblocks * ((a.tiles + num_sms() - 1) / num_sms());
+    const int64_t kb_per_cta = (int64_t)a.kblocks * ((a.tiles + num_sms() - 1) / num_sms());
     a.stages = (int)std::max<int64_t>(2, std::min<int64_t>(C::STAGES, kb_per_cta));
     const int smem = a.stages * C::STAGE_BYTES + kEpiStageBytes + 1024 + 256;
     int occ = 1;
     WB_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, gemm_tc_kernel<BN, FP8, SWAP>, kGemmThreads, smem));
     const int per_sm = std::max(1, std::min({occ, 512 / C::TMEM_COLS, 4}));
-    int grid = a.stream_k ? num_sms() : num_sms() * per_sm;
+    int grid = num_sms() * per_sm;
     if (max_ctas > 0) grid = std::min(grid, max_ctas);
-    grid = (int)std::min<int64_t>(grid, a.stream_k ? a.tiles * a.kb_all : a.tiles);
+    grid = (int)std::min<int64_t>(grid, a.tiles);
     if (grid <= 0) return WB_OK;
     WB_CUDA(launch_k(gemm_tc_kernel<BN, FP8, SWAP>, dim3(grid), dim3(kGemmThreads), smem, s, p.tma_a, p.tma_b, a, err));
     WB_CUDA(cudaGetLastError());
@@ -999,11 +1002,6 @@ wb_status gemm_run(const GemmPlan& p, const GemmEpi& epi, unsigned* err, cudaStr
         if (epi.out_type != OUT_F32 && epi.out_type != OUT_F32_ACC) return fail(WB_ERR_INVALID_ARG, "split-K needs fp32 output");
         if (epi.gelu || epi.add || epi.mode != MODE_PLAIN) return fail(WB_ERR_INVALID_ARG, "split-K: linear epilogue only");
         if (ksplit > kb_all) ksplit = kb_all;
-    }
-    a.stream_k = (p.swap && p.stream_k) ? 1 : 0;
-    if (a.stream_k) {
-        if (epi.out_type != OUT_F32 && epi.out_type != OUT_F32_ACC) return fail(WB_ERR_INVALID_ARG, "stream-K needs fp32 output");
-        ksplit = 1;
     }
     a.ksplit = ksplit;
     a.tiles = a.mt_total * a.nt_total * ksplit;

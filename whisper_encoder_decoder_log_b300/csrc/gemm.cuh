@@ -65,7 +65,6 @@ struct GemmPlan {
     bool swap = false;     // small-M form: weights are the 128-row MMA operand
     bool w_const = false;  // the weight operand is not written by kernels this GEMM may overlap
     bool pair = false;     // CTA pairs: cta_group::2 MMAs over 256-row tiles, each CTA loads half of B
-    bool stream_k = false; // swapped form: one CTA per SM, each an equal share of all (tile, k-block) pairs
     bool ok = false;
 };
 
@@ -79,8 +78,7 @@ wb_status gemm_plan(GemmPlan* plan, const GemmOperand& A, const GemmOperand& B, 
 wb_status gemm_plan_swap(GemmPlan* plan, const GemmOperand& X, const GemmOperand& W, int64_t N, int64_t K,
                          bool fp8, int bn, int64_t w_kwrap = 0);
 // ksplit > 1 partitions K across CTAs and adds partial tiles with fp32
-// atomics (fp32 outputs only; the caller zeroes a non-residual output first);
-// plan.stream_k does the same with an even share of k-blocks per CTA.
+// atomics (fp32 outputs only; the caller zeroes a non-residual output first).
 // rows_override < M_rows restricts the launch to the first rows.
 wb_status gemm_run(const GemmPlan& plan, const GemmEpi& epi, unsigned* err, cudaStream_t s,
                    int max_ctas = 0, int ksplit = 1, int64_t rows_override = 0);

@@ -12,11 +12,13 @@
 // 400-point FFT (z = x_a + i x_b), split as 400 = 16 x 25:
 //   stage 1: per (pair, n2) a 16-point DFT over n1 of z[25 n1 + n2], times
 //            the twiddle W400^(n2 k1);
-//   stage 2: per (pair, k1) a 25-point DFT (as 5 x 5) over n2, in place, so
-//            slot k1 + 16 k2 ends up holding Z[k1 + 16 k2];
-// then X_a, X_b are separated from Z[k] and Z[400-k], the power of bins 0..200
-// goes through the sparse mel filterbank (each bin feeds at most two
-// filters), and log10 is taken.  The unfloored value (l + 4) / 4 is written
+//   stage 2: per (pair, k1) a 25-point DFT (as 5 x 5) over n2 in registers,
+//            giving Z[k1 + 16 k2] for k2 = 0..24;
+// then X_a, X_b are separated from Z[k] and Z[400-k] (exchanged between the
+// threads that hold them by warp shuffles), the power of bins 0..200 goes
+// through the sparse mel filterbank (each bin feeds at most two filters;
+// one thread takes a filter over four frames), and log10 is taken.  The
+// unfloored value (l + 4) / 4 is written
 // to HBM right away, and the CTA keeps its maximum and each sub-block's
 // minimum; the cluster then reduces the chunk maximum through distributed
 // shared memory, and each CTA re-reads (from L2, 16 bytes at a time) only
@@ -48,6 +50,9 @@ constexpr int kThreads = 256;
 constexpr int kMaxMels = 128;
 constexpr int kMaxFbNnz = 512;
 constexpr int kSubBlocks = (kFramesPerCta + kSub - 1) / kSub;   // 12
+// stage 2 runs one (pair, k1) per thread, all threads at once (its power
+// step exchanges values between threads with warp shuffles)
+static_assert(kPairs * 16 == kThreads, "stage 2 needs one thread per (pair, k1)");
 
 // float -> unsigned key with the same order (for atomicMin on shared memory)
 __device__ __forceinline__ unsigned order_key(float f) {
@@ -59,7 +64,6 @@ __device__ __forceinline__ float key_value(unsigned k) {
 }
 
 struct MelTables {
-    float2 tw[kNFFT];          // W400^j = exp(-2 pi i j / 400)
     float2 tw1[16 * 25];       // stage-1 twiddles W400^(n2 k1) at [k1][n2]
     float win[kNFFT];          // periodic Hann
     int4 meta[kMaxMels];       // filter m: first bin, bin count, weight offset
@@ -83,6 +87,31 @@ __device__ __forceinline__ float2 cadd(float2 a, float2 b) { return make_float2(
 __device__ __forceinline__ float2 csub(float2 a, float2 b) { return make_float2(a.x - b.x, a.y - b.y); }
 // -i * a
 __device__ __forceinline__ float2 cmi(float2 a) { return make_float2(a.y, -a.x); }
+
+// Inner twiddles of the 16-point (W16^k = W400^(25 k), k = b c <= 9) and
+// 25-point (W25^k = W400^(16 k), k <= 16) transforms: constants once the
+// loops over b and c are unrolled (fp32 roundings of cos and -sin).
+__device__ __forceinline__ float2 w16c(int k) {
+    constexpr float c[10] = {1.0f, 0.9238795042037964f, 0.7071067690849304f, 0.3826834261417389f, 0.0f,
+                             -0.3826834261417389f, -0.7071067690849304f, -0.9238795042037964f, -1.0f,
+                             -0.9238795042037964f};
+    constexpr float s[10] = {-0.0f, -0.3826834261417389f, -0.7071067690849304f, -0.9238795042037964f, -1.0f,
+                             -0.9238795042037964f, -0.7071067690849304f, -0.3826834261417389f, 0.0f,
+                             0.3826834261417389f};
+    return make_float2(c[k], s[k]);
+}
+__device__ __forceinline__ float2 w25c(int k) {
+    constexpr float c[17] = {1.0f, 0.9685831665992737f, 0.8763066530227661f, 0.728968620300293f, 0.5358268022537231f,
+                             0.30901700258255005f, 0.06279052048921585f, -0.187381312251091f, -0.4257792830467224f,
+                             -0.6374239921569824f, -0.80901700258255f, -0.9297764897346497f, -0.9921147227287292f,
+                             -0.9921147227287292f, -0.9297764897346497f, -0.80901700258255f, -0.6374239921569824f};
+    constexpr float s[17] = {-0.0f, -0.24868988990783691f, -0.4817536771297455f, -0.6845471262931824f,
+                             -0.8443279266357422f, -0.9510565400123596f, -0.9980267286300659f, -0.9822872281074524f,
+                             -0.9048270583152771f, -0.7705132365226746f, -0.5877852439880371f, -0.3681245446205139f,
+                             -0.12533323466777802f, 0.12533323466777802f, 0.3681245446205139f, 0.5877852439880371f,
+                             0.7705132365226746f};
+    return make_float2(c[k], s[k]);
+}
 
 // 4-point DFT with W4 = -i, in place.
 __device__ __forceinline__ void dft4(float2& x0, float2& x1, float2& x2, float2& x3) {
@@ -182,7 +211,8 @@ mel_kernel(const float* __restrict__ audio, const MelTables* __restrict__ tables
 #pragma unroll
             for (int b = 1; b < 4; ++b)
 #pragma unroll
-                for (int c = 1; c < 4; ++c) v[4 * c + b] = cmul(v[4 * c + b], S.t.tw[25 * b * c]);
+                for (int c = 1; c < 4; ++c)
+                    v[4 * c + b] = (b * c == 4) ? cmi(v[4 * c + b]) : cmul(v[4 * c + b], w16c(b * c));
 #pragma unroll
             for (int c = 0; c < 4; ++c) dft4(v[4 * c + 0], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
             // v[4 c + d] now holds Y[k1 = c + 4 d]
@@ -211,42 +241,62 @@ mel_kernel(const float* __restrict__ audio, const MelTables* __restrict__ tables
 #pragma unroll
             for (int b = 1; b < 5; ++b)
 #pragma unroll
-                for (int c = 1; c < 5; ++c) v[5 * c + b] = cmul(v[5 * c + b], S.t.tw[16 * b * c]);
+                for (int c = 1; c < 5; ++c) v[5 * c + b] = cmul(v[5 * c + b], w25c(b * c));
 #pragma unroll
             for (int c = 0; c < 5; ++c)
                 dft5(v[5 * c + 0], v[5 * c + 1], v[5 * c + 2], v[5 * c + 3], v[5 * c + 4]);
-            // v[5 c + d] holds Z[k1 + 16 (c + 5 d)]
+            // v[5 c + d] holds Z[k1 + 16 k2], k2 = c + 5 d.
+            // ---- separate the two real frames and take the power of the bins
+            // k = k1 + 16 k2 <= 200 held here: Z[400 - k] is held by the
+            // thread (16 - k1, 24 - k2) of the same pair, in the same half-warp
+            // (k1 = 0: by this thread, as Z[16 (25 - k2) mod 400])
+            const int partner = (tid & 16) | ((16 - k1) & 15);
+            float* pa = S.p + (2 * pr) * kPStride;
+            float* pb = pa + kPStride;
 #pragma unroll
-            for (int c = 0; c < 5; ++c)
-#pragma unroll
-                for (int d = 0; d < 5; ++d) zp[17 * (c + 5 * d)] = v[5 * c + d];
+            for (int k2 = 0; k2 <= 12; ++k2) {
+                const int sk = 24 - k2;                  // the value the partner takes from this thread
+                const float2 mine = v[5 * (sk % 5) + sk / 5];
+                float2 zn;
+                zn.x = __shfl_sync(0xffffffffu, mine.x, partner);
+                zn.y = __shfl_sync(0xffffffffu, mine.y, partner);
+                if (k1 == 0) {
+                    const int q = (25 - k2) % 25;
+                    zn = v[5 * (q % 5) + q / 5];
+                }
+                const int k = k1 + 16 * k2;
+                if (k < kBins) {
+                    const float2 zk = v[5 * (k2 % 5) + k2 / 5];
+                    const float ar = zk.x + zn.x, ai = zk.y - zn.y;     // 2 X_a
+                    const float br = zk.y + zn.y, bi = zn.x - zk.x;     // 2 X_b
+                    pa[k] = 0.25f * (ar * ar + ai * ai);
+                    pb[k] = 0.25f * (br * br + bi * bi);
+                }
+            }
         }
         __syncthreads();
-        // ---- separate the two real frames, power spectrum
-        for (int it = tid; it < kPairs * kBins; it += kThreads) {
-            const int pr = it / kBins, k = it % kBins;
-            const int kk = (kNFFT - k) % kNFFT;
-            const float2 zk = S.z[pr * kZStride + k + k / 16];
-            const float2 zn = S.z[pr * kZStride + kk + kk / 16];
-            const float ar = zk.x + zn.x, ai = zk.y - zn.y;     // 2 X_a
-            const float br = zk.y + zn.y, bi = zn.x - zk.x;     // 2 X_b
-            S.p[(2 * pr) * kPStride + k] = 0.25f * (ar * ar + ai * ai);
-            S.p[(2 * pr + 1) * kPStride + k] = 0.25f * (br * br + bi * bi);
-        }
-        __syncthreads();
-        // ---- mel filterbank, log10, unfloored output
+        // ---- mel filterbank, log10, unfloored output: one item = filter m
+        // over frames f, f + 8, f + 16, f + 24 (each weight read once for 4)
         float smin = 1e30f;
-        for (int it = tid; it < n_mels * kSub; it += kThreads) {
-            const int m = it / kSub, f = it % kSub;
-            if (f >= nf) continue;
-            const float* pf = S.p + f * kPStride;
+        for (int it = tid; it < n_mels * (kSub / 4); it += kThreads) {
+            const int m = it / (kSub / 4), f = it % (kSub / 4);
             const int4 mt = S.t.meta[m];
-            float e = 0.f;
-            for (int j = 0; j < mt.y; ++j) e = fmaf(S.t.w[mt.z + j], pf[mt.x + j], e);
-            const float ell = __log2f(fmaxf(e, 1e-10f)) * 0.30102999566398120f;
-            tmax = fmaxf(tmax, ell);
-            smin = fminf(smin, ell);
-            o[(int64_t)m * kFrames + f0 + f] = (ell + 4.0f) * 0.25f;
+            const float* pf = S.p + f * kPStride + mt.x;
+            float e[4] = {0.f, 0.f, 0.f, 0.f};
+            for (int j = 0; j < mt.y; ++j) {
+                const float w = S.t.w[mt.z + j];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) e[i] = fmaf(w, pf[i * 8 * kPStride + j], e[i]);
+            }
+            float* orow = o + (int64_t)m * kFrames + f0 + f;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                if (f + 8 * i >= nf) break;
+                const float ell = __log2f(fmaxf(e[i], 1e-10f)) * 0.30102999566398120f;
+                tmax = fmaxf(tmax, ell);
+                smin = fminf(smin, ell);
+                orow[8 * i] = (ell + 4.0f) * 0.25f;
+            }
         }
         smin = warp_min(smin);
         if ((tid & 31) == 0) atomicMin(&S.smin[sb], order_key(smin));
@@ -301,12 +351,12 @@ double mel_to_hz_slaney(double m) {
 
 bool build_tables(int n_mels, MelTables* t) {
     const double pi = 3.14159265358979323846;
-    for (int j = 0; j < kNFFT; ++j) {
-        t->tw[j] = make_float2((float)std::cos(2 * pi * j / kNFFT), (float)-std::sin(2 * pi * j / kNFFT));
-        t->win[j] = (float)(0.5 - 0.5 * std::cos(2 * pi * j / kNFFT));
-    }
+    for (int j = 0; j < kNFFT; ++j) t->win[j] = (float)(0.5 - 0.5 * std::cos(2 * pi * j / kNFFT));
     for (int k1 = 0; k1 < 16; ++k1)
-        for (int n2 = 0; n2 < 25; ++n2) t->tw1[k1 * 25 + n2] = t->tw[(k1 * n2) % kNFFT];
+        for (int n2 = 0; n2 < 25; ++n2) {
+            const int j = (k1 * n2) % kNFFT;
+            t->tw1[k1 * 25 + n2] = make_float2((float)std::cos(2 * pi * j / kNFFT), (float)-std::sin(2 * pi * j / kNFFT));
+        }
     const double mlo = hz_to_mel_slaney(0.0), mhi = hz_to_mel_slaney(8000.0);
     std::vector<double> pts(n_mels + 2);
     for (int i = 0; i < n_mels + 2; ++i)
