@@ -261,36 +261,53 @@ __global__ void kv_append_kernel(const float* __restrict__ qkv, int64_t n_chunks
     }
 }
 
-// Per-row E4M3 quantisation of an fp32 matrix; with GELU, of GELU(x) (the
-// value is recomputed in both passes instead of being stored).
+// Per-row E4M3 quantisation of an fp32 matrix; with GELU, of GELU(x).  One
+// CTA per row: each thread keeps its (at most kQuantRowVec) float4 pieces in
+// registers between the row's amax and the codes, so GELU runs once per
+// element and the row is read once.
+constexpr int kQuantRowThreads = 256;
+constexpr int kQuantRowVec = 8;            // K <= 4 * 256 * 8 = 8192
+
 template <bool GELU>
-__global__ void quant_rows_f32_kernel(const float* __restrict__ x, int64_t rows, int K, uint8_t* __restrict__ q,
-                                      float* __restrict__ row_scale) {
+__global__ void __launch_bounds__(kQuantRowThreads)
+quant_rows_f32_kernel(const float* __restrict__ x, int64_t rows, int K, uint8_t* __restrict__ q,
+                      float* __restrict__ row_scale) {
     griddep_wait();
     griddep_launch();
-    const int64_t r = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
-    const int lane = threadIdx.x & 31;
+    __shared__ float red[kQuantRowThreads / 32];
+    const int64_t r = blockIdx.x;
     if (r >= rows) return;
     const float* xr = x + r * K;
+    float4 v[kQuantRowVec];
     float m = 0.f;
-    auto load = [&](int i) {
-        float4 a = *reinterpret_cast<const float4*>(xr + i);
-        if (GELU) { a.x = gelu_f(a.x); a.y = gelu_f(a.y); a.z = gelu_f(a.z); a.w = gelu_f(a.w); }
-        return a;
-    };
-    for (int i = lane * 4; i < K; i += 128) {
-        const float4 a = load(i);
-        m = fmaxf(m, fmaxf(fmaxf(fabsf(a.x), fabsf(a.y)), fmaxf(fabsf(a.z), fabsf(a.w))));
+#pragma unroll
+    for (int j = 0; j < kQuantRowVec; ++j) {
+        const int i = (threadIdx.x + j * kQuantRowThreads) * 4;
+        if (i < K) {
+            float4 a = *reinterpret_cast<const float4*>(xr + i);
+            if (GELU) { a.x = gelu_f(a.x); a.y = gelu_f(a.y); a.z = gelu_f(a.z); a.w = gelu_f(a.w); }
+            v[j] = a;
+            m = fmaxf(m, fmaxf(fmaxf(fabsf(a.x), fabsf(a.y)), fmaxf(fabsf(a.z), fabsf(a.w))));
+        }
     }
     m = warp_max(m);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+    __syncthreads();
+    m = red[0];
+#pragma unroll
+    for (int w = 1; w < kQuantRowThreads / 32; ++w) m = fmaxf(m, red[w]);
     const float sc = m > 0.f ? m / 448.0f : 1.0f;
     const float inv = 1.0f / sc;
-    for (int i = lane * 4; i < K; i += 128) {
-        const float4 a = load(i);
-        const uint32_t o = (uint32_t)f2e4m3x2(a.x * inv, a.y * inv) | ((uint32_t)f2e4m3x2(a.z * inv, a.w * inv) << 16);
-        *reinterpret_cast<uint32_t*>(q + r * K + i) = o;
+#pragma unroll
+    for (int j = 0; j < kQuantRowVec; ++j) {
+        const int i = (threadIdx.x + j * kQuantRowThreads) * 4;
+        if (i < K) {
+            const float4 a = v[j];
+            const uint32_t o = (uint32_t)f2e4m3x2(a.x * inv, a.y * inv) | ((uint32_t)f2e4m3x2(a.z * inv, a.w * inv) << 16);
+            *reinterpret_cast<uint32_t*>(q + r * K + i) = o;
+        }
     }
-    if (lane == 0) row_scale[r] = sc;
+    if (threadIdx.x == 0) row_scale[r] = sc;
 }
 
 // amax of each group of group_elems consecutive fp32 values: grid (slices,
@@ -884,12 +901,13 @@ wb_status kv_append(const float* qkv, int64_t n_chunks, int P, int p0, int d, in
 wb_status quant_rows_f32(const float* x, int64_t rows, int K, uint8_t* q, float* row_scale, cudaStream_t s,
                          bool gelu) {
     if (rows <= 0) return WB_OK;
-    if (K % 128) return fail(WB_ERR_SHAPE, "row quantiser needs K % 128 == 0");
+    if (K % 128 || K > 4 * kQuantRowThreads * kQuantRowVec)
+        return fail(WB_ERR_SHAPE, "row quantiser needs K % 128 == 0 and K <= 8192");
     if (gelu)
-        WB_CUDA(launch_k(quant_rows_f32_kernel<true>, dim3((unsigned)((rows + 7) / 8)), dim3(256), 0, s, x, rows, K, q,
-                         row_scale));
+        WB_CUDA(launch_k(quant_rows_f32_kernel<true>, dim3((unsigned)rows), dim3(kQuantRowThreads), 0, s, x, rows, K,
+                         q, row_scale));
     else
-        WB_CUDA(launch_k(quant_rows_f32_kernel<false>, dim3((unsigned)((rows + 7) / 8)), dim3(256), 0, s, x, rows, K,
+        WB_CUDA(launch_k(quant_rows_f32_kernel<false>, dim3((unsigned)rows), dim3(kQuantRowThreads), 0, s, x, rows, K,
                          q, row_scale));
     WB_CUDA(cudaGetLastError());
     return WB_OK;

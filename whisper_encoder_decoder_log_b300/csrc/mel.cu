@@ -113,30 +113,71 @@ __device__ __forceinline__ float2 w25c(int k) {
     return make_float2(c[k], s[k]);
 }
 
+// Packed fp32 pair arithmetic (add/sub/mul/fma .f32x2: one instruction for
+// both halves of a complex value); the butterflies below use it.
+__device__ __forceinline__ float2 add2(float2 a, float2 b) {
+    unsigned long long r, x, y;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "f"(a.x), "f"(a.y));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(y) : "f"(b.x), "f"(b.y));
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(x), "l"(y));
+    float2 o;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(o.x), "=f"(o.y) : "l"(r));
+    return o;
+}
+__device__ __forceinline__ float2 sub2(float2 a, float2 b) {
+    unsigned long long r, x, y;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "f"(a.x), "f"(a.y));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(y) : "f"(b.x), "f"(b.y));
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(x), "l"(y));
+    float2 o;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(o.x), "=f"(o.y) : "l"(r));
+    return o;
+}
+// a * (c, c) + b
+__device__ __forceinline__ float2 fma2s(float2 a, float c, float2 b) {
+    unsigned long long r, x, y, cc;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "f"(a.x), "f"(a.y));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(y) : "f"(b.x), "f"(b.y));
+    asm("mov.b64 %0, {%1, %1};" : "=l"(cc) : "f"(c));
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(x), "l"(cc), "l"(y));
+    float2 o;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(o.x), "=f"(o.y) : "l"(r));
+    return o;
+}
+__device__ __forceinline__ float2 mul2s(float2 a, float c) {
+    unsigned long long r, x, cc;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "f"(a.x), "f"(a.y));
+    asm("mov.b64 %0, {%1, %1};" : "=l"(cc) : "f"(c));
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(x), "l"(cc));
+    float2 o;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(o.x), "=f"(o.y) : "l"(r));
+    return o;
+}
+
 // 4-point DFT with W4 = -i, in place.
 __device__ __forceinline__ void dft4(float2& x0, float2& x1, float2& x2, float2& x3) {
-    float2 a = cadd(x0, x2), b = csub(x0, x2), c = cadd(x1, x3), d = cmi(csub(x1, x3));
-    x0 = cadd(a, c);
-    x2 = csub(a, c);
-    x1 = cadd(b, d);
-    x3 = csub(b, d);
+    float2 a = add2(x0, x2), b = sub2(x0, x2), c = add2(x1, x3), d = cmi(sub2(x1, x3));
+    x0 = add2(a, c);
+    x2 = sub2(a, c);
+    x1 = add2(b, d);
+    x3 = sub2(b, d);
 }
 
 // 5-point DFT with W5 = exp(-2 pi i / 5), in place.
 __device__ __forceinline__ void dft5(float2& x0, float2& x1, float2& x2, float2& x3, float2& x4) {
     const float c1 = 0.30901699437494742f, c2 = -0.80901699437494742f;
     const float s1 = 0.95105651629515357f, s2 = 0.58778525229247313f;
-    float2 t1 = cadd(x1, x4), t2 = cadd(x2, x3), t3 = csub(x1, x4), t4 = csub(x2, x3);
-    float2 a1 = make_float2(x0.x + c1 * t1.x + c2 * t2.x, x0.y + c1 * t1.y + c2 * t2.y);
-    float2 a2 = make_float2(x0.x + c2 * t1.x + c1 * t2.x, x0.y + c2 * t1.y + c1 * t2.y);
-    float2 b1 = make_float2(s1 * t3.x + s2 * t4.x, s1 * t3.y + s2 * t4.y);
-    float2 b2 = make_float2(s2 * t3.x - s1 * t4.x, s2 * t3.y - s1 * t4.y);
-    x0 = cadd(x0, cadd(t1, t2));
+    float2 t1 = add2(x1, x4), t2 = add2(x2, x3), t3 = sub2(x1, x4), t4 = sub2(x2, x3);
+    float2 a1 = fma2s(t2, c2, fma2s(t1, c1, x0));
+    float2 a2 = fma2s(t2, c1, fma2s(t1, c2, x0));
+    float2 b1 = fma2s(t4, s2, mul2s(t3, s1));
+    float2 b2 = fma2s(t4, -s1, mul2s(t3, s2));
+    x0 = add2(x0, add2(t1, t2));
     float2 ib1 = cmi(b1), ib2 = cmi(b2);                // -i b
-    x1 = cadd(a1, ib1);
-    x4 = csub(a1, ib1);
-    x2 = cadd(a2, ib2);
-    x3 = csub(a2, ib2);
+    x1 = add2(a1, ib1);
+    x4 = sub2(a1, ib1);
+    x2 = add2(a2, ib2);
+    x3 = sub2(a2, ib2);
 }
 
 __global__ void __launch_bounds__(kThreads, 2)
