@@ -591,7 +591,7 @@ def main():
         # three launches over 128 chunks x 20 heads (cross_attn_decode_turbo.md)
         KIND["cross_attn"]: ((983.81e6 + 3.03e6) + (983.73e6 + 0.45e6) + (983.73e6 + 0.44e6)) / 3
                             / (128 * 20 * (2 * 1500 * 64 * 2 + 64 * 4 + 64 * 2)),
-        KIND["mel"]: (139.39e6 + 63.99e6) / (64 * (480000 * 4 + 128 * 3000 * 4)),
+        KIND["mel"]: (126.83e6 + 62.09e6) / (64 * (480000 * 4 + 128 * 3000 * 4)),
     }
     if w.kv_fp8 == KV_FP8_CROSS:      # the E4M3 cross-attention has no capture of its own
         traffic_ratio.pop(KIND["cross_attn"])

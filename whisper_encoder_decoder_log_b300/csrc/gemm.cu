@@ -454,18 +454,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant_
                 int64_t mt, nt;
                 int kb0, kb1;
                 while (pre < STAGES && work_next(args, wi, mt, nt, kb0, kb1)) {
-                    const int pre0 = pre;
                     for (int kb = kb0; kb < kb1 && pre < STAGES; ++kb, ++pre) {
                         arm(pre);
                         load_w(pre, mt, (int)(nt * BN), kb * (FP8 ? 128 : 64));
                     }
-                    // few-row GEMMs: the rest of this tile's weights go to L2
-                    // now, so that the ring refills hit L2 instead of HBM
-                    if (SWAP)
-                        for (int kb = kb0 + (pre - pre0); kb < kb1; ++kb) {
-                            const int kx = kb * (FP8 ? 128 : 64);
-                            tma_prefetch_l2_3d(&tma_a, args.b_kwrap ? kx % args.b_kwrap : kx, (int)(mt * kBM), 0);
-                        }
                 }
             }
             griddep_wait();

@@ -138,8 +138,16 @@ def main():
         for _ in range(a.iters):
             d = wb.wb_decoder_init(model, lens, enc, tok, dws)
             wb.wb_decode_prefix(d, 4)
-            for _ in range(a.steps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            for i in range(a.steps):
+                if i == min(2, a.steps - 1):
+                    e0.record()
                 wb.wb_decode_step(d, B)
+            e1.record()
+            torch.cuda.synchronize()
+            if a.time and a.steps > 2:
+                print(f"profile case decode8: {e0.elapsed_time(e1) * 1e3 / (a.steps - 2):.1f} us per decode step "
+                      f"({B} chunks, graph replay)")
             wb.wb_decoder_destroy(d)
         wb.wb_sync_status(model)
         wb.wb_model_destroy(model)
