@@ -1,6 +1,6 @@
 """End-to-end GPU parity of the model path against the CPU oracle.
 
-Tolerances (spec contract): mel 1e-4 absolute; teacher-forced logits
+Tolerances (the stated bar): mel 1e-4 absolute; teacher-forced logits
 2e-2 max-abs for bf16 and 6e-2 with the E4M3 KV cache / FP8 GEMMs; top-1
 agreement >= 99 % of positions.  The fp32 tiny model is expected ~1e-4.
 """
