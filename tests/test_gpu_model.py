@@ -148,3 +148,33 @@ def test_mixed_fp8_decoder_on_seeded_encoder_states():
         # (tests/test_oracle_model.py::test_fp8_decoder_moves_with_float32_level_perturbations),
         # so no float32 implementation can hold the bar against a float64 oracle.
         pytest.xfail(f"mixed_fp8 decoder misses the bar: worst {worst:.3e}, top-1 {agree / total:.4f}")
+
+
+def test_decoder_wide_logits_on_cta_pairs():
+    """Decode steps over 300 chunks: the logits GEMM (51866 wide, >= 256
+    rows) runs on 256 x 256 CTA-pair tiles instead of the few-row form.
+    Sampled chunks' step logits within 6e-2 of the oracle and top-1 equal."""
+    dims = _dims(TURBO, 0, 2)
+    m = GpuModel(dims, wb.PREC_BF16, wb.KV_FP8_SELF, seed=8)
+    B = 300
+    rng = np.random.default_rng(81)
+    enc_np = round_to_bf16(rng.normal(size=(B, 1500, dims.d_model)).astype(np.float32))
+    enc = torch.from_numpy(enc_np).to(torch.bfloat16).cuda()
+    lens = np.full(B, 7, np.int32)
+    prefix = np.tile(forced_prefix(4, dims.vocab), (B, 1))
+    tok, outs = m.decode(enc, prefix, lens, steps=2)
+    assert outs[1].shape == (B, dims.vocab) and outs[2].shape == (B, dims.vocab)
+    worst, agree, total = 0.0, 0, 0
+    for c in (0, 151, 299):
+        ref, _ = omodel.decode_teacher_forced(tok[c, :6], enc_np[c].astype(np.float64), m.W, dims, kv_fp8=True,
+                                              act16=True)
+        for j, got in enumerate((outs[1][c], outs[2][c])):
+            r = ref[4 + j]
+            worst = max(worst, float(np.abs(got - r).max()))
+            agree += int(np.argmax(got) == np.argmax(r))
+            total += 1
+            assert tok[c, 5 + j] == np.argmax(got)
+    print(f"wide logits over {B} rows: worst {worst:.3e}, top-1 {agree}/{total}")
+    m.close()
+    assert worst <= 6e-2, worst
+    assert agree == total

@@ -272,7 +272,12 @@ LinChoice linear_choose(const Lin& L, const GemmEpi& e, bool simt_fp32) {
     const bool linear_f32 = (e.out_type == OUT_F32 || e.out_type == OUT_F32_ACC) && !e.gelu && !e.add &&
                             e.mode == MODE_PLAIN;
     const int64_t kb_all = (L.split ? 2 * L.K : L.K) / (f8 ? 128 : 64);
-    if (linear_f32 && L.batches == 1 && L.rows <= kSwapRows && !e.out_batch_rows && !e.out_row_offset) {
+    // a wide GEMM (the logits) over at least 256 rows has enough 256 x 256
+    // CTA-pair tiles to fill the GPU; the pair form reads each operand tile
+    // for twice the outputs of the swapped form
+    const bool wide_pair = L.rows >= 256 && ((L.rows + 255) / 256) * ((L.N + 255) / 256) >= 2 * sms;
+    if (linear_f32 && L.batches == 1 && L.rows <= kSwapRows && !wide_pair && !e.out_batch_rows &&
+        !e.out_row_offset) {
         // few rows: weights as the 128-row MMA operand, rows as the MMA N
         c.swap = true;
         c.bn = L.rows <= 32 ? 32 : (L.rows <= 64 ? 64 : 128);
