@@ -178,4 +178,7 @@ def test_mixed_serving_batch_full_size():
         # FP8 logits move by more than 6e-2 under a relative 1e-7 perturbation
         # (tests/test_oracle_model.py::test_fp8_decoder_moves_with_float32_level_perturbations);
         # the bookkeeping of all chunks above is exact
+        # floors: a fault (a wrong scale, a misrouted row) falls far below them,
+        # the measured FP8 spread (greedy >= 98.5 %, worst <= 0.21) stays above
+        assert agree >= 0.95 and top1 >= 0.95 and worst <= 0.5, (agree, top1, worst)
         pytest.xfail(f"mixed_fp8 full size: greedy {agree:.4f}, decoder API worst {worst:.3e} top-1 {top1:.4f}")

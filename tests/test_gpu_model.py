@@ -147,6 +147,9 @@ def test_mixed_fp8_decoder_on_seeded_encoder_states():
         # by more than 6e-2 when its LayerNorm outputs move by a relative 1e-7
         # (tests/test_oracle_model.py::test_fp8_decoder_moves_with_float32_level_perturbations),
         # so no float32 implementation can hold the bar against a float64 oracle.
+        # floors: a fault (a wrong scale, a misrouted row) falls far below them,
+        # the measured FP8 spread (top-1 >= 92 %, worst <= 0.15) stays above
+        assert agree / total >= 0.85 and worst <= 0.5, (agree / total, worst)
         pytest.xfail(f"mixed_fp8 decoder misses the bar: worst {worst:.3e}, top-1 {agree / total:.4f}")
 
 

@@ -67,6 +67,9 @@ def test_transcribe_batch_matches_oracle(prec, kv):
     if prec == wb.PREC_MIXED_FP8 and agree / total < 0.99:
         # known miss: FP8 logits move with float32-level differences
         # (tests/test_oracle_model.py::test_fp8_decoder_moves_with_float32_level_perturbations)
+        # floor: a fault (a wrong scale, a misrouted slot) falls far below it,
+        # the measured FP8 spread (>= 98.5 %) stays above
+        assert agree / total >= 0.95, agree / total
         pytest.xfail(f"mixed_fp8 greedy agreement {agree / total:.4f} < 0.99")
     assert agree / total >= 0.99, agree / total
 
@@ -159,5 +162,8 @@ def test_transcribe_continuous_matches_oracle(prec, kv):
     if fp8 and agree / total < 0.99:
         # known miss: FP8 logits move with float32-level differences
         # (tests/test_oracle_model.py::test_fp8_decoder_moves_with_float32_level_perturbations)
+        # floor: a fault (a wrong scale, a misrouted slot) falls far below it,
+        # the measured FP8 spread (>= 98.5 %) stays above
+        assert agree / total >= 0.95, agree / total
         pytest.xfail(f"mixed_fp8 greedy agreement {agree / total:.4f} < 0.99")
     assert agree / total >= 0.99, agree / total

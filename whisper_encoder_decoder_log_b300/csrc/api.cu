@@ -1753,7 +1753,6 @@ wb_status wb_transcribe_batch_continuous(wb_model* m, const float* audio, const 
         return slot_out(cb.sl_tok, cb.out_slot, cb.out_chunk, cb.out_len, (int)k, tokens, s);
     };
     size_t qi = 0;
-    int64_t refills = 0;
     while (true) {
         std::vector<int32_t> free_slots;
         int64_t active = 0;
@@ -1779,15 +1778,10 @@ wb_status wb_transcribe_batch_continuous(wb_model* m, const float* audio, const 
             if (wb_status st = wb_decode_prefix(stg, 4, nullptr, stream)) return done(st);
             WB_CUDA(cudaMemcpyAsync(cb.slot_of, slots.data(), k * 4, cudaMemcpyHostToDevice, s));
             WB_CUDA(cudaMemcpyAsync(cb.new_len, lens.data(), k * 4, cudaMemcpyHostToDevice, s));
-            if (wb_status st = slot_cross_copy(stg->crosskv, sl->crosskv, cb.slot_of, (int)k, p.R, p.S, Ld, cross_blk, s))
+            const bool c8 = m->desc.kv_fp8 == WB_KV_FP8_CROSS;
+            if (wb_status st = slot_cross_copy(stg->crosskv, sl->crosskv, cb.slot_of, (int)k, p.R, p.S, Ld, cross_blk, s,
+                                               c8 ? stg->cscale : nullptr, c8 ? sl->cscale : nullptr))
                 return done(st);
-            if (m->desc.kv_fp8 == WB_KV_FP8_CROSS)
-                for (int l = 0; l < Ld; ++l)
-                    for (int kv = 0; kv < 2; ++kv)
-                        for (int64_t i = 0; i < k; ++i)
-                            WB_CUDA(cudaMemcpyAsync(sl->cscale + (size_t)(2 * l + kv) * p.S + slots[i],
-                                                    stg->cscale + (size_t)(2 * l + kv) * p.R + i, 4,
-                                                    cudaMemcpyDeviceToDevice, s));
             if (wb_status st = slot_state(reinterpret_cast<const uint8_t*>(stg->cache), reinterpret_cast<uint8_t*>(sl->cache),
                                           stg->kscale, stg->vscale, sl->kscale, sl->vscale, cb.st_tok, cb.sl_tok,
                                           sl->pos_dev, sl->len_dev, cb.slot_of, cb.new_len, (int)k, (int)p.R,
@@ -1797,7 +1791,6 @@ wb_status wb_transcribe_batch_continuous(wb_model* m, const float* audio, const 
                 slot_chunk[slots[i]] = chunks[i];
                 remaining[slots[i]] = lens[i] - 5;       // steps at positions 4 .. len - 2
             }
-            ++refills;
             continue;
         }
         if (active == 0) break;
@@ -1809,7 +1802,6 @@ wb_status wb_transcribe_batch_continuous(wb_model* m, const float* audio, const 
     for (int64_t q = 0; q < p.S; ++q) all[q] = (int32_t)q;
     if (wb_status st = flush(all)) return done(st);
     if (n_slots_out) *n_slots_out = (int32_t)p.S;
-    (void)refills;
     done(WB_OK);
     return wb_sync_status(m, stream);
 }

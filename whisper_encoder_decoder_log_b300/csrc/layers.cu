@@ -601,12 +601,15 @@ __global__ void beam_init_kernel(int32_t* __restrict__ hist, float* __restrict__
 // blocks of blk16 16-byte words), copied into the blocks of their slots
 // ([layer][S] blocks).  grid (x, n, layers).
 __global__ void slot_cross_copy_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst,
-                                       const int32_t* __restrict__ slot_of, int64_t R, int64_t S, int64_t blk16) {
+                                       const int32_t* __restrict__ slot_of, int64_t R, int64_t S, int64_t blk16,
+                                       const float* __restrict__ cs_src, float* __restrict__ cs_dst) {
     griddep_wait();
     griddep_launch();
     const int64_t i = blockIdx.y, l = blockIdx.z;
     const uint4* a = src + (l * R + i) * blk16;
     uint4* b = dst + (l * S + slot_of[i]) * blk16;
+    if (cs_src && blockIdx.x == 0 && threadIdx.x < 2)     // E4M3 cross K/V: scales [layer][K|V][rows]
+        cs_dst[(2 * l + threadIdx.x) * S + slot_of[i]] = cs_src[(2 * l + threadIdx.x) * R + i];
     for (int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; k < blk16; k += (int64_t)gridDim.x * blockDim.x)
         b[k] = a[k];
 }
@@ -994,13 +997,14 @@ wb_status beam_init(int32_t* hist, float* scores, int64_t rows, int K, cudaStrea
 }
 
 wb_status slot_cross_copy(const void* src, void* dst, const int32_t* slot_of, int n, int64_t R, int64_t S, int layers,
-                          int64_t blk_bytes, cudaStream_t s) {
+                          int64_t blk_bytes, cudaStream_t s, const float* cs_src, float* cs_dst) {
     if (n <= 0 || layers <= 0) return WB_OK;
     if (blk_bytes % 16) return fail(WB_ERR_ALIGN, "slot cross copy: blocks of whole 16-byte words");
     const int64_t blk16 = blk_bytes / 16;
     const unsigned gx = (unsigned)std::max<int64_t>(1, std::min<int64_t>(64, (blk16 + 1023) / 1024));
     WB_CUDA(launch_k(slot_cross_copy_kernel, dim3(gx, (unsigned)n, (unsigned)layers), dim3(256), 0, s,
-                     reinterpret_cast<const uint4*>(src), reinterpret_cast<uint4*>(dst), slot_of, R, S, blk16));
+                     reinterpret_cast<const uint4*>(src), reinterpret_cast<uint4*>(dst), slot_of, R, S, blk16, cs_src,
+                     cs_dst));
     WB_CUDA(cudaGetLastError());
     return WB_OK;
 }

@@ -74,11 +74,12 @@ wb_status beam_best(const float* scores, const int32_t* tokens, int64_t n_chunks
 wb_status beam_init(int32_t* hist, float* scores, int64_t rows, int K, cudaStream_t s);
 // Continuous batching: move the decode state of n chunks prepared in a
 // staging decoder of R rows into their slots of an S-row decoder (cross K/V
-// blocks of blk_bytes per layer and chunk; the first P cache rows of each
-// (layer, K|V, head) block of lay rows, cache scales, token rows, position P,
-// decode length), and copy finished slots' token rows to the output.
+// blocks of blk_bytes per layer and chunk, with their [layer][K|V][rows]
+// scales when cs_src is given; the first P cache rows of each (layer, K|V,
+// head) block of lay rows, cache scales, token rows, position P, decode
+// length), and copy finished slots' token rows to the output.
 wb_status slot_cross_copy(const void* src, void* dst, const int32_t* slot_of, int n, int64_t R, int64_t S, int layers,
-                          int64_t blk_bytes, cudaStream_t s);
+                          int64_t blk_bytes, cudaStream_t s, const float* cs_src = nullptr, float* cs_dst = nullptr);
 wb_status slot_state(const uint8_t* st_cache, uint8_t* sl_cache, const float* st_ks, const float* st_vs, float* sl_ks,
                      float* sl_vs, const int32_t* st_tok, int32_t* sl_tok, int* pos, int32_t* len, const int32_t* slot_of,
                      const int32_t* new_len, int n, int R, int S, int layers, int heads, int lay, int P, cudaStream_t s);
