@@ -1365,7 +1365,8 @@ wb_status wb_shard_batch(int32_t n_req, const int64_t* req_offset, const int64_t
 struct TranscribeBufs {
     float* chunk_audio = nullptr;
     float* mel = nullptr;
-    uint8_t* enc = nullptr;
+    uint8_t* enc = nullptr;          // encoder states of one wave
+    uint8_t* enc2 = nullptr;         // the next wave's, encoded while this one decodes (several waves)
     int32_t* wave_tok = nullptr;
     int64_t* src = nullptr;
     int32_t* valid = nullptr;
@@ -1388,11 +1389,14 @@ static size_t transcribe_ws(const wb_model* m, int64_t max_wave, const std::vect
     t.chunk_audio = c.take<float>((size_t)max_wave * kChunkSamples);
     t.mel = c.take<float>((size_t)max_wave * m->desc.n_mels * kFrames);
     t.enc = c.take<uint8_t>((size_t)max_wave * kCtx * d * act);
+    if (waves.size() > 1) t.enc2 = c.take<uint8_t>((size_t)max_wave * kCtx * d * act);
     t.wave_tok = c.take<int32_t>((size_t)max_wave * kMaxPos);
-    t.src = c.take<int64_t>(max_wave);
-    t.valid = c.take<int32_t>(max_wave);
-    t.dst_row = c.take<int32_t>(max_wave);
-    t.wlen = c.take<int32_t>(max_wave);
+    // per-chunk tables of all waves, in wave order
+    const int64_t n_all = (int64_t)lens.size();
+    t.src = c.take<int64_t>(n_all);
+    t.valid = c.take<int32_t>(n_all);
+    t.dst_row = c.take<int32_t>(n_all);
+    t.wlen = c.take<int32_t>(n_all);
     t.enc_ws_bytes = carve_encoder(m, EB, nullptr, nullptr, 0, nullptr);
     t.enc_ws = c.take<uint8_t>(t.enc_ws_bytes);
     for (const auto& w : waves) {
@@ -1518,51 +1522,108 @@ static wb_status transcribe_impl(wb_model* m, const float* audio, const int64_t*
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const int d = m->d();
     const size_t act = m->fp32() ? 4 : 2;
-    for (const auto& w : waves) {
-        const int64_t nw = (int64_t)w.size();
-        std::vector<int64_t> hsrc(nw);
-        std::vector<int32_t> hvalid(nw), hdst(nw), wl(nw);
-        for (int64_t i = 0; i < nw; ++i) {
-            const int32_t c = w[i];
-            hsrc[i] = req_offset[req[c]] + idx[c] * stride;
-            hvalid[i] = valid[c];
-            hdst[i] = c;
-            wl[i] = lens[c];
+    // chunk tables of all waves, wave after wave
+    const size_t nwav = waves.size();
+    std::vector<int64_t> wave_off(nwav + 1, 0), hsrc((size_t)n);
+    std::vector<int32_t> hvalid((size_t)n), hdst((size_t)n), hlen((size_t)n);
+    for (size_t wi = 0; wi < nwav; ++wi) {
+        wave_off[wi + 1] = wave_off[wi] + (int64_t)waves[wi].size();
+        for (size_t i = 0; i < waves[wi].size(); ++i) {
+            const int32_t c = waves[wi][i];
+            const int64_t k = wave_off[wi] + (int64_t)i;
+            hsrc[k] = req_offset[req[c]] + idx[c] * stride;
+            hvalid[k] = valid[c];
+            hdst[k] = c;
+            hlen[k] = lens[c];
         }
-        WB_CUDA(cudaMemcpyAsync(tb.src, hsrc.data(), nw * 8, cudaMemcpyHostToDevice, s));
-        WB_CUDA(cudaMemcpyAsync(tb.valid, hvalid.data(), nw * 4, cudaMemcpyHostToDevice, s));
-        WB_CUDA(cudaMemcpyAsync(tb.dst_row, hdst.data(), nw * 4, cudaMemcpyHostToDevice, s));
-        WB_CUDA(cudaMemcpyAsync(tb.wlen, wl.data(), nw * 4, cudaMemcpyHostToDevice, s));
-        // pageable host sources: make sure they are consumed before the vectors go away
-        WB_CUDA(cudaStreamSynchronize(s));
-        WB_CUDA(launch_k(gather_chunks_kernel, dim3(dim3((kChunkSamples / 4 + 255) / 256, (unsigned)nw)), dim3(256), 0, s, 
-            audio, tb.src, tb.valid, tb.chunk_audio));
+    }
+    WB_CUDA(cudaMemcpyAsync(tb.src, hsrc.data(), (size_t)n * 8, cudaMemcpyHostToDevice, s));
+    WB_CUDA(cudaMemcpyAsync(tb.valid, hvalid.data(), (size_t)n * 4, cudaMemcpyHostToDevice, s));
+    WB_CUDA(cudaMemcpyAsync(tb.dst_row, hdst.data(), (size_t)n * 4, cudaMemcpyHostToDevice, s));
+    WB_CUDA(cudaMemcpyAsync(tb.wlen, hlen.data(), (size_t)n * 4, cudaMemcpyHostToDevice, s));
+    WB_CUDA(cudaStreamSynchronize(s));        // pageable sources are consumed before the vectors go away
+    // The next wave's mel and encoder run on a second, lower-priority stream
+    // while this wave decodes: the decode steps are bound by HBM (the
+    // cross-attention stream), the encoder by the tensor cores.
+    cudaStream_t es = nullptr;
+    cudaEvent_t ev_enc[2] = {nullptr, nullptr}, ev_init[2] = {nullptr, nullptr};
+    auto release = [&](wb_status st) {
+        for (int b = 0; b < 2; ++b) {
+            if (ev_enc[b]) cudaEventDestroy(ev_enc[b]);
+            if (ev_init[b]) cudaEventDestroy(ev_init[b]);
+        }
+        if (es) cudaStreamDestroy(es);
+        return st;
+    };
+    {
+        int lo = 0, hi = 0;
+        if (cudaDeviceGetStreamPriorityRange(&lo, &hi) != cudaSuccess ||
+            cudaStreamCreateWithPriority(&es, cudaStreamNonBlocking, lo) != cudaSuccess)
+            return release(fail(WB_ERR_CUDA, "wb_transcribe_batch: encoder stream"));
+        for (int b = 0; b < 2; ++b)
+            if (cudaEventCreateWithFlags(&ev_enc[b], cudaEventDisableTiming) != cudaSuccess ||
+                cudaEventCreateWithFlags(&ev_init[b], cudaEventDisableTiming) != cudaSuccess)
+                return release(fail(WB_ERR_CUDA, "wb_transcribe_batch: events"));
+    }
+    // the ordering of the caller's stream so far (the tables above) precedes the encoder stream's work
+    if (cudaEventRecord(ev_init[1], s) != cudaSuccess || cudaStreamWaitEvent(es, ev_init[1], 0) != cudaSuccess)
+        return release(fail(WB_ERR_CUDA, "wb_transcribe_batch: stream order"));
+    uint8_t* enc_buf[2] = {tb.enc, tb.enc2 ? tb.enc2 : tb.enc};
+    auto encode_wave = [&](size_t wi) -> wb_status {
+        const int64_t nw = (int64_t)waves[wi].size(), off = wave_off[wi];
+        uint8_t* enc = enc_buf[wi & 1];
+        WB_CUDA(launch_k(gather_chunks_kernel, dim3((kChunkSamples / 4 + 255) / 256, (unsigned)nw), dim3(256), 0, es,
+                         audio, tb.src + off, tb.valid + off, tb.chunk_audio));
         WB_CUDA(cudaGetLastError());
-        if (wb_status st = wb_mel(tb.chunk_audio, nw, m->desc.n_mels, tb.mel, stream)) return st;
+        if (wb_status st = wb_mel(tb.chunk_audio, nw, m->desc.n_mels, tb.mel, reinterpret_cast<wb_stream>(es)))
+            return st;
         for (int64_t i0 = 0; i0 < nw; i0 += kEncSubBatch) {
             const int64_t nb = std::min<int64_t>(kEncSubBatch, nw - i0);
-            if (wb_status st = wb_encode(m, tb.mel + i0 * m->desc.n_mels * kFrames, nb,
-                                         tb.enc + (size_t)i0 * kCtx * d * act, tb.enc_ws, tb.enc_ws_bytes, stream))
+            if (wb_status st = wb_encode(m, tb.mel + i0 * m->desc.n_mels * kFrames, nb, enc + (size_t)i0 * kCtx * d * act,
+                                         tb.enc_ws, tb.enc_ws_bytes, reinterpret_cast<wb_stream>(es)))
                 return st;
         }
-        WB_CUDA(launch_k(fill_prefix_kernel, dim3((unsigned)((nw + 255) / 256)), dim3(256), 0, s, tb.wave_tok, nw, prefix[0], prefix[1],
-                                                                        prefix[2], prefix[3]));
-        WB_CUDA(cudaGetLastError());
-        wb_decoder* dec = nullptr;
-        if (wb_status st = wb_decoder_init(m, nw, wl.data(), tb.enc, tb.wave_tok, tb.dec_ws, tb.dec_ws_bytes, stream,
-                                           &dec))
-            return st;
-        wb_status st = wb_decode_prefix(dec, 4, nullptr, stream);
-        for (int t = 4; !st && t + 1 < wl[0]; ++t) {
-            int64_t na = 0;
-            while (na < nw && wl[na] > t + 1) ++na;
-            st = wb_decode_step(dec, na, nullptr, stream);
+        WB_CUDA(cudaEventRecord(ev_enc[wi & 1], es));
+        return WB_OK;
+    };
+    auto run = [&]() -> wb_status {
+        if (wb_status st = encode_wave(0)) return st;
+        for (size_t wi = 0; wi < nwav; ++wi) {
+            const int64_t nw = (int64_t)waves[wi].size(), off = wave_off[wi];
+            const int32_t* wl = hlen.data() + off;
+            WB_CUDA(cudaStreamWaitEvent(s, ev_enc[wi & 1], 0));
+            WB_CUDA(launch_k(fill_prefix_kernel, dim3((unsigned)((nw + 255) / 256)), dim3(256), 0, s, tb.wave_tok, nw,
+                             prefix[0], prefix[1], prefix[2], prefix[3]));
+            WB_CUDA(cudaGetLastError());
+            wb_decoder* dec = nullptr;
+            if (wb_status st = wb_decoder_init(m, nw, wl, enc_buf[wi & 1], tb.wave_tok, tb.dec_ws, tb.dec_ws_bytes, stream,
+                                               &dec))
+                return st;
+            // this wave's encoder states are consumed (cross K/V computed): the
+            // buffer takes wave wi + 2
+            WB_CUDA(cudaEventRecord(ev_init[wi & 1], s));
+            if (wi + 1 < nwav) {
+                WB_CUDA(cudaStreamWaitEvent(es, ev_init[(wi + 1) & 1], 0));
+                if (wb_status st = encode_wave(wi + 1)) {
+                    wb_decoder_destroy(dec);
+                    return st;
+                }
+            }
+            wb_status st = wb_decode_prefix(dec, 4, nullptr, stream);
+            for (int t = 4; !st && t + 1 < wl[0]; ++t) {
+                int64_t na = 0;
+                while (na < nw && wl[na] > t + 1) ++na;
+                st = wb_decode_step(dec, na, nullptr, stream);
+            }
+            wb_decoder_destroy(dec);
+            if (st) return st;
+            WB_CUDA(launch_k(scatter_tokens_kernel, dim3((unsigned)nw), dim3(128), 0, s, tb.wave_tok, tb.dst_row + off,
+                             tb.wlen + off, tokens));
+            WB_CUDA(cudaGetLastError());
         }
-        wb_decoder_destroy(dec);
-        if (st) return st;
-        WB_CUDA(launch_k(scatter_tokens_kernel, dim3((unsigned)nw), dim3(128), 0, s, tb.wave_tok, tb.dst_row, tb.wlen, tokens));
-        WB_CUDA(cudaGetLastError());
-    }
+        return WB_OK;
+    };
+    if (wb_status st = release(run())) return st;
     if (n_waves_out) *n_waves_out = (int32_t)waves.size();
     return wb_sync_status(m, stream);
 }
