@@ -116,23 +116,35 @@ def make_workload(cfg: str, seed: int, world: int = 1, rank: int = 0, with_audio
         w.audio_s = 16 * 30.0
         w.kind = "encode"
         w.bound_kernel = KIND["gemm_tc"]
-    elif cfg in ("c4", "c5", "c5x"):
+    elif cfg in ("c4", "c4o", "c4b", "c5", "c5x", "c5c"):
         w = Workload()
-        w.kind = "batch"
+        w.kind = {"c4o": "overlap", "c4b": "beam", "c5c": "cont"}.get(cfg, "batch")
         w.budget = 180 * 10 ** 9
-        if cfg == "c4":
-            w.name = "large-v3-turbo transcription, 16-min recording = 32x30s chunks, prefix 4 + 224 greedy tokens"
+        w.overlap = 16000 if cfg == "c4o" else 0
+        w.beams = 4 if cfg == "c4b" else 1
+        if cfg in ("c4", "c4o", "c4b"):
+            w.name = {"c4": "large-v3-turbo transcription, 16-min recording = 32x30s chunks, prefix 4 + 224 greedy "
+                            "tokens",
+                      "c4o": "large-v3-turbo transcription of the c4 recording in overlapping 30 s windows (1 s "
+                             "shared between neighbours: 34 windows), prefix 4 + 224 greedy tokens, stitched",
+                      "c4b": "large-v3-turbo, the c4 recording's 32 chunks decoded by beam search with 4 beams, "
+                             "prefix 4 + 224 tokens"}[cfg]
             w.dims, w.precision, w.kv_fp8 = TURBO, PREC_BF16, True
             n = 32                                    # one 16-minute recording per GPU
             g_samples = np.full(world, n * CHUNK, np.int64)
             g_offsets = np.arange(world, dtype=np.int64) * n * CHUNK
-            g_len = np.full(n * world, 228, np.int32)
+            n_chunks = 1 + (n * CHUNK - CHUNK + (CHUNK - w.overlap) - 1) // (CHUNK - w.overlap)
+            g_len = np.full(n_chunks * world, 228, np.int32)
             gen = lambda r: synth.batch_audio("sine", n, seed + r).reshape(-1)  # noqa: E731
             w.bound_kernel = KIND["gemm_tc"]
         else:
             if cfg == "c5":
                 w.name = ("large-v3 mixed serving: 48 requests 2-15 min, mixed_fp8 (one E4M3 scale per chunk and "
                           "GEMM input), E4M3 KV, lengths 64-448, waves <= 180 GB")
+                w.dims, w.precision, w.kv_fp8 = LARGE_V3, PREC_MIXED_FP8, True
+            elif cfg == "c5c":
+                w.name = ("large-v3 mixed serving as c5 by continuous batching: decode slots for <= 180 GB, "
+                          "refilled as chunks finish")
                 w.dims, w.precision, w.kv_fp8 = LARGE_V3, PREC_MIXED_FP8, True
             else:
                 w.name = ("large-v3 mixed serving as c5, with E4M3 cross-attention K/V as well: 48 requests 2-15 min, "
@@ -145,6 +157,8 @@ def make_workload(cfg: str, seed: int, world: int = 1, rank: int = 0, with_audio
         w.global_chunk_len = g_len
         if world > 1:
             import whisper_encoder_decoder_log_b300 as wb
+            if w.overlap:
+                raise SystemExit("overlapping windows are measured on one GPU")
             offs, samples, c0, cn = wb.wb_shard_batch(g_offsets, g_samples, g_len, world, rank)
         else:
             offs, samples, c0, cn = g_offsets, g_samples, 0, int(g_len.size)
@@ -169,7 +183,7 @@ class GpuRunner:
         import whisper_encoder_decoder_log_b300 as wb
         self.torch, self.wb, self.w = torch, wb, w
         self.model = None
-        self.idle = w.kind == "batch" and w.chunk_count == 0     # a rank whose share is empty
+        self.idle = w.kind in ("batch", "overlap", "cont", "beam") and w.chunk_count == 0   # an empty share
         if w.precision is not None:
             desc = wb.make_desc(w.dims, w.precision, w.kv_fp8)
             W = synth.make_weights(w.dims, seed, bf16=w.precision != PREC_FP32)
@@ -179,19 +193,37 @@ class GpuRunner:
             self.model = wb.wb_model_create(desc, self.wbuf)
         dev = "cuda"
         self.h2d = self.d2h = 0
-        if w.kind == "batch":
+        if w.kind in ("batch", "overlap", "cont", "beam"):
             if self.idle:
                 return
             self.audio_host = torch.from_numpy(w.audio_flat).pin_memory()
             self.audio = self.audio_host.to(dev)
             n_chunks = w.chunk_len.size
-            self.tokens = torch.zeros(n_chunks, 448, dtype=torch.int32, device=dev)
-            self.tokens_host = torch.empty(n_chunks, 448, dtype=torch.int32).pin_memory()
+            rows = n_chunks * w.beams
+            self.tokens = torch.zeros(rows, 448, dtype=torch.int32, device=dev)
+            self.tokens_host = torch.empty(rows, 448, dtype=torch.int32).pin_memory()
             self.prefix = synth.forced_prefix(seed, w.dims.vocab)
-            nbytes = wb.wb_transcribe_workspace_size(self.model, w.req_samples, w.chunk_len, w.budget)
+            if w.kind == "cont":
+                nbytes = wb.wb_transcribe_workspace_size_continuous(self.model, w.req_samples, w.budget)
+            elif w.kind == "overlap":
+                nbytes = wb.wb_transcribe_workspace_size_overlap(self.model, w.req_samples, w.chunk_len, w.budget,
+                                                                 w.overlap)
+            elif w.kind == "batch":
+                nbytes = wb.wb_transcribe_workspace_size(self.model, w.req_samples, w.chunk_len, w.budget)
+            else:
+                # beam search through the decoder API: mel, encoder in groups of 16, K beams per chunk
+                self.chunk_audio = torch.empty(n_chunks, CHUNK, device=dev)
+                self.mel = torch.empty(n_chunks, w.dims.n_mels, 3000, device=dev)
+                self.enc = torch.empty(n_chunks, 1500, w.dims.d_model, dtype=torch.bfloat16, device=dev)
+                self.ews = torch.empty(wb.wb_encode_workspace_size(self.model, min(16, n_chunks)), dtype=torch.uint8,
+                                       device=dev)
+                self.best = torch.empty(n_chunks, 448, dtype=torch.int32, device=dev)
+                self.best_host = torch.empty(n_chunks, 448, dtype=torch.int32).pin_memory()
+                self.best_scores = torch.empty(n_chunks, device=dev)
+                nbytes = wb.wb_decoder_workspace_size_beams(self.model, w.chunk_len, w.beams)
             self.ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
             self.h2d = int(w.audio_flat.nbytes)
-            self.d2h = int(self.tokens.numel() * 4)
+            self.d2h = int((self.best if w.kind == "beam" else self.tokens).numel() * 4)
         else:
             self.audio_host = torch.from_numpy(np.ascontiguousarray(w.audio)).pin_memory()
             self.audio = self.audio_host.to(dev)
@@ -228,13 +260,23 @@ class GpuRunner:
         wb, w = self.wb, self.w
         if self.idle:
             return
-        if w.kind == "batch":
+        if w.kind in ("batch", "overlap", "cont", "beam"):
             if host_io:
                 self.audio.copy_(self.audio_host, non_blocking=True)
-            wb.wb_transcribe_batch(self.model, self.audio, w.req_offsets, w.req_samples, self.prefix, w.chunk_len,
-                                   self.tokens, w.budget, self.ws)
+            if w.kind == "batch":
+                wb.wb_transcribe_batch(self.model, self.audio, w.req_offsets, w.req_samples, self.prefix, w.chunk_len,
+                                       self.tokens, w.budget, self.ws)
+            elif w.kind == "overlap":
+                wb.wb_transcribe_batch_overlap(self.model, self.audio, w.req_offsets, w.req_samples, w.overlap,
+                                               self.prefix, w.chunk_len, self.tokens, w.budget, self.ws)
+            elif w.kind == "cont":
+                wb.wb_transcribe_batch_continuous(self.model, self.audio, w.req_offsets, w.req_samples, self.prefix,
+                                                  w.chunk_len, self.tokens, w.budget, self.ws)
+            else:
+                self._beam_step()
             if host_io:
-                self.tokens_host.copy_(self.tokens, non_blocking=True)
+                (self.best_host if w.kind == "beam" else self.tokens_host).copy_(
+                    self.best if w.kind == "beam" else self.tokens, non_blocking=True)
             return
         if host_io:
             self.audio.copy_(self.audio_host, non_blocking=True)
@@ -253,6 +295,26 @@ class GpuRunner:
         wb.wb_decoder_destroy(dec)
         if host_io:
             self.logits_host.copy_(self.logits, non_blocking=True)
+
+    def _beam_step(self):
+        """Mel and encoder of the recording's chunks, then K-beam decoding of
+        every chunk to its length (one chunk = consecutive 30 s of the
+        recording), and the best hypothesis per chunk."""
+        wb, w, torch = self.wb, self.w, self.torch
+        n = w.chunk_len.size
+        self.chunk_audio.copy_(self.audio.view(-1)[:n * CHUNK].view(n, CHUNK))
+        wb.wb_mel(self.chunk_audio, w.dims.n_mels, self.mel)
+        for i0 in range(0, n, 16):
+            i1 = min(n, i0 + 16)
+            wb.wb_encode(self.model, self.mel[i0:i1], self.enc[i0:i1], self.ews)
+        self.tokens[:, :4] = torch.from_numpy(np.tile(self.prefix, (n * w.beams, 1))).to(self.tokens.device)
+        dec = wb.wb_decoder_init_beams(self.model, w.chunk_len, w.beams, self.enc, self.tokens, self.ws)
+        wb.wb_decode_prefix(dec, 4)
+        L = int(w.chunk_len.max())
+        for t in range(4, L - 1):
+            wb.wb_decode_step_beams(dec, int((w.chunk_len > t + 1).sum()))
+        wb.wb_decoder_best_beams(dec, self.best, self.best_scores)
+        wb.wb_decoder_destroy(dec)
 
     def sync_check(self):
         self.torch.cuda.synchronize()
@@ -374,7 +436,7 @@ class OracleSample:
         self.cross8 = w.cfg == "c5x"
         if w.kind == "teacher":
             self.L = int(w.tokens.shape[1])
-        elif w.kind == "batch":
+        elif w.kind in ("batch", "overlap", "cont", "beam"):
             self.L = int(round(float(np.mean(w.global_chunk_len))))
         else:
             self.L = 0
@@ -430,10 +492,17 @@ class OracleSample:
                 per_layer = {T: max(0.0, tt[T] - head_pos * T) / self.n_dec for T in (T1, T2)}
                 slope = max(0.0, per_layer[T2] - per_layer[T1]) / (T2 - T1)
                 L = self.L
-                est += dims.dec_layers * (per_layer[T1] + slope * (L - T1)) + head_pos * L
+                K = getattr(w, "beams", 1)            # beam search: K hypotheses decoded per chunk
+                est += K * (dims.dec_layers * (per_layer[T1] + slope * (L - T1)) + head_pos * L)
                 desc += (f", {self.n_dec} of {dims.dec_layers} decoder layers teacher-forced over {T1} and {T2} "
-                         f"positions extrapolated linearly to {L} positions and scaled, output head timed alone")
+                         f"positions extrapolated linearly to {L} positions and scaled, output head timed alone"
+                         + (f", times {K} hypotheses" if K > 1 else ""))
         spent = time.perf_counter() - t0
+        if w.kind in ("batch", "overlap", "cont", "beam"):
+            # audio per chunk of the workload: partial last chunks, windows that overlap
+            per_chunk = w.audio_s / max(1, w.chunk_len.size)
+            return (per_chunk / est, spent,
+                    desc + f"; RTFx = {per_chunk:.2f} s of audio per chunk / the estimated time of one chunk")
         return 30.0 / est, spent, desc + "; RTFx = 30 s / the estimated time of one 30 s chunk"
 
 
@@ -468,7 +537,7 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2)
     ap.add_argument("--warmup", type=int, default=3)
-    ap.add_argument("--config", default="c5", choices=["c1", "c2", "c3", "c4", "c5", "c5x"])
+    ap.add_argument("--config", default="c5", choices=["c1", "c2", "c3", "c4", "c4o", "c4b", "c5", "c5x", "c5c"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
