@@ -1855,7 +1855,10 @@ wb_status wb_transcribe_batch_continuous(wb_model* m, const float* audio, const 
             continue;
         }
         if (active == 0) break;
-        if (wb_status st = replay_step(sl, p.S, s)) return done(st);
+        // per-kernel timing cannot bracket kernels inside a graph: launch directly then
+        if (wb_status st = (graphs_enabled() && !prof_any_active()) ? replay_step(sl, p.S, s)
+                                                                     : run_step(sl, p.S, nullptr, s))
+            return done(st);
         for (int64_t q = 0; q < p.S; ++q)
             if (remaining[q] > 0) --remaining[q];
     }
