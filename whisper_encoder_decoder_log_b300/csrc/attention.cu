@@ -434,10 +434,12 @@ wb_status launch_rows_nq(const void* q, int64_t q_ld, int64_t n_chunks, int rows
         reinterpret_cast<const TQ*>(q), q_ld, rows_per_chunk, (int)(n_chunks * rows_per_chunk), kv, kv_len,
         causal ? 1 : 0, q_pos0, reinterpret_cast<TO*>(out), o_ld, o_split));
     if (slot >= 0) {
-        // K and V rows attended (each read once), queries in, outputs out
+        // K and V rows attended (each read once: beams of a chunk share its
+        // cross K/V), queries in, outputs out
         const double kv_rows = causal ? (double)(q_pos0 + rows_per_chunk) : (double)kv_len;
-        const double bytes = (double)n_chunks * heads *
-                             (2.0 * kv_rows * 64.0 * sizeof(TKV) + (double)rows_per_chunk * 64.0 * (sizeof(TQ) + sizeof(TO)));
+        const double kv_sets = (double)n_chunks / (causal ? 1 : std::max(1, kv.beam_div));
+        const double bytes = (double)heads * (kv_sets * 2.0 * kv_rows * 64.0 * sizeof(TKV) +
+                                              (double)n_chunks * rows_per_chunk * 64.0 * (sizeof(TQ) + sizeof(TO)));
         prof_end(slot, s, bytes);
     }
     WB_CUDA(cudaGetLastError());
@@ -459,7 +461,8 @@ wb_status launch_rows(const void* q, int64_t q_ld, int64_t n_chunks, int rows_pe
         WB_CUDA(launch_k(self_attn_step_kernel<__nv_bfloat16, true>, grid, dim3(32 * kStepHeads), 0, s,
                          reinterpret_cast<const float*>(q), q_ld, heads, kv, q_pos0,
                          reinterpret_cast<__nv_bfloat16*>(out), o_ld, o_split));
-        prof_end(slot, s, (double)n_chunks * heads * (2.0 * kCtx * 64.0 + 64.0 * (4 + 2)));
+        prof_end(slot, s, (double)heads * ((double)n_chunks / std::max(1, kv.beam_div) * 2.0 * kCtx * 64.0 +
+                                           (double)n_chunks * 64.0 * (4 + 2)));
         WB_CUDA(cudaGetLastError());
         return WB_OK;
     }
