@@ -431,9 +431,9 @@ class OracleSample:
                                    self.n_dec, dims.vocab)
         self.W = synth.make_weights(dims, seed, bf16=w.precision != PREC_FP32, enc_layers=range(self.n_enc),
                                     dec_layers=range(self.n_dec))
-        self.fp8 = w.cfg in ("c5", "c5x")
+        self.fp8 = w.precision == PREC_MIXED_FP8
         self.act16 = w.precision != PREC_FP32
-        self.cross8 = w.cfg == "c5x"
+        self.cross8 = w.kv_fp8 == KV_FP8_CROSS
         if w.kind == "teacher":
             self.L = int(w.tokens.shape[1])
         elif w.kind in ("batch", "overlap", "cont", "beam"):

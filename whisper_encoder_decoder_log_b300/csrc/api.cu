@@ -1855,10 +1855,20 @@ wb_status wb_transcribe_batch_continuous(wb_model* m, const float* audio, const 
             continue;
         }
         if (active == 0) break;
-        // per-kernel timing cannot bracket kernels inside a graph: launch directly then
-        if (wb_status st = (graphs_enabled() && !prof_any_active()) ? replay_step(sl, p.S, s)
-                                                                     : run_step(sl, p.S, nullptr, s))
-            return done(st);
+        if (graphs_enabled() && !prof_any_active()) {
+            if (wb_status st = replay_step(sl, p.S, s)) return done(st);
+        } else {
+            // per-kernel timing cannot bracket kernels inside a graph: launch
+            // directly, with the attention work of the active slots only (a
+            // slot at position pos attends pos earlier cache rows)
+            double cached = 0;
+            for (int64_t q = 0; q < p.S; ++q)
+                if (remaining[q] > 0) cached += chunk_len[slot_chunk[q]] - 1 - remaining[q];
+            prof_set_rows((double)active / (double)p.S, cached);
+            const wb_status st = run_step(sl, p.S, nullptr, s);
+            prof_set_rows(1.0, -1.0);
+            if (st) return done(st);
+        }
         for (int64_t q = 0; q < p.S; ++q)
             if (remaining[q] > 0) --remaining[q];
     }

@@ -440,7 +440,7 @@ wb_status launch_rows_nq(const void* q, int64_t q_ld, int64_t n_chunks, int rows
         const double kv_sets = (double)n_chunks / (causal ? 1 : std::max(1, kv.beam_div));
         const double bytes = (double)heads * (kv_sets * 2.0 * kv_rows * 64.0 * sizeof(TKV) +
                                               (double)n_chunks * rows_per_chunk * 64.0 * (sizeof(TQ) + sizeof(TO)));
-        prof_end(slot, s, bytes);
+        prof_end(slot, s, bytes * prof_row_share());
     }
     WB_CUDA(cudaGetLastError());
     return WB_OK;
@@ -461,8 +461,9 @@ wb_status launch_rows(const void* q, int64_t q_ld, int64_t n_chunks, int rows_pe
         WB_CUDA(launch_k(self_attn_step_kernel<__nv_bfloat16, true>, grid, dim3(32 * kStepHeads), 0, s,
                          reinterpret_cast<const float*>(q), q_ld, heads, kv, q_pos0,
                          reinterpret_cast<__nv_bfloat16*>(out), o_ld, o_split));
-        prof_end(slot, s, (double)heads * ((double)n_chunks / std::max(1, kv.beam_div) * 2.0 * kCtx * 64.0 +
-                                           (double)n_chunks * 64.0 * (4 + 2)));
+        prof_end(slot, s, prof_row_share() * (double)heads *
+                              ((double)n_chunks / std::max(1, kv.beam_div) * 2.0 * kCtx * 64.0 +
+                               (double)n_chunks * 64.0 * (4 + 2)));
         WB_CUDA(cudaGetLastError());
         return WB_OK;
     }
@@ -486,7 +487,9 @@ wb_status attn_self_step_e4m3(const float* qkv, int64_t q_ld, int64_t n_chunks, 
     const int slot = prof_begin(WB_KERNEL_SELF_ATTN, s);
     WB_CUDA(launch_k(self_attn_step_kernel<__nv_bfloat16, false>, grid, dim3(32 * kStepHeads), 0, s, qkv, q_ld, heads,
                      kv, q_pos, reinterpret_cast<__nv_bfloat16*>(out), o_ld, o_split));
-    prof_end(slot, s, (double)n_chunks * heads * (2.0 * q_pos * 64.0 + 2.0 * 64.0 * (4 + 1) + 64.0 * (4 + 2)));
+    const double cached = prof_cached_rows() >= 0 ? prof_cached_rows() : (double)n_chunks * q_pos;
+    prof_end(slot, s, (double)heads * (2.0 * cached * 64.0 +
+                                       prof_row_share() * (double)n_chunks * (2.0 * 64.0 * (4 + 1) + 64.0 * (4 + 2))));
     WB_CUDA(cudaGetLastError());
     return WB_OK;
 }

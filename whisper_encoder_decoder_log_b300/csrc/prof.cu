@@ -44,6 +44,17 @@ bool pdl_enabled() {
 bool prof_active(int kind) { return g_prof.kind != 0 && (g_prof.kind == kind || g_prof.kind == -1); }
 bool prof_any_active() { return g_prof.kind != 0; }
 
+namespace {
+thread_local double t_row_share = 1.0;
+thread_local double t_cached_rows = -1.0;
+}
+void prof_set_rows(double share, double cached_rows) {
+    t_row_share = share;
+    t_cached_rows = cached_rows;
+}
+double prof_row_share() { return t_row_share; }
+double prof_cached_rows() { return t_cached_rows; }
+
 int prof_begin(int kind, cudaStream_t s) {
     if (!prof_active(kind)) return -1;
     std::lock_guard<std::mutex> lk(g_prof.mu);

@@ -15,6 +15,13 @@ bool prof_any_active();
 int prof_begin(int kind, cudaStream_t s);
 // Closes the slot; `units` is the launch's algorithmic bytes or flops.
 void prof_end(int slot, cudaStream_t s, double units);
+// The attention work of a continuous-batching decode step: the share of its
+// rows that hold an active chunk (the others read nothing) and the cache rows
+// those attend, summed over the rows (each row has its own position); set
+// by the caller around such a step, (1, -1: one position for all) otherwise.
+void prof_set_rows(double share, double cached_rows);
+double prof_row_share();
+double prof_cached_rows();
 // Counts kernel launches (wb_launch_count).
 void count_launch(int n = 1);
 
