@@ -39,3 +39,28 @@ def test_reference_arm_finishes_the_serving_workload_at_driver_step_counts():
     d = json.loads([l for l in out.stdout.splitlines() if l.startswith("{")][0])
     assert d["impl"] == "reference" and d["steps"] == 20 and d["warmup"] == 5 and d["value"] > 0
     assert "extrapolated" in d["cpu_baseline"]["sample"]
+
+
+def test_row_workloads_match_the_oracle_tables():
+    """The continuous (c5c), overlapping-window (c4o) and beam (c4b) bench
+    workloads are the c5 / c4 inputs: the same requests, and for c4o the
+    oracle's chunk table with 1 s of overlap."""
+    import importlib.util
+
+    import numpy as np
+
+    from oracle import plan as oplan
+    spec = importlib.util.spec_from_file_location("bench_mod", os.path.join(ROOT, "bench.py"))
+    bench = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(bench)
+    c5 = bench.make_workload("c5", 0, with_audio=False)
+    c5c = bench.make_workload("c5c", 0, with_audio=False)
+    assert np.array_equal(c5.req_samples, c5c.req_samples) and np.array_equal(c5.chunk_len, c5c.chunk_len)
+    assert c5c.kind == "cont" and c5c.budget == c5.budget
+    c4 = bench.make_workload("c4", 0, with_audio=False)
+    c4o = bench.make_workload("c4o", 0, with_audio=False)
+    req, idx, valid = oplan.chunk_table(c4o.req_samples, c4o.overlap)
+    assert c4o.overlap == 16000 and c4o.chunk_len.size == req.size == 34
+    assert np.array_equal(c4.req_samples, c4o.req_samples) and c4o.audio_s == c4.audio_s
+    c4b = bench.make_workload("c4b", 0, with_audio=False)
+    assert c4b.beams == 4 and np.array_equal(c4b.chunk_len, c4.chunk_len)
