@@ -662,7 +662,8 @@ def main():
                             / (128 * 20 * (2 * 1500 * 64 * 2 + 64 * 4 + 64 * 2)),
         KIND["mel"]: (126.83e6 + 62.09e6) / (64 * (480000 * 4 + 128 * 3000 * 4)),
     }
-    if w.kv_fp8 == KV_FP8_CROSS:      # the E4M3 cross-attention has no capture of its own
+    if w.kv_fp8 == KV_FP8_CROSS or getattr(w, "beams", 1) > 1:
+        # no capture of their own: the E4M3 cross-attention; beams re-reading their chunk's K/V from L2
         traffic_ratio.pop(KIND["cross_attn"])
     roof["traffic"] = units_launch * traffic_ratio[dom] if (dom in traffic_ratio and roof["bound"] == "hbm") else None
     roof["traffic_unit"] = "DRAM bytes per launch"
