@@ -299,6 +299,10 @@ WB_API wb_status wb_decoder_destroy(wb_decoder* dec);
  *   workspace   [dev] scratch of workspace_bytes; wb_transcribe_workspace_size
  *               tells how much a given batch needs
  *   n_waves_out [host] optional: number of waves used
+ * With several waves, the next wave's mel and encoder run on a stream of the
+ * library's own (lower priority, ordered after the caller's stream's earlier
+ * work) while the current wave decodes; the encoder states are
+ * double-buffered in the workspace.
  * Synchronises the stream before returning (it reads nothing back per step,
  * but checks the device error word at the end).
  */
