@@ -167,3 +167,36 @@ def test_transcribe_continuous_matches_oracle(prec, kv):
         assert agree / total >= 0.95, agree / total
         pytest.xfail(f"mixed_fp8 greedy agreement {agree / total:.4f} < 0.99")
     assert agree / total >= 0.99, agree / total
+
+
+def test_transcribe_three_waves_reuse_encoder_buffers():
+    """Three waves: the third wave's encoder states go to the buffer the first
+    wave's decoder init has consumed, while the second wave decodes.  Every
+    chunk's greedy tokens agree >= 99 % with the oracle."""
+    dims = ModelDims("turbo-2enc", 128, 1280, 20, 5120, 2, 4, TURBO.vocab)
+    m = GpuModel(dims, wb.PREC_BF16, wb.KV_FP8_SELF, seed=15)
+    audio, offs, samples = _requests([50.0, 70.5, 12.0], seed=110)
+    req, idx, valid = oplan.chunk_table(samples)
+    n = req.size
+    lens = np.array([12, 20, 9, 30, 16, 7], np.int32)
+    prefix = forced_prefix(9, dims.vocab)
+    budget = 2 * oplan.chunk_state_bytes(dims.d_model, dims.dec_layers, 30)
+    waves = oplan.plan_waves(lens, dims.d_model, dims.dec_layers, budget)
+    assert len(waves) >= 3
+    ws = torch.empty(wb.wb_transcribe_workspace_size(m.h, samples, lens, budget), dtype=torch.uint8, device="cuda")
+    tokens = torch.full((n, 448), -7, dtype=torch.int32, device="cuda")
+    nw = wb.wb_transcribe_batch(m.h, torch.from_numpy(audio).cuda(), offs, samples, prefix, lens, tokens, budget, ws)
+    assert nw == len(waves)
+    tok = tokens.cpu().numpy()
+    chunks, _, _, _ = omel.split_into_chunks(audio, offs, samples)
+    agree, total = 0, 0
+    for c in range(n):
+        L = int(lens[c])
+        assert np.array_equal(tok[c, :4], prefix) and (tok[c, L:] == -7).all()
+        enc = omodel.encode(omel.log_mel(chunks[c], 128), m.W, dims, act16=True)
+        ref, _ = omodel.decode_teacher_forced(tok[c, :L - 1], enc, m.W, dims, kv_fp8=True, act16=True)
+        agree += int((omodel.greedy(ref[3:L - 1]) == tok[c, 4:L]).sum())
+        total += L - 4
+    print(f"{len(waves)} waves: greedy agreement {agree / total:.4f}")
+    m.close()
+    assert agree / total >= 0.99
