@@ -171,12 +171,13 @@ def test_transcribe_continuous_matches_oracle(prec, kv):
 
 def test_transcribe_three_waves_reuse_encoder_buffers():
     """Three waves: the third wave's encoder states go to the buffer the first
-    wave's decoder init has consumed, while the second wave decodes.  The
-    tokens equal those of the same batch in one wave (a chunk's result does not
-    depend on its wave), and against the oracle every position whose greedy
-    choice is unique within the 2e-2 logit bound agrees, while at the others
-    the GPU's token is one of the tied ones (its oracle logit within 2e-2 of
-    the maximum)."""
+    wave's decoder init has consumed, while the second wave decodes.  The same
+    batch also runs as one wave.  For both layouts, against the oracle, every
+    position whose greedy choice is unique within the 2e-2 logit bound agrees,
+    and at the others the GPU's token is one of the tied ones (its oracle logit
+    within 2e-2 of the maximum).  The two layouts need not give identical
+    tokens: split-K sums are added atomically in any order, and a last-bit
+    change can move an E4M3 cache code."""
     dims = ModelDims("turbo-2enc", 128, 1280, 20, 5120, 2, 4, TURBO.vocab)
     m = GpuModel(dims, wb.PREC_BF16, wb.KV_FP8_SELF, seed=15)
     audio, offs, samples = _requests([50.0, 70.5, 12.0], seed=110)
@@ -196,25 +197,25 @@ def test_transcribe_three_waves_reuse_encoder_buffers():
         rows[len(waves)] = tokens.cpu().numpy()
         del ws
     assert sorted(rows) == [1, 3]
-    tok = rows[3]
-    assert np.array_equal(tok, rows[1])                   # the wave layout does not change any token
     chunks, _, _, _ = omel.split_into_chunks(audio, offs, samples)
-    unique_agree, unique_total, tied = 0, 0, 0
-    for c in range(n):
-        L = int(lens[c])
-        assert np.array_equal(tok[c, :4], prefix) and (tok[c, L:] == -7).all()
-        enc = omodel.encode(omel.log_mel(chunks[c], 128), m.W, dims, act16=True)
-        ref, _ = omodel.decode_teacher_forced(tok[c, :L - 1], enc, m.W, dims, kv_fp8=True, act16=True)
-        for j in range(3, L - 1):
-            r = ref[j]
-            top2 = np.sort(r)[-2:]
-            gpu_tok = int(tok[c, j + 1])
-            if top2[1] - top2[0] >= 2e-2:
-                unique_total += 1
-                unique_agree += int(gpu_tok == int(np.argmax(r)))
-            else:
-                tied += 1
-                assert r.max() - r[gpu_tok] <= 2e-2, (c, j)
-    print(f"three waves = one wave; unique positions {unique_agree}/{unique_total}, near-ties {tied}")
+    encs = [omodel.encode(omel.log_mel(chunks[c], 128), m.W, dims, act16=True) for c in range(n)]
+    for n_waves, tok in sorted(rows.items()):
+        unique_agree, unique_total, tied = 0, 0, 0
+        for c in range(n):
+            L = int(lens[c])
+            assert np.array_equal(tok[c, :4], prefix) and (tok[c, L:] == -7).all()
+            ref, _ = omodel.decode_teacher_forced(tok[c, :L - 1], encs[c], m.W, dims, kv_fp8=True, act16=True)
+            for j in range(3, L - 1):
+                r = ref[j]
+                top2 = np.sort(r)[-2:]
+                gpu_tok = int(tok[c, j + 1])
+                if top2[1] - top2[0] >= 2e-2:
+                    unique_total += 1
+                    unique_agree += int(gpu_tok == int(np.argmax(r)))
+                else:
+                    tied += 1
+                    assert r.max() - r[gpu_tok] <= 2e-2, (n_waves, c, j)
+        print(f"{n_waves} wave(s): unique positions {unique_agree}/{unique_total}, near-ties {tied}")
+        assert unique_agree / unique_total >= 0.99, (n_waves, unique_agree, unique_total)
+    print(f"tokens that differ between the layouts: {int((rows[1] != rows[3]).sum())}")
     m.close()
-    assert unique_agree / unique_total >= 0.99
