@@ -70,3 +70,22 @@ class GpuModel:
 
 def to_np(t):
     return t.float().cpu().numpy().astype(np.float64)
+
+
+def greedy_choice_check(ref, chosen, tol=2e-2):
+    """Greedy decisions against the oracle's logits (several correct results:
+    compare what is unique, check that the rest is valid).
+
+    ref [n, V] oracle logits, chosen [n] the GPU's token ids.  A position
+    whose oracle top-2 gap is at least tol (the logit bound) has one valid
+    greedy token, the oracle's argmax; at a near-tie any token within tol of
+    the oracle's maximum is a valid choice.  Returns (agreeing unique
+    positions, unique positions, near-ties, near-ties outside tol)."""
+    ref = np.asarray(ref, np.float64)
+    chosen = np.asarray(chosen).astype(np.int64)
+    top2 = np.sort(ref, axis=1)[:, -2:]
+    unique = (top2[:, 1] - top2[:, 0]) >= tol
+    agree = int((chosen[unique] == np.argmax(ref[unique], axis=1)).sum())
+    picked = ref[np.arange(ref.shape[0]), chosen]
+    bad = int(((ref.max(axis=1) - picked) > tol)[~unique].sum())
+    return agree, int(unique.sum()), int((~unique).sum()), bad

@@ -12,7 +12,7 @@ import whisper_encoder_decoder_log_b300 as wb
 from oracle import mel as omel
 from oracle import model as omodel
 from synth import TINY, TURBO, ModelDims, batch_audio, forced_prefix, make_weights, random_tokens, round_to_bf16
-from tests.gpu_util import GpuModel, to_np
+from tests.gpu_util import GpuModel, greedy_choice_check, to_np
 
 pytestmark = pytest.mark.gpu
 
@@ -97,17 +97,20 @@ def test_turbo_decoder_fp8_kv_greedy_steps(kv):
             r = ref[3 + j]
             worst = max(worst, np.abs(g - r).max())
             se += float(np.mean((g - r) ** 2))
-            agree += int(np.argmax(g) == np.argmax(r))
             if cross:
                 se_ref += float(np.mean((r - exact[3 + j]) ** 2))
                 agree_ref += int(np.argmax(r) == np.argmax(exact[3 + j]))
-            total += 1
+        # unique greedy choices agree with the oracle; near-ties within the bound
+        a, u, _, b = greedy_choice_check(ref[3:3 + len(got)], np.argmax(np.stack(got), axis=1), tol=6e-2)
+        assert b == 0, c
+        agree, total = agree + a, total + u
         # bookkeeping: the generated tokens are the greedy choice of the GPU's own logits
         for j, g in enumerate(got):
             assert tok[c, 4 + j] == np.argmax(g)
         assert (tok[c, L:] == 0).all()
-    print(f"turbo decoder kv {kv}: worst {worst:.3e}, rms {np.sqrt(se / total):.3e}, top-1 {agree / total:.4f}"
-          + (f"; E4M3 cross K/V effect rms {np.sqrt(se_ref / total):.3e}" if cross else ""))
+    n_pos = sum(int(x) - 5 for x in lens)
+    print(f"turbo decoder kv {kv}: worst {worst:.3e}, rms {np.sqrt(se / n_pos):.3e}, top-1 {agree / total:.4f} on "
+          f"{total} unique positions" + (f"; E4M3 cross K/V effect rms {np.sqrt(se_ref / n_pos):.3e}" if cross else ""))
     assert worst <= 6e-2, worst
     assert agree / total >= 0.99, agree / total
     m.close()
@@ -171,13 +174,14 @@ def test_decoder_wide_logits_on_cta_pairs():
     for c in (0, 151, 299):
         ref, _ = omodel.decode_teacher_forced(tok[c, :6], enc_np[c].astype(np.float64), m.W, dims, kv_fp8=True,
                                               act16=True)
-        for j, got in enumerate((outs[1][c], outs[2][c])):
-            r = ref[4 + j]
-            worst = max(worst, float(np.abs(got - r).max()))
-            agree += int(np.argmax(got) == np.argmax(r))
-            total += 1
-            assert tok[c, 5 + j] == np.argmax(got)
-    print(f"wide logits over {B} rows: worst {worst:.3e}, top-1 {agree}/{total}")
+        got = np.stack([outs[1][c], outs[2][c]])
+        for j in range(2):
+            worst = max(worst, float(np.abs(got[j] - ref[4 + j]).max()))
+            assert tok[c, 5 + j] == np.argmax(got[j])
+        a, u, _, b = greedy_choice_check(ref[4:6], np.argmax(got, axis=1), tol=6e-2)
+        assert b == 0, c
+        agree, total = agree + a, total + u
+    print(f"wide logits over {B} rows: worst {worst:.3e}, top-1 {agree}/{total} unique positions")
     m.close()
     assert worst <= 6e-2, worst
     assert agree == total

@@ -11,7 +11,7 @@ from oracle import mel as omel
 from oracle import model as omodel
 from oracle import plan as oplan
 from synth import TURBO, ModelDims, forced_prefix, sine_chunk_audio
-from tests.gpu_util import GpuModel
+from tests.gpu_util import GpuModel, greedy_choice_check
 
 pytestmark = pytest.mark.gpu
 
@@ -49,7 +49,7 @@ def test_transcribe_batch_matches_oracle(prec, kv):
     chunks, oreq, oidx, ovalid = omel.split_into_chunks(audio, offs, samples)
     assert np.array_equal(oreq, req) and np.array_equal(ovalid, valid)
     fp8 = prec == wb.PREC_MIXED_FP8
-    agree, total = 0, 0
+    agree, total, bad = 0, 0, 0
     for c in range(n):
         L = int(lens[c])
         assert np.array_equal(tok[c, :4], prefix)
@@ -58,20 +58,21 @@ def test_transcribe_batch_matches_oracle(prec, kv):
         enc = omodel.encode(omel.log_mel(chunks[c], 128), m.W, dims, fp8=fp8, act16=True)
         ref, _ = omodel.decode_teacher_forced(tok[c, :L - 1], enc, m.W, dims, kv_fp8=True, fp8=fp8, cross_fp8=cross,
                                               act16=True)
-        pred = omodel.greedy(ref[3:L - 1])
-        agree += int((pred == tok[c, 4:L]).sum())
-        total += L - 4
-    # at least 99 % of greedy tokens agree with the oracle's argmax
-    print(f"precision {prec}, kv {kv}: greedy agreement {agree / total:.4f}")
+        a, u, _, b = greedy_choice_check(ref[3:L - 1], tok[c, 4:L])
+        agree, total, bad = agree + a, total + u, bad + b
+    # at least 99 % of the unique greedy choices agree with the oracle's argmax;
+    # near-ties (top-2 gap below the 2e-2 logit bound) take a token within it
+    print(f"precision {prec}, kv {kv}: greedy agreement {agree / total:.4f} on {total} unique positions, "
+          f"{bad} near-ties outside the bound")
     m.close()
-    if prec == wb.PREC_MIXED_FP8 and agree / total < 0.99:
+    if prec == wb.PREC_MIXED_FP8 and (agree / total < 0.99 or bad):
         # known miss: FP8 logits move with float32-level differences
         # (tests/test_oracle_model.py::test_fp8_decoder_moves_with_float32_level_perturbations)
         # floor: a fault (a wrong scale, a misrouted slot) falls far below it,
         # the measured FP8 spread (>= 98.5 %) stays above
         assert agree / total >= 0.95, agree / total
         pytest.xfail(f"mixed_fp8 greedy agreement {agree / total:.4f} < 0.99")
-    assert agree / total >= 0.99, agree / total
+    assert agree / total >= 0.99 and bad == 0, (agree / total, bad)
 
 
 def test_transcribe_overlapping_windows_and_stitch():
@@ -97,16 +98,16 @@ def test_transcribe_overlapping_windows_and_stitch():
     tok = tokens.cpu().numpy()
     chunks, oreq, oidx, ovalid = omel.split_into_chunks(audio, offs, samples, overlap=overlap)
     assert np.array_equal(oreq, req) and np.array_equal(ovalid, valid)
-    agree, total = 0, 0
+    agree, total, bad = 0, 0, 0
     for c in range(n):
         L = int(lens[c])
         assert np.array_equal(tok[c, :4], prefix) and (tok[c, L:] == -7).all()
         enc = omodel.encode(omel.log_mel(chunks[c], 128), m.W, dims, act16=True)
         ref, _ = omodel.decode_teacher_forced(tok[c, :L - 1], enc, m.W, dims, kv_fp8=True, act16=True)
-        agree += int((omodel.greedy(ref[3:L - 1]) == tok[c, 4:L]).sum())
-        total += L - 4
-    print(f"overlapping windows: greedy agreement {agree / total:.4f}")
-    assert agree / total >= 0.99
+        a, u, _, b = greedy_choice_check(ref[3:L - 1], tok[c, 4:L])
+        agree, total, bad = agree + a, total + u, bad + b
+    print(f"overlapping windows: greedy agreement {agree / total:.4f} on {total} unique positions")
+    assert agree / total >= 0.99 and bad == 0, (agree / total, bad)
     texts = wb.wb_stitch_tokens(samples, overlap, tok, lens, 4)
     for r in range(samples.size):
         rows = [tok[c, 4:lens[c]] for c in range(n) if req[c] == r]
@@ -146,7 +147,7 @@ def test_transcribe_continuous_matches_oracle(prec, kv):
     tok = tokens.cpu().numpy()
     chunks, _, _, _ = omel.split_into_chunks(audio, offs, samples)
     fp8 = prec == wb.PREC_MIXED_FP8
-    agree, total = 0, 0
+    agree, total, bad = 0, 0, 0
     for c in range(n):
         L = int(lens[c])
         assert np.array_equal(tok[c, :4], prefix)
@@ -155,18 +156,19 @@ def test_transcribe_continuous_matches_oracle(prec, kv):
         enc = omodel.encode(omel.log_mel(chunks[c], 128), m.W, dims, fp8=fp8, act16=True)
         ref, _ = omodel.decode_teacher_forced(tok[c, :L - 1], enc, m.W, dims, kv_fp8=True, fp8=fp8, cross_fp8=cross,
                                               act16=True)
-        agree += int((omodel.greedy(ref[3:L - 1]) == tok[c, 4:L]).sum())
-        total += L - 4
-    print(f"continuous batching (precision {prec}, kv {kv}): greedy agreement {agree / total:.4f} over {total}")
+        a, u, _, b = greedy_choice_check(ref[3:L - 1], tok[c, 4:L])
+        agree, total, bad = agree + a, total + u, bad + b
+    print(f"continuous batching (precision {prec}, kv {kv}): greedy agreement {agree / total:.4f} on {total} unique "
+          f"positions, {bad} near-ties outside the bound")
     m.close()
-    if fp8 and agree / total < 0.99:
+    if fp8 and (agree / total < 0.99 or bad):
         # known miss: FP8 logits move with float32-level differences
         # (tests/test_oracle_model.py::test_fp8_decoder_moves_with_float32_level_perturbations)
         # floor: a fault (a wrong scale, a misrouted slot) falls far below it,
         # the measured FP8 spread (>= 98.5 %) stays above
         assert agree / total >= 0.95, agree / total
         pytest.xfail(f"mixed_fp8 greedy agreement {agree / total:.4f} < 0.99")
-    assert agree / total >= 0.99, agree / total
+    assert agree / total >= 0.99 and bad == 0, (agree / total, bad)
 
 
 def test_transcribe_three_waves_reuse_encoder_buffers():
@@ -205,16 +207,9 @@ def test_transcribe_three_waves_reuse_encoder_buffers():
             L = int(lens[c])
             assert np.array_equal(tok[c, :4], prefix) and (tok[c, L:] == -7).all()
             ref, _ = omodel.decode_teacher_forced(tok[c, :L - 1], encs[c], m.W, dims, kv_fp8=True, act16=True)
-            for j in range(3, L - 1):
-                r = ref[j]
-                top2 = np.sort(r)[-2:]
-                gpu_tok = int(tok[c, j + 1])
-                if top2[1] - top2[0] >= 2e-2:
-                    unique_total += 1
-                    unique_agree += int(gpu_tok == int(np.argmax(r)))
-                else:
-                    tied += 1
-                    assert r.max() - r[gpu_tok] <= 2e-2, (n_waves, c, j)
+            a, u, t, b = greedy_choice_check(ref[3:L - 1], tok[c, 4:L])
+            assert b == 0, (n_waves, c)
+            unique_agree, unique_total, tied = unique_agree + a, unique_total + u, tied + t
         print(f"{n_waves} wave(s): unique positions {unique_agree}/{unique_total}, near-ties {tied}")
         assert unique_agree / unique_total >= 0.99, (n_waves, unique_agree, unique_total)
     print(f"tokens that differ between the layouts: {int((rows[1] != rows[3]).sum())}")
