@@ -141,6 +141,32 @@ def _host_arr(a, dtype):
     return a, a.ctypes.data
 
 
+def _room(t, n: int, what: str):
+    """Reject a buffer smaller than the n elements the call will touch: the C
+    ABI takes every size from the other arguments, so a short buffer would be
+    read or written past its end on the device."""
+    if t is not None and t.numel() < n:
+        raise ValueError(f"{what} holds {t.numel()} elements; the call touches {n}")
+
+
+def _batch_args(audio, ro, rs, pf, cl, tokens, overlap: int = 0, rows_per_chunk: int = 1) -> int:
+    """Host-side size checks shared by the batch entry points: one offset per
+    request, one decode length per chunk, a 4-token prefix, audio covering
+    every request and a token row per chunk.  Returns the chunk count."""
+    if ro.size != rs.size:
+        raise ValueError(f"{ro.size} request offsets for {rs.size} requests")
+    n_chunks = wb_chunk_count(rs, overlap)
+    if cl.size != n_chunks:
+        raise ValueError(f"chunk_len has {cl.size} entries; the requests make {n_chunks} chunks")
+    if pf.size != 4:
+        raise ValueError(f"the forced prefix has {pf.size} ids, not 4")
+    if rs.size and (ro < 0).any():
+        raise ValueError("negative request offset")
+    _room(audio, int((ro + rs).max()) if rs.size else 0, "audio")
+    _room(tokens, n_chunks * rows_per_chunk * MAX_POS, "tokens")
+    return n_chunks
+
+
 # ----------------------------------------------------------------- thin wrappers
 
 def wb_version() -> int:
@@ -150,6 +176,8 @@ def wb_version() -> int:
 def wb_mel(audio, n_mels: int, mel, stream=None):
     _need(audio, "float32", "audio")
     _need(mel, "float32", "mel")
+    _room(audio, audio.shape[0] * CHUNK_SAMPLES, "audio")
+    _room(mel, audio.shape[0] * n_mels * N_FRAMES, "mel")
     _check(lib().wb_mel(_p(audio), audio.shape[0], n_mels, _p(mel), _stream(stream)))
 
 
@@ -193,6 +221,7 @@ def wb_decoder_workspace_size(model: int, chunk_len) -> int:
 def wb_decoder_init(model: int, chunk_len, enc, tokens, workspace, stream=None) -> int:
     arr, ptr = _host_arr(chunk_len, np.int32)
     _need(tokens, "int32", "tokens")
+    _room(tokens, arr.size * MAX_POS, "tokens")
     h = _VP(0)
     _check(lib().wb_decoder_init(model, arr.size, ptr, _p(enc), _p(tokens), _p(workspace),
                                  workspace.numel() * workspace.element_size(), _stream(stream), ctypes.byref(h)))
@@ -217,6 +246,7 @@ def wb_decoder_workspace_size_beams(model: int, chunk_len, beams: int) -> int:
 def wb_decoder_init_beams(model: int, chunk_len, beams: int, enc, tokens, workspace, stream=None) -> int:
     arr, ptr = _host_arr(chunk_len, np.int32)
     _need(tokens, "int32", "tokens")
+    _room(tokens, arr.size * max(int(beams), 1) * MAX_POS, "tokens")
     h = _VP(0)
     _check(lib().wb_decoder_init_beams(model, arr.size, ptr, beams, _p(enc), _p(tokens), _p(workspace),
                                        workspace.numel() * workspace.element_size(), _stream(stream), ctypes.byref(h)))
@@ -262,6 +292,7 @@ def wb_transcribe_batch(model: int, audio, req_offset, req_samples, prefix, chun
     cl, clp = _host_arr(chunk_len, np.int32)
     _need(audio, "float32", "audio")
     _need(tokens, "int32", "tokens")
+    _batch_args(audio, ro, rs, pf, cl, tokens)
     nw = _I32(0)
     _check(lib().wb_transcribe_batch(model, _p(audio), rop, rsp, rs.size, pfp, clp, _p(tokens), budget,
                                      _p(workspace), workspace.numel() * workspace.element_size(),
@@ -283,6 +314,7 @@ def wb_transcribe_batch_continuous(model: int, audio, req_offset, req_samples, p
     cl, clp = _host_arr(chunk_len, np.int32)
     _need(audio, "float32", "audio")
     _need(tokens, "int32", "tokens")
+    _batch_args(audio, ro, rs, pf, cl, tokens)
     ns = _I32(0)
     _check(lib().wb_transcribe_batch_continuous(model, _p(audio), rop, rsp, rs.size, pfp, clp, _p(tokens), budget,
                                                 _p(workspace), workspace.numel() * workspace.element_size(),
@@ -312,6 +344,7 @@ def wb_transcribe_batch_overlap(model: int, audio, req_offset, req_samples, over
     cl, clp = _host_arr(chunk_len, np.int32)
     _need(audio, "float32", "audio")
     _need(tokens, "int32", "tokens")
+    _batch_args(audio, ro, rs, pf, cl, tokens, overlap)
     nw = _I32(0)
     _check(lib().wb_transcribe_batch_overlap(model, _p(audio), rop, rsp, rs.size, overlap, pfp, clp, _p(tokens), budget,
                                              _p(workspace), workspace.numel() * workspace.element_size(),
@@ -324,6 +357,9 @@ def wb_stitch_tokens(req_samples, overlap: int, tokens, chunk_len, prefix_len: i
     rs, rsp = _host_arr(req_samples, np.int64)
     tk, tkp = _host_arr(tokens, np.int32)
     cl, clp = _host_arr(chunk_len, np.int32)
+    n_chunks = wb_chunk_count(rs, overlap)
+    if cl.size != n_chunks or tk.size < n_chunks * MAX_POS:
+        raise ValueError(f"{n_chunks} chunks need {n_chunks} decode lengths and [{n_chunks}, 448] tokens")
     cap = int(np.maximum(cl - prefix_len, 0).sum())
     out = np.zeros(max(cap, 1), np.int32)
     off = np.zeros(rs.size + 1, np.int64)
@@ -347,6 +383,8 @@ def wb_shard_batch(req_offset, req_samples, chunk_len, world: int, rank: int):
     ro, rop = _host_arr(req_offset, np.int64)
     rs, rsp = _host_arr(req_samples, np.int64)
     cl, clp = _host_arr(chunk_len, np.int32)
+    if ro.size != rs.size or cl.size != wb_chunk_count(rs):
+        raise ValueError("one offset per request and one decode length per chunk are needed")
     oo = np.zeros(rs.size, np.int64)
     os_ = np.zeros(rs.size, np.int64)
     nr, c0, cn = _I32(0), _I32(0), _I32(0)
@@ -355,10 +393,19 @@ def wb_shard_batch(req_offset, req_samples, chunk_len, world: int, rank: int):
     return oo[:nr.value].copy(), os_[:nr.value].copy(), c0.value, cn.value
 
 
-def wb_quantise_e4m3(x, codes, scale, stream=None):
-    import torch
+def _quant_args(x, codes, scale, n_scales: int = 1):
+    if str(x.dtype) not in ("torch.float32", "torch.bfloat16"):
+        raise TypeError(f"x must be float32 or bfloat16, got {x.dtype}")
+    _need(x, str(x.dtype)[6:], "x")
     _need(codes, "uint8", "codes")
     _need(scale, "float32", "scale")
+    _room(codes, x.numel(), "codes")
+    _room(scale, n_scales, "scale")
+
+
+def wb_quantise_e4m3(x, codes, scale, stream=None):
+    import torch
+    _quant_args(x, codes, scale)
     _check(lib().wb_quantise_e4m3(_p(x), 1 if x.dtype == torch.bfloat16 else 0, x.numel(), _p(codes), _p(scale),
                                   _stream(stream)))
 
@@ -366,8 +413,7 @@ def wb_quantise_e4m3(x, codes, scale, stream=None):
 def wb_quantise_e4m3_static(x, codes, scale, stream=None):
     """wb_quantise_e4m3 without any device allocation (n <= 2^26)."""
     import torch
-    _need(codes, "uint8", "codes")
-    _need(scale, "float32", "scale")
+    _quant_args(x, codes, scale)
     _check(lib().wb_quantise_e4m3_static(_p(x), 1 if x.dtype == torch.bfloat16 else 0, x.numel(), _p(codes),
                                          _p(scale), _stream(stream)))
 
@@ -377,22 +423,41 @@ def wb_quantise_e4m3_groups(x, n_groups: int, codes, scales, stream=None):
     _need(x, "float32", "x")
     _need(codes, "uint8", "codes")
     _need(scales, "float32", "scales")
-    if x.numel() % n_groups:
+    if n_groups < 1 or x.numel() % n_groups:
         raise ValueError("x.numel() must be a multiple of n_groups")
+    _room(codes, x.numel(), "codes")
+    _room(scales, n_groups, "scales")
     _check(lib().wb_quantise_e4m3_groups(_p(x), n_groups, x.numel() // n_groups, _p(codes), _p(scales),
                                          _stream(stream)))
 
 
 def wb_dequantise_e4m3(codes, scale, out, stream=None):
+    _need(codes, "uint8", "codes")
+    _need(scale, "float32", "scale")
     _need(out, "float32", "out")
+    _room(scale, 1, "scale")
+    _room(out, codes.numel(), "out")
     _check(lib().wb_dequantise_e4m3(_p(codes), _p(scale), codes.numel(), _p(out), _stream(stream)))
 
 
 def wb_gemm(A, B, C, bias=None, gelu=False, row_scale=None, col_scale=None, stream=None):
     import torch
     fp8 = A.dtype == torch.uint8
+    if A.dtype not in (torch.bfloat16, torch.uint8) or B.dtype != A.dtype:
+        raise TypeError(f"A and B must both be bfloat16 or both E4M3 codes (uint8), got {A.dtype} and {B.dtype}")
+    if C.dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError(f"C must be float32 or bfloat16, got {C.dtype}")
+    for t, what in ((A, "A"), (B, "B"), (C, "C"), (bias, "bias"), (row_scale, "row_scale"), (col_scale, "col_scale")):
+        if t is not None and not t.is_contiguous():
+            raise ValueError(f"{what} must be contiguous")
     M, K = A.shape
     N = B.shape[0]
+    if B.dim() != 2 or B.shape[1] != K:
+        raise ValueError(f"B must be [N, {K}], got {tuple(B.shape)}")
+    _room(C, M * N, "C")
+    for t, n, what in ((bias, N, "bias"), (row_scale, M, "row_scale"), (col_scale, N, "col_scale")):
+        _need(t, "float32", what)
+        _room(t, n, what)
     _check(lib().wb_gemm(_p(A), _p(B), M, N, K, 1 if fp8 else 0, _p(row_scale), _p(col_scale), _p(bias),
                          1 if gelu else 0, _p(C), 1 if C.dtype == torch.bfloat16 else 0, _stream(stream)))
 
