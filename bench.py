@@ -657,16 +657,16 @@ def main():
     # (profiles/) of kernels unchanged since, as a ratio to the capture's
     # algorithmic bytes, applied to this launch's algorithmic bytes
     traffic_ratio = {
+        # three launches over 128 chunks x 20 heads (cross_attn_decode_turbo.md)
+        KIND["cross_attn"]: ((983.745e6 + 3.027e6) + (983.727e6 + 0.506e6) + (983.804e6 + 0.812e6)) / 3
+                            / (128 * 20 * (2 * 1500 * 64 * 2 + 64 * 4 + 64 * 2)),
         KIND["mel"]: (126.83e6 + 62.09e6) / (64 * (480000 * 4 + 128 * 3000 * 4)),
     }
+    if w.kv_fp8 == KV_FP8_CROSS or getattr(w, "beams", 1) > 1:
+        # no capture of their own: the E4M3 cross-attention; beams re-reading their chunk's K/V from L2
+        traffic_ratio.pop(KIND["cross_attn"])
     roof["traffic"] = units_launch * traffic_ratio[dom] if (dom in traffic_ratio and roof["bound"] == "hbm") else None
     roof["traffic_unit"] = "DRAM bytes per launch"
-    if (roof["traffic"] is None and dom == KIND["cross_attn"] and w.kv_fp8 != KV_FP8_CROSS
-            and getattr(w, "beams", 1) == 1):
-        # the 128-chunk capture (1.001 x algorithmic bytes) predates the
-        # kernel's 40-register launch bound, so it is not this kernel's count
-        roof["traffic_note"] = ("no capture of the current kernel; an earlier build with the same access pattern "
-                                "read 1.001 x the algorithmic bytes (profiles/cross_attn_decode_turbo.md)")
     if roof["bound"] == "hbm" and roof["frac"] and roof["frac"] > 1.0:
         roof["note"] = ("a read-mostly stream measured against the copy (read + write) peak can exceed 1.0; "
                         "traffic / algorithmic bytes shows whether bytes are re-read")
