@@ -380,6 +380,43 @@ def test_fp8_decoder_moves_with_float32_level_perturbations():
     assert moved[True] > 6e-2, moved
 
 
+def test_fp8_oracle_misses_its_own_bar_on_the_gpu_test_inputs():
+    """The same effect on the inputs of the GPU mixed_fp8 decoder test (4
+    large-v3-turbo-shaped layers, weights seed 6, three chunks of seeded
+    bf16-exact encoder states, decode lengths 48, 30 and 9): the oracle
+    against itself with float32-sized noise (relative 1e-7) on its LayerNorm
+    outputs moves a logit by more than 6e-2 and changes the top-1 token at
+    some positions, as the GPU path does against the oracle (worst about
+    0.14, top-1 92-96 %)."""
+    from synth import TURBO, ModelDims, forced_prefix, random_tokens, round_to_bf16
+    dims = ModelDims(TURBO.name, TURBO.n_mels, TURBO.d_model, TURBO.n_heads, TURBO.d_ffn, 0, 4, TURBO.vocab)
+    W = make_weights(dims, 6, bf16=True)
+    enc_all = round_to_bf16(np.random.default_rng(61).normal(size=(3, 1500, dims.d_model)).astype(np.float32))
+    orig = model.layer_norm
+    worst, agree, total = 0.0, 0, 0
+    for c, L in enumerate((48, 30, 9)):
+        toks = np.concatenate([forced_prefix(2, dims.vocab), random_tokens(100 + c, L - 5, dims.vocab)])
+        enc = enc_all[c].astype(np.float64)
+        ref, _ = model.decode_teacher_forced(toks, enc, W, dims, kv_fp8=True, fp8=True, act16=True)
+        prng = np.random.default_rng(1 + c)
+
+        def perturbed(x, g, b, eps=1e-5):
+            y = orig(x, g, b, eps)
+            return y * (1.0 + 1e-7 * prng.standard_normal(y.shape))
+        model.layer_norm = perturbed
+        try:
+            alt, _ = model.decode_teacher_forced(toks, enc, W, dims, kv_fp8=True, fp8=True, act16=True)
+        finally:
+            model.layer_norm = orig
+        a, r = alt[3:L - 1], ref[3:L - 1]       # the positions the GPU test compares
+        worst = max(worst, float(np.abs(a - r).max()))
+        agree += int((a.argmax(1) == r.argmax(1)).sum())
+        total += a.shape[0]
+    print(f"oracle vs itself under 1e-7 noise: worst {worst:.3e}, top-1 {agree}/{total}")
+    assert worst > 6e-2, worst
+    assert agree < total, (agree, total)
+
+
 def test_beam_candidates_rank_by_score_then_beam_then_token():
     logits = np.log(np.array([[0.5, 0.25, 0.25], [0.25, 0.5, 0.25]]))
     s, p, v = model.beam_candidates(np.array([0.0, 0.0]), logits, 4)
