@@ -665,6 +665,10 @@ def main():
     if w.kv_fp8 == KV_FP8_CROSS or getattr(w, "beams", 1) > 1:
         # no capture of their own: the E4M3 cross-attention; beams re-reading their chunk's K/V from L2
         traffic_ratio.pop(KIND["cross_attn"])
+    if w.cfg != "c2":
+        # the mel capture is of the 64-chunk batch; a single chunk's output
+        # stays in L2, so its DRAM bytes do not scale from that capture
+        traffic_ratio.pop(KIND["mel"])
     roof["traffic"] = units_launch * traffic_ratio[dom] if (dom in traffic_ratio and roof["bound"] == "hbm") else None
     roof["traffic_unit"] = "DRAM bytes per launch"
     if roof["bound"] == "hbm" and roof["frac"] and roof["frac"] > 1.0:
