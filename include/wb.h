@@ -290,6 +290,8 @@ WB_API wb_status wb_decoder_destroy(wb_decoder* dec);
  *
  *   audio       [dev] float32, requests back to back
  *   req_offset  [host] int64 [n_req] first sample of each request in audio
+ *               (>= 0, else WB_ERR_SHAPE; offset + samples must lie inside
+ *               audio, whose length the library does not see)
  *   req_samples [host] int64 [n_req] samples of each request (>= 1)
  *   prefix      [host] int32 [4] forced prefix token ids (< vocab)
  *   chunk_len   [host] int32 [n_chunks] decode length of each chunk in

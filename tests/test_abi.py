@@ -127,6 +127,26 @@ def test_host_side_argument_checks_need_no_gpu():
     assert L.wb_transcribe_workspace_size_continuous(None, 1, None, 1 << 30) == 0
 
 
+def test_negative_request_offsets_are_rejected_before_any_launch():
+    """A negative request offset would make the chunk gather read before the
+    audio buffer; every batch entry point refuses it on the host, before it
+    touches the model (a dummy non-null handle is enough to reach the check)."""
+    L = wb.lib()
+    offs = np.array([0, -480000], np.int64)
+    samples = np.array([480000, 480000], np.int64)
+    prefix = np.zeros(4, np.int32)
+    lens = np.full(2, 10, np.int32)
+    nw = ctypes.c_int32(0)
+    args = (16, 16, offs.ctypes.data, samples.ctypes.data, 2)
+    tail = (prefix.ctypes.data, lens.ctypes.data, 16, 1 << 30, 16, 1 << 30, ctypes.addressof(nw), None)
+    assert L.wb_transcribe_batch(*args, *tail) == -2
+    assert b"negative request offset" in L.wb_last_error()
+    assert L.wb_transcribe_batch_continuous(*args, *tail) == -2
+    assert b"negative request offset" in L.wb_last_error()
+    assert L.wb_transcribe_batch_overlap(*args, 16000, *tail) == -2
+    assert b"negative request offset" in L.wb_last_error()
+
+
 def test_kv_modes_are_validated_on_the_host():
     L = wb.lib()
     from synth import TURBO

@@ -1498,6 +1498,8 @@ static wb_status transcribe_impl(wb_model* m, const float* audio, const int64_t*
     if (n_req < 1) return fail(WB_ERR_SHAPE, "wb_transcribe_batch: n_req < 1");
     if (!aligned16(audio) || !aligned16(tokens) || !aligned16(workspace))
         return fail(WB_ERR_ALIGN, "wb_transcribe_batch: alignment");
+    for (int32_t r = 0; r < n_req; ++r)
+        if (req_offset[r] < 0) return fail(WB_ERR_SHAPE, "wb_transcribe_batch: negative request offset");
     for (int i = 0; i < 4; ++i)
         if (prefix[i] < 0 || prefix[i] >= m->desc.vocab) return fail(WB_ERR_SHAPE, "wb_transcribe_batch: prefix id");
     std::vector<int32_t> req, valid;
@@ -1726,6 +1728,8 @@ wb_status wb_transcribe_batch_continuous(wb_model* m, const float* audio, const 
     if (n_req < 1) return fail(WB_ERR_SHAPE, "wb_transcribe_batch_continuous: n_req < 1");
     if (!aligned16(audio) || !aligned16(tokens) || !aligned16(workspace))
         return fail(WB_ERR_ALIGN, "wb_transcribe_batch_continuous: alignment");
+    for (int32_t r = 0; r < n_req; ++r)
+        if (req_offset[r] < 0) return fail(WB_ERR_SHAPE, "wb_transcribe_batch_continuous: negative request offset");
     if (m->fp32() || !m->desc.kv_fp8)
         return fail(WB_ERR_UNSUPPORTED, "wb_transcribe_batch_continuous: needs a bf16 model with the E4M3 cache");
     for (int i = 0; i < 4; ++i)
