@@ -165,6 +165,28 @@ def test_decoder_causality_and_prefix_consistency(kv_fp8, cross_fp8, act16):
         np.testing.assert_allclose(part[t], full[t], atol=1e-12)
 
 
+def test_kv_cache_scale_is_fixed_by_the_prefix_rows():
+    """The E4M3 self-attention cache scale of each (layer, K|V) comes from the
+    forced-prefix rows alone: changing any token after the prefix leaves every
+    scale as it was, changing the last prefix token moves them, and a longer
+    prefix takes more rows into the amax."""
+    W = make_weights(MINI, 9, bf16=True)
+    rng = np.random.default_rng(9)
+    enc = rng.normal(size=(20, MINI.d_model))
+    tok = rng.integers(0, MINI.vocab, size=10)
+    _, info = model.decode_teacher_forced(tok, enc, W, MINI, kv_fp8=True)
+    later = tok.copy()
+    later[4:] = (later[4:] + 1 + rng.integers(0, MINI.vocab - 1, size=6)) % MINI.vocab
+    _, info_later = model.decode_teacher_forced(later, enc, W, MINI, kv_fp8=True)
+    assert info_later["kv_scales"] == info["kv_scales"]
+    last = tok.copy()
+    last[3] = (last[3] + 1) % MINI.vocab
+    _, info_last = model.decode_teacher_forced(last, enc, W, MINI, kv_fp8=True)
+    assert info_last["kv_scales"][0] != info["kv_scales"][0]
+    _, info_p5 = model.decode_teacher_forced(tok, enc, W, MINI, kv_fp8=True, prefix_len=5)
+    assert all(a5 >= a4 for s5, s4 in zip(info_p5["kv_scales"][:1], info["kv_scales"][:1]) for a5, a4 in zip(s5, s4))
+
+
 def test_cross_kv_fp8_round_trip_bounds():
     """Per-tensor E4M3 of a cross K/V: the largest magnitude maps to the top code
     (448 x scale = amax up to fp32 rounding of the scale), normal values keep a
